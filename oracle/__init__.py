@@ -1,0 +1,202 @@
+"""CPU oracle for the block-quantized matmul (ctypes wrapper over qmm_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: tests/, the smoke check in __graft_entry__.py and the
+CPU-baseline leg of bench.py use it; the product package never imports it and
+shares no code with it.
+
+Every function returns fp64 results of the plain definitions (see the C file's
+header for the readings of the pages that it takes).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qmm_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_qmm.so")
+
+TYPES = {"q8_0": 8, "q4_K": 12, "q6_K": 14}
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (fp64, no fast-math, no FP contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
+           "-std=c11", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        L.oracle_half_to_double.restype = ctypes.c_double
+        L.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        L.oracle_float_to_half.restype = ctypes.c_uint16
+        L.oracle_float_to_half.argtypes = [ctypes.c_float]
+        L.oracle_quantize_q8_1.argtypes = [P, I64, I64, P]
+        L.oracle_dequant_q8_1.argtypes = [P, I64, I64, P]
+        L.oracle_block_bytes.argtypes = [ctypes.c_int]
+        L.oracle_block_elems.argtypes = [ctypes.c_int]
+        L.oracle_q4_K_fields.argtypes = [P, P, P, P, P, P]
+        L.oracle_q6_K_fields.argtypes = [P, P, P, P]
+        L.oracle_dequant.argtypes = [ctypes.c_int, P, I64, I64, P]
+        L.oracle_mul_mat.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P, P]
+        L.oracle_mul_mat_at.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P, P, I64, P, P]
+        L.oracle_brute.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P]
+        L.oracle_bucket.restype = I64
+        L.oracle_bucket.argtypes = [P, I64, I64, I64, P, P]
+        L.oracle_mul_mat_id.restype = I64
+        L.oracle_mul_mat_id.argtypes = [ctypes.c_int, P, I64, I64, I64, P, P, I64, I64, P, P]
+        L.oracle_set_threads.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u8(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    return a.view(np.uint8) if a.dtype != np.uint8 else a
+
+
+def _check(rc):
+    if rc < 0:
+        raise ValueError(f"oracle call failed with code {rc}")
+    return rc
+
+
+def set_threads(n: int) -> int:
+    return lib().oracle_set_threads(int(n))
+
+
+def half_to_double(h: int) -> float:
+    return lib().oracle_half_to_double(int(h))
+
+
+def float_to_half(x: float) -> int:
+    return lib().oracle_float_to_half(float(np.float32(x)))
+
+
+def block_bytes(fmt: str) -> int:
+    return lib().oracle_block_bytes(TYPES[fmt])
+
+
+def block_elems(fmt: str) -> int:
+    return lib().oracle_block_elems(TYPES[fmt])
+
+
+def quantize_q8_1(x: np.ndarray) -> np.ndarray:
+    """fp32 [m][k] -> q8_1 bytes uint8 [m][k/32*36]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    m, k = x.shape
+    out = np.empty((m, (k // 32) * 36), dtype=np.uint8)
+    _check(lib().oracle_quantize_q8_1(_p(x), m, k, _p(out)))
+    return out
+
+
+def dequant_q8_1(xq: np.ndarray, m: int, k: int) -> np.ndarray:
+    xq = _u8(xq)
+    out = np.empty((m, k), dtype=np.float64)
+    _check(lib().oracle_dequant_q8_1(_p(xq), m, k, _p(out)))
+    return out
+
+
+def dequant(W: np.ndarray, fmt: str, n: int, k: int) -> np.ndarray:
+    W = _u8(W)
+    out = np.empty((n, k), dtype=np.float64)
+    _check(lib().oracle_dequant(TYPES[fmt], _p(W), n, k, _p(out)))
+    return out
+
+
+def q4_K_fields(blk: np.ndarray):
+    blk = _u8(blk)
+    d = ctypes.c_double()
+    dmin = ctypes.c_double()
+    sc = np.empty(8, np.int32)
+    mn = np.empty(8, np.int32)
+    q = np.empty(256, np.int32)
+    lib().oracle_q4_K_fields(_p(blk), ctypes.byref(d), ctypes.byref(dmin), _p(sc), _p(mn), _p(q))
+    return d.value, dmin.value, sc, mn, q
+
+
+def q6_K_fields(blk: np.ndarray):
+    blk = _u8(blk)
+    d = ctypes.c_double()
+    sc = np.empty(16, np.int32)
+    q = np.empty(256, np.int32)
+    lib().oracle_q6_K_fields(_p(blk), ctypes.byref(d), _p(sc), _p(q))
+    return d.value, sc, q
+
+
+def mul_mat(W: np.ndarray, fmt: str, n: int, k: int, xq: np.ndarray, m: int):
+    """(y, T), both fp64 [m][n]: the fold and the sum of |block terms|."""
+    W = _u8(W)
+    xq = _u8(xq)
+    y = np.empty((m, n), dtype=np.float64)
+    T = np.empty((m, n), dtype=np.float64)
+    _check(lib().oracle_mul_mat(TYPES[fmt], _p(W), n, k, _p(xq), m, _p(y), _p(T)))
+    return y, T
+
+
+def mul_mat_at(W, fmt, n, k, xq, m, rows, cols):
+    """Fold at selected output positions (rows = W rows, cols = activation rows)."""
+    W = _u8(W)
+    xq = _u8(xq)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    y = np.empty(len(rows), dtype=np.float64)
+    T = np.empty(len(rows), dtype=np.float64)
+    _check(lib().oracle_mul_mat_at(TYPES[fmt], _p(W), n, k, _p(xq), m, _p(rows), _p(cols), len(rows), _p(y), _p(T)))
+    return y, T
+
+
+def brute(W, fmt, n, k, xq, m) -> np.ndarray:
+    W = _u8(W)
+    xq = _u8(xq)
+    y = np.empty((m, n), dtype=np.float64)
+    _check(lib().oracle_brute(TYPES[fmt], _p(W), n, k, _p(xq), m, _p(y)))
+    return y
+
+
+def bucket(ids: np.ndarray, n_experts: int):
+    """(bounds int32 [E+1], perm int32 [valid pairs], n_invalid)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    t, kk = ids.shape
+    bounds = np.empty(n_experts + 1, np.int32)
+    perm = np.empty(t * kk, np.int32)
+    bad = lib().oracle_bucket(_p(ids), t, kk, n_experts, _p(bounds), _p(perm))
+    return bounds, perm[: bounds[-1]], int(bad)
+
+
+def mul_mat_id(W, fmt, n_experts, n, k, xq, ids):
+    """(y, T, n_invalid) with y, T fp64 [n_tokens][top_k][n]."""
+    W = _u8(W)
+    xq = _u8(xq)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    t, kk = ids.shape
+    y = np.empty((t, kk, n), np.float64)
+    T = np.empty((t, kk, n), np.float64)
+    bad = lib().oracle_mul_mat_id(TYPES[fmt], _p(W), n_experts, n, k, _p(xq), _p(ids), kk, t, _p(y), _p(T))
+    _check(bad)
+    return y, T, int(bad)
+
+
+if __name__ == "__main__":  # pragma: no cover
+    print(build(force="--force" in sys.argv))

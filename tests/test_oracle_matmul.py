@@ -1,0 +1,191 @@
+"""Pins for the oracle's fold: special cases that reduce to an integer matmul,
+brute force against the dequantized fp64 matmul, the min term's sign and
+indexing, MoE reduction to the dense routine, and bucketing against a stable
+sort."""
+import numpy as np
+import pytest
+
+import qmm_synth
+from blockpack import pack_q4_K, pack_q6_K, pack_q8_0, pack_q8_1
+
+
+def _q8_1_rows(q: np.ndarray, d: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """q8_1 bytes from int8 q [m][k] and per-block fp16 d, s [m][k/32]."""
+    m, k = q.shape
+    out = np.zeros((m, k // 32, 36), np.uint8)
+    for r in range(m):
+        for b in range(k // 32):
+            out[r, b] = pack_q8_1(d[r, b], s[r, b], q[r, 32 * b:32 * b + 32])
+    return out.reshape(m, -1)
+
+
+def test_q4_K_integer_matmul_special_case(oracle_mod):
+    """d = 1, dmin = 0, all sub-block scales 1 and q8_1 d = 1: the fold is the
+    plain integer matmul of the nibble codes with the int8 activations."""
+    rng = np.random.default_rng(21)
+    n, k, m = 5, 512, 3
+    Qw = rng.integers(0, 16, (n, k))
+    rows = []
+    for r in range(n):
+        rows.append(np.concatenate([pack_q4_K(1.0, 0.0, np.ones(8, int), rng.integers(0, 64, 8), Qw[r, 256 * s:256 * s + 256])
+                                    for s in range(k // 256)]))
+    W = np.stack(rows)
+    Qx = rng.integers(-127, 128, (m, k))
+    xq = _q8_1_rows(Qx, np.ones((m, k // 32)), rng.uniform(-3, 3, (m, k // 32)))
+    y, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    assert np.array_equal(y, (Qx @ Qw.T).astype(np.float64))
+
+
+def test_q4_K_min_term_special_case(oracle_mod):
+    """All scales 0, d = 0, dmin = 1: y[c][r] = -sum_b m[r,b] * s[c,b]."""
+    rng = np.random.default_rng(22)
+    n, k, m = 4, 768, 3
+    M = rng.integers(0, 64, (n, k // 32))
+    rows = []
+    for r in range(n):
+        rows.append(np.concatenate([pack_q4_K(0.0, 1.0, np.zeros(8, int), M[r, 8 * s:8 * s + 8], rng.integers(0, 16, 256))
+                                    for s in range(k // 256)]))
+    W = np.stack(rows)
+    S = rng.uniform(-4, 4, (m, k // 32)).astype(np.float16).astype(np.float64)
+    xq = _q8_1_rows(rng.integers(-127, 128, (m, k)), rng.uniform(0, 1, (m, k // 32)), S)
+    y, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    assert np.allclose(y, -(S @ M.T), rtol=1e-15, atol=0)
+    assert np.allclose(T, np.abs(S) @ M.T, rtol=1e-15, atol=0)
+
+
+def test_q6_K_integer_matmul_special_case(oracle_mod):
+    """d = 1, q8_1 d = 1: the fold is sum_j sc_j * (int dot of sub-block j)."""
+    rng = np.random.default_rng(23)
+    n, k, m = 4, 512, 3
+    V = rng.integers(-32, 32, (n, k))
+    SC = rng.integers(-128, 128, (n, k // 16))
+    W = np.stack([np.concatenate([pack_q6_K(1.0, SC[r, 16 * s:16 * s + 16], V[r, 256 * s:256 * s + 256])
+                                  for s in range(k // 256)]) for r in range(n)])
+    Qx = rng.integers(-127, 128, (m, k))
+    xq = _q8_1_rows(Qx, np.ones((m, k // 32)), np.zeros((m, k // 32)))
+    y, _ = oracle_mod.mul_mat(W, "q6_K", n, k, xq, m)
+    assert np.array_equal(y, (Qx @ (V * np.repeat(SC, 16, axis=1)).T).astype(np.float64))
+
+
+def test_q8_0_integer_matmul_special_case(oracle_mod):
+    rng = np.random.default_rng(24)
+    n, k, m = 6, 320, 4
+    Qw = rng.integers(-128, 128, (n, k))
+    W = np.stack([np.concatenate([pack_q8_0(1.0, Qw[r, 32 * b:32 * b + 32]) for b in range(k // 32)]) for r in range(n)])
+    Qx = rng.integers(-127, 128, (m, k))
+    xq = _q8_1_rows(Qx, np.ones((m, k // 32)), np.zeros((m, k // 32)))
+    y, _ = oracle_mod.mul_mat(W, "q8_0", n, k, xq, m)
+    assert np.array_equal(y, (Qx @ Qw.T).astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt", ["q6_K", "q8_0"])
+def test_brute_force_agrees(oracle_mod, fmt):
+    """Without a min term the fold equals the fp64 matmul of dequantized W and
+    dequantized q8_1 x up to fp64 rounding; and the brute force itself equals
+    numpy's matmul of the two dequantized matrices."""
+    rng = np.random.default_rng(31)
+    n, k, m = 9, 512, 5
+    W = qmm_synth.gen_weights(fmt, rng, n, k)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, m, k))
+    yA, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
+    yB = oracle_mod.brute(W, fmt, n, k, xq, m)
+    assert np.all(np.abs(yA - yB) <= 1e-12 * T)
+    ref = oracle_mod.dequant_q8_1(xq, m, k) @ oracle_mod.dequant(W, fmt, n, k).T
+    assert np.allclose(yB, ref, rtol=0, atol=1e-12 * np.abs(T).max())
+
+
+def test_brute_force_agrees_q4_K_exact_s(oracle_mod):
+    """Q4_K: when s = d*sum(q) is exact in fp16 the fold equals the brute force
+    to fp64 rounding (power-of-two d and small sums make d*sum(q) exact)."""
+    rng = np.random.default_rng(32)
+    n, k, m = 7, 512, 4
+    W = qmm_synth.gen_q4_K(rng, n, k)
+    Qx = rng.integers(-60, 61, (m, k))
+    d = 2.0 ** rng.integers(-8, -2, (m, k // 32))
+    S = Qx.reshape(m, k // 32, 32).sum(axis=2)
+    xq = _q8_1_rows(Qx, d, d * S)
+    yA, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    yB = oracle_mod.brute(W, "q4_K", n, k, xq, m)
+    assert np.all(np.abs(yA - yB) <= 1e-12 * T)
+
+
+def test_brute_force_q4_K_s_rounding_bound(oracle_mod):
+    """Q4_K with quantized activations: the fold uses the stored fp16 s, the brute
+    force d*sum(q); they differ by at most the fp16 rounding of s in the min terms."""
+    rng = np.random.default_rng(33)
+    n, k, m = 8, 1024, 3
+    W = qmm_synth.gen_q4_K(rng, n, k)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, m, k))
+    yA, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    yB = oracle_mod.brute(W, "q4_K", n, k, xq, m)
+    assert np.all(np.abs(yA - yB) <= 2.0 ** -10 * T)
+
+
+def test_activation_quantization_error_reported(oracle_mod, capsys):
+    """Reported, not a pass criterion: relative RMS of the q8_1 path against the
+    fp64 product of dequantized W with the raw fp32 activations."""
+    rng = np.random.default_rng(34)
+    res = {}
+    for fmt in ("q4_K", "q6_K", "q8_0"):
+        n, k, m = 64, 2048, 4
+        W = qmm_synth.gen_weights(fmt, rng, n, k)
+        x = qmm_synth.gen_x(rng, m, k)
+        yA, _ = oracle_mod.mul_mat(W, fmt, n, k, oracle_mod.quantize_q8_1(x), m)
+        yR = x.astype(np.float64) @ oracle_mod.dequant(W, fmt, n, k).T
+        res[fmt] = float(np.sqrt(np.mean((yA - yR) ** 2) / np.mean(yR ** 2)))
+    print("activation-quantization rel RMS:", res)
+    assert all(v < 0.05 for v in res.values())
+
+
+def test_mul_mat_at_matches_full(oracle_mod):
+    rng = np.random.default_rng(41)
+    n, k, m = 33, 512, 3
+    W = qmm_synth.gen_q4_K(rng, n, k)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, m, k))
+    y, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    rows = rng.integers(0, n, 50)
+    cols = rng.integers(0, m, 50)
+    y2, T2 = oracle_mod.mul_mat_at(W, "q4_K", n, k, xq, m, rows, cols)
+    assert np.array_equal(y2, y[cols, rows]) and np.array_equal(T2, T[cols, rows])
+
+
+def test_bucket_is_stable_sort(oracle_mod):
+    rng = np.random.default_rng(51)
+    ids = qmm_synth.gen_moe_ids(rng, 200, 8, 32)
+    ids[3, 2] = -1
+    ids[7, 0] = 32
+    bounds, perm, bad = oracle_mod.bucket(ids, 32)
+    assert bad == 2
+    flat = ids.ravel()
+    valid = np.nonzero((flat >= 0) & (flat < 32))[0]
+    order = valid[np.argsort(flat[valid], kind="stable")]
+    assert np.array_equal(perm, order)
+    assert np.array_equal(np.diff(bounds), np.bincount(flat[valid], minlength=32))
+
+
+def test_mul_mat_id_reduces_to_dense(oracle_mod):
+    rng = np.random.default_rng(52)
+    E, n, k, T_, K = 6, 16, 512, 5, 3
+    W = qmm_synth.gen_q4_K(rng, E * n, k).reshape(E, n, -1)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, T_, k))
+    ids = qmm_synth.gen_moe_ids(rng, T_, K, E)
+    ids[1, 1] = 99
+    y, T, bad = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, xq, ids)
+    assert bad == 1
+    for t in range(T_):
+        for s in range(K):
+            e = ids[t, s]
+            if e >= E:
+                assert np.all(y[t, s] == 0) and np.all(T[t, s] == 0)
+                continue
+            yd, Td = oracle_mod.mul_mat(W[e], "q4_K", n, k, xq[t:t + 1], 1)
+            assert np.array_equal(y[t, s], yd[0]) and np.array_equal(T[t, s], Td[0])
+
+
+def test_synthetic_moe_histogram_is_skewed():
+    """The MoE workload recipe (seed 0) is as skewed as intended: one hot expert,
+    many cold ones, every expert used."""
+    _, _, ids = qmm_synth.make_moe(128, 8, 256, 512, 8)
+    c = np.bincount(ids.ravel(), minlength=128)
+    assert c.sum() == 4096 and c.max() > 300 and np.median(c) < 32 and c.min() >= 1
+    assert all(len(set(r)) == 8 for r in ids)
