@@ -1,0 +1,359 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-quantized matmul on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input:
+q8_1 quantization of x followed by y = x * dequant(W)^T.
+
+Headline workload (the pages' decode GEMV shape): Q4_K W n=17408 x k=5120, m=1
+fp32 activation row.  The metric is HBM GB/s of algorithmic bytes; the roofline
+object reports the GEMV kernel against the measured HBM copy bandwidth.  The
+"secondary" object reports the prefill GEMM (m=512) and the MoE mul_mat_id in
+TOPS (2*m*n*k integer multiply-adds).
+
+Timing: CUDA events on the launching stream around exactly K steps after W warm-up
+steps, a barrier and a device synchronise on both sides, max over ranks.  L2 is
+defeated by rotating among weight copies whose total size exceeds 3x the 129 MB L2.
+
+--impl reference times the CPU oracle (test infrastructure, plain fp64 C) on the
+host cores, on a bounded sample of the same workload, and prints the same JSON line
+with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import qmm_synth  # noqa: E402
+
+METRIC = "Q4_K matmul HBM GB/s at m=1 and int8 TOPS at m=512/MoE, % of GB300 roofline"
+UNIT = "GB/s"
+N, K, M = 17408, 5120, 1
+WORKLOAD = "decode GEMV Q4_K n=17408 k=5120 m=1 (quantize x + mul_mat)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def step_bytes(n, k, m, row_bytes):
+    """Algorithmic bytes of one step: W once, x read, q8_1 written and read, y written."""
+    return n * row_bytes + m * k * 4 + 2 * m * (k // 32) * 36 + m * n * 4
+
+
+def gemv_bytes(n, k, m, row_bytes):
+    """Algorithmic bytes of one GEMV launch: W once, q8_1 read, y written."""
+    return n * row_bytes + m * (k // 32) * 36 + m * n * 4
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_matmul_q8_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
+        if not self.path or not os.path.exists(self.path):
+            return out
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if sm:
+            loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+            out = {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                   "samples": len(sm)}
+        return out
+
+
+def oracle_baseline(W, x, n, k, m, row_bytes, budget_s=12.0):
+    """The CPU oracle (as it stands) on the host cores: quantize + fold over whole rows,
+    repeated over row slices until about budget_s seconds of work; returns GB/s of
+    the same algorithmic bytes."""
+    import oracle
+    threads = oracle.set_threads(os.cpu_count() or 1)
+    rows_per = max(1, n // 8)
+    done_rows, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        r0 = (reps * rows_per) % n
+        r1 = min(n, r0 + rows_per)
+        xq = oracle.quantize_q8_1(x)
+        oracle.mul_mat(W[r0:r1], "q4_K", r1 - r0, k, xq, m)
+        done_rows += r1 - r0
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 64:
+            break
+    bytes_done = done_rows * row_bytes + reps * (m * k * 4 + 2 * m * (k // 32) * 36) + done_rows * m * 4
+    return {"value": bytes_done / el / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done_rows} weight rows of the n={n} k={k} m={m} Q4_K problem in {reps} slices "
+                      f"(quantize + fp64 fold), {el:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    row_bytes = (K // 256) * 144
+    W, x = qmm_synth.make_dense("q4_K", N, K, M, seed=0)
+    import oracle
+    oracle.build()
+    steps = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_baseline(W, x, N, K, M, row_bytes, budget_s=max(2.0, 20.0 / max(1, args.steps + args.warmup)))
+        if i >= args.warmup:
+            steps.append(r)
+    val = statistics.median(s["value"] for s in steps)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "bounded slices of the workload per step"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": steps[0]["cores"], "kind": "oracle",
+                             "sample": steps[0]["sample"]},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_region(torch, fn, steps, warmup, stream, barrier):
+    for i in range(warmup):
+        fn(i)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        fn(warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1)
+
+
+def secondary(torch, qmm, dev, stream, steps):
+    """Prefill GEMM (m=512) and MoE mul_mat_id throughput in TOPS, device-timed."""
+    out = {}
+    # prefill: Q4_K n=14336 k=4096, m=512
+    n, k, m = 14336, 4096, 512
+    W, x = qmm_synth.make_dense("q4_K", n, k, m, seed=0)
+    copies = max(2, int(3 * L2_BYTES // W.nbytes) + 1)
+    Wd = [torch.from_numpy(W).to(dev) for _ in range(copies)]
+    xq = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
+    y = torch.empty((m, n), device=dev)
+    ws = torch.empty(max(1, qmm.qmm_workspace_bytes("q4_K", n, k, m)), dtype=torch.uint8, device=dev)
+    fn = lambda i: qmm.qmm_mul_mat(Wd[i % copies], "q4_K", n, k, xq, m, y=y, workspace=ws, stream=stream)
+    ms = time_region(torch, fn, steps, 3, stream, lambda: None) / steps
+    out["prefill_q4K_n14336_k4096_m512"] = {"tops": 2 * m * n * k / (ms * 1e-3) / 1e12, "ms": ms}
+    del Wd
+    # MoE: 128 experts x Q4_K n=1536 k=4096, 512 tokens top-8 Zipf(1.1)
+    E, n, k, T_, Kt = 128, 1536, 4096, 512, 8
+    W, x, ids = qmm_synth.make_moe(E, n, k, T_, Kt, seed=0)
+    Wd = torch.from_numpy(W).to(dev)
+    xq = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
+    idd = torch.from_numpy(ids).to(dev)
+    y = torch.empty((T_, Kt, n), device=dev)
+    ws = torch.empty(qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, Kt), dtype=torch.uint8, device=dev)
+    fn = lambda i: qmm.qmm_mul_mat_id(Wd, "q4_K", E, n, k, xq, idd, Kt, T_, y=y, workspace=ws, stream=stream)
+    ms = time_region(torch, fn, steps, 3, stream, lambda: None) / steps
+    out["moe_q4K_e128_n1536_k4096_t512_top8"] = {"tops": 2 * T_ * Kt * n * k / (ms * 1e-3) / 1e12, "ms": ms,
+                                                 "l2": "weights 453 MB > 3x L2"}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="qmm", choices=["qmm", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    import torch.distributed as dist
+
+    import block_quantized_matmul_q8_gb300 as qmm
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qmm.build()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    row_bytes = qmm.qmm_row_bytes("q4_K", K)
+    W, x = qmm_synth.make_dense("q4_K", N, K, M, seed=0)
+    copies = max(2, int(3 * L2_BYTES // W.nbytes) + 1)
+    Wd = [torch.from_numpy(W).to(dev) for _ in range(copies)]
+    x_h = torch.from_numpy(x).pin_memory()
+    x_d = x_h.to(dev)
+    xq = torch.empty((M, (K // 32) * 36), dtype=torch.uint8, device=dev)
+    y = torch.empty((M, N), device=dev)
+    y_h = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    # --- device-resident step, GEMV launches bracketed by events for the roofline
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def step(i):
+        qmm.qmm_quantize_q8_1(x_d, out=xq, stream=stream)
+        j = i - args.warmup
+        if 0 <= j < args.steps:
+            ev[j][0].record(stream)
+        qmm.qmm_mul_mat(Wd[i % copies], "q4_K", N, K, xq, M, y=y, stream=stream)
+        if 0 <= j < args.steps:
+            ev[j][1].record(stream)
+
+    with ClockSampler(local) as clk:
+        ms_total = time_region(torch, step, args.steps, args.warmup, stream, barrier)
+    clocks = clk.summary()
+    gemv_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    # --- end to end through the public API with host buffers (pinned), copies inside the region
+    def step_e2e(i):
+        x_d.copy_(x_h, non_blocking=True)
+        qmm.qmm_quantize_q8_1(x_d, out=xq, stream=stream)
+        qmm.qmm_mul_mat(Wd[i % copies], "q4_K", N, K, xq, M, y=y, stream=stream)
+        y_h.copy_(y, non_blocking=True)
+
+    ms_e2e = time_region(torch, step_e2e, args.steps, args.warmup, stream, barrier)
+
+    t = torch.tensor([ms_total, ms_e2e, gemv_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total, ms_e2e, gemv_ms = t.tolist()
+    ms_step = ms_total / args.steps
+    sb = step_bytes(N, K, M, row_bytes)
+    value = world * sb / (ms_step * 1e-3) / 1e9
+    e2e_value = world * sb / (ms_e2e / args.steps * 1e-3) / 1e9
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    kb = gemv_bytes(N, K, M, row_bytes)
+    achieved = kb / (gemv_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("gemv_kernel<Q4_K,1>")
+
+    sec = None
+    if rank == 0 and not args.no_secondary:
+        sec = secondary(torch, qmm, dev, stream, steps=10)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_baseline(W, x, N, K, M, row_bytes)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8 dot (exact int32) + fp32 fold", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n": N, "k": K, "m": M, "format": "Q4_K", "seed": 0,
+                       "l2": f"rotating {copies} weight copies ({copies * W.nbytes / 1e6:.0f} MB > 3x L2)",
+                       "replicas": world},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "gemv_kernel<Q4_K,1>",
+                         "peak_source": f"{peak_src} HBM copy bandwidth", "kernel_ms": gemv_ms,
+                         "algorithmic_bytes": kb},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": M * K * 4,
+                    "d2h_bytes_per_step": M * N * 4, "ms_per_step": ms_e2e / args.steps},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "secondary": sec,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

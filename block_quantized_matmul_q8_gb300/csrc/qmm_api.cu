@@ -1,0 +1,248 @@
+// qmm_api.cu -- the C ABI (include/qmm.h): argument checks, path choice, planning.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "qmm.h"
+#include "qmm_common.cuh"
+#include "qmm_internal.h"
+#include "qmm_moe.h"
+
+namespace qmm {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_optin[kMaxDevices];
+std::atomic<int> g_force_path{0};
+std::atomic<int> g_stream_k_mode{0};
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return dev;
+}
+}  // namespace
+
+int device_sm_count() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 1;
+    int v = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+        g_sm_count[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+int device_smem_optin() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 48 * 1024;
+    int v = g_smem_optin[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || v <= 0)
+            v = 48 * 1024;
+        g_smem_optin[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+static bool type_ok(qmm_type t) { return t == QMM_Q4_K || t == QMM_Q6_K || t == QMM_Q8_0; }
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+constexpr int64_t kMaxK = int64_t(1) << 20;
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+
+static qmm_status check_k(qmm_type t, int64_t k) {
+    if (!type_ok(t)) return QMM_ERR_TYPE;
+    if (k <= 0) return QMM_ERR_ARG;
+    if (k % block_elems(t) != 0 || k % 32 != 0 || k > kMaxK) return QMM_ERR_SHAPE;
+    return QMM_OK;
+}
+
+static qmm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
+
+// Which kernel family qmm_mul_mat uses for these sizes.
+enum Path { kGemv = 1, kGemmDp4a = 2, kGemmTc = 3 };
+
+static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    const int force = g_force_path.load(std::memory_order_relaxed);
+    const bool gemv_fits = gemv_smem_bytes(k, 1) <= size_t(device_smem_optin());
+    if (force == kGemv && gemv_fits && m <= 64) return kGemv;
+    if (force == kGemmDp4a) return kGemmDp4a;
+    if (force == kGemmTc && gemm_tc_supported(t, n, k, m)) return kGemmTc;
+    if (m <= 8 && gemv_fits) return kGemv;
+    if (gemm_tc_supported(t, n, k, m)) return kGemmTc;
+    return kGemmDp4a;
+}
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+const char *qmm_status_string(qmm_status s) {
+    switch (s) {
+    case QMM_OK: return "QMM_OK";
+    case QMM_ERR_ARG: return "QMM_ERR_ARG";
+    case QMM_ERR_SHAPE: return "QMM_ERR_SHAPE";
+    case QMM_ERR_TYPE: return "QMM_ERR_TYPE";
+    case QMM_ERR_ALIGN: return "QMM_ERR_ALIGN";
+    case QMM_ERR_WORKSPACE: return "QMM_ERR_WORKSPACE";
+    case QMM_ERR_CUDA: return "QMM_ERR_CUDA";
+    case QMM_ERR_IDS: return "QMM_ERR_IDS";
+    case QMM_ERR_DEVICE: return "QMM_ERR_DEVICE";
+    }
+    return "QMM_ERR_UNKNOWN";
+}
+
+size_t qmm_q8_1_bytes(int64_t m, int64_t k) {
+    if (m < 0 || k < 0) return 0;
+    return size_t(m) * size_t(k / 32) * kQ81Bytes;
+}
+
+size_t qmm_row_bytes(qmm_type t, int64_t k) {
+    if (!type_ok(t) || k < 0 || k % block_elems(t)) return 0;
+    return size_t(k / block_elems(t)) * size_t(block_bytes(t));
+}
+
+size_t qmm_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t n_experts, int64_t top_k) {
+    if (!type_ok(t) || n < 0 || k <= 0 || m < 0) return 0;
+    if (n_experts > 0) return moe_workspace_bytes(t, n, k, m, n_experts, top_k);
+    return gemm_tc_supported(t, n, k, m) ? gemm_tc_workspace_bytes(t, n, k, m) : 0;
+}
+
+qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void *xq, void *stream) {
+    if (m < 0 || k <= 0) return QMM_ERR_ARG;
+    if (k % 32 || k > kMaxK || m > kMaxRows) return QMM_ERR_SHAPE;
+    if (m == 0) return QMM_OK;
+    if (!x || !xq) return QMM_ERR_ARG;
+    if (!aligned16(x) || !aligned16(xq)) return QMM_ERR_ALIGN;
+    return cuda_status(launch_quantize_q8_1(x, m, k, xq, static_cast<cudaStream_t>(stream)));
+}
+
+qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                       void *workspace, size_t ws_bytes, void *stream) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n < 0 || m < 0) return QMM_ERR_ARG;
+    if (n > kMaxRows || m > kMaxRows) return QMM_ERR_SHAPE;
+    if (n == 0 || m == 0) return QMM_OK;
+    if (!W || !xq || !y) return QMM_ERR_ARG;
+    if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return QMM_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (choose_path(t, n, k, m)) {
+    case kGemv: return cuda_status(launch_gemv(t, W, n, k, xq, m, y, st));
+    case kGemmTc: {
+        const size_t need = gemm_tc_workspace_bytes(t, n, k, m);
+        if (need > 0) {
+            if (!workspace || ws_bytes < need) return QMM_ERR_WORKSPACE;
+            if (!aligned256(workspace)) return QMM_ERR_ALIGN;
+        }
+        return cuda_status(launch_gemm_tc(t, W, n, k, xq, m, y, workspace, ws_bytes,
+                                          g_stream_k_mode.load(std::memory_order_relaxed), st));
+    }
+    default: return cuda_status(launch_gemm_dp4a(t, W, n, k, xq, m, y, st));
+    }
+}
+
+qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
+                          const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
+                          void *workspace, size_t ws_bytes, void *stream) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n_experts <= 0 || top_k <= 0 || n < 0 || n_tokens < 0) return QMM_ERR_ARG;
+    if (n_experts > kMaxExperts || n > kMaxRows || n_tokens * top_k > kMaxRows) return QMM_ERR_SHAPE;
+    if (!workspace) return QMM_ERR_WORKSPACE;
+    if (!aligned256(workspace)) return QMM_ERR_ALIGN;
+    const size_t need = moe_workspace_bytes(t, n, k, n_tokens, n_experts, top_k);
+    if (ws_bytes < need) return QMM_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n == 0 || n_tokens == 0) {
+        // empty problem: only reset the status word
+        return cuda_status(cudaMemsetAsync(workspace, 0, 16, st));
+    }
+    if (!W_experts || !xq || !ids || !y) return QMM_ERR_ARG;
+    if (!aligned16(W_experts) || !aligned16(xq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(ids) & 3u))
+        return QMM_ERR_ALIGN;
+    return cuda_status(launch_mul_mat_id(t, W_experts, n_experts, n, k, xq, ids, top_k, n_tokens, y, workspace,
+                                         ws_bytes, st));
+}
+
+qmm_status qmm_read_device_status(const void *workspace, int32_t *status, void *stream) {
+    if (!workspace || !status) return QMM_ERR_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, static_cast<const uint8_t *>(workspace) + kStatusOffset, sizeof(v),
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return QMM_ERR_CUDA;
+    *status = v;
+    return QMM_OK;
+}
+
+int qmm_tile_efficiency_percent(int64_t ntiles, int64_t nsm) {
+    if (ntiles <= 0 || nsm <= 0) return 0;
+    const int64_t nwaves = (ntiles + nsm - 1) / nsm;
+    return (int)(100 * ntiles / (nsm * nwaves));
+}
+
+qmm_status qmm_plan_gemm(qmm_type t, int64_t n, int64_t k, int64_t m, int32_t nsm, int32_t stream_k_mode,
+                         qmm_gemm_plan *plan) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n <= 0 || m <= 0 || nsm <= 0 || !plan) return QMM_ERR_ARG;
+    qmm_gemm_plan p{};
+    p.tile_n = 128;
+    p.tile_m = (int32_t)gemm_tc_tile_m(m);
+    p.iter_k = 256;
+    p.tiles_n = (n + p.tile_n - 1) / p.tile_n;
+    p.tiles_m = (m + p.tile_m - 1) / p.tile_m;
+    p.ntiles = p.tiles_n * p.tiles_m;
+    p.iters_per_tile = (k + p.iter_k - 1) / p.iter_k;
+    p.nwork = p.ntiles * p.iters_per_tile;
+    p.efficiency_percent = qmm_tile_efficiency_percent(p.ntiles, nsm);
+    const bool sk = stream_k_mode == 2 || (stream_k_mode == 0 && p.efficiency_percent < 90);
+    if (!sk) {
+        p.stream_k = 0;
+        p.ctas = (int32_t)std::min<int64_t>(p.ntiles, kMaxRows);
+        p.fixup = 0;
+    } else {
+        p.stream_k = 1;
+        p.ctas = (int32_t)std::min<int64_t>(nsm, p.nwork);
+        p.fixup = 0;
+        for (int32_t c = 1; c < p.ctas; ++c) {
+            const int64_t b = (int64_t)c * p.nwork / p.ctas;
+            if (b % p.iters_per_tile) {
+                p.fixup = 1;
+                break;
+            }
+        }
+    }
+    *plan = p;
+    return QMM_OK;
+}
+
+void qmm_plan_cta_range(const qmm_gemm_plan *plan, int32_t cta, int64_t *begin, int64_t *end) {
+    if (!plan || !begin || !end || cta < 0 || cta >= plan->ctas) {
+        if (begin) *begin = 0;
+        if (end) *end = 0;
+        return;
+    }
+    if (!plan->stream_k) {
+        *begin = (int64_t)cta * plan->iters_per_tile;
+        *end = *begin + plan->iters_per_tile;
+        return;
+    }
+    *begin = (int64_t)cta * plan->nwork / plan->ctas;
+    *end = (int64_t)(cta + 1) * plan->nwork / plan->ctas;
+}
+
+void qmm_set_force_path(int path) { g_force_path.store(path, std::memory_order_relaxed); }
+void qmm_set_stream_k_mode(int mode) { g_stream_k_mode.store(mode, std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,196 @@
+// qmm_common.cuh -- block formats and shared device helpers of the CUDA path.
+//
+// Block layouts (see include/qmm.h):
+//   q8_1 36 B: fp16 d | fp16 s | int8 q[32]
+//   Q4_K 144 B: fp16 d | fp16 dmin | 12 B packed 6-bit scales/mins | 128 B nibbles
+//   Q6_K 210 B: ql[128] | qh[64] | int8 sc[16] | fp16 d
+//   Q8_0 34 B: fp16 d | int8 q[32]
+//
+// Work is cut into "units" of 64 consecutive k values of one weight row: a quarter
+// superblock for Q4_K / Q6_K, two blocks for Q8_0.  A unit always lines up with two
+// q8_1 activation blocks (2u, 2u+1), so one decode routine serves the GEMV and the
+// CUDA-core GEMM.  A decoded unit holds
+//   q[16]   : 64 signed 8-bit weight codes, 4 per word, in k order
+//   isc[4]  : integer scale of each 16-wide quarter (Q4_K: the 6-bit sub-block scale,
+//             twice per 32-block; Q6_K: the int8 sub-scale; Q8_0: 1)
+//   fd[2]   : fp32 factor of each 32-block's integer dot (Q4_K/Q6_K: d, Q8_0: d of the block)
+//   fm[2]   : fp32 factor of each 32-block's min term (Q4_K: dmin*m, otherwise 0)
+// so that one 32-block's term is  fd * d8 * (isc0*dot16_0 + isc1*dot16_1) - fm * s8
+// ([MMQ] sections "dp4a 路径的 Q4_K" and "Q6_K: 子块尺度与 q8_1 块长错位").
+#pragma once
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "qmm.h"
+
+namespace qmm {
+
+constexpr int kQ4KBytes = 144;
+constexpr int kQ6KBytes = 210;
+constexpr int kQ80Bytes = 34;
+constexpr int kQ81Bytes = 36;
+
+struct Unit {
+    int q[16];
+    int isc[4];
+    float fd[2];
+    float fm[2];
+};
+
+__host__ __device__ constexpr int block_bytes(int t) {
+    return t == QMM_Q4_K ? kQ4KBytes : t == QMM_Q6_K ? kQ6KBytes : t == QMM_Q8_0 ? kQ80Bytes : 0;
+}
+__host__ __device__ constexpr int block_elems(int t) { return t == QMM_Q8_0 ? 32 : 256; }
+
+__device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
+__device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
+__device__ __forceinline__ uint4 ldg16(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ldg4(const void *p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ldg2(const void *p) {
+    unsigned short r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+// Q4_K: 6-bit scale and min of sub-block j from the 12 packed bytes held in three
+// little-endian words s0 (bytes 0..3), s1 (4..7), s2 (8..11).
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int &sc, int &mn) {
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63;
+        mn = (s1 >> (8 * j)) & 63;
+    } else {
+        const int jj = 8 * (j - 4);
+        sc = ((s2 >> jj) & 15) | (((s0 >> (jj + 6)) & 3) << 4);
+        mn = ((s2 >> (jj + 4)) & 15) | (((s1 >> (jj + 6)) & 3) << 4);
+    }
+}
+
+// Q4_K unit u (chunk c = u % 4 of superblock u / 4): qs bytes 32c..32c+31 hold
+// weights 64c+l (low nibble, sub-block 2c) and 64c+32+l (high nibble, sub-block 2c+1).
+__device__ __forceinline__ void decode_q4_K(const uint8_t *row, int u, Unit &o) {
+    const uint8_t *blk = row + (u >> 2) * kQ4KBytes;
+    const int c = u & 3;
+    const uint4 h = ldg16(blk);
+    const uint4 a = ldg16(blk + 16 + 32 * c);
+    const uint4 b = ldg16(blk + 32 + 32 * c);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        o.q[i] = (int)(w[i] & 0x0f0f0f0fu);
+        o.q[8 + i] = (int)((w[i] >> 4) & 0x0f0f0f0fu);
+    }
+    const float d = half_lo(h.x), dmin = half_hi(h.x);
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(h.y, h.z, h.w, 2 * c, sc0, m0);
+    q4k_scale_min(h.y, h.z, h.w, 2 * c + 1, sc1, m1);
+    o.isc[0] = o.isc[1] = sc0;
+    o.isc[2] = o.isc[3] = sc1;
+    o.fd[0] = o.fd[1] = d;
+    o.fm[0] = dmin * (float)m0;
+    o.fm[1] = dmin * (float)m1;
+}
+
+// Load n 4-byte words starting at a 2-byte aligned address p into w[0..n-1]
+// (byte i of the stream = byte p[i]).  Reads whole aligned words only: when p is
+// not 4-byte aligned it also touches the 2 bytes before p and the 2 bytes after
+// p + 4n, so callers keep [p-2, p+4n+2) inside the buffer.
+template <int N>
+__device__ __forceinline__ void ldg_words_a2(const uint8_t *p, uint32_t (&w)[N]) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t *base = reinterpret_cast<const uint32_t *>(a & ~uintptr_t(3));
+    if ((a & 3) == 0) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) w[i] = ldg4(base + i);
+    } else {
+        uint32_t prev = ldg4(base);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const uint32_t next = ldg4(base + i + 1);
+            w[i] = __funnelshift_r(prev, next, 16);
+            prev = next;
+        }
+    }
+}
+
+// Q6_K unit u (v = u % 4 of superblock u / 4) covers weights 64v..64v+63 of the
+// superblock: half h = v/2, groups t = 2(v%2) and 2(v%2)+1.  Weight 128h+32t+l takes
+// its low 4 bits from ql[64h + 32(t&1) + l] (nibble t>>1) and its top 2 bits from
+// bits 2t..2t+1 of qh[32h + l] ([MMQ] section "Q6_K: 6 位数据要多占一半的共享内存").
+__device__ __forceinline__ void decode_q6_K(const uint8_t *row, int u, Unit &o) {
+    const uint8_t *blk = row + (u >> 2) * kQ6KBytes;
+    const int v = u & 3, h = v >> 1, p = v & 1;
+    // A block that is not 4-byte aligned starts 2 bytes past a word boundary, so the
+    // 2 bytes before it belong to the previous block of the same buffer; every word
+    // read below ends at or before byte 210 of this block.
+    uint32_t ql[16], qh[8], tail[4];
+    ldg_words_a2<16>(blk + 64 * h, ql);        // ql[64h .. 64h+64)
+    ldg_words_a2<8>(blk + 128 + 32 * h, qh);   // qh[32h .. 32h+32)
+    ldg_words_a2<4>(blk + 192, tail);          // 16 int8 sub-scales
+    const int shift_l = 4 * p;
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+        const int t = 2 * p + tt;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = (ql[8 * tt + i] >> shift_l) & 0x0f0f0f0fu;
+            const uint32_t hi = ((qh[i] >> (2 * t)) & 0x03030303u) << 4;
+            o.q[8 * tt + i] = (int)__vsub4(lo | hi, 0x20202020u);
+        }
+    }
+    const int j0 = 4 * v;  // first 16-wide sub-block of this unit
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = j0 + i;
+        o.isc[i] = (int)(int8_t)((tail[j >> 2] >> (8 * (j & 3))) & 0xff);
+    }
+    const float d = half_lo(ldg2(blk + 208));
+    o.fd[0] = o.fd[1] = d;
+    o.fm[0] = o.fm[1] = 0.f;
+}
+
+// Q8_0 unit u: blocks 2u and 2u+1 (68 bytes at offset 68u of the row).  Rows with an
+// odd number of blocks are only 2-byte aligned, so the words come through
+// ldg_words_a2: a two-block unit is never the last unit of its row, so the 2 bytes
+// after it exist; a single-block unit (odd block count, last unit of the row) reads
+// its 34 bytes as 8 words plus one 2-byte load.
+__device__ __forceinline__ void decode_q8_0(const uint8_t *row, int u, bool two, Unit &o) {
+    const uint8_t *p = row + 68 * u;
+    uint32_t w[17];
+    if (two) {
+        ldg_words_a2<17>(p, w);
+    } else {
+        uint32_t a[8];
+        ldg_words_a2<8>(p, a);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = a[i];
+        w[8] = ldg2(p + 32);
+#pragma unroll
+        for (int i = 9; i < 17; ++i) w[i] = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o.q[i] = (int)__funnelshift_r(w[i], w[i + 1], 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o.q[8 + i] = (int)w[9 + i];
+    o.isc[0] = o.isc[1] = o.isc[2] = o.isc[3] = 1;
+    o.fd[0] = half_lo(w[0]);
+    o.fd[1] = two ? half_hi(w[8]) : 0.f;
+    o.fm[0] = o.fm[1] = 0.f;
+}
+
+template <int T>
+__device__ __forceinline__ void decode_unit(const uint8_t *row, int u, int nblk32, Unit &o) {
+    if constexpr (T == QMM_Q4_K) decode_q4_K(row, u, o);
+    else if constexpr (T == QMM_Q6_K) decode_q6_K(row, u, o);
+    else decode_q8_0(row, u, 2 * u + 1 < nblk32, o);
+}
+
+}  // namespace qmm

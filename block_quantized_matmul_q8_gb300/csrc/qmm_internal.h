@@ -1,0 +1,45 @@
+// qmm_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "qmm.h"
+
+namespace qmm {
+
+// SM count of the current device (cached per device).
+int device_sm_count();
+// Opt-in shared memory per block of the current device (cached per device).
+int device_smem_optin();
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_quantize_q8_1(const float *x, int64_t m, int64_t k, void *xq, cudaStream_t st);
+
+// GEMV, m <= 8: y[m][n] from W rows and q8_1 activations.  Columns beyond the shared
+// memory budget are processed in several launches by the caller.
+size_t gemv_smem_bytes(int64_t k, int ncols);
+cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                        cudaStream_t st);
+
+// CUDA-core tiled GEMM (dp4a), any m.
+cudaError_t launch_gemm_dp4a(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                             cudaStream_t st);
+
+// Tensor-core GEMM (tcgen05, kind::f16 on integer-valued operands).
+int64_t gemm_tc_tile_m(int64_t m);
+size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m);
+bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
+cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                           void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st);
+
+// MoE: device bucketing + grouped GEMM.
+size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k);
+cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                              const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *ws,
+                              size_t ws_bytes, cudaStream_t st);
+
+// Offset of the device status word inside a mul_mat_id workspace.
+constexpr size_t kStatusOffset = 0;
+
+}  // namespace qmm

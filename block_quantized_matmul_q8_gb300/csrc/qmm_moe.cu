@@ -1,0 +1,195 @@
+// qmm_moe.cu -- expert-routed matmul: device bucketing and the grouped launch.
+//
+// [MMQ] sections "专家边界: 在 GPU 上做分段, 而不是在 host 上" and "MoE 的二次账":
+// the (token, slot) pairs are sorted by expert on the device into expert_bounds and
+// a pair list, so the host never reads the routing ids and the call stays
+// asynchronous; each expert's pairs are cut into tiles of up to `tile_tokens`
+// columns and every tile of every expert goes into one work list, which one
+// persistent launch walks ([MMQ] section "局限与工程含义": merging the experts'
+// small GEMMs into one schedule).
+//
+// Bucketing is a stable counting sort done by one CTA:
+//   pass 1  counts per expert (shared-memory atomics) and invalid ids;
+//   scan    bounds[e] (exclusive prefix) and each expert's tile offset;
+//   pass 2  rounds of 1024 pairs; within a warp, lanes with the same expert find
+//           each other with __match_any_sync, a per-(warp, expert) count table is
+//           scanned over warps, and each pair lands at
+//           bounds[e] + (earlier rounds) + (earlier warps) + (earlier lanes).
+//   Invalid pairs are appended after the valid ones; their output rows are zeroed.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "qmm_common.cuh"
+#include "qmm_internal.h"
+#include "qmm_moe.h"
+
+namespace qmm {
+
+constexpr int kBucketThreads = 1024;
+constexpr int kBucketWarps = kBucketThreads / 32;
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+MoELayout moe_layout(int64_t n_pairs, int64_t n_experts, int tile_tokens, size_t gemm_bytes) {
+    MoELayout L{};
+    size_t off = 0;
+    L.status = off;
+    off += 256;
+    L.bounds = off;
+    off = align256(off + sizeof(int32_t) * size_t(n_experts + 1));
+    L.perm = off;
+    off = align256(off + sizeof(int32_t) * size_t(n_pairs));
+    L.tiles = off;
+    const int64_t max_tiles = n_pairs / tile_tokens + n_experts + 1;
+    off = align256(off + sizeof(MoETile) * size_t(max_tiles));
+    L.gemm = off;
+    off = align256(off + gemm_bytes);
+    L.total = off;
+    return L;
+}
+
+__global__ void __launch_bounds__(kBucketThreads) moe_bucket_kernel(const int32_t *__restrict__ ids, int64_t n_pairs,
+                                                                    int E, int tile_tokens, int32_t *status,
+                                                                    int32_t *bounds, int32_t *perm, MoETile *tiles) {
+    extern __shared__ __align__(16) int32_t sm[];
+    int32_t *cnt = sm;                          // [E]   counts, then running bases
+    int32_t *toff = cnt + E;                    // [E]   tile offsets
+    int32_t *wcnt = toff + E;                   // [32][E] per-warp counts of a round
+    int32_t *wofs = wcnt + kBucketWarps * E;    // [32][E] per-warp offsets of a round
+    __shared__ int32_t s_bad, s_bad_pos;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int i = tid; i < E; i += kBucketThreads) cnt[i] = 0;
+    for (int i = tid; i < kBucketWarps * E; i += kBucketThreads) wcnt[i] = 0;
+    if (tid == 0) {
+        s_bad = 0;
+        s_bad_pos = 0;
+    }
+    __syncthreads();
+
+    // pass 1: counts
+    for (int64_t i = tid; i < n_pairs; i += kBucketThreads) {
+        const int e = ids[i];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else atomicAdd(&s_bad, 1);
+    }
+    __syncthreads();
+
+    // scan (one thread: E <= kMaxExperts)
+    if (tid == 0) {
+        int run = 0, trun = 0;
+        for (int e = 0; e < E; ++e) {
+            const int c = cnt[e];
+            bounds[e] = run;
+            cnt[e] = run;  // running base for pass 2
+            toff[e] = trun;
+            run += c;
+            trun += (c + tile_tokens - 1) / tile_tokens;
+        }
+        bounds[E] = run;
+        status[0] = s_bad ? (int32_t)QMM_ERR_IDS : (int32_t)QMM_OK;
+        status[1] = trun;
+        status[2] = s_bad;
+    }
+    __syncthreads();
+
+    // tile list
+    for (int e = warp; e < E; e += kBucketWarps) {
+        const int b0 = bounds[e], c = bounds[e + 1] - b0;
+        const int nt = (c + tile_tokens - 1) / tile_tokens;
+        for (int t = lane; t < nt; t += 32) {
+            MoETile mt;
+            mt.expert = e;
+            mt.first = t * tile_tokens;
+            mt.count = c;
+            mt.pad = 0;
+            tiles[toff[e] + t] = mt;
+        }
+    }
+
+    // pass 2: stable scatter, rounds of kBucketThreads pairs
+    const int nvalid = bounds[E];
+    for (int64_t base = 0; base < n_pairs; base += kBucketThreads) {
+        const int64_t i = base + tid;
+        const int e = i < n_pairs ? ids[i] : -1;
+        const bool valid = e >= 0 && e < E;
+        const unsigned key = valid ? (unsigned)e : (unsigned)(E + lane);  // invalid lanes stay alone
+        const unsigned grp = __match_any_sync(0xffffffffu, key);
+        const unsigned lt = grp & ((1u << lane) - 1u);
+        const int rank = __popc(lt);
+        if (valid && lt == 0) wcnt[warp * E + e] = __popc(grp);
+        __syncthreads();
+        for (int x = tid; x < E; x += kBucketThreads) {
+            int run = cnt[x];
+            for (int w = 0; w < kBucketWarps; ++w) {
+                const int c = wcnt[w * E + x];
+                wofs[w * E + x] = run;
+                wcnt[w * E + x] = 0;
+                run += c;
+            }
+            cnt[x] = run;
+        }
+        __syncthreads();
+        if (valid) perm[wofs[warp * E + e] + rank] = (int32_t)i;
+        // invalid pairs go after the valid ones, in index order
+        const unsigned bad = __ballot_sync(0xffffffffu, i < n_pairs && !valid);
+        if (bad) {
+            int wbase = 0;
+            if (lane == 0) wbase = atomicAdd(&s_bad_pos, __popc(bad));  // warps may interleave; order within a warp kept
+            wbase = __shfl_sync(0xffffffffu, wbase, 0);
+            if (i < n_pairs && !valid) perm[nvalid + wbase + __popc(bad & ((1u << lane) - 1u))] = (int32_t)i;
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void moe_zero_invalid_kernel(const int32_t *status, const int32_t *perm, const int32_t *bounds, int E,
+                                        float *y, int64_t n) {
+    const int nbad = status[2];
+    const int nvalid = bounds[E];
+    for (int b = blockIdx.x; b < nbad; b += gridDim.x) {
+        float *row = y + int64_t(perm[nvalid + b]) * n;
+        for (int64_t j = threadIdx.x; j < n; j += blockDim.x) row[j] = 0.f;
+    }
+}
+
+cudaError_t launch_moe_bucket(const int32_t *ids, int64_t n_pairs, int n_experts, int tile_tokens, void *ws,
+                              const MoELayout &L, cudaStream_t st) {
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    const size_t smem = sizeof(int32_t) * size_t(n_experts) * (2 + 2 * kBucketWarps);
+    cudaError_t e = cudaFuncSetAttribute(moe_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    moe_bucket_kernel<<<1, kBucketThreads, smem, st>>>(
+        ids, n_pairs, n_experts, tile_tokens, reinterpret_cast<int32_t *>(base + L.status),
+        reinterpret_cast<int32_t *>(base + L.bounds), reinterpret_cast<int32_t *>(base + L.perm),
+        reinterpret_cast<MoETile *>(base + L.tiles));
+    return cudaGetLastError();
+}
+
+size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k) {
+    (void)t; (void)n; (void)k;
+    return moe_layout(n_tokens * top_k, n_experts, 64, 0).total;
+}
+
+cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                              const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *ws,
+                              size_t ws_bytes, cudaStream_t st) {
+    const int tile_tokens = 64;
+    const int64_t n_pairs = n_tokens * top_k;
+    const MoELayout L = moe_layout(n_pairs, n_experts, tile_tokens, 0);
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    cudaError_t e = launch_moe_bucket(ids, n_pairs, (int)n_experts, tile_tokens, ws, L, st);
+    if (e != cudaSuccess) return e;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    const int32_t *status = reinterpret_cast<const int32_t *>(base + L.status);
+    const int32_t *bounds = reinterpret_cast<const int32_t *>(base + L.bounds);
+    const int32_t *perm = reinterpret_cast<const int32_t *>(base + L.perm);
+    const MoETile *tiles = reinterpret_cast<const MoETile *>(base + L.tiles);
+    moe_zero_invalid_kernel<<<64, 256, 0, st>>>(status, perm, bounds, (int)n_experts, y, n);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_gemm_dp4a_grouped(t, W, n, k, xq, y, tiles, status + 1, bounds, perm, (int)top_k, st);
+}
+
+}  // namespace qmm

@@ -1,0 +1,40 @@
+// qmm_moe.h -- device-side expert bucketing shared by the MoE kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qmm.h"
+
+namespace qmm {
+
+// One work item of the expert-grouped GEMM: pairs [first, min(first + tile, count))
+// of expert `expert` in the sorted order (count = that expert's pair count).
+struct MoETile {
+    int32_t expert;
+    int32_t first;
+    int32_t count;
+    int32_t pad;
+};
+
+// Largest expert count the single-CTA bucketing kernel supports.
+constexpr int kMaxExperts = 512;
+
+// Workspace layout of qmm_mul_mat_id (offsets in bytes, 256-byte aligned pieces).
+struct MoELayout {
+    size_t status;   // int32 status word, int32 tile count, int32 invalid-pair count
+    size_t bounds;   // int32 [E + 1]
+    size_t perm;     // int32 [pairs]: valid pairs sorted by expert, then invalid pairs
+    size_t tiles;    // MoETile [max tiles]
+    size_t gemm;     // scratch of the grouped GEMM
+    size_t total;
+};
+MoELayout moe_layout(int64_t n_pairs, int64_t n_experts, int tile_tokens, size_t gemm_bytes);
+
+cudaError_t launch_moe_bucket(const int32_t *ids, int64_t n_pairs, int n_experts, int tile_tokens, void *ws,
+                              const MoELayout &L, cudaStream_t st);
+
+cudaError_t launch_gemm_dp4a_grouped(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, float *y,
+                                     const MoETile *tiles, const int32_t *ntiles, const int32_t *bounds,
+                                     const int32_t *perm, int top_k, cudaStream_t st);
+
+}  // namespace qmm

@@ -1,0 +1,185 @@
+/*
+ * qmm.h -- C ABI of the block-quantized matmul library for GB300 (sm_103a).
+ *
+ * The library computes y[m][n] = sum_k x[m][k] * dequant(W)[n][k] with W kept in
+ * its block-quantized form (Q4_K, Q6_K or Q8_0) and x quantized to q8_1 first.
+ * Every product is formed from exact integer sub-block dot products that are
+ * then folded with the block scales in fp32.
+ *
+ * Sources (web pages on block-quantized matmul), cited by title and section:
+ *   [MMQ]   "llama.cpp 源码完全拆解(十五): 量化 GEMM 的矩阵编队 -- MMQ 如何把 MoE 与预填充塞满 GPU"
+ *   [P0007] "Patch 0007: an fp16 matrix-vector path for GP100"
+ *   [QMM]   "QTensor 与 QMatMul" (candle 0.11.0 notes)
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     keeps no reference to them after a call returns and allocates no device
+ *     memory per call: scratch lives in the caller's workspace.
+ *   - Every call enqueues its work on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns without synchronising the host.
+ *   - Row-major layouts.  W is [n] rows of k/QK blocks, one row per output
+ *     feature, as PyTorch Linear stores weights ([QMM] section "QMatMul:
+ *     三种形态": weights are stored [n, k]).  x is [m][k] fp32, y is [m][n] fp32.
+ *   - Argument errors are returned synchronously and nothing is enqueued.
+ *     QMM_ERR_CUDA reports a failed launch (cudaGetLastError after the launch).
+ *   - The library works on the CUDA device that is current when a call is made.
+ *
+ * Block formats (bytes, little-endian fp16 fields):
+ *   q8_1 (36 B / 32 values): fp16 d, fp16 s, int8 q[32]; s = d * sum(q)
+ *        ([MMQ] section "dp4a 路径的 Q4_K": the activation block carries d and s).
+ *   Q4_K (144 B / 256):      fp16 d, fp16 dmin, 12 B of 6-bit sub-block scales
+ *        and mins, 128 B of nibbles; w = d*sc*q - dmin*m
+ *        ([MMQ] section "Q4_K: 在加载期就把两层 scale 合并成 half2").
+ *   Q6_K (210 B / 256):      ql[128], qh[64], int8 scales[16], fp16 d;
+ *        w = d*sc*(code-32) ([MMQ] section "Q6_K: 6 位数据要多占一半的共享内存").
+ *   Q8_0 (34 B / 32):        fp16 d, int8 q[32]; w = d*q.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 12, QMM_Q6_K = 14 } qmm_type;
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_ARG = 1,       /* null pointer, m/n/k/top_k/n_experts <= 0 where not allowed */
+    QMM_ERR_SHAPE = 2,     /* k not a multiple of the block size, or a size above the library limits */
+    QMM_ERR_TYPE = 3,      /* unknown qmm_type */
+    QMM_ERR_ALIGN = 4,     /* a pointer not 16-byte aligned */
+    QMM_ERR_WORKSPACE = 5, /* workspace smaller than qmm_workspace_bytes() */
+    QMM_ERR_CUDA = 6,      /* a CUDA runtime call or kernel launch failed */
+    QMM_ERR_IDS = 7,       /* device status only: a routing id was outside [0, n_experts) */
+    QMM_ERR_DEVICE = 8     /* device status only: a kernel gave up on a bounded wait */
+} qmm_status;
+
+/* Human-readable name of a status code (static string). */
+QMM_API const char *qmm_status_string(qmm_status s);
+
+/* Bytes of the q8_1 blocks for an [m][k] activation: m * (k/32) * 36. */
+QMM_API size_t qmm_q8_1_bytes(int64_t m, int64_t k);
+
+/* Bytes of one weight row of k values in format t (k/QK blocks), 0 if k is not a
+ * multiple of the block size or t is unknown. */
+QMM_API size_t qmm_row_bytes(qmm_type t, int64_t k);
+
+/* Workspace bytes that qmm_mul_mat (n_experts == 0) or qmm_mul_mat_id
+ * (n_experts > 0) needs for these sizes.  The workspace must be 256-byte
+ * aligned device memory; its contents need no initialisation. */
+QMM_API size_t qmm_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t n_experts, int64_t top_k);
+
+/*
+ * Quantize fp32 activations to q8_1 ([MMQ] sections "引言" and
+ * "mul_mat_id 的第三条路": activations stay fp32 and are compressed to q8_1 on
+ * the device; [QMM] section "CPU: 先量化激活, 再逐行点积").
+ *   x   : fp32 [m][k], 16-byte aligned, k % 32 == 0.
+ *   xq  : output, qmm_q8_1_bytes(m, k) bytes, 16-byte aligned; block (r, b)
+ *         at byte (r*(k/32) + b)*36.
+ * Per 32-block: d = amax/127 (fp32), q = round-half-away(x/d) (IEEE fp32 division),
+ * stored fp16 d and s = fp16(d_stored * sum(q)); a block whose fp32 d is 0 is all
+ * zero.  The result is bit-identical on every run.  Non-finite x is outside the
+ * contract (the q values of such a block are unspecified).
+ */
+QMM_API qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void *xq, void *stream);
+
+/*
+ * y = x * dequant(W)^T with x given as q8_1 blocks ([MMQ] sections "形状判据",
+ * "dp4a 路径的 Q4_K", "Q6_K: 子块尺度与 q8_1 块长错位"; [QMM] section "QMatMul").
+ *   W      : [n][k/QK] blocks of type t, contiguous rows, 16-byte aligned.
+ *   xq     : q8_1 blocks of x [m][k] as written by qmm_quantize_q8_1.
+ *   y      : fp32 [m][n] output, 16-byte aligned; every element is written.
+ *   workspace, ws_bytes: at least qmm_workspace_bytes(t, n, k, m, 0, 0) bytes.
+ * k % 256 == 0 for Q4_K/Q6_K, k % 32 == 0 for Q8_0.  m <= 8 runs the GEMV path
+ * (each weight byte read once, every column reusing the decoded weight);
+ * larger m runs the tiled tensor-core GEMM with a stream-K schedule.
+ * Accuracy: |y - y_exact| <= 1e-5 * sum over blocks of |block term| per element.
+ */
+QMM_API qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                       void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Expert-routed matmul ([MMQ] sections "派发路径", "专家边界: 在 GPU 上做分段,
+ * 而不是在 host 上", "MoE 的二次账"):
+ *   y[t][s][:] = x[t] * dequant(W_experts[ids[t][s]])^T
+ *   W_experts : [n_experts][n][k/QK] blocks of type t, 16-byte aligned.
+ *   xq        : q8_1 blocks of x [n_tokens][k]; a token's row is shared by all
+ *               of its top_k slots.
+ *   ids       : int32 [n_tokens][top_k] expert ids (device memory).
+ *   y         : fp32 [n_tokens][top_k][n]; every element is written.
+ *   workspace : at least qmm_workspace_bytes(t, n, k, n_tokens, n_experts, top_k)
+ *               bytes; it also holds the device status word read by
+ *               qmm_read_device_status.
+ * The (token, slot) pairs are bucketed by expert on the device (a stable counting
+ * sort) and the per-expert tiles are walked by one persistent launch; the host
+ * never reads ids, so the call does not synchronise.  A pair whose id is outside
+ * [0, n_experts) gets a zero output row and sets QMM_ERR_IDS in the status word.
+ */
+QMM_API qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                          const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *workspace,
+                          size_t ws_bytes, void *stream);
+
+/* Copy the device status word of the last qmm_mul_mat_id on this workspace to
+ * *status (QMM_OK, QMM_ERR_IDS or QMM_ERR_DEVICE).  This call synchronises
+ * `stream`.  Returns QMM_ERR_CUDA if the copy fails. */
+QMM_API qmm_status qmm_read_device_status(const void *workspace, int32_t *status, void *stream);
+
+/* ------------------------------------------------------------------ host-side planning
+ * These functions run on the host only and never touch a GPU. */
+
+/* Tile efficiency of one-tile-per-CTA scheduling ([MMQ] section
+ * "朴素切法的负载缺口"): nwaves = ceil(ntiles/nsm), percent = 100*ntiles/(nsm*nwaves). */
+QMM_API int qmm_tile_efficiency_percent(int64_t ntiles, int64_t nsm);
+
+/* Schedule of one GEMM launch ([MMQ] sections "stream-K 的切法",
+ * "fixup: 部分和的归约", "什么时候不用 stream-K"). */
+typedef struct {
+    int64_t tiles_n;      /* tiles along the W rows (n) */
+    int64_t tiles_m;      /* tiles along the activation rows (m) */
+    int64_t ntiles;       /* tiles_n * tiles_m */
+    int64_t iters_per_tile; /* K iterations per tile */
+    int64_t nwork;        /* ntiles * iters_per_tile */
+    int32_t ctas;         /* CTAs launched */
+    int32_t stream_k;     /* 1: the flattened (tile, k-iteration) stream is split evenly over ctas */
+    int32_t fixup;        /* 1: some tile is shared by two or more CTAs and needs the fixup pass */
+    int32_t efficiency_percent; /* qmm_tile_efficiency_percent(ntiles, nsm) */
+    int32_t tile_n;       /* W rows per tile */
+    int32_t tile_m;       /* activation rows per tile */
+    int32_t iter_k;       /* K values per iteration */
+} qmm_gemm_plan;
+
+/* Fill *plan for a dense GEMM of these sizes on a GPU with nsm SMs.
+ * stream_k_mode: 0 = automatic (stream-K only when the tile efficiency is below 90%),
+ * 1 = never, 2 = always.  Returns QMM_ERR_ARG/SHAPE/TYPE on bad sizes. */
+QMM_API qmm_status qmm_plan_gemm(qmm_type t, int64_t n, int64_t k, int64_t m, int32_t nsm, int32_t stream_k_mode,
+                         qmm_gemm_plan *plan);
+
+/* The half-open range [*begin, *end) of flattened work units (tile * iters_per_tile
+ * + k-iteration) that CTA `cta` of the plan processes. */
+QMM_API void qmm_plan_cta_range(const qmm_gemm_plan *plan, int32_t cta, int64_t *begin, int64_t *end);
+
+/* ------------------------------------------------------------------ test controls
+ * Process-wide switches for tests and benchmarks; read at every call. */
+
+/* Path override for qmm_mul_mat: 0 = automatic, 1 = GEMV for any m <= 64,
+ * 2 = the CUDA-core (dp4a) tiled GEMM, 3 = the tensor-core GEMM for any m. */
+QMM_API void qmm_set_force_path(int path);
+
+/* Stream-K mode for the tensor-core GEMM: 0 = automatic, 1 = never, 2 = always. */
+QMM_API void qmm_set_stream_k_mode(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

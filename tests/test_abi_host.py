@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared symbol,
+rejects bad arguments before touching a GPU, and plans schedules as the pages'
+worked examples say.  No kernel runs here."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import block_quantized_matmul_q8_gb300 as qmm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    qmm.build()
+    return qmm.lib()
+
+
+def declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    return sorted(set(re.findall(r"QMM_API\s+[\w\s\*]*?\b(qmm_\w+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_symbols()
+    assert len(names) >= 13
+    assert sorted(qmm.EXPORTS) == names
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code, name in qmm.STATUS.items():
+        assert qmm.qmm_status_string(code) == name
+
+
+def test_sizes():
+    assert qmm.qmm_q8_1_bytes(3, 256) == 3 * 8 * 36
+    assert qmm.qmm_row_bytes("q4_K", 5120) == 20 * 144
+    assert qmm.qmm_row_bytes("q6_K", 5120) == 20 * 210
+    assert qmm.qmm_row_bytes("q8_0", 96) == 3 * 34
+    assert qmm.qmm_row_bytes("q4_K", 100) == 0
+    assert qmm.qmm_row_bytes(99, 256) == 0
+
+
+def _mm(L, W=1024, t=12, n=8, k=256, xq=2048, m=4, y=4096, ws=None, wsb=0):
+    P = ctypes.c_void_p
+    return L.qmm_mul_mat(P(W), t, n, k, P(xq), m, P(y), P(ws) if ws else None, wsb, None)
+
+
+def test_argument_errors_need_no_gpu(L):
+    assert _mm(L, t=13) == 3                      # unknown type
+    assert _mm(L, k=100) == 2                     # not a multiple of 256
+    assert _mm(L, t=8, k=48) == 2                 # Q8_0 needs k % 32
+    assert _mm(L, k=0) == 1
+    assert _mm(L, n=-1) == 1
+    assert _mm(L, W=0) == 1                       # null pointer
+    assert _mm(L, W=1032) == 4                    # misaligned
+    assert _mm(L, y=4100) == 4
+    assert _mm(L, n=0) == 0 and _mm(L, m=0) == 0  # empty problems are no-ops
+    P = ctypes.c_void_p
+    assert L.qmm_quantize_q8_1(P(1024), 2, 48, P(2048), None) == 2
+    assert L.qmm_quantize_q8_1(P(1024), 0, 64, P(2048), None) == 0
+    assert L.qmm_quantize_q8_1(P(1028), 2, 64, P(2048), None) == 4
+    # mul_mat_id: workspace and expert checks
+    args = [P(1024), 12, 4, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
+    assert L.qmm_mul_mat_id(*args, None, 0, None) == 5
+    ws_need = L.qmm_workspace_bytes(12, 8, 256, 3, 4, 2)
+    assert ws_need > 0
+    assert L.qmm_mul_mat_id(*args, P(1 << 20), ws_need - 1, None) == 5
+    assert L.qmm_mul_mat_id(*args, P((1 << 20) + 16), ws_need, None) == 4
+    bad_e = [P(1024), 12, 0, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
+    assert L.qmm_mul_mat_id(*bad_e, P(1 << 20), ws_need, None) == 1
+    many = [P(1024), 12, 100000, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
+    assert L.qmm_mul_mat_id(*many, P(1 << 20), 1 << 40, None) == 2
+
+
+def test_tile_efficiency_matches_page_examples():
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "schedule_examples.json")))
+    for c in g["tile_efficiency"]["cases"]:
+        assert qmm.qmm_tile_efficiency_percent(c["ntiles"], c["nsm"]) == c["percent"]
+
+
+def test_plan_tile_counts_match_prefill_example():
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "schedule_examples.json")))["prefill_8k_gate_up"]
+    p = qmm.qmm_plan_gemm("q4_K", g["n_rows"], 4096, g["ncols"], 108)
+    assert p.tile_n == g["I"] == 128
+    assert p.tiles_n == g["row_tiles"]
+    assert p.tiles_n * ((g["ncols"] + g["J"] - 1) // g["J"]) == g["tiles"]
+    assert p.ntiles == p.tiles_n * p.tiles_m
+
+
+@pytest.mark.parametrize("n,k,m,nsm,mode", [(14336, 4096, 512, 152, 0), (4100, 4096, 512, 152, 0),
+                                            (1024, 2048, 16, 152, 0), (1024, 2048, 16, 152, 2),
+                                            (151936, 5120, 512, 152, 0), (1536, 4096, 700, 13, 2),
+                                            (5120, 5120, 512, 152, 1)])
+def test_plan_partitions_all_work_exactly_once(n, k, m, nsm, mode):
+    p = qmm.qmm_plan_gemm("q4_K", n, k, m, nsm, mode)
+    eff = qmm.qmm_tile_efficiency_percent(p.ntiles, nsm)
+    assert p.efficiency_percent == eff
+    assert p.stream_k == (mode == 2 or (mode == 0 and eff < 90))
+    covered = 0
+    prev_end = 0
+    split_tiles = set()
+    for c in range(p.ctas):
+        b, e = qmm.qmm_plan_cta_range(p, c)
+        assert b == prev_end and e >= b
+        if b % p.iters_per_tile:
+            split_tiles.add(b // p.iters_per_tile)
+        prev_end = e
+        covered += e - b
+    assert covered == p.nwork and prev_end == p.nwork
+    assert p.fixup == (len(split_tiles) > 0)
+    if p.stream_k:
+        assert p.ctas == min(nsm, p.nwork)
+        sizes = [qmm.qmm_plan_cta_range(p, c)[1] - qmm.qmm_plan_cta_range(p, c)[0] for c in range(p.ctas)]
+        assert max(sizes) - min(sizes) <= 1

@@ -1,0 +1,154 @@
+"""GPU parity: every path of the CUDA library against the CPU oracle on the same
+seeded inputs.  q8_1 must be bit-exact; y must satisfy |y - y_oracle| <= 1e-5 * T
+with T the per-element sum of |block terms|."""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_matmul_q8_gb300 as qmm
+import qmm_synth
+from parity import TOL, adversarial_x_rows, assert_within
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    qmm.build()
+    qmm.lib()
+    yield
+    qmm.qmm_set_force_path(0)
+    qmm.qmm_set_stream_k_mode(0)
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def run_mul_mat(W, fmt, n, k, xq, m, path=0):
+    qmm.qmm_set_force_path(path)
+    try:
+        y = qmm.qmm_mul_mat(to_dev(W), fmt, n, k, to_dev(xq), m)
+        torch.cuda.synchronize()
+    finally:
+        qmm.qmm_set_force_path(0)
+    return y.cpu().numpy()
+
+
+# ---------------------------------------------------------------- quantizer
+
+@pytest.mark.parametrize("m,k", [(1, 32), (3, 5120), (16, 2048), (2048, 4096), (7, 96)])
+def test_quantize_bitexact_random(oracle_mod, m, k):
+    x = qmm_synth.gen_x(np.random.default_rng(m * 1000 + k), m, k)
+    x[0, :32] *= 1000.0
+    got = qmm.qmm_quantize_q8_1(to_dev(x)).cpu().numpy()
+    assert np.array_equal(got, oracle_mod.quantize_q8_1(x))
+
+
+def test_quantize_bitexact_adversarial(oracle_mod):
+    x = adversarial_x_rows().reshape(1, -1)
+    got = qmm.qmm_quantize_q8_1(to_dev(x)).cpu().numpy()
+    assert np.array_equal(got, oracle_mod.quantize_q8_1(x))
+
+
+def test_quantize_tie_and_scale_edges(oracle_mod):
+    """Values that land exactly on .5 after the fp32 division, for many scales."""
+    rng = np.random.default_rng(9)
+    rows = []
+    for _ in range(64):
+        amax = np.float32(rng.uniform(0.01, 100))
+        d = amax / np.float32(127)
+        q = rng.integers(-126, 127, 32).astype(np.float32)
+        x = ((q + np.float32(0.5)) * d).astype(np.float32)
+        x[rng.integers(0, 32)] = amax
+        rows.append(x)
+    x = np.stack(rows).reshape(2, -1)
+    got = qmm.qmm_quantize_q8_1(to_dev(x)).cpu().numpy()
+    assert np.array_equal(got, oracle_mod.quantize_q8_1(x))
+
+
+# ---------------------------------------------------------------- GEMV (m <= 8)
+
+GEMV_SHAPES = {"q4_K": [(1, 256), (7, 512), (129, 2304)], "q6_K": [(1, 256), (7, 512), (129, 2304)],
+               "q8_0": [(1, 32), (7, 96), (129, 1056), (33, 2048)]}
+
+
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q8_0"])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_gemv_parity(oracle_mod, fmt, m):
+    for (n, k) in GEMV_SHAPES[fmt]:
+        W, x = qmm_synth.make_dense(fmt, n, k, m, seed=n + k + m)
+        xq = oracle_mod.quantize_q8_1(x)
+        y_ref, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
+        assert_within(run_mul_mat(W, fmt, n, k, xq, m, path=1), y_ref, T, f"gemv {fmt} n={n} k={k} m={m}")
+
+
+# ---------------------------------------------------------------- tiled GEMM paths
+
+GEMM_CASES = [("q4_K", 129, 512, 9), ("q4_K", 300, 1024, 65), ("q4_K", 64, 256, 130), ("q4_K", 1, 256, 17),
+              ("q6_K", 129, 512, 17), ("q6_K", 200, 768, 64), ("q8_0", 129, 1056, 33), ("q8_0", 70, 96, 127)]
+
+
+@pytest.mark.parametrize("fmt,n,k,m", GEMM_CASES)
+@pytest.mark.parametrize("path", [2, 0])
+def test_gemm_parity(oracle_mod, fmt, n, k, m, path):
+    W, x = qmm_synth.make_dense(fmt, n, k, m, seed=3 * n + k + m)
+    xq = oracle_mod.quantize_q8_1(x)
+    y_ref, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
+    assert_within(run_mul_mat(W, fmt, n, k, xq, m, path=path), y_ref, T, f"gemm path={path} {fmt} n={n} k={k} m={m}")
+
+
+@pytest.mark.parametrize("m", [1, 4, 8, 9, 16])
+def test_gemv_and_gemm_agree(oracle_mod, m):
+    """The same m through the GEMV and the tiled GEMM: both within the bound, and
+    within 2x the bound of each other."""
+    n, k = 257, 1024
+    W, x = qmm_synth.make_dense("q4_K", n, k, m, seed=77 + m)
+    xq = oracle_mod.quantize_q8_1(x)
+    y_ref, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    a = run_mul_mat(W, "q4_K", n, k, xq, m, path=1)
+    b = run_mul_mat(W, "q4_K", n, k, xq, m, path=2)
+    assert_within(a, y_ref, T, "gemv")
+    assert_within(b, y_ref, T, "gemm")
+    assert np.all(np.abs(a.astype(np.float64) - b) <= 2 * TOL * T)
+
+
+def test_zero_activation_gives_exact_zero(oracle_mod):
+    n, k, m = 65, 512, 12
+    W, _ = qmm_synth.make_dense("q4_K", n, k, m)
+    xq = oracle_mod.quantize_q8_1(np.zeros((m, k), np.float32))
+    for path in (1, 2, 0):
+        if path == 1 and m > 8:
+            continue
+        y = run_mul_mat(W, "q4_K", n, k, xq, m, path=path)
+        assert np.all(y == 0)
+
+
+# ---------------------------------------------------------------- MoE
+
+def moe_check(oracle_mod, E, n, k, T_, K, seed, corrupt=0):
+    W, x, ids = qmm_synth.make_moe(E, n, k, T_, K, seed=seed)
+    if corrupt:
+        rng = np.random.default_rng(seed)
+        for _ in range(corrupt):
+            ids[rng.integers(0, T_), rng.integers(0, K)] = rng.choice([-1, E, E + 5])
+    xq = oracle_mod.quantize_q8_1(x)
+    y_ref, Tr, bad = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, xq, ids)
+    ws = torch.empty(qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, K), dtype=torch.uint8, device=DEV)
+    y = torch.full((T_, K, n), float("nan"), device=DEV)
+    qmm.qmm_mul_mat_id(to_dev(W), "q4_K", E, n, k, to_dev(xq), to_dev(ids), K, T_, y=y, workspace=ws)
+    status = qmm.qmm_read_device_status(ws)
+    assert status == (7 if bad else 0)
+    assert_within(y.cpu().numpy(), y_ref, Tr, f"moe E={E} n={n} k={k} T={T_} K={K}")
+
+
+@pytest.mark.parametrize("E,n,k,T_,K", [(4, 64, 256, 9, 2), (16, 130, 512, 70, 4), (128, 96, 256, 512, 8),
+                                        (3, 33, 512, 200, 3)])
+def test_moe_parity(oracle_mod, E, n, k, T_, K):
+    moe_check(oracle_mod, E, n, k, T_, K, seed=E + n + T_)
+
+
+def test_moe_invalid_ids_flagged_and_zeroed(oracle_mod):
+    moe_check(oracle_mod, 8, 64, 256, 40, 4, seed=5, corrupt=6)
