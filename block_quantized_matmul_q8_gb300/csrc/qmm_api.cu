@@ -66,12 +66,14 @@ static qmm_status check_k(qmm_type t, int64_t k) {
 static qmm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
 // Which kernel family qmm_mul_mat uses for these sizes.
-enum Path { kGemv = 1, kGemmDp4a = 2, kGemmTc = 3 };
+enum Path { kGemv = 1, kGemmDp4a = 2, kGemmTc = 3, kGemvDirect = 4 };
+
+bool gemv_tma_enabled() { return g_force_path.load(std::memory_order_relaxed) != kGemvDirect; }
 
 static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
     const int force = g_force_path.load(std::memory_order_relaxed);
     const bool gemv_fits = gemv_smem_bytes(k, 1) <= size_t(device_smem_optin());
-    if (force == kGemv && gemv_fits && m <= 64) return kGemv;
+    if ((force == kGemv || force == kGemvDirect) && gemv_fits && m <= 64) return kGemv;
     if (force == kGemmDp4a) return kGemmDp4a;
     if (force == kGemmTc && gemm_tc_supported(t, n, k, m)) return kGemmTc;
     if (m <= 8 && gemv_fits) return kGemv;

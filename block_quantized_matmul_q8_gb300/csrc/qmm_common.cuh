@@ -186,6 +186,142 @@ __device__ __forceinline__ void decode_q8_0(const uint8_t *row, int u, bool two,
     o.fm[0] = o.fm[1] = 0.f;
 }
 
+// ---------------------------------------------------------------------------
+// Two-phase decode for latency hiding: load_raw<T> issues only the loads of one unit
+// (no arithmetic on loaded data, so a caller can put many units' loads in flight
+// before the first one is used), convert_raw<T> turns the words into a Unit.
+// The loads stay inside the same byte ranges as the one-phase decoders above.
+
+template <int T> struct Raw;
+template <> struct Raw<QMM_Q4_K> { uint4 h, a, b; };
+template <> struct Raw<QMM_Q6_K> { uint32_t ql[17], qh[9], sc[5]; uint32_t shift; };
+template <> struct Raw<QMM_Q8_0> { uint32_t w[18]; uint32_t shift; bool two; };
+
+// units per lane kept in flight by the GEMV
+template <int T> constexpr int kRawChunk = T == QMM_Q4_K ? 5 : T == QMM_Q6_K ? 2 : 3;
+
+__device__ __forceinline__ void load_raw(const uint8_t *row, int u, int, Raw<QMM_Q4_K> &r) {
+    const uint8_t *blk = row + (u >> 2) * kQ4KBytes;
+    const int c = u & 3;
+    r.h = ldg16(blk);
+    r.a = ldg16(blk + 16 + 32 * c);
+    r.b = ldg16(blk + 32 + 32 * c);
+}
+
+__device__ __forceinline__ void convert_raw(const Raw<QMM_Q4_K> &r, int u, Unit &o) {
+    const int c = u & 3;
+    const uint32_t w[8] = {r.a.x, r.a.y, r.a.z, r.a.w, r.b.x, r.b.y, r.b.z, r.b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        o.q[i] = (int)(w[i] & 0x0f0f0f0fu);
+        o.q[8 + i] = (int)((w[i] >> 4) & 0x0f0f0f0fu);
+    }
+    const float d = half_lo(r.h.x), dmin = half_hi(r.h.x);
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(r.h.y, r.h.z, r.h.w, 2 * c, sc0, m0);
+    q4k_scale_min(r.h.y, r.h.z, r.h.w, 2 * c + 1, sc1, m1);
+    o.isc[0] = o.isc[1] = sc0;
+    o.isc[2] = o.isc[3] = sc1;
+    o.fd[0] = o.fd[1] = d;
+    o.fm[0] = dmin * (float)m0;
+    o.fm[1] = dmin * (float)m1;
+}
+
+// Q6_K: a block is either 4-byte aligned or 2 bytes past a word boundary (then the
+// 2 bytes before it belong to the previous block).  Aligned: ql/qh load one word past
+// their range (still inside the block), the scales load 4 words + the fp16 d as a
+// 2-byte load.  Misaligned: every part starts one halfword early; the scale words
+// [190, 210) end exactly at the block end.
+__device__ __forceinline__ void load_raw(const uint8_t *row, int u, int, Raw<QMM_Q6_K> &r) {
+    const uint8_t *blk = row + (u >> 2) * kQ6KBytes;
+    const int v = u & 3, h = v >> 1;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(blk);
+    const uint32_t mis = (uint32_t)(a & 2u);  // 0 or 2
+    r.shift = mis * 8u;                       // 0 or 16 bits
+    const uint32_t *ql = reinterpret_cast<const uint32_t *>((a + 64 * h) - mis);
+    const uint32_t *qh = reinterpret_cast<const uint32_t *>((a + 128 + 32 * h) - mis);
+    const uint32_t *sc = reinterpret_cast<const uint32_t *>((a + 192) - mis);
+#pragma unroll
+    for (int i = 0; i < 17; ++i) r.ql[i] = ldg4(ql + i);
+#pragma unroll
+    for (int i = 0; i < 9; ++i) r.qh[i] = ldg4(qh + i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.sc[i] = ldg4(sc + i);
+    r.sc[4] = mis ? ldg4(sc + 4) : ldg2(sc + 4);
+}
+
+__device__ __forceinline__ void convert_raw(const Raw<QMM_Q6_K> &r, int u, Unit &o) {
+    const int v = u & 3, p = v & 1;
+    uint32_t ql[16], qh[8], sc[5];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ql[i] = __funnelshift_r(r.ql[i], r.ql[i + 1], r.shift);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qh[i] = __funnelshift_r(r.qh[i], r.qh[i + 1], r.shift);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] = __funnelshift_r(r.sc[i], r.sc[i + 1], r.shift);
+    sc[4] = r.shift ? (r.sc[4] >> 16) : r.sc[4];  // the fp16 d
+    const int shift_l = 4 * p;
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+        const int t = 2 * p + tt;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = (ql[8 * tt + i] >> shift_l) & 0x0f0f0f0fu;
+            const uint32_t hi = ((qh[i] >> (2 * t)) & 0x03030303u) << 4;
+            o.q[8 * tt + i] = (int)__vsub4(lo | hi, 0x20202020u);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = 4 * v + i;
+        o.isc[i] = (int)(int8_t)((sc[j >> 2] >> (8 * (j & 3))) & 0xff);
+    }
+    o.fd[0] = o.fd[1] = half_lo(sc[4]);
+    o.fm[0] = o.fm[1] = 0.f;
+}
+
+// Q8_0: a unit of two blocks is 68 bytes at 68u; rows with an odd block count are
+// only 2-byte aligned.  Two-block units are never the last unit of their row, so a
+// misaligned load of 18 words [68u-2, 68u+70) stays inside the row's bytes plus the
+// next unit's; a single-block unit reads exactly [68u, 68u+34) (or from 68u-2).
+__device__ __forceinline__ void load_raw(const uint8_t *row, int u, int nblk32, Raw<QMM_Q8_0> &r) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row + 68 * u);
+    const uint32_t mis = (uint32_t)(a & 2u);
+    r.shift = mis * 8u;
+    r.two = 2 * u + 1 < nblk32;
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(a - mis);
+    if (r.two) {
+#pragma unroll
+        for (int i = 0; i < 17; ++i) r.w[i] = ldg4(p + i);
+        r.w[17] = mis ? ldg4(p + 17) : 0u;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r.w[i] = ldg4(p + i);
+        r.w[8] = mis ? ldg4(p + 8) : ldg2(p + 8);
+#pragma unroll
+        for (int i = 9; i < 18; ++i) r.w[i] = 0u;
+    }
+}
+
+__device__ __forceinline__ void convert_raw(const Raw<QMM_Q8_0> &r, int, Unit &o) {
+    uint32_t w[17];
+#pragma unroll
+    for (int i = 0; i < 17; ++i) w[i] = __funnelshift_r(r.w[i], r.w[i + 1], r.shift);
+    if (!r.two) {
+        w[8] &= 0xffffu;
+#pragma unroll
+        for (int i = 9; i < 17; ++i) w[i] = 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o.q[i] = (int)__funnelshift_r(w[i], w[i + 1], 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o.q[8 + i] = (int)w[9 + i];
+    o.isc[0] = o.isc[1] = o.isc[2] = o.isc[3] = 1;
+    o.fd[0] = half_lo(w[0]);
+    o.fd[1] = r.two ? half_hi(w[8]) : 0.f;
+    o.fm[0] = o.fm[1] = 0.f;
+}
+
 template <int T>
 __device__ __forceinline__ void decode_unit(const uint8_t *row, int u, int nblk32, Unit &o) {
     if constexpr (T == QMM_Q4_K) decode_q4_K(row, u, o);

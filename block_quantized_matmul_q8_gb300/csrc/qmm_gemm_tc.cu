@@ -1,16 +1,649 @@
-// qmm_gemm_tc.cu -- tensor-core GEMM (placeholder until the tcgen05 kernel lands).
+// qmm_gemm_tc.cu -- tensor-core GEMM for m > 8 (tcgen05, TMEM accumulators, TMA).
+//
+// What it computes is the exact-integer fold of [MMQ] sections "dp4a 路径的 Q4_K"
+// and "输出端": per 32-wide sub-block an exact integer dot, folded in fp32 with the
+// activation scale d8 and the weight scales d*sc, minus dmin*m*s.
+//
+// How, on sm_103a (where tcgen05 has no int8 kind): the integer dots run as
+// kind::f16 MMAs on integer-valued fp16 operands with fp32 accumulators.  Every
+// operand value is an exact fp16 integer (activation codes |q| <= 127, weight codes
+// times the 6-bit sub-block scale <= 15*63 = 945) and every partial sum of one
+// 32-wide sub-block is an integer below 32*945*127 < 2^24, so the fp32 accumulator
+// holds the exact int32 dot whatever order the tensor core adds in.
+//
+// Tile: 128 activation rows (MMA M, TMEM lanes) x 128 weight rows (MMA N, TMEM
+// columns); K advances by half a superblock (128 values) per pipeline stage.
+//   warp 0      TMA: fp16 activation slabs (128-byte swizzle), the per-superblock
+//               s tile (for the min term) and the per-superblock d8 tile.
+//   warp 1      TMEM allocation; one lane issues the MMAs.  Each 32-wide sub-block
+//               accumulates into its own TMEM slot (a ring of 4 slots of 128
+//               columns); once per superblock one more K=16 MMA forms
+//               sum_b s[m,b] * min[n,b] (8 real terms, 8 zeros) in a slot.
+//   warps 2-5   unpack: one weight row each; Q4_K nibbles -> fp16 (q * sc) written
+//               straight into the 128-byte-swizzled K-major layout the MMA reads,
+//               the 6-bit mins -> fp16 for the min-term MMA, (d, dmin) for the epilogue.
+//   warps 6-13  epilogue: one activation row (TMEM lane) and 64 weight columns per
+//               thread; per sub-block acc += d8 * slot (fp32), per superblock
+//               total += d * acc - dmin * minslot; the running total lives in shared
+//               memory (each thread its own entries).
+// Work is a flattened stream of (tile, superblock) units split over the CTAs
+// ([MMQ] section "stream-K 的切法"); a tile shared by several CTAs is summed by a
+// separate fixup kernel in CTA order ([MMQ] section "fixup: 部分和的归约"), so no
+// CTA ever waits on another.
+#include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <mutex>
+
+#include "qmm_common.cuh"
 #include "qmm_internal.h"
+#include "qmm_tc_ptx.cuh"
 
 namespace qmm {
 
-int64_t gemm_tc_tile_m(int64_t m) { return m <= 64 ? 64 : 128; }
-size_t gemm_tc_workspace_bytes(qmm_type, int64_t, int64_t, int64_t) { return 0; }
-bool gemm_tc_supported(qmm_type, int64_t, int64_t, int64_t) { return false; }
-cudaError_t launch_gemm_tc(qmm_type, const void *, int64_t, int64_t, const void *, int64_t, float *, void *, size_t,
-                           int, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int kTM = 128;  // activation rows per tile
+constexpr int kTN = 128;  // weight rows per tile
+constexpr int kStages = 2;
+constexpr int kSlots = 4;
+constexpr int kThreads = 448;  // 14 warps
+constexpr int kEpiWarp0 = 6;
+constexpr int kMaxPartialCtas = 256;
+
+// dynamic shared memory map (offsets from a 1024-aligned base)
+constexpr uint32_t kSlabBytes = 128 * 128;                       // 128 rows x 64 fp16
+constexpr uint32_t kOffX = 0;                                     // [stage][2 slabs]
+constexpr uint32_t kOffW = kOffX + kStages * 2 * kSlabBytes;      // [stage][2 slabs]
+constexpr uint32_t kOffXmin = kOffW + kStages * 2 * kSlabBytes;   // [stage][128][32 B]
+constexpr uint32_t kOffWmin = kOffXmin + kStages * 4096;          // [stage][128][32 B]
+constexpr uint32_t kOffDX = kOffWmin + kStages * 4096;            // [2][128][8] fp32
+constexpr uint32_t kOffDD = kOffDX + 2 * 4096;                    // [2][128] float2
+constexpr uint32_t kOffTot = kOffDD + 2 * 1024;                   // [2 wg][16][128] float4
+constexpr uint32_t kSmemBytes = kOffTot + 2 * 16 * 128 * 16;
+constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+
+struct TcArgs {
+    const uint8_t *W;
+    int64_t n;
+    int64_t m;
+    int k;
+    int64_t row_bytes;
+    float *y;
+    float *partial;
+    int *status;
+    int64_t tiles_n;
+    int64_t nsb;
+    int64_t nwork;
+    int ctas;
+    int stream_k;
+};
+
+struct Barriers {
+    uint64_t x_full[kStages], x_empty[kStages], w_full[kStages], w_empty[kStages];
+    uint64_t acc_full[kSlots], acc_empty[kSlots];
+    uint64_t sd_full[2], sd_empty[2];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void cta_range(const TcArgs &a, int cta, int64_t &b, int64_t &e) {
+    if (a.stream_k) {
+        b = a.nwork * cta / a.ctas;
+        e = a.nwork * (cta + 1) / a.ctas;
+    } else {
+        b = int64_t(cta) * a.nsb;
+        e = b + a.nsb;
+    }
+}
+
+// the segments of a CTA's unit range: (tile, s0, s1) with s in [s0, s1) superblocks
+struct Seg {
+    int64_t tile, s0, s1;
+};
+__device__ __forceinline__ bool next_seg(const TcArgs &a, int64_t &u, int64_t end, Seg &sg) {
+    if (u >= end) return false;
+    sg.tile = u / a.nsb;
+    sg.s0 = u - sg.tile * a.nsb;
+    sg.s1 = min(a.nsb, sg.s0 + (end - u));
+    u += sg.s1 - sg.s0;
+    return true;
+}
+
+__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// 8 nibbles (low or high half of bytes w0, w1) -> 8 fp16 values q*sc, exact.
+// (0x6400 | q) is the fp16 value 1024 + q; fma((1024+q), sc, -1024*sc) = q*sc exactly.
+__device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w0, uint32_t w1, int shift, __half2 sc2, __half2 nsc2) {
+    uint32_t p[4];
+    const uint32_t a0 = __byte_perm(w0, 0, 0x4140), a1 = __byte_perm(w0, 0, 0x4342);
+    const uint32_t b0 = __byte_perm(w1, 0, 0x4140), b1 = __byte_perm(w1, 0, 0x4342);
+    p[0] = ((a0 >> shift) & 0x000F000Fu) | 0x64006400u;
+    p[1] = ((a1 >> shift) & 0x000F000Fu) | 0x64006400u;
+    p[2] = ((b0 >> shift) & 0x000F000Fu) | 0x64006400u;
+    p[3] = ((b1 >> shift) & 0x000F000Fu) | 0x64006400u;
+    uint4 r;
+    r.x = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[0]), sc2, nsc2));
+    r.y = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[1]), sc2, nsc2));
+    r.z = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[2]), sc2, nsc2));
+    r.w = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[3]), sc2, nsc2));
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
+                       const __grid_constant__ CUtensorMap tm_dx, TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ Barriers B;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int *abortp = &B.abort;
+
+    if (tid == 0) {
+        B.abort = 0;
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&B.x_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&B.x_empty[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&B.w_full[s]), 128);
+            ptx::mbar_init(ptx::smem_u32(&B.w_empty[s]), 1);
+        }
+        for (int s = 0; s < kSlots; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&B.acc_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&B.acc_empty[s]), 8);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&B.sd_full[s]), 1 + 128);
+            ptx::mbar_init(ptx::smem_u32(&B.sd_empty[s]), 8);
+        }
+        ptx::mbar_init(ptx::smem_u32(&B.done), 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&B.tmem_base), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = B.tmem_base;
+
+    int64_t ubeg, uend;
+    cta_range(a, blockIdx.x, ubeg, uend);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tm_x);
+            ptx::prefetch_tmap(&tm_xmin);
+            ptx::prefetch_tmap(&tm_dx);
+            int64_t u = ubeg;
+            Seg sg;
+            uint32_t x_it = 0, sd_it = 0;
+            bool ok = true;
+            while (ok && next_seg(a, u, uend, sg)) {
+                const int m0 = (int)((sg.tile / a.tiles_n) * kTM);
+                for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
+                    const uint32_t sdi = sd_it & 1;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[sdi]), ((sd_it >> 1) & 1) ^ 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sdbar = ptx::smem_u32(&B.sd_full[sdi]);
+                    ptx::mbar_arrive_expect_tx(sdbar, 128 * 8 * 4);
+                    ptx::tma_load_2d(sbase + kOffDX + sdi * 4096, &tm_dx, (int)(8 * sb), m0, sdbar);
+                    ++sd_it;
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t st = x_it % kStages;
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.x_empty[st]), ((x_it / kStages) & 1) ^ 1, abortp)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bar = ptx::smem_u32(&B.x_full[st]);
+                        ptx::mbar_arrive_expect_tx(bar, 2 * kSlabBytes + (h ? 4096u : 0u));
+                        const int kx = (int)(256 * sb + 128 * h);
+                        ptx::tma_load_2d(sbase + kOffX + st * 2 * kSlabBytes, &tm_x, kx, m0, bar);
+                        ptx::tma_load_2d(sbase + kOffX + st * 2 * kSlabBytes + kSlabBytes, &tm_x, kx + 64, m0, bar);
+                        if (h) ptx::tma_load_2d(sbase + kOffXmin + st * 4096, &tm_xmin, (int)(16 * sb), m0, bar);
+                        ++x_it;
+                    }
+                }
+            }
+            // drain: every armed copy must have landed before the CTA may exit
+            int dummy = 0;
+            for (uint32_t i = (x_it > kStages ? x_it - kStages : 0); i < x_it; ++i)
+                ptx::mbar_wait(ptx::smem_u32(&B.x_full[i % kStages]), (i / kStages) & 1, &dummy);
+            for (uint32_t i = (sd_it > 2 ? sd_it - 2 : 0); i < sd_it; ++i)
+                ptx::mbar_wait(ptx::smem_u32(&B.sd_full[i & 1]), (i >> 1) & 1, &dummy);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_f16_f32(kTM, kTN);
+            int64_t u = ubeg;
+            Seg sg;
+            uint32_t x_it = 0, g = 0;
+            bool ok = true;
+            while (ok && next_seg(a, u, uend, sg)) {
+                for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
+                    for (int h = 0; ok && h < 2; ++h) {
+                        const uint32_t st = x_it % kStages, par = (x_it / kStages) & 1;
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.x_full[st]), par, abortp) ||
+                            !ptx::mbar_wait(ptx::smem_u32(&B.w_full[st]), par, abortp)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint32_t xa = sbase + kOffX + st * 2 * kSlabBytes;
+                        const uint32_t wa = sbase + kOffW + st * 2 * kSlabBytes;
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t slot = g % kSlots;
+                            if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_empty[slot]), ((g / kSlots) & 1) ^ 1, abortp)) {
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            const uint32_t slab = (q >> 1) * kSlabBytes;
+                            for (int t = 0; t < 2; ++t) {
+                                const uint32_t koff = ((q & 1) * 2 + t) * 32;  // K16 step inside the 128-byte row
+                                ptx::mma_f16(tmem + slot * kTN, ptx::smem_desc(xa + slab + koff, 1024, 2),
+                                             ptx::smem_desc(wa + slab + koff, 1024, 2), idesc, t);
+                            }
+                            ptx::mma_commit(ptx::smem_u32(&B.acc_full[slot]));
+                            ++g;
+                        }
+                        if (ok && h == 1) {
+                            const uint32_t slot = g % kSlots;
+                            if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_empty[slot]), ((g / kSlots) & 1) ^ 1, abortp)) {
+                                ok = false;
+                                break;
+                            }
+                            ptx::tc_fence_after();
+                            ptx::mma_f16(tmem + slot * kTN, ptx::smem_desc(sbase + kOffXmin + st * 4096, 256, 6),
+                                         ptx::smem_desc(sbase + kOffWmin + st * 4096, 256, 6), idesc, 0);
+                            ptx::mma_commit(ptx::smem_u32(&B.acc_full[slot]));
+                            ++g;
+                        }
+                        ptx::mma_commit(ptx::smem_u32(&B.x_empty[st]));
+                        ptx::mma_commit(ptx::smem_u32(&B.w_empty[st]));
+                        ++x_it;
+                    }
+                }
+            }
+            // every MMA must be complete before TMEM is freed
+            ptx::mma_commit(ptx::smem_u32(&B.done));
+            int dummy = 0;
+            ptx::mbar_wait(ptx::smem_u32(&B.done), 0, &dummy);
+        }
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------------ weight unpack
+        const int r = tid - 64;  // weight row within the tile
+        int64_t u = ubeg;
+        Seg sg;
+        uint32_t w_it = 0, sd_it = 0;
+        bool ok = true;
+        while (ok && next_seg(a, u, uend, sg)) {
+            const int64_t row = (sg.tile % a.tiles_n) * kTN + r;
+            const bool valid = row < a.n;
+            const uint8_t *rowp = a.W + (valid ? row : 0) * a.row_bytes;
+            for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
+                const uint8_t *blk = rowp + sb * kQ4KBytes;
+                uint4 hd = make_uint4(0, 0, 0, 0);
+                if (valid) hd = ldg16(blk);
+                const float d = half_lo(hd.x), dmin = half_hi(hd.x);
+                // (d, dmin) for the epilogue
+                const uint32_t sdi = sd_it & 1;
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[sdi]), ((sd_it >> 1) & 1) ^ 1, abortp)) {
+                    ok = false;
+                    break;
+                }
+                reinterpret_cast<float2 *>(smem + kOffDD + sdi * 1024)[r] = make_float2(d, dmin);
+                ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[sdi]));
+                ++sd_it;
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t st = w_it % kStages;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.w_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    uint4 q4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) q4[i] = valid ? ldg16(blk + 16 + 64 * h + 16 * i) : make_uint4(0, 0, 0, 0);
+                    uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {  // slab j <-> qs chunk c = 2h + j
+                        const int c = 2 * h + j;
+                        int sc_lo, m_lo, sc_hi, m_hi;
+                        q4k_scale_min(hd.y, hd.z, hd.w, 2 * c, sc_lo, m_lo);
+                        q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sc_hi, m_hi);
+                        const __half2 s_lo = __float2half2_rn((float)sc_lo), ns_lo = __float2half2_rn(-1024.f * sc_lo);
+                        const __half2 s_hi = __float2half2_rn((float)sc_hi), ns_hi = __float2half2_rn(-1024.f * sc_hi);
+                        const uint32_t w[8] = {q4[2 * j].x, q4[2 * j].y, q4[2 * j].z, q4[2 * j].w,
+                                               q4[2 * j + 1].x, q4[2 * j + 1].y, q4[2 * j + 1].z, q4[2 * j + 1].w};
+                        uint8_t *rowdst = wst + j * kSlabBytes + r * 128;
+#pragma unroll
+                        for (int cq = 0; cq < 4; ++cq) {
+                            const uint4 lo = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 0, s_lo, ns_lo);
+                            const uint4 hi = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 4, s_hi, ns_hi);
+                            *reinterpret_cast<uint4 *>(rowdst + ((cq ^ (r & 7)) << 4)) = lo;
+                            *reinterpret_cast<uint4 *>(rowdst + (((cq + 4) ^ (r & 7)) << 4)) = hi;
+                        }
+                    }
+                    if (h == 1) {  // mins of the 8 sub-blocks as fp16, then 8 zeros (32-byte swizzle)
+                        uint32_t mm[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            int s0_, m0_, s1_, m1_;
+                            q4k_scale_min(hd.y, hd.z, hd.w, 2 * i, s0_, m0_);
+                            q4k_scale_min(hd.y, hd.z, hd.w, 2 * i + 1, s1_, m1_);
+                            mm[i] = h2bits(__floats2half2_rn((float)m0_, (float)m1_));
+                        }
+                        uint8_t *mdst = smem + kOffWmin + st * 4096 + r * 32;
+                        const int sw = (r >> 2) & 1;
+                        *reinterpret_cast<uint4 *>(mdst + ((0 ^ sw) << 4)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
+                        *reinterpret_cast<uint4 *>(mdst + ((1 ^ sw) << 4)) = make_uint4(0, 0, 0, 0);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(ptx::smem_u32(&B.w_full[st]));
+                    ++w_it;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - kEpiWarp0;       // 0..7
+        const int wg = ew >> 2;                // column half: columns 64wg .. 64wg+63
+        const int qd = warp & 3;               // TMEM lane quarter this warp may access
+        const int tl = 32 * qd + lane;         // activation row within the tile
+        float4 *tot = reinterpret_cast<float4 *>(smem + kOffTot) + (wg * 16) * 128 + tl;  // [16][128] float4
+        int64_t u = ubeg;
+        Seg sg;
+        uint32_t g = 0, sd_it = 0;
+        int seg_i = 0;
+        bool ok = true;
+        while (ok && next_seg(a, u, uend, sg)) {
+            bool first = true;
+            for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
+                const uint32_t sdi = sd_it & 1;
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_full[sdi]), (sd_it >> 1) & 1, abortp)) {
+                    ok = false;
+                    break;
+                }
+                const float4 *dxp = reinterpret_cast<const float4 *>(smem + kOffDX + sdi * 4096 + tl * 32);
+                const float4 dxa = dxp[0], dxb = dxp[1];
+                const float dx[8] = {dxa.x, dxa.y, dxa.z, dxa.w, dxb.x, dxb.y, dxb.z, dxb.w};
+                float acc[64];
+                for (int b = 0; b < 9; ++b) {
+                    const uint32_t slot = g % kSlots;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), (g / kSlots) & 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + slot * kTN + 64 * wg;
+                    if (b < 8) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            float v[32];
+                            ptx::tmem_ld_32x32b_x32(taddr + 32 * hh, v);
+                            ptx::tmem_ld_wait();
+                            if (b == 0) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) acc[32 * hh + i] = dx[0] * v[i];
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) acc[32 * hh + i] = fmaf(dx[b], v[i], acc[32 * hh + i]);
+                            }
+                        }
+                    } else {
+                        const float4 *dd = reinterpret_cast<const float4 *>(smem + kOffDD + sdi * 1024);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            float v[32];
+                            ptx::tmem_ld_32x32b_x32(taddr + 32 * hh, v);
+                            ptx::tmem_ld_wait();
+#pragma unroll
+                            for (int i4 = 0; i4 < 8; ++i4) {
+                                const int c = 32 * hh + 4 * i4;              // column within this thread's 64
+                                const int cc = 64 * wg + c;                   // column within the tile
+                                const float4 p0 = dd[cc / 2], p1 = dd[cc / 2 + 1];  // (d, dmin) of 4 columns
+                                float4 t = first ? make_float4(0.f, 0.f, 0.f, 0.f) : tot[(c / 4) * 128];
+                                t.x = fmaf(-p0.y, v[4 * i4 + 0], fmaf(p0.x, acc[c + 0], t.x));
+                                t.y = fmaf(-p0.w, v[4 * i4 + 1], fmaf(p0.z, acc[c + 1], t.y));
+                                t.z = fmaf(-p1.y, v[4 * i4 + 2], fmaf(p1.x, acc[c + 2], t.z));
+                                t.w = fmaf(-p1.w, v[4 * i4 + 3], fmaf(p1.z, acc[c + 3], t.w));
+                                tot[(c / 4) * 128] = t;
+                            }
+                        }
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[slot]));
+                    ++g;
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.sd_empty[sdi]));
+                ++sd_it;
+                first = false;
+            }
+            if (!ok) break;
+            // write the segment's result: whole tile -> y, part of a tile -> this CTA's partial slot
+            const int64_t tm = sg.tile / a.tiles_n, tn = sg.tile % a.tiles_n;
+            const int64_t token = tm * kTM + tl;
+            const int64_t col0 = tn * kTN + 64 * wg;
+            const bool full = sg.s0 == 0 && sg.s1 == a.nsb;
+            if (full) {
+                if (token < a.m) {
+                    float *dst = a.y + token * a.n + col0;
+                    const bool vec = (a.n % 4 == 0) && (col0 + 64 <= a.n);
+                    for (int i4 = 0; i4 < 16; ++i4) {
+                        const float4 t = tot[i4 * 128];
+                        if (vec) {
+                            reinterpret_cast<float4 *>(dst)[i4] = t;
+                        } else {
+                            const float tv[4] = {t.x, t.y, t.z, t.w};
+                            for (int j = 0; j < 4; ++j)
+                                if (col0 + 4 * i4 + j < a.n) dst[4 * i4 + j] = tv[j];
+                        }
+                    }
+                }
+            } else {
+                const int slotidx = seg_i == 0 ? 0 : 1;
+                float4 *dst = reinterpret_cast<float4 *>(a.partial + ((int64_t(blockIdx.x) * 2 + slotidx) * kTM + tl) * kTN +
+                                                         64 * wg);
+                for (int i4 = 0; i4 < 16; ++i4) dst[i4] = tot[i4 * 128];
+            }
+            ++seg_i;
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem, 512);
+    if (tid == 0 && B.abort && a.status) atomicExch(a.status, (int)QMM_ERR_DEVICE);
+}
+
+// q8_1 blocks -> fp16 activation codes [m][k], fp32 d8 [m][k/32], fp16 s tile
+// [m][k/256][16] (8 values then 8 zeros) for the tensor-core GEMM.
+__global__ void tc_prep_kernel(const uint8_t *__restrict__ xq, int64_t m, int k, __half *__restrict__ xh,
+                               float *__restrict__ dx, __half *__restrict__ smin, int *status) {
+    const int nb32 = k / 32;
+    const int64_t total = m * nb32;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && status) *status = (int)QMM_OK;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t r = i / nb32;
+        const int b = (int)(i - r * nb32);
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + i * kQ81Bytes);
+        const uint32_t dsw = ldg4(src);
+        uint4 *dst = reinterpret_cast<uint4 *>(xh + r * k + 32 * b);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t w0 = ldg4(src + 1 + 2 * j), w1 = ldg4(src + 2 + 2 * j);
+            const int8_t *c0 = reinterpret_cast<const int8_t *>(&w0);
+            const int8_t *c1 = reinterpret_cast<const int8_t *>(&w1);
+            uint4 o;
+            o.x = h2bits(__halves2half2(__int2half_rn(c0[0]), __int2half_rn(c0[1])));
+            o.y = h2bits(__halves2half2(__int2half_rn(c0[2]), __int2half_rn(c0[3])));
+            o.z = h2bits(__halves2half2(__int2half_rn(c1[0]), __int2half_rn(c1[1])));
+            o.w = h2bits(__halves2half2(__int2half_rn(c1[2]), __int2half_rn(c1[3])));
+            dst[j] = o;
+        }
+        dx[i] = half_lo(dsw);
+        __half *sp = smin + (r * (nb32 / 8) + b / 8) * 16;
+        sp[b % 8] = __ushort_as_half((unsigned short)(dsw >> 16));
+        sp[8 + b % 8] = __ushort_as_half(0);
+    }
+}
+
+// stream-K fixup: every tile that several CTAs share is summed in CTA order.
+__global__ void tc_fixup_kernel(TcArgs a) {
+    const int64_t t = blockIdx.x;
+    const int64_t u0 = t * a.nsb, u1 = u0 + a.nsb - 1;
+    auto owner = [&](int64_t uu) {
+        int64_t c = uu * a.ctas / a.nwork;
+        while (c + 1 < a.ctas && a.nwork * (c + 1) / a.ctas <= uu) ++c;
+        while (c > 0 && a.nwork * c / a.ctas > uu) --c;
+        return c;
+    };
+    const int64_t c0 = owner(u0), c1 = owner(u1);
+    if (c0 == c1) return;  // the tile was written whole by one CTA
+    const int64_t tm = t / a.tiles_n, tn = t % a.tiles_n;
+    for (int e = threadIdx.x; e < kTM * kTN; e += blockDim.x) {
+        const int tl = e / kTN, cl = e % kTN;
+        const int64_t token = tm * kTM + tl, col = tn * kTN + cl;
+        float s = 0.f;
+        for (int64_t c = c0; c <= c1; ++c) {
+            const int64_t cb = a.nwork * c / a.ctas;
+            const int slotidx = (cb / a.nsb == t) ? 0 : 1;  // tile t is this CTA's first segment?
+            s += a.partial[((c * 2 + slotidx) * kTM + tl) * kTN + cl];
+        }
+        if (token < a.m && col < a.n) a.y[token * a.n + col] = s;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * esize};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct TcLayout {
+    size_t status, xh, dx, smin, partial, total;
+};
+TcLayout tc_layout(int64_t m, int64_t k, int64_t partial_ctas) {
+    TcLayout L{};
+    size_t off = 256;
+    L.status = 0;
+    L.xh = off;
+    off = align256(off + size_t(m) * k * 2);
+    L.dx = off;
+    off = align256(off + size_t(m) * (k / 32) * 4);
+    L.smin = off;
+    off = align256(off + size_t(m) * (k / 256) * 32);
+    L.partial = off;
+    off = align256(off + size_t(partial_ctas) * 2 * kTM * kTN * 4);
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+int64_t gemm_tc_tile_m(int64_t) { return kTM; }
+
+bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    return t == QMM_Q4_K && k % 256 == 0 && n > 0 && m > 0 && m <= (int64_t(1) << 30);
+}
+
+size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    if (!gemm_tc_supported(t, n, k, m)) return 0;
+    const int64_t nwork = ((n + kTN - 1) / kTN) * ((m + kTM - 1) / kTM) * (k / 256);
+    return tc_layout(m, k, std::min<int64_t>(kMaxPartialCtas, nwork)).total;
+}
+
+cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                           void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st) {
+    if (!gemm_tc_supported(t, n, k, m)) return cudaErrorNotSupported;
+    qmm_gemm_plan p{};
+    const int nsm = std::min(device_sm_count(), kMaxPartialCtas);
+    if (qmm_plan_gemm(t, n, k, m, nsm, stream_k_mode, &p) != QMM_OK) return cudaErrorInvalidValue;
+    const TcLayout L = tc_layout(m, k, std::min<int64_t>(kMaxPartialCtas, p.nwork));
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    int *status = reinterpret_cast<int *>(base + L.status);
+    __half *xh = reinterpret_cast<__half *>(base + L.xh);
+    float *dx = reinterpret_cast<float *>(base + L.dx);
+    __half *smin = reinterpret_cast<__half *>(base + L.smin);
+
+    const int64_t nblk = m * (k / 32);
+    const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
+    tc_prep_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), m, (int)k, xh, dx, smin,
+                                                      status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap tm_x, tm_xmin, tm_dx;
+    if (!make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, k, m, 64, kTM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tm_xmin, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, smin, (k / 256) * 16, m, 16, kTM,
+                     CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx, k / 32, m, 8, kTM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+
+    TcArgs args{};
+    args.W = static_cast<const uint8_t *>(W);
+    args.n = n;
+    args.m = m;
+    args.k = (int)k;
+    args.row_bytes = (k / 256) * kQ4KBytes;
+    args.y = y;
+    args.partial = reinterpret_cast<float *>(base + L.partial);
+    args.status = status;
+    args.tiles_n = p.tiles_n;
+    args.nsb = p.iters_per_tile;
+    args.nwork = p.nwork;
+    args.ctas = p.ctas;
+    args.stream_k = p.stream_k;
+
+    e = cudaFuncSetAttribute(gemm_tc_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    gemm_tc_q4k_kernel<<<p.ctas, kThreads, kSmemAlloc, st>>>(tm_x, tm_xmin, tm_dx, args);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (p.stream_k && p.fixup) {
+        tc_fixup_kernel<<<(unsigned)p.ntiles, 256, 0, st>>>(args);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace qmm

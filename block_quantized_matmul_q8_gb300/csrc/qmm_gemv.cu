@@ -22,6 +22,7 @@
 
 #include "qmm_common.cuh"
 #include "qmm_internal.h"
+#include "qmm_tc_ptx.cuh"
 
 namespace qmm {
 
@@ -35,17 +36,69 @@ size_t gemv_smem_bytes(int64_t k, int ncols) {
     return size_t(ncols) * size_t(U) * (kUnitStride + 16);
 }
 
+// Fold one decoded unit into the NC column accumulators.
+template <int NC>
+__device__ __forceinline__ void fold_unit(const Unit &w, const uint8_t *xs, const float2 *xds, int U, int u,
+                                          float (&acc)[NC]) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int4 *xv = reinterpret_cast<const int4 *>(xs + (size_t(c) * U + u) * kUnitStride);
+        const float4 ds = reinterpret_cast<const float4 *>(xds + size_t(c) * 2 * U)[u];
+        int s[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const int4 xw = xv[qq];
+            int a = __dp4a(w.q[4 * qq + 0], xw.x, 0);
+            a = __dp4a(w.q[4 * qq + 1], xw.y, a);
+            a = __dp4a(w.q[4 * qq + 2], xw.z, a);
+            a = __dp4a(w.q[4 * qq + 3], xw.w, a);
+            s[qq] = a;
+        }
+        // exact int32 per 32-block: |isc*dot16| sums stay below 2^24
+        const int b0 = w.isc[0] * s[0] + w.isc[1] * s[1];
+        const int b1 = w.isc[2] * s[2] + w.isc[3] * s[3];
+        float a = acc[c];
+        a = fmaf(w.fd[0] * ds.x, (float)b0, a);
+        a = fmaf(-w.fm[0], ds.y, a);
+        a = fmaf(w.fd[1] * ds.z, (float)b1, a);
+        a = fmaf(-w.fm[1], ds.w, a);
+        acc[c] = a;
+    }
+}
+
+// Each lane keeps CH units' loads in flight: all loads of a chunk are issued before
+// the first of them is used.  The first chunk of a warp's first row pair is issued
+// before the activations are staged, so HBM traffic starts at kernel entry.
 template <int T, int NC>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const uint8_t *__restrict__ W, int64_t n, int k,
                                                             int64_t row_bytes, const uint8_t *__restrict__ xq,
                                                             float *__restrict__ y, int64_t y_ld) {
     extern __shared__ __align__(16) uint8_t smem[];
+    constexpr int CH = kRawChunk<T>;
     const int U = (int)gemv_units(k);
     const int nb32 = k / 32;
-    uint8_t *xs = smem;                                                      // [NC][U][80]
+    uint8_t *xs = smem;                                                             // [NC][U][80]
     float2 *xds = reinterpret_cast<float2 *>(smem + size_t(NC) * U * kUnitStride);  // [NC][2U]
 
-    // ---- stage the q8_1 columns
+    const int lane = threadIdx.x & 31;
+    const int l16 = lane & 15;
+    const int64_t npairs = (n + 1) / 2;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
+
+    Raw<T> raw[CH];
+    auto issue = [&](int64_t pair, int base) {
+        const int64_t r = 2 * pair + (lane >> 4);
+        const uint8_t *row = W + r * row_bytes;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int u = base + 16 * c;
+            if (r < n && u < U) load_raw(row, u, nb32, raw[c]);
+        }
+    };
+    if (warp < npairs) issue(warp, l16);
+
+    // ---- stage the q8_1 columns (the first weight loads are already in flight)
     for (int i = threadIdx.x; i < NC * nb32; i += blockDim.x) {
         const int c = i / nb32, b = i - c * nb32;
         const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (size_t(c) * nb32 + b) * kQ81Bytes);
@@ -65,54 +118,24 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const uint8_t *__res
     }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int l16 = lane & 15;
-    const int64_t npairs = (n + 1) / 2;
-    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarp = (int64_t(gridDim.x) * blockDim.x) >> 5;
-
+    bool first = true;
     for (int64_t pair = warp; pair < npairs; pair += nwarp) {
         const int64_t r = 2 * pair + (lane >> 4);
         const bool valid = r < n;
-        const uint8_t *row = W + (valid ? r : 0) * row_bytes;
         float acc[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) acc[c] = 0.f;
-
-        for (int u = l16; u < U; u += 16) {
-            Unit w;
-            if (valid) {
-                decode_unit<T>(row, u, nb32, w);
-            } else {
+        for (int base = l16; base < U; base += 16 * CH) {
+            if (!first) issue(pair, base);
+            first = false;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) w.q[i] = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) w.isc[i] = 0;
-                w.fd[0] = w.fd[1] = w.fm[0] = w.fm[1] = 0.f;
-            }
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                const int4 *xv = reinterpret_cast<const int4 *>(xs + (size_t(c) * U + u) * kUnitStride);
-                const float4 ds = reinterpret_cast<const float4 *>(xds + size_t(c) * 2 * U)[u];
-                int s[4];
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const int4 xw = xv[qq];
-                    int a = __dp4a(w.q[4 * qq + 0], xw.x, 0);
-                    a = __dp4a(w.q[4 * qq + 1], xw.y, a);
-                    a = __dp4a(w.q[4 * qq + 2], xw.z, a);
-                    a = __dp4a(w.q[4 * qq + 3], xw.w, a);
-                    s[qq] = a;
+            for (int c = 0; c < CH; ++c) {
+                const int u = base + 16 * c;
+                if (valid && u < U) {
+                    Unit w;
+                    convert_raw(raw[c], u, w);
+                    fold_unit<NC>(w, xs, xds, U, u, acc);
                 }
-                // exact int32 per 32-block: |isc*dot16| sums stay below 2^24
-                const int b0 = w.isc[0] * s[0] + w.isc[1] * s[1];
-                const int b1 = w.isc[2] * s[2] + w.isc[3] * s[3];
-                float a = acc[c];
-                a = fmaf(w.fd[0] * ds.x, (float)b0, a);
-                a = fmaf(-w.fm[0], ds.y, a);
-                a = fmaf(w.fd[1] * ds.z, (float)b1, a);
-                a = fmaf(-w.fm[1], ds.w, a);
-                acc[c] = a;
             }
         }
 #pragma unroll
@@ -129,6 +152,205 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const uint8_t *__res
             for (int c = 0; c < NC; ++c) y[c * y_ld + r] = acc[c];
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Bulk-copy variant for Q4_K (rows are whole multiples of 16 bytes): one persistent
+// CTA per SM owns a contiguous range of rows and streams it through a ring of
+// shared-memory stages with 1D bulk copies (cp.async.bulk, completion counted on an
+// mbarrier), so every byte of W moves in large contiguous transfers and up to
+// kTmaStages chunks per SM are in flight.  A dedicated producer warp issues the
+// copies; two groups of 8 consumer warps take alternate chunks (a half-warp per row,
+// lane l16 takes units l16, l16+16, ...).
+constexpr int kTmaStages = 4;
+constexpr int kTmaGroups = 2;
+constexpr int kTmaGroupWarps = 8;
+constexpr int kTmaConsumerWarps = kTmaGroups * kTmaGroupWarps;
+constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
+constexpr int kTmaChunkRows = 2 * kTmaGroupWarps;  // one row per half-warp
+
+size_t gemv_tma_smem_bytes(int64_t k, int ncols) {
+    const int64_t row_bytes = (k / 256) * kQ4KBytes;
+    return 1024 + size_t(kTmaStages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, ncols);
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Q4_K scales and mins of sub-blocks 2c and 2c+1 without a branch on c (c = 0..3):
+// for c < 2 they are the low 6 bits of bytes 2c, 2c+1 of s0 (scales) and s1 (mins);
+// for c >= 2 the low/high nibbles of bytes 2c-4, 2c-3 of s2 plus the top 2 bits of the
+// same bytes of s0 / s1.
+__device__ __forceinline__ void q4k_pair_scales(uint32_t s0, uint32_t s1, uint32_t s2, int c, int &sc0, int &sc1,
+                                                int &m0, int &m1) {
+    const int sh = 16 * (c & 1);
+    const uint32_t a0 = (s0 >> sh) & 0xffffu, a1 = (s1 >> sh) & 0xffffu, a2 = (s2 >> sh) & 0xffffu;
+    const uint32_t lo_sc = a0 & 0x3f3fu, lo_m = a1 & 0x3f3fu;
+    const uint32_t hi_sc = (a2 & 0x0f0fu) | ((a0 >> 2) & 0x3030u);
+    const uint32_t hi_m = ((a2 >> 4) & 0x0f0fu) | ((a1 >> 2) & 0x3030u);
+    const uint32_t scp = c < 2 ? lo_sc : hi_sc, mp = c < 2 ? lo_m : hi_m;
+    sc0 = scp & 0xff;
+    sc1 = scp >> 8;
+    m0 = mp & 0xff;
+    m1 = mp >> 8;
+}
+
+template <int NC>
+__global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint8_t *__restrict__ W, int64_t n,
+                                                                      int k, int64_t row_bytes,
+                                                                      const uint8_t *__restrict__ xq,
+                                                                      float *__restrict__ y, int64_t y_ld,
+                                                                      int *status) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full[kTmaStages], empty[kTmaStages];
+    __shared__ int abort_flag;
+    const int U = (int)gemv_units(k);
+    const int nb32 = k / 32;
+    const size_t stage_bytes = size_t(kTmaChunkRows) * size_t(row_bytes);
+    uint8_t *stages = smem;
+    uint8_t *xs = smem + kTmaStages * stage_bytes;
+    float2 *xds = reinterpret_cast<float2 *>(xs + size_t(NC) * U * kUnitStride);
+
+    const int64_t r0 = n * blockIdx.x / gridDim.x, r1 = n * (blockIdx.x + 1) / gridDim.x;
+    const int nchunks = (int)((r1 - r0 + kTmaChunkRows - 1) / kTmaChunkRows);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, l16 = lane & 15;
+    volatile int *abortp = &abort_flag;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < kTmaStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&empty[s]), kTmaGroupWarps);
+        }
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kTmaConsumerWarps) {
+        // ---------------- producer warp: one lane issues every copy
+        if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % kTmaStages;
+                if (c >= kTmaStages && !ptx::mbar_wait(ptx::smem_u32(&empty[s]), ((c / kTmaStages) - 1) & 1, abortp))
+                    break;
+                const int64_t a = r0 + int64_t(c) * kTmaChunkRows;
+                const int64_t b = min(r1, a + kTmaChunkRows);
+                const uint32_t bytes = uint32_t((b - a) * row_bytes);
+                const uint32_t bar = ptx::smem_u32(&full[s]);
+                ptx::mbar_arrive_expect_tx(bar, bytes);
+                bulk_copy_g2s(ptx::smem_u32(stages + s * stage_bytes), W + a * row_bytes, bytes, bar);
+                ++issued;
+            }
+            // no copy may still be writing shared memory when the CTA exits: wait for the
+            // last kTmaStages issued chunks (each wait bounded, independent of the abort flag)
+            int dummy = 0;
+            for (int c = max(0, issued - kTmaStages); c < issued; ++c)
+                ptx::mbar_wait(ptx::smem_u32(&full[c % kTmaStages]), (c / kTmaStages) & 1, &dummy);
+        }
+    } else {
+        // ---------------- consumers: stage the activations, then fold the chunks
+        for (int i = tid; i < NC * nb32; i += kTmaConsumerWarps * 32) {
+            const int c = i / nb32, b = i - c * nb32;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (size_t(c) * nb32 + b) * kQ81Bytes);
+            const uint32_t dsw = src[0];
+            uint32_t *dst =
+                reinterpret_cast<uint32_t *>(xs + (size_t(c) * U + (b >> 1)) * kUnitStride + 32 * (b & 1));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = src[1 + j];
+            xds[size_t(c) * 2 * U + b] = make_float2(half_lo(dsw), half_hi(dsw));
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumerWarps * 32) : "memory");
+
+        const int grp = warp / kTmaGroupWarps, gw = warp % kTmaGroupWarps;
+        const int rr = 2 * gw + (lane >> 4);  // row within a chunk
+        const int c4 = l16 & 3;               // qs chunk of every unit this lane takes
+        for (int c = grp; c < nchunks; c += kTmaGroups) {
+            const int s = c % kTmaStages;
+            if (!ptx::mbar_wait(ptx::smem_u32(&full[s]), (c / kTmaStages) & 1, abortp)) break;
+            const int64_t a = r0 + int64_t(c) * kTmaChunkRows;
+            const bool valid = a + rr < r1;
+            float acc[NC];
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) acc[cc] = 0.f;
+            if (valid) {
+                const uint8_t *row = stages + s * stage_bytes + size_t(rr) * row_bytes;
+                for (int u = l16; u < U; u += 16) {
+                    const uint8_t *blk = row + (u >> 2) * kQ4KBytes;
+                    const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
+                    const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c4);
+                    const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c4);
+                    const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                    int sc0, sc1, m0, m1;
+                    q4k_pair_scales(hd.y, hd.z, hd.w, c4, sc0, sc1, m0, m1);
+                    const float d = half_lo(hd.x), dmin = half_hi(hd.x);
+#pragma unroll
+                    for (int cc = 0; cc < NC; ++cc) {
+                        const int4 *xv = reinterpret_cast<const int4 *>(xs + (size_t(cc) * U + u) * kUnitStride);
+                        const float4 ds = reinterpret_cast<const float4 *>(xds + size_t(cc) * 2 * U)[u];
+                        const int4 x0 = xv[0], x1 = xv[1], x2 = xv[2], x3 = xv[3];
+                        int slo = __dp4a((int)(w[0] & 0x0f0f0f0fu), x0.x, 0);
+                        slo = __dp4a((int)(w[1] & 0x0f0f0f0fu), x0.y, slo);
+                        slo = __dp4a((int)(w[2] & 0x0f0f0f0fu), x0.z, slo);
+                        slo = __dp4a((int)(w[3] & 0x0f0f0f0fu), x0.w, slo);
+                        slo = __dp4a((int)(w[4] & 0x0f0f0f0fu), x1.x, slo);
+                        slo = __dp4a((int)(w[5] & 0x0f0f0f0fu), x1.y, slo);
+                        slo = __dp4a((int)(w[6] & 0x0f0f0f0fu), x1.z, slo);
+                        slo = __dp4a((int)(w[7] & 0x0f0f0f0fu), x1.w, slo);
+                        int shi = __dp4a((int)((w[0] >> 4) & 0x0f0f0f0fu), x2.x, 0);
+                        shi = __dp4a((int)((w[1] >> 4) & 0x0f0f0f0fu), x2.y, shi);
+                        shi = __dp4a((int)((w[2] >> 4) & 0x0f0f0f0fu), x2.z, shi);
+                        shi = __dp4a((int)((w[3] >> 4) & 0x0f0f0f0fu), x2.w, shi);
+                        shi = __dp4a((int)((w[4] >> 4) & 0x0f0f0f0fu), x3.x, shi);
+                        shi = __dp4a((int)((w[5] >> 4) & 0x0f0f0f0fu), x3.y, shi);
+                        shi = __dp4a((int)((w[6] >> 4) & 0x0f0f0f0fu), x3.z, shi);
+                        shi = __dp4a((int)((w[7] >> 4) & 0x0f0f0f0fu), x3.w, shi);
+                        // exact int32 sub-block dots times the 6-bit scales, folded in fp32
+                        float t = ds.x * (float)(sc0 * slo);
+                        t = fmaf(ds.z, (float)(sc1 * shi), t);
+                        float mm = ds.y * (float)m0;
+                        mm = fmaf(ds.w, (float)m1, mm);
+                        acc[cc] = fmaf(d, t, fmaf(-dmin, mm, acc[cc]));
+                    }
+                }
+            }
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+                float v = acc[cc];
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                acc[cc] = v;
+            }
+            if (valid && l16 == 0) {
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) y[cc * y_ld + a + rr] = acc[cc];
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && abort_flag && status) atomicExch(status, (int)QMM_ERR_DEVICE);
+}
+
+template <int NC>
+static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, const void *xq, float *y, int64_t y_ld,
+                                      cudaStream_t st) {
+    const int64_t row_bytes = (k / 256) * kQ4KBytes;
+    const size_t smem = gemv_tma_smem_bytes(k, NC);
+    auto kern = gemv_q4k_tma_kernel<NC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
+    kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(static_cast<const uint8_t *>(W), n, (int)k, row_bytes,
+                                                    static_cast<const uint8_t *>(xq), y, y_ld, nullptr);
+    return cudaGetLastError();
 }
 
 template <int T, int NC>
@@ -167,6 +389,21 @@ static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void
         cudaError_t e;
         const void *xc = x + c0 * xrow;
         float *yc = y + c0 * n;
+        if (T == QMM_Q4_K && gemv_tma_smem_bytes(k, nc) <= budget && gemv_tma_enabled()) {
+            switch (nc) {
+            case 1: e = launch_gemv_tma_nc<1>(W, n, k, xc, yc, n, st); break;
+            case 2: e = launch_gemv_tma_nc<2>(W, n, k, xc, yc, n, st); break;
+            case 3: e = launch_gemv_tma_nc<3>(W, n, k, xc, yc, n, st); break;
+            case 4: e = launch_gemv_tma_nc<4>(W, n, k, xc, yc, n, st); break;
+            case 5: e = launch_gemv_tma_nc<5>(W, n, k, xc, yc, n, st); break;
+            case 6: e = launch_gemv_tma_nc<6>(W, n, k, xc, yc, n, st); break;
+            case 7: e = launch_gemv_tma_nc<7>(W, n, k, xc, yc, n, st); break;
+            default: e = launch_gemv_tma_nc<8>(W, n, k, xc, yc, n, st); break;
+            }
+            if (e != cudaSuccess) return e;
+            c0 += nc;
+            continue;
+        }
         switch (nc) {
         case 1: e = launch_gemv_nc<T, 1>(W, n, k, xc, yc, n, st); break;
         case 2: e = launch_gemv_nc<T, 2>(W, n, k, xc, yc, n, st); break;

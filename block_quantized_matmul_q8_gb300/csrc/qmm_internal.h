@@ -16,6 +16,9 @@ int device_smem_optin();
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_quantize_q8_1(const float *x, int64_t m, int64_t k, void *xq, cudaStream_t st);
 
+// False when the test switch asks for the direct-load GEMV only.
+bool gemv_tma_enabled();
+
 // GEMV, m <= 8: y[m][n] from W rows and q8_1 activations.  Columns beyond the shared
 // memory budget are processed in several launches by the caller.
 size_t gemv_smem_bytes(int64_t k, int ncols);

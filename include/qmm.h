@@ -172,7 +172,8 @@ QMM_API void qmm_plan_cta_range(const qmm_gemm_plan *plan, int32_t cta, int64_t 
  * Process-wide switches for tests and benchmarks; read at every call. */
 
 /* Path override for qmm_mul_mat: 0 = automatic, 1 = GEMV for any m <= 64,
- * 2 = the CUDA-core (dp4a) tiled GEMM, 3 = the tensor-core GEMM for any m. */
+ * 2 = the CUDA-core (dp4a) tiled GEMM, 3 = the tensor-core GEMM for any m,
+ * 4 = GEMV for any m <= 64 with direct global loads only (no bulk copies). */
 QMM_API void qmm_set_force_path(int path);
 
 /* Stream-K mode for the tensor-core GEMM: 0 = automatic, 1 = never, 2 = always. */

@@ -1,0 +1,66 @@
+"""Parity of the tensor-core GEMM (tcgen05, kind::f16 on integer-valued operands)
+against the oracle: ragged tile edges in both dimensions, one to many superblocks,
+with and without the stream-K split and its fixup pass."""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_matmul_q8_gb300 as qmm
+import qmm_synth
+from parity import assert_within
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    qmm.build()
+    yield
+    qmm.qmm_set_force_path(0)
+    qmm.qmm_set_stream_k_mode(0)
+
+
+def run_tc(oracle_mod, n, k, m, sk_mode, seed=0, x=None):
+    W, xr = qmm_synth.make_dense("q4_K", n, k, m, seed=seed)
+    if x is not None:
+        xr = x
+    xq = oracle_mod.quantize_q8_1(xr)
+    qmm.qmm_set_force_path(qmm.PATH_GEMM_TC)
+    qmm.qmm_set_stream_k_mode(sk_mode)
+    try:
+        ws = torch.empty(max(256, qmm.qmm_workspace_bytes("q4_K", n, k, m)), dtype=torch.uint8, device=DEV)
+        y = torch.full((m, n), float("nan"), device=DEV)
+        qmm.qmm_mul_mat(torch.from_numpy(W).to(DEV), "q4_K", n, k, torch.from_numpy(xq).to(DEV), m, y=y,
+                        workspace=ws)
+        torch.cuda.synchronize()
+        status = qmm.qmm_read_device_status(ws)
+    finally:
+        qmm.qmm_set_force_path(0)
+        qmm.qmm_set_stream_k_mode(0)
+    assert status == 0, f"device status {status}"
+    y_ref, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    assert_within(y.cpu().numpy(), y_ref, T, f"tc n={n} k={k} m={m} sk={sk_mode}")
+
+
+def test_tc_single_tile_smallest(oracle_mod):
+    run_tc(oracle_mod, 128, 256, 128, 1)
+
+
+@pytest.mark.parametrize("n,k,m", [(128, 512, 128), (129, 256, 9), (1, 256, 17), (300, 1024, 130), (256, 768, 256),
+                                   (77, 2048, 200)])
+@pytest.mark.parametrize("sk", [1, 2])
+def test_tc_parity(oracle_mod, n, k, m, sk):
+    run_tc(oracle_mod, n, k, m, sk, seed=n + k + m)
+
+
+def test_tc_auto_schedule(oracle_mod):
+    run_tc(oracle_mod, 1000, 1024, 300, 0, seed=3)
+
+
+def test_tc_integer_exactness(oracle_mod):
+    """Activations whose q8_1 codes hit +-127 everywhere: the largest integer dots
+    (32 * 945 * 127 per sub-block) must still be exact in the fp32 accumulators."""
+    n, k, m = 130, 512, 20
+    x = np.where(np.random.default_rng(5).random((m, k)) < 0.5, -1.0, 1.0).astype(np.float32)
+    run_tc(oracle_mod, n, k, m, 1, seed=9, x=x)
