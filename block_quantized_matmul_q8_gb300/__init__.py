@@ -27,7 +27,8 @@ PATH_AUTO, PATH_GEMV, PATH_GEMM_DP4A, PATH_GEMM_TC, PATH_GEMV_DIRECT = 0, 1, 2, 
 # Every function that include/qmm.h declares.
 EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspace_bytes", "qmm_quantize_q8_1",
            "qmm_mul_mat", "qmm_mul_mat_id", "qmm_read_device_status", "qmm_tile_efficiency_percent",
-           "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode")
+           "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode",
+           "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes")
 
 
 class QMMError(RuntimeError):
@@ -84,6 +85,10 @@ def lib():
     L.qmm_set_force_path.argtypes = [ctypes.c_int]
     L.qmm_set_stream_k_mode.restype = None
     L.qmm_set_stream_k_mode.argtypes = [ctypes.c_int]
+    L.qmm_mul_mat_id_noalloc.restype = ctypes.c_int
+    L.qmm_mul_mat_id_noalloc.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P]
+    L.qmm_noalloc_scratch_bytes.restype = SZ
+    L.qmm_noalloc_scratch_bytes.argtypes = []
     _lib = L
     return L
 
@@ -182,6 +187,23 @@ def qmm_mul_mat_id(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, xq: t
     _check(lib().qmm_mul_mat_id(_ptr(W), _qtype(qtype), n_experts, n, k, _ptr(xq), _ptr(ids), top_k, n_tokens,
                                 _ptr(y), _ptr(workspace), ws_bytes, _stream(stream)), "qmm_mul_mat_id")
     return y
+
+
+def qmm_mul_mat_id_noalloc(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, xq: torch.Tensor,
+                           ids: torch.Tensor, top_k: int, n_tokens: int, y: torch.Tensor, stream=None) -> torch.Tensor:
+    """qmm_mul_mat_id with the library's fixed device scratch instead of a workspace;
+    y must be given (the call allocates nothing)."""
+    _dev(W, "W")
+    _dev(xq, "xq")
+    _dev(ids, "ids", torch.int32)
+    _dev(y, "y", torch.float32)
+    _check(lib().qmm_mul_mat_id_noalloc(_ptr(W), _qtype(qtype), n_experts, n, k, _ptr(xq), _ptr(ids), top_k,
+                                        n_tokens, _ptr(y), _stream(stream)), "qmm_mul_mat_id_noalloc")
+    return y
+
+
+def qmm_noalloc_scratch_bytes() -> int:
+    return lib().qmm_noalloc_scratch_bytes()
 
 
 def qmm_read_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -129,6 +129,29 @@ QMM_API qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_e
                           const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *workspace,
                           size_t ws_bytes, void *stream);
 
+/*
+ * qmm_mul_mat_id without a workspace argument, for callers that cannot allocate
+ * device memory where they make this call (a fixed memory pool owned by someone
+ * else, a plugin that may not call cudaMalloc, code that runs between graph
+ * captures).  The pages have no counterpart of this call.
+ *   Arguments, layouts and results are those of qmm_mul_mat_id.
+ *   Scratch: one file-scope device array of qmm_noalloc_scratch_bytes() (1 MiB),
+ *   present in every GPU that loads the library until the process exits.  A problem
+ *   whose qmm_workspace_bytes() exceeds it is rejected with QMM_ERR_WORKSPACE and
+ *   nothing is enqueued.  The call allocates nothing and frees nothing.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.  Every call on a device shares the array: calls whose work can
+ *   overlap on the GPU (different streams without ordering) race on it.
+ *   The device status word is kept in the array and is not reported.
+ */
+QMM_API qmm_status qmm_mul_mat_id_noalloc(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
+                                          const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
+                                          float *y, void *stream);
+
+/* Size in bytes of the fixed scratch array used by qmm_mul_mat_id_noalloc. */
+QMM_API size_t qmm_noalloc_scratch_bytes(void);
+
 /* Copy the device status word of the last qmm_mul_mat_id on this workspace to
  * *status (QMM_OK, QMM_ERR_IDS or QMM_ERR_DEVICE).  This call synchronises
  * `stream`.  Returns QMM_ERR_CUDA if the copy fails. */
