@@ -49,9 +49,19 @@ namespace {
 constexpr int kTM = 128;  // activation rows per tile
 constexpr int kTN = 128;  // weight rows per tile
 constexpr int kStages = 2;
-constexpr int kSlots = 4;
-constexpr int kThreads = 448;  // 14 warps
-constexpr int kEpiWarp0 = 6;
+constexpr int kSlots = 3;          // accumulator slots of 128 TMEM columns; columns 384..511 hold the running total
+constexpr uint32_t kTotCol = 384;
+constexpr int kThreads = 768;      // 24 warps = 6 warpgroups
+constexpr int kUnpackWarp0 = 4;
+constexpr int kEpiWarp0 = 8;
+constexpr int kEpiWarps = 16;
+// Registers per thread after the split.  The block is launched with 80 registers per
+// thread (65536 / 768 rounded down to a multiple of 8), so the split may hand out at
+// most 768 x 80 registers; setmaxnreg.inc would otherwise wait forever.
+constexpr int kLaunchRegs = 80;
+constexpr int kRegsProducer = 32, kRegsUnpack = 64, kRegsEpilogue = 96;
+static_assert(128 * kRegsProducer + 128 * kRegsUnpack + 32 * kEpiWarps * kRegsEpilogue <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kMaxPartialCtas = 256;
 
 // dynamic shared memory map (offsets from a 1024-aligned base)
@@ -61,9 +71,10 @@ constexpr uint32_t kOffW = kOffX + kStages * 2 * kSlabBytes;      // [stage][2 s
 constexpr uint32_t kOffXmin = kOffW + kStages * 2 * kSlabBytes;   // [stage][128][32 B]
 constexpr uint32_t kOffWmin = kOffXmin + kStages * 4096;          // [stage][128][32 B]
 constexpr uint32_t kOffDX = kOffWmin + kStages * 4096;            // [2][128][8] fp32
-constexpr uint32_t kOffDD = kOffDX + 2 * 4096;                    // [2][128] float2
-constexpr uint32_t kOffTot = kOffDD + 2 * 1024;                   // [2 wg][16][128] float4
-constexpr uint32_t kSmemBytes = kOffTot + 2 * 16 * 128 * 16;
+constexpr uint32_t kOffDD = kOffDX + 2 * 4096;                    // [2][d[128], -dmin[128]] fp32
+constexpr uint32_t kRawBytes = 128 * kQ4KBytes;                   // raw Q4_K superblocks of 128 weight rows
+constexpr uint32_t kOffRaw = (kOffDD + 2 * 1024 + 1023) & ~1023u;  // [2][128][144]
+constexpr uint32_t kSmemBytes = kOffRaw + 2 * kRawBytes;
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 
 struct TcArgs {
@@ -86,6 +97,7 @@ struct Barriers {
     uint64_t x_full[kStages], x_empty[kStages], w_full[kStages], w_empty[kStages];
     uint64_t acc_full[kSlots], acc_empty[kSlots];
     uint64_t sd_full[2], sd_empty[2];
+    uint64_t raw_full[2], raw_empty[2];
     uint64_t done;
     uint32_t tmem_base;
     int abort;
@@ -116,6 +128,9 @@ __device__ __forceinline__ bool next_seg(const TcArgs &a, int64_t &u, int64_t en
 
 __device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 
+template <int N> __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N> __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
 // 8 nibbles (low or high half of bytes w0, w1) -> 8 fp16 values q*sc, exact.
 // (0x6400 | q) is the fp16 value 1024 + q; fma((1024+q), sc, -1024*sc) = q*sc exactly.
 __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w0, uint32_t w1, int shift, __half2 sc2, __half2 nsc2) {
@@ -136,7 +151,8 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w0, uint32_t w1, int sh
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
-                       const __grid_constant__ CUtensorMap tm_dx, TcArgs a) {
+                       const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
+                       TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ Barriers B;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,11 +170,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kSlots; ++s) {
             ptx::mbar_init(ptx::smem_u32(&B.acc_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&B.acc_empty[s]), 8);
+            ptx::mbar_init(ptx::smem_u32(&B.acc_empty[s]), kEpiWarps);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&B.raw_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&B.raw_empty[s]), 128);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(ptx::smem_u32(&B.sd_full[s]), 1 + 128);
-            ptx::mbar_init(ptx::smem_u32(&B.sd_empty[s]), 8);
+            ptx::mbar_init(ptx::smem_u32(&B.sd_empty[s]), kEpiWarps);
         }
         ptx::mbar_init(ptx::smem_u32(&B.done), 1);
         ptx::fence_mbar_init();
@@ -177,16 +197,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        regs_dec<kRegsProducer>();
         if (lane == 0) {
             ptx::prefetch_tmap(&tm_x);
             ptx::prefetch_tmap(&tm_xmin);
             ptx::prefetch_tmap(&tm_dx);
+            ptx::prefetch_tmap(&tm_w);
             int64_t u = ubeg;
             Seg sg;
             uint32_t x_it = 0, sd_it = 0;
             bool ok = true;
             while (ok && next_seg(a, u, uend, sg)) {
                 const int m0 = (int)((sg.tile / a.tiles_n) * kTM);
+                const int n0 = (int)((sg.tile % a.tiles_n) * kTN);
                 for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                     const uint32_t sdi = sd_it & 1;
                     if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[sdi]), ((sd_it >> 1) & 1) ^ 1, abortp)) {
@@ -196,6 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sdbar = ptx::smem_u32(&B.sd_full[sdi]);
                     ptx::mbar_arrive_expect_tx(sdbar, 128 * 8 * 4);
                     ptx::tma_load_2d(sbase + kOffDX + sdi * 4096, &tm_dx, (int)(8 * sb), m0, sdbar);
+                    // raw weight bytes of this superblock for the tile's 128 weight rows
+                    const uint32_t ri = sd_it & 1;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_empty[ri]), ((sd_it >> 1) & 1) ^ 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t rbar = ptx::smem_u32(&B.raw_full[ri]);
+                    ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
+                    ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, (int)(sb * kQ4KBytes), n0, rbar);
                     ++sd_it;
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t st = x_it % kStages;
@@ -217,11 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             int dummy = 0;
             for (uint32_t i = (x_it > kStages ? x_it - kStages : 0); i < x_it; ++i)
                 ptx::mbar_wait(ptx::smem_u32(&B.x_full[i % kStages]), (i / kStages) & 1, &dummy);
-            for (uint32_t i = (sd_it > 2 ? sd_it - 2 : 0); i < sd_it; ++i)
+            for (uint32_t i = (sd_it > 2 ? sd_it - 2 : 0); i < sd_it; ++i) {
                 ptx::mbar_wait(ptx::smem_u32(&B.sd_full[i & 1]), (i >> 1) & 1, &dummy);
+                ptx::mbar_wait(ptx::smem_u32(&B.raw_full[i & 1]), (i >> 1) & 1, &dummy);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        regs_dec<kRegsProducer>();
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f16_f32(kTM, kTN);
             int64_t u = ubeg;
@@ -279,52 +314,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             int dummy = 0;
             ptx::mbar_wait(ptx::smem_u32(&B.done), 0, &dummy);
         }
+    } else if (warp < kUnpackWarp0) {
+        regs_dec<kRegsProducer>();  // warps 2-3: no role, give their registers away
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ weight unpack
-        const int r = tid - 64;  // weight row within the tile
+        // One weight row per thread, reading the raw superblock that the TMA warp put in
+        // shared memory (rows 144 bytes apart: 8 consecutive rows hit distinct banks).
+        regs_dec<kRegsUnpack>();
+        const int r = tid - 32 * kUnpackWarp0;  // weight row within the tile
         int64_t u = ubeg;
         Seg sg;
-        uint32_t w_it = 0, sd_it = 0;
+        uint32_t w_it = 0, sb_it = 0;
         bool ok = true;
         while (ok && next_seg(a, u, uend, sg)) {
-            const int64_t row = (sg.tile % a.tiles_n) * kTN + r;
-            const bool valid = row < a.n;
-            const uint8_t *rowp = a.W + (valid ? row : 0) * a.row_bytes;
             for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
-                const uint8_t *blk = rowp + sb * kQ4KBytes;
-                uint4 hd = make_uint4(0, 0, 0, 0);
-                if (valid) hd = ldg16(blk);
-                const float d = half_lo(hd.x), dmin = half_hi(hd.x);
-                // (d, dmin) for the epilogue
-                const uint32_t sdi = sd_it & 1;
-                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[sdi]), ((sd_it >> 1) & 1) ^ 1, abortp)) {
+                const uint32_t ri = sb_it & 1;
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_full[ri]), (sb_it >> 1) & 1, abortp)) {
                     ok = false;
                     break;
                 }
-                reinterpret_cast<float2 *>(smem + kOffDD + sdi * 1024)[r] = make_float2(d, dmin);
-                ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[sdi]));
-                ++sd_it;
+                const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + r * kQ4KBytes;
+                const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
+                // (d, -dmin) for the epilogue
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[ri]), ((sb_it >> 1) & 1) ^ 1, abortp)) {
+                    ok = false;
+                    break;
+                }
+                float *dd = reinterpret_cast<float *>(smem + kOffDD + ri * 1024);
+                dd[r] = half_lo(hd.x);
+                dd[128 + r] = -half_hi(hd.x);
+                ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t st = w_it % kStages;
                     if (!ptx::mbar_wait(ptx::smem_u32(&B.w_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
                         ok = false;
                         break;
                     }
-                    uint4 q4[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) q4[i] = valid ? ldg16(blk + 16 + 64 * h + 16 * i) : make_uint4(0, 0, 0, 0);
                     uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {  // slab j <-> qs chunk c = 2h + j
-                        const int c = 2 * h + j;
+                    for (int j2 = 0; j2 < 2; ++j2) {  // slab j2 <-> qs chunk c = 2h + j2
+                        const int c = 2 * h + j2;
+                        const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
+                        const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
                         int sc_lo, m_lo, sc_hi, m_hi;
                         q4k_scale_min(hd.y, hd.z, hd.w, 2 * c, sc_lo, m_lo);
                         q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sc_hi, m_hi);
                         const __half2 s_lo = __float2half2_rn((float)sc_lo), ns_lo = __float2half2_rn(-1024.f * sc_lo);
                         const __half2 s_hi = __float2half2_rn((float)sc_hi), ns_hi = __float2half2_rn(-1024.f * sc_hi);
-                        const uint32_t w[8] = {q4[2 * j].x, q4[2 * j].y, q4[2 * j].z, q4[2 * j].w,
-                                               q4[2 * j + 1].x, q4[2 * j + 1].y, q4[2 * j + 1].z, q4[2 * j + 1].w};
-                        uint8_t *rowdst = wst + j * kSlabBytes + r * 128;
+                        const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                        uint8_t *rowdst = wst + j2 * kSlabBytes + r * 128;
 #pragma unroll
                         for (int cq = 0; cq < 4; ++cq) {
                             const uint4 lo = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 0, s_lo, ns_lo);
@@ -336,11 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (h == 1) {  // mins of the 8 sub-blocks as fp16, then 8 zeros (32-byte swizzle)
                         uint32_t mm[4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                        for (int i2 = 0; i2 < 4; ++i2) {
                             int s0_, m0_, s1_, m1_;
-                            q4k_scale_min(hd.y, hd.z, hd.w, 2 * i, s0_, m0_);
-                            q4k_scale_min(hd.y, hd.z, hd.w, 2 * i + 1, s1_, m1_);
-                            mm[i] = h2bits(__floats2half2_rn((float)m0_, (float)m1_));
+                            q4k_scale_min(hd.y, hd.z, hd.w, 2 * i2, s0_, m0_);
+                            q4k_scale_min(hd.y, hd.z, hd.w, 2 * i2 + 1, s1_, m1_);
+                            mm[i2] = h2bits(__floats2half2_rn((float)m0_, (float)m1_));
                         }
                         uint8_t *mdst = smem + kOffWmin + st * 4096 + r * 32;
                         const int sw = (r >> 2) & 1;
@@ -351,15 +389,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive(ptx::smem_u32(&B.w_full[st]));
                     ++w_it;
                 }
+                ptx::mbar_arrive(ptx::smem_u32(&B.raw_empty[ri]));
+                ++sb_it;
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - kEpiWarp0;       // 0..7
-        const int wg = ew >> 2;                // column half: columns 64wg .. 64wg+63
+        // 16 warps: warp w reads TMEM lanes 32*(w%4).. (one activation row per thread)
+        // and one quarter of the 128 columns (32 weight rows).  Per superblock: 8 slots
+        // fold into acc (fp32), then the min slot and the running total (TMEM columns
+        // 384..511) are updated in two 16-column halves.
+        regs_inc<kRegsEpilogue>();
+        const int ew = warp - kEpiWarp0;       // 0..15
+        const int cq = ew >> 2;                // column quarter: columns 32cq .. 32cq+31
         const int qd = warp & 3;               // TMEM lane quarter this warp may access
         const int tl = 32 * qd + lane;         // activation row within the tile
-        float4 *tot = reinterpret_cast<float4 *>(smem + kOffTot) + (wg * 16) * 128 + tl;  // [16][128] float4
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         int64_t u = ubeg;
         Seg sg;
         uint32_t g = 0, sd_it = 0;
@@ -373,90 +418,100 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const float4 *dxp = reinterpret_cast<const float4 *>(smem + kOffDX + sdi * 4096 + tl * 32);
-                const float4 dxa = dxp[0], dxb = dxp[1];
-                const float dx[8] = {dxa.x, dxa.y, dxa.z, dxa.w, dxb.x, dxb.y, dxb.z, dxb.w};
-                float acc[64];
-                for (int b = 0; b < 9; ++b) {
-                    const uint32_t slot = g % kSlots;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), (g / kSlots) & 1, abortp)) {
+                const float *dxs = reinterpret_cast<const float *>(smem + kOffDX + sdi * 4096 + tl * 32);
+                const float4 *ddd = reinterpret_cast<const float4 *>(smem + kOffDD + sdi * 1024) + 8 * cq;
+                const float4 *ddm = reinterpret_cast<const float4 *>(smem + kOffDD + sdi * 1024 + 512) + 8 * cq;
+                float acc[32];
+                for (int G = 0; G < 8 && ok; ++G) {
+                    const uint32_t slot = (g + G) % kSlots;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), ((g + G) / kSlots) & 1, abortp)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + slot * kTN + 64 * wg;
-                    if (b < 8) {
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            float v[32];
-                            ptx::tmem_ld_32x32b_x32(taddr + 32 * hh, v);
-                            ptx::tmem_ld_wait();
-                            if (b == 0) {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) acc[32 * hh + i] = dx[0] * v[i];
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) acc[32 * hh + i] = fmaf(dx[b], v[i], acc[32 * hh + i]);
-                            }
-                        }
-                    } else {
-                        const float4 *dd = reinterpret_cast<const float4 *>(smem + kOffDD + sdi * 1024);
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            float v[32];
-                            ptx::tmem_ld_32x32b_x32(taddr + 32 * hh, v);
-                            ptx::tmem_ld_wait();
-#pragma unroll
-                            for (int i4 = 0; i4 < 8; ++i4) {
-                                const int c = 32 * hh + 4 * i4;              // column within this thread's 64
-                                const int cc = 64 * wg + c;                   // column within the tile
-                                const float4 p0 = dd[cc / 2], p1 = dd[cc / 2 + 1];  // (d, dmin) of 4 columns
-                                float4 t = first ? make_float4(0.f, 0.f, 0.f, 0.f) : tot[(c / 4) * 128];
-                                t.x = fmaf(-p0.y, v[4 * i4 + 0], fmaf(p0.x, acc[c + 0], t.x));
-                                t.y = fmaf(-p0.w, v[4 * i4 + 1], fmaf(p0.z, acc[c + 1], t.y));
-                                t.z = fmaf(-p1.y, v[4 * i4 + 2], fmaf(p1.x, acc[c + 2], t.z));
-                                t.w = fmaf(-p1.w, v[4 * i4 + 3], fmaf(p1.z, acc[c + 3], t.w));
-                                tot[(c / 4) * 128] = t;
-                            }
-                        }
-                    }
+                    float v[32];
+                    ptx::tmem_ld_32x32b_x32(lane_base + slot * kTN + 32 * cq, v);
+                    ptx::tmem_ld_wait();
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[slot]));
-                    ++g;
+                    const float dg = dxs[G];
+                    if (G == 0) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[i] = dg * v[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[i] = fmaf(dg, v[i], acc[i]);
+                    }
                 }
                 if (!ok) break;
+                // min slot and running total
+                const uint32_t slot = (g + 8) % kSlots;
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), ((g + 8) / kSlots) & 1, abortp)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float vm[16], t[16];
+                    ptx::tmem_ld_32x32b_x16(lane_base + slot * kTN + 32 * cq + 16 * hh, vm);
+                    if (!first) ptx::tmem_ld_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int i4 = 0; i4 < 4; ++i4) {
+                        const float4 d4 = ddd[4 * hh + i4], m4 = ddm[4 * hh + i4];
+                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 4 * i4 + e;
+                            const float base = first ? 0.f : t[i];
+                            t[i] = fmaf(mv[e], vm[i], fmaf(dv[e], acc[16 * hh + i], base));
+                        }
+                    }
+                    ptx::tmem_st_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
+                }
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.sd_empty[sdi]));
+                if (lane == 0) {
+                    ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[slot]));
+                    ptx::mbar_arrive(ptx::smem_u32(&B.sd_empty[sdi]));
+                }
+                g += 9;
                 ++sd_it;
                 first = false;
             }
             if (!ok) break;
             // write the segment's result: whole tile -> y, part of a tile -> this CTA's partial slot
+            float res[32];
+            ptx::tmem_ld_32x32b_x32(lane_base + kTotCol + 32 * cq, res);
+            ptx::tmem_ld_wait();
             const int64_t tm = sg.tile / a.tiles_n, tn = sg.tile % a.tiles_n;
             const int64_t token = tm * kTM + tl;
-            const int64_t col0 = tn * kTN + 64 * wg;
+            const int64_t col0 = tn * kTN + 32 * cq;
             const bool full = sg.s0 == 0 && sg.s1 == a.nsb;
             if (full) {
                 if (token < a.m) {
                     float *dst = a.y + token * a.n + col0;
-                    const bool vec = (a.n % 4 == 0) && (col0 + 64 <= a.n);
-                    for (int i4 = 0; i4 < 16; ++i4) {
-                        const float4 t = tot[i4 * 128];
-                        if (vec) {
-                            reinterpret_cast<float4 *>(dst)[i4] = t;
-                        } else {
-                            const float tv[4] = {t.x, t.y, t.z, t.w};
-                            for (int j = 0; j < 4; ++j)
-                                if (col0 + 4 * i4 + j < a.n) dst[4 * i4 + j] = tv[j];
-                        }
+                    if ((a.n % 4 == 0) && (col0 + 32 <= a.n)) {
+#pragma unroll
+                        for (int i4 = 0; i4 < 8; ++i4)
+                            reinterpret_cast<float4 *>(dst)[i4] =
+                                make_float4(res[4 * i4], res[4 * i4 + 1], res[4 * i4 + 2], res[4 * i4 + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < a.n) dst[i] = res[i];
                     }
                 }
             } else {
                 const int slotidx = seg_i == 0 ? 0 : 1;
                 float4 *dst = reinterpret_cast<float4 *>(a.partial + ((int64_t(blockIdx.x) * 2 + slotidx) * kTM + tl) * kTN +
-                                                         64 * wg);
-                for (int i4 = 0; i4 < 16; ++i4) dst[i4] = tot[i4 * 128];
+                                                         32 * cq);
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4)
+                    dst[i4] = make_float4(res[4 * i4], res[4 * i4 + 1], res[4 * i4 + 2], res[4 * i4 + 3]);
             }
             ++seg_i;
         }
@@ -612,11 +667,13 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    CUtensorMap tm_x, tm_xmin, tm_dx;
+    CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
     if (!make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, k, m, 64, kTM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&tm_xmin, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, smin, (k / 256) * 16, m, 16, kTM,
                      CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_map_2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx, k / 32, m, 8, kTM, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map_2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx, k / 32, m, 8, kTM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, (k / 256) * kQ4KBytes, n, kQ4KBytes, kTN,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
     TcArgs args{};
@@ -636,7 +693,16 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
 
     e = cudaFuncSetAttribute(gemm_tc_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
-    gemm_tc_q4k_kernel<<<p.ctas, kThreads, kSmemAlloc, st>>>(tm_x, tm_xmin, tm_dx, args);
+    // The setmaxnreg split hands out exactly kThreads x kLaunchRegs registers; a build that
+    // launches with fewer registers per thread would leave setmaxnreg.inc waiting forever.
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, gemm_tc_q4k_kernel) != cudaSuccess) return cudaErrorInvalidValue;
+        launch_regs = fa.numRegs;
+    }
+    if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    gemm_tc_q4k_kernel<<<p.ctas, kThreads, kSmemAlloc, st>>>(tm_x, tm_xmin, tm_dx, tm_w, args);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.stream_k && p.fixup) {

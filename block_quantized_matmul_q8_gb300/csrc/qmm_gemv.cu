@@ -230,6 +230,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
     }
     __syncthreads();
 
+    // The weights are never written by the kernels of this library, so their copies may
+    // start before the preceding kernel in the stream (typically the activation
+    // quantizer) has finished; everything else waits for it.
+    ptx::grid_launch_dependents();
     if (warp == kTmaConsumerWarps) {
         // ---------------- producer warp: one lane issues every copy
         if (lane == 0) {
@@ -254,6 +258,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
         }
     } else {
         // ---------------- consumers: stage the activations, then fold the chunks
+        ptx::grid_dependency_wait();
         for (int i = tid; i < NC * nb32; i += kTmaConsumerWarps * 32) {
             const int c = i / nb32, b = i - c * nb32;
             const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (size_t(c) * nb32 + b) * kQ81Bytes);
@@ -348,9 +353,8 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, const
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
-    kern<<<(unsigned)grid, kTmaThreads, smem, st>>>(static_cast<const uint8_t *>(W), n, (int)k, row_bytes,
-                                                    static_cast<const uint8_t *>(xq), y, y_ld, nullptr);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(W), n,
+                      (int)k, row_bytes, static_cast<const uint8_t *>(xq), y, y_ld, static_cast<int *>(nullptr));
 }
 
 template <int T, int NC>

@@ -4,12 +4,34 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "qmm.h"
 
 namespace qmm {
 
 // SM count of the current device (cached per device).
 int device_sm_count();
+
+// Launch kern<<<grid, block, smem, st>>>(args...) with programmatic stream
+// serialization, so that it may start while the previous kernel in the stream is
+// still running; the kernel itself waits (griddepcontrol.wait) before it touches
+// anything that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 // Opt-in shared memory per block of the current device (cached per device).
 int device_smem_optin();
 

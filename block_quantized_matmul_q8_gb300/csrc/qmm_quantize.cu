@@ -12,11 +12,15 @@
 
 #include "qmm_common.cuh"
 #include "qmm_internal.h"
+#include "qmm_tc_ptx.cuh"
 
 namespace qmm {
 
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restrict__ x, int64_t m, int64_t k,
                                                             uint8_t *__restrict__ xq) {
+    // x may be written by the preceding kernel and xq read by it: wait for it first.
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t nb = k / 32;
     const int64_t nblocks = m * nb;
@@ -53,8 +57,8 @@ cudaError_t launch_quantize_q8_1(const float *x, int64_t m, int64_t k, void *xq,
     int64_t grid = (nblocks + 7) / 8;  // 8 warps per CTA
     const int64_t cap = int64_t(device_sm_count()) * 16;
     if (grid > cap) grid = cap;
-    quantize_q8_1_kernel<<<(unsigned)grid, threads, 0, st>>>(x, m, k, static_cast<uint8_t *>(xq));
-    return cudaGetLastError();
+    return launch_pdl(quantize_q8_1_kernel, dim3((unsigned)grid), dim3(threads), 0, st, x, m, k,
+                      static_cast<uint8_t *>(xq));
 }
 
 }  // namespace qmm
