@@ -159,19 +159,26 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const uint8_t *__res
 // CTA per SM owns a contiguous range of rows and streams it through a ring of
 // shared-memory stages with 1D bulk copies (cp.async.bulk, completion counted on an
 // mbarrier), so every byte of W moves in large contiguous transfers and up to
-// kTmaStages chunks per SM are in flight.  A dedicated producer warp issues the
-// copies; two groups of 8 consumer warps take alternate chunks (a half-warp per row,
-// lane l16 takes units l16, l16+16, ...).
-constexpr int kTmaStages = 4;
-constexpr int kTmaGroups = 2;
-constexpr int kTmaGroupWarps = 8;
+// nstages chunks per SM are in flight (up to 8 chunks of 8 rows, as many as fit next
+// to the staged activations).  A dedicated producer warp issues the copies; four
+// groups of 4 consumer warps take chunks in turn (a half-warp per row, lane l16 takes
+// units l16, l16+16, ...).
+constexpr int kTmaMaxStages = 8;
+constexpr int kTmaMinStages = 3;
+constexpr int kTmaGroups = 4;
+constexpr int kTmaGroupWarps = 4;
 constexpr int kTmaConsumerWarps = kTmaGroups * kTmaGroupWarps;
 constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
 constexpr int kTmaChunkRows = 2 * kTmaGroupWarps;  // one row per half-warp
 
-size_t gemv_tma_smem_bytes(int64_t k, int ncols) {
+// Stages of kTmaChunkRows rows that fit next to the staged activations (0: too few).
+int gemv_tma_stages(int64_t k, int ncols, size_t budget) {
     const int64_t row_bytes = (k / 256) * kQ4KBytes;
-    return 1024 + size_t(kTmaStages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, ncols);
+    const size_t fixed = 1024 + gemv_smem_bytes(k, ncols);
+    if (fixed >= budget) return 0;
+    const int64_t st = int64_t(budget - fixed) / (int64_t(kTmaChunkRows) * row_bytes);
+    const int s = (int)std::min<int64_t>(st, kTmaMaxStages);
+    return s >= kTmaMinStages ? s : 0;
 }
 
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
@@ -200,19 +207,19 @@ __device__ __forceinline__ void q4k_pair_scales(uint32_t s0, uint32_t s1, uint32
 
 template <int NC>
 __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint8_t *__restrict__ W, int64_t n,
-                                                                      int k, int64_t row_bytes,
+                                                                      int k, int64_t row_bytes, int nstages,
                                                                       const uint8_t *__restrict__ xq,
                                                                       float *__restrict__ y, int64_t y_ld,
                                                                       int *status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t full[kTmaStages], empty[kTmaStages];
+    __shared__ __align__(8) uint64_t full[kTmaMaxStages], empty[kTmaMaxStages];
     __shared__ int abort_flag;
     const int U = (int)gemv_units(k);
     const int nb32 = k / 32;
     const size_t stage_bytes = size_t(kTmaChunkRows) * size_t(row_bytes);
     uint8_t *stages = smem;
-    uint8_t *xs = smem + kTmaStages * stage_bytes;
+    uint8_t *xs = smem + nstages * stage_bytes;
     float2 *xds = reinterpret_cast<float2 *>(xs + size_t(NC) * U * kUnitStride);
 
     const int64_t r0 = n * blockIdx.x / gridDim.x, r1 = n * (blockIdx.x + 1) / gridDim.x;
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
 
     if (tid == 0) {
         abort_flag = 0;
-        for (int s = 0; s < kTmaStages; ++s) {
+        for (int s = 0; s < nstages; ++s) {
             ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&empty[s]), kTmaGroupWarps);
         }
@@ -239,8 +246,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
         if (lane == 0) {
             int issued = 0;
             for (int c = 0; c < nchunks; ++c) {
-                const int s = c % kTmaStages;
-                if (c >= kTmaStages && !ptx::mbar_wait(ptx::smem_u32(&empty[s]), ((c / kTmaStages) - 1) & 1, abortp))
+                const int s = c % nstages;
+                if (c >= nstages && !ptx::mbar_wait(ptx::smem_u32(&empty[s]), ((c / nstages) - 1) & 1, abortp))
                     break;
                 const int64_t a = r0 + int64_t(c) * kTmaChunkRows;
                 const int64_t b = min(r1, a + kTmaChunkRows);
@@ -251,10 +258,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
                 ++issued;
             }
             // no copy may still be writing shared memory when the CTA exits: wait for the
-            // last kTmaStages issued chunks (each wait bounded, independent of the abort flag)
+            // last nstages issued chunks (each wait bounded, independent of the abort flag)
             int dummy = 0;
-            for (int c = max(0, issued - kTmaStages); c < issued; ++c)
-                ptx::mbar_wait(ptx::smem_u32(&full[c % kTmaStages]), (c / kTmaStages) & 1, &dummy);
+            for (int c = max(0, issued - nstages); c < issued; ++c)
+                ptx::mbar_wait(ptx::smem_u32(&full[c % nstages]), (c / nstages) & 1, &dummy);
         }
     } else {
         // ---------------- consumers: stage the activations, then fold the chunks
@@ -275,8 +282,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
         const int rr = 2 * gw + (lane >> 4);  // row within a chunk
         const int c4 = l16 & 3;               // qs chunk of every unit this lane takes
         for (int c = grp; c < nchunks; c += kTmaGroups) {
-            const int s = c % kTmaStages;
-            if (!ptx::mbar_wait(ptx::smem_u32(&full[s]), (c / kTmaStages) & 1, abortp)) break;
+            const int s = c % nstages;
+            if (!ptx::mbar_wait(ptx::smem_u32(&full[s]), (c / nstages) & 1, abortp)) break;
             const int64_t a = r0 + int64_t(c) * kTmaChunkRows;
             const bool valid = a + rr < r1;
             float acc[NC];
@@ -346,15 +353,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
 
 template <int NC>
 static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, const void *xq, float *y, int64_t y_ld,
-                                      cudaStream_t st) {
+                                      int nstages, cudaStream_t st) {
     const int64_t row_bytes = (k / 256) * kQ4KBytes;
-    const size_t smem = gemv_tma_smem_bytes(k, NC);
+    const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, NC);
     auto kern = gemv_q4k_tma_kernel<NC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(W), n,
-                      (int)k, row_bytes, static_cast<const uint8_t *>(xq), y, y_ld, static_cast<int *>(nullptr));
+                      (int)k, row_bytes, nstages, static_cast<const uint8_t *>(xq), y, y_ld,
+                      static_cast<int *>(nullptr));
 }
 
 template <int T, int NC>
@@ -393,16 +401,17 @@ static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void
         cudaError_t e;
         const void *xc = x + c0 * xrow;
         float *yc = y + c0 * n;
-        if (T == QMM_Q4_K && gemv_tma_smem_bytes(k, nc) <= budget && gemv_tma_enabled()) {
+        const int nst = T == QMM_Q4_K ? gemv_tma_stages(k, nc, budget) : 0;
+        if (nst > 0 && gemv_tma_enabled()) {
             switch (nc) {
-            case 1: e = launch_gemv_tma_nc<1>(W, n, k, xc, yc, n, st); break;
-            case 2: e = launch_gemv_tma_nc<2>(W, n, k, xc, yc, n, st); break;
-            case 3: e = launch_gemv_tma_nc<3>(W, n, k, xc, yc, n, st); break;
-            case 4: e = launch_gemv_tma_nc<4>(W, n, k, xc, yc, n, st); break;
-            case 5: e = launch_gemv_tma_nc<5>(W, n, k, xc, yc, n, st); break;
-            case 6: e = launch_gemv_tma_nc<6>(W, n, k, xc, yc, n, st); break;
-            case 7: e = launch_gemv_tma_nc<7>(W, n, k, xc, yc, n, st); break;
-            default: e = launch_gemv_tma_nc<8>(W, n, k, xc, yc, n, st); break;
+            case 1: e = launch_gemv_tma_nc<1>(W, n, k, xc, yc, n, nst, st); break;
+            case 2: e = launch_gemv_tma_nc<2>(W, n, k, xc, yc, n, nst, st); break;
+            case 3: e = launch_gemv_tma_nc<3>(W, n, k, xc, yc, n, nst, st); break;
+            case 4: e = launch_gemv_tma_nc<4>(W, n, k, xc, yc, n, nst, st); break;
+            case 5: e = launch_gemv_tma_nc<5>(W, n, k, xc, yc, n, nst, st); break;
+            case 6: e = launch_gemv_tma_nc<6>(W, n, k, xc, yc, n, nst, st); break;
+            case 7: e = launch_gemv_tma_nc<7>(W, n, k, xc, yc, n, nst, st); break;
+            default: e = launch_gemv_tma_nc<8>(W, n, k, xc, yc, n, nst, st); break;
             }
             if (e != cudaSuccess) return e;
             c0 += nc;
