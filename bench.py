@@ -51,6 +51,22 @@ WORKLOAD = "decode GEMV Q4_K n=17408 k=5120 m=1 (quantize x + mul_mat)"
 L2_BYTES = 129 * 1024 * 1024
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings over all ranks (identity with one rank)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def aggregate_rate(world, bytes_per_step, ms_per_step):
+    """Whole-job throughput in GB/s: every rank processes bytes_per_step per step;
+    the job's step time is the slowest rank's."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 def step_bytes(n, k, m, row_bytes):
     """Algorithmic bytes of one step: W once, x read, q8_1 written and read, y written."""
     return n * row_bytes + m * k * 4 + 2 * m * (k // 32) * 36 + m * n * 4
@@ -191,10 +207,13 @@ def run_reference(args):
         if i >= args.warmup:
             steps.append(r)
     val = statistics.median(s["value"] for s in steps)
+    # time one whole step of the workload would take at the measured rate
+    ms_step = step_bytes(N, K, M, row_bytes) / (val * 1e9) * 1e3
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": "bounded slices of the workload per step"},
+            "config": {"workload": WORKLOAD, "n": N, "k": K, "m": M, "format": "Q4_K", "seed": 0,
+                       "sample": "each step times bounded slices of the workload on the host cores"},
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": steps[0]["cores"], "kind": "oracle",
                              "sample": steps[0]["sample"]},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -346,14 +365,11 @@ def main():
 
     ms_e2e = time_region(torch, step_e2e, args.steps, args.warmup, stream, barrier)
 
-    t = torch.tensor([ms_total, ms_e2e, gemv_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total, ms_e2e, gemv_ms = t.tolist()
+    ms_total, ms_e2e, gemv_ms = max_over_ranks([ms_total, ms_e2e, gemv_ms], device=dev)
     ms_step = ms_total / args.steps
     sb = step_bytes(N, K, M, row_bytes)
-    value = world * sb / (ms_step * 1e-3) / 1e9
-    e2e_value = world * sb / (ms_e2e / args.steps * 1e-3) / 1e9
+    value = aggregate_rate(world, sb, ms_step)
+    e2e_value = aggregate_rate(world, sb, ms_e2e / args.steps)
     hbm_peak, tf_peak, peak_src = measured_peaks()
     kb = gemv_bytes(N, K, M, row_bytes)
     achieved = kb / (gemv_ms * 1e-3) / 1e9
