@@ -8,7 +8,8 @@ Headline workload (the pages' decode GEMV shape): Q4_K W n=17408 x k=5120, m=1
 fp32 activation row.  The metric is HBM GB/s of algorithmic bytes; the roofline
 object reports the GEMV kernel against the measured HBM copy bandwidth.  The
 "secondary" object reports the prefill GEMM (m=512) and the MoE mul_mat_id in
-TOPS (2*m*n*k integer multiply-adds).
+TOPS (2*m*n*k integer multiply-adds), and every other workload shape of the pages is
+timed the same way.
 
 Timing: the K timed steps (and, separately, the W warm-up steps) are captured once
 into a CUDA graph and replayed, so the device-side numbers carry no Python launch
@@ -269,22 +270,40 @@ def time_graphs(torch, fn, steps, warmup, barrier):
     return e0.elapsed_time(e1)
 
 
-def secondary(torch, qmm, dev, stream, steps):
-    """Prefill GEMM (m=512) and MoE mul_mat_id throughput in TOPS, device-timed."""
+def secondary(torch, qmm, dev, stream, steps, hbm_peak):
+    """Every other workload of the pages, device-timed by graph replay: GEMV rows in
+    GB/s (and fraction of the HBM peak), GEMM and MoE rows in TOPS (2*m*n*k)."""
     out = {}
-    # prefill: Q4_K n=14336 k=4096, m=512
-    n, k, m = 14336, 4096, 512
-    W, x = qmm_synth.make_dense("q4_K", n, k, m, seed=0)
-    copies = max(2, int(3 * L2_BYTES // W.nbytes) + 1)
-    Wd = [torch.from_numpy(W).to(dev) for _ in range(copies)]
-    xq = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
-    y = torch.empty((m, n), device=dev)
-    ws = torch.empty(max(1, qmm.qmm_workspace_bytes("q4_K", n, k, m)), dtype=torch.uint8, device=dev)
-    fn = lambda i: qmm.qmm_mul_mat(Wd[i % copies], "q4_K", n, k, xq, m, y=y, workspace=ws)
-    ms = time_graphs(torch, fn, steps, 3, lambda: None) / steps
-    out["prefill_q4K_n14336_k4096_m512"] = {"tops": 2 * m * n * k / (ms * 1e-3) / 1e12, "ms": ms,
-                                            "l2": f"rotating {copies} weight copies"}
-    del Wd
+
+    def dense(fmt, n, k, ms):
+        rows = {}
+        W, x = qmm_synth.make_dense(fmt, n, k, max(ms), seed=0)
+        copies = max(1, int(3 * L2_BYTES // W.nbytes) + 1)
+        Wd = [torch.from_numpy(W).to(dev) for _ in range(copies)]
+        xq_all = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
+        for m in ms:
+            xq = xq_all[:m].contiguous()
+            y = torch.empty((m, n), device=dev)
+            ws = torch.empty(max(1, qmm.qmm_workspace_bytes(fmt, n, k, m)), dtype=torch.uint8, device=dev)
+            fn = lambda i: qmm.qmm_mul_mat(Wd[i % copies], fmt, n, k, xq, m, y=y, workspace=ws)
+            ms_call = time_graphs(torch, fn, steps, 3, lambda: None) / steps
+            key = f"{fmt}_n{n}_k{k}_m{m}"
+            if m <= 8:
+                b = W.nbytes + m * (k // 32) * 36 + m * n * 4
+                rows[key] = {"GB/s": b / (ms_call * 1e-3) / 1e9, "hbm_frac": b / (ms_call * 1e-3) / 1e9 / hbm_peak,
+                             "ms": ms_call}
+            else:
+                rows[key] = {"tops": 2 * m * n * k / (ms_call * 1e-3) / 1e12, "ms": ms_call}
+            rows[key]["l2"] = f"{copies} weight copies ({copies * W.nbytes / 1e6:.0f} MB)"
+        del Wd
+        return rows
+
+    out.update(dense("q4_K", 17408, 5120, [2, 4, 5, 8]))
+    out.update(dense("q4_K", 1024, 2048, [16]))
+    out.update(dense("q4_K", 14336, 4096, [512, 2048]))
+    out.update(dense("q4_K", 4100, 4096, [512]))
+    out.update(dense("q6_K", 151936, 5120, [1, 512]))
+    out.update(dense("q8_0", 5120, 5120, [1, 512]))
     # MoE: 128 experts x Q4_K n=1536 k=4096, 512 tokens top-8 Zipf(1.1)
     E, n, k, T_, Kt = 128, 1536, 4096, 512, 8
     W, x, ids = qmm_synth.make_moe(E, n, k, T_, Kt, seed=0)
@@ -377,7 +396,7 @@ def main():
 
     sec = None
     if rank == 0 and not args.no_secondary:
-        sec = secondary(torch, qmm, dev, stream, steps=10)
+        sec = secondary(torch, qmm, dev, stream, steps=10, hbm_peak=measured_peaks()[0])
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_baseline(W, x, N, K, M, row_bytes)

@@ -13,19 +13,22 @@
 //
 // Tile: 128 activation rows (MMA M, TMEM lanes) x 128 weight rows (MMA N, TMEM
 // columns); K advances by half a superblock (128 values) per pipeline stage.
+// 24 warps, registers split with setmaxnreg (32 / 64 / 96 per thread):
 //   warp 0      TMA: fp16 activation slabs (128-byte swizzle), the per-superblock
 //               s tile (for the min term) and the per-superblock d8 tile.
 //   warp 1      TMEM allocation; one lane issues the MMAs.  Each 32-wide sub-block
-//               accumulates into its own TMEM slot (a ring of 4 slots of 128
+//               accumulates into its own TMEM slot (a ring of 3 slots of 128
 //               columns); once per superblock one more K=16 MMA forms
 //               sum_b s[m,b] * min[n,b] (8 real terms, 8 zeros) in a slot.
-//   warps 2-5   unpack: one weight row each; Q4_K nibbles -> fp16 (q * sc) written
-//               straight into the 128-byte-swizzled K-major layout the MMA reads,
-//               the 6-bit mins -> fp16 for the min-term MMA, (d, dmin) for the epilogue.
-//   warps 6-13  epilogue: one activation row (TMEM lane) and 64 weight columns per
-//               thread; per sub-block acc += d8 * slot (fp32), per superblock
-//               total += d * acc - dmin * minslot; the running total lives in shared
-//               memory (each thread its own entries).
+//   warp 2      TMA: the raw Q4_K superblock of the tile's 128 weight rows.
+//   warps 4-7   unpack: one weight row each, from the raw bytes in shared memory;
+//               nibbles -> fp16 (q * sc) written straight into the 128-byte-swizzled
+//               K-major layout the MMA reads, the 6-bit mins -> fp16 for the min-term
+//               MMA, (d, -dmin) for the epilogue.
+//   warps 8-23  epilogue: one activation row (TMEM lane) and 32 weight columns per
+//               thread; per sub-block acc += d8 * slot (fp32 FMA), per superblock
+//               total += d * acc - dmin * minslot, the total kept in TMEM columns
+//               384..511.
 // Work is a flattened stream of (tile, superblock) units split over the CTAs
 // ([MMQ] section "stream-K 的切法"); a tile shared by several CTAs is summed by a
 // separate fixup kernel in CTA order ([MMQ] section "fixup: 部分和的归约"), so no
@@ -202,14 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::prefetch_tmap(&tm_x);
             ptx::prefetch_tmap(&tm_xmin);
             ptx::prefetch_tmap(&tm_dx);
-            ptx::prefetch_tmap(&tm_w);
             int64_t u = ubeg;
             Seg sg;
             uint32_t x_it = 0, sd_it = 0;
             bool ok = true;
             while (ok && next_seg(a, u, uend, sg)) {
                 const int m0 = (int)((sg.tile / a.tiles_n) * kTM);
-                const int n0 = (int)((sg.tile % a.tiles_n) * kTN);
                 for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                     const uint32_t sdi = sd_it & 1;
                     if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[sdi]), ((sd_it >> 1) & 1) ^ 1, abortp)) {
@@ -219,15 +220,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sdbar = ptx::smem_u32(&B.sd_full[sdi]);
                     ptx::mbar_arrive_expect_tx(sdbar, 128 * 8 * 4);
                     ptx::tma_load_2d(sbase + kOffDX + sdi * 4096, &tm_dx, (int)(8 * sb), m0, sdbar);
-                    // raw weight bytes of this superblock for the tile's 128 weight rows
-                    const uint32_t ri = sd_it & 1;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_empty[ri]), ((sd_it >> 1) & 1) ^ 1, abortp)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t rbar = ptx::smem_u32(&B.raw_full[ri]);
-                    ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
-                    ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, (int)(sb * kQ4KBytes), n0, rbar);
                     ++sd_it;
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t st = x_it % kStages;
@@ -249,10 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int dummy = 0;
             for (uint32_t i = (x_it > kStages ? x_it - kStages : 0); i < x_it; ++i)
                 ptx::mbar_wait(ptx::smem_u32(&B.x_full[i % kStages]), (i / kStages) & 1, &dummy);
-            for (uint32_t i = (sd_it > 2 ? sd_it - 2 : 0); i < sd_it; ++i) {
+            for (uint32_t i = (sd_it > 2 ? sd_it - 2 : 0); i < sd_it; ++i)
                 ptx::mbar_wait(ptx::smem_u32(&B.sd_full[i & 1]), (i >> 1) & 1, &dummy);
-                ptx::mbar_wait(ptx::smem_u32(&B.raw_full[i & 1]), (i >> 1) & 1, &dummy);
-            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -314,8 +304,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             int dummy = 0;
             ptx::mbar_wait(ptx::smem_u32(&B.done), 0, &dummy);
         }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ raw weight TMA
+        // The raw Q4_K superblock of the tile's 128 weight rows, one per superblock,
+        // into a 2-deep ring; independent of the activation stream so neither waits on
+        // the other.
+        regs_dec<kRegsProducer>();
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tm_w);
+            int64_t u = ubeg;
+            Seg sg;
+            uint32_t r_it = 0;
+            bool ok = true;
+            while (ok && next_seg(a, u, uend, sg)) {
+                const int n0 = (int)((sg.tile % a.tiles_n) * kTN);
+                for (int64_t sb = sg.s0; sb < sg.s1; ++sb) {
+                    const uint32_t ri = r_it & 1;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_empty[ri]), ((r_it >> 1) & 1) ^ 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t rbar = ptx::smem_u32(&B.raw_full[ri]);
+                    ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
+                    ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, (int)(sb * kQ4KBytes), n0, rbar);
+                    ++r_it;
+                }
+            }
+            int dummy = 0;
+            for (uint32_t i = (r_it > 2 ? r_it - 2 : 0); i < r_it; ++i)
+                ptx::mbar_wait(ptx::smem_u32(&B.raw_full[i & 1]), (i >> 1) & 1, &dummy);
+        }
     } else if (warp < kUnpackWarp0) {
-        regs_dec<kRegsProducer>();  // warps 2-3: no role, give their registers away
+        regs_dec<kRegsProducer>();  // warp 3: no role, gives its registers away
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ weight unpack
         // One weight row per thread, reading the raw superblock that the TMA warp put in
@@ -456,7 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int hh = 0; hh < 2; ++hh) {
                     float vm[16], t[16];
                     ptx::tmem_ld_32x32b_x16(lane_base + slot * kTN + 32 * cq + 16 * hh, vm);
-                    if (!first) ptx::tmem_ld_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
+                    if (!first) {
+                        if (hh == 0) ptx::tmem_st_wait();  // the previous superblock's stores
+                        ptx::tmem_ld_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
+                    }
                     ptx::tmem_ld_wait();
 #pragma unroll
                     for (int i4 = 0; i4 < 4; ++i4) {
@@ -471,7 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tmem_st_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
                 }
-                ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -485,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             // write the segment's result: whole tile -> y, part of a tile -> this CTA's partial slot
             float res[32];
+            ptx::tmem_st_wait();
             ptx::tmem_ld_32x32b_x32(lane_base + kTotCol + 32 * cq, res);
             ptx::tmem_ld_wait();
             const int64_t tm = sg.tile / a.tiles_n, tn = sg.tile % a.tiles_n;
@@ -558,7 +581,10 @@ __global__ void tc_prep_kernel(const uint8_t *__restrict__ xq, int64_t m, int k,
 }
 
 // stream-K fixup: every tile that several CTAs share is summed in CTA order.
-__global__ void tc_fixup_kernel(TcArgs a) {
+// Grid (tiles, 16): CTA (t, part) owns 8 activation rows of tile t, one float4 of
+// 4 weight columns per thread.
+constexpr int kFixupParts = 16;
+__global__ void __launch_bounds__(256) tc_fixup_kernel(TcArgs a) {
     const int64_t t = blockIdx.x;
     const int64_t u0 = t * a.nsb, u1 = u0 + a.nsb - 1;
     auto owner = [&](int64_t uu) {
@@ -570,17 +596,25 @@ __global__ void tc_fixup_kernel(TcArgs a) {
     const int64_t c0 = owner(u0), c1 = owner(u1);
     if (c0 == c1) return;  // the tile was written whole by one CTA
     const int64_t tm = t / a.tiles_n, tn = t % a.tiles_n;
-    for (int e = threadIdx.x; e < kTM * kTN; e += blockDim.x) {
-        const int tl = e / kTN, cl = e % kTN;
-        const int64_t token = tm * kTM + tl, col = tn * kTN + cl;
-        float s = 0.f;
-        for (int64_t c = c0; c <= c1; ++c) {
-            const int64_t cb = a.nwork * c / a.ctas;
-            const int slotidx = (cb / a.nsb == t) ? 0 : 1;  // tile t is this CTA's first segment?
-            s += a.partial[((c * 2 + slotidx) * kTM + tl) * kTN + cl];
-        }
-        if (token < a.m && col < a.n) a.y[token * a.n + col] = s;
+    const int tl = blockIdx.y * (kTM / kFixupParts) + (threadIdx.x >> 5);  // 8 rows per CTA
+    const int cl = 4 * (threadIdx.x & 31);                                 // 4 columns per thread
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t c = c0; c <= c1; ++c) {
+        const int64_t cb = a.nwork * c / a.ctas;
+        const int slotidx = (cb / a.nsb == t) ? 0 : 1;  // tile t is this CTA's first segment?
+        const float4 p = *reinterpret_cast<const float4 *>(a.partial + ((c * 2 + slotidx) * kTM + tl) * kTN + cl);
+        s.x += p.x;
+        s.y += p.y;
+        s.z += p.z;
+        s.w += p.w;
     }
+    const int64_t token = tm * kTM + tl, col = tn * kTN + cl;
+    if (token >= a.m) return;
+    float *dst = a.y + token * a.n + col;
+    const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (col + j < a.n) dst[j] = sv[j];
 }
 
 // ---------------------------------------------------------------- host side
@@ -706,7 +740,7 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.stream_k && p.fixup) {
-        tc_fixup_kernel<<<(unsigned)p.ntiles, 256, 0, st>>>(args);
+        tc_fixup_kernel<<<dim3((unsigned)p.ntiles, kFixupParts), 256, 0, st>>>(args);
         e = cudaGetLastError();
     }
     return e;
