@@ -81,6 +81,21 @@ static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
     return kGemmDp4a;
 }
 
+qmm_status moe_check_sizes(qmm_type t, int64_t n_experts, int64_t n, int64_t k, int64_t top_k, int64_t n_tokens) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n_experts <= 0 || top_k <= 0 || n < 0 || n_tokens < 0) return QMM_ERR_ARG;
+    if (n_experts > kMaxExperts || n > kMaxRows || n_tokens * top_k > kMaxRows) return QMM_ERR_SHAPE;
+    return QMM_OK;
+}
+
+qmm_status moe_check_pointers(const void *W_experts, const void *xq, const int32_t *ids, const float *y) {
+    if (!W_experts || !xq || !ids || !y) return QMM_ERR_ARG;
+    if (!aligned16(W_experts) || !aligned16(xq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(ids) & 3u))
+        return QMM_ERR_ALIGN;
+    return QMM_OK;
+}
+
 }  // namespace qmm
 
 using namespace qmm;
@@ -155,10 +170,8 @@ qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, const vo
 qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
                           const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
                           void *workspace, size_t ws_bytes, void *stream) {
-    qmm_status s = check_k(t, k);
+    qmm_status s = moe_check_sizes(t, n_experts, n, k, top_k, n_tokens);
     if (s != QMM_OK) return s;
-    if (n_experts <= 0 || top_k <= 0 || n < 0 || n_tokens < 0) return QMM_ERR_ARG;
-    if (n_experts > kMaxExperts || n > kMaxRows || n_tokens * top_k > kMaxRows) return QMM_ERR_SHAPE;
     if (!workspace) return QMM_ERR_WORKSPACE;
     if (!aligned256(workspace)) return QMM_ERR_ALIGN;
     const size_t need = moe_workspace_bytes(t, n, k, n_tokens, n_experts, top_k);
@@ -168,9 +181,8 @@ qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, 
         // empty problem: only reset the status word
         return cuda_status(cudaMemsetAsync(workspace, 0, 16, st));
     }
-    if (!W_experts || !xq || !ids || !y) return QMM_ERR_ARG;
-    if (!aligned16(W_experts) || !aligned16(xq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(ids) & 3u))
-        return QMM_ERR_ALIGN;
+    s = moe_check_pointers(W_experts, xq, ids, y);
+    if (s != QMM_OK) return s;
     return cuda_status(launch_mul_mat_id(t, W_experts, n_experts, n, k, xq, ids, top_k, n_tokens, y, workspace,
                                          ws_bytes, st));
 }

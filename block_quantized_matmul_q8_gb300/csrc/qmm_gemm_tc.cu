@@ -43,6 +43,7 @@
 
 #include "qmm_common.cuh"
 #include "qmm_internal.h"
+#include "qmm_moe.h"
 #include "qmm_tc_ptx.cuh"
 
 namespace qmm {
@@ -94,7 +95,37 @@ struct TcArgs {
     int64_t nwork;
     int ctas;
     int stream_k;
+    // expert-grouped mode (tiles != nullptr): the activation arrays hold the (token,
+    // slot) pairs in expert-sorted order, W is [E][n] rows, y is [pairs][n]
+    const MoETile *tiles;
+    const int32_t *ntiles;  // device: number of token tiles in `tiles`
+    const int32_t *bounds;
+    const int32_t *perm;
 };
+
+// Where tile t lives: m0 = first activation row (sorted row in grouped mode), rows =
+// valid activation rows, n0w = first row in the weight tensor map, col0 = first output
+// column.
+struct TileInfo {
+    int m0, rows, n0w;
+    int64_t col0;
+};
+__device__ __forceinline__ TileInfo resolve_tile(const TcArgs &a, int64_t t) {
+    TileInfo ti;
+    const int64_t tn = t % a.tiles_n;
+    ti.col0 = tn * kTN;
+    if (a.tiles) {
+        const MoETile mt = a.tiles[t / a.tiles_n];
+        ti.m0 = a.bounds[mt.expert] + mt.first;
+        ti.rows = min(kTM, mt.count - mt.first);
+        ti.n0w = (int)(int64_t(mt.expert) * a.n + ti.col0);
+    } else {
+        ti.m0 = (int)((t / a.tiles_n) * kTM);
+        ti.rows = a.m - ti.m0 < kTM ? (int)(a.m - ti.m0) : kTM;
+        ti.n0w = (int)ti.col0;
+    }
+    return ti;
+}
 
 struct Barriers {
     uint64_t x_full[kStages], x_empty[kStages], w_full[kStages], w_empty[kStages];
@@ -195,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = B.tmem_base;
 
+    if (a.tiles) a.nwork = int64_t(*a.ntiles) * a.tiles_n * a.nsb;
     int64_t ubeg, uend;
     cta_range(a, blockIdx.x, ubeg, uend);
 
@@ -210,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t x_it = 0, sd_it = 0;
             bool ok = true;
             while (ok && next_seg(a, u, uend, sg)) {
-                const int m0 = (int)((sg.tile / a.tiles_n) * kTM);
+                const int m0 = resolve_tile(a, sg.tile).m0;
                 for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                     const uint32_t sdi = sd_it & 1;
                     if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[sdi]), ((sd_it >> 1) & 1) ^ 1, abortp)) {
@@ -317,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r_it = 0;
             bool ok = true;
             while (ok && next_seg(a, u, uend, sg)) {
-                const int n0 = (int)((sg.tile % a.tiles_n) * kTN);
+                const int n0 = resolve_tile(a, sg.tile).n0w;
                 for (int64_t sb = sg.s0; sb < sg.s1; ++sb) {
                     const uint32_t ri = r_it & 1;
                     if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_empty[ri]), ((r_it >> 1) & 1) ^ 1, abortp)) {
@@ -510,13 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_st_wait();
             ptx::tmem_ld_32x32b_x32(lane_base + kTotCol + 32 * cq, res);
             ptx::tmem_ld_wait();
-            const int64_t tm = sg.tile / a.tiles_n, tn = sg.tile % a.tiles_n;
-            const int64_t token = tm * kTM + tl;
-            const int64_t col0 = tn * kTN + 32 * cq;
+            const TileInfo ti = resolve_tile(a, sg.tile);
+            const int64_t col0 = ti.col0 + 32 * cq;
             const bool full = sg.s0 == 0 && sg.s1 == a.nsb;
             if (full) {
-                if (token < a.m) {
-                    float *dst = a.y + token * a.n + col0;
+                if (tl < ti.rows) {
+                    const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
+                    float *dst = a.y + yrow * a.n + col0;
                     if ((a.n % 4 == 0) && (col0 + 32 <= a.n)) {
 #pragma unroll
                         for (int i4 = 0; i4 < 8; ++i4)
@@ -580,12 +612,52 @@ __global__ void tc_prep_kernel(const uint8_t *__restrict__ xq, int64_t m, int k,
     }
 }
 
+// Expert-grouped variant of tc_prep_kernel: sorted row j holds the activation row of
+// pair perm[j] (token perm[j] / top_k).  Rows of invalid pairs are left as they are:
+// the GEMM computes them but never stores them.
+__global__ void tc_prep_gather_kernel(const uint8_t *__restrict__ xq, int k, const int32_t *__restrict__ perm,
+                                      const int32_t *__restrict__ bounds, int E, int top_k, int64_t n_pairs,
+                                      __half *__restrict__ xh, float *__restrict__ dx, __half *__restrict__ smin) {
+    const int nb32 = k / 32;
+    const int64_t nvalid = bounds[E];
+    const int64_t total = n_pairs * nb32;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t j = i / nb32;
+        if (j >= nvalid) continue;
+        const int b = (int)(i - j * nb32);
+        const int64_t tok = perm[j] / top_k;
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (tok * nb32 + b) * kQ81Bytes);
+        const uint32_t dsw = ldg4(src);
+        uint4 *dst = reinterpret_cast<uint4 *>(xh + j * k + 32 * b);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t w0 = ldg4(src + 1 + 2 * q), w1 = ldg4(src + 2 + 2 * q);
+            const int8_t *c0 = reinterpret_cast<const int8_t *>(&w0);
+            const int8_t *c1 = reinterpret_cast<const int8_t *>(&w1);
+            uint4 o;
+            o.x = h2bits(__halves2half2(__int2half_rn(c0[0]), __int2half_rn(c0[1])));
+            o.y = h2bits(__halves2half2(__int2half_rn(c0[2]), __int2half_rn(c0[3])));
+            o.z = h2bits(__halves2half2(__int2half_rn(c1[0]), __int2half_rn(c1[1])));
+            o.w = h2bits(__halves2half2(__int2half_rn(c1[2]), __int2half_rn(c1[3])));
+            dst[q] = o;
+        }
+        dx[i] = half_lo(dsw);
+        __half *sp = smin + (j * (nb32 / 8) + b / 8) * 16;
+        sp[b % 8] = __ushort_as_half((unsigned short)(dsw >> 16));
+        sp[8 + b % 8] = __ushort_as_half(0);
+    }
+}
+
 // stream-K fixup: every tile that several CTAs share is summed in CTA order.
 // Grid (tiles, 16): CTA (t, part) owns 8 activation rows of tile t, one float4 of
 // 4 weight columns per thread.
 constexpr int kFixupParts = 16;
 __global__ void __launch_bounds__(256) tc_fixup_kernel(TcArgs a) {
     const int64_t t = blockIdx.x;
+    if (a.tiles) {
+        a.nwork = int64_t(*a.ntiles) * a.tiles_n * a.nsb;
+        if (t >= int64_t(*a.ntiles) * a.tiles_n) return;
+    }
     const int64_t u0 = t * a.nsb, u1 = u0 + a.nsb - 1;
     auto owner = [&](int64_t uu) {
         int64_t c = uu * a.ctas / a.nwork;
@@ -595,12 +667,13 @@ __global__ void __launch_bounds__(256) tc_fixup_kernel(TcArgs a) {
     };
     const int64_t c0 = owner(u0), c1 = owner(u1);
     if (c0 == c1) return;  // the tile was written whole by one CTA
-    const int64_t tm = t / a.tiles_n, tn = t % a.tiles_n;
+    const TileInfo ti = resolve_tile(a, t);
     const int tl = blockIdx.y * (kTM / kFixupParts) + (threadIdx.x >> 5);  // 8 rows per CTA
     const int cl = 4 * (threadIdx.x & 31);                                 // 4 columns per thread
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t c = c0; c <= c1; ++c) {
         const int64_t cb = a.nwork * c / a.ctas;
+        if (a.nwork * (c + 1) / a.ctas == cb) continue;  // fewer units than CTAs: c owns nothing
         const int slotidx = (cb / a.nsb == t) ? 0 : 1;  // tile t is this CTA's first segment?
         const float4 p = *reinterpret_cast<const float4 *>(a.partial + ((c * 2 + slotidx) * kTM + tl) * kTN + cl);
         s.x += p.x;
@@ -608,9 +681,10 @@ __global__ void __launch_bounds__(256) tc_fixup_kernel(TcArgs a) {
         s.z += p.z;
         s.w += p.w;
     }
-    const int64_t token = tm * kTM + tl, col = tn * kTN + cl;
-    if (token >= a.m) return;
-    float *dst = a.y + token * a.n + col;
+    const int64_t col = ti.col0 + cl;
+    if (tl >= ti.rows) return;
+    const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
+    float *dst = a.y + yrow * a.n + col;
     const float sv[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -680,6 +754,43 @@ size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m) {
     return tc_layout(m, k, std::min<int64_t>(kMaxPartialCtas, nwork)).total;
 }
 
+namespace {
+
+// Launch the GEMM kernel (and the fixup pass when asked) once the maps are built.
+cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CUtensorMap &tm_dx,
+                   const CUtensorMap &tm_w, const TcArgs &args, int ctas, int64_t fixup_tiles, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    // The setmaxnreg split hands out exactly kThreads x kLaunchRegs registers; a build that
+    // launches with fewer registers per thread would leave setmaxnreg.inc waiting forever.
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, gemm_tc_q4k_kernel) != cudaSuccess) return cudaErrorInvalidValue;
+        launch_regs = fa.numRegs;
+    }
+    if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    gemm_tc_q4k_kernel<<<ctas, kThreads, kSmemAlloc, st>>>(tm_x, tm_xmin, tm_dx, tm_w, args);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (fixup_tiles > 0) {
+        tc_fixup_kernel<<<dim3((unsigned)fixup_tiles, kFixupParts), 256, 0, st>>>(args);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+bool make_act_maps(CUtensorMap &tm_x, CUtensorMap &tm_xmin, CUtensorMap &tm_dx, const __half *xh, const float *dx,
+                   const __half *smin, int64_t rows, int64_t k) {
+    return make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, k, rows, 64, kTM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map_2d(&tm_xmin, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, smin, (k / 256) * 16, rows, 16, kTM,
+                       CU_TENSOR_MAP_SWIZZLE_32B) &&
+           make_map_2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx, k / 32, rows, 8, kTM, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
                            void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st) {
     if (!gemm_tc_supported(t, n, k, m)) return cudaErrorNotSupported;
@@ -702,10 +813,7 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     if (e != cudaSuccess) return e;
 
     CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
-    if (!make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, k, m, 64, kTM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&tm_xmin, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, smin, (k / 256) * 16, m, 16, kTM,
-                     CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_map_2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx, k / 32, m, 8, kTM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) ||
         !make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, (k / 256) * kQ4KBytes, n, kQ4KBytes, kTN,
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
@@ -724,26 +832,63 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     args.nwork = p.nwork;
     args.ctas = p.ctas;
     args.stream_k = p.stream_k;
+    return run_tc(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, (p.stream_k && p.fixup) ? p.ntiles : 0, st);
+}
 
-    e = cudaFuncSetAttribute(gemm_tc_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+// ---------------------------------------------------------------- expert-grouped mode
+
+bool gemm_tc_grouped_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k) {
+    return t == QMM_Q4_K && k % 256 == 0 && n > 0 && n_experts * n < (int64_t(1) << 31);
+}
+
+size_t gemm_tc_grouped_bytes(int64_t n_pairs, int64_t k) {
+    return tc_layout(n_pairs, k, device_sm_count() < kMaxPartialCtas ? device_sm_count() : kMaxPartialCtas).total;
+}
+
+cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                                   int64_t top_k, int64_t n_pairs, float *y, const MoETile *tiles,
+                                   const int32_t *ntiles, int64_t max_token_tiles, const int32_t *bounds,
+                                   const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st) {
+    const int ctas = std::min(device_sm_count(), kMaxPartialCtas);
+    const TcLayout L = tc_layout(n_pairs, k, ctas);
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    __half *xh = reinterpret_cast<__half *>(base + L.xh);
+    float *dx = reinterpret_cast<float *>(base + L.dx);
+    __half *smin = reinterpret_cast<__half *>(base + L.smin);
+
+    const int64_t nblk = n_pairs * (k / 32);
+    const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
+    tc_prep_gather_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), (int)k, perm, bounds,
+                                                             (int)n_experts, (int)top_k, n_pairs, xh, dx, smin);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // The setmaxnreg split hands out exactly kThreads x kLaunchRegs registers; a build that
-    // launches with fewer registers per thread would leave setmaxnreg.inc waiting forever.
-    static int launch_regs = -1;
-    if (launch_regs < 0) {
-        cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, gemm_tc_q4k_kernel) != cudaSuccess) return cudaErrorInvalidValue;
-        launch_regs = fa.numRegs;
-    }
-    if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    gemm_tc_q4k_kernel<<<p.ctas, kThreads, kSmemAlloc, st>>>(tm_x, tm_xmin, tm_dx, tm_w, args);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (p.stream_k && p.fixup) {
-        tc_fixup_kernel<<<dim3((unsigned)p.ntiles, kFixupParts), 256, 0, st>>>(args);
-        e = cudaGetLastError();
-    }
-    return e;
+
+    CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
+    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, n_pairs, k) ||
+        !make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, (k / 256) * kQ4KBytes, n_experts * n, kQ4KBytes,
+                     kTN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+
+    TcArgs args{};
+    args.W = static_cast<const uint8_t *>(W);
+    args.n = n;
+    args.m = n_pairs;
+    args.k = (int)k;
+    args.row_bytes = (k / 256) * kQ4KBytes;
+    args.y = y;
+    args.partial = reinterpret_cast<float *>(base + L.partial);
+    args.status = status;
+    args.tiles_n = (n + kTN - 1) / kTN;
+    args.nsb = k / 256;
+    args.nwork = 0;  // read from the device tile count by the kernels
+    args.ctas = ctas;
+    args.stream_k = 1;
+    args.tiles = tiles;
+    args.ntiles = ntiles;
+    args.bounds = bounds;
+    args.perm = perm;
+    return run_tc(tm_x, tm_xmin, tm_dx, tm_w, args, ctas, max_token_tiles * args.tiles_n, st);
 }
 
 }  // namespace qmm

@@ -58,11 +58,28 @@ bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
 cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
                            void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st);
 
+// Expert-grouped tensor-core GEMM over a device-built tile list (see qmm_moe.h).
+struct MoETile;
+bool gemm_tc_grouped_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k);
+size_t gemm_tc_grouped_bytes(int64_t n_pairs, int64_t k);
+cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                                   int64_t top_k, int64_t n_pairs, float *y, const MoETile *tiles,
+                                   const int32_t *ntiles, int64_t max_token_tiles, const int32_t *bounds,
+                                   const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st);
+
 // MoE: device bucketing + grouped GEMM.
 size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k);
 cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                               const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *ws,
                               size_t ws_bytes, cudaStream_t st);
+// Argument checks of qmm_mul_mat_id shared by its entry points.
+qmm_status moe_check_sizes(qmm_type t, int64_t n_experts, int64_t n, int64_t k, int64_t top_k, int64_t n_tokens);
+qmm_status moe_check_pointers(const void *W_experts, const void *xq, const int32_t *ids, const float *y);
+// The same computation on CUDA-core tiles only; its scratch is small (bucketing only).
+size_t moe_dp4a_workspace_bytes(int64_t n_tokens, int64_t n_experts, int64_t top_k);
+cudaError_t launch_mul_mat_id_dp4a(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k,
+                                   const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
+                                   void *ws, size_t ws_bytes, cudaStream_t st);
 
 // Offset of the device status word inside a mul_mat_id workspace.
 constexpr size_t kStatusOffset = 0;

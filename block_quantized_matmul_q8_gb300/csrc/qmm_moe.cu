@@ -167,19 +167,27 @@ cudaError_t launch_moe_bucket(const int32_t *ids, int64_t n_pairs, int n_experts
     return cudaGetLastError();
 }
 
-size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k) {
-    (void)t; (void)n; (void)k;
-    return moe_layout(n_tokens * top_k, n_experts, 64, 0).total;
+constexpr int kDp4aTileTokens = 64;   // pairs per token tile of the CUDA-core grouped GEMM
+constexpr int kTcTileTokens = 128;    // pairs per token tile of the tensor-core grouped GEMM
+
+size_t moe_dp4a_workspace_bytes(int64_t n_tokens, int64_t n_experts, int64_t top_k) {
+    return moe_layout(n_tokens * top_k, n_experts, kDp4aTileTokens, 0).total;
 }
 
-cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
-                              const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *ws,
-                              size_t ws_bytes, cudaStream_t st) {
-    const int tile_tokens = 64;
+size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k) {
     const int64_t n_pairs = n_tokens * top_k;
-    const MoELayout L = moe_layout(n_pairs, n_experts, tile_tokens, 0);
+    if (gemm_tc_grouped_supported(t, n_experts, n, k))
+        return moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k)).total;
+    return moe_dp4a_workspace_bytes(n_tokens, n_experts, top_k);
+}
+
+cudaError_t launch_mul_mat_id_dp4a(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k,
+                                   const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
+                                   void *ws, size_t ws_bytes, cudaStream_t st) {
+    const int64_t n_pairs = n_tokens * top_k;
+    const MoELayout L = moe_layout(n_pairs, n_experts, kDp4aTileTokens, 0);
     if (ws_bytes < L.total) return cudaErrorInvalidValue;
-    cudaError_t e = launch_moe_bucket(ids, n_pairs, (int)n_experts, tile_tokens, ws, L, st);
+    cudaError_t e = launch_moe_bucket(ids, n_pairs, (int)n_experts, kDp4aTileTokens, ws, L, st);
     if (e != cudaSuccess) return e;
     uint8_t *base = static_cast<uint8_t *>(ws);
     const int32_t *status = reinterpret_cast<const int32_t *>(base + L.status);
@@ -190,6 +198,29 @@ cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int6
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_gemm_dp4a_grouped(t, W, n, k, xq, y, tiles, status + 1, bounds, perm, (int)top_k, st);
+}
+
+cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                              const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *ws,
+                              size_t ws_bytes, cudaStream_t st) {
+    if (!gemm_tc_grouped_supported(t, n_experts, n, k))
+        return launch_mul_mat_id_dp4a(t, W, n_experts, n, k, xq, ids, top_k, n_tokens, y, ws, ws_bytes, st);
+    const int64_t n_pairs = n_tokens * top_k;
+    const MoELayout L = moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k));
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    cudaError_t e = launch_moe_bucket(ids, n_pairs, (int)n_experts, kTcTileTokens, ws, L, st);
+    if (e != cudaSuccess) return e;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    int32_t *status = reinterpret_cast<int32_t *>(base + L.status);
+    const int32_t *bounds = reinterpret_cast<const int32_t *>(base + L.bounds);
+    const int32_t *perm = reinterpret_cast<const int32_t *>(base + L.perm);
+    const MoETile *tiles = reinterpret_cast<const MoETile *>(base + L.tiles);
+    moe_zero_invalid_kernel<<<64, 256, 0, st>>>(status, perm, bounds, (int)n_experts, y, n);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t max_token_tiles = n_pairs / kTcTileTokens + n_experts + 1;
+    return launch_gemm_tc_grouped(W, n_experts, n, k, xq, top_k, n_pairs, y, tiles, status + 1, max_token_tiles,
+                                  bounds, perm, status, base + L.gemm, L.total - L.gemm, st);
 }
 
 }  // namespace qmm

@@ -54,15 +54,25 @@ using namespace qmm;
 
 extern "C" size_t qmm_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
+// The workspace variant hands Q4_K problems to the tensor-core grouped GEMM, whose
+// scratch (an fp16 copy of the gathered activations) grows with the problem; this
+// entry point keeps to the CUDA-core grouped GEMM, whose scratch is only the
+// bucketing state, so that the fixed array stays small.
 extern "C" qmm_status qmm_mul_mat_id_noalloc(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n,
                                              int64_t k, const void *xq, const int32_t *ids, int64_t top_k,
                                              int64_t n_tokens, float *y, void *stream) {
-    if (n_experts <= 0 || top_k <= 0 || n < 0 || n_tokens < 0) return QMM_ERR_ARG;
-    const size_t need = qmm_workspace_bytes(t, n, k, n_tokens, n_experts, top_k);
-    if (need == 0) return QMM_ERR_ARG;
+    qmm_status s = moe_check_sizes(t, n_experts, n, k, top_k, n_tokens);
+    if (s != QMM_OK) return s;
+    const size_t need = moe_dp4a_workspace_bytes(n_tokens, n_experts, top_k);
     if (need > kNoAllocScratchBytes) return QMM_ERR_WORKSPACE;  // problem needs more than the fixed scratch
     void *ws = scratch_ptr();
     if (!ws) return QMM_ERR_CUDA;
-    return qmm_mul_mat_id(W_experts, t, n_experts, n, k, xq, ids, top_k, n_tokens, y, ws, kNoAllocScratchBytes,
-                          stream);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n == 0 || n_tokens == 0) return cudaMemsetAsync(ws, 0, 16, st) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    s = moe_check_pointers(W_experts, xq, ids, y);
+    if (s != QMM_OK) return s;
+    return launch_mul_mat_id_dp4a(t, W_experts, n_experts, n, k, xq, ids, top_k, n_tokens, y, ws,
+                                  kNoAllocScratchBytes, st) == cudaSuccess
+               ? QMM_OK
+               : QMM_ERR_CUDA;
 }

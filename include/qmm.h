@@ -75,8 +75,11 @@ QMM_API size_t qmm_q8_1_bytes(int64_t m, int64_t k);
 QMM_API size_t qmm_row_bytes(qmm_type t, int64_t k);
 
 /* Workspace bytes that qmm_mul_mat (n_experts == 0) or qmm_mul_mat_id
- * (n_experts > 0) needs for these sizes.  The workspace must be 256-byte
- * aligned device memory; its contents need no initialisation. */
+ * (n_experts > 0) needs for these sizes on the CURRENT device (the tensor-core
+ * paths keep one partial-sum slot per SM, so the figure depends on the SM count:
+ * size the workspace with the device current on which the call will run).  The
+ * workspace must be 256-byte aligned device memory; its contents need no
+ * initialisation. */
 QMM_API size_t qmm_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t n_experts, int64_t top_k);
 
 /*
@@ -124,6 +127,9 @@ QMM_API qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, 
  * sort) and the per-expert tiles are walked by one persistent launch; the host
  * never reads ids, so the call does not synchronise.  A pair whose id is outside
  * [0, n_experts) gets a zero output row and sets QMM_ERR_IDS in the status word.
+ * Q4_K with k % 256 == 0 runs on the tensor cores (128-pair tiles, stream-K over
+ * the device-built tile list; the workspace then also holds an fp16 copy of the
+ * gathered activations); the other formats run the CUDA-core grouped GEMM.
  */
 QMM_API qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                           const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *workspace,
@@ -136,9 +142,13 @@ QMM_API qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_e
  * captures).  The pages have no counterpart of this call.
  *   Arguments, layouts and results are those of qmm_mul_mat_id.
  *   Scratch: one file-scope device array of qmm_noalloc_scratch_bytes() (1 MiB),
- *   present in every GPU that loads the library until the process exits.  A problem
- *   whose qmm_workspace_bytes() exceeds it is rejected with QMM_ERR_WORKSPACE and
- *   nothing is enqueued.  The call allocates nothing and frees nothing.
+ *   present in every GPU that loads the library until the process exits.  This call
+ *   always runs the CUDA-core grouped GEMM, whose scratch is the bucketing state
+ *   alone: 256 B of status, 4*(n_experts+1) B of bounds, 4 B per (token, slot)
+ *   pair and 16 B per tile (pairs/64 + n_experts + 1 tiles), each piece rounded up
+ *   to 256 B, so up to about 240K pairs fit.  A larger problem is rejected with
+ *   QMM_ERR_WORKSPACE and nothing is enqueued.  The call allocates nothing and
+ *   frees nothing.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture.  Every call on a device shares the array: calls whose work can

@@ -144,8 +144,10 @@ def moe_check(oracle_mod, E, n, k, T_, K, seed, corrupt=0):
     assert_within(y.cpu().numpy(), y_ref, Tr, f"moe E={E} n={n} k={k} T={T_} K={K}")
 
 
+# The last two put several 128-pair tiles on each expert and split tiles between
+# CTAs of the stream-K schedule of the tensor-core grouped GEMM (partials + fixup).
 @pytest.mark.parametrize("E,n,k,T_,K", [(4, 64, 256, 9, 2), (16, 130, 512, 70, 4), (128, 96, 256, 512, 8),
-                                        (3, 33, 512, 200, 3)])
+                                        (3, 33, 512, 200, 3), (8, 384, 2048, 600, 2), (5, 200, 1024, 333, 3)])
 def test_moe_parity(oracle_mod, E, n, k, T_, K):
     moe_check(oracle_mod, E, n, k, T_, K, seed=E + n + T_)
 

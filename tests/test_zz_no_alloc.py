@@ -30,7 +30,6 @@ def test_noalloc_matches_workspace_call_twice():
         Wd = torch.from_numpy(W).to(DEV)
         idd = torch.from_numpy(ids).to(DEV)
         xq = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(DEV))
-        assert qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, K) <= L.qmm_noalloc_scratch_bytes()
         ws = torch.empty(qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, K), dtype=torch.uint8, device=DEV)
         y_ref = qmm.qmm_mul_mat_id(Wd, "q4_K", E, n, k, xq, idd, K, T_, workspace=ws)
         torch.cuda.synchronize()
@@ -44,7 +43,9 @@ def test_noalloc_matches_workspace_call_twice():
             torch.cuda.synchronize()
             got = y.cpu().numpy().astype(np.float64)
             assert np.all(np.isfinite(got)), f"call {call}: unwritten outputs"
-            # same kernels on the same inputs: agreement far inside the parity tolerance
+            # the workspace call may take the tensor-core grouped GEMM and this one the
+            # CUDA-core one: both sum the same exact integer dots and differ only in the
+            # fp32 order of the fold, far inside the parity tolerance
             assert np.all(np.abs(got - ref) <= TOL * scale), f"call {call}: differs from the workspace call"
 
 
