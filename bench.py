@@ -48,7 +48,7 @@ import qmm_synth  # noqa: E402
 METRIC = "Q4_K matmul HBM GB/s at m=1 and int8 TOPS at m=512/MoE, % of GB300 roofline"
 UNIT = "GB/s"
 N, K, M = 17408, 5120, 1
-WORKLOAD = "decode GEMV Q4_K n=17408 k=5120 m=1 (quantize x + mul_mat)"
+WORKLOAD = "decode GEMV Q4_K n=17408 k=5120 m=1 (fp32 x in, quantized in the GEMV prologue, y out: one launch)"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -69,12 +69,14 @@ def aggregate_rate(world, bytes_per_step, ms_per_step):
 
 
 def step_bytes(n, k, m, row_bytes):
-    """Algorithmic bytes of one step: W once, x read, q8_1 written and read, y written."""
-    return n * row_bytes + m * k * 4 + 2 * m * (k // 32) * 36 + m * n * 4
+    """Algorithmic bytes of one step (fp32 x in, quantized on chip, y out): W once, x
+    read, y written.  At m <= 8 the step is one launch, so these are also the bytes of
+    that launch."""
+    return n * row_bytes + m * k * 4 + m * n * 4
 
 
-def gemv_bytes(n, k, m, row_bytes):
-    """Algorithmic bytes of one GEMV launch: W once, q8_1 read, y written."""
+def gemv_q8_bytes(n, k, m, row_bytes):
+    """Algorithmic bytes of one GEMV launch from q8_1 activations: W once, q8_1 read, y written."""
     return n * row_bytes + m * (k // 32) * 36 + m * n * 4
 
 
@@ -248,9 +250,15 @@ def capture(torch, fn, first, count):
     return g
 
 
+HOLD_CYCLES = 200_000  # ~0.1 ms of device time at 2 GHz
+
+
 def time_graphs(torch, fn, steps, warmup, barrier):
     """Graph timing: eager warm-up, a graph of the W warm-up steps replayed, then a
-    graph of exactly K steps replayed once between two events."""
+    graph of exactly K steps replayed once between two events.  A short device-side
+    hold is queued in front of the first event, so that the GPU is still busy while the
+    host submits the graph: the events then time the K steps on the device, not the
+    host's graph-submission latency."""
     for i in range(2):
         fn(i)
     torch.cuda.synchronize()
@@ -262,6 +270,7 @@ def time_graphs(torch, fn, steps, warmup, barrier):
     stream = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(HOLD_CYCLES)
     e0.record(stream)
     gt.replay()
     e1.record(stream)
@@ -275,21 +284,31 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak):
     GB/s (and fraction of the HBM peak), GEMM and MoE rows in TOPS (2*m*n*k)."""
     out = {}
 
-    def dense(fmt, n, k, ms):
+    def dense(fmt, n, k, ms, q8_input=False):
+        """Whole path from fp32 x (qmm_mul_mat_f32); q8_input times qmm_mul_mat on
+        pre-quantized activations instead."""
         rows = {}
         W, x = qmm_synth.make_dense(fmt, n, k, max(ms), seed=0)
         copies = max(1, int(3 * L2_BYTES // W.nbytes) + 1)
         Wd = [torch.from_numpy(W).to(dev) for _ in range(copies)]
-        xq_all = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
+        x_all = torch.from_numpy(x).to(dev)
+        xq_all = qmm.qmm_quantize_q8_1(x_all)
         for m in ms:
+            xm = x_all[:m].contiguous()
             xq = xq_all[:m].contiguous()
             y = torch.empty((m, n), device=dev)
-            ws = torch.empty(max(1, qmm.qmm_workspace_bytes(fmt, n, k, m)), dtype=torch.uint8, device=dev)
-            fn = lambda i: qmm.qmm_mul_mat(Wd[i % copies], fmt, n, k, xq, m, y=y, workspace=ws)
+            if q8_input:
+                ws = torch.empty(max(1, qmm.qmm_workspace_bytes(fmt, n, k, m)), dtype=torch.uint8, device=dev)
+                fn = lambda i: qmm.qmm_mul_mat(Wd[i % copies], fmt, n, k, xq, m, y=y, workspace=ws)
+                xb = m * (k // 32) * 36
+            else:
+                ws = torch.empty(max(1, qmm.qmm_workspace_bytes_f32(fmt, n, k, m)), dtype=torch.uint8, device=dev)
+                fn = lambda i: qmm.qmm_mul_mat_f32(Wd[i % copies], fmt, n, k, xm, m, y=y, workspace=ws)
+                xb = m * k * 4
             ms_call = time_graphs(torch, fn, steps, 3, lambda: None) / steps
-            key = f"{fmt}_n{n}_k{k}_m{m}"
+            key = f"{fmt}_n{n}_k{k}_m{m}" + ("_q8_1_input" if q8_input else "")
             if m <= 8:
-                b = W.nbytes + m * (k // 32) * 36 + m * n * 4
+                b = W.nbytes + xb + m * n * 4
                 rows[key] = {"GB/s": b / (ms_call * 1e-3) / 1e9, "hbm_frac": b / (ms_call * 1e-3) / 1e9 / hbm_peak,
                              "ms": ms_call}
             else:
@@ -298,6 +317,7 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak):
         del Wd
         return rows
 
+    out.update(dense("q4_K", 17408, 5120, [1], q8_input=True))
     out.update(dense("q4_K", 17408, 5120, [2, 4, 5, 8]))
     out.update(dense("q4_K", 1024, 2048, [16]))
     out.update(dense("q4_K", 14336, 4096, [512, 2048]))
@@ -357,40 +377,36 @@ def main():
     Wd = [torch.from_numpy(W).to(dev) for _ in range(copies)]
     x_h = torch.from_numpy(x).pin_memory()
     x_d = x_h.to(dev)
-    xq = torch.empty((M, (K // 32) * 36), dtype=torch.uint8, device=dev)
     y = torch.empty((M, N), device=dev)
     y_h = torch.empty((M, N), dtype=torch.float32).pin_memory()
     stream = torch.cuda.current_stream()
 
-    # --- device-resident steps (graph-replayed): quantize x, then the GEMV
+    # --- device-resident steps (graph-replayed): one call from fp32 x, which at m = 1 is
+    # one launch of the GEMV that quantizes x in its prologue
     def step(i):
-        qmm.qmm_quantize_q8_1(x_d, out=xq)
-        qmm.qmm_mul_mat(Wd[i % copies], "q4_K", N, K, xq, M, y=y)
-
-    def gemv_only(i):
-        qmm.qmm_mul_mat(Wd[i % copies], "q4_K", N, K, xq, M, y=y)
+        qmm.qmm_mul_mat_f32(Wd[i % copies], "q4_K", N, K, x_d, M, y=y)
 
     with ClockSampler(local) as clk:
         ms_total = time_graphs(torch, step, args.steps, args.warmup, barrier)
-        gemv_ms = time_graphs(torch, gemv_only, args.steps, args.warmup, barrier) / args.steps
     clocks = clk.summary()
 
     # --- end to end through the public API with host buffers (pinned), copies inside the region
     def step_e2e(i):
         x_d.copy_(x_h, non_blocking=True)
-        qmm.qmm_quantize_q8_1(x_d, out=xq, stream=stream)
-        qmm.qmm_mul_mat(Wd[i % copies], "q4_K", N, K, xq, M, y=y, stream=stream)
+        qmm.qmm_mul_mat_f32(Wd[i % copies], "q4_K", N, K, x_d, M, y=y, stream=stream)
         y_h.copy_(y, non_blocking=True)
 
     ms_e2e = time_region(torch, step_e2e, args.steps, args.warmup, stream, barrier)
 
-    ms_total, ms_e2e, gemv_ms = max_over_ranks([ms_total, ms_e2e, gemv_ms], device=dev)
+    ms_total, ms_e2e = max_over_ranks([ms_total, ms_e2e], device=dev)
     ms_step = ms_total / args.steps
     sb = step_bytes(N, K, M, row_bytes)
     value = aggregate_rate(world, sb, ms_step)
     e2e_value = aggregate_rate(world, sb, ms_e2e / args.steps)
     hbm_peak, tf_peak, peak_src = measured_peaks()
-    kb = gemv_bytes(N, K, M, row_bytes)
+    # the step is one launch of the GEMV kernel: its duration is the step's
+    gemv_ms = ms_step
+    kb = sb
     achieved = kb / (gemv_ms * 1e-3) / 1e9
     traffic = recorded_traffic("gemv_q4k_tma_kernel<1>")
 
@@ -406,18 +422,19 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8 dot (exact int32) + fp32 fold", "data": "synthetic",
             "config": {"workload": WORKLOAD, "n": N, "k": K, "m": M, "format": "Q4_K", "seed": 0,
-                       "timing": "CUDA graph replay of exactly K steps between events",
+                       "timing": "CUDA graph replay of exactly K steps between events (device-side hold "
+                                 "queued before the first event hides the host's graph submission)",
                        "l2": f"rotating {copies} weight copies ({copies * W.nbytes / 1e6:.0f} MB > 3x L2)",
                        "replicas": world},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "gemv_q4k_tma_kernel<1>",
                          "peak_source": f"{peak_src} HBM copy bandwidth", "kernel_ms": gemv_ms,
-                         "kernel_timing": "graph of K back-to-back GEMV launches between events",
+                         "kernel_timing": "graph of K back-to-back steps (one GEMV launch each) between events",
                          "algorithmic_bytes": kb},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": M * K * 4,
                     "d2h_bytes_per_step": M * N * 4, "ms_per_step": ms_e2e / args.steps,
                     "how": "eager Python calls (no graph), pinned host x copied in and y copied out each step"},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "secondary": sec,

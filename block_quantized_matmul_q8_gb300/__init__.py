@@ -28,7 +28,7 @@ PATH_AUTO, PATH_GEMV, PATH_GEMM_DP4A, PATH_GEMM_TC, PATH_GEMV_DIRECT = 0, 1, 2, 
 EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspace_bytes", "qmm_quantize_q8_1",
            "qmm_mul_mat", "qmm_mul_mat_id", "qmm_read_device_status", "qmm_tile_efficiency_percent",
            "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode",
-           "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes")
+           "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32")
 
 
 class QMMError(RuntimeError):
@@ -89,6 +89,10 @@ def lib():
     L.qmm_mul_mat_id_noalloc.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P]
     L.qmm_noalloc_scratch_bytes.restype = SZ
     L.qmm_noalloc_scratch_bytes.argtypes = []
+    L.qmm_workspace_bytes_f32.restype = SZ
+    L.qmm_workspace_bytes_f32.argtypes = [ctypes.c_int, I64, I64, I64]
+    L.qmm_mul_mat_f32.restype = ctypes.c_int
+    L.qmm_mul_mat_f32.argtypes = [P, ctypes.c_int, I64, I64, P, I64, P, P, SZ, P]
     _lib = L
     return L
 
@@ -167,6 +171,28 @@ def qmm_mul_mat(W: torch.Tensor, qtype, n: int, k: int, xq: torch.Tensor, m: int
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().qmm_mul_mat(_ptr(W), _qtype(qtype), n, k, _ptr(xq), m, _ptr(y), _ptr(workspace), ws_bytes,
                              _stream(stream)), "qmm_mul_mat")
+    return y
+
+
+def qmm_workspace_bytes_f32(qtype, n: int, k: int, m: int) -> int:
+    return int(lib().qmm_workspace_bytes_f32(_qtype(qtype), n, k, m))
+
+
+def qmm_mul_mat_f32(W: torch.Tensor, qtype, n: int, k: int, x: torch.Tensor, m: int, y: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[m, n] fp32 = x * dequant(W)^T from fp32 activations x, quantized to q8_1 inside
+    the call (one launch for m == 1, which needs no workspace; a workspace is made here
+    for m > 1 when none is given)."""
+    _dev(W, "W")
+    _dev(x, "x", torch.float32)
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=W.device)
+    _dev(y, "y", torch.float32)
+    if workspace is None and m > 1:
+        workspace = torch.empty(qmm_workspace_bytes_f32(qtype, n, k, m), dtype=torch.uint8, device=W.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().qmm_mul_mat_f32(_ptr(W), _qtype(qtype), n, k, _ptr(x), m, _ptr(y), _ptr(workspace), ws_bytes,
+                                 _stream(stream)), "qmm_mul_mat_f32")
     return y
 
 

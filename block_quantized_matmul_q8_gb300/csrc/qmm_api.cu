@@ -81,6 +81,12 @@ static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
     return kGemmDp4a;
 }
 
+// Bytes at the head of the qmm_mul_mat_f32 workspace that hold the q8_1 activations.
+size_t q8_region_bytes(int64_t m, int64_t k) { return ((size_t(m) * size_t(k / 32) * kQ81Bytes) + 255) & ~size_t(255); }
+
+qmm_status mul_mat_q8(const void *W, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                      void *workspace, size_t ws_bytes, cudaStream_t st);
+
 qmm_status moe_check_sizes(qmm_type t, int64_t n_experts, int64_t n, int64_t k, int64_t top_k, int64_t n_tokens) {
     qmm_status s = check_k(t, k);
     if (s != QMM_OK) return s;
@@ -151,9 +157,47 @@ qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, const vo
     if (n == 0 || m == 0) return QMM_OK;
     if (!W || !xq || !y) return QMM_ERR_ARG;
     if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return QMM_ERR_ALIGN;
+    return mul_mat_q8(W, t, n, k, xq, m, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t qmm_workspace_bytes_f32(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    if (!type_ok(t) || n < 0 || k <= 0 || m < 0 || k % 32) return 0;
+    return q8_region_bytes(m, k) + qmm_workspace_bytes(t, n, k, m, 0, 0);
+}
+
+qmm_status qmm_mul_mat_f32(const void *W, qmm_type t, int64_t n, int64_t k, const float *x, int64_t m, float *y,
+                           void *workspace, size_t ws_bytes, void *stream) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n < 0 || m < 0) return QMM_ERR_ARG;
+    if (n > kMaxRows || m > kMaxRows) return QMM_ERR_SHAPE;
+    if (n == 0 || m == 0) return QMM_OK;
+    if (!W || !x || !y) return QMM_ERR_ARG;
+    if (!aligned16(W) || !aligned16(x) || !aligned16(y)) return QMM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // m == 1: one launch; every CTA quantizes the activation row into its shared memory
+    // while its first weight copies are in flight.  For m > 1 the redundant per-CTA
+    // quantization (m*k values on every CTA, its loads exposed before the first fold)
+    // costs more than the separate quantizer launch, so the q8_1 route below is taken.
+    const int path = choose_path(t, n, k, m);
+    if (path == kGemv && m == 1) return cuda_status(launch_gemv(t, W, n, k, nullptr, x, m, y, st));
+    // otherwise: the quantizer writes q8_1 into the head of the workspace, then the product
+    if (!workspace || ws_bytes < qmm_workspace_bytes_f32(t, n, k, m)) return QMM_ERR_WORKSPACE;
+    if (!aligned256(workspace)) return QMM_ERR_ALIGN;
+    const size_t off = q8_region_bytes(m, k);
+    uint8_t *xq = static_cast<uint8_t *>(workspace);
+    cudaError_t e = launch_quantize_q8_1(x, m, k, xq, st);
+    if (e != cudaSuccess) return QMM_ERR_CUDA;
+    return mul_mat_q8(W, t, n, k, xq, m, y, xq + off, ws_bytes - off, st);
+}
+
+}  // extern "C"
+
+namespace qmm {
+qmm_status mul_mat_q8(const void *W, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                      void *workspace, size_t ws_bytes, cudaStream_t st) {
     switch (choose_path(t, n, k, m)) {
-    case kGemv: return cuda_status(launch_gemv(t, W, n, k, xq, m, y, st));
+    case kGemv: return cuda_status(launch_gemv(t, W, n, k, xq, nullptr, m, y, st));
     case kGemmTc: {
         const size_t need = gemm_tc_workspace_bytes(t, n, k, m);
         if (need > 0) {
@@ -166,6 +210,9 @@ qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, const vo
     default: return cuda_status(launch_gemm_dp4a(t, W, n, k, xq, m, y, st));
     }
 }
+}  // namespace qmm
+
+extern "C" {
 
 qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
                           const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,

@@ -50,6 +50,35 @@ __device__ __forceinline__ uint4 ldg16(const void *p) {
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     return r;
 }
+// ---- q8_1 arithmetic, shared by every kernel that quantizes activations so that all
+// of them give the same bytes ([MMQ] section "引言"; [QMM] section "CPU: 先量化激活,
+// 再逐行点积"): d = amax/127 and q = round-half-away(v/d), both IEEE fp32 divisions;
+// stored d_h = fp16(d), s_h = fp16(float(d_h) * sum q); a block with d == 0 is all zero.
+__device__ __forceinline__ float q8_1_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+__device__ __forceinline__ int q8_1_code(float v, float d) { return d != 0.0f ? (int)roundf(__fdiv_rn(v, d)) : 0; }
+// The same code with the division replaced by a product with rd = 1/d (correctly
+// rounded) wherever that cannot change the integer.  With d normal and |v| <= 127.00001 d
+// (v in the block of amax = 127 d), the product t = v*rd is within 2^-16 of v/d
+// (two roundings of relative size 2^-24, |v/d| < 128) and the IEEE quotient within
+// 2^-17, so the two round to the same integer unless |t| lies within 2^-15 of a
+// half-integer; within 2^-14 of one, or when d is tiny or zero (rd == 0), the IEEE
+// quotient is computed after all.
+__device__ __forceinline__ float q8_1_recip(float d) { return d >= 0x1p-100f ? __frcp_rn(d) : 0.0f; }
+__device__ __forceinline__ int q8_1_code_fast(float v, float d, float rd) {
+    if (rd == 0.0f) return q8_1_code(v, d);
+    const float t = v * rd;
+    const float a = fabsf(t);
+    if (fabsf((a - truncf(a)) - 0.5f) < 0x1p-14f) return q8_1_code(v, d);
+    return (int)rintf(t);  // not within 2^-14 of a tie: the nearest integer either way
+}
+// The (d_h, s_h) word of a block: d_h in the low half, s_h in the high half.
+__device__ __forceinline__ uint32_t q8_1_ds_word(float d, int sum_q) {
+    if (d == 0.0f) return 0u;
+    const __half dh = __float2half_rn(d);
+    const __half sh = __float2half_rn(__half2float(dh) * (float)sum_q);
+    return uint32_t(__half_as_ushort(dh)) | (uint32_t(__half_as_ushort(sh)) << 16);
+}
+
 __device__ __forceinline__ uint32_t ldg4(const void *p) {
     uint32_t r;
     asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));

@@ -66,12 +66,87 @@ __device__ __forceinline__ void fold_unit(const Unit &w, const uint8_t *xs, cons
     }
 }
 
+// ---- activation staging.  A launch takes its NC activation columns either as q8_1
+// blocks (xq) or as fp32 values (xf, k per column), which it then quantizes itself with
+// the activation quantizer's arithmetic (the q8_1_* helpers), so that the staged bytes
+// are the same either way and the fp32 call needs no separate quantizer launch
+// ([MMQ] section "引言": activations are compressed to q8_1 on the device).
+struct XIn {
+    const uint8_t *xq;
+    const float *xf;  // non-null: quantize these instead of reading xq
+};
+
+template <int NC>
+__device__ __forceinline__ void stage_x(const XIn &x, int k, int U, uint8_t *xs, float2 *xds, int t, int nthreads) {
+    const int nb32 = k / 32;
+    const int total = NC * nb32;
+    if (x.xf == nullptr) {
+        for (int i = t; i < total; i += nthreads) {
+            const int c = i / nb32, b = i - c * nb32;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(x.xq + (size_t(c) * nb32 + b) * kQ81Bytes);
+            const uint32_t dsw = src[0];
+            uint32_t *dst =
+                reinterpret_cast<uint32_t *>(xs + (size_t(c) * U + (b >> 1)) * kUnitStride + 32 * (b & 1));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = src[1 + j];
+            xds[size_t(c) * 2 * U + b] = make_float2(half_lo(dsw), half_hi(dsw));
+        }
+        return;
+    }
+    // 8 lanes per 32-value block, 4 values (one 16-byte load) per lane: a warp
+    // quantizes 4 blocks per pass, and the loads of kBatch passes are issued before
+    // the first is used.  Max and integer sum are exact in any order, so the result
+    // is the quantizer kernel's to the bit.
+    constexpr int kBatch = 4;
+    const int lane = t & 31, w = t >> 5, nw = nthreads >> 5, g = lane >> 3, l8 = lane & 7;
+    const int ngroups = (total + 3) / 4;
+    for (int i0 = w; i0 < ngroups; i0 += nw * kBatch) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int blk = 4 * (i0 + j * nw) + g;
+            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (blk < total) {
+                const int c = blk / nb32, b = blk - c * nb32;
+                v[j] = reinterpret_cast<const float4 *>(x.xf + size_t(c) * k + 32 * b)[l8];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (i0 + j * nw >= ngroups) break;  // warp-uniform
+            const int blk = 4 * (i0 + j * nw) + g;
+            float amax = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            const float d = q8_1_scale(amax), rd = q8_1_recip(d);
+            const int q0 = q8_1_code_fast(v[j].x, d, rd), q1 = q8_1_code_fast(v[j].y, d, rd);
+            const int q2 = q8_1_code_fast(v[j].z, d, rd), q3 = q8_1_code_fast(v[j].w, d, rd);
+            int S = q0 + q1 + q2 + q3;
+            S += __shfl_xor_sync(0xffffffffu, S, 4);
+            S += __shfl_xor_sync(0xffffffffu, S, 2);
+            S += __shfl_xor_sync(0xffffffffu, S, 1);
+            if (blk < total) {
+                const int c = blk / nb32, b = blk - c * nb32;
+                const uint32_t packed = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) |
+                                        ((uint32_t(q2) & 0xffu) << 16) | ((uint32_t(q3) & 0xffu) << 24);
+                reinterpret_cast<uint32_t *>(xs + (size_t(c) * U + (b >> 1)) * kUnitStride + 32 * (b & 1))[l8] =
+                    packed;
+                if (l8 == 0) {
+                    const uint32_t dsw = q8_1_ds_word(d, S);
+                    xds[size_t(c) * 2 * U + b] = make_float2(half_lo(dsw), half_hi(dsw));
+                }
+            }
+        }
+    }
+}
+
 // Each lane keeps CH units' loads in flight: all loads of a chunk are issued before
 // the first of them is used.  The first chunk of a warp's first row pair is issued
 // before the activations are staged, so HBM traffic starts at kernel entry.
 template <int T, int NC>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const uint8_t *__restrict__ W, int64_t n, int k,
-                                                            int64_t row_bytes, const uint8_t *__restrict__ xq,
+                                                            int64_t row_bytes, const XIn x,
                                                             float *__restrict__ y, int64_t y_ld) {
     extern __shared__ __align__(16) uint8_t smem[];
     constexpr int CH = kRawChunk<T>;
@@ -98,16 +173,8 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const uint8_t *__res
     };
     if (warp < npairs) issue(warp, l16);
 
-    // ---- stage the q8_1 columns (the first weight loads are already in flight)
-    for (int i = threadIdx.x; i < NC * nb32; i += blockDim.x) {
-        const int c = i / nb32, b = i - c * nb32;
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (size_t(c) * nb32 + b) * kQ81Bytes);
-        const uint32_t dsw = src[0];
-        uint32_t *dst = reinterpret_cast<uint32_t *>(xs + (size_t(c) * U + (b >> 1)) * kUnitStride + 32 * (b & 1));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j] = src[1 + j];
-        xds[size_t(c) * 2 * U + b] = make_float2(half_lo(dsw), half_hi(dsw));
-    }
+    // ---- stage the activation columns (the first weight loads are already in flight)
+    stage_x<NC>(x, k, U, xs, xds, threadIdx.x, blockDim.x);
     // an odd block count leaves the second half of the last unit unset: zero it
     if (nb32 & 1) {
         for (int i = threadIdx.x; i < NC * 8; i += blockDim.x) {
@@ -208,9 +275,8 @@ __device__ __forceinline__ void q4k_pair_scales(uint32_t s0, uint32_t s1, uint32
 template <int NC>
 __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint8_t *__restrict__ W, int64_t n,
                                                                       int k, int64_t row_bytes, int nstages,
-                                                                      const uint8_t *__restrict__ xq,
-                                                                      float *__restrict__ y, int64_t y_ld,
-                                                                      int *status) {
+                                                                      const XIn x, float *__restrict__ y,
+                                                                      int64_t y_ld, int *status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full[kTmaMaxStages], empty[kTmaMaxStages];
@@ -266,16 +332,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
     } else {
         // ---------------- consumers: stage the activations, then fold the chunks
         ptx::grid_dependency_wait();
-        for (int i = tid; i < NC * nb32; i += kTmaConsumerWarps * 32) {
-            const int c = i / nb32, b = i - c * nb32;
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (size_t(c) * nb32 + b) * kQ81Bytes);
-            const uint32_t dsw = src[0];
-            uint32_t *dst =
-                reinterpret_cast<uint32_t *>(xs + (size_t(c) * U + (b >> 1)) * kUnitStride + 32 * (b & 1));
-#pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = src[1 + j];
-            xds[size_t(c) * 2 * U + b] = make_float2(half_lo(dsw), half_hi(dsw));
-        }
+        stage_x<NC>(x, k, U, xs, xds, tid, kTmaConsumerWarps * 32);
         asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumerWarps * 32) : "memory");
 
         const int grp = warp / kTmaGroupWarps, gw = warp % kTmaGroupWarps;
@@ -352,7 +409,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
 }
 
 template <int NC>
-static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, const void *xq, float *y, int64_t y_ld,
+static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x, float *y, int64_t y_ld,
                                       int nstages, cudaStream_t st) {
     const int64_t row_bytes = (k / 256) * kQ4KBytes;
     const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, NC);
@@ -361,12 +418,11 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, const
     if (e != cudaSuccess) return e;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(W), n,
-                      (int)k, row_bytes, nstages, static_cast<const uint8_t *>(xq), y, y_ld,
-                      static_cast<int *>(nullptr));
+                      (int)k, row_bytes, nstages, x, y, y_ld, static_cast<int *>(nullptr));
 }
 
 template <int T, int NC>
-static cudaError_t launch_gemv_nc(const void *W, int64_t n, int64_t k, const void *xq, float *y, int64_t y_ld,
+static cudaError_t launch_gemv_nc(const void *W, int64_t n, int64_t k, XIn x, float *y, int64_t y_ld,
                                   cudaStream_t st) {
     const size_t smem = gemv_smem_bytes(k, NC);
     auto kern = gemv_kernel<T, NC>;
@@ -382,15 +438,14 @@ static cudaError_t launch_gemv_nc(const void *W, int64_t n, int64_t k, const voi
     const int64_t need = (npairs + kGemvThreads / 32 - 1) / (kGemvThreads / 32);
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, int64_t(device_sm_count()) * per_sm));
     const int64_t row_bytes = int64_t(k / block_elems(T)) * block_bytes(T);
-    kern<<<(unsigned)grid, kGemvThreads, smem, st>>>(static_cast<const uint8_t *>(W), n, (int)k, row_bytes,
-                                                     static_cast<const uint8_t *>(xq), y, y_ld);
+    kern<<<(unsigned)grid, kGemvThreads, smem, st>>>(static_cast<const uint8_t *>(W), n, (int)k, row_bytes, x, y,
+                                                     y_ld);
     return cudaGetLastError();
 }
 
 template <int T>
-static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                                 cudaStream_t st) {
-    const uint8_t *x = static_cast<const uint8_t *>(xq);
+static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
+                                 float *y, cudaStream_t st) {
     const size_t xrow = size_t(k / 32) * kQ81Bytes;
     const size_t budget = size_t(device_smem_optin());
     int64_t c0 = 0;
@@ -399,7 +454,9 @@ static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void
         while (nc > 1 && gemv_smem_bytes(k, nc) > budget) --nc;
         if (gemv_smem_bytes(k, nc) > budget) return cudaErrorInvalidValue;
         cudaError_t e;
-        const void *xc = x + c0 * xrow;
+        XIn xc;
+        xc.xq = xf ? nullptr : static_cast<const uint8_t *>(xq) + c0 * xrow;
+        xc.xf = xf ? xf + c0 * k : nullptr;
         float *yc = y + c0 * n;
         const int nst = T == QMM_Q4_K ? gemv_tma_stages(k, nc, budget) : 0;
         if (nst > 0 && gemv_tma_enabled()) {
@@ -433,12 +490,12 @@ static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void
     return cudaSuccess;
 }
 
-cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                        cudaStream_t st) {
+cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
+                        float *y, cudaStream_t st) {
     switch (t) {
-    case QMM_Q4_K: return launch_gemv_t<QMM_Q4_K>(W, n, k, xq, m, y, st);
-    case QMM_Q6_K: return launch_gemv_t<QMM_Q6_K>(W, n, k, xq, m, y, st);
-    case QMM_Q8_0: return launch_gemv_t<QMM_Q8_0>(W, n, k, xq, m, y, st);
+    case QMM_Q4_K: return launch_gemv_t<QMM_Q4_K>(W, n, k, xq, xf, m, y, st);
+    case QMM_Q6_K: return launch_gemv_t<QMM_Q6_K>(W, n, k, xq, xf, m, y, st);
+    case QMM_Q8_0: return launch_gemv_t<QMM_Q8_0>(W, n, k, xq, xf, m, y, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -41,11 +41,12 @@ cudaError_t launch_quantize_q8_1(const float *x, int64_t m, int64_t k, void *xq,
 // False when the test switch asks for the direct-load GEMV only.
 bool gemv_tma_enabled();
 
-// GEMV, m <= 8: y[m][n] from W rows and q8_1 activations.  Columns beyond the shared
-// memory budget are processed in several launches by the caller.
+// GEMV, m <= 8: y[m][n] from W rows and the activations, given either as q8_1 blocks
+// (xq) or as fp32 values (xf != nullptr), which each CTA then quantizes itself to the
+// same bytes as launch_quantize_q8_1.  Columns are taken in groups of up to 8 per launch.
 size_t gemv_smem_bytes(int64_t k, int ncols);
-cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                        cudaStream_t st);
+cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
+                        float *y, cudaStream_t st);
 
 // CUDA-core tiled GEMM (dp4a), any m.
 cudaError_t launch_gemm_dp4a(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,

@@ -7,7 +7,8 @@
 //   d    = amax / 127         (IEEE fp32 division, __fdiv_rn)
 //   q    = roundf(x / d)      (IEEE fp32 division, halves away from zero)
 //   d_h  = fp16_rne(d),  s_h = fp16_rne(float(d_h) * sum(q))   (the product is exact)
-// A block whose fp32 d is 0 is stored as all zero.  Bit-identical to the definition.
+// A block whose fp32 d is 0 is stored as all zero.  Bit-identical to the definition;
+// the arithmetic is the q8_1_* helpers, which the fused GEMV staging uses as well.
 #include <cuda_runtime.h>
 
 #include "qmm_common.cuh"
@@ -32,21 +33,12 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restr
         float amax = fabsf(v);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float d = __fdiv_rn(amax, 127.0f);
-        int q = 0;
-        if (d != 0.0f) q = (int)roundf(__fdiv_rn(v, d));
+        const float d = q8_1_scale(amax);
+        const int q = q8_1_code_fast(v, d, q8_1_recip(d));
         const int S = __reduce_add_sync(0xffffffffu, q);
         uint8_t *ob = xq + blk * kQ81Bytes;
         ob[4 + lane] = (uint8_t)(int8_t)q;
-        if (lane == 0) {
-            __half dh = __float2half_rn(d);
-            __half sh = __float2half_rn(__half2float(dh) * (float)S);
-            if (d == 0.0f) {
-                dh = __ushort_as_half(0);
-                sh = __ushort_as_half(0);
-            }
-            *reinterpret_cast<__half2 *>(ob) = __halves2half2(dh, sh);
-        }
+        if (lane == 0) *reinterpret_cast<uint32_t *>(ob) = q8_1_ds_word(d, S);
     }
 }
 

@@ -112,6 +112,26 @@ QMM_API qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, 
                        void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * The same product from fp32 activations: the call quantizes x to q8_1 itself
+ * (qmm_quantize_q8_1's arithmetic, to the bit) and then multiplies, so that
+ *   qmm_mul_mat_f32(W, t, n, k, x, m, y, ...)
+ * gives exactly the y of qmm_quantize_q8_1(x) followed by qmm_mul_mat ([MMQ]
+ * section "引言": the activations stay fp32 and are quantized on the device).
+ *   x  : fp32 [m][k], 16-byte aligned, k % 32 == 0 (and the format's block size).
+ *   W, y, stream: as qmm_mul_mat.
+ *   workspace: at least qmm_workspace_bytes_f32(t, n, k, m) bytes, 256-byte aligned.
+ *              When m == 1 and the GEMV runs, the workspace is not used (may be NULL):
+ *              that case is ONE launch in which every CTA quantizes x into its shared
+ *              memory while its first weight copies are in flight.  Otherwise the
+ *              q8_1 blocks go to the head of the workspace (the quantizer kernel writes
+ *              them) and the rest is the qmm_mul_mat workspace.
+ * Errors as qmm_mul_mat (QMM_ERR_WORKSPACE when the workspace is needed and short).
+ */
+QMM_API size_t qmm_workspace_bytes_f32(qmm_type t, int64_t n, int64_t k, int64_t m);
+QMM_API qmm_status qmm_mul_mat_f32(const void *W, qmm_type t, int64_t n, int64_t k, const float *x, int64_t m,
+                                   float *y, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Expert-routed matmul ([MMQ] sections "派发路径", "专家边界: 在 GPU 上做分段,
  * 而不是在 host 上", "MoE 的二次账"):
  *   y[t][s][:] = x[t] * dequant(W_experts[ids[t][s]])^T

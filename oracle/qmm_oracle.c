@@ -14,7 +14,7 @@
  *   [P0007] "Patch 0007: an fp16 matrix-vector path for GP100" (p100-llama-cpp, docs/fp16-mmvq.md)
  *   [QMM]   "QTensor 与 QMatMul" (candle 0.11.0 notes, rustineverything.app)
  *
- * Readings taken where the pages are silent or garbled (each also listed in the design doc):
+ * Readings taken where the pages are silent or garbled:
  *   - q8_1 block = {fp16 d, fp16 s, int8 q[32]} (36 B); d = amax/127 in fp32,
  *     q = roundf(x/d) with IEEE fp32 division (ties away from zero),
  *     stored d_h = fp16_rne(d), s_h = fp16_rne(d_h * sum(q)); if the fp32 d is 0

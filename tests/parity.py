@@ -41,3 +41,28 @@ def adversarial_x_rows():
         r[pos] = 9.0
         rows.append(r)
     return np.stack(rows)
+
+
+def near_tie_rows(seed, nblocks, exp_range=(-20, 20)):
+    """Blocks whose values sit within a few ulps of (q + 1/2) * d, d = amax/127 in fp32:
+    the quotients x/d land on or next to the rounding ties, where a quantizer that does
+    not divide exactly in IEEE fp32 would pick another integer.  amax is uniform in
+    [1e-3, 1e3] times 2^e, e drawn from exp_range."""
+    rng = np.random.default_rng(seed)
+    out = np.empty((nblocks, 32), np.float32)
+    for b in range(nblocks):
+        amax = np.float32(rng.uniform(1e-3, 1e3)) * np.float32(2.0) ** int(rng.integers(*exp_range))
+        d = np.float32(amax / np.float32(127))
+        q = rng.integers(-127, 127, 32).astype(np.float32)
+        v = ((q + np.float32(0.5)) * d).astype(np.float32)
+        steps = rng.integers(-6, 7, 32)
+        for i in range(32):
+            s = int(steps[i])
+            while s > 0:
+                v[i] = np.nextafter(v[i], np.float32(np.inf)); s -= 1
+            while s < 0:
+                v[i] = np.nextafter(v[i], np.float32(-np.inf)); s += 1
+        v = np.clip(v, -amax, amax)
+        v[rng.integers(0, 32)] = amax if rng.random() < 0.5 else -amax
+        out[b] = v
+    return out

@@ -78,6 +78,27 @@ def test_argument_errors_need_no_gpu(L):
     assert L.qmm_mul_mat_id(*many, P(1 << 20), 1 << 40, None) == 2
 
 
+def test_f32_call_argument_errors_need_no_gpu(L):
+    P = ctypes.c_void_p
+
+    def mm(W=1024, t=12, n=8, k=256, x=2048, m=4, y=4096, ws=None, wsb=0):
+        return L.qmm_mul_mat_f32(P(W), t, n, k, P(x), m, P(y), P(ws) if ws else None, wsb, None)
+
+    assert mm(t=13) == 3
+    assert mm(k=100) == 2
+    assert mm(t=8, k=48) == 2
+    assert mm(x=0) == 1
+    assert mm(x=2052) == 4                        # fp32 activations need 16-byte alignment
+    assert mm(n=0) == 0 and mm(m=0) == 0
+    # m > 8 needs the workspace (q8_1 head + GEMM scratch)
+    need = L.qmm_workspace_bytes_f32(12, 8, 256, 20)
+    assert need == ((20 * 8 * 36 + 255) // 256) * 256 + L.qmm_workspace_bytes(12, 8, 256, 20, 0, 0)
+    assert mm(m=20) == 5
+    assert mm(m=20, ws=1 << 20, wsb=need - 1) == 5
+    assert mm(m=20, ws=(1 << 20) + 16, wsb=need) == 4
+    assert L.qmm_workspace_bytes_f32(12, 8, 100, 20) == 0
+
+
 def test_tile_efficiency_matches_page_examples():
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "schedule_examples.json")))
     for c in g["tile_efficiency"]["cases"]:

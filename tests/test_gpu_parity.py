@@ -7,7 +7,7 @@ import torch
 
 import block_quantized_matmul_q8_gb300 as qmm
 import qmm_synth
-from parity import TOL, adversarial_x_rows, assert_within
+from parity import TOL, adversarial_x_rows, assert_within, near_tie_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +65,13 @@ def test_quantize_tie_and_scale_edges(oracle_mod):
         x[rng.integers(0, 32)] = amax
         rows.append(x)
     x = np.stack(rows).reshape(2, -1)
+    got = qmm.qmm_quantize_q8_1(to_dev(x)).cpu().numpy()
+    assert np.array_equal(got, oracle_mod.quantize_q8_1(x))
+
+
+def test_quantize_near_ties_bitexact(oracle_mod):
+    """Quotients within a few ulps of the rounding ties, over scales from 2^-20 to 2^20."""
+    x = near_tie_rows(21, 4096).reshape(8, -1)
     got = qmm.qmm_quantize_q8_1(to_dev(x)).cpu().numpy()
     assert np.array_equal(got, oracle_mod.quantize_q8_1(x))
 
