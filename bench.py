@@ -89,26 +89,32 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_source_sha():
+# the sources each profiled kernel is built from (its own file and the headers it includes)
+_HEADERS = ["qmm_common.cuh", "qmm_tc_ptx.cuh", "qmm_internal.h", "qmm_moe.h", "../../include/qmm.h"]
+KERNEL_SOURCES = {"gemv_q4k_tma_kernel<1>": ["qmm_gemv.cu"] + _HEADERS,
+                  "gemm_tc_q4k_kernel": ["qmm_gemm_tc.cu"] + _HEADERS}
+
+
+def kernel_source_sha(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_matmul_q8_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(os.path.basename(name).encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    """DRAM bytes per launch from a committed ncu summary, if taken on the kernel's
+    current sources (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != kernel_source_sha(kernel):
         return None
     return e.get("bytes_per_launch")
 
@@ -279,12 +285,16 @@ def time_graphs(torch, fn, steps, warmup, barrier):
     return e0.elapsed_time(e1)
 
 
-def secondary(torch, qmm, dev, stream, steps, hbm_peak):
+def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
     """Every other workload of the pages, device-timed by graph replay: GEMV rows in
-    GB/s (and fraction of the HBM peak), GEMM and MoE rows in TOPS (2*m*n*k)."""
+    GB/s (and fraction of the HBM peak), GEMM and MoE rows in TOPS (2*m*n*k).  `only`
+    keeps the rows whose name contains it."""
     out = {}
 
     def dense(fmt, n, k, ms, q8_input=False):
+        ms = [m for m in ms if only in f"{fmt}_n{n}_k{k}_m{m}" + ("_q8_1_input" if q8_input else "")]
+        if not ms:
+            return {}
         """Whole path from fp32 x (qmm_mul_mat_f32); q8_input times qmm_mul_mat on
         pre-quantized activations instead."""
         rows = {}
@@ -325,6 +335,8 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak):
     out.update(dense("q6_K", 151936, 5120, [1, 512]))
     out.update(dense("q8_0", 5120, 5120, [1, 512]))
     # MoE: 128 experts x Q4_K n=1536 k=4096, 512 tokens top-8 Zipf(1.1)
+    if only not in "moe_q4K_e128_n1536_k4096_t512_top8":
+        return out
     E, n, k, T_, Kt = 128, 1536, 4096, 512, 8
     W, x, ids = qmm_synth.make_moe(E, n, k, T_, Kt, seed=0)
     Wd = torch.from_numpy(W).to(dev)
@@ -347,6 +359,7 @@ def main():
     ap.add_argument("--impl", default="qmm", choices=["qmm", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--rows", default="", help="only the secondary rows whose name contains this text")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -412,7 +425,7 @@ def main():
 
     sec = None
     if rank == 0 and not args.no_secondary:
-        sec = secondary(torch, qmm, dev, stream, steps=10, hbm_peak=measured_peaks()[0])
+        sec = secondary(torch, qmm, dev, stream, steps=10, hbm_peak=measured_peaks()[0], only=args.rows)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_baseline(W, x, N, K, M, row_bytes)

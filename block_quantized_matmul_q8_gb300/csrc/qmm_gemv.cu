@@ -254,24 +254,43 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
                  : "memory");
 }
 
-// Q4_K scales and mins of sub-blocks 2c and 2c+1 without a branch on c (c = 0..3):
-// for c < 2 they are the low 6 bits of bytes 2c, 2c+1 of s0 (scales) and s1 (mins);
-// for c >= 2 the low/high nibbles of bytes 2c-4, 2c-3 of s2 plus the top 2 bits of the
-// same bytes of s0 / s1.
-__device__ __forceinline__ void q4k_pair_scales(uint32_t s0, uint32_t s1, uint32_t s2, int c, int &sc0, int &sc1,
-                                                int &m0, int &m1) {
-    const int sh = 16 * (c & 1);
-    const uint32_t a0 = (s0 >> sh) & 0xffffu, a1 = (s1 >> sh) & 0xffffu, a2 = (s2 >> sh) & 0xffffu;
-    const uint32_t lo_sc = a0 & 0x3f3fu, lo_m = a1 & 0x3f3fu;
-    const uint32_t hi_sc = (a2 & 0x0f0fu) | ((a0 >> 2) & 0x3030u);
-    const uint32_t hi_m = ((a2 >> 4) & 0x0f0fu) | ((a1 >> 2) & 0x3030u);
-    const uint32_t scp = c < 2 ? lo_sc : hi_sc, mp = c < 2 ? lo_m : hi_m;
-    sc0 = scp & 0xff;
-    sc1 = scp >> 8;
-    m0 = mp & 0xff;
-    m1 = mp >> 8;
+// Q4_K scales and mins of sub-blocks 2c and 2c+1 (c = 0..3) from the 12 packed bytes
+// q[0..11] = s0 | s1 | s2 (GGUF 6-bit rule: for j < 4, sc = q[j] & 63, m = q[j+4] & 63;
+// for j >= 4, sc = (q[j+4] & 15) | (q[j-4] >> 6) << 4, m = (q[j+4] >> 4) | (q[j] >> 6) << 4).
+// A lane always takes the same c, so one byte permutation per word with a per-lane
+// selector gathers the bytes of both sub-blocks, and per-lane masks finish the job:
+//   sc pair = (P(s0, s2) & m1) | ((P(s0, s2) >> 18) & m2)
+//   m  pair = ((P(s1, s2) >> sh) & m1) | ((P(s1, s2) >> 18) & m2)
+// (low byte: sub-block 2c, high byte: 2c+1).
+struct Q4KPairSel {
+    uint32_t sel, m1, m2, sh;
+};
+__device__ __forceinline__ Q4KPairSel q4k_pair_sel(int c) {
+    const uint32_t b = 2u * (c & 1);
+    Q4KPairSel p;
+    p.sel = c < 2 ? (b | (b + 1) << 4) : ((4 + b) | (5 + b) << 4 | b << 8 | (b + 1) << 12);
+    p.m1 = c < 2 ? 0x3f3fu : 0x0f0fu;
+    p.m2 = c < 2 ? 0u : 0x3030u;
+    p.sh = c < 2 ? 0u : 4u;
+    return p;
+}
+__device__ __forceinline__ void q4k_pair_scales(uint32_t s0, uint32_t s1, uint32_t s2, const Q4KPairSel &p, int &sc0,
+                                                int &sc1, int &m0, int &m1) {
+    const uint32_t a = __byte_perm(s0, s2, p.sel), q = __byte_perm(s1, s2, p.sel);
+    const uint32_t sc = (a & p.m1) | ((a >> 18) & p.m2);
+    const uint32_t mn = ((q >> p.sh) & p.m1) | ((q >> 18) & p.m2);
+    sc0 = sc & 0xff;
+    sc1 = sc >> 8;
+    m0 = mn & 0xff;
+    m1 = mn >> 8;
 }
 
+// dp4a of unsigned bytes (a) with signed bytes (b).
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 template <int NC>
 __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint8_t *__restrict__ W, int64_t n,
                                                                       int k, int64_t row_bytes, int nstages,
@@ -338,6 +357,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
         const int grp = warp / kTmaGroupWarps, gw = warp % kTmaGroupWarps;
         const int rr = 2 * gw + (lane >> 4);  // row within a chunk
         const int c4 = l16 & 3;               // qs chunk of every unit this lane takes
+        const Q4KPairSel psel = q4k_pair_sel(c4);
         for (int c = grp; c < nchunks; c += kTmaGroups) {
             const int s = c % nstages;
             if (!ptx::mbar_wait(ptx::smem_u32(&full[s]), (c / nstages) & 1, abortp)) break;
@@ -355,7 +375,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
                     const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c4);
                     const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
                     int sc0, sc1, m0, m1;
-                    q4k_pair_scales(hd.y, hd.z, hd.w, c4, sc0, sc1, m0, m1);
+                    q4k_pair_scales(hd.y, hd.z, hd.w, psel, sc0, sc1, m0, m1);
                     const float d = half_lo(hd.x), dmin = half_hi(hd.x);
 #pragma unroll
                     for (int cc = 0; cc < NC; ++cc) {
@@ -370,14 +390,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
                         slo = __dp4a((int)(w[5] & 0x0f0f0f0fu), x1.y, slo);
                         slo = __dp4a((int)(w[6] & 0x0f0f0f0fu), x1.z, slo);
                         slo = __dp4a((int)(w[7] & 0x0f0f0f0fu), x1.w, slo);
-                        int shi = __dp4a((int)((w[0] >> 4) & 0x0f0f0f0fu), x2.x, 0);
-                        shi = __dp4a((int)((w[1] >> 4) & 0x0f0f0f0fu), x2.y, shi);
-                        shi = __dp4a((int)((w[2] >> 4) & 0x0f0f0f0fu), x2.z, shi);
-                        shi = __dp4a((int)((w[3] >> 4) & 0x0f0f0f0fu), x2.w, shi);
-                        shi = __dp4a((int)((w[4] >> 4) & 0x0f0f0f0fu), x3.x, shi);
-                        shi = __dp4a((int)((w[5] >> 4) & 0x0f0f0f0fu), x3.y, shi);
-                        shi = __dp4a((int)((w[6] >> 4) & 0x0f0f0f0fu), x3.z, shi);
-                        shi = __dp4a((int)((w[7] >> 4) & 0x0f0f0f0fu), x3.w, shi);
+                        // high nibbles in place: bytes & 0xF0 are 16 q, so the dot is 16 times
+                        // the wanted one and the shift divides it exactly
+                        int shi = dp4a_us(w[0] & 0xf0f0f0f0u, x2.x, 0);
+                        shi = dp4a_us(w[1] & 0xf0f0f0f0u, x2.y, shi);
+                        shi = dp4a_us(w[2] & 0xf0f0f0f0u, x2.z, shi);
+                        shi = dp4a_us(w[3] & 0xf0f0f0f0u, x2.w, shi);
+                        shi = dp4a_us(w[4] & 0xf0f0f0f0u, x3.x, shi);
+                        shi = dp4a_us(w[5] & 0xf0f0f0f0u, x3.y, shi);
+                        shi = dp4a_us(w[6] & 0xf0f0f0f0u, x3.z, shi);
+                        shi = dp4a_us(w[7] & 0xf0f0f0f0u, x3.w, shi);
+                        shi >>= 4;
                         // exact int32 sub-block dots times the 6-bit scales, folded in fp32
                         float t = ds.x * (float)(sc0 * slo);
                         t = fmaf(ds.z, (float)(sc1 * shi), t);
@@ -396,12 +419,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 acc[cc] = v;
             }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));  // the stage is read: free it first
             if (valid && l16 == 0) {
 #pragma unroll
                 for (int cc = 0; cc < NC; ++cc) y[cc * y_ld + a + rr] = acc[cc];
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));
         }
     }
     __syncthreads();
