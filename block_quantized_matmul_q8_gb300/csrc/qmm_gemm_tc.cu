@@ -26,9 +26,10 @@
 //               K-major layout the MMA reads, the 6-bit mins -> fp16 for the min-term
 //               MMA, (d, -dmin) for the epilogue.
 //   warps 8-23  epilogue: one activation row (TMEM lane) and 32 weight columns per
-//               thread; per sub-block acc += d8 * slot (fp32 FMA), per superblock
-//               total += d * acc - dmin * minslot, the total kept in TMEM columns
-//               384..511.
+//               thread; per sub-block acc += d8 * slot (fp32 FMA, two columns per
+//               packed fma.rn.f32x2, the slot read in two 16-column halves), per
+//               superblock total += d * acc - dmin * minslot, the total kept in TMEM
+//               columns 384..511.
 // Work is a flattened stream of (tile, superblock) units split over the CTAs
 // ([MMQ] section "stream-K 的切法"); a tile shared by several CTAs is summed by a
 // separate fixup kernel in CTA order ([MMQ] section "fixup: 部分和的归约"), so no
@@ -54,6 +55,9 @@ constexpr int kTM = 128;  // activation rows per tile
 constexpr int kTN = 128;  // weight rows per tile
 constexpr int kStages = 2;
 constexpr int kSlots = 3;          // accumulator slots of 128 TMEM columns; columns 384..511 hold the running total
+// 9 slot uses per superblock (8 sub-blocks + the min term): the epilogue relies on each
+// superblock starting at slot 0
+static_assert(9 % kSlots == 0, "slot ring must divide the 9 slot uses of a superblock");
 constexpr uint32_t kTotCol = 384;
 constexpr int kThreads = 768;      // 24 warps = 6 warpgroups
 constexpr int kUnpackWarp0 = 4;
@@ -470,36 +474,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const float *dxs = reinterpret_cast<const float *>(smem + kOffDX + sdi * 4096 + tl * 32);
+                // the row's 8 d8 values, two 16-byte reads (scalar reads at the 32-byte row
+                // stride would put 8 lanes on each bank)
+                const float4 *dxv = reinterpret_cast<const float4 *>(smem + kOffDX + sdi * 4096 + tl * 32);
+                const float4 dxa = dxv[0], dxb = dxv[1];
+                const float dxs[8] = {dxa.x, dxa.y, dxa.z, dxa.w, dxb.x, dxb.y, dxb.z, dxb.w};
                 const float4 *ddd = reinterpret_cast<const float4 *>(smem + kOffDD + sdi * 1024) + 8 * cq;
                 const float4 *ddm = reinterpret_cast<const float4 *>(smem + kOffDD + sdi * 1024 + 512) + 8 * cq;
-                float acc[32];
-                for (int G = 0; G < 8 && ok; ++G) {
-                    const uint32_t slot = (g + G) % kSlots;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), ((g + G) / kSlots) & 1, abortp)) {
+                // g is a multiple of 9 here (9 slot uses per superblock, kSlots = 3), so
+                // sub-block G always uses slot G % 3, with parity ph ^ (G / 3 & 1)
+                const uint32_t ph = (g / kSlots) & 1;
+                float2 acc[16];  // columns 2i, 2i+1 of this thread's 32
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int G = 0; G < 8; ++G) {
+                    const uint32_t slot = G % kSlots;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), ph ^ ((G / kSlots) & 1), abortp)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    float v[32];
-                    ptx::tmem_ld_32x32b_x32(lane_base + slot * kTN + 32 * cq, v);
-                    ptx::tmem_ld_wait();
+                    const float2 dg = make_float2(dxs[G], dxs[G]);
+#pragma unroll
+                    for (int hv = 0; hv < 2; ++hv) {  // two 16-column halves: 16 registers live, not 32
+                        float v[16];
+                        ptx::tmem_ld_32x32b_x16(lane_base + slot * kTN + 32 * cq + 16 * hv, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            acc[8 * hv + i] = __ffma2_rn(dg, make_float2(v[2 * i], v[2 * i + 1]), acc[8 * hv + i]);
+                    }
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[slot]));
-                    const float dg = dxs[G];
-                    if (G == 0) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[i] = dg * v[i];
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[i] = fmaf(dg, v[i], acc[i]);
-                    }
                 }
                 if (!ok) break;
                 // min slot and running total
-                const uint32_t slot = (g + 8) % kSlots;
-                if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), ((g + 8) / kSlots) & 1, abortp)) {
+                const uint32_t slot = 8 % kSlots;
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), ph ^ ((8 / kSlots) & 1), abortp)) {
                     ok = false;
                     break;
                 }
@@ -513,15 +526,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tmem_ld_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
                     }
                     ptx::tmem_ld_wait();
+                    // t = m * vm + (d * acc + t), two columns per packed fma
 #pragma unroll
                     for (int i4 = 0; i4 < 4; ++i4) {
                         const float4 d4 = ddd[4 * hh + i4], m4 = ddm[4 * hh + i4];
-                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
+                        for (int e = 0; e < 4; e += 2) {
                             const int i = 4 * i4 + e;
-                            const float base = first ? 0.f : t[i];
-                            t[i] = fmaf(mv[e], vm[i], fmaf(dv[e], acc[16 * hh + i], base));
+                            const float2 dv = e == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
+                            const float2 mv = e == 0 ? make_float2(m4.x, m4.y) : make_float2(m4.z, m4.w);
+                            const float2 base = first ? make_float2(0.f, 0.f) : make_float2(t[i], t[i + 1]);
+                            const float2 r = __ffma2_rn(mv, make_float2(vm[i], vm[i + 1]),
+                                                        __ffma2_rn(dv, acc[8 * hh + i / 2], base));
+                            t[i] = r.x;
+                            t[i + 1] = r.y;
                         }
                     }
                     ptx::tmem_st_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
