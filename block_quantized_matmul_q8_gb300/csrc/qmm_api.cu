@@ -66,7 +66,7 @@ static qmm_status check_k(qmm_type t, int64_t k) {
 static qmm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
 // Which kernel family qmm_mul_mat uses for these sizes.
-enum Path { kGemv = 1, kGemmDp4a = 2, kGemmTc = 3, kGemvDirect = 4 };
+enum Path { kGemv = 1, kGemmDp4a = 2, kGemmTc = 3, kGemvDirect = 4, kGemvTc = 5 };
 
 bool gemv_tma_enabled() { return g_force_path.load(std::memory_order_relaxed) != kGemvDirect; }
 
@@ -76,7 +76,10 @@ static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
     if ((force == kGemv || force == kGemvDirect) && gemv_fits && m <= 64) return kGemv;
     if (force == kGemmDp4a) return kGemmDp4a;
     if (force == kGemmTc && gemm_tc_supported(t, n, k, m)) return kGemmTc;
+    if (force == kGemvTc && gemv_tc_supported(t, n, k, m)) return kGemvTc;
     if (m <= 8 && gemv_fits) return kGemv;
+    // skinny activations on the tensor cores (weights as the MMA's M side)
+    if (gemv_tc_supported(t, n, k, m)) return kGemvTc;
     if (gemm_tc_supported(t, n, k, m)) return kGemmTc;
     return kGemmDp4a;
 }
@@ -136,7 +139,9 @@ size_t qmm_row_bytes(qmm_type t, int64_t k) {
 size_t qmm_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t n_experts, int64_t top_k) {
     if (!type_ok(t) || n < 0 || k <= 0 || m < 0) return 0;
     if (n_experts > 0) return moe_workspace_bytes(t, n, k, m, n_experts, top_k);
-    return gemm_tc_supported(t, n, k, m) ? gemm_tc_workspace_bytes(t, n, k, m) : 0;
+    // enough for every path the call may take (the forced ones included)
+    const size_t gemm = gemm_tc_supported(t, n, k, m) ? gemm_tc_workspace_bytes(t, n, k, m) : 0;
+    return std::max(gemm, gemv_tc_workspace_bytes(t, n, k, m));
 }
 
 qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void *xq, void *stream) {
@@ -198,6 +203,12 @@ qmm_status mul_mat_q8(const void *W, qmm_type t, int64_t n, int64_t k, const voi
                       void *workspace, size_t ws_bytes, cudaStream_t st) {
     switch (choose_path(t, n, k, m)) {
     case kGemv: return cuda_status(launch_gemv(t, W, n, k, xq, nullptr, m, y, st));
+    case kGemvTc: {
+        const size_t need = gemv_tc_workspace_bytes(t, n, k, m);
+        if (!workspace || ws_bytes < need) return QMM_ERR_WORKSPACE;
+        if (!aligned256(workspace)) return QMM_ERR_ALIGN;
+        return cuda_status(launch_gemv_tc(t, W, n, k, xq, m, y, workspace, ws_bytes, st));
+    }
     case kGemmTc: {
         const size_t need = gemm_tc_workspace_bytes(t, n, k, m);
         if (need > 0) {

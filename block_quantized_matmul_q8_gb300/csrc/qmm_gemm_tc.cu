@@ -45,6 +45,7 @@
 #include "qmm_common.cuh"
 #include "qmm_internal.h"
 #include "qmm_moe.h"
+#include "qmm_tc_common.cuh"
 #include "qmm_tc_ptx.cuh"
 
 namespace qmm {
@@ -164,28 +165,6 @@ __device__ __forceinline__ bool next_seg(const TcArgs &a, int64_t &u, int64_t en
     return true;
 }
 
-__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-
-template <int N> __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
-template <int N> __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
-
-// 8 nibbles (low or high half of bytes w0, w1) -> 8 fp16 values q*sc, exact.
-// (0x6400 | q) is the fp16 value 1024 + q; fma((1024+q), sc, -1024*sc) = q*sc exactly.
-__device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w0, uint32_t w1, int shift, __half2 sc2, __half2 nsc2) {
-    uint32_t p[4];
-    const uint32_t a0 = __byte_perm(w0, 0, 0x4140), a1 = __byte_perm(w0, 0, 0x4342);
-    const uint32_t b0 = __byte_perm(w1, 0, 0x4140), b1 = __byte_perm(w1, 0, 0x4342);
-    p[0] = ((a0 >> shift) & 0x000F000Fu) | 0x64006400u;
-    p[1] = ((a1 >> shift) & 0x000F000Fu) | 0x64006400u;
-    p[2] = ((b0 >> shift) & 0x000F000Fu) | 0x64006400u;
-    p[3] = ((b1 >> shift) & 0x000F000Fu) | 0x64006400u;
-    uint4 r;
-    r.x = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[0]), sc2, nsc2));
-    r.y = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[1]), sc2, nsc2));
-    r.z = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[2]), sc2, nsc2));
-    r.w = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[3]), sc2, nsc2));
-    return r;
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
@@ -711,30 +690,9 @@ __global__ void __launch_bounds__(256) tc_fixup_kernel(TcArgs a) {
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner, uint64_t outer,
                  uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-    auto enc = get_encode();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * esize};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t es[2] = {1, 1};
-    return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tc_make_map_2d(map, dt, esize, base, inner, outer, inner * esize, box_inner, box_outer, sw);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -907,6 +865,31 @@ cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     args.bounds = bounds;
     args.perm = perm;
     return run_tc(tm_x, tm_xmin, tm_dx, tm_w, args, ctas, max_token_tiles * args.tiles_n, st);
+}
+
+// ---------------------------------------------------------------- shared with the skinny path
+
+bool tc_make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner,
+                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle sw) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn) return false;
+    (void)esize;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace qmm

@@ -48,6 +48,13 @@ size_t gemv_smem_bytes(int64_t k, int ncols);
 cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
                         float *y, cudaStream_t st);
 
+// Tensor-core path for skinny activations (Q4_K, 1 <= m <= 16): weights as the MMA's
+// 128-row M side, activations as N = 16; stream-K over (row tile, superblock) units.
+bool gemv_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
+size_t gemv_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m);
+cudaError_t launch_gemv_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                           void *ws, size_t ws_bytes, cudaStream_t st);
+
 // CUDA-core tiled GEMM (dp4a), any m.
 cudaError_t launch_gemm_dp4a(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
                              cudaStream_t st);

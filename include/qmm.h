@@ -103,9 +103,13 @@ QMM_API qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void 
  *   xq     : q8_1 blocks of x [m][k] as written by qmm_quantize_q8_1.
  *   y      : fp32 [m][n] output, 16-byte aligned; every element is written.
  *   workspace, ws_bytes: at least qmm_workspace_bytes(t, n, k, m, 0, 0) bytes.
- * k % 256 == 0 for Q4_K/Q6_K, k % 32 == 0 for Q8_0.  m <= 8 runs the GEMV path
- * (each weight byte read once, every column reusing the decoded weight);
- * larger m runs the tiled tensor-core GEMM with a stream-K schedule.
+ * k % 256 == 0 for Q4_K/Q6_K, k % 32 == 0 for Q8_0.  Paths (each weight byte is read
+ * once, every column reusing the decoded weight):
+ *   Q4_K, m <= 8:       the bulk-copy GEMV (dp4a);
+ *   Q4_K, 9 <= m <= 16: the skinny tensor-core path (weight rows as the MMA's M side);
+ *   Q4_K, m > 16:       the tiled tensor-core GEMM;
+ *   Q6_K/Q8_0:          the GEMV for m <= 8, else the CUDA-core tiled GEMM;
+ * the tensor-core paths split their work with a stream-K schedule.
  * Accuracy: |y - y_exact| <= 1e-5 * sum over blocks of |block term| per element.
  */
 QMM_API qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
@@ -226,7 +230,9 @@ QMM_API void qmm_plan_cta_range(const qmm_gemm_plan *plan, int32_t cta, int64_t 
 
 /* Path override for qmm_mul_mat: 0 = automatic, 1 = GEMV for any m <= 64,
  * 2 = the CUDA-core (dp4a) tiled GEMM, 3 = the tensor-core GEMM for any m,
- * 4 = GEMV for any m <= 64 with direct global loads only (no bulk copies). */
+ * 4 = GEMV for any m <= 64 with direct global loads only (no bulk copies),
+ * 5 = the skinny tensor-core path (Q4_K, m <= 16).  A forced path that does not
+ * support the call's type or sizes falls back to the automatic choice. */
 QMM_API void qmm_set_force_path(int path);
 
 /* Stream-K mode for the tensor-core GEMM: 0 = automatic, 1 = never, 2 = always. */
