@@ -20,14 +20,16 @@
 //               s tile of the min term, and d8 per superblock (transposed:
 //               [sub-block][token]).
 //   warp 1      TMEM allocation; one lane issues the MMAs: per superblock 8 sub-blocks
-//               of two K=16 MMAs each into 8 accumulator slots, plus one K=16 MMA for
-//               sum_b min * s; slots form a ring of 3 superblocks.
-//   warp 2      TMA: raw Q4_K superblocks of the tile's 128 rows, a 6-deep ring (the HBM
+//               of two K=16 MMAs each (A, the weights, read from TMEM; B, the
+//               activations, from shared memory) into 8 accumulator slots, plus one K=16
+//               MMA for sum_b min * s; slots form a ring of 2 superblocks.
+//   warp 2      TMA: raw Q4_K superblocks of the tile's 128 rows, an 8-deep ring (the HBM
 //               stream).
 //   warps 4-11  unpack, two groups of 4 warps: group h converts half h of every
-//               superblock (one weight row per thread) into the 128-byte-swizzled
-//               K-major layout the MMA reads; group 1 also writes the fp16 mins, group 0
-//               (d, -dmin) for the epilogue.
+//               superblock, one weight row per thread, and stores it with tcgen05.st into
+//               that row's TMEM lane (the MMA's A operand: fp16 pairs along the columns),
+//               so the unpacked weights never pass through shared memory; group 1 also
+//               writes the fp16 mins (shared memory), group 0 (d, -dmin) for the epilogue.
 //   warps 12-15 epilogue: one weight row per thread, 16 activation columns, the running
 //               sums in registers.
 // Every wait is bounded (qmm_tc_ptx.cuh); a wait that gives up raises the CTA's abort
@@ -50,25 +52,28 @@ namespace {
 constexpr int kRows = 128;        // weight rows per tile: MMA M, TMEM lanes
 constexpr int kNT = 16;           // activation rows per tile: MMA N, TMEM columns per slot
 constexpr int kMaxM = kNT;
-constexpr int kRawStages = 6;
+constexpr int kRawStages = 8;
 constexpr int kXStages = 8;       // activation half-superblocks in flight (they come from L2)
 constexpr int kSdRing = 4;        // superblocks of d8 / (d, -dmin) in flight
-constexpr int kSbRing = 3;        // superblocks of accumulator slots in TMEM
+constexpr int kSbRing = 2;        // superblocks of accumulator slots in TMEM
 constexpr int kSlotsPerSb = 9;    // 8 sub-blocks + the min term
 constexpr int kThreads = 512;
 constexpr int kUnpackWarp0 = 4;
 constexpr int kEpiWarp0 = 12;
 constexpr int kEpiWarps = 4;
 constexpr int kMaxPartialCtas = 256;
-static_assert(kSbRing * kSlotsPerSb * kNT <= 512, "accumulator ring exceeds TMEM");
+// TMEM columns: a ring of kABufs half-superblocks of unpacked weights (the MMA's A
+// operand, 64 columns of fp16 pairs each), then the accumulator slots
+constexpr uint32_t kAColsHalf = 64;
+constexpr int kABufs = 3;
+constexpr uint32_t kSlotCol0 = kABufs * kAColsHalf;
+static_assert(kSlotCol0 + kSbRing * kSlotsPerSb * kNT <= 512, "accumulator ring exceeds TMEM");
 
 // dynamic shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t kWSlab = kRows * 128;                      // 128 rows x 64 fp16
 constexpr uint32_t kXSlab = kNT * 128;                        // 16 rows x 64 fp16
-constexpr uint32_t kOffW = 0;                                 // [half][2 slabs]
-constexpr uint32_t kOffX = kOffW + 2 * 2 * kWSlab;            // [kXStages][2 slabs]
-constexpr uint32_t kOffWmin = kOffX + kXStages * 2 * kXSlab;  // [128][32 B]
-constexpr uint32_t kOffXmin = kOffWmin + kRows * 32;          // [kSdRing][16][32 B]
+constexpr uint32_t kOffX = 0;                                 // [kXStages][2 slabs]
+constexpr uint32_t kOffWmin = kOffX + kXStages * 2 * kXSlab;  // [2][128][32 B], by superblock parity
+constexpr uint32_t kOffXmin = kOffWmin + 2 * kRows * 32;      // [kSdRing][16][32 B]
 constexpr uint32_t kOffDX = kOffXmin + kSdRing * kNT * 32;    // [kSdRing][8][16] fp32
 constexpr uint32_t kDXBytes = 8 * kNT * 4;
 constexpr uint32_t kOffDD = kOffDX + kSdRing * kDXBytes;      // [kSdRing][d[128], -dmin[128]] fp32
@@ -92,7 +97,7 @@ struct SkArgs {
 };
 
 struct Barriers {
-    uint64_t x_full[kXStages], x_empty[kXStages], w_full[2], w_empty[2];
+    uint64_t x_full[kXStages], x_empty[kXStages], w_full[kABufs], w_empty[kABufs];
     uint64_t raw_full[kRawStages], raw_empty[kRawStages];
     uint64_t sd_full[kSdRing], sd_empty[kSdRing];
     uint64_t acc_full[kSbRing], acc_empty[kSbRing];
@@ -119,7 +124,7 @@ __device__ __forceinline__ bool next_seg(const SkArgs &a, int64_t &u, int64_t en
     return true;
 }
 
-__device__ __forceinline__ uint32_t slot_col(uint32_t sbs, int G) { return (sbs * kSlotsPerSb + G) * kNT; }
+__device__ __forceinline__ uint32_t slot_col(uint32_t sbs, int G) { return kSlotCol0 + (sbs * kSlotsPerSb + G) * kNT; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_tc_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
@@ -134,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         B.abort = 0;
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kABufs; ++s) {
             ptx::mbar_init(ptx::smem_u32(&B.w_full[s]), kRows);
             ptx::mbar_init(ptx::smem_u32(&B.w_empty[s]), 1);
         }
@@ -225,35 +230,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ok && next_seg(a, u, uend, sg)) {
                 for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb, ++sbc) {
                     const uint32_t sbs = sbc % kSbRing, aph = (sbc / kSbRing) & 1;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_empty[sbs]), aph ^ 1, abortp)) {
+                    if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_empty[sbs]), aph ^ 1, abortp)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     for (int h = 0; ok && h < 2; ++h) {
                         const uint32_t xi = (2 * sbc + h) % kXStages, xph = ((2 * sbc + h) / kXStages) & 1;
-                        if (!ptx::mbar_wait(ptx::smem_u32(&B.x_full[xi]), xph, abortp) ||
-                            !ptx::mbar_wait(ptx::smem_u32(&B.w_full[h]), sbc & 1, abortp)) {
+                        const uint32_t ai = (2 * sbc + h) % kABufs, aph2 = ((2 * sbc + h) / kABufs) & 1;
+                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.x_full[xi]), xph, abortp) ||
+                            !ptx::mbar_wait_spin(ptx::smem_u32(&B.w_full[ai]), aph2, abortp)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint32_t wa = sbase + kOffW + h * 2 * kWSlab;
-                        const uint32_t xa = sbase + kOffX + xi * 2 * kXSlab;
-                        for (int q = 0; q < 4; ++q) {
-                            const uint32_t col = slot_col(sbs, 4 * h + q);
+                        // descriptors of the two activation slabs, built once; a K16 step of 32
+                        // bytes inside the 128-byte swizzled row adds 2 to the start-address field
+                        const uint64_t xd0 = ptx::smem_desc(sbase + kOffX + xi * 2 * kXSlab, 1024, 2);
+                        const uint64_t xd1 = ptx::smem_desc(sbase + kOffX + xi * 2 * kXSlab + kXSlab, 1024, 2);
+                        const uint32_t dcol = tmem + slot_col(sbs, 4 * h), acol = tmem + ai * kAColsHalf;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {  // sub-block 4h + q: K = 128h + 32q ..
+#pragma unroll
                             for (int t = 0; t < 2; ++t) {
-                                const uint32_t koff = ((q & 1) * 2 + t) * 32;  // K16 step in the 128-byte row
-                                ptx::mma_f16(tmem + col, ptx::smem_desc(wa + (q >> 1) * kWSlab + koff, 1024, 2),
-                                             ptx::smem_desc(xa + (q >> 1) * kXSlab + koff, 1024, 2), idesc, t);
+                                const uint32_t kstep = (q & 1) * 2 + t;  // K16 step in the 128-byte row
+                                ptx::mma_f16_tmem_a(dcol + kNT * q, acol + 16 * q + 8 * t,
+                                                    ((q >> 1) ? xd1 : xd0) + 2 * kstep, idesc, t);
                             }
                         }
                         if (h == 1)
-                            ptx::mma_f16(tmem + slot_col(sbs, 8), ptx::smem_desc(sbase + kOffWmin, 256, 6),
+                            ptx::mma_f16(tmem + slot_col(sbs, 8),
+                                         ptx::smem_desc(sbase + kOffWmin + (sbc & 1) * (kRows * 32), 256, 6),
                                          ptx::smem_desc(sbase + kOffXmin + (sbc % kSdRing) * (kNT * 32), 256, 6),
                                          idesc, 0);
                         ptx::mma_commit(ptx::smem_u32(&B.x_empty[xi]));
-                        ptx::mma_commit(ptx::smem_u32(&B.w_empty[h]));
+                        ptx::mma_commit(ptx::smem_u32(&B.w_empty[ai]));
                     }
                     if (ok) ptx::mma_commit(ptx::smem_u32(&B.acc_full[sbs]));
                 }
@@ -318,13 +329,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dd[kRows + r] = -half_hi(hd.x);
                     ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[sdi]));
                 }
-                if (!ptx::mbar_wait(ptx::smem_u32(&B.w_empty[h]), (sbc & 1) ^ 1, abortp)) {
+                const uint32_t ai = (2 * sbc + h) % kABufs;
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.w_empty[ai]), (((2 * sbc + h) / kABufs) & 1) ^ 1, abortp)) {
                     ok = false;
                     break;
                 }
-                uint8_t *wst = smem + kOffW + h * 2 * kWSlab;
+                ptx::tc_fence_after();  // after the MMAs that read the previous contents
+                // this thread's row is TMEM lane r: the warp's lane quarter is r / 32 = warp % 4
+                const uint32_t arow = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + ai * kAColsHalf;
 #pragma unroll
-                for (int j2 = 0; j2 < 2; ++j2) {  // slab j2 <-> qs chunk c = 2h + j2
+                for (int j2 = 0; j2 < 2; ++j2) {  // qs chunk c = 2h + j2: sub-blocks 2c (low), 2c+1 (high)
                     const int c = 2 * h + j2;
                     const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
                     const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
@@ -334,14 +348,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __half2 s_lo = __float2half2_rn((float)sc_lo), ns_lo = __float2half2_rn(-1024.f * sc_lo);
                     const __half2 s_hi = __float2half2_rn((float)sc_hi), ns_hi = __float2half2_rn(-1024.f * sc_hi);
                     const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-                    uint8_t *rowdst = wst + j2 * kWSlab + r * 128;
+                    uint32_t lo[16], hi[16];  // 32 fp16 values each, two per column
 #pragma unroll
                     for (int cq = 0; cq < 4; ++cq) {
-                        const uint4 lo = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 0, s_lo, ns_lo);
-                        const uint4 hi = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 4, s_hi, ns_hi);
-                        *reinterpret_cast<uint4 *>(rowdst + ((cq ^ (r & 7)) << 4)) = lo;
-                        *reinterpret_cast<uint4 *>(rowdst + (((cq + 4) ^ (r & 7)) << 4)) = hi;
+                        const uint4 l4 = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 0, s_lo, ns_lo);
+                        const uint4 h4 = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 4, s_hi, ns_hi);
+                        lo[4 * cq] = l4.x; lo[4 * cq + 1] = l4.y; lo[4 * cq + 2] = l4.z; lo[4 * cq + 3] = l4.w;
+                        hi[4 * cq] = h4.x; hi[4 * cq + 1] = h4.y; hi[4 * cq + 2] = h4.z; hi[4 * cq + 3] = h4.w;
                     }
+                    ptx::tmem_st_32x32b_x16(arow + 32 * j2, lo);
+                    ptx::tmem_st_32x32b_x16(arow + 32 * j2 + 16, hi);
                 }
                 if (h == 1) {  // mins of the 8 sub-blocks as fp16, then 8 zeros (32-byte swizzle)
                     uint32_t mm[4];
@@ -352,13 +368,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         q4k_scale_min(hd.y, hd.z, hd.w, 2 * i2 + 1, s1_, m1_);
                         mm[i2] = h2bits(__floats2half2_rn((float)m0_, (float)m1_));
                     }
-                    uint8_t *mdst = smem + kOffWmin + r * 32;
+                    // by superblock parity: this group may write superblock s+1's mins while
+                    // the MMA of superblock s is still to read its own (the A ring lets it
+                    // run one half ahead); the buffer of s-1 is free, since the use of the
+                    // A buffer waited for the MMAs of (s, half 0), issued after (s-1, half 1)
+                    uint8_t *mdst = smem + kOffWmin + (sbc & 1) * (kRows * 32) + r * 32;
                     const int sw = (r >> 2) & 1;
                     *reinterpret_cast<uint4 *>(mdst + ((0 ^ sw) << 4)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
                     *reinterpret_cast<uint4 *>(mdst + ((1 ^ sw) << 4)) = make_uint4(0, 0, 0, 0);
                 }
-                ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(ptx::smem_u32(&B.w_full[h]));
+                ptx::tmem_st_wait();
+                ptx::fence_proxy_async_smem();  // the mins are read by the MMA (async proxy)
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_u32(&B.w_full[ai]));
                 ptx::mbar_arrive(ptx::smem_u32(&B.raw_empty[ri]));
             }
         }
