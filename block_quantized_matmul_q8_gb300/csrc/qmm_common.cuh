@@ -90,6 +90,36 @@ __device__ __forceinline__ uint32_t ldg2(const void *p) {
     return r;
 }
 
+// Load policies of the two-phase decode below: rows read from global memory (read-only
+// path) or rows staged in shared memory by a bulk copy.
+struct LdGlobal {
+    static __device__ __forceinline__ uint32_t u32(const void *p) { return ldg4(p); }
+    static __device__ __forceinline__ uint32_t u16(const void *p) { return ldg2(p); }
+    static __device__ __forceinline__ uint4 u128(const void *p) { return ldg16(p); }
+};
+struct LdShared {
+    static __device__ __forceinline__ uint32_t saddr(const void *p) {
+        return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    }
+    static __device__ __forceinline__ uint32_t u32(const void *p) {
+        uint32_t r;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(saddr(p)));
+        return r;
+    }
+    static __device__ __forceinline__ uint32_t u16(const void *p) {
+        unsigned short r;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(saddr(p)));
+        return r;
+    }
+    static __device__ __forceinline__ uint4 u128(const void *p) {
+        uint4 r;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                     : "r"(saddr(p)));
+        return r;
+    }
+};
+
 // Q4_K: 6-bit scale and min of sub-block j from the 12 packed bytes held in three
 // little-endian words s0 (bytes 0..3), s1 (4..7), s2 (8..11).
 __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int &sc, int &mn) {
@@ -229,12 +259,13 @@ template <> struct Raw<QMM_Q8_0> { uint32_t w[18]; uint32_t shift; bool two; };
 // units per lane kept in flight by the GEMV
 template <int T> constexpr int kRawChunk = T == QMM_Q4_K ? 5 : T == QMM_Q6_K ? 2 : 3;
 
+template <class Ld = LdGlobal>
 __device__ __forceinline__ void load_raw(const uint8_t *row, int u, int, Raw<QMM_Q4_K> &r) {
     const uint8_t *blk = row + (u >> 2) * kQ4KBytes;
     const int c = u & 3;
-    r.h = ldg16(blk);
-    r.a = ldg16(blk + 16 + 32 * c);
-    r.b = ldg16(blk + 32 + 32 * c);
+    r.h = Ld::u128(blk);
+    r.a = Ld::u128(blk + 16 + 32 * c);
+    r.b = Ld::u128(blk + 32 + 32 * c);
 }
 
 __device__ __forceinline__ void convert_raw(const Raw<QMM_Q4_K> &r, int u, Unit &o) {
@@ -261,6 +292,7 @@ __device__ __forceinline__ void convert_raw(const Raw<QMM_Q4_K> &r, int u, Unit 
 // their range (still inside the block), the scales load 4 words + the fp16 d as a
 // 2-byte load.  Misaligned: every part starts one halfword early; the scale words
 // [190, 210) end exactly at the block end.
+template <class Ld = LdGlobal>
 __device__ __forceinline__ void load_raw(const uint8_t *row, int u, int, Raw<QMM_Q6_K> &r) {
     const uint8_t *blk = row + (u >> 2) * kQ6KBytes;
     const int v = u & 3, h = v >> 1;
@@ -271,12 +303,12 @@ __device__ __forceinline__ void load_raw(const uint8_t *row, int u, int, Raw<QMM
     const uint32_t *qh = reinterpret_cast<const uint32_t *>((a + 128 + 32 * h) - mis);
     const uint32_t *sc = reinterpret_cast<const uint32_t *>((a + 192) - mis);
 #pragma unroll
-    for (int i = 0; i < 17; ++i) r.ql[i] = ldg4(ql + i);
+    for (int i = 0; i < 17; ++i) r.ql[i] = Ld::u32(ql + i);
 #pragma unroll
-    for (int i = 0; i < 9; ++i) r.qh[i] = ldg4(qh + i);
+    for (int i = 0; i < 9; ++i) r.qh[i] = Ld::u32(qh + i);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) r.sc[i] = ldg4(sc + i);
-    r.sc[4] = mis ? ldg4(sc + 4) : ldg2(sc + 4);
+    for (int i = 0; i < 4; ++i) r.sc[i] = Ld::u32(sc + i);
+    r.sc[4] = mis ? Ld::u32(sc + 4) : Ld::u16(sc + 4);
 }
 
 __device__ __forceinline__ void convert_raw(const Raw<QMM_Q6_K> &r, int u, Unit &o) {
@@ -313,6 +345,7 @@ __device__ __forceinline__ void convert_raw(const Raw<QMM_Q6_K> &r, int u, Unit 
 // only 2-byte aligned.  Two-block units are never the last unit of their row, so a
 // misaligned load of 18 words [68u-2, 68u+70) stays inside the row's bytes plus the
 // next unit's; a single-block unit reads exactly [68u, 68u+34) (or from 68u-2).
+template <class Ld = LdGlobal>
 __device__ __forceinline__ void load_raw(const uint8_t *row, int u, int nblk32, Raw<QMM_Q8_0> &r) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(row + 68 * u);
     const uint32_t mis = (uint32_t)(a & 2u);
@@ -321,12 +354,12 @@ __device__ __forceinline__ void load_raw(const uint8_t *row, int u, int nblk32, 
     const uint32_t *p = reinterpret_cast<const uint32_t *>(a - mis);
     if (r.two) {
 #pragma unroll
-        for (int i = 0; i < 17; ++i) r.w[i] = ldg4(p + i);
-        r.w[17] = mis ? ldg4(p + 17) : 0u;
+        for (int i = 0; i < 17; ++i) r.w[i] = Ld::u32(p + i);
+        r.w[17] = mis ? Ld::u32(p + 17) : 0u;
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r.w[i] = ldg4(p + i);
-        r.w[8] = mis ? ldg4(p + 8) : ldg2(p + 8);
+        for (int i = 0; i < 8; ++i) r.w[i] = Ld::u32(p + i);
+        r.w[8] = mis ? Ld::u32(p + 8) : Ld::u16(p + 8);
 #pragma unroll
         for (int i = 9; i < 18; ++i) r.w[i] = 0u;
     }

@@ -239,8 +239,7 @@ constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
 constexpr int kTmaChunkRows = 2 * kTmaGroupWarps;  // one row per half-warp
 
 // Stages of kTmaChunkRows rows that fit next to the staged activations (0: too few).
-int gemv_tma_stages(int64_t k, int ncols, size_t budget) {
-    const int64_t row_bytes = (k / 256) * kQ4KBytes;
+int gemv_tma_stages(int64_t row_bytes, int64_t k, int ncols, size_t budget) {
     const size_t fixed = 1024 + gemv_smem_bytes(k, ncols);
     if (fixed >= budget) return 0;
     const int64_t st = int64_t(budget - fixed) / (int64_t(kTmaChunkRows) * row_bytes);
@@ -291,11 +290,14 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-template <int NC>
-__global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint8_t *__restrict__ W, int64_t n,
-                                                                      int k, int64_t row_bytes, int nstages,
-                                                                      const XIn x, float *__restrict__ y,
-                                                                      int64_t y_ld, int *status) {
+// The body of the bulk-copy GEMV for format T.  Q6_K rows (210-byte blocks) keep their
+// chunks 16-byte aligned only from an even row on, so for Q6_K the CTAs' row ranges
+// start on even rows (the host takes this kernel for Q6_K only when n is even or the
+// rows are whole multiples of 16 bytes).
+template <int T, int NC>
+__device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int64_t n, int k, int64_t row_bytes,
+                                              int nstages, const XIn &x, float *__restrict__ y, int64_t y_ld,
+                                              int *status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full[kTmaMaxStages], empty[kTmaMaxStages];
@@ -307,7 +309,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
     uint8_t *xs = smem + nstages * stage_bytes;
     float2 *xds = reinterpret_cast<float2 *>(xs + size_t(NC) * U * kUnitStride);
 
-    const int64_t r0 = n * blockIdx.x / gridDim.x, r1 = n * (blockIdx.x + 1) / gridDim.x;
+    const int64_t ra = (T == QMM_Q6_K && (row_bytes & 15)) ? 2 : 1;  // row granularity of the split
+    const int64_t nr = (n + ra - 1) / ra;
+    const int64_t r0 = ra * (nr * blockIdx.x / gridDim.x);
+    const int64_t r1 = min(n, ra * (nr * (blockIdx.x + 1) / gridDim.x));
     const int nchunks = (int)((r1 - r0 + kTmaChunkRows - 1) / kTmaChunkRows);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, l16 = lane & 15;
     volatile int *abortp = &abort_flag;
@@ -356,7 +361,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
 
         const int grp = warp / kTmaGroupWarps, gw = warp % kTmaGroupWarps;
         const int rr = 2 * gw + (lane >> 4);  // row within a chunk
-        const int c4 = l16 & 3;               // qs chunk of every unit this lane takes
+        const int c4 = l16 & 3;               // qs chunk of every unit this lane takes (Q4_K)
         const Q4KPairSel psel = q4k_pair_sel(c4);
         for (int c = grp; c < nchunks; c += kTmaGroups) {
             const int s = c % nstages;
@@ -366,7 +371,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
             float acc[NC];
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) acc[cc] = 0.f;
-            if (valid) {
+            if (T == QMM_Q4_K && valid) {
                 const uint8_t *row = stages + s * stage_bytes + size_t(rr) * row_bytes;
                 for (int u = l16; u < U; u += 16) {
                     const uint8_t *blk = row + (u >> 2) * kQ4KBytes;
@@ -410,6 +415,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
                     }
                 }
             }
+            if (T != QMM_Q4_K && valid) {
+                // Q6_K / Q8_0: the two-phase decode of the direct kernel, reading the staged row
+                const uint8_t *row = stages + s * stage_bytes + size_t(rr) * row_bytes;
+                for (int u = l16; u < U; u += 16) {
+                    Raw<T> raw;
+                    load_raw<LdShared>(row, u, nb32, raw);
+                    Unit w;
+                    convert_raw(raw, u, w);
+                    fold_unit<NC>(w, xs, xds, U, u, acc);
+                }
+            }
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) {
                 float v = acc[cc];
@@ -432,11 +448,40 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
 }
 
 template <int NC>
+__global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint8_t *__restrict__ W, int64_t n,
+                                                                      int k, int64_t row_bytes, int nstages,
+                                                                      const XIn x, float *__restrict__ y,
+                                                                      int64_t y_ld, int *status) {
+    gemv_tma_body<QMM_Q4_K, NC>(W, n, k, row_bytes, nstages, x, y, y_ld, status);
+}
+
+template <int T, int NC>
+__global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const uint8_t *__restrict__ W, int64_t n, int k,
+                                                                  int64_t row_bytes, int nstages, const XIn x,
+                                                                  float *__restrict__ y, int64_t y_ld, int *status) {
+    gemv_tma_body<T, NC>(W, n, k, row_bytes, nstages, x, y, y_ld, status);
+}
+
+// Rows that a bulk-copy GEMV can stream: every chunk must start on and span whole
+// 16-byte units.  Q4_K rows always are; Q8_0 rows when k/32 is a multiple of 8; Q6_K
+// rows when (k/256) * 210 is, or else from an even row on when n is even.
+template <int T> static int64_t gemv_tma_row_bytes(int64_t n, int64_t k) {
+    const int64_t rb = (k / block_elems(T)) * block_bytes(T);
+    if (rb % 16 == 0) return rb;
+    if (T == QMM_Q6_K && rb % 8 == 0 && n % 2 == 0) return rb;
+    return 0;
+}
+
+template <int T, int NC>
 static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x, float *y, int64_t y_ld,
                                       int nstages, cudaStream_t st) {
-    const int64_t row_bytes = (k / 256) * kQ4KBytes;
+    const int64_t row_bytes = gemv_tma_row_bytes<T>(n, k);
     const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, NC);
-    auto kern = gemv_q4k_tma_kernel<NC>;
+    void (*kern)(const uint8_t *, int64_t, int, int64_t, int, const XIn, float *, int64_t, int *);
+    if constexpr (T == QMM_Q4_K)
+        kern = gemv_q4k_tma_kernel<NC>;
+    else
+        kern = gemv_tma_kernel<T, NC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
@@ -481,17 +526,18 @@ static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void
         xc.xq = xf ? nullptr : static_cast<const uint8_t *>(xq) + c0 * xrow;
         xc.xf = xf ? xf + c0 * k : nullptr;
         float *yc = y + c0 * n;
-        const int nst = T == QMM_Q4_K ? gemv_tma_stages(k, nc, budget) : 0;
+        const int64_t trb = gemv_tma_row_bytes<T>(n, k);
+        const int nst = trb > 0 ? gemv_tma_stages(trb, k, nc, budget) : 0;
         if (nst > 0 && gemv_tma_enabled()) {
             switch (nc) {
-            case 1: e = launch_gemv_tma_nc<1>(W, n, k, xc, yc, n, nst, st); break;
-            case 2: e = launch_gemv_tma_nc<2>(W, n, k, xc, yc, n, nst, st); break;
-            case 3: e = launch_gemv_tma_nc<3>(W, n, k, xc, yc, n, nst, st); break;
-            case 4: e = launch_gemv_tma_nc<4>(W, n, k, xc, yc, n, nst, st); break;
-            case 5: e = launch_gemv_tma_nc<5>(W, n, k, xc, yc, n, nst, st); break;
-            case 6: e = launch_gemv_tma_nc<6>(W, n, k, xc, yc, n, nst, st); break;
-            case 7: e = launch_gemv_tma_nc<7>(W, n, k, xc, yc, n, nst, st); break;
-            default: e = launch_gemv_tma_nc<8>(W, n, k, xc, yc, n, nst, st); break;
+            case 1: e = launch_gemv_tma_nc<T, 1>(W, n, k, xc, yc, n, nst, st); break;
+            case 2: e = launch_gemv_tma_nc<T, 2>(W, n, k, xc, yc, n, nst, st); break;
+            case 3: e = launch_gemv_tma_nc<T, 3>(W, n, k, xc, yc, n, nst, st); break;
+            case 4: e = launch_gemv_tma_nc<T, 4>(W, n, k, xc, yc, n, nst, st); break;
+            case 5: e = launch_gemv_tma_nc<T, 5>(W, n, k, xc, yc, n, nst, st); break;
+            case 6: e = launch_gemv_tma_nc<T, 6>(W, n, k, xc, yc, n, nst, st); break;
+            case 7: e = launch_gemv_tma_nc<T, 7>(W, n, k, xc, yc, n, nst, st); break;
+            default: e = launch_gemv_tma_nc<T, 8>(W, n, k, xc, yc, n, nst, st); break;
             }
             if (e != cudaSuccess) return e;
             c0 += nc;

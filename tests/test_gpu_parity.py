@@ -78,8 +78,11 @@ def test_quantize_near_ties_bitexact(oracle_mod):
 
 # ---------------------------------------------------------------- GEMV (m <= 8)
 
-GEMV_SHAPES = {"q4_K": [(1, 256), (7, 512), (129, 2304)], "q6_K": [(1, 256), (7, 512), (129, 2304)],
-               "q8_0": [(1, 32), (7, 96), (129, 1056), (33, 2048)]}
+# Q6_K with an even n and Q8_0 with k/32 a multiple of 8 stream their rows with bulk
+# copies; the other shapes take the direct-load kernel.
+GEMV_SHAPES = {"q4_K": [(1, 256), (7, 512), (129, 2304)],
+               "q6_K": [(1, 256), (7, 512), (129, 2304), (130, 2304), (64, 512), (2, 5120)],
+               "q8_0": [(1, 32), (7, 96), (129, 1056), (33, 2048), (130, 256), (64, 5120)]}
 
 
 @pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q8_0"])
@@ -161,3 +164,18 @@ def test_moe_parity(oracle_mod, E, n, k, T_, K):
 
 def test_moe_invalid_ids_flagged_and_zeroed(oracle_mod):
     moe_check(oracle_mod, 8, 64, 256, 40, 4, seed=5, corrupt=6)
+
+
+@pytest.mark.parametrize("fmt,n,k", [("q6_K", 130, 2304), ("q6_K", 1000, 5120), ("q8_0", 130, 256),
+                                     ("q8_0", 512, 5120)])
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_gemv_bulk_and_direct_agree(oracle_mod, fmt, n, k, m):
+    """The bulk-copy GEMV (path 1) and the direct-load GEMV (path 4) fold the same
+    decoded units in the same order: their outputs agree to the bit."""
+    W, x = qmm_synth.make_dense(fmt, n, k, m, seed=n + m)
+    xq = oracle_mod.quantize_q8_1(x)
+    a = run_mul_mat(W, fmt, n, k, xq, m, path=1)
+    b = run_mul_mat(W, fmt, n, k, xq, m, path=4)
+    assert np.array_equal(a, b)
+    y_ref, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
+    assert_within(a, y_ref, T, f"bulk gemv {fmt} n={n} k={k} m={m}")
