@@ -55,11 +55,8 @@ namespace {
 constexpr int kTM = 128;  // activation rows per tile
 constexpr int kTN = 128;  // weight rows per tile
 constexpr int kStages = 2;
-constexpr int kSlots = 3;          // accumulator slots of 128 TMEM columns; columns 384..511 hold the running total
-// 9 slot uses per superblock (8 sub-blocks + the min term): the epilogue relies on each
-// superblock starting at slot 0
-static_assert(9 % kSlots == 0, "slot ring must divide the 9 slot uses of a superblock");
-constexpr uint32_t kTotCol = 384;
+constexpr int kMaxSlots = 4;       // accumulator slots of 128 TMEM columns
+constexpr uint32_t kTotCol = 384;  // Q4_K: columns 384..511 hold the running total
 constexpr int kThreads = 768;      // 24 warps = 6 warpgroups
 constexpr int kUnpackWarp0 = 4;
 constexpr int kEpiWarp0 = 8;
@@ -73,18 +70,45 @@ static_assert(128 * kRegsProducer + 128 * kRegsUnpack + 32 * kEpiWarps * kRegsEp
               "register split exceeds the launch allocation");
 constexpr int kMaxPartialCtas = 256;
 
+// Per-format constants.  Q4_K: 144-byte superblocks, a min term, 9 slot uses per
+// superblock (8 sub-blocks + the min term), (d, -dmin) per row.  Q8_0: the 256 k values
+// of a step are eight 34-byte blocks, no min term, 8 slot uses, a d per 32-block and row.
+// Each superblock starts at slot 0 (the uses are a multiple of the ring).
+template <int T> struct TcFmt;
+template <> struct TcFmt<QMM_Q4_K> {
+    static constexpr uint32_t kRawRow = kQ4KBytes;  // raw bytes of one weight row per 256 k
+    static constexpr uint32_t kRawElem = 1;         // element size of the raw tensor map
+    static constexpr bool kMin = true;
+    static constexpr int kSlots = 3;
+    static constexpr int kUses = 9;
+    static constexpr uint32_t kDDBytes = 2 * 128 * 4;  // d[128], -dmin[128]
+};
+template <> struct TcFmt<QMM_Q8_0> {
+    static constexpr uint32_t kRawRow = 8 * kQ80Bytes;  // 272
+    static constexpr uint32_t kRawElem = 2;             // 136 uint16 per row: a box dimension <= 256
+    static constexpr bool kMin = false;
+    static constexpr int kSlots = 4;
+    static constexpr int kUses = 8;
+    static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
+};
+
 // dynamic shared memory map (offsets from a 1024-aligned base)
-constexpr uint32_t kSlabBytes = 128 * 128;                       // 128 rows x 64 fp16
-constexpr uint32_t kOffX = 0;                                     // [stage][2 slabs]
-constexpr uint32_t kOffW = kOffX + kStages * 2 * kSlabBytes;      // [stage][2 slabs]
-constexpr uint32_t kOffXmin = kOffW + kStages * 2 * kSlabBytes;   // [stage][128][32 B]
-constexpr uint32_t kOffWmin = kOffXmin + kStages * 4096;          // [stage][128][32 B]
-constexpr uint32_t kOffDX = kOffWmin + kStages * 4096;            // [2][128][8] fp32
-constexpr uint32_t kOffDD = kOffDX + 2 * 4096;                    // [2][d[128], -dmin[128]] fp32
-constexpr uint32_t kRawBytes = 128 * kQ4KBytes;                   // raw Q4_K superblocks of 128 weight rows
-constexpr uint32_t kOffRaw = (kOffDD + 2 * 1024 + 1023) & ~1023u;  // [2][128][144]
-constexpr uint32_t kSmemBytes = kOffRaw + 2 * kRawBytes;
-constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
+constexpr uint32_t kSlabBytes = 128 * 128;  // 128 rows x 64 fp16
+template <int T> struct TcMap {
+    using F = TcFmt<T>;
+    static_assert(F::kUses % F::kSlots == 0 && F::kSlots <= kMaxSlots, "slot ring");
+    static constexpr uint32_t kOffX = 0;                                    // [stage][2 slabs]
+    static constexpr uint32_t kOffW = kOffX + kStages * 2 * kSlabBytes;     // [stage][2 slabs]
+    static constexpr uint32_t kMinBytes = F::kMin ? kStages * 4096 : 0;
+    static constexpr uint32_t kOffXmin = kOffW + kStages * 2 * kSlabBytes;  // [stage][128][32 B]
+    static constexpr uint32_t kOffWmin = kOffXmin + kMinBytes;              // [stage][128][32 B]
+    static constexpr uint32_t kOffDX = kOffWmin + kMinBytes;                // [2][128][8] fp32
+    static constexpr uint32_t kOffDD = kOffDX + 2 * 4096;                   // [2][kDDBytes]
+    static constexpr uint32_t kRawBytes = 128 * F::kRawRow;                 // raw weights of 128 rows
+    static constexpr uint32_t kOffRaw = (kOffDD + 2 * F::kDDBytes + 1023) & ~1023u;
+    static constexpr uint32_t kSmemAlloc = kOffRaw + 2 * kRawBytes + 1024;
+    static_assert(kSmemAlloc <= 227 * 1024, "shared memory map exceeds the per-CTA limit");
+};
 
 struct TcArgs {
     const uint8_t *W;
@@ -134,7 +158,7 @@ __device__ __forceinline__ TileInfo resolve_tile(const TcArgs &a, int64_t t) {
 
 struct Barriers {
     uint64_t x_full[kStages], x_empty[kStages], w_full[kStages], w_empty[kStages];
-    uint64_t acc_full[kSlots], acc_empty[kSlots];
+    uint64_t acc_full[kMaxSlots], acc_empty[kMaxSlots];
     uint64_t sd_full[2], sd_empty[2];
     uint64_t raw_full[2], raw_empty[2];
     uint64_t done;
@@ -166,10 +190,14 @@ __device__ __forceinline__ bool next_seg(const TcArgs &a, int64_t &u, int64_t en
 }
 
 
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
-                       const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
-                       TcArgs a) {
+template <int T>
+__device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin,
+                                             const CUtensorMap &tm_dx, const CUtensorMap &tm_w, TcArgs a) {
+    using F = TcFmt<T>;
+    using Mp = TcMap<T>;
+    constexpr int kSlots = F::kSlots;
+    constexpr uint32_t kOffX = Mp::kOffX, kOffW = Mp::kOffW, kOffXmin = Mp::kOffXmin, kOffWmin = Mp::kOffWmin;
+    constexpr uint32_t kOffDX = Mp::kOffDX, kOffDD = Mp::kOffDD, kOffRaw = Mp::kOffRaw, kRawBytes = Mp::kRawBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ Barriers B;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -218,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         regs_dec<kRegsProducer>();
         if (lane == 0) {
             ptx::prefetch_tmap(&tm_x);
-            ptx::prefetch_tmap(&tm_xmin);
+            if (F::kMin) ptx::prefetch_tmap(&tm_xmin);
             ptx::prefetch_tmap(&tm_dx);
             int64_t u = ubeg;
             Seg sg;
@@ -243,11 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         const uint32_t bar = ptx::smem_u32(&B.x_full[st]);
-                        ptx::mbar_arrive_expect_tx(bar, 2 * kSlabBytes + (h ? 4096u : 0u));
+                        ptx::mbar_arrive_expect_tx(bar, 2 * kSlabBytes + ((F::kMin && h) ? 4096u : 0u));
                         const int kx = (int)(256 * sb + 128 * h);
                         ptx::tma_load_2d(sbase + kOffX + st * 2 * kSlabBytes, &tm_x, kx, m0, bar);
                         ptx::tma_load_2d(sbase + kOffX + st * 2 * kSlabBytes + kSlabBytes, &tm_x, kx + 64, m0, bar);
-                        if (h) ptx::tma_load_2d(sbase + kOffXmin + st * 4096, &tm_xmin, (int)(16 * sb), m0, bar);
+                        if (F::kMin && h)
+                            ptx::tma_load_2d(sbase + kOffXmin + st * 4096, &tm_xmin, (int)(16 * sb), m0, bar);
                         ++x_it;
                     }
                 }
@@ -296,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::mma_commit(ptx::smem_u32(&B.acc_full[slot]));
                             ++g;
                         }
-                        if (ok && h == 1) {
+                        if (F::kMin && ok && h == 1) {
                             const uint32_t slot = g % kSlots;
                             if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_empty[slot]), ((g / kSlots) & 1) ^ 1, abortp)) {
                                 ok = false;
@@ -341,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t rbar = ptx::smem_u32(&B.raw_full[ri]);
                     ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
-                    ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, (int)(sb * kQ4KBytes), n0, rbar);
+                    ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, (int)(sb * (F::kRawRow / F::kRawElem)),
+                                     n0, rbar);
                     ++r_it;
                 }
             }
@@ -368,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + r * kQ4KBytes;
+                const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + r * F::kRawRow;
+                if constexpr (T == QMM_Q4_K) {
                 const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
                 // (d, -dmin) for the epilogue
                 if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[ri]), ((sb_it >> 1) & 1) ^ 1, abortp)) {
@@ -424,6 +455,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive(ptx::smem_u32(&B.w_full[st]));
                     ++w_it;
                 }
+                } else {
+                // Q8_0: the row's 256 k values are 8 blocks of {fp16 d, int8 q[32]}, block b at
+                // byte 34b.  The d of every block goes to the epilogue; the codes become
+                // exact fp16 integers: (q ^ 0x80) | 0x6400 is the fp16 1024 + q + 128.
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[ri]), ((sb_it >> 1) & 1) ^ 1, abortp)) {
+                    ok = false;
+                    break;
+                }
+                float *dw = reinterpret_cast<float *>(smem + kOffDD + ri * F::kDDBytes);
+#pragma unroll
+                for (int b = 0; b < 8; ++b) dw[b * 128 + r] = __half2float(*reinterpret_cast<const __half *>(blk + 34 * b));
+                ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
+                const __half2 bias = __float2half2_rn(-1152.f);
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t st = w_it % kStages;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.w_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    // blocks 4h .. 4h+3: 136 bytes from byte 136h (rows are 272 = 16*17 bytes apart,
+                    // so the range is 8-byte aligned); block b2 starts at byte 34 b2 of it
+                    uint32_t w[34];
+                    const uint2 *src = reinterpret_cast<const uint2 *>(blk + 136 * h);
+#pragma unroll
+                    for (int i2 = 0; i2 < 17; ++i2) {
+                        const uint2 t2 = src[i2];
+                        w[2 * i2] = t2.x;
+                        w[2 * i2 + 1] = t2.y;
+                    }
+                    uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
+#pragma unroll
+                    for (int b2 = 0; b2 < 4; ++b2) {
+                        const int o = (b2 >> 1) * 17;
+                        uint32_t q[8];
+#pragma unroll
+                        for (int i2 = 0; i2 < 8; ++i2)  // codes at byte 34 b2 + 2: word-aligned for odd b2
+                            q[i2] = (b2 & 1) ? w[o + 9 + i2] : __funnelshift_r(w[o + i2], w[o + i2 + 1], 16);
+                        uint8_t *rowdst = wst + (b2 >> 1) * kSlabBytes + r * 128;
+#pragma unroll
+                        for (int cq = 0; cq < 4; ++cq) {
+                            uint32_t pr[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const uint32_t uu = q[2 * cq + e2] ^ 0x80808080u;
+                                uint32_t lo = __byte_perm(uu, 0x64646464u, 0x4140);
+                                uint32_t hi = __byte_perm(uu, 0x64646464u, 0x4342);
+                                lo = h2bits(__hadd2(*reinterpret_cast<__half2 *>(&lo), bias));
+                                hi = h2bits(__hadd2(*reinterpret_cast<__half2 *>(&hi), bias));
+                                pr[2 * e2] = lo;
+                                pr[2 * e2 + 1] = hi;
+                            }
+                            const int chunk = (b2 & 1) * 4 + cq;  // 16-byte chunk of the 128-byte row
+                            *reinterpret_cast<uint4 *>(rowdst + ((chunk ^ (r & 7)) << 4)) =
+                                make_uint4(pr[0], pr[1], pr[2], pr[3]);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(ptx::smem_u32(&B.w_full[st]));
+                    ++w_it;
+                }
+                }
                 ptx::mbar_arrive(ptx::smem_u32(&B.raw_empty[ri]));
                 ++sb_it;
             }
@@ -435,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fold into acc (fp32), then the min slot and the running total (TMEM columns
         // 384..511) are updated in two 16-column halves.
         regs_inc<kRegsEpilogue>();
+        if constexpr (T == QMM_Q4_K) {
         const int ew = warp - kEpiWarp0;       // 0..15
         const int cq = ew >> 2;                // column quarter: columns 32cq .. 32cq+31
         const int qd = warp & 3;               // TMEM lane quarter this warp may access
@@ -567,6 +660,106 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++seg_i;
         }
+        } else {
+        // Q8_0: per sub-block acc += (d8 * d_w) * slot, two columns per packed product and
+        // fma; there is no per-superblock scale, so the sums stay in registers for the
+        // whole segment and no TMEM total is kept.
+        const int ew = warp - kEpiWarp0;
+        const int cq = ew >> 2;
+        const int qd = warp & 3;
+        const int tl = 32 * qd + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
+        int64_t u = ubeg;
+        Seg sg;
+        uint32_t sd_it = 0;
+        int seg_i = 0;
+        bool ok = true;
+        while (ok && next_seg(a, u, uend, sg)) {
+            float2 acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = make_float2(0.f, 0.f);
+            for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
+                const uint32_t sdi = sd_it & 1;
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_full[sdi]), (sd_it >> 1) & 1, abortp)) {
+                    ok = false;
+                    break;
+                }
+                const float4 *dxv = reinterpret_cast<const float4 *>(smem + kOffDX + sdi * 4096 + tl * 32);
+                const float4 dxa = dxv[0], dxb = dxv[1];
+                const float dxs[8] = {dxa.x, dxa.y, dxa.z, dxa.w, dxb.x, dxb.y, dxb.z, dxb.w};
+                const float *dw = reinterpret_cast<const float *>(smem + kOffDD + sdi * F::kDDBytes);
+#pragma unroll
+                for (int G = 0; G < 8; ++G) {
+                    // 8 uses per superblock on a ring of 4: sub-block G uses slot G % 4 for the
+                    // (G / 4)-th time in this superblock, an even count before it
+                    const uint32_t slot = G % kSlots;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), (G / kSlots) & 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const float2 d8 = make_float2(dxs[G], dxs[G]);
+                    const float4 *dwg = reinterpret_cast<const float4 *>(dw + G * 128 + 32 * cq);
+#pragma unroll
+                    for (int hv = 0; hv < 2; ++hv) {
+                        float v[16];
+                        ptx::tmem_ld_32x32b_x16(lane_base + slot * kTN + 32 * cq + 16 * hv, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; ++i4) {
+                            const float4 w4 = dwg[4 * hv + i4];
+                            const float2 s0 = __fmul2_rn(d8, make_float2(w4.x, w4.y));
+                            const float2 s1 = __fmul2_rn(d8, make_float2(w4.z, w4.w));
+                            acc[8 * hv + 2 * i4] =
+                                __ffma2_rn(s0, make_float2(v[4 * i4], v[4 * i4 + 1]), acc[8 * hv + 2 * i4]);
+                            acc[8 * hv + 2 * i4 + 1] =
+                                __ffma2_rn(s1, make_float2(v[4 * i4 + 2], v[4 * i4 + 3]), acc[8 * hv + 2 * i4 + 1]);
+                        }
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[slot]));
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.sd_empty[sdi]));
+                ++sd_it;
+            }
+            if (!ok) break;
+            float res[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                res[2 * i] = acc[i].x;
+                res[2 * i + 1] = acc[i].y;
+            }
+            const TileInfo ti = resolve_tile(a, sg.tile);
+            const int64_t col0 = ti.col0 + 32 * cq;
+            const bool full = sg.s0 == 0 && sg.s1 == a.nsb;
+            if (full) {
+                if (tl < ti.rows) {
+                    float *dst = a.y + int64_t(ti.m0 + tl) * a.n + col0;
+                    if ((a.n % 4 == 0) && (col0 + 32 <= a.n)) {
+#pragma unroll
+                        for (int i4 = 0; i4 < 8; ++i4)
+                            reinterpret_cast<float4 *>(dst)[i4] =
+                                make_float4(res[4 * i4], res[4 * i4 + 1], res[4 * i4 + 2], res[4 * i4 + 3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < a.n) dst[i] = res[i];
+                    }
+                }
+            } else {
+                const int slotidx = seg_i == 0 ? 0 : 1;
+                float4 *dst = reinterpret_cast<float4 *>(a.partial + ((int64_t(blockIdx.x) * 2 + slotidx) * kTM + tl) * kTN +
+                                                         32 * cq);
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4)
+                    dst[i4] = make_float4(res[4 * i4], res[4 * i4 + 1], res[4 * i4 + 2], res[4 * i4 + 3]);
+            }
+            ++seg_i;
+        }
+        }
     }
 
     // ---------------------------------------------------------------- teardown
@@ -575,6 +768,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc(tmem, 512);
     if (tid == 0 && B.abort && a.status) atomicExch(a.status, (int)QMM_ERR_DEVICE);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
+                       const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
+                       TcArgs a) {
+    gemm_tc_body<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, a);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_q80_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
+                       const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
+                       TcArgs a) {
+    gemm_tc_body<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, a);
 }
 
 // q8_1 blocks -> fp16 activation codes [m][k], fp32 d8 [m][k/32], fp16 s tile
@@ -721,7 +928,7 @@ TcLayout tc_layout(int64_t m, int64_t k, int64_t partial_ctas) {
 int64_t gemm_tc_tile_m(int64_t) { return kTM; }
 
 bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
-    return t == QMM_Q4_K && k % 256 == 0 && n > 0 && m > 0 && m <= (int64_t(1) << 30);
+    return (t == QMM_Q4_K || t == QMM_Q8_0) && k % 256 == 0 && n > 0 && m > 0 && m <= (int64_t(1) << 30);
 }
 
 size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m) {
@@ -732,22 +939,24 @@ size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m) {
 
 namespace {
 
-// Launch the GEMM kernel (and the fixup pass when asked) once the maps are built.
+// Launch the GEMM kernel of format T (and the fixup pass when asked) once the maps are built.
+template <int T>
 cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CUtensorMap &tm_dx,
                    const CUtensorMap &tm_w, const TcArgs &args, int ctas, int64_t fixup_tiles, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemAlloc);
+    auto kern = T == QMM_Q4_K ? gemm_tc_q4k_kernel : gemm_tc_q80_kernel;
+    constexpr uint32_t smem = TcMap<T>::kSmemAlloc;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // The setmaxnreg split hands out exactly kThreads x kLaunchRegs registers; a build that
     // launches with fewer registers per thread would leave setmaxnreg.inc waiting forever.
     static int launch_regs = -1;
     if (launch_regs < 0) {
         cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, gemm_tc_q4k_kernel) != cudaSuccess) return cudaErrorInvalidValue;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return cudaErrorInvalidValue;
         launch_regs = fa.numRegs;
     }
     if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    gemm_tc_q4k_kernel<<<ctas, kThreads, kSmemAlloc, st>>>(tm_x, tm_xmin, tm_dx, tm_w, args);
+    kern<<<ctas, kThreads, smem, st>>>(tm_x, tm_xmin, tm_dx, tm_w, args);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (fixup_tiles > 0) {
@@ -789,17 +998,21 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     if (e != cudaSuccess) return e;
 
     CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
-    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) ||
-        !make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, (k / 256) * kQ4KBytes, n, kQ4KBytes, kTN,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
+    const bool q8 = t == QMM_Q8_0;
+    const int64_t row_bytes = (k / 256) * (q8 ? TcFmt<QMM_Q8_0>::kRawRow : TcFmt<QMM_Q4_K>::kRawRow);
+    // Q8_0 rows are read as uint16 so that one superblock's 272 bytes are a box of 136
+    const bool wmap = q8 ? make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, W, row_bytes / 2, n,
+                                       TcFmt<QMM_Q8_0>::kRawRow / 2, kTN, CU_TENSOR_MAP_SWIZZLE_NONE)
+                         : make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, n, kQ4KBytes, kTN,
+                                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) || !wmap) return cudaErrorInvalidValue;
 
     TcArgs args{};
     args.W = static_cast<const uint8_t *>(W);
     args.n = n;
     args.m = m;
     args.k = (int)k;
-    args.row_bytes = (k / 256) * kQ4KBytes;
+    args.row_bytes = row_bytes;
     args.y = y;
     args.partial = reinterpret_cast<float *>(base + L.partial);
     args.status = status;
@@ -808,7 +1021,9 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     args.nwork = p.nwork;
     args.ctas = p.ctas;
     args.stream_k = p.stream_k;
-    return run_tc(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, (p.stream_k && p.fixup) ? p.ntiles : 0, st);
+    const int64_t fixup_tiles = (p.stream_k && p.fixup) ? p.ntiles : 0;
+    return q8 ? run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st)
+              : run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st);
 }
 
 // ---------------------------------------------------------------- expert-grouped mode
@@ -864,7 +1079,7 @@ cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     args.ntiles = ntiles;
     args.bounds = bounds;
     args.perm = perm;
-    return run_tc(tm_x, tm_xmin, tm_dx, tm_w, args, ctas, max_token_tiles * args.tiles_n, st);
+    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, args, ctas, max_token_tiles * args.tiles_n, st);
 }
 
 // ---------------------------------------------------------------- shared with the skinny path

@@ -21,17 +21,17 @@ def _lib():
     qmm.qmm_set_stream_k_mode(0)
 
 
-def run_tc(oracle_mod, n, k, m, sk_mode, seed=0, x=None):
-    W, xr = qmm_synth.make_dense("q4_K", n, k, m, seed=seed)
+def run_tc(oracle_mod, n, k, m, sk_mode, seed=0, x=None, fmt="q4_K"):
+    W, xr = qmm_synth.make_dense(fmt, n, k, m, seed=seed)
     if x is not None:
         xr = x
     xq = oracle_mod.quantize_q8_1(xr)
     qmm.qmm_set_force_path(qmm.PATH_GEMM_TC)
     qmm.qmm_set_stream_k_mode(sk_mode)
     try:
-        ws = torch.empty(max(256, qmm.qmm_workspace_bytes("q4_K", n, k, m)), dtype=torch.uint8, device=DEV)
+        ws = torch.empty(max(256, qmm.qmm_workspace_bytes(fmt, n, k, m)), dtype=torch.uint8, device=DEV)
         y = torch.full((m, n), float("nan"), device=DEV)
-        qmm.qmm_mul_mat(torch.from_numpy(W).to(DEV), "q4_K", n, k, torch.from_numpy(xq).to(DEV), m, y=y,
+        qmm.qmm_mul_mat(torch.from_numpy(W).to(DEV), fmt, n, k, torch.from_numpy(xq).to(DEV), m, y=y,
                         workspace=ws)
         torch.cuda.synchronize()
         status = qmm.qmm_read_device_status(ws)
@@ -39,8 +39,8 @@ def run_tc(oracle_mod, n, k, m, sk_mode, seed=0, x=None):
         qmm.qmm_set_force_path(0)
         qmm.qmm_set_stream_k_mode(0)
     assert status == 0, f"device status {status}"
-    y_ref, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
-    assert_within(y.cpu().numpy(), y_ref, T, f"tc n={n} k={k} m={m} sk={sk_mode}")
+    y_ref, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
+    assert_within(y.cpu().numpy(), y_ref, T, f"tc {fmt} n={n} k={k} m={m} sk={sk_mode}")
 
 
 def test_tc_single_tile_smallest(oracle_mod):
@@ -64,3 +64,29 @@ def test_tc_integer_exactness(oracle_mod):
     n, k, m = 130, 512, 20
     x = np.where(np.random.default_rng(5).random((m, k)) < 0.5, -1.0, 1.0).astype(np.float32)
     run_tc(oracle_mod, n, k, m, 1, seed=9, x=x)
+
+
+# Q8_0 on the tensor cores: int8 codes as exact fp16, a d per 32-block folded with d8
+@pytest.mark.parametrize("n,k,m", [(128, 256, 128), (129, 512, 9), (300, 1024, 130), (77, 2048, 200),
+                                   (1000, 1024, 300)])
+@pytest.mark.parametrize("sk", [1, 2])
+def test_tc_q8_0_parity(oracle_mod, n, k, m, sk):
+    run_tc(oracle_mod, n, k, m, sk, seed=n + k + m, fmt="q8_0")
+
+
+def test_tc_q8_0_extreme_codes(oracle_mod):
+    """Codes -128 and 127 everywhere: the fp16 conversion must keep both ends exact."""
+    n, k, m = 130, 512, 20
+    W, x = qmm_synth.make_dense("q8_0", n, k, m, seed=4)
+    blk = W.reshape(n, k // 32, 34)
+    blk[:, ::2, 2:] = np.uint8(0x80)   # -128
+    blk[:, 1::2, 2:] = np.uint8(0x7f)  # 127
+    xq = oracle_mod.quantize_q8_1(x)
+    qmm.qmm_set_force_path(qmm.PATH_GEMM_TC)
+    try:
+        y = qmm.qmm_mul_mat(torch.from_numpy(W).to(DEV), "q8_0", n, k, torch.from_numpy(xq).to(DEV), m)
+        torch.cuda.synchronize()
+    finally:
+        qmm.qmm_set_force_path(0)
+    y_ref, T = oracle_mod.mul_mat(W, "q8_0", n, k, xq, m)
+    assert_within(y.cpu().numpy(), y_ref, T, "tc q8_0 extreme codes")
