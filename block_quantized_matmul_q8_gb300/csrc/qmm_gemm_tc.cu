@@ -13,23 +13,28 @@
 //
 // Tile: 128 activation rows (MMA M, TMEM lanes) x 128 weight rows (MMA N, TMEM
 // columns); K advances by half a superblock (128 values) per pipeline stage.
+// Each 32-wide sub-block accumulates into its own TMEM slot of 128 columns.  The
+// four slots are handed between the MMA issuer and the epilogue in pairs (one commit,
+// one wait and one release per two sub-blocks, double-buffered): on this part every
+// barrier completion that the lone MMA thread has to observe costs a few hundred
+// cycles during which the tensor pipe idles, so the kernel is built to need as few
+// of them as possible (one per stage, one per pair of sub-blocks).
 // 24 warps, registers split with setmaxnreg (32 / 64 / 96 per thread):
-//   warp 0      TMA: fp16 activation slabs (128-byte swizzle), the per-superblock
-//               s tile (for the min term) and the per-superblock d8 tile.
-//   warp 1      TMEM allocation; one lane issues the MMAs.  Each 32-wide sub-block
-//               accumulates into its own TMEM slot (a ring of 3 slots of 128
-//               columns); once per superblock one more K=16 MMA forms
-//               sum_b s[m,b] * min[n,b] (8 real terms, 8 zeros) in a slot.
-//   warp 2      TMA: the raw Q4_K superblock of the tile's 128 weight rows.
+//   warp 0      TMA: fp16 activation slabs (128-byte swizzle), per superblock the
+//               fp32 d8 tile and, for Q4_K, the fp16 s tile of the min term.
+//   warp 1      TMEM allocation; one lane issues the MMAs.
+//   warp 2      TMA: the raw superblocks of the tile's 128 weight rows.
 //   warps 4-7   unpack: one weight row each, from the raw bytes in shared memory;
-//               nibbles -> fp16 (q * sc) written straight into the 128-byte-swizzled
-//               K-major layout the MMA reads, the 6-bit mins -> fp16 for the min-term
-//               MMA, (d, -dmin) for the epilogue.
+//               weight codes -> fp16 written straight into the 128-byte-swizzled
+//               K-major layout the MMA reads, the 6-bit mins as fp16 for the min-term
+//               MMA, and the per-row fp32 factors of the epilogue (Q4_K: d and -dmin;
+//               Q8_0: d per block).
 //   warps 8-23  epilogue: one activation row (TMEM lane) and 32 weight columns per
-//               thread; per sub-block acc += d8 * slot (fp32 FMA, two columns per
-//               packed fma.rn.f32x2, the slot read in two 16-column halves), per
-//               superblock total += d * acc - dmin * minslot, the total kept in TMEM
-//               columns 384..511.
+//               thread; Q4_K: per sub-block acc += d8 * slot, per superblock
+//               total += d * acc - dmin * minslot, where one more K=16 MMA (a group of
+//               its own) forms minslot = sum_b s[m,b] * m[n,b] (8 real terms, 8 zeros);
+//               Q8_0: total += d8 d * slot.  The total stays in registers for the
+//               whole segment.
 // Work is a flattened stream of (tile, superblock) units split over the CTAs
 // ([MMQ] section "stream-K 的切法"); a tile shared by several CTAs is summed by a
 // separate fixup kernel in CTA order ([MMQ] section "fixup: 部分和的归约"), so no
@@ -55,8 +60,8 @@ namespace {
 constexpr int kTM = 128;  // activation rows per tile
 constexpr int kTN = 128;  // weight rows per tile
 constexpr int kStages = 2;
-constexpr int kMaxSlots = 4;       // accumulator slots of 128 TMEM columns
-constexpr uint32_t kTotCol = 384;  // Q4_K: columns 384..511 hold the running total
+constexpr int kSlots = 4;          // accumulator slots of 128 TMEM columns: all of TMEM
+constexpr int kPair = 2;           // slots handed over per barrier round trip
 constexpr int kThreads = 768;      // 24 warps = 6 warpgroups
 constexpr int kUnpackWarp0 = 4;
 constexpr int kEpiWarp0 = 8;
@@ -70,41 +75,40 @@ static_assert(128 * kRegsProducer + 128 * kRegsUnpack + 32 * kEpiWarps * kRegsEp
               "register split exceeds the launch allocation");
 constexpr int kMaxPartialCtas = 256;
 
-// Per-format constants.  Q4_K: 144-byte superblocks, a min term, 9 slot uses per
-// superblock (8 sub-blocks + the min term), (d, -dmin) per row.  Q8_0: the 256 k values
-// of a step are eight 34-byte blocks, no min term, 8 slot uses, a d per 32-block and row.
-// Each superblock starts at slot 0 (the uses are a multiple of the ring).
+// Per-format constants.  Q4_K: 144-byte superblocks and a min-term MMA per superblock.
+// Q8_0: the 256 k values of a step are eight 34-byte blocks, a d per 32-block and row.
+// kUses counts the sub-block slots of one superblock (whole pairs), kDDBytes the
+// per-row factors the unpack hands to the epilogue, raw_x the raw tensor map's x
+// coordinate of superblock sb (in its elements).
 template <int T> struct TcFmt;
 template <> struct TcFmt<QMM_Q4_K> {
     static constexpr uint32_t kRawRow = kQ4KBytes;  // raw bytes of one weight row per 256 k
-    static constexpr uint32_t kRawElem = 1;         // element size of the raw tensor map
     static constexpr bool kMin = true;
-    static constexpr int kSlots = 3;
-    static constexpr int kUses = 9;
+    static constexpr int kUses = 8;
     static constexpr uint32_t kDDBytes = 2 * 128 * 4;  // d[128], -dmin[128]
+    static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * kQ4KBytes); }
 };
 template <> struct TcFmt<QMM_Q8_0> {
     static constexpr uint32_t kRawRow = 8 * kQ80Bytes;  // 272
-    static constexpr uint32_t kRawElem = 2;             // 136 uint16 per row: a box dimension <= 256
     static constexpr bool kMin = false;
-    static constexpr int kSlots = 4;
     static constexpr int kUses = 8;
     static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
+    static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * 136); }
 };
 
 // dynamic shared memory map (offsets from a 1024-aligned base)
 constexpr uint32_t kSlabBytes = 128 * 128;  // 128 rows x 64 fp16
 template <int T> struct TcMap {
     using F = TcFmt<T>;
-    static_assert(F::kUses % F::kSlots == 0 && F::kSlots <= kMaxSlots, "slot ring");
-    static constexpr uint32_t kOffX = 0;                                    // [stage][2 slabs]
-    static constexpr uint32_t kOffW = kOffX + kStages * 2 * kSlabBytes;     // [stage][2 slabs]
+    static_assert(F::kUses % (2 * kPair) == 0, "a superblock must start on the first pair of the ring");
+    static constexpr uint32_t kOffX = 0;                                 // [stage][2 slabs]
+    static constexpr uint32_t kOffW = kOffX + kStages * 2 * kSlabBytes;  // [stage][2 slabs]
     static constexpr uint32_t kMinBytes = F::kMin ? kStages * 4096 : 0;
     static constexpr uint32_t kOffXmin = kOffW + kStages * 2 * kSlabBytes;  // [stage][128][32 B]
     static constexpr uint32_t kOffWmin = kOffXmin + kMinBytes;              // [stage][128][32 B]
-    static constexpr uint32_t kOffDX = kOffWmin + kMinBytes;                // [2][128][8] fp32
+    static constexpr uint32_t kOffDX = kOffWmin + kMinBytes;                // [2][128][8] fp32 d8
     static constexpr uint32_t kOffDD = kOffDX + 2 * 4096;                   // [2][kDDBytes]
-    static constexpr uint32_t kRawBytes = 128 * F::kRawRow;                 // raw weights of 128 rows
+    static constexpr uint32_t kRawBytes = 128 * F::kRawRow;              // raw weights of 128 rows
     static constexpr uint32_t kOffRaw = (kOffDD + 2 * F::kDDBytes + 1023) & ~1023u;
     static constexpr uint32_t kSmemAlloc = kOffRaw + 2 * kRawBytes + 1024;
     static_assert(kSmemAlloc <= 227 * 1024, "shared memory map exceeds the per-CTA limit");
@@ -156,9 +160,13 @@ __device__ __forceinline__ TileInfo resolve_tile(const TcArgs &a, int64_t t) {
     return ti;
 }
 
+// Stage barriers: st_full completes when the activation slabs have landed (TMA
+// transaction bytes) and all 128 unpack threads have written the weight slabs;
+// st_empty when the MMAs reading the stage are done (TMA producer and unpack both wait
+// on it).  sd_full / sd_empty guard the per-superblock scale tiles the same way.
 struct Barriers {
-    uint64_t x_full[kStages], x_empty[kStages], w_full[kStages], w_empty[kStages];
-    uint64_t acc_full[kMaxSlots], acc_empty[kMaxSlots];
+    uint64_t st_full[kStages], st_empty[kStages];
+    uint64_t acc_full[kSlots / kPair], acc_empty[kSlots / kPair];
     uint64_t sd_full[2], sd_empty[2];
     uint64_t raw_full[2], raw_empty[2];
     uint64_t done;
@@ -189,15 +197,46 @@ __device__ __forceinline__ bool next_seg(const TcArgs &a, int64_t &u, int64_t en
     return true;
 }
 
+// One epilogue thread's 32 results of a segment: a whole tile goes to y, part of a
+// tile to this CTA's partial slot (0 for its first segment, 1 for its last).
+__device__ __forceinline__ void store_segment(const TcArgs &a, const Seg &sg, int seg_i, int tl, int cq,
+                                              const float2 (&tot)[16]) {
+    const TileInfo ti = resolve_tile(a, sg.tile);
+    const int64_t col0 = ti.col0 + 32 * cq;
+    if (sg.s0 == 0 && sg.s1 == a.nsb) {
+        if (tl >= ti.rows) return;
+        const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
+        float *dst = a.y + yrow * a.n + col0;
+        if ((a.n % 4 == 0) && (col0 + 32 <= a.n)) {
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4)
+                reinterpret_cast<float4 *>(dst)[i4] =
+                    make_float4(tot[2 * i4].x, tot[2 * i4].y, tot[2 * i4 + 1].x, tot[2 * i4 + 1].y);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (col0 + 2 * i < a.n) dst[2 * i] = tot[i].x;
+                if (col0 + 2 * i + 1 < a.n) dst[2 * i + 1] = tot[i].y;
+            }
+        }
+    } else {
+        const int slotidx = seg_i == 0 ? 0 : 1;
+        float4 *dst =
+            reinterpret_cast<float4 *>(a.partial + ((int64_t(blockIdx.x) * 2 + slotidx) * kTM + tl) * kTN + 32 * cq);
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4)
+            dst[i4] = make_float4(tot[2 * i4].x, tot[2 * i4].y, tot[2 * i4 + 1].x, tot[2 * i4 + 1].y);
+    }
+}
 
 template <int T>
 __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin,
                                              const CUtensorMap &tm_dx, const CUtensorMap &tm_w, TcArgs a) {
     using F = TcFmt<T>;
     using Mp = TcMap<T>;
-    constexpr int kSlots = F::kSlots;
     constexpr uint32_t kOffX = Mp::kOffX, kOffW = Mp::kOffW, kOffXmin = Mp::kOffXmin, kOffWmin = Mp::kOffWmin;
     constexpr uint32_t kOffDX = Mp::kOffDX, kOffDD = Mp::kOffDD, kOffRaw = Mp::kOffRaw, kRawBytes = Mp::kRawBytes;
+    constexpr int kGroups = F::kUses / kPair;  // slot pairs per superblock (the min group comes on top)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ Barriers B;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -208,20 +247,16 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
     if (tid == 0) {
         B.abort = 0;
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&B.x_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&B.x_empty[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&B.w_full[s]), 128);
-            ptx::mbar_init(ptx::smem_u32(&B.w_empty[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&B.st_full[s]), 1 + 128);
+            ptx::mbar_init(ptx::smem_u32(&B.st_empty[s]), 1);
         }
-        for (int s = 0; s < kSlots; ++s) {
+        for (int s = 0; s < kSlots / kPair; ++s) {
             ptx::mbar_init(ptx::smem_u32(&B.acc_full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&B.acc_empty[s]), kEpiWarps);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(ptx::smem_u32(&B.raw_full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&B.raw_empty[s]), 128);
-        }
-        for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(ptx::smem_u32(&B.sd_full[s]), 1 + 128);
             ptx::mbar_init(ptx::smem_u32(&B.sd_empty[s]), kEpiWarps);
         }
@@ -261,16 +296,16 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         break;
                     }
                     const uint32_t sdbar = ptx::smem_u32(&B.sd_full[sdi]);
-                    ptx::mbar_arrive_expect_tx(sdbar, 128 * 8 * 4);
+                    ptx::mbar_arrive_expect_tx(sdbar, 4096);
                     ptx::tma_load_2d(sbase + kOffDX + sdi * 4096, &tm_dx, (int)(8 * sb), m0, sdbar);
                     ++sd_it;
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t st = x_it % kStages;
-                        if (!ptx::mbar_wait(ptx::smem_u32(&B.x_empty[st]), ((x_it / kStages) & 1) ^ 1, abortp)) {
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((x_it / kStages) & 1) ^ 1, abortp)) {
                             ok = false;
                             break;
                         }
-                        const uint32_t bar = ptx::smem_u32(&B.x_full[st]);
+                        const uint32_t bar = ptx::smem_u32(&B.st_full[st]);
                         ptx::mbar_arrive_expect_tx(bar, 2 * kSlabBytes + ((F::kMin && h) ? 4096u : 0u));
                         const int kx = (int)(256 * sb + 128 * h);
                         ptx::tma_load_2d(sbase + kOffX + st * 2 * kSlabBytes, &tm_x, kx, m0, bar);
@@ -284,61 +319,67 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
             // drain: every armed copy must have landed before the CTA may exit
             int dummy = 0;
             for (uint32_t i = (x_it > kStages ? x_it - kStages : 0); i < x_it; ++i)
-                ptx::mbar_wait(ptx::smem_u32(&B.x_full[i % kStages]), (i / kStages) & 1, &dummy);
+                ptx::mbar_wait(ptx::smem_u32(&B.st_full[i % kStages]), (i / kStages) & 1, &dummy);
             for (uint32_t i = (sd_it > 2 ? sd_it - 2 : 0); i < sd_it; ++i)
                 ptx::mbar_wait(ptx::smem_u32(&B.sd_full[i & 1]), (i >> 1) & 1, &dummy);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Per stage: one wait for the stage, then per pair of slots one wait for the
+        // pair's release, the MMAs of both sub-blocks and one commit; for Q4_K the min
+        // MMA follows the last pair as a group of its own.
         regs_dec<kRegsProducer>();
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f16_f32(kTM, kTN);
             int64_t u = ubeg;
             Seg sg;
-            uint32_t x_it = 0, g = 0;
+            uint32_t x_it = 0, gq = 0;
             bool ok = true;
             while (ok && next_seg(a, u, uend, sg)) {
                 for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                     for (int h = 0; ok && h < 2; ++h) {
                         const uint32_t st = x_it % kStages, par = (x_it / kStages) & 1;
-                        if (!ptx::mbar_wait(ptx::smem_u32(&B.x_full[st]), par, abortp) ||
-                            !ptx::mbar_wait(ptx::smem_u32(&B.w_full[st]), par, abortp)) {
+                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.st_full[st]), par, abortp)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
                         const uint32_t xa = sbase + kOffX + st * 2 * kSlabBytes;
                         const uint32_t wa = sbase + kOffW + st * 2 * kSlabBytes;
-                        for (int q = 0; q < 4; ++q) {
-                            const uint32_t slot = g % kSlots;
-                            if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_empty[slot]), ((g / kSlots) & 1) ^ 1, abortp)) {
+                        for (int q = 0; q < kGroups / 2; ++q) {  // the pairs of this half
+                            const uint32_t e = gq & 1;
+                            if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_empty[e]), ((gq >> 1) & 1) ^ 1, abortp)) {
                                 ok = false;
                                 break;
                             }
                             ptx::tc_fence_after();
-                            const uint32_t slab = (q >> 1) * kSlabBytes;
-                            for (int t = 0; t < 2; ++t) {
-                                const uint32_t koff = ((q & 1) * 2 + t) * 32;  // K16 step inside the 128-byte row
-                                ptx::mma_f16(tmem + slot * kTN, ptx::smem_desc(xa + slab + koff, 1024, 2),
-                                             ptx::smem_desc(wa + slab + koff, 1024, 2), idesc, t);
+#pragma unroll
+                            for (int b2 = 0; b2 < kPair; ++b2) {
+                                const uint32_t d = tmem + (kPair * e + b2) * kTN;
+#pragma unroll
+                                for (int t = 0; t < 2; ++t) {  // two K16 steps per 32-wide sub-block
+                                    const int step = (q * kPair + b2) * 2 + t;  // slab step/4, 32 bytes each
+                                    const uint32_t off = (step >> 2) * kSlabBytes + (step & 3) * 32;
+                                    ptx::mma_f16(d, ptx::smem_desc(xa + off, 1024, 2), ptx::smem_desc(wa + off, 1024, 2),
+                                                 idesc, t);
+                                }
                             }
-                            ptx::mma_commit(ptx::smem_u32(&B.acc_full[slot]));
-                            ++g;
+                            ptx::mma_commit(ptx::smem_u32(&B.acc_full[e]));
+                            ++gq;
                         }
-                        if (F::kMin && ok && h == 1) {
-                            const uint32_t slot = g % kSlots;
-                            if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_empty[slot]), ((g / kSlots) & 1) ^ 1, abortp)) {
+                        if (F::kMin && ok && h == 1) {  // the min term: a group of one slot
+                            const uint32_t e = gq & 1;
+                            if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_empty[e]), ((gq >> 1) & 1) ^ 1, abortp)) {
                                 ok = false;
                                 break;
                             }
                             ptx::tc_fence_after();
-                            ptx::mma_f16(tmem + slot * kTN, ptx::smem_desc(sbase + kOffXmin + st * 4096, 256, 6),
+                            ptx::mma_f16(tmem + kPair * e * kTN, ptx::smem_desc(sbase + kOffXmin + st * 4096, 256, 6),
                                          ptx::smem_desc(sbase + kOffWmin + st * 4096, 256, 6), idesc, 0);
-                            ptx::mma_commit(ptx::smem_u32(&B.acc_full[slot]));
-                            ++g;
+                            ptx::mma_commit(ptx::smem_u32(&B.acc_full[e]));
+                            ++gq;
                         }
-                        ptx::mma_commit(ptx::smem_u32(&B.x_empty[st]));
-                        ptx::mma_commit(ptx::smem_u32(&B.w_empty[st]));
+                        ptx::mma_commit(ptx::smem_u32(&B.st_empty[st]));
                         ++x_it;
                     }
                 }
@@ -350,9 +391,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ raw weight TMA
-        // The raw Q4_K superblock of the tile's 128 weight rows, one per superblock,
-        // into a 2-deep ring; independent of the activation stream so neither waits on
-        // the other.
+        // The raw superblock of the tile's 128 weight rows, one per superblock, into a
+        // 2-deep ring; independent of the activation stream so neither waits on the other.
         regs_dec<kRegsProducer>();
         if (lane == 0) {
             ptx::prefetch_tmap(&tm_w);
@@ -370,8 +410,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     }
                     const uint32_t rbar = ptx::smem_u32(&B.raw_full[ri]);
                     ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
-                    ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, (int)(sb * (F::kRawRow / F::kRawElem)),
-                                     n0, rbar);
+                    ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, F::raw_x(sb), n0, rbar);
                     ++r_it;
                 }
             }
@@ -394,25 +433,22 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         while (ok && next_seg(a, u, uend, sg)) {
             for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                 const uint32_t ri = sb_it & 1;
-                if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_full[ri]), (sb_it >> 1) & 1, abortp)) {
+                if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_full[ri]), (sb_it >> 1) & 1, abortp) ||
+                    !ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[ri]), ((sb_it >> 1) & 1) ^ 1, abortp)) {
                     ok = false;
                     break;
                 }
                 const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + r * F::kRawRow;
+                float *dd = reinterpret_cast<float *>(smem + kOffDD + ri * F::kDDBytes);
                 if constexpr (T == QMM_Q4_K) {
                 const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
                 // (d, -dmin) for the epilogue
-                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[ri]), ((sb_it >> 1) & 1) ^ 1, abortp)) {
-                    ok = false;
-                    break;
-                }
-                float *dd = reinterpret_cast<float *>(smem + kOffDD + ri * 1024);
                 dd[r] = half_lo(hd.x);
                 dd[128 + r] = -half_hi(hd.x);
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t st = w_it % kStages;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.w_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
                         ok = false;
                         break;
                     }
@@ -452,25 +488,20 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         *reinterpret_cast<uint4 *>(mdst + ((1 ^ sw) << 4)) = make_uint4(0, 0, 0, 0);
                     }
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(ptx::smem_u32(&B.w_full[st]));
+                    ptx::mbar_arrive(ptx::smem_u32(&B.st_full[st]));
                     ++w_it;
                 }
                 } else {
                 // Q8_0: the row's 256 k values are 8 blocks of {fp16 d, int8 q[32]}, block b at
                 // byte 34b.  The d of every block goes to the epilogue; the codes become
                 // exact fp16 integers: (q ^ 0x80) | 0x6400 is the fp16 1024 + q + 128.
-                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[ri]), ((sb_it >> 1) & 1) ^ 1, abortp)) {
-                    ok = false;
-                    break;
-                }
-                float *dw = reinterpret_cast<float *>(smem + kOffDD + ri * F::kDDBytes);
 #pragma unroll
-                for (int b = 0; b < 8; ++b) dw[b * 128 + r] = __half2float(*reinterpret_cast<const __half *>(blk + 34 * b));
+                for (int b = 0; b < 8; ++b) dd[b * 128 + r] = __half2float(*reinterpret_cast<const __half *>(blk + 34 * b));
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 const __half2 bias = __float2half2_rn(-1152.f);
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t st = w_it % kStages;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.w_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
                         ok = false;
                         break;
                     }
@@ -512,7 +543,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         }
                     }
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(ptx::smem_u32(&B.w_full[st]));
+                    ptx::mbar_arrive(ptx::smem_u32(&B.st_full[st]));
                     ++w_it;
                 }
                 }
@@ -523,23 +554,24 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
     } else {
         // ------------------------------------------------------------ epilogue
         // 16 warps: warp w reads TMEM lanes 32*(w%4).. (one activation row per thread)
-        // and one quarter of the 128 columns (32 weight rows).  Per superblock: 8 slots
-        // fold into acc (fp32), then the min slot and the running total (TMEM columns
-        // 384..511) are updated in two 16-column halves.
+        // and one quarter of the 128 columns (32 weight rows).  Slots arrive in pairs;
+        // both are read (16 columns at a time) and the pair is handed back before the
+        // next pair is awaited.  The segment's total stays in registers.
         regs_inc<kRegsEpilogue>();
-        if constexpr (T == QMM_Q4_K) {
-        const int ew = warp - kEpiWarp0;       // 0..15
-        const int cq = ew >> 2;                // column quarter: columns 32cq .. 32cq+31
-        const int qd = warp & 3;               // TMEM lane quarter this warp may access
-        const int tl = 32 * qd + lane;         // activation row within the tile
+        const int ew = warp - kEpiWarp0;  // 0..15
+        const int cq = ew >> 2;           // column quarter: columns 32cq .. 32cq+31
+        const int qd = warp & 3;          // TMEM lane quarter this warp may access
+        const int tl = 32 * qd + lane;    // activation row within the tile
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         int64_t u = ubeg;
         Seg sg;
-        uint32_t g = 0, sd_it = 0;
+        uint32_t ge = 0, sd_it = 0;
         int seg_i = 0;
         bool ok = true;
         while (ok && next_seg(a, u, uend, sg)) {
-            bool first = true;
+            float2 tot[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) tot[i] = make_float2(0.f, 0.f);
             for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                 const uint32_t sdi = sd_it & 1;
                 if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_full[sdi]), (sd_it >> 1) & 1, abortp)) {
@@ -549,216 +581,116 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 // the row's 8 d8 values, two 16-byte reads (scalar reads at the 32-byte row
                 // stride would put 8 lanes on each bank)
                 const float4 *dxv = reinterpret_cast<const float4 *>(smem + kOffDX + sdi * 4096 + tl * 32);
-                const float4 dxa = dxv[0], dxb = dxv[1];
-                const float dxs[8] = {dxa.x, dxa.y, dxa.z, dxa.w, dxb.x, dxb.y, dxb.z, dxb.w};
-                const float4 *ddd = reinterpret_cast<const float4 *>(smem + kOffDD + sdi * 1024) + 8 * cq;
-                const float4 *ddm = reinterpret_cast<const float4 *>(smem + kOffDD + sdi * 1024 + 512) + 8 * cq;
-                // g is a multiple of 9 here (9 slot uses per superblock, kSlots = 3), so
-                // sub-block G always uses slot G % 3, with parity ph ^ (G / 3 & 1)
-                const uint32_t ph = (g / kSlots) & 1;
-                float2 acc[16];  // columns 2i, 2i+1 of this thread's 32
+                const float *dd = reinterpret_cast<const float *>(smem + kOffDD + sdi * F::kDDBytes);
+                if constexpr (F::kMin) {
+                    float2 acc[16];  // columns 2i, 2i+1 of this thread's 32
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = make_float2(0.f, 0.f);
+                    for (int i = 0; i < 16; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int G = 0; G < 8; ++G) {
-                    const uint32_t slot = G % kSlots;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), ph ^ ((G / kSlots) & 1), abortp)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const float2 dg = make_float2(dxs[G], dxs[G]);
-#pragma unroll
-                    for (int hv = 0; hv < 2; ++hv) {  // two 16-column halves: 16 registers live, not 32
-                        float v[16];
-                        ptx::tmem_ld_32x32b_x16(lane_base + slot * kTN + 32 * cq + 16 * hv, v);
-                        ptx::tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            acc[8 * hv + i] = __ffma2_rn(dg, make_float2(v[2 * i], v[2 * i + 1]), acc[8 * hv + i]);
-                    }
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[slot]));
-                }
-                if (!ok) break;
-                // min slot and running total
-                const uint32_t slot = 8 % kSlots;
-                if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), ph ^ ((8 / kSlots) & 1), abortp)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float vm[16], t[16];
-                    ptx::tmem_ld_32x32b_x16(lane_base + slot * kTN + 32 * cq + 16 * hh, vm);
-                    if (!first) {
-                        if (hh == 0) ptx::tmem_st_wait();  // the previous superblock's stores
-                        ptx::tmem_ld_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
-                    }
-                    ptx::tmem_ld_wait();
-                    // t = m * vm + (d * acc + t), two columns per packed fma
-#pragma unroll
-                    for (int i4 = 0; i4 < 4; ++i4) {
-                        const float4 d4 = ddd[4 * hh + i4], m4 = ddm[4 * hh + i4];
-#pragma unroll
-                        for (int e = 0; e < 4; e += 2) {
-                            const int i = 4 * i4 + e;
-                            const float2 dv = e == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);
-                            const float2 mv = e == 0 ? make_float2(m4.x, m4.y) : make_float2(m4.z, m4.w);
-                            const float2 base = first ? make_float2(0.f, 0.f) : make_float2(t[i], t[i + 1]);
-                            const float2 r = __ffma2_rn(mv, make_float2(vm[i], vm[i + 1]),
-                                                        __ffma2_rn(dv, acc[8 * hh + i / 2], base));
-                            t[i] = r.x;
-                            t[i + 1] = r.y;
+                    for (int j = 0; j < kGroups; ++j) {
+                        const uint32_t e = ge & 1;
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                            ok = false;
+                            break;
                         }
+                        ptx::tc_fence_after();
+                        const float4 d4 = dxv[j >> 1];
+                        const float d8a = (j & 1) ? d4.z : d4.x, d8b = (j & 1) ? d4.w : d4.y;
+#pragma unroll
+                        for (int b2 = 0; b2 < kPair; ++b2) {
+                            const float2 dg = b2 ? make_float2(d8b, d8b) : make_float2(d8a, d8a);
+#pragma unroll
+                            for (int hv = 0; hv < 2; ++hv) {
+                                float v[16];
+                                ptx::tmem_ld_32x32b_x16(lane_base + (kPair * e + b2) * kTN + 32 * cq + 16 * hv, v);
+                                ptx::tmem_ld_wait();
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    acc[8 * hv + i] = __ffma2_rn(dg, make_float2(v[2 * i], v[2 * i + 1]), acc[8 * hv + i]);
+                            }
+                        }
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[e]));
+                        ++ge;
                     }
-                    ptx::tmem_st_32x32b_x16(lane_base + kTotCol + 32 * cq + 16 * hh, t);
-                }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[slot]));
-                    ptx::mbar_arrive(ptx::smem_u32(&B.sd_empty[sdi]));
-                }
-                g += 9;
-                ++sd_it;
-                first = false;
-            }
-            if (!ok) break;
-            // write the segment's result: whole tile -> y, part of a tile -> this CTA's partial slot
-            float res[32];
-            ptx::tmem_st_wait();
-            ptx::tmem_ld_32x32b_x32(lane_base + kTotCol + 32 * cq, res);
-            ptx::tmem_ld_wait();
-            const TileInfo ti = resolve_tile(a, sg.tile);
-            const int64_t col0 = ti.col0 + 32 * cq;
-            const bool full = sg.s0 == 0 && sg.s1 == a.nsb;
-            if (full) {
-                if (tl < ti.rows) {
-                    const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
-                    float *dst = a.y + yrow * a.n + col0;
-                    if ((a.n % 4 == 0) && (col0 + 32 <= a.n)) {
-#pragma unroll
-                        for (int i4 = 0; i4 < 8; ++i4)
-                            reinterpret_cast<float4 *>(dst)[i4] =
-                                make_float4(res[4 * i4], res[4 * i4 + 1], res[4 * i4 + 2], res[4 * i4 + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (col0 + i < a.n) dst[i] = res[i];
-                    }
-                }
-            } else {
-                const int slotidx = seg_i == 0 ? 0 : 1;
-                float4 *dst = reinterpret_cast<float4 *>(a.partial + ((int64_t(blockIdx.x) * 2 + slotidx) * kTM + tl) * kTN +
-                                                         32 * cq);
-#pragma unroll
-                for (int i4 = 0; i4 < 8; ++i4)
-                    dst[i4] = make_float4(res[4 * i4], res[4 * i4 + 1], res[4 * i4 + 2], res[4 * i4 + 3]);
-            }
-            ++seg_i;
-        }
-        } else {
-        // Q8_0: per sub-block acc += (d8 * d_w) * slot, two columns per packed product and
-        // fma; there is no per-superblock scale, so the sums stay in registers for the
-        // whole segment and no TMEM total is kept.
-        const int ew = warp - kEpiWarp0;
-        const int cq = ew >> 2;
-        const int qd = warp & 3;
-        const int tl = 32 * qd + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
-        int64_t u = ubeg;
-        Seg sg;
-        uint32_t sd_it = 0;
-        int seg_i = 0;
-        bool ok = true;
-        while (ok && next_seg(a, u, uend, sg)) {
-            float2 acc[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = make_float2(0.f, 0.f);
-            for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
-                const uint32_t sdi = sd_it & 1;
-                if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_full[sdi]), (sd_it >> 1) & 1, abortp)) {
-                    ok = false;
-                    break;
-                }
-                const float4 *dxv = reinterpret_cast<const float4 *>(smem + kOffDX + sdi * 4096 + tl * 32);
-                const float4 dxa = dxv[0], dxb = dxv[1];
-                const float dxs[8] = {dxa.x, dxa.y, dxa.z, dxa.w, dxb.x, dxb.y, dxb.z, dxb.w};
-                const float *dw = reinterpret_cast<const float *>(smem + kOffDD + sdi * F::kDDBytes);
-#pragma unroll
-                for (int G = 0; G < 8; ++G) {
-                    // 8 uses per superblock on a ring of 4: sub-block G uses slot G % 4 for the
-                    // (G / 4)-th time in this superblock, an even count before it
-                    const uint32_t slot = G % kSlots;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[slot]), (G / kSlots) & 1, abortp)) {
+                    if (!ok) break;
+                    // the min group: total += d * acc + (-dmin) * minslot
+                    const uint32_t e = ge & 1;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const float2 d8 = make_float2(dxs[G], dxs[G]);
-                    const float4 *dwg = reinterpret_cast<const float4 *>(dw + G * 128 + 32 * cq);
+                    const float4 *ddd = reinterpret_cast<const float4 *>(dd) + 8 * cq;
+                    const float4 *ddm = reinterpret_cast<const float4 *>(dd + 128) + 8 * cq;
 #pragma unroll
                     for (int hv = 0; hv < 2; ++hv) {
-                        float v[16];
-                        ptx::tmem_ld_32x32b_x16(lane_base + slot * kTN + 32 * cq + 16 * hv, v);
+                        float vm[16];
+                        ptx::tmem_ld_32x32b_x16(lane_base + kPair * e * kTN + 32 * cq + 16 * hv, vm);
                         ptx::tmem_ld_wait();
 #pragma unroll
                         for (int i4 = 0; i4 < 4; ++i4) {
-                            const float4 w4 = dwg[4 * hv + i4];
-                            const float2 s0 = __fmul2_rn(d8, make_float2(w4.x, w4.y));
-                            const float2 s1 = __fmul2_rn(d8, make_float2(w4.z, w4.w));
-                            acc[8 * hv + 2 * i4] =
-                                __ffma2_rn(s0, make_float2(v[4 * i4], v[4 * i4 + 1]), acc[8 * hv + 2 * i4]);
-                            acc[8 * hv + 2 * i4 + 1] =
-                                __ffma2_rn(s1, make_float2(v[4 * i4 + 2], v[4 * i4 + 3]), acc[8 * hv + 2 * i4 + 1]);
+                            const float4 d4 = ddd[4 * hv + i4], m4 = ddm[4 * hv + i4];
+                            const int i = 8 * hv + 2 * i4;
+                            tot[i] = __ffma2_rn(make_float2(m4.x, m4.y), make_float2(vm[4 * i4], vm[4 * i4 + 1]),
+                                                __ffma2_rn(make_float2(d4.x, d4.y), acc[i], tot[i]));
+                            tot[i + 1] = __ffma2_rn(make_float2(m4.z, m4.w), make_float2(vm[4 * i4 + 2], vm[4 * i4 + 3]),
+                                                    __ffma2_rn(make_float2(d4.z, d4.w), acc[i + 1], tot[i + 1]));
                         }
                     }
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[slot]));
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[e]));
+                    ++ge;
+                } else {
+                    // Q8_0: total += (d8 * d_w) * slot, two columns per packed product and fma
+#pragma unroll
+                    for (int j = 0; j < kGroups; ++j) {
+                        const uint32_t e = ge & 1;
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const float4 d4 = dxv[j >> 1];
+#pragma unroll
+                        for (int b2 = 0; b2 < kPair; ++b2) {
+                            const int G = kPair * j + b2;
+                            const float dgs = (j & 1) ? (b2 ? d4.w : d4.z) : (b2 ? d4.y : d4.x);
+                            const float2 d8 = make_float2(dgs, dgs);
+                            const float4 *dwg = reinterpret_cast<const float4 *>(dd + G * 128 + 32 * cq);
+#pragma unroll
+                            for (int hv = 0; hv < 2; ++hv) {
+                                float v[16];
+                                ptx::tmem_ld_32x32b_x16(lane_base + (kPair * e + b2) * kTN + 32 * cq + 16 * hv, v);
+                                ptx::tmem_ld_wait();
+#pragma unroll
+                                for (int i4 = 0; i4 < 4; ++i4) {
+                                    const float4 w4 = dwg[4 * hv + i4];
+                                    const float2 s0 = __fmul2_rn(d8, make_float2(w4.x, w4.y));
+                                    const float2 s1 = __fmul2_rn(d8, make_float2(w4.z, w4.w));
+                                    tot[8 * hv + 2 * i4] =
+                                        __ffma2_rn(s0, make_float2(v[4 * i4], v[4 * i4 + 1]), tot[8 * hv + 2 * i4]);
+                                    tot[8 * hv + 2 * i4 + 1] =
+                                        __ffma2_rn(s1, make_float2(v[4 * i4 + 2], v[4 * i4 + 3]), tot[8 * hv + 2 * i4 + 1]);
+                                }
+                            }
+                        }
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[e]));
+                        ++ge;
+                    }
+                    if (!ok) break;
                 }
-                if (!ok) break;
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.sd_empty[sdi]));
                 ++sd_it;
             }
             if (!ok) break;
-            float res[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                res[2 * i] = acc[i].x;
-                res[2 * i + 1] = acc[i].y;
-            }
-            const TileInfo ti = resolve_tile(a, sg.tile);
-            const int64_t col0 = ti.col0 + 32 * cq;
-            const bool full = sg.s0 == 0 && sg.s1 == a.nsb;
-            if (full) {
-                if (tl < ti.rows) {
-                    float *dst = a.y + int64_t(ti.m0 + tl) * a.n + col0;
-                    if ((a.n % 4 == 0) && (col0 + 32 <= a.n)) {
-#pragma unroll
-                        for (int i4 = 0; i4 < 8; ++i4)
-                            reinterpret_cast<float4 *>(dst)[i4] =
-                                make_float4(res[4 * i4], res[4 * i4 + 1], res[4 * i4 + 2], res[4 * i4 + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (col0 + i < a.n) dst[i] = res[i];
-                    }
-                }
-            } else {
-                const int slotidx = seg_i == 0 ? 0 : 1;
-                float4 *dst = reinterpret_cast<float4 *>(a.partial + ((int64_t(blockIdx.x) * 2 + slotidx) * kTM + tl) * kTN +
-                                                         32 * cq);
-#pragma unroll
-                for (int i4 = 0; i4 < 8; ++i4)
-                    dst[i4] = make_float4(res[4 * i4], res[4 * i4 + 1], res[4 * i4 + 2], res[4 * i4 + 3]);
-            }
+            store_segment(a, sg, seg_i, tl, cq, tot);
             ++seg_i;
-        }
         }
     }
 
