@@ -45,6 +45,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "qmm_common.cuh"
@@ -83,17 +84,43 @@ constexpr int kMaxPartialCtas = 256;
 template <int T> struct TcFmt;
 template <> struct TcFmt<QMM_Q4_K> {
     static constexpr uint32_t kRawRow = kQ4KBytes;  // raw bytes of one weight row per 256 k
+    static constexpr uint32_t kRawBuf = 128 * kRawRow;  // one raw buffer: the tile's 128 rows
     static constexpr bool kMin = true;
     static constexpr int kUses = 8;
+    static constexpr int kSub = 32;  // k values per slot
     static constexpr uint32_t kDDBytes = 2 * 128 * 4;  // d[128], -dmin[128]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * kQ4KBytes); }
 };
 template <> struct TcFmt<QMM_Q8_0> {
     static constexpr uint32_t kRawRow = 8 * kQ80Bytes;  // 272
+    static constexpr uint32_t kRawBuf = 128 * kRawRow;
     static constexpr bool kMin = false;
     static constexpr int kUses = 8;
+    static constexpr int kSub = 32;
     static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * 136); }
+};
+// Q6_K: a row is 210 bytes per superblock, so neither a row (210 * k/256 bytes) nor a
+// superblock is a whole number of 16-byte units and the rows cannot be a 2-D tensor map.
+// The raw warp instead issues one 224-byte bulk copy per row: the window starting at the
+// 16-byte boundary at or below the row's superblock (offset <= 14 inside it, the bytes
+// after it belong to the next row).  With n a multiple of 8 the weight tensor ends on a
+// 16-byte boundary, so the last row's last window ends exactly there.  Windows sit 240
+// bytes apart in shared memory: 8 consecutive rows start on different banks.  One slot
+// per 16-wide sub-block, since each has its own int8 scale: the weight operand is the
+// bare 6-bit code (exact), and d * sc joins the fold.
+template <> struct TcFmt<QMM_Q6_K> {
+    static constexpr uint32_t kRawRow = 240;    // shared-memory stride of the row windows
+    static constexpr uint32_t kCopyBytes = 224;  // window bytes per row
+    static constexpr uint32_t kRawBuf = 128 * kRawRow;
+    static constexpr bool kMin = false;
+    static constexpr int kUses = 16;
+    static constexpr int kSub = 16;
+    static constexpr uint32_t kDDBytes = 16 * 128 * 4;  // d * sc[16 sub-blocks][128 rows]
+    // byte offset of superblock sb of weight row `row` from the start of W
+    static __device__ __forceinline__ int64_t pos(int64_t row, int64_t sb, int64_t row_bytes) {
+        return row * row_bytes + sb * kQ6KBytes;
+    }
 };
 
 // dynamic shared memory map (offsets from a 1024-aligned base)
@@ -101,6 +128,7 @@ constexpr uint32_t kSlabBytes = 128 * 128;  // 128 rows x 64 fp16
 template <int T> struct TcMap {
     using F = TcFmt<T>;
     static_assert(F::kUses % (2 * kPair) == 0, "a superblock must start on the first pair of the ring");
+    static_assert(F::kRawBuf % 16 == 0, "raw buffers must keep TMA destinations 16-byte aligned");
     static constexpr uint32_t kOffX = 0;                                 // [stage][2 slabs]
     static constexpr uint32_t kOffW = kOffX + kStages * 2 * kSlabBytes;  // [stage][2 slabs]
     static constexpr uint32_t kMinBytes = F::kMin ? kStages * 4096 : 0;
@@ -108,7 +136,7 @@ template <int T> struct TcMap {
     static constexpr uint32_t kOffWmin = kOffXmin + kMinBytes;              // [stage][128][32 B]
     static constexpr uint32_t kOffDX = kOffWmin + kMinBytes;                // [2][128][8] fp32 d8
     static constexpr uint32_t kOffDD = kOffDX + 2 * 4096;                   // [2][kDDBytes]
-    static constexpr uint32_t kRawBytes = 128 * F::kRawRow;              // raw weights of 128 rows
+    static constexpr uint32_t kRawBytes = F::kRawBuf;                    // raw weights of 128 rows
     static constexpr uint32_t kOffRaw = (kOffDD + 2 * F::kDDBytes + 1023) & ~1023u;
     static constexpr uint32_t kSmemAlloc = kOffRaw + 2 * kRawBytes + 1024;
     static_assert(kSmemAlloc <= 227 * 1024, "shared memory map exceeds the per-CTA limit");
@@ -357,8 +385,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                             for (int b2 = 0; b2 < kPair; ++b2) {
                                 const uint32_t d = tmem + (kPair * e + b2) * kTN;
 #pragma unroll
-                                for (int t = 0; t < 2; ++t) {  // two K16 steps per 32-wide sub-block
-                                    const int step = (q * kPair + b2) * 2 + t;  // slab step/4, 32 bytes each
+                                for (int t = 0; t < F::kSub / 16; ++t) {  // K16 steps per slot
+                                    const int step = (q * kPair + b2) * (F::kSub / 16) + t;  // slab step/4, 32 bytes each
                                     const uint32_t off = (step >> 2) * kSlabBytes + (step & 3) * 32;
                                     ptx::mma_f16(d, ptx::smem_desc(xa + off, 1024, 2), ptx::smem_desc(wa + off, 1024, 2),
                                                  idesc, t);
@@ -393,9 +421,11 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         // ------------------------------------------------------------ raw weight TMA
         // The raw superblock of the tile's 128 weight rows, one per superblock, into a
         // 2-deep ring; independent of the activation stream so neither waits on the other.
+        // Q4_K / Q8_0: one tensor-map box (lane 0); Q6_K: one bulk copy per valid row,
+        // spread over the 32 lanes.
         regs_dec<kRegsProducer>();
-        if (lane == 0) {
-            ptx::prefetch_tmap(&tm_w);
+        if (T == QMM_Q6_K || lane == 0) {
+            if constexpr (T != QMM_Q6_K) ptx::prefetch_tmap(&tm_w);
             int64_t u = ubeg;
             Seg sg;
             uint32_t r_it = 0;
@@ -409,8 +439,20 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         break;
                     }
                     const uint32_t rbar = ptx::smem_u32(&B.raw_full[ri]);
-                    ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
-                    ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, F::raw_x(sb), n0, rbar);
+                    if constexpr (T == QMM_Q6_K) {
+                        const int64_t nval = a.n - n0 < 128 ? a.n - n0 : 128;  // rows of W in this tile
+                        if (lane == 0) ptx::mbar_arrive_expect_tx(rbar, (uint32_t)nval * F::kCopyBytes);
+                        __syncwarp();
+#pragma unroll 1
+                        for (int r = lane; r < nval; r += 32) {
+                            const int64_t p = F::pos(n0 + r, sb, a.row_bytes);
+                            ptx::bulk_g2s(sbase + kOffRaw + ri * kRawBytes + r * F::kRawRow, a.W + (p & ~int64_t(15)),
+                                          F::kCopyBytes, rbar);
+                        }
+                    } else {
+                        ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
+                        ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, F::raw_x(sb), n0, rbar);
+                    }
                     ++r_it;
                 }
             }
@@ -431,6 +473,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         uint32_t w_it = 0, sb_it = 0;
         bool ok = true;
         while (ok && next_seg(a, u, uend, sg)) {
+            const int64_t n0w = resolve_tile(a, sg.tile).n0w + r;  // this thread's row of W
+            (void)n0w;
             for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                 const uint32_t ri = sb_it & 1;
                 if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_full[ri]), (sb_it >> 1) & 1, abortp) ||
@@ -439,6 +483,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     break;
                 }
                 const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + r * F::kRawRow;
+                if constexpr (T == QMM_Q6_K)  // the superblock's offset inside its window
+                    blk += (int)(F::pos(n0w, sb, a.row_bytes) & 15);
                 float *dd = reinterpret_cast<float *>(smem + kOffDD + ri * F::kDDBytes);
                 if constexpr (T == QMM_Q4_K) {
                 const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
@@ -486,6 +532,60 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         const int sw = (r >> 2) & 1;
                         *reinterpret_cast<uint4 *>(mdst + ((0 ^ sw) << 4)) = make_uint4(mm[0], mm[1], mm[2], mm[3]);
                         *reinterpret_cast<uint4 *>(mdst + ((1 ^ sw) << 4)) = make_uint4(0, 0, 0, 0);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(ptx::smem_u32(&B.st_full[st]));
+                    ++w_it;
+                }
+                } else if constexpr (T == QMM_Q6_K) {
+                // Q6_K: d * sc of the 16 sub-blocks for the epilogue (the superblock starts 0 or 2
+                // bytes past a word boundary: its words are read from the boundary below and
+                // shifted), then per half the two 64-value units as exact fp16 codes q - 32.
+                {
+                    const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 2u), sh = 8u * mis;
+                    uint32_t scw[5];
+#pragma unroll
+                    for (int i2 = 0; i2 < 5; ++i2) scw[i2] = LdShared::u32(blk + 192 - mis + 4 * i2);
+                    const float d = half_lo(mis ? (scw[4] >> 16) : scw[4]);
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2) {
+                        const uint32_t w4 = __funnelshift_r(scw[i2], scw[i2 + 1], sh);
+#pragma unroll
+                        for (int bb = 0; bb < 4; ++bb)
+                            dd[(4 * i2 + bb) * 128 + r] = d * (float)(int8_t)((w4 >> (8 * bb)) & 0xffu);
+                    }
+                }
+                ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
+                const __half2 bias = __float2half2_rn(-1152.f);
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t st = w_it % kStages;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
+#pragma unroll 1
+                    for (int j2 = 0; j2 < 2; ++j2) {  // slab j2 <-> unit 2h + j2 (64 k values)
+                        Raw<QMM_Q6_K> raw;
+                        Unit w;
+                        load_raw<LdShared>(blk, 2 * h + j2, 0, raw);
+                        convert_raw(raw, 2 * h + j2, w);
+                        uint8_t *rowdst = wst + j2 * kSlabBytes + r * 128;
+#pragma unroll
+                        for (int cq = 0; cq < 8; ++cq) {  // 16-byte chunk cq: codes 8cq .. 8cq+7
+                            uint32_t pr[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const uint32_t uu = (uint32_t)w.q[2 * cq + e2] ^ 0x80808080u;
+                                uint32_t lo = __byte_perm(uu, 0x64646464u, 0x4140);
+                                uint32_t hi = __byte_perm(uu, 0x64646464u, 0x4342);
+                                lo = h2bits(__hadd2(*reinterpret_cast<__half2 *>(&lo), bias));
+                                hi = h2bits(__hadd2(*reinterpret_cast<__half2 *>(&hi), bias));
+                                pr[2 * e2] = lo;
+                                pr[2 * e2 + 1] = hi;
+                            }
+                            *reinterpret_cast<uint4 *>(rowdst + ((cq ^ (r & 7)) << 4)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+                        }
                     }
                     ptx::fence_proxy_async_smem();
                     ptx::mbar_arrive(ptx::smem_u32(&B.st_full[st]));
@@ -644,7 +744,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[e]));
                     ++ge;
                 } else {
-                    // Q8_0: total += (d8 * d_w) * slot, two columns per packed product and fma
+                    // Q8_0 / Q6_K: total += (d8 * w) * slot with w the per-row factor of the slot's
+                    // sub-block (Q8_0: the block's d; Q6_K: d * sc), two columns per packed op
 #pragma unroll
                     for (int j = 0; j < kGroups; ++j) {
                         const uint32_t e = ge & 1;
@@ -653,11 +754,12 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                             break;
                         }
                         ptx::tc_fence_after();
-                        const float4 d4 = dxv[j >> 1];
 #pragma unroll
                         for (int b2 = 0; b2 < kPair; ++b2) {
                             const int G = kPair * j + b2;
-                            const float dgs = (j & 1) ? (b2 ? d4.w : d4.z) : (b2 ? d4.y : d4.x);
+                            const int g32 = G * F::kSub / 32;  // the sub-block's 32-block: its d8
+                            const float4 d4 = dxv[g32 >> 2];
+                            const float dgs = (g32 & 3) == 0 ? d4.x : (g32 & 3) == 1 ? d4.y : (g32 & 3) == 2 ? d4.z : d4.w;
                             const float2 d8 = make_float2(dgs, dgs);
                             const float4 *dwg = reinterpret_cast<const float4 *>(dd + G * 128 + 32 * cq);
 #pragma unroll
@@ -714,6 +816,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
                        TcArgs a) {
     gemm_tc_body<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, a);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_q6k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
+                       const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
+                       TcArgs a) {
+    gemm_tc_body<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, a);
 }
 
 // q8_1 blocks -> fp16 activation codes [m][k], fp32 d8 [m][k/32], fp16 s tile
@@ -860,7 +969,10 @@ TcLayout tc_layout(int64_t m, int64_t k, int64_t partial_ctas) {
 int64_t gemm_tc_tile_m(int64_t) { return kTM; }
 
 bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
-    return (t == QMM_Q4_K || t == QMM_Q8_0) && k % 256 == 0 && n > 0 && m > 0 && m <= (int64_t(1) << 30);
+    if (!(k % 256 == 0 && n > 0 && m > 0 && m <= (int64_t(1) << 30))) return false;
+    if (t == QMM_Q4_K || t == QMM_Q8_0) return true;
+    // Q6_K's raw map views W as groups of 8 rows, so n must be a multiple of 8
+    return t == QMM_Q6_K && n % 8 == 0;
 }
 
 size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m) {
@@ -875,7 +987,7 @@ namespace {
 template <int T>
 cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CUtensorMap &tm_dx,
                    const CUtensorMap &tm_w, const TcArgs &args, int ctas, int64_t fixup_tiles, cudaStream_t st) {
-    auto kern = T == QMM_Q4_K ? gemm_tc_q4k_kernel : gemm_tc_q80_kernel;
+    auto kern = T == QMM_Q4_K ? gemm_tc_q4k_kernel : T == QMM_Q6_K ? gemm_tc_q6k_kernel : gemm_tc_q80_kernel;
     constexpr uint32_t smem = TcMap<T>::kSmemAlloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -930,13 +1042,18 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     if (e != cudaSuccess) return e;
 
     CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
-    const bool q8 = t == QMM_Q8_0;
-    const int64_t row_bytes = (k / 256) * (q8 ? TcFmt<QMM_Q8_0>::kRawRow : TcFmt<QMM_Q4_K>::kRawRow);
-    // Q8_0 rows are read as uint16 so that one superblock's 272 bytes are a box of 136
-    const bool wmap = q8 ? make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, W, row_bytes / 2, n,
-                                       TcFmt<QMM_Q8_0>::kRawRow / 2, kTN, CU_TENSOR_MAP_SWIZZLE_NONE)
-                         : make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, n, kQ4KBytes, kTN,
-                                       CU_TENSOR_MAP_SWIZZLE_NONE);
+    const int64_t row_bytes = (k / 256) * block_bytes(t) * (t == QMM_Q8_0 ? 8 : 1);
+    bool wmap;
+    if (t == QMM_Q8_0)  // rows read as uint16 so that one superblock's 272 bytes are a box of 136
+        wmap = make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, W, row_bytes / 2, n, TcFmt<QMM_Q8_0>::kRawRow / 2,
+                           kTN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    else if (t == QMM_Q6_K) {  // bulk copies from W itself: it must start on a 16-byte boundary
+        memset(&tm_w, 0, sizeof(tm_w));
+        wmap = (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
+    }
+    else
+        wmap = make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, n, kQ4KBytes, kTN,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) || !wmap) return cudaErrorInvalidValue;
 
     TcArgs args{};
@@ -954,8 +1071,9 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     args.ctas = p.ctas;
     args.stream_k = p.stream_k;
     const int64_t fixup_tiles = (p.stream_k && p.fixup) ? p.ntiles : 0;
-    return q8 ? run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st)
-              : run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st);
+    if (t == QMM_Q8_0) return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st);
+    if (t == QMM_Q6_K) return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st);
+    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st);
 }
 
 // ---------------------------------------------------------------- expert-grouped mode

@@ -247,11 +247,6 @@ int gemv_tma_stages(int64_t row_bytes, int64_t k, int ncols, size_t budget) {
     return s >= kTmaMinStages ? s : 0;
 }
 
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
 
 // Q4_K scales and mins of sub-blocks 2c and 2c+1 (c = 0..3) from the 12 packed bytes
 // q[0..11] = s0 | s1 | s2 (GGUF 6-bit rule: for j < 4, sc = q[j] & 63, m = q[j+4] & 63;
@@ -344,7 +339,7 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
                 const uint32_t bytes = uint32_t((b - a) * row_bytes);
                 const uint32_t bar = ptx::smem_u32(&full[s]);
                 ptx::mbar_arrive_expect_tx(bar, bytes);
-                bulk_copy_g2s(ptx::smem_u32(stages + s * stage_bytes), W + a * row_bytes, bytes, bar);
+                ptx::bulk_g2s(ptx::smem_u32(stages + s * stage_bytes), W + a * row_bytes, bytes, bar);
                 ++issued;
             }
             // no copy may still be writing shared memory when the CTA exits: wait for the

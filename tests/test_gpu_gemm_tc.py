@@ -90,3 +90,51 @@ def test_tc_q8_0_extreme_codes(oracle_mod):
         qmm.qmm_set_force_path(0)
     y_ref, T = oracle_mod.mul_mat(W, "q8_0", n, k, xq, m)
     assert_within(y.cpu().numpy(), y_ref, T, "tc q8_0 extreme codes")
+
+
+# Q6_K on the tensor cores: 6-bit codes q - 32 as exact fp16, one slot per 16-wide
+# sub-block, d * sc (int8) folded with d8.  n must be a multiple of 8 (the raw copies
+# are 16-byte windows of the row-major weight rows).
+@pytest.mark.parametrize("n,k,m", [(128, 256, 128), (136, 512, 9), (8, 256, 17), (1000, 1024, 300),
+                                   (2048, 768, 200)])
+@pytest.mark.parametrize("sk", [1, 2])
+def test_tc_q6_k_parity(oracle_mod, n, k, m, sk):
+    run_tc(oracle_mod, n, k, m, sk, seed=3 * n + k + m, fmt="q6_K")
+
+
+def test_tc_q6_k_extreme_scales_and_codes(oracle_mod):
+    """int8 sub-scales -128 and 127, codes 63 and 15 (q - 32 = 31 and -17): the largest
+    per-16 dots and the fold with d * sc must stay within the bound."""
+    n, k, m = 136, 512, 20
+    W, x = qmm_synth.make_dense("q6_K", n, k, m, seed=8)
+    blk = W.reshape(n, k // 256, 210)
+    blk[:, :, 0:128] = np.uint8(0xFF)                      # low nibbles 15
+    blk[:, 0::2, 128:192] = np.uint8(0xFF)                 # high bits 3 -> code 63
+    blk[:, 1::2, 128:192] = np.uint8(0x00)                 # code 15
+    blk[:, :, 192:200] = np.uint8(0x80)                    # sc = -128
+    blk[:, :, 200:208] = np.uint8(0x7F)                    # sc = 127
+    xq = oracle_mod.quantize_q8_1(x)
+    qmm.qmm_set_force_path(qmm.PATH_GEMM_TC)
+    try:
+        y = qmm.qmm_mul_mat(torch.from_numpy(W).to(DEV), "q6_K", n, k, torch.from_numpy(xq).to(DEV), m)
+        torch.cuda.synchronize()
+    finally:
+        qmm.qmm_set_force_path(0)
+    y_ref, T = oracle_mod.mul_mat(W, "q6_K", n, k, xq, m)
+    assert_within(y.cpu().numpy(), y_ref, T, "tc q6_K extreme scales")
+
+
+def test_tc_q6_k_odd_n_falls_back(oracle_mod):
+    """n not a multiple of 8: the forced tensor-core path is not available for Q6_K and
+    the call still returns the right product (CUDA-core GEMM)."""
+    n, k, m = 130, 512, 40
+    W, x = qmm_synth.make_dense("q6_K", n, k, m, seed=11)
+    xq = oracle_mod.quantize_q8_1(x)
+    qmm.qmm_set_force_path(qmm.PATH_GEMM_TC)
+    try:
+        y = qmm.qmm_mul_mat(torch.from_numpy(W).to(DEV), "q6_K", n, k, torch.from_numpy(xq).to(DEV), m)
+        torch.cuda.synchronize()
+    finally:
+        qmm.qmm_set_force_path(0)
+    y_ref, T = oracle_mod.mul_mat(W, "q6_K", n, k, xq, m)
+    assert_within(y.cpu().numpy(), y_ref, T, "q6_K odd n")
