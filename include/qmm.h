@@ -108,7 +108,9 @@ QMM_API qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void 
  *   Q4_K, m <= 8:       the bulk-copy GEMV (dp4a);
  *   Q4_K, 9 <= m <= 16: the skinny tensor-core path (weight rows as the MMA's M side);
  *   Q4_K, m > 16:       the tiled tensor-core GEMM;
- *   Q6_K/Q8_0:          the GEMV for m <= 8, else the CUDA-core tiled GEMM;
+ *   Q6_K/Q8_0, m <= 8:  the bulk-copy GEMV;
+ *   Q6_K/Q8_0, m > 8:   the tiled tensor-core GEMM (Q8_0: k % 256 == 0; Q6_K: n % 8
+ *                       == 0), otherwise the CUDA-core tiled GEMM;
  * the tensor-core paths split their work with a stream-K schedule.
  * Accuracy: |y - y_exact| <= 1e-5 * sum over blocks of |block term| per element.
  */
