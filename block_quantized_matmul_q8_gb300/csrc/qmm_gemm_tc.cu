@@ -656,7 +656,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         // 16 warps: warp w reads TMEM lanes 32*(w%4).. (one activation row per thread)
         // and one quarter of the 128 columns (32 weight rows).  Slots arrive in pairs;
         // both are read (16 columns at a time) and the pair is handed back before the
-        // next pair is awaited.  The segment's total stays in registers.
+        // next pair is awaited (probing, not suspending: the pairs come every few hundred
+        // cycles).  The segment's total stays in registers.
         regs_inc<kRegsEpilogue>();
         const int ew = warp - kEpiWarp0;  // 0..15
         const int cq = ew >> 2;           // column quarter: columns 32cq .. 32cq+31
@@ -689,7 +690,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
 #pragma unroll
                     for (int j = 0; j < kGroups; ++j) {
                         const uint32_t e = ge & 1;
-                        if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
                             ok = false;
                             break;
                         }
@@ -717,7 +718,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     if (!ok) break;
                     // the min group: total += d * acc + (-dmin) * minslot
                     const uint32_t e = ge & 1;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                    if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
                         ok = false;
                         break;
                     }
@@ -749,7 +750,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
 #pragma unroll
                     for (int j = 0; j < kGroups; ++j) {
                         const uint32_t e = ge & 1;
-                        if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
                             ok = false;
                             break;
                         }
