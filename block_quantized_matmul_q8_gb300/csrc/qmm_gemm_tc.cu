@@ -434,7 +434,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 const int n0 = resolve_tile(a, sg.tile).n0w;
                 for (int64_t sb = sg.s0; sb < sg.s1; ++sb) {
                     const uint32_t ri = r_it & 1;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_empty[ri]), ((r_it >> 1) & 1) ^ 1, abortp)) {
+                    const bool got = ptx::mbar_wait(ptx::smem_u32(&B.raw_empty[ri]), ((r_it >> 1) & 1) ^ 1, abortp);
+                    // Q6_K: all 32 lanes take part, so they must agree before the warp barrier
+                    if (!(T == QMM_Q6_K ? __all_sync(0xffffffffu, got) != 0 : got)) {
                         ok = false;
                         break;
                     }
@@ -679,9 +681,12 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     ok = false;
                     break;
                 }
-                // the row's 8 d8 values, two 16-byte reads (scalar reads at the 32-byte row
-                // stride would put 8 lanes on each bank)
-                const float4 *dxv = reinterpret_cast<const float4 *>(smem + kOffDX + sdi * 4096 + tl * 32);
+                // the row's 8 d8 values as two 16-byte chunks; the tile comes with the 32-byte
+                // swizzle (chunk c of row tl at chunk c ^ (tl >> 2 & 1)), so the 8 lanes of a
+                // quarter warp read 8 different bank groups
+                const uint8_t *dxrow = smem + kOffDX + sdi * 4096 + tl * 32;
+                const int dxsw = (tl >> 2) & 1;
+                auto dxv = [&](int c) { return *reinterpret_cast<const float4 *>(dxrow + ((c ^ dxsw) << 4)); };
                 const float *dd = reinterpret_cast<const float *>(smem + kOffDD + sdi * F::kDDBytes);
                 if constexpr (F::kMin) {
                     float2 acc[16];  // columns 2i, 2i+1 of this thread's 32
@@ -695,7 +700,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                             break;
                         }
                         ptx::tc_fence_after();
-                        const float4 d4 = dxv[j >> 1];
+                        const float4 d4 = dxv(j >> 1);
                         const float d8a = (j & 1) ? d4.z : d4.x, d8b = (j & 1) ? d4.w : d4.y;
 #pragma unroll
                         for (int b2 = 0; b2 < kPair; ++b2) {
@@ -759,7 +764,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         for (int b2 = 0; b2 < kPair; ++b2) {
                             const int G = kPair * j + b2;
                             const int g32 = G * F::kSub / 32;  // the sub-block's 32-block: its d8
-                            const float4 d4 = dxv[g32 >> 2];
+                            const float4 d4 = dxv(g32 >> 2);
                             const float dgs = (g32 & 3) == 0 ? d4.x : (g32 & 3) == 1 ? d4.y : (g32 & 3) == 2 ? d4.z : d4.w;
                             const float2 d8 = make_float2(dgs, dgs);
                             const float4 *dwg = reinterpret_cast<const float4 *>(dd + G * 128 + 32 * cq);
@@ -1016,7 +1021,7 @@ bool make_act_maps(CUtensorMap &tm_x, CUtensorMap &tm_xmin, CUtensorMap &tm_dx, 
     return make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, k, rows, 64, kTM, CU_TENSOR_MAP_SWIZZLE_128B) &&
            make_map_2d(&tm_xmin, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, smin, (k / 256) * 16, rows, 16, kTM,
                        CU_TENSOR_MAP_SWIZZLE_32B) &&
-           make_map_2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx, k / 32, rows, 8, kTM, CU_TENSOR_MAP_SWIZZLE_NONE);
+           make_map_2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx, k / 32, rows, 8, kTM, CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
 }  // namespace
