@@ -334,20 +334,34 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
     out.update(dense("q4_K", 4100, 4096, [512]))
     out.update(dense("q6_K", 151936, 5120, [1, 512]))
     out.update(dense("q8_0", 5120, 5120, [1, 512]))
-    # MoE: 128 experts x Q4_K n=1536 k=4096, 512 tokens top-8 Zipf(1.1)
-    if only not in "moe_q4K_e128_n1536_k4096_t512_top8":
+    # MoE: 128 experts x Q4_K n=1536 k=4096, 512 tokens top-8 Zipf(1.1); and its decode
+    # form, one token top-8, whose calls route to disjoint sets of 8 experts in turn (16
+    # calls cover all 128 experts, 453 MB, so no call finds its experts in L2)
+    key_p, key_d = "moe_q4K_e128_n1536_k4096_t512_top8", "moe_decode_q4K_e128_n1536_k4096_t1_top8"
+    if only not in key_p and only not in key_d:
         return out
     E, n, k, T_, Kt = 128, 1536, 4096, 512, 8
     W, x, ids = qmm_synth.make_moe(E, n, k, T_, Kt, seed=0)
     Wd = torch.from_numpy(W).to(dev)
-    xq = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
-    idd = torch.from_numpy(ids).to(dev)
-    y = torch.empty((T_, Kt, n), device=dev)
-    ws = torch.empty(qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, Kt), dtype=torch.uint8, device=dev)
-    fn = lambda i: qmm.qmm_mul_mat_id(Wd, "q4_K", E, n, k, xq, idd, Kt, T_, y=y, workspace=ws)
-    ms = time_graphs(torch, fn, steps, 3, lambda: None) / steps
-    out["moe_q4K_e128_n1536_k4096_t512_top8"] = {"tops": 2 * T_ * Kt * n * k / (ms * 1e-3) / 1e12, "ms": ms,
-                                                 "l2": "weights 453 MB > 3x L2"}
+    if only in key_p:
+        xq = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
+        idd = torch.from_numpy(ids).to(dev)
+        y = torch.empty((T_, Kt, n), device=dev)
+        ws = torch.empty(qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, Kt), dtype=torch.uint8, device=dev)
+        fn = lambda i: qmm.qmm_mul_mat_id(Wd, "q4_K", E, n, k, xq, idd, Kt, T_, y=y, workspace=ws)
+        ms = time_graphs(torch, fn, steps, 3, lambda: None) / steps
+        out[key_p] = {"tops": 2 * T_ * Kt * n * k / (ms * 1e-3) / 1e12, "ms": ms, "l2": "weights 453 MB > 3x L2"}
+    if only in key_d:
+        order = np.random.default_rng(7).permutation(E).astype(np.int32)
+        ids_d = [torch.from_numpy(order[8 * j:8 * j + 8].reshape(1, Kt).copy()).to(dev) for j in range(E // Kt)]
+        xq1 = qmm.qmm_quantize_q8_1(torch.from_numpy(x[:1]).to(dev))
+        y1 = torch.empty((1, Kt, n), device=dev)
+        ws1 = torch.empty(qmm.qmm_workspace_bytes("q4_K", n, k, 1, E, Kt), dtype=torch.uint8, device=dev)
+        fn = lambda i: qmm.qmm_mul_mat_id(Wd, "q4_K", E, n, k, xq1, ids_d[i % len(ids_d)], Kt, 1, y=y1, workspace=ws1)
+        ms = time_graphs(torch, fn, steps, 3, lambda: None) / steps
+        b = Kt * n * (k // 256) * 144 + (k // 32) * 36 + Kt * n * 4
+        out[key_d] = {"GB/s": b / (ms * 1e-3) / 1e9, "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "ms": ms,
+                      "l2": "16 routings cycle through the 128 experts (453 MB)"}
     return out
 
 

@@ -28,7 +28,8 @@ PATH_AUTO, PATH_GEMV, PATH_GEMM_DP4A, PATH_GEMM_TC, PATH_GEMV_DIRECT, PATH_GEMV_
 EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspace_bytes", "qmm_quantize_q8_1",
            "qmm_mul_mat", "qmm_mul_mat_id", "qmm_read_device_status", "qmm_tile_efficiency_percent",
            "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode",
-           "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32")
+           "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32",
+           "qmm_mul_mat_id_slot")
 
 
 class QMMError(RuntimeError):
@@ -87,6 +88,8 @@ def lib():
     L.qmm_set_stream_k_mode.argtypes = [ctypes.c_int]
     L.qmm_mul_mat_id_noalloc.restype = ctypes.c_int
     L.qmm_mul_mat_id_noalloc.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P]
+    L.qmm_mul_mat_id_slot.restype = ctypes.c_int
+    L.qmm_mul_mat_id_slot.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P, ctypes.c_size_t, P]
     L.qmm_noalloc_scratch_bytes.restype = SZ
     L.qmm_noalloc_scratch_bytes.argtypes = []
     L.qmm_workspace_bytes_f32.restype = SZ
@@ -196,10 +199,7 @@ def qmm_mul_mat_f32(W: torch.Tensor, qtype, n: int, k: int, x: torch.Tensor, m: 
     return y
 
 
-def qmm_mul_mat_id(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, xq: torch.Tensor, ids: torch.Tensor,
-                   top_k: int, n_tokens: int, y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                   stream=None) -> torch.Tensor:
-    """y[n_tokens, top_k, n] fp32 with y[t, s] = x[t] * dequant(W[ids[t, s]])^T."""
+def _mul_mat_id(fn, name, W, qtype, n_experts, n, k, xq, ids, top_k, n_tokens, y, workspace, stream):
     _dev(W, "W")
     _dev(xq, "xq")
     _dev(ids, "ids", torch.int32)
@@ -210,9 +210,26 @@ def qmm_mul_mat_id(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, xq: t
         workspace = torch.empty(qmm_workspace_bytes(qtype, n, k, n_tokens, n_experts, top_k), dtype=torch.uint8,
                                 device=W.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib().qmm_mul_mat_id(_ptr(W), _qtype(qtype), n_experts, n, k, _ptr(xq), _ptr(ids), top_k, n_tokens,
-                                _ptr(y), _ptr(workspace), ws_bytes, _stream(stream)), "qmm_mul_mat_id")
+    _check(fn(_ptr(W), _qtype(qtype), n_experts, n, k, _ptr(xq), _ptr(ids), top_k, n_tokens, _ptr(y),
+              _ptr(workspace), ws_bytes, _stream(stream)), name)
     return y
+
+
+def qmm_mul_mat_id(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, xq: torch.Tensor, ids: torch.Tensor,
+                   top_k: int, n_tokens: int, y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """y[n_tokens, top_k, n] fp32 with y[t, s] = x[t] * dequant(W[ids[t, s]])^T."""
+    return _mul_mat_id(lib().qmm_mul_mat_id, "qmm_mul_mat_id", W, qtype, n_experts, n, k, xq, ids, top_k, n_tokens,
+                       y, workspace, stream)
+
+
+def qmm_mul_mat_id_slot(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, xq: torch.Tensor, ids: torch.Tensor,
+                        top_k: int, n_tokens: int, y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """y[n_tokens, top_k, n] fp32 with y[t, s] = x[t, s] * dequant(W[ids[t, s]])^T: xq holds
+    one q8_1 row per (token, slot) pair, row t*top_k + s."""
+    return _mul_mat_id(lib().qmm_mul_mat_id_slot, "qmm_mul_mat_id_slot", W, qtype, n_experts, n, k, xq, ids, top_k,
+                       n_tokens, y, workspace, stream)
 
 
 def qmm_mul_mat_id_noalloc(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, xq: torch.Tensor,

@@ -109,6 +109,26 @@ qmm_status moe_check_pointers(const void *W_experts, const void *xq, const int32
 
 using namespace qmm;
 
+static qmm_status mul_mat_id_common(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
+                                    const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
+                                    bool x_per_slot, float *y, void *workspace, size_t ws_bytes, void *stream) {
+    qmm_status s = moe_check_sizes(t, n_experts, n, k, top_k, n_tokens);
+    if (s != QMM_OK) return s;
+    if (!workspace) return QMM_ERR_WORKSPACE;
+    if (!aligned256(workspace)) return QMM_ERR_ALIGN;
+    const size_t need = moe_workspace_bytes(t, n, k, n_tokens, n_experts, top_k);
+    if (ws_bytes < need) return QMM_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n == 0 || n_tokens == 0) {
+        // empty problem: only reset the status word
+        return cuda_status(cudaMemsetAsync(workspace, 0, 16, st));
+    }
+    s = moe_check_pointers(W_experts, xq, ids, y);
+    if (s != QMM_OK) return s;
+    return cuda_status(launch_mul_mat_id(t, W_experts, n_experts, n, k, xq, ids, top_k, n_tokens, x_per_slot, y,
+                                         workspace, ws_bytes, st));
+}
+
 extern "C" {
 
 const char *qmm_status_string(qmm_status s) {
@@ -228,21 +248,15 @@ extern "C" {
 qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
                           const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
                           void *workspace, size_t ws_bytes, void *stream) {
-    qmm_status s = moe_check_sizes(t, n_experts, n, k, top_k, n_tokens);
-    if (s != QMM_OK) return s;
-    if (!workspace) return QMM_ERR_WORKSPACE;
-    if (!aligned256(workspace)) return QMM_ERR_ALIGN;
-    const size_t need = moe_workspace_bytes(t, n, k, n_tokens, n_experts, top_k);
-    if (ws_bytes < need) return QMM_ERR_WORKSPACE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (n == 0 || n_tokens == 0) {
-        // empty problem: only reset the status word
-        return cuda_status(cudaMemsetAsync(workspace, 0, 16, st));
-    }
-    s = moe_check_pointers(W_experts, xq, ids, y);
-    if (s != QMM_OK) return s;
-    return cuda_status(launch_mul_mat_id(t, W_experts, n_experts, n, k, xq, ids, top_k, n_tokens, y, workspace,
-                                         ws_bytes, st));
+    return mul_mat_id_common(W_experts, t, n_experts, n, k, xq, ids, top_k, n_tokens, false, y, workspace, ws_bytes,
+                             stream);
+}
+
+qmm_status qmm_mul_mat_id_slot(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
+                               const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
+                               void *workspace, size_t ws_bytes, void *stream) {
+    return mul_mat_id_common(W_experts, t, n_experts, n, k, xq, ids, top_k, n_tokens, true, y, workspace, ws_bytes,
+                             stream);
 }
 
 qmm_status qmm_read_device_status(const void *workspace, int32_t *status, void *stream) {

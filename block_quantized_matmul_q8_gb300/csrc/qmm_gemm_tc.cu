@@ -863,11 +863,12 @@ __global__ void tc_prep_kernel(const uint8_t *__restrict__ xq, int64_t m, int k,
     }
 }
 
-// Expert-grouped variant of tc_prep_kernel: sorted row j holds the activation row of
-// pair perm[j] (token perm[j] / top_k).  Rows of invalid pairs are left as they are:
+// Expert-grouped variant of tc_prep_kernel: sorted row j holds activation row
+// perm[j] / x_div of xq (x_div = top_k: the pair's token; 1: one row per pair).
+// Rows of invalid pairs are left as they are:
 // the GEMM computes them but never stores them.
 __global__ void tc_prep_gather_kernel(const uint8_t *__restrict__ xq, int k, const int32_t *__restrict__ perm,
-                                      const int32_t *__restrict__ bounds, int E, int top_k, int64_t n_pairs,
+                                      const int32_t *__restrict__ bounds, int E, int x_div, int64_t n_pairs,
                                       __half *__restrict__ xh, float *__restrict__ dx, __half *__restrict__ smin) {
     const int nb32 = k / 32;
     const int64_t nvalid = bounds[E];
@@ -876,7 +877,7 @@ __global__ void tc_prep_gather_kernel(const uint8_t *__restrict__ xq, int k, con
         const int64_t j = i / nb32;
         if (j >= nvalid) continue;
         const int b = (int)(i - j * nb32);
-        const int64_t tok = perm[j] / top_k;
+        const int64_t tok = perm[j] / x_div;
         const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (tok * nb32 + b) * kQ81Bytes);
         const uint32_t dsw = ldg4(src);
         uint4 *dst = reinterpret_cast<uint4 *>(xh + j * k + 32 * b);
@@ -1093,7 +1094,7 @@ size_t gemm_tc_grouped_bytes(int64_t n_pairs, int64_t k) {
 }
 
 cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
-                                   int64_t top_k, int64_t n_pairs, float *y, const MoETile *tiles,
+                                   int64_t x_div, int64_t n_pairs, float *y, const MoETile *tiles,
                                    const int32_t *ntiles, int64_t max_token_tiles, const int32_t *bounds,
                                    const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st) {
     const int ctas = std::min(device_sm_count(), kMaxPartialCtas);
@@ -1107,7 +1108,7 @@ cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     const int64_t nblk = n_pairs * (k / 32);
     const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
     tc_prep_gather_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), (int)k, perm, bounds,
-                                                             (int)n_experts, (int)top_k, n_pairs, xh, dx, smin);
+                                                             (int)n_experts, (int)x_div, n_pairs, xh, dx, smin);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

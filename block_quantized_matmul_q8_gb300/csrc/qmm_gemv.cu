@@ -462,6 +462,42 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const uint8_t 
     gemv_tma_body<T, NC>(W, n, k, row_bytes, nstages, x, y, y_ld, status);
 }
 
+// Expert-routed decode ([MMQ] section "派发路径": mul_mat_id with a handful of pairs):
+// one GEMV per (token, slot) pair instead of 128-pair GEMM tiles that hold one pair
+// each.  Grid (CTAs per pair, pairs); CTA (c, p) reads pair p's expert id on the device
+// and streams its share of that expert's n rows with the bulk-copy body.  The ids are
+// typically written by the preceding kernel (the router), so they are read after the
+// grid dependency wait.  A pair whose id is outside [0, E) gets a zero output row and
+// flags the call (QMM_ERR_IDS), as on the grouped paths: CTA (0, 0) scans all the ids
+// and writes the call's status word, so no reset precedes the launch.  Activation row
+// of pair p: xq row p / x_div (x_div = top_k: shared by a token's slots; 1: one row per
+// slot).
+template <int T>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    gemv_id_kernel(const uint8_t *__restrict__ W, int n_experts, int64_t n, int k, int64_t row_bytes, int nstages,
+                   const uint8_t *__restrict__ xq, int64_t x_div, const int32_t *__restrict__ ids, int n_pairs,
+                   float *__restrict__ y, int *status) {
+    const int64_t p = blockIdx.y;
+    ptx::grid_dependency_wait();
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32) {
+        bool bad = false;
+        for (int i = threadIdx.x; i < n_pairs; i += 32) bad |= ids[i] < 0 || ids[i] >= n_experts;
+        bad = __any_sync(0xffffffffu, bad);
+        if (threadIdx.x == 0) status[0] = bad ? (int)QMM_ERR_IDS : (int)QMM_OK;
+    }
+    const int e = ids[p];
+    float *yp = y + p * n;
+    if (e < 0 || e >= n_experts) {
+        const int64_t r0 = n * blockIdx.x / gridDim.x, r1 = n * (blockIdx.x + 1) / gridDim.x;
+        for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) yp[r] = 0.f;
+        return;
+    }
+    XIn x;
+    x.xq = xq + (p / x_div) * int64_t(k / 32) * kQ81Bytes;
+    x.xf = nullptr;
+    gemv_tma_body<T, 1>(W + int64_t(e) * n * row_bytes, n, k, row_bytes, nstages, x, yp, n, status);
+}
+
 // Rows that a bulk-copy GEMV can stream: every chunk must start on and span whole
 // 16-byte units.  Q4_K rows always are; Q8_0 rows when k/32 is a multiple of 8; Q6_K
 // rows when (k/256) * 210 is, or else from an even row on when n is even.
@@ -487,6 +523,25 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(W), n,
                       (int)k, row_bytes, nstages, x, y, y_ld, static_cast<int *>(nullptr));
+}
+
+template <int T>
+static cudaError_t launch_gemv_id_t(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                                    int64_t x_div, const int32_t *ids, int64_t n_pairs, float *y, int *status,
+                                    cudaStream_t st) {
+    const int64_t row_bytes = gemv_tma_row_bytes<T>(n, k);
+    const int nstages = row_bytes > 0 ? gemv_tma_stages(row_bytes, k, 1, size_t(device_smem_optin())) : 0;
+    if (nstages <= 0) return cudaErrorNotSupported;
+    const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, 1);
+    auto kern = gemv_id_kernel<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // enough CTAs per pair to cover the SMs once, at least 2 rows each
+    const int64_t per_pair = std::max<int64_t>(
+        1, std::min<int64_t>((n + 1) / 2, (device_sm_count() + n_pairs - 1) / n_pairs));
+    return launch_pdl(kern, dim3((unsigned)per_pair, (unsigned)n_pairs), dim3(kTmaThreads), smem, st,
+                      static_cast<const uint8_t *>(W), (int)n_experts, n, (int)k, row_bytes, nstages,
+                      static_cast<const uint8_t *>(xq), x_div, ids, (int)n_pairs, y, status);
 }
 
 template <int T, int NC>
@@ -565,6 +620,27 @@ cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const v
     case QMM_Q4_K: return launch_gemv_t<QMM_Q4_K>(W, n, k, xq, xf, m, y, st);
     case QMM_Q6_K: return launch_gemv_t<QMM_Q6_K>(W, n, k, xq, xf, m, y, st);
     case QMM_Q8_0: return launch_gemv_t<QMM_Q8_0>(W, n, k, xq, xf, m, y, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool gemv_id_supported(qmm_type t, int64_t n, int64_t k) {
+    int64_t rb = 0;
+    switch (t) {
+    case QMM_Q4_K: rb = gemv_tma_row_bytes<QMM_Q4_K>(n, k); break;
+    case QMM_Q6_K: rb = gemv_tma_row_bytes<QMM_Q6_K>(n, k); break;
+    case QMM_Q8_0: rb = gemv_tma_row_bytes<QMM_Q8_0>(n, k); break;
+    }
+    return n > 0 && rb > 0 && gemv_tma_stages(rb, k, 1, size_t(device_smem_optin())) > 0;
+}
+
+cudaError_t launch_gemv_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                           int64_t x_div, const int32_t *ids, int64_t n_pairs, float *y, int *status,
+                           cudaStream_t st) {
+    switch (t) {
+    case QMM_Q4_K: return launch_gemv_id_t<QMM_Q4_K>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
+    case QMM_Q6_K: return launch_gemv_id_t<QMM_Q6_K>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
+    case QMM_Q8_0: return launch_gemv_id_t<QMM_Q8_0>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
     }
     return cudaErrorInvalidValue;
 }

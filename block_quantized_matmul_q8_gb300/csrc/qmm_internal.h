@@ -47,6 +47,13 @@ bool gemv_tma_enabled();
 size_t gemv_smem_bytes(int64_t k, int ncols);
 cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
                         float *y, cudaStream_t st);
+// Expert-routed decode: one bulk-copy GEMV per (token, slot) pair, expert ids read on the
+// device; pair p's activation row is xq row p / x_div.  Invalid ids give zero rows; the
+// kernel writes *status (QMM_OK, or QMM_ERR_IDS if any id is invalid).
+bool gemv_id_supported(qmm_type t, int64_t n, int64_t k);
+cudaError_t launch_gemv_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                           int64_t x_div, const int32_t *ids, int64_t n_pairs, float *y, int *status,
+                           cudaStream_t st);
 
 // Tensor-core path for skinny activations (Q4_K, 1 <= m <= 16): weights as the MMA's
 // 128-row M side, activations as N = 16; stream-K over (row tile, superblock) units.
@@ -66,28 +73,30 @@ bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
 cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
                            void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st);
 
-// Expert-grouped tensor-core GEMM over a device-built tile list (see qmm_moe.h).
+// Expert-grouped tensor-core GEMM over a device-built tile list (see qmm_moe.h); sorted
+// pair row j takes xq row perm[j] / x_div.
 struct MoETile;
 bool gemm_tc_grouped_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k);
 size_t gemm_tc_grouped_bytes(int64_t n_pairs, int64_t k);
 cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
-                                   int64_t top_k, int64_t n_pairs, float *y, const MoETile *tiles,
+                                   int64_t x_div, int64_t n_pairs, float *y, const MoETile *tiles,
                                    const int32_t *ntiles, int64_t max_token_tiles, const int32_t *bounds,
                                    const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st);
 
-// MoE: device bucketing + grouped GEMM.
+// MoE: device bucketing + grouped GEMM, or one GEMV per pair for a handful of pairs.
+// x_per_slot: xq holds one activation row per (token, slot) pair instead of one per token.
 size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k);
 cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
-                              const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *ws,
-                              size_t ws_bytes, cudaStream_t st);
+                              const int32_t *ids, int64_t top_k, int64_t n_tokens, bool x_per_slot, float *y,
+                              void *ws, size_t ws_bytes, cudaStream_t st);
 // Argument checks of qmm_mul_mat_id shared by its entry points.
 qmm_status moe_check_sizes(qmm_type t, int64_t n_experts, int64_t n, int64_t k, int64_t top_k, int64_t n_tokens);
 qmm_status moe_check_pointers(const void *W_experts, const void *xq, const int32_t *ids, const float *y);
 // The same computation on CUDA-core tiles only; its scratch is small (bucketing only).
 size_t moe_dp4a_workspace_bytes(int64_t n_tokens, int64_t n_experts, int64_t top_k);
 cudaError_t launch_mul_mat_id_dp4a(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k,
-                                   const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
-                                   void *ws, size_t ws_bytes, cudaStream_t st);
+                                   const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
+                                   bool x_per_slot, float *y, void *ws, size_t ws_bytes, cudaStream_t st);
 
 // Offset of the device status word inside a mul_mat_id workspace.
 constexpr size_t kStatusOffset = 0;

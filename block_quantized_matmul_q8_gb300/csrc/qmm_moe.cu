@@ -182,8 +182,8 @@ size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, i
 }
 
 cudaError_t launch_mul_mat_id_dp4a(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k,
-                                   const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
-                                   void *ws, size_t ws_bytes, cudaStream_t st) {
+                                   const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
+                                   bool x_per_slot, float *y, void *ws, size_t ws_bytes, cudaStream_t st) {
     const int64_t n_pairs = n_tokens * top_k;
     const MoELayout L = moe_layout(n_pairs, n_experts, kDp4aTileTokens, 0);
     if (ws_bytes < L.total) return cudaErrorInvalidValue;
@@ -197,15 +197,25 @@ cudaError_t launch_mul_mat_id_dp4a(qmm_type t, const void *W, int64_t n_experts,
     moe_zero_invalid_kernel<<<64, 256, 0, st>>>(status, perm, bounds, (int)n_experts, y, n);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_gemm_dp4a_grouped(t, W, n, k, xq, y, tiles, status + 1, bounds, perm, (int)top_k, st);
+    return launch_gemm_dp4a_grouped(t, W, n, k, xq, y, tiles, status + 1, bounds, perm, x_per_slot ? 1 : (int)top_k,
+                                    st);
 }
 
+// Up to this many (token, slot) pairs, one GEMV per pair beats the grouped GEMM, whose
+// 128-pair tiles would each hold one or two pairs.
+constexpr int64_t kMoeGemvMaxPairs = 32;
+
 cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
-                              const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *ws,
-                              size_t ws_bytes, cudaStream_t st) {
-    if (!gemm_tc_grouped_supported(t, n_experts, n, k))
-        return launch_mul_mat_id_dp4a(t, W, n_experts, n, k, xq, ids, top_k, n_tokens, y, ws, ws_bytes, st);
+                              const int32_t *ids, int64_t top_k, int64_t n_tokens, bool x_per_slot, float *y,
+                              void *ws, size_t ws_bytes, cudaStream_t st) {
     const int64_t n_pairs = n_tokens * top_k;
+    if (n_pairs <= kMoeGemvMaxPairs && gemv_id_supported(t, n, k)) {
+        int32_t *status = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + kStatusOffset);
+        return launch_gemv_id(t, W, n_experts, n, k, xq, x_per_slot ? 1 : top_k, ids, n_pairs, y, status, st);
+    }
+    if (!gemm_tc_grouped_supported(t, n_experts, n, k))
+        return launch_mul_mat_id_dp4a(t, W, n_experts, n, k, xq, ids, top_k, n_tokens, x_per_slot, y, ws, ws_bytes,
+                                      st);
     const MoELayout L = moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k));
     if (ws_bytes < L.total) return cudaErrorInvalidValue;
     cudaError_t e = launch_moe_bucket(ids, n_pairs, (int)n_experts, kTcTileTokens, ws, L, st);
@@ -219,7 +229,8 @@ cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int6
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t max_token_tiles = n_pairs / kTcTileTokens + n_experts + 1;
-    return launch_gemm_tc_grouped(W, n_experts, n, k, xq, top_k, n_pairs, y, tiles, status + 1, max_token_tiles,
+    return launch_gemm_tc_grouped(W, n_experts, n, k, xq, x_per_slot ? 1 : top_k, n_pairs, y, tiles, status + 1,
+                                  max_token_tiles,
                                   bounds, perm, status, base + L.gemm, L.total - L.gemm, st);
 }
 

@@ -71,7 +71,7 @@ extern "C" qmm_status qmm_mul_mat_id_noalloc(const void *W_experts, qmm_type t, 
     if (n == 0 || n_tokens == 0) return cudaMemsetAsync(ws, 0, 16, st) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     s = moe_check_pointers(W_experts, xq, ids, y);
     if (s != QMM_OK) return s;
-    return launch_mul_mat_id_dp4a(t, W_experts, n_experts, n, k, xq, ids, top_k, n_tokens, y, ws,
+    return launch_mul_mat_id_dp4a(t, W_experts, n_experts, n, k, xq, ids, top_k, n_tokens, false, y, ws,
                                   kNoAllocScratchBytes, st) == cudaSuccess
                ? QMM_OK
                : QMM_ERR_CUDA;

@@ -149,17 +149,33 @@ QMM_API qmm_status qmm_mul_mat_f32(const void *W, qmm_type t, int64_t n, int64_t
  *   workspace : at least qmm_workspace_bytes(t, n, k, n_tokens, n_experts, top_k)
  *               bytes; it also holds the device status word read by
  *               qmm_read_device_status.
- * The (token, slot) pairs are bucketed by expert on the device (a stable counting
- * sort) and the per-expert tiles are walked by one persistent launch; the host
- * never reads ids, so the call does not synchronise.  A pair whose id is outside
- * [0, n_experts) gets a zero output row and sets QMM_ERR_IDS in the status word.
- * Q4_K with k % 256 == 0 runs on the tensor cores (128-pair tiles, stream-K over
- * the device-built tile list; the workspace then also holds an fp16 copy of the
- * gathered activations); the other formats run the CUDA-core grouped GEMM.
+ * The host never reads ids, so the call does not synchronise.  A pair whose id is
+ * outside [0, n_experts) gets a zero output row and sets QMM_ERR_IDS in the status
+ * word.  Paths:
+ *   n_tokens * top_k <= 32 (decode): one bulk-copy GEMV per (token, slot) pair, the
+ *     pair's expert id read on the device (for the shapes the GEMV streams: Q4_K
+ *     always, Q8_0 with k/32 % 8 == 0, Q6_K with 16-byte rows or even n);
+ *   otherwise the pairs are bucketed by expert on the device (a stable counting sort)
+ *     and the per-expert tiles are walked by one persistent launch: Q4_K with
+ *     k % 256 == 0 on the tensor cores (128-pair tiles, stream-K over the device-built
+ *     tile list; the workspace then also holds an fp16 copy of the gathered
+ *     activations), the other formats on the CUDA-core grouped GEMM.
  */
 QMM_API qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                           const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *workspace,
                           size_t ws_bytes, void *stream);
+
+/*
+ * qmm_mul_mat_id with one activation row per (token, slot) pair, as in a MoE down
+ * projection, where each slot's input is that expert's own up/gate output:
+ *   y[t][s][:] = x[t][s] * dequant(W_experts[ids[t][s]])^T
+ *   xq : q8_1 blocks of x [n_tokens][top_k][k] (pair (t, s) at row t*top_k + s).
+ * Everything else (arguments, workspace size, status word, paths) is as for
+ * qmm_mul_mat_id.
+ */
+QMM_API qmm_status qmm_mul_mat_id_slot(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
+                                       const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
+                                       void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * qmm_mul_mat_id without a workspace argument, for callers that cannot allocate

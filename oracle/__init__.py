@@ -62,6 +62,8 @@ def lib():
         L.oracle_bucket.argtypes = [P, I64, I64, I64, P, P]
         L.oracle_mul_mat_id.restype = I64
         L.oracle_mul_mat_id.argtypes = [ctypes.c_int, P, I64, I64, I64, P, P, I64, I64, P, P]
+        L.oracle_mul_mat_id_slot.restype = I64
+        L.oracle_mul_mat_id_slot.argtypes = [ctypes.c_int, P, I64, I64, I64, P, P, I64, I64, P, P]
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = L
     return _lib
@@ -185,15 +187,17 @@ def bucket(ids: np.ndarray, n_experts: int):
     return bounds, perm[: bounds[-1]], int(bad)
 
 
-def mul_mat_id(W, fmt, n_experts, n, k, xq, ids):
-    """(y, T, n_invalid) with y, T fp64 [n_tokens][top_k][n]."""
+def mul_mat_id(W, fmt, n_experts, n, k, xq, ids, per_slot=False):
+    """(y, T, n_invalid) with y, T fp64 [n_tokens][top_k][n].  xq holds one q8_1 row
+    per token, or with per_slot one row per (token, slot) pair (row t*top_k + s)."""
     W = _u8(W)
     xq = _u8(xq)
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     t, kk = ids.shape
     y = np.empty((t, kk, n), np.float64)
     T = np.empty((t, kk, n), np.float64)
-    bad = lib().oracle_mul_mat_id(TYPES[fmt], _p(W), n_experts, n, k, _p(xq), _p(ids), kk, t, _p(y), _p(T))
+    fn = lib().oracle_mul_mat_id_slot if per_slot else lib().oracle_mul_mat_id
+    bad = fn(TYPES[fmt], _p(W), n_experts, n, k, _p(xq), _p(ids), kk, t, _p(y), _p(T))
     _check(bad)
     return y, T, int(bad)
 

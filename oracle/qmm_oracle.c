@@ -369,12 +369,13 @@ ORACLE_API int64_t oracle_bucket(const int32_t *ids, int64_t n_tokens, int64_t t
     return bad;
 }
 
-/* mul_mat_id: y[t][s][n] = mul_mat(W_experts[ids[t][s]], x row t)[n]; the activation
- * row of token t is shared by all its slots.  Invalid ids give a zero output row
- * (and T = 0).  Returns the number of invalid ids, or a negative error. */
-ORACLE_API int64_t oracle_mul_mat_id(int type, const uint8_t *W, int64_t n_experts, int64_t n, int64_t k,
-                                     const uint8_t *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
-                                     double *y, double *T) {
+/* mul_mat_id: y[t][s][n] = mul_mat(W_experts[ids[t][s]], x row)[n], the x row being
+ * t (shared by a token's slots) or, with x_per_slot, t*top_k + s (one row per slot, as
+ * in a MoE down projection).  Invalid ids give a zero output row (and T = 0).  Returns
+ * the number of invalid ids, or a negative error. */
+static int64_t mul_mat_id_rows(int type, const uint8_t *W, int64_t n_experts, int64_t n, int64_t k,
+                               const uint8_t *xq, int x_per_slot, const int32_t *ids, int64_t top_k,
+                               int64_t n_tokens, double *y, double *T) {
     int rc = check_shape(type, k);
     if (rc) return rc;
     int64_t rb = (k / block_elems(type)) * block_bytes(type);
@@ -384,7 +385,7 @@ ORACLE_API int64_t oracle_mul_mat_id(int type, const uint8_t *W, int64_t n_exper
         if (ids[i] < 0 || ids[i] >= n_experts) ++bad;
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n_tokens * top_k; ++i) {
-        int64_t t = i / top_k;
+        int64_t xrow = x_per_slot ? i : i / top_k;
         int32_t e = ids[i];
         for (int64_t r = 0; r < n; ++r) {
             double *yy = &y[i * n + r];
@@ -393,11 +394,23 @@ ORACLE_API int64_t oracle_mul_mat_id(int type, const uint8_t *W, int64_t n_exper
                 *yy = 0.0;
                 if (tt) *tt = 0.0;
             } else {
-                fold_one(type, W + ((int64_t)e * n + r) * rb, xq + t * xb, k, yy, tt);
+                fold_one(type, W + ((int64_t)e * n + r) * rb, xq + xrow * xb, k, yy, tt);
             }
         }
     }
     return bad;
+}
+
+ORACLE_API int64_t oracle_mul_mat_id(int type, const uint8_t *W, int64_t n_experts, int64_t n, int64_t k,
+                                     const uint8_t *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
+                                     double *y, double *T) {
+    return mul_mat_id_rows(type, W, n_experts, n, k, xq, 0, ids, top_k, n_tokens, y, T);
+}
+
+ORACLE_API int64_t oracle_mul_mat_id_slot(int type, const uint8_t *W, int64_t n_experts, int64_t n, int64_t k,
+                                          const uint8_t *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
+                                          double *y, double *T) {
+    return mul_mat_id_rows(type, W, n_experts, n, k, xq, 1, ids, top_k, n_tokens, y, T);
 }
 
 /* ---------------------------------------------------------------- threads */

@@ -138,20 +138,23 @@ def test_zero_activation_gives_exact_zero(oracle_mod):
 
 # ---------------------------------------------------------------- MoE
 
-def moe_check(oracle_mod, E, n, k, T_, K, seed, corrupt=0):
-    W, x, ids = qmm_synth.make_moe(E, n, k, T_, K, seed=seed)
+def moe_check(oracle_mod, E, n, k, T_, K, seed, corrupt=0, fmt="q4_K", per_slot=False):
+    W, x, ids = qmm_synth.make_moe(E, n, k, T_, K, seed=seed, fmt=fmt)
     if corrupt:
         rng = np.random.default_rng(seed)
         for _ in range(corrupt):
             ids[rng.integers(0, T_), rng.integers(0, K)] = rng.choice([-1, E, E + 5])
+    if per_slot:  # one activation row per (token, slot): fresh rows, seeded
+        x = qmm_synth.gen_x(np.random.default_rng(seed + 1), T_ * K, k)
     xq = oracle_mod.quantize_q8_1(x)
-    y_ref, Tr, bad = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, xq, ids)
-    ws = torch.empty(qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, K), dtype=torch.uint8, device=DEV)
+    y_ref, Tr, bad = oracle_mod.mul_mat_id(W, fmt, E, n, k, xq, ids, per_slot=per_slot)
+    ws = torch.empty(qmm.qmm_workspace_bytes(fmt, n, k, T_, E, K), dtype=torch.uint8, device=DEV)
     y = torch.full((T_, K, n), float("nan"), device=DEV)
-    qmm.qmm_mul_mat_id(to_dev(W), "q4_K", E, n, k, to_dev(xq), to_dev(ids), K, T_, y=y, workspace=ws)
+    call = qmm.qmm_mul_mat_id_slot if per_slot else qmm.qmm_mul_mat_id
+    call(to_dev(W), fmt, E, n, k, to_dev(xq), to_dev(ids), K, T_, y=y, workspace=ws)
     status = qmm.qmm_read_device_status(ws)
     assert status == (7 if bad else 0)
-    assert_within(y.cpu().numpy(), y_ref, Tr, f"moe E={E} n={n} k={k} T={T_} K={K}")
+    assert_within(y.cpu().numpy(), y_ref, Tr, f"moe {fmt} E={E} n={n} k={k} T={T_} K={K} per_slot={per_slot}")
 
 
 # The last two put several 128-pair tiles on each expert and split tiles between
@@ -179,3 +182,28 @@ def test_gemv_bulk_and_direct_agree(oracle_mod, fmt, n, k, m):
     assert np.array_equal(a, b)
     y_ref, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
     assert_within(a, y_ref, T, f"bulk gemv {fmt} n={n} k={k} m={m}")
+
+
+# Decode-size routing (tokens x top_k <= 32 pairs): one GEMV per pair, expert ids read on
+# the device.  32 pairs is the largest such call, 33 goes back to the grouped GEMM; Q6_K
+# rows of 9 superblocks (k = 2304) are not bulk-copy aligned and take the grouped GEMM too.
+@pytest.mark.parametrize("fmt,E,n,k,T_,K", [("q4_K", 32, 384, 2048, 1, 8), ("q4_K", 16, 1000, 512, 3, 8),
+                                            ("q4_K", 8, 256, 256, 4, 8), ("q4_K", 8, 256, 256, 11, 3),
+                                            ("q6_K", 16, 130, 1024, 2, 4), ("q6_K", 8, 96, 2048, 1, 8),
+                                            ("q6_K", 8, 96, 2304, 1, 8),
+                                            ("q8_0", 16, 136, 256, 2, 8), ("q8_0", 8, 100, 512, 1, 2)])
+def test_moe_decode_gemv_parity(oracle_mod, fmt, E, n, k, T_, K):
+    moe_check(oracle_mod, E, n, k, T_, K, seed=E + n + T_ + K, fmt=fmt)
+
+
+def test_moe_decode_gemv_invalid_ids_flagged_and_zeroed(oracle_mod):
+    moe_check(oracle_mod, 16, 200, 512, 2, 8, seed=17, corrupt=3)
+
+
+# One activation row per (token, slot) pair (a down projection): the decode GEMV, the
+# tensor-core grouped GEMM and the CUDA-core grouped GEMM
+@pytest.mark.parametrize("fmt,E,n,k,T_,K", [("q4_K", 16, 256, 512, 2, 4), ("q4_K", 16, 130, 512, 64, 4),
+                                            ("q4_K", 8, 384, 1024, 300, 2), ("q6_K", 8, 130, 512, 40, 2),
+                                            ("q8_0", 8, 64, 256, 50, 3)])
+def test_moe_per_slot_parity(oracle_mod, fmt, E, n, k, T_, K):
+    moe_check(oracle_mod, E, n, k, T_, K, seed=2 * E + n + T_, fmt=fmt, per_slot=True)

@@ -189,3 +189,30 @@ def test_synthetic_moe_histogram_is_skewed():
     c = np.bincount(ids.ravel(), minlength=128)
     assert c.sum() == 4096 and c.max() > 300 and np.median(c) < 32 and c.min() >= 1
     assert all(len(set(r)) == 8 for r in ids)
+
+
+def test_mul_mat_id_per_slot_reduces_to_dense(oracle_mod):
+    """One activation row per (token, slot): each output row is the dense routine on that
+    pair's own row and expert; with every slot's row equal to its token's row it is the
+    shared-row call, to the bit."""
+    rng = np.random.default_rng(53)
+    E, n, k, T_, K = 5, 24, 512, 4, 3
+    W = qmm_synth.gen_q4_K(rng, E * n, k).reshape(E, n, -1)
+    xs = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, T_ * K, k))
+    ids = qmm_synth.gen_moe_ids(rng, T_, K, E)
+    ids[2, 0] = -1
+    y, T, bad = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, xs, ids, per_slot=True)
+    assert bad == 1
+    for t in range(T_):
+        for s in range(K):
+            e = ids[t, s]
+            if e < 0:
+                assert np.all(y[t, s] == 0) and np.all(T[t, s] == 0)
+                continue
+            yd, Td = oracle_mod.mul_mat(W[e], "q4_K", n, k, xs[t * K + s:t * K + s + 1], 1)
+            assert np.array_equal(y[t, s], yd[0]) and np.array_equal(T[t, s], Td[0])
+    xt = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, T_, k))
+    rep = np.repeat(xt, K, axis=0)
+    y1, T1, _ = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, rep, ids, per_slot=True)
+    y2, T2, _ = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, xt, ids)
+    assert np.array_equal(y1, y2) and np.array_equal(T1, T2)
