@@ -157,6 +157,30 @@ def mul_mat(W: np.ndarray, fmt: str, n: int, k: int, xq: np.ndarray, m: int):
     return y, T
 
 
+def silu(v):
+    """v * sigmoid(v) in fp64: the SwiGLU gate ([MMQ] section "「分专家」与「整批」之间: host
+    侧的代价": the fused gate/up kernel applies the GLU right after the dots; [P0007]'s
+    coverage list: fused ffn gate/up/SWIGLU)."""
+    v = np.asarray(v, dtype=np.float64)
+    return v / (1.0 + np.exp(-v))
+
+
+def mul_mat_glu(W_gate, W_up, fmt, n, k, xq, m):
+    """(y, tol), both fp64 [m][n]: y = silu(g) * u with g, u the folds of the gate and up
+    rows (each W [n][k]).  tol is the per-element bound that the GPU result must meet:
+    the fold bound of each dot (1e-5 of its sum of |block terms|) carried through the
+    product to first order, plus 2^-20 of |y| for evaluating silu and the product in fp32:
+        tol = 1e-5 * (|silu'(g)| T_g |u| + |silu(g)| T_u) + 2^-20 |y|."""
+    g, Tg = mul_mat(W_gate, fmt, n, k, xq, m)
+    u, Tu = mul_mat(W_up, fmt, n, k, xq, m)
+    sg = 1.0 / (1.0 + np.exp(-g))
+    a = g * sg
+    da = sg * (1.0 + g * (1.0 - sg))
+    y = a * u
+    tol = 1e-5 * (np.abs(da) * Tg * np.abs(u) + np.abs(a) * Tu) + 2.0 ** -20 * np.abs(y)
+    return y, tol
+
+
 def mul_mat_at(W, fmt, n, k, xq, m, rows, cols):
     """Fold at selected output positions (rows = W rows, cols = activation rows)."""
     W = _u8(W)

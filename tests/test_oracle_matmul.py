@@ -216,3 +216,32 @@ def test_mul_mat_id_per_slot_reduces_to_dense(oracle_mod):
     y1, T1, _ = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, rep, ids, per_slot=True)
     y2, T2, _ = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, xt, ids)
     assert np.array_equal(y1, y2) and np.array_equal(T1, T2)
+
+
+def test_silu_closed_forms(oracle_mod):
+    """silu(0) = 0, silu(v) - silu(-v) = v, silu(1) = 1 / (1 + 1/e), and silu(v) -> v for
+    large v, -> 0 for very negative v."""
+    v = np.linspace(-30, 30, 121)
+    s = oracle_mod.silu(v)
+    assert oracle_mod.silu(0.0) == 0.0
+    np.testing.assert_allclose(s - oracle_mod.silu(-v), v, rtol=0, atol=1e-12)
+    assert abs(oracle_mod.silu(1.0) - 1.0 / (1.0 + np.exp(-1.0))) < 1e-15
+    assert abs(oracle_mod.silu(40.0) - 40.0) < 1e-12 and abs(oracle_mod.silu(-40.0)) < 1e-15
+
+
+def test_mul_mat_glu_pins(oracle_mod):
+    """The GLU oracle against a hand-built case: gate rows equal to the up rows give
+    silu(u) * u; a zero gate row gives exactly 0; the bound is non-negative and shrinks
+    to the fp32 term when the gate's dots carry no error bound."""
+    rng = np.random.default_rng(61)
+    n, k, m = 6, 512, 3
+    Wu = qmm_synth.gen_q4_K(rng, n, k)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, m, k))
+    u, _ = oracle_mod.mul_mat(Wu, "q4_K", n, k, xq, m)
+    y, tol = oracle_mod.mul_mat_glu(Wu, Wu, "q4_K", n, k, xq, m)
+    np.testing.assert_allclose(y, u * u / (1.0 + np.exp(-u)), rtol=1e-14, atol=0)
+    assert np.all(tol >= 0)
+    Wg = Wu.copy()
+    Wg.reshape(n, k // 256, 144)[2, :, :4] = 0  # row 2: d = dmin = 0, every term 0
+    y2, tol2 = oracle_mod.mul_mat_glu(Wg, Wu, "q4_K", n, k, xq, m)
+    assert np.all(y2[:, 2] == 0) and np.all(tol2[:, 2] >= 0)
