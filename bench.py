@@ -327,6 +327,36 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
         del Wd
         return rows
 
+    def glu(n, k, ms):
+        """Fused gate/up + SwiGLU from q8_1 input: both weights (n rows each) in GB/s at
+        m <= 8, TOPS over both products (2 * m * 2n * k) above."""
+        ms = [m for m in ms if only in f"glu_q4_K_n{n}_k{k}_m{m}"]
+        if not ms:
+            return {}
+        rows = {}
+        W, x = qmm_synth.make_dense("q4_K", 2 * n, k, max(ms), seed=0)
+        copies = max(1, int(3 * L2_BYTES // W.nbytes) + 1)
+        Wg = [torch.from_numpy(W[:n].copy()).to(dev) for _ in range(copies)]
+        Wu = [torch.from_numpy(W[n:].copy()).to(dev) for _ in range(copies)]
+        xq_all = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
+        for m in ms:
+            xq = xq_all[:m].contiguous()
+            y = torch.empty((m, n), device=dev)
+            need = qmm.qmm_workspace_bytes_glu("q4_K", n, k, m)
+            ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
+            fn = lambda i: qmm.qmm_mul_mat_glu(Wg[i % copies], Wu[i % copies], "q4_K", n, k, xq, m, y=y, workspace=ws)
+            ms_call = time_graphs(torch, fn, steps, 3, lambda: None) / steps
+            key = f"glu_q4_K_n{n}_k{k}_m{m}"
+            if m <= 8:
+                b = W.nbytes + m * (k // 32) * 36 + m * n * 4
+                rows[key] = {"GB/s": b / (ms_call * 1e-3) / 1e9, "hbm_frac": b / (ms_call * 1e-3) / 1e9 / hbm_peak,
+                             "ms": ms_call}
+            else:
+                rows[key] = {"tops": 2 * m * 2 * n * k / (ms_call * 1e-3) / 1e12, "ms": ms_call}
+            rows[key]["l2"] = f"{copies} copies of both weights ({copies * W.nbytes / 1e6:.0f} MB)"
+        del Wg, Wu
+        return rows
+
     out.update(dense("q4_K", 17408, 5120, [1], q8_input=True))
     out.update(dense("q4_K", 17408, 5120, [2, 4, 5, 8]))
     out.update(dense("q4_K", 1024, 2048, [16]))
@@ -334,6 +364,7 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
     out.update(dense("q4_K", 4100, 4096, [512]))
     out.update(dense("q6_K", 151936, 5120, [1, 512]))
     out.update(dense("q8_0", 5120, 5120, [1, 512]))
+    out.update(glu(14336, 4096, [1, 512]))
     # MoE: 128 experts x Q4_K n=1536 k=4096, 512 tokens top-8 Zipf(1.1); and its decode
     # form, one token top-8, whose calls route to disjoint sets of 8 experts in turn (16
     # calls cover all 128 experts, 453 MB, so no call finds its experts in L2)

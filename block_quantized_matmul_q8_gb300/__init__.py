@@ -29,7 +29,7 @@ EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspac
            "qmm_mul_mat", "qmm_mul_mat_id", "qmm_read_device_status", "qmm_tile_efficiency_percent",
            "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode",
            "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32",
-           "qmm_mul_mat_id_slot")
+           "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu")
 
 
 class QMMError(RuntimeError):
@@ -88,6 +88,10 @@ def lib():
     L.qmm_set_stream_k_mode.argtypes = [ctypes.c_int]
     L.qmm_mul_mat_id_noalloc.restype = ctypes.c_int
     L.qmm_mul_mat_id_noalloc.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P]
+    L.qmm_workspace_bytes_glu.restype = ctypes.c_size_t
+    L.qmm_workspace_bytes_glu.argtypes = [ctypes.c_int, I64, I64, I64]
+    L.qmm_mul_mat_glu.restype = ctypes.c_int
+    L.qmm_mul_mat_glu.argtypes = [P, P, ctypes.c_int, I64, I64, P, I64, P, P, ctypes.c_size_t, P]
     L.qmm_mul_mat_id_slot.restype = ctypes.c_int
     L.qmm_mul_mat_id_slot.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P, ctypes.c_size_t, P]
     L.qmm_noalloc_scratch_bytes.restype = SZ
@@ -174,6 +178,29 @@ def qmm_mul_mat(W: torch.Tensor, qtype, n: int, k: int, xq: torch.Tensor, m: int
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().qmm_mul_mat(_ptr(W), _qtype(qtype), n, k, _ptr(xq), m, _ptr(y), _ptr(workspace), ws_bytes,
                              _stream(stream)), "qmm_mul_mat")
+    return y
+
+
+def qmm_workspace_bytes_glu(qtype, n: int, k: int, m: int) -> int:
+    return lib().qmm_workspace_bytes_glu(_qtype(qtype), n, k, m)
+
+
+def qmm_mul_mat_glu(W_gate: torch.Tensor, W_up: torch.Tensor, qtype, n: int, k: int, xq: torch.Tensor, m: int,
+                    y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[m, n] fp32 = silu(x * dequant(W_gate)^T) * (x * dequant(W_up)^T) from q8_1 activations."""
+    _dev(W_gate, "W_gate")
+    _dev(W_up, "W_up")
+    _dev(xq, "xq")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=W_gate.device)
+    _dev(y, "y", torch.float32)
+    need = qmm_workspace_bytes_glu(qtype, n, k, m)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=W_gate.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().qmm_mul_mat_glu(_ptr(W_gate), _ptr(W_up), _qtype(qtype), n, k, _ptr(xq), m, _ptr(y),
+                                 _ptr(workspace) if workspace is not None else None, ws_bytes, _stream(stream)),
+           "qmm_mul_mat_glu")
     return y
 
 

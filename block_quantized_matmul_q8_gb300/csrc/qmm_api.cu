@@ -51,6 +51,7 @@ int device_smem_optin() {
 
 static bool type_ok(qmm_type t) { return t == QMM_Q4_K || t == QMM_Q6_K || t == QMM_Q8_0; }
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
 constexpr int64_t kMaxK = int64_t(1) << 20;
@@ -108,6 +109,24 @@ qmm_status moe_check_pointers(const void *W_experts, const void *xq, const int32
 }  // namespace qmm
 
 using namespace qmm;
+
+// Unfused SwiGLU for the shapes the fused kernels do not take: y = silu(g) * u.
+__global__ void glu_combine_kernel(const float *__restrict__ g, const float *__restrict__ u, int64_t total,
+                                   float *__restrict__ y) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x)
+        y[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
+}
+
+enum GluPath { kGluGemv = 1, kGluTc = 2, kGluUnfused = 3 };
+static int choose_glu_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    const int force = g_force_path.load(std::memory_order_relaxed);
+    if (force == kGemmDp4a) return kGluUnfused;
+    if (force == kGemmTc && gemm_tc_glu_supported(t, n, k, m)) return kGluTc;
+    if (force == kGemv && gemv_glu_supported(t, n, k, m)) return kGluGemv;
+    if (m <= 8 && gemv_glu_supported(t, n, k, m)) return kGluGemv;
+    if (gemm_tc_glu_supported(t, n, k, m)) return kGluTc;
+    return kGluUnfused;
+}
 
 static qmm_status mul_mat_id_common(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
                                     const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
@@ -183,6 +202,46 @@ qmm_status qmm_mul_mat(const void *W, qmm_type t, int64_t n, int64_t k, const vo
     if (!W || !xq || !y) return QMM_ERR_ARG;
     if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return QMM_ERR_ALIGN;
     return mul_mat_q8(W, t, n, k, xq, m, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t qmm_workspace_bytes_glu(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    if (!type_ok(t) || n <= 0 || k <= 0 || m <= 0 || check_k(t, k) != QMM_OK) return 0;
+    switch (choose_glu_path(t, n, k, m)) {
+    case kGluGemv: return 0;
+    case kGluTc: return gemm_tc_glu_workspace_bytes(t, n, k, m);
+    default: return align256(size_t(2) * m * n * 4) + qmm_workspace_bytes(t, n, k, m, 0, 0);
+    }
+}
+
+qmm_status qmm_mul_mat_glu(const void *W_gate, const void *W_up, qmm_type t, int64_t n, int64_t k, const void *xq,
+                           int64_t m, float *y, void *workspace, size_t ws_bytes, void *stream) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n < 0 || m < 0) return QMM_ERR_ARG;
+    if (n > kMaxRows || m > kMaxRows) return QMM_ERR_SHAPE;
+    if (n == 0 || m == 0) return QMM_OK;
+    if (!W_gate || !W_up || !xq || !y) return QMM_ERR_ARG;
+    if (!aligned16(W_gate) || !aligned16(W_up) || !aligned16(xq) || !aligned16(y)) return QMM_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int path = choose_glu_path(t, n, k, m);
+    if (path == kGluGemv) return cuda_status(launch_gemv_glu(t, W_gate, W_up, n, k, xq, m, y, st));
+    const size_t need = qmm_workspace_bytes_glu(t, n, k, m);
+    if (!workspace || ws_bytes < need) return QMM_ERR_WORKSPACE;
+    if (!aligned256(workspace)) return QMM_ERR_ALIGN;
+    if (path == kGluTc)
+        return cuda_status(launch_gemm_tc_glu(t, W_gate, W_up, n, k, xq, m, y, workspace, ws_bytes, st));
+    // unfused: both products into the workspace, then the combine pass
+    float *g = static_cast<float *>(workspace), *u = g + m * n;
+    uint8_t *rest = static_cast<uint8_t *>(workspace) + align256(size_t(2) * m * n * 4);
+    const size_t rest_bytes = ws_bytes - align256(size_t(2) * m * n * 4);
+    s = mul_mat_q8(W_gate, t, n, k, xq, m, g, rest, rest_bytes, st);
+    if (s != QMM_OK) return s;
+    s = mul_mat_q8(W_up, t, n, k, xq, m, u, rest, rest_bytes, st);
+    if (s != QMM_OK) return s;
+    const int64_t total = m * n;
+    const int grid = (int)std::min<int64_t>((total + 255) / 256, int64_t(device_sm_count()) * 8);
+    glu_combine_kernel<<<std::max(grid, 1), 256, 0, st>>>(g, u, total, y);
+    return cuda_status(cudaGetLastError());
 }
 
 size_t qmm_workspace_bytes_f32(qmm_type t, int64_t n, int64_t k, int64_t m) {

@@ -162,6 +162,9 @@ struct TcArgs {
     const int32_t *ntiles;  // device: number of token tiles in `tiles`
     const int32_t *bounds;
     const int32_t *perm;
+    // fused gate/up + SwiGLU (n_out > 0, Q4_K): the tile space has n = 2 n_out columns,
+    // column 2j the gate row j (tm_w) and 2j+1 the up row j (tm_w2); y is [m][n_out]
+    int64_t n_out;
 };
 
 // Where tile t lives: m0 = first activation row (sorted row in grouped mode), rows =
@@ -231,6 +234,14 @@ __device__ __forceinline__ void store_segment(const TcArgs &a, const Seg &sg, in
                                               const float2 (&tot)[16]) {
     const TileInfo ti = resolve_tile(a, sg.tile);
     const int64_t col0 = ti.col0 + 32 * cq;
+    if (a.n_out) {  // GLU (whole tiles only): columns 2i, 2i+1 are the gate and up dots of output col0/2 + i
+        if (tl >= ti.rows) return;
+        float *dst = a.y + int64_t(ti.m0 + tl) * a.n_out + col0 / 2;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (col0 / 2 + i < a.n_out) dst[i] = tot[i].x / (1.0f + expf(-tot[i].x)) * tot[i].y;
+        return;
+    }
     if (sg.s0 == 0 && sg.s1 == a.nsb) {
         if (tl >= ti.rows) return;
         const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
@@ -259,7 +270,8 @@ __device__ __forceinline__ void store_segment(const TcArgs &a, const Seg &sg, in
 
 template <int T>
 __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin,
-                                             const CUtensorMap &tm_dx, const CUtensorMap &tm_w, TcArgs a) {
+                                             const CUtensorMap &tm_dx, const CUtensorMap &tm_w,
+                                             const CUtensorMap &tm_w2, TcArgs a) {
     using F = TcFmt<T>;
     using Mp = TcMap<T>;
     constexpr uint32_t kOffX = Mp::kOffX, kOffW = Mp::kOffW, kOffXmin = Mp::kOffXmin, kOffWmin = Mp::kOffWmin;
@@ -426,6 +438,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         regs_dec<kRegsProducer>();
         if (T == QMM_Q6_K || lane == 0) {
             if constexpr (T != QMM_Q6_K) ptx::prefetch_tmap(&tm_w);
+            if (a.n_out) ptx::prefetch_tmap(&tm_w2);
             int64_t u = ubeg;
             Seg sg;
             uint32_t r_it = 0;
@@ -451,6 +464,11 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                             ptx::bulk_g2s(sbase + kOffRaw + ri * kRawBytes + r * F::kRawRow, a.W + (p & ~int64_t(15)),
                                           F::kCopyBytes, rbar);
                         }
+                    } else if (a.n_out) {  // GLU: 64 gate rows, then the 64 up rows of the same outputs
+                        ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
+                        ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, F::raw_x(sb), n0 / 2, rbar);
+                        ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes + 64 * F::kRawRow, &tm_w2, F::raw_x(sb),
+                                         n0 / 2, rbar);
                     } else {
                         ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
                         ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, F::raw_x(sb), n0, rbar);
@@ -484,7 +502,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     ok = false;
                     break;
                 }
-                const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + r * F::kRawRow;
+                // GLU: tile column r is gate row r/2 (r even) or up row r/2 (r odd)
+                const int rsrc = a.n_out ? (r & 1) * 64 + (r >> 1) : r;
+                const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + rsrc * F::kRawRow;
                 if constexpr (T == QMM_Q6_K)  // the superblock's offset inside its window
                     blk += (int)(F::pos(n0w, sb, a.row_bytes) & 15);
                 float *dd = reinterpret_cast<float *>(smem + kOffDD + ri * F::kDDBytes);
@@ -813,22 +833,22 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
                        const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
-                       TcArgs a) {
-    gemm_tc_body<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, a);
+                       const __grid_constant__ CUtensorMap tm_w2, TcArgs a) {
+    gemm_tc_body<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, a);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_q80_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
                        const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
-                       TcArgs a) {
-    gemm_tc_body<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, a);
+                       const __grid_constant__ CUtensorMap tm_w2, TcArgs a) {
+    gemm_tc_body<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, a);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_q6k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
                        const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
-                       TcArgs a) {
-    gemm_tc_body<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, a);
+                       const __grid_constant__ CUtensorMap tm_w2, TcArgs a) {
+    gemm_tc_body<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, a);
 }
 
 // q8_1 blocks -> fp16 activation codes [m][k], fp32 d8 [m][k/32], fp16 s tile
@@ -993,7 +1013,8 @@ namespace {
 // Launch the GEMM kernel of format T (and the fixup pass when asked) once the maps are built.
 template <int T>
 cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CUtensorMap &tm_dx,
-                   const CUtensorMap &tm_w, const TcArgs &args, int ctas, int64_t fixup_tiles, cudaStream_t st) {
+                   const CUtensorMap &tm_w, const CUtensorMap &tm_w2, const TcArgs &args, int ctas, int64_t fixup_tiles,
+                   cudaStream_t st) {
     auto kern = T == QMM_Q4_K ? gemm_tc_q4k_kernel : T == QMM_Q6_K ? gemm_tc_q6k_kernel : gemm_tc_q80_kernel;
     constexpr uint32_t smem = TcMap<T>::kSmemAlloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1007,7 +1028,7 @@ cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CU
         launch_regs = fa.numRegs;
     }
     if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    kern<<<ctas, kThreads, smem, st>>>(tm_x, tm_xmin, tm_dx, tm_w, args);
+    kern<<<ctas, kThreads, smem, st>>>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, args);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (fixup_tiles > 0) {
@@ -1078,9 +1099,66 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     args.ctas = p.ctas;
     args.stream_k = p.stream_k;
     const int64_t fixup_tiles = (p.stream_k && p.fixup) ? p.ntiles : 0;
-    if (t == QMM_Q8_0) return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st);
-    if (t == QMM_Q6_K) return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st);
-    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, args, p.ctas, fixup_tiles, st);
+    if (t == QMM_Q8_0) return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
+    if (t == QMM_Q6_K) return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
+    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
+}
+
+// ---------------------------------------------------------------- fused gate/up + SwiGLU
+
+bool gemm_tc_glu_supported(qmm_type t, int64_t n_out, int64_t k, int64_t m) {
+    return t == QMM_Q4_K && n_out > 0 && gemm_tc_supported(t, 2 * n_out, k, m);
+}
+
+size_t gemm_tc_glu_workspace_bytes(qmm_type t, int64_t n_out, int64_t k, int64_t m) {
+    return gemm_tc_glu_supported(t, n_out, k, m) ? tc_layout(m, k, 0).total : 0;
+}
+
+// Whole tiles only (the GLU needs both complete dots in one thread, [MMQ] section
+// "「分专家」与「整批」之间: host 侧的代价"), so the schedule is one tile per CTA.
+cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_out, int64_t k, const void *xq,
+                               int64_t m, float *y, void *ws, size_t ws_bytes, cudaStream_t st) {
+    if (!gemm_tc_glu_supported(t, n_out, k, m)) return cudaErrorNotSupported;
+    qmm_gemm_plan p{};
+    const int nsm = std::min(device_sm_count(), kMaxPartialCtas);
+    if (qmm_plan_gemm(t, 2 * n_out, k, m, nsm, 1, &p) != QMM_OK || p.stream_k) return cudaErrorInvalidValue;
+    const TcLayout L = tc_layout(m, k, 0);
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    int *status = reinterpret_cast<int *>(base + L.status);
+    __half *xh = reinterpret_cast<__half *>(base + L.xh);
+    float *dx = reinterpret_cast<float *>(base + L.dx);
+    __half *smin = reinterpret_cast<__half *>(base + L.smin);
+    const int64_t nblk = m * (k / 32);
+    const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
+    tc_prep_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), m, (int)k, xh, dx, smin,
+                                                      status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t row_bytes = (k / 256) * kQ4KBytes;
+    CUtensorMap tm_x, tm_xmin, tm_dx, tm_w, tm_w2;
+    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) ||
+        !make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wg, row_bytes, n_out, kQ4KBytes, kTN / 2,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wu, row_bytes, n_out, kQ4KBytes, kTN / 2,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    TcArgs args{};
+    args.W = static_cast<const uint8_t *>(Wg);
+    args.n = 2 * n_out;
+    args.m = m;
+    args.k = (int)k;
+    args.row_bytes = row_bytes;
+    args.y = y;
+    args.partial = nullptr;
+    args.status = status;
+    args.tiles_n = p.tiles_n;
+    args.nsb = p.iters_per_tile;
+    args.nwork = p.nwork;
+    args.ctas = p.ctas;
+    args.stream_k = 0;
+    args.n_out = n_out;
+    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, args, p.ctas, 0, st);
 }
 
 // ---------------------------------------------------------------- expert-grouped mode
@@ -1136,7 +1214,7 @@ cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     args.ntiles = ntiles;
     args.bounds = bounds;
     args.perm = perm;
-    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, args, ctas, max_token_tiles * args.tiles_n, st);
+    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, max_token_tiles * args.tiles_n, st);
 }
 
 // ---------------------------------------------------------------- shared with the skinny path

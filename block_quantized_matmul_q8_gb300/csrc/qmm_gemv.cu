@@ -289,10 +289,17 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
 // chunks 16-byte aligned only from an even row on, so for Q6_K the CTAs' row ranges
 // start on even rows (the host takes this kernel for Q6_K only when n is even or the
 // rows are whole multiples of 16 bytes).
-template <int T, int NC>
+// GLU: fused gate/up with SwiGLU ([MMQ] sections "「分专家」与「整批」之间: host 侧的代价"
+// and "输出端: 写回与 scale 修正": gate and up rows interleaved so that one thread holds
+// both dots of an output, no stream-K).  n counts outputs; W is the gate and W2 the up
+// weight, each [n] rows.  A chunk holds 4 outputs as 8 staged rows (gate j, up j, ...),
+// one bulk copy per row; the two half-warps of a warp fold one pair and lane 0 writes
+// silu(gate) * up.
+template <int T, int NC, bool GLU = false>
 __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int64_t n, int k, int64_t row_bytes,
                                               int nstages, const XIn &x, float *__restrict__ y, int64_t y_ld,
-                                              int *status) {
+                                              int *status, const uint8_t *__restrict__ W2 = nullptr) {
+    constexpr int kCR = GLU ? kTmaChunkRows / 2 : kTmaChunkRows;  // outputs per chunk
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full[kTmaMaxStages], empty[kTmaMaxStages];
@@ -308,7 +315,7 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
     const int64_t nr = (n + ra - 1) / ra;
     const int64_t r0 = ra * (nr * blockIdx.x / gridDim.x);
     const int64_t r1 = min(n, ra * (nr * (blockIdx.x + 1) / gridDim.x));
-    const int nchunks = (int)((r1 - r0 + kTmaChunkRows - 1) / kTmaChunkRows);
+    const int nchunks = (int)((r1 - r0 + kCR - 1) / kCR);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, l16 = lane & 15;
     volatile int *abortp = &abort_flag;
 
@@ -334,12 +341,21 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
                 const int s = c % nstages;
                 if (c >= nstages && !ptx::mbar_wait(ptx::smem_u32(&empty[s]), ((c / nstages) - 1) & 1, abortp))
                     break;
-                const int64_t a = r0 + int64_t(c) * kTmaChunkRows;
-                const int64_t b = min(r1, a + kTmaChunkRows);
-                const uint32_t bytes = uint32_t((b - a) * row_bytes);
+                const int64_t a = r0 + int64_t(c) * kCR;
+                const int64_t b = min(r1, a + kCR);
                 const uint32_t bar = ptx::smem_u32(&full[s]);
-                ptx::mbar_arrive_expect_tx(bar, bytes);
-                ptx::bulk_g2s(ptx::smem_u32(stages + s * stage_bytes), W + a * row_bytes, bytes, bar);
+                if constexpr (GLU) {
+                    ptx::mbar_arrive_expect_tx(bar, uint32_t(2 * (b - a) * row_bytes));
+                    for (int64_t i = 0; i < b - a; ++i) {
+                        const uint32_t dst = ptx::smem_u32(stages + s * stage_bytes + size_t(2 * i) * row_bytes);
+                        ptx::bulk_g2s(dst, W + (a + i) * row_bytes, uint32_t(row_bytes), bar);
+                        ptx::bulk_g2s(dst + uint32_t(row_bytes), W2 + (a + i) * row_bytes, uint32_t(row_bytes), bar);
+                    }
+                } else {
+                    const uint32_t bytes = uint32_t((b - a) * row_bytes);
+                    ptx::mbar_arrive_expect_tx(bar, bytes);
+                    ptx::bulk_g2s(ptx::smem_u32(stages + s * stage_bytes), W + a * row_bytes, bytes, bar);
+                }
                 ++issued;
                 // Every CTA asks for its first two chunks and lets them land before asking
                 // for the rest: requested all at once, the first chunks of all CTAs queue
@@ -366,8 +382,8 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
         for (int c = grp; c < nchunks; c += kTmaGroups) {
             const int s = c % nstages;
             if (!ptx::mbar_wait(ptx::smem_u32(&full[s]), (c / nstages) & 1, abortp)) break;
-            const int64_t a = r0 + int64_t(c) * kTmaChunkRows;
-            const bool valid = a + rr < r1;
+            const int64_t a = r0 + int64_t(c) * kCR;
+            const bool valid = GLU ? a + gw < r1 : a + rr < r1;  // GLU: warp gw folds output a + gw
             float acc[NC];
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) acc[cc] = 0.f;
@@ -437,7 +453,15 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));  // the stage is read: free it first
-            if (valid && l16 == 0) {
+            if constexpr (GLU) {
+                // lane 0 holds the gate dot, lane 16 the up dot of the same output
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) {
+                    const float up = __shfl_xor_sync(0xffffffffu, acc[cc], 16);
+                    const float g = acc[cc];
+                    if (valid && lane == 0) y[cc * y_ld + a + gw] = g / (1.0f + expf(-g)) * up;
+                }
+            } else if (valid && l16 == 0) {
 #pragma unroll
                 for (int cc = 0; cc < NC; ++cc) y[cc * y_ld + a + rr] = acc[cc];
             }
@@ -453,6 +477,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
                                                                       const XIn x, float *__restrict__ y,
                                                                       int64_t y_ld, int *status) {
     gemv_tma_body<QMM_Q4_K, NC>(W, n, k, row_bytes, nstages, x, y, y_ld, status);
+}
+
+template <int NC>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    gemv_q4k_glu_kernel(const uint8_t *__restrict__ Wg, const uint8_t *__restrict__ Wu, int64_t n, int k,
+                        int64_t row_bytes, int nstages, const XIn x, float *__restrict__ y, int64_t y_ld,
+                        int *status) {
+    gemv_tma_body<QMM_Q4_K, NC, true>(Wg, n, k, row_bytes, nstages, x, y, y_ld, status, Wu);
 }
 
 template <int T, int NC>
@@ -523,6 +555,20 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(W), n,
                       (int)k, row_bytes, nstages, x, y, y_ld, static_cast<int *>(nullptr));
+}
+
+template <int NC>
+static cudaError_t launch_gemv_glu_nc(const void *Wg, const void *Wu, int64_t n, int64_t k, XIn x, float *y,
+                                      int nstages, cudaStream_t st) {
+    const int64_t row_bytes = gemv_tma_row_bytes<QMM_Q4_K>(n, k);
+    const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, NC);
+    auto kern = gemv_q4k_glu_kernel<NC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), n));
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(Wg),
+                      static_cast<const uint8_t *>(Wu), n, (int)k, row_bytes, nstages, x, y, n,
+                      static_cast<int *>(nullptr));
 }
 
 template <int T>
@@ -622,6 +668,33 @@ cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const v
     case QMM_Q8_0: return launch_gemv_t<QMM_Q8_0>(W, n, k, xq, xf, m, y, st);
     }
     return cudaErrorInvalidValue;
+}
+
+bool gemv_glu_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    if (t != QMM_Q4_K || n <= 0 || m <= 0 || m > 8 || k % 256 != 0) return false;
+    const int64_t rb = gemv_tma_row_bytes<QMM_Q4_K>(n, k);
+    const size_t budget = size_t(device_smem_optin());
+    return gemv_tma_stages(rb, k, (int)std::min<int64_t>(m, 8), budget) > 0;
+}
+
+cudaError_t launch_gemv_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n, int64_t k, const void *xq,
+                            int64_t m, float *y, cudaStream_t st) {
+    if (!gemv_glu_supported(t, n, k, m)) return cudaErrorNotSupported;
+    const int64_t rb = gemv_tma_row_bytes<QMM_Q4_K>(n, k);
+    const int nst = gemv_tma_stages(rb, k, (int)m, size_t(device_smem_optin()));
+    XIn x;
+    x.xq = static_cast<const uint8_t *>(xq);
+    x.xf = nullptr;
+    switch (m) {
+    case 1: return launch_gemv_glu_nc<1>(Wg, Wu, n, k, x, y, nst, st);
+    case 2: return launch_gemv_glu_nc<2>(Wg, Wu, n, k, x, y, nst, st);
+    case 3: return launch_gemv_glu_nc<3>(Wg, Wu, n, k, x, y, nst, st);
+    case 4: return launch_gemv_glu_nc<4>(Wg, Wu, n, k, x, y, nst, st);
+    case 5: return launch_gemv_glu_nc<5>(Wg, Wu, n, k, x, y, nst, st);
+    case 6: return launch_gemv_glu_nc<6>(Wg, Wu, n, k, x, y, nst, st);
+    case 7: return launch_gemv_glu_nc<7>(Wg, Wu, n, k, x, y, nst, st);
+    default: return launch_gemv_glu_nc<8>(Wg, Wu, n, k, x, y, nst, st);
+    }
 }
 
 bool gemv_id_supported(qmm_type t, int64_t n, int64_t k) {

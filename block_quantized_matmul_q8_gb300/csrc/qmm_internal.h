@@ -47,6 +47,11 @@ bool gemv_tma_enabled();
 size_t gemv_smem_bytes(int64_t k, int ncols);
 cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
                         float *y, cudaStream_t st);
+// Fused gate/up + SwiGLU GEMV (Q4_K, m <= 8): y[m][n] = silu(x Wg^T) * (x Wu^T) from
+// q8_1 activations, both weights read once.
+bool gemv_glu_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
+cudaError_t launch_gemv_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n, int64_t k, const void *xq,
+                            int64_t m, float *y, cudaStream_t st);
 // Expert-routed decode: one bulk-copy GEMV per (token, slot) pair, expert ids read on the
 // device; pair p's activation row is xq row p / x_div.  Invalid ids give zero rows; the
 // kernel writes *status (QMM_OK, or QMM_ERR_IDS if any id is invalid).
@@ -72,6 +77,13 @@ size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m);
 bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
 cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
                            void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st);
+
+// Fused gate/up + SwiGLU on the tensor-core GEMM (Q4_K): y[m][n_out] = silu(x Wg^T) * (x Wu^T),
+// one whole 128-column tile (64 outputs) per CTA.
+bool gemm_tc_glu_supported(qmm_type t, int64_t n_out, int64_t k, int64_t m);
+size_t gemm_tc_glu_workspace_bytes(qmm_type t, int64_t n_out, int64_t k, int64_t m);
+cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_out, int64_t k, const void *xq,
+                               int64_t m, float *y, void *ws, size_t ws_bytes, cudaStream_t st);
 
 // Expert-grouped tensor-core GEMM over a device-built tile list (see qmm_moe.h); sorted
 // pair row j takes xq row perm[j] / x_div.

@@ -138,6 +138,30 @@ QMM_API qmm_status qmm_mul_mat_f32(const void *W, qmm_type t, int64_t n, int64_t
                                    float *y, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Fused gate/up matmul with SwiGLU ([MMQ] sections "「分专家」与「整批」之间: host 侧的
+ * 代价" and "输出端: 写回与 scale 修正": the gate and up weights are loaded and dotted
+ * together and the GLU is applied right after the dots; [P0007]: fused ffn
+ * gate/up/SWIGLU):
+ *   y[m][n] = silu(x * dequant(W_gate)^T) * (x * dequant(W_up)^T),  silu(g) = g / (1 + e^-g)
+ *   W_gate, W_up : [n][k/QK] blocks of type t each, 16-byte aligned.
+ *   xq, m, y, stream : as qmm_mul_mat (y is [m][n]).
+ *   workspace : at least qmm_workspace_bytes_glu(t, n, k, m) bytes, 256-byte aligned
+ *               (may be NULL when that is 0).
+ * Paths: Q4_K, m <= 8: one bulk-copy GEMV reading both weights once (each output's
+ * gate and up rows are folded by the two halves of one warp); Q4_K, m > 8: the
+ * tensor-core GEMM with gate and up rows interleaved in its tile (one thread holds both
+ * dots of an output), whole tiles only, no stream-K; other types and shapes: the two
+ * products into the workspace, then a combine pass.  Accuracy: each dot within 1e-5
+ * of its sum of |block terms|, carried through silu(g) * u to first order, plus
+ * 2^-20 |y| for evaluating silu and the product in fp32, plus 2^-120 |u| where silu
+ * underflows fp32 (gate dots below -88.7 give 0).
+ */
+QMM_API size_t qmm_workspace_bytes_glu(qmm_type t, int64_t n, int64_t k, int64_t m);
+QMM_API qmm_status qmm_mul_mat_glu(const void *W_gate, const void *W_up, qmm_type t, int64_t n, int64_t k,
+                                   const void *xq, int64_t m, float *y, void *workspace, size_t ws_bytes,
+                                   void *stream);
+
+/*
  * Expert-routed matmul ([MMQ] sections "派发路径", "专家边界: 在 GPU 上做分段,
  * 而不是在 host 上", "MoE 的二次账"):
  *   y[t][s][:] = x[t] * dequant(W_experts[ids[t][s]])^T

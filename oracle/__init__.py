@@ -169,15 +169,17 @@ def mul_mat_glu(W_gate, W_up, fmt, n, k, xq, m):
     """(y, tol), both fp64 [m][n]: y = silu(g) * u with g, u the folds of the gate and up
     rows (each W [n][k]).  tol is the per-element bound that the GPU result must meet:
     the fold bound of each dot (1e-5 of its sum of |block terms|) carried through the
-    product to first order, plus 2^-20 of |y| for evaluating silu and the product in fp32:
-        tol = 1e-5 * (|silu'(g)| T_g |u| + |silu(g)| T_u) + 2^-20 |y|."""
+    product to first order, plus 2^-20 of |y| for evaluating silu and the product in fp32,
+    plus 2^-120 |u| for the fp32 range: e^-g overflows fp32 for g < -88.7, where the true
+    silu(g) is below 88.7 e^-88.7 < 3e-37 in magnitude and fp32 gives 0:
+        tol = 1e-5 * (|silu'(g)| T_g |u| + |silu(g)| T_u) + 2^-20 |y| + 2^-120 |u|."""
     g, Tg = mul_mat(W_gate, fmt, n, k, xq, m)
     u, Tu = mul_mat(W_up, fmt, n, k, xq, m)
     sg = 1.0 / (1.0 + np.exp(-g))
     a = g * sg
     da = sg * (1.0 + g * (1.0 - sg))
     y = a * u
-    tol = 1e-5 * (np.abs(da) * Tg * np.abs(u) + np.abs(a) * Tu) + 2.0 ** -20 * np.abs(y)
+    tol = 1e-5 * (np.abs(da) * Tg * np.abs(u) + np.abs(a) * Tu) + 2.0 ** -20 * np.abs(y) + 2.0 ** -120 * np.abs(u)
     return y, tol
 
 
