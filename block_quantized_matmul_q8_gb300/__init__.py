@@ -29,7 +29,7 @@ EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspac
            "qmm_mul_mat", "qmm_mul_mat_id", "qmm_read_device_status", "qmm_tile_efficiency_percent",
            "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode",
            "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32",
-           "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu")
+           "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu", "qmm_gemv_ring_stages")
 
 
 class QMMError(RuntimeError):
@@ -78,6 +78,8 @@ def lib():
     L.qmm_read_device_status.argtypes = [P, ctypes.POINTER(I32), P]
     L.qmm_tile_efficiency_percent.restype = ctypes.c_int
     L.qmm_tile_efficiency_percent.argtypes = [I64, I64]
+    L.qmm_gemv_ring_stages.restype = ctypes.c_int
+    L.qmm_gemv_ring_stages.argtypes = [ctypes.c_int, I64, I64, I32, I64]
     L.qmm_plan_gemm.restype = ctypes.c_int
     L.qmm_plan_gemm.argtypes = [ctypes.c_int, I64, I64, I64, I32, I32, ctypes.POINTER(GemmPlan)]
     L.qmm_plan_cta_range.restype = None
@@ -284,6 +286,10 @@ def qmm_read_device_status(workspace: torch.Tensor, stream=None) -> int:
 
 def qmm_tile_efficiency_percent(ntiles: int, nsm: int) -> int:
     return lib().qmm_tile_efficiency_percent(ntiles, nsm)
+
+
+def qmm_gemv_ring_stages(t, n: int, k: int, ncols: int, smem_bytes: int) -> int:
+    return lib().qmm_gemv_ring_stages(_qtype(t), n, k, ncols, smem_bytes)
 
 
 def qmm_plan_gemm(qtype, n: int, k: int, m: int, nsm: int, stream_k_mode: int = 0) -> GemmPlan:

@@ -336,6 +336,11 @@ int qmm_tile_efficiency_percent(int64_t ntiles, int64_t nsm) {
     return (int)(100 * ntiles / (nsm * nwaves));
 }
 
+int qmm_gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int32_t ncols, int64_t smem_bytes) {
+    if (n <= 0 || ncols < 1 || ncols > 8 || smem_bytes <= 0 || check_k(t, k) != QMM_OK) return 0;
+    return gemv_ring_stages(t, n, k, ncols, size_t(smem_bytes));
+}
+
 qmm_status qmm_plan_gemm(qmm_type t, int64_t n, int64_t k, int64_t m, int32_t nsm, int32_t stream_k_mode,
                          qmm_gemm_plan *plan) {
     qmm_status s = check_k(t, k);

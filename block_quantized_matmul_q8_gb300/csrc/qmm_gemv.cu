@@ -226,25 +226,39 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const uint8_t *__res
 // CTA per SM owns a contiguous range of rows and streams it through a ring of
 // shared-memory stages with 1D bulk copies (cp.async.bulk, completion counted on an
 // mbarrier), so every byte of W moves in large contiguous transfers and up to
-// nstages chunks per SM are in flight (up to 8 chunks of 8 rows, as many as fit next
-// to the staged activations).  A dedicated producer warp issues the copies; four
-// groups of 4 consumer warps take chunks in turn (a half-warp per row, lane l16 takes
-// units l16, l16+16, ...).
+// nstages chunks per SM are in flight (8 chunks of 8 rows, or 6, 4 or 3 where 8 do not
+// fit next to the staged activations).  A dedicated producer warp issues the copies;
+// four groups of 4 consumer warps (three for rings of 6 or 3 stages) take chunks in
+// turn (a half-warp per row, lane l16 takes units l16, l16+16, ...).
 constexpr int kTmaMaxStages = 8;
-constexpr int kTmaMinStages = 3;
 constexpr int kTmaGroups = 4;
 constexpr int kTmaGroupWarps = 4;
 constexpr int kTmaConsumerWarps = kTmaGroups * kTmaGroupWarps;
 constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
 constexpr int kTmaChunkRows = 2 * kTmaGroupWarps;  // one row per half-warp
+static_assert(kTmaMaxStages == 8 && kTmaGroups == 4, "ring depths and group splits below assume 8 stages, 4 groups");
 
-// Stages of kTmaChunkRows rows that fit next to the staged activations (0: too few).
+// Consumer groups that take a ring of nstages stages (0: no valid split).  Chunk c goes
+// to stage c % nstages and to group c % groups, and a wait on a stage's full barrier
+// names only the parity of the phase it expects.  With nstages a multiple of the group
+// count, a stage is always consumed by the same group, so the stage's previous chunk is
+// that group's own, already folded, and the phase waited for is the barrier's current
+// one.  Otherwise a group's first chunk may sit on a stage whose earlier chunk has not
+// landed: the parity of that incomplete phase reads as complete, the group reads the
+// stage early and its release throws the ring's counts off (3 stages for 4 groups
+// faulted on the GPU); other depths leave the same race open whenever one chunk lands
+// later than the chunk issued after it.
+__host__ __device__ constexpr int gemv_ring_groups(int nstages) {
+    return nstages <= 0 || nstages > kTmaMaxStages ? 0 : nstages % 4 == 0 ? 4 : nstages % 3 == 0 ? 3 : 0;
+}
+
+// Stages of kTmaChunkRows rows that fit next to the staged activations: the deepest
+// ring of 8, 6, 4 or 3 stages (4 consumer groups for 8 and 4, 3 for 6 and 3), or 0.
 int gemv_tma_stages(int64_t row_bytes, int64_t k, int ncols, size_t budget) {
     const size_t fixed = 1024 + gemv_smem_bytes(k, ncols);
-    if (fixed >= budget) return 0;
+    if (fixed >= budget || row_bytes <= 0) return 0;
     const int64_t st = int64_t(budget - fixed) / (int64_t(kTmaChunkRows) * row_bytes);
-    const int s = (int)std::min<int64_t>(st, kTmaMaxStages);
-    return s >= kTmaMinStages ? s : 0;
+    return st >= 8 ? 8 : st >= 6 ? 6 : st >= 4 ? 4 : st >= 3 ? 3 : 0;
 }
 
 
@@ -318,6 +332,13 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
     const int nchunks = (int)((r1 - r0 + kCR - 1) / kCR);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, l16 = lane & 15;
     volatile int *abortp = &abort_flag;
+    // the ring protocol needs whole rounds of stages (gemv_ring_groups): any other depth
+    // is refused before a copy is issued
+    const int ngroups = gemv_ring_groups(nstages);
+    if (ngroups == 0) {
+        if (tid == 0 && status) atomicExch(status, (int)QMM_ERR_DEVICE);
+        return;
+    }
 
     if (tid == 0) {
         abort_flag = 0;
@@ -379,7 +400,7 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
         const int rr = 2 * gw + (lane >> 4);  // row within a chunk
         const int c4 = l16 & 3;               // qs chunk of every unit this lane takes (Q4_K)
         const Q4KPairSel psel = q4k_pair_sel(c4);
-        for (int c = grp; c < nchunks; c += kTmaGroups) {
+        for (int c = grp; grp < ngroups && c < nchunks; c += ngroups) {
             const int s = c % nstages;
             if (!ptx::mbar_wait(ptx::smem_u32(&full[s]), (c / nstages) & 1, abortp)) break;
             const int64_t a = r0 + int64_t(c) * kCR;
@@ -538,6 +559,17 @@ template <int T> static int64_t gemv_tma_row_bytes(int64_t n, int64_t k) {
     if (rb % 16 == 0) return rb;
     if (T == QMM_Q6_K && rb % 8 == 0 && n % 2 == 0) return rb;
     return 0;
+}
+
+int gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int ncols, size_t budget) {
+    int64_t rb = 0;
+    switch (t) {
+    case QMM_Q4_K: rb = gemv_tma_row_bytes<QMM_Q4_K>(n, k); break;
+    case QMM_Q6_K: rb = gemv_tma_row_bytes<QMM_Q6_K>(n, k); break;
+    case QMM_Q8_0: rb = gemv_tma_row_bytes<QMM_Q8_0>(n, k); break;
+    default: return 0;
+    }
+    return rb > 0 ? gemv_tma_stages(rb, k, ncols, budget) : 0;
 }
 
 template <int T, int NC>

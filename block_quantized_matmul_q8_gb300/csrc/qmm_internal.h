@@ -45,6 +45,8 @@ bool gemv_tma_enabled();
 // (xq) or as fp32 values (xf != nullptr), which each CTA then quantizes itself to the
 // same bytes as launch_quantize_q8_1.  Columns are taken in groups of up to 8 per launch.
 size_t gemv_smem_bytes(int64_t k, int ncols);
+// ring depth of the bulk-copy GEMV for ncols columns in budget bytes (0: direct kernel)
+int gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int ncols, size_t budget);
 cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
                         float *y, cudaStream_t st);
 // Fused gate/up + SwiGLU GEMV (Q4_K, m <= 8): y[m][n] = silu(x Wg^T) * (x Wu^T) from

@@ -267,6 +267,19 @@ QMM_API qmm_status qmm_plan_gemm(qmm_type t, int64_t n, int64_t k, int64_t m, in
  * + k-iteration) that CTA `cta` of the plan processes. */
 QMM_API void qmm_plan_cta_range(const qmm_gemm_plan *plan, int32_t cta, int64_t *begin, int64_t *end);
 
+/* Ring depth of the bulk-copy GEMV, which streams the weight rows once through
+ * shared-memory stages ([MMQ] section "与 MMVQ 的边界": the m <= 8 path is bound by
+ * reading W), for one launch of ncols (1..8) activation columns,
+ * given smem_bytes of shared memory per block: the deepest of 8, 6, 4 or 3 stages of 8
+ * weight rows that fits.  The consumer groups take the stages in turn, 4 groups for 8
+ * and 4 stages, 3 for 6 and 3, so that each stage always goes to the same group.  0
+ * when the rows cannot be streamed in whole 16-byte units (Q8_0 unless k/32 is a
+ * multiple of 8; Q6_K unless k/256 is a multiple of 8, or of 4 with n even) or when not
+ * even 3 stages fit next to the staged activations (Q4_K at one column from k = 15616
+ * on, with 227 KB): the call then runs on the direct-load GEMV kernel.  Bad arguments
+ * give 0. */
+QMM_API int qmm_gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int32_t ncols, int64_t smem_bytes);
+
 /* ------------------------------------------------------------------ test controls
  * Process-wide switches for tests and benchmarks; read at every call. */
 

@@ -139,3 +139,46 @@ def test_plan_partitions_all_work_exactly_once(n, k, m, nsm, mode):
         assert p.ctas == min(nsm, p.nwork)
         sizes = [qmm.qmm_plan_cta_range(p, c)[1] - qmm.qmm_plan_cta_range(p, c)[0] for c in range(p.ctas)]
         assert max(sizes) - min(sizes) <= 1
+
+
+# Ring depth of the bulk-copy GEMV: stages of 8 weight rows next to the staged
+# activations (ncols units of 64 values, 96 bytes each, plus 1 KB of alignment slack),
+# at most 8, and only depths that 4 or 3 consumer groups split into whole stages each.
+ROW = {"q4_K": lambda k: k // 256 * 144, "q6_K": lambda k: k // 256 * 210, "q8_0": lambda k: k // 32 * 34}
+
+
+def expected_depth(fmt, n, k, ncols, budget):
+    rb = ROW[fmt](k)
+    if rb % 16 and not (fmt == "q6_K" and rb % 8 == 0 and n % 2 == 0):
+        return 0
+    fixed = 1024 + ncols * ((k + 63) // 64) * 96
+    if fixed >= budget:
+        return 0
+    st = (budget - fixed) // (8 * rb)
+    return max([d for d in (8, 6, 4, 3) if d <= st], default=0)
+
+
+def test_gemv_ring_depth_whole_rounds(L):
+    budget = 227 * 1024
+    seen = set()
+    for fmt, ks in (("q4_K", range(256, 40000, 256)), ("q6_K", range(256, 30000, 256)),
+                    ("q8_0", range(32, 20000, 32))):
+        for k in ks:
+            for ncols in (1, 2, 5, 8):
+                for n in (4096, 4097):
+                    d = qmm.qmm_gemv_ring_stages(fmt, n, k, ncols, budget)
+                    assert d in (0, 3, 4, 6, 8), (fmt, n, k, ncols, d)
+                    assert d == expected_depth(fmt, n, k, ncols, budget), (fmt, n, k, ncols, d)
+                    seen.add(d)
+    assert seen == {0, 3, 4, 6, 8}
+    # shapes where 3, 5, 6 or 7 stages fit
+    assert qmm.qmm_gemv_ring_stages("q4_K", 4096, 14336, 1, budget) == 3
+    assert qmm.qmm_gemv_ring_stages("q8_0", 5120, 8192, 1, budget) == 3
+    assert qmm.qmm_gemv_ring_stages("q8_0", 5120, 5120, 1, budget) == 4
+    assert qmm.qmm_gemv_ring_stages("q6_K", 151936, 5120, 1, budget) == 6
+    assert qmm.qmm_gemv_ring_stages("q4_K", 4096, 15616, 1, budget) == 0
+    assert qmm.qmm_gemv_ring_stages("q4_K", 17408, 5120, 1, budget) == 8
+    # bad arguments
+    assert qmm.qmm_gemv_ring_stages("q4_K", 0, 5120, 1, budget) == 0
+    assert qmm.qmm_gemv_ring_stages("q4_K", 16, 5000, 1, budget) == 0
+    assert qmm.qmm_gemv_ring_stages("q4_K", 16, 5120, 9, budget) == 0
