@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qmm_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle_qmm.so")
 
-TYPES = {"q8_0": 8, "q4_K": 12, "q6_K": 14}
+TYPES = {"q4_0": 2, "q8_0": 8, "q4_K": 12, "q6_K": 14}
 _lib = None
 
 

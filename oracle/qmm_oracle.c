@@ -28,6 +28,12 @@
  *   - Q6_K block = {ql[128], qh[64], int8 sc[16], fp16 d}; bit placement as pinned by
  *     the index arithmetic in [MMQ] "Q6_K: 6 位数据要多占一半的共享内存"; code - 32.
  *   - Q8_0 block = {fp16 d, int8 q[32]}.
+ *   - Q4_0 block = {fp16 d, 16 B nibbles} (18 B per 32 weights, [MMQ] sections
+ *     "tile_x_sizes" and "Q4_0: 一个 get_int_b2 搬进 8 个 4-bit"): byte i holds weight i
+ *     in its low nibble and weight 16+i in its high nibble (the load side splits the
+ *     nibbles of a word into the front and back halves of the block); the value is
+ *     d*(q - 8), and the dot takes the offset codes q - 8 in -8..7 as its integers,
+ *     as the load side does with __vsub4 before the dot.
  *
  * Parity status: every exported function is pinned by tests under tests/ against
  * closed forms, library routines, brute force or the pages' printed sizes
@@ -43,7 +49,7 @@
 
 #define ORACLE_API __attribute__((visibility("default")))
 
-enum { OT_Q8_0 = 8, OT_Q4_K = 12, OT_Q6_K = 14 };
+enum { OT_Q4_0 = 2, OT_Q8_0 = 8, OT_Q4_K = 12, OT_Q6_K = 14 };
 
 /* ---------------------------------------------------------------- fp16 */
 
@@ -144,12 +150,13 @@ ORACLE_API int oracle_dequant_q8_1(const uint8_t *xq, int64_t m, int64_t k, doub
 
 /* ---------------------------------------------------------------- weight blocks */
 
-static int block_elems(int type) { return type == OT_Q8_0 ? 32 : 256; }
+static int block_elems(int type) { return type == OT_Q8_0 || type == OT_Q4_0 ? 32 : 256; }
 static int block_bytes(int type) {
     switch (type) {
     case OT_Q4_K: return 144;
     case OT_Q6_K: return 210;
     case OT_Q8_0: return 34;
+    case OT_Q4_0: return 18;
     default: return -1;
     }
 }
@@ -182,6 +189,12 @@ static int q6k_value(const uint8_t *blk, int i) {
     int low = (ql[64 * h + l + 32 * (t & 1)] >> (4 * (t >> 1))) & 0x0f;
     int high = (qh[32 * h + l] >> (2 * t)) & 3;
     return (low | (high << 4)) - 32;
+}
+
+/* Q4_0 weight i (0..31): its offset code q - 8, in -8..7. */
+static int q40_value(const uint8_t *blk, int i) {
+    const uint8_t *qs = blk + 2;
+    return (i < 16 ? (qs[i] & 0x0f) : (qs[i - 16] >> 4)) - 8;
 }
 
 /* Decoded fields of one Q4_K block, for tests. */
@@ -221,6 +234,9 @@ ORACLE_API int oracle_dequant(int type, const uint8_t *W, int64_t n, int64_t k, 
             } else if (type == OT_Q6_K) {
                 double d = h2d(blk + 208);
                 for (int i = 0; i < 256; ++i) o[i] = d * (int8_t)blk[192 + i / 16] * q6k_value(blk, i);
+            } else if (type == OT_Q4_0) {
+                double d = h2d(blk);
+                for (int i = 0; i < 32; ++i) o[i] = d * q40_value(blk, i);
             } else {
                 double d = h2d(blk);
                 for (int i = 0; i < 32; ++i) o[i] = d * (int8_t)blk[2 + i];
@@ -240,6 +256,7 @@ ORACLE_API int oracle_dequant(int type, const uint8_t *W, int64_t n, int64_t k, 
  * Q6_K ([MMQ] "Q6_K: 子块尺度与 q8_1 块长错位"): per 16-wide sub-block j,
  *     d*sc_j*d8_{j/2}*sumi_j.
  * Q8_0: per 32-block, d_w*d8*sumi.
+ * Q4_0: per 32-block, d_w*d8*sumi with sumi over the offset codes q - 8.
  */
 static void fold_one(int type, const uint8_t *wrow, const uint8_t *xrow, int64_t k, double *y, double *T) {
     double acc = 0.0, tabs = 0.0;
@@ -276,6 +293,16 @@ static void fold_one(int type, const uint8_t *wrow, const uint8_t *xrow, int64_t
                 acc += t;
                 tabs += fabs(t);
             }
+        }
+    } else if (type == OT_Q4_0) {
+        for (int64_t b = 0; b < k / 32; ++b) {
+            const uint8_t *blk = wrow + b * 18;
+            const uint8_t *xb = xrow + b * 36;
+            int64_t sumi = 0;
+            for (int i = 0; i < 32; ++i) sumi += (int64_t)q40_value(blk, i) * (int8_t)xb[4 + i];
+            double t = h2d(blk) * h2d(xb) * (double)sumi;
+            acc += t;
+            tabs += fabs(t);
         }
     } else {
         for (int64_t b = 0; b < k / 32; ++b) {

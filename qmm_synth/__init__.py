@@ -15,10 +15,14 @@ Block byte layouts (what each generator fills):
   int8 sub-block scales at 192, fp16 ``d`` at 208.  Uniform ql/qh bytes give
   uniform 6-bit codes.
 * Q8_0, 34 bytes per 32 weights: fp16 ``d`` at 0, 32 int8 at 2.
+* Q4_0, 18 bytes per 32 weights: fp16 ``d`` at 0, 16 bytes of nibbles at 2.  Uniform
+  bytes give nibble codes uniform on 0..15.
 
 Workload shapes and value ranges follow the pages' workloads: Q4_K with
 d, dmin uniform on [1e-4, 1e-3]; Q6_K with int8 sub-scales uniform on -64..63 and
 d uniform on [1e-5, 1e-4]; Q8_0 with int8 uniform and d uniform on [1e-3, 1e-2];
+Q4_0 (the pages time it at 8192 x 4096 without giving a value distribution) with
+nibbles uniform and d uniform on [1e-3, 1e-2];
 activations N(0, 1) in fp32; MoE routing top-8 of 128 experts drawn without
 replacement with Zipf(1.1) weights.
 """
@@ -29,8 +33,8 @@ import numpy as np
 QK_K = 256
 QK8_0 = 32
 QK8_1 = 32
-BLOCK_BYTES = {"q4_K": 144, "q6_K": 210, "q8_0": 34}
-BLOCK_ELEMS = {"q4_K": QK_K, "q6_K": QK_K, "q8_0": QK8_0}
+BLOCK_BYTES = {"q4_K": 144, "q6_K": 210, "q8_0": 34, "q4_0": 18}
+BLOCK_ELEMS = {"q4_K": QK_K, "q6_K": QK_K, "q8_0": QK8_0, "q4_0": QK8_0}
 Q8_1_BLOCK_BYTES = 36
 
 
@@ -85,7 +89,18 @@ def gen_q8_0(rng, n: int, k: int, d_range=(1e-3, 1e-2)) -> np.ndarray:
     return blk.reshape(n, nb * 34)
 
 
-GEN = {"q4_K": gen_q4_K, "q6_K": gen_q6_K, "q8_0": gen_q8_0}
+def gen_q4_0(rng, n: int, k: int, d_range=(1e-3, 1e-2)) -> np.ndarray:
+    """Random Q4_0 matrix as uint8 of shape (n, k/32*18); nibble codes uniform on 0..15."""
+    nb = k // QK8_0
+    if k % QK8_0:
+        raise ValueError("k must be a multiple of 32 for Q4_0")
+    blk = np.empty((n, nb, 18), dtype=np.uint8)
+    blk[:, :, 2:] = rng.integers(0, 256, size=(n, nb, 16), dtype=np.uint8)
+    blk[:, :, 0:2] = _fp16_uniform(rng, (n, nb), *d_range).view(np.uint8).reshape(n, nb, 2)
+    return blk.reshape(n, nb * 18)
+
+
+GEN = {"q4_K": gen_q4_K, "q6_K": gen_q6_K, "q8_0": gen_q8_0, "q4_0": gen_q4_0}
 
 
 def gen_weights(fmt: str, rng, n: int, k: int) -> np.ndarray:
@@ -124,6 +139,7 @@ WORKLOADS = {
     "prefill_q4K_n4100_k4096": dict(fmt="q4_K", n=4100, k=4096, m=(512,)),
     "mixed_q6K_n151936_k5120": dict(fmt="q6_K", n=151936, k=5120, m=(1, 512)),
     "mixed_q80_n5120_k5120": dict(fmt="q8_0", n=5120, k=5120, m=(1, 512)),
+    "q40_n8192_k4096": dict(fmt="q4_0", n=8192, k=4096, m=(1, 512)),
     "moe_q4K_e128_n1536_k4096_t512_top8": dict(fmt="q4_K", n=1536, k=4096, n_experts=128, n_tokens=512, top_k=8),
 }
 

@@ -16,6 +16,8 @@ forms.  They hold no matmul arithmetic.
   for t < 2, high nibble for t >= 2) and its high 2 bits from bits 2t..2t+1 of
   qh[32h + l]; the stored code is value + 32.
 * Q8_0: {fp16 d, int8 q[32]}.   q8_1: {fp16 d, fp16 s, int8 q[32]}.
+* Q4_0: {fp16 d, 16 B nibbles}: weight i (i < 16) is the low nibble of byte i and
+  weight 16 + i its high nibble; the stored code is value + 8.
 """
 from __future__ import annotations
 
@@ -75,6 +77,16 @@ def pack_q8_0(d: float, q: np.ndarray) -> np.ndarray:
     b = np.zeros(34, dtype=np.uint8)
     b[0:2] = f16_bytes(d)
     b[2:] = np.asarray(q, dtype=np.int8).view(np.uint8)
+    return b
+
+
+def pack_q4_0(d: float, q: np.ndarray) -> np.ndarray:
+    """q: 32 codes in 0..15 (value + 8)."""
+    q = np.asarray(q, dtype=np.int64)
+    assert q.shape == (32,) and q.min() >= 0 and q.max() < 16
+    b = np.zeros(18, dtype=np.uint8)
+    b[0:2] = f16_bytes(d)
+    b[2:] = (q[:16] | (q[16:] << 4)).astype(np.uint8)
     return b
 
 

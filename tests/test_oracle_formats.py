@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import qmm_synth
-from blockpack import pack_q4_K, pack_q6_K, pack_q8_0, pack_q8_1, unpack_q8_1
+from blockpack import pack_q4_0, pack_q4_K, pack_q6_K, pack_q8_0, pack_q8_1, unpack_q8_1
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -37,7 +37,10 @@ def test_block_sizes_match_pages(oracle_mod):
     assert oracle_mod.quantize_q8_1(x).nbytes == t["value"] * 4
     # Q6_K: 128 B ql + 64 B qh + 16 B scales + 2 B d (by construction of the reading).
     assert oracle_mod.block_bytes("q6_K") == 210
-    for fmt in ("q4_K", "q6_K", "q8_0"):
+    q40 = n * (k // oracle_mod.block_elems("q4_0")) * oracle_mod.block_bytes("q4_0")
+    assert round(q40 / 1e6, 1) == mb["q4_0"]
+    assert oracle_mod.block_elems("q4_0") == 32
+    for fmt in ("q4_K", "q6_K", "q8_0", "q4_0"):
         assert qmm_synth.BLOCK_BYTES[fmt] == oracle_mod.block_bytes(fmt)
 
 
@@ -222,3 +225,26 @@ def test_q8_0_decode(oracle_mod):
     q = np.arange(-16, 16)
     w = oracle_mod.dequant(pack_q8_0(0.5, q), "q8_0", 1, 32)[0]
     assert np.array_equal(w, 0.5 * q)
+
+
+def test_q4_0_nibble_positions_and_offset(oracle_mod):
+    """Byte i's low nibble is weight i and its high nibble weight 16 + i; the value is
+    d * (code - 8), so code 8 everywhere decodes to exact zeros."""
+    w = oracle_mod.dequant(pack_q4_0(0.25, np.full(32, 8)), "q4_0", 1, 32)[0]
+    assert np.array_equal(w, np.zeros(32))
+    for i in range(32):
+        q = np.full(32, 8)
+        q[i] = 15
+        w = oracle_mod.dequant(pack_q4_0(0.25, q), "q4_0", 1, 32)[0]
+        assert list(np.nonzero(w)[0]) == [i] and w[i] == 0.25 * 7
+    # raw bytes: byte 3 = 0x1f puts code 15 at weight 3 and code 1 at weight 19
+    blk = pack_q4_0(1.0, np.full(32, 8))
+    blk[2 + 3] = 0x1F
+    w = oracle_mod.dequant(blk, "q4_0", 1, 32)[0]
+    assert w[3] == 7 and w[19] == -7 and np.count_nonzero(w) == 2
+
+
+def test_q4_0_decode_all_codes(oracle_mod):
+    q = np.concatenate([np.arange(16), np.arange(15, -1, -1)])
+    w = oracle_mod.dequant(pack_q4_0(-0.5, q), "q4_0", 1, 32)[0]
+    assert np.array_equal(w, -0.5 * (q - 8))

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import qmm_synth
-from blockpack import pack_q4_K, pack_q6_K, pack_q8_0, pack_q8_1
+from blockpack import pack_q4_0, pack_q4_K, pack_q6_K, pack_q8_0, pack_q8_1
 
 
 def _q8_1_rows(q: np.ndarray, d: np.ndarray, s: np.ndarray) -> np.ndarray:
@@ -78,7 +78,23 @@ def test_q8_0_integer_matmul_special_case(oracle_mod):
     assert np.array_equal(y, (Qx @ Qw.T).astype(np.float64))
 
 
-@pytest.mark.parametrize("fmt", ["q6_K", "q8_0"])
+def test_q4_0_integer_matmul_special_case(oracle_mod):
+    """d = 1 and q8_1 d = 1: the fold is the integer matmul of the offset codes q - 8
+    with the int8 activations (the q8_1 s plays no part)."""
+    rng = np.random.default_rng(25)
+    n, k, m = 5, 384, 3
+    Qw = rng.integers(0, 16, (n, k))
+    W = np.stack([np.concatenate([pack_q4_0(1.0, Qw[r, 32 * b:32 * b + 32]) for b in range(k // 32)]) for r in range(n)])
+    Qx = rng.integers(-127, 128, (m, k))
+    xq = _q8_1_rows(Qx, np.ones((m, k // 32)), rng.uniform(-3, 3, (m, k // 32)))
+    y, T = oracle_mod.mul_mat(W, "q4_0", n, k, xq, m)
+    assert np.array_equal(y, (Qx @ (Qw - 8).T).astype(np.float64))
+    # T: per 32-block |d_w d8 sumi|
+    blk = np.abs(np.einsum("mbi,nbi->mnb", Qx.reshape(m, -1, 32), (Qw - 8).reshape(n, -1, 32)))
+    assert np.array_equal(T, blk.sum(axis=2).astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt", ["q6_K", "q8_0", "q4_0"])
 def test_brute_force_agrees(oracle_mod, fmt):
     """Without a min term the fold equals the fp64 matmul of dequantized W and
     dequantized q8_1 x up to fp64 rounding; and the brute force itself equals
