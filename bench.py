@@ -364,6 +364,7 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
     out.update(dense("q4_K", 4100, 4096, [512]))
     out.update(dense("q6_K", 151936, 5120, [1, 512]))
     out.update(dense("q8_0", 5120, 5120, [1, 512]))
+    out.update(dense("q4_0", 8192, 4096, [1, 512]))
     out.update(glu(14336, 4096, [1, 512]))
     # MoE: 128 experts x Q4_K n=1536 k=4096, 512 tokens top-8 Zipf(1.1); and its decode
     # form, one token top-8, whose calls route to disjoint sets of 8 experts in turn (16

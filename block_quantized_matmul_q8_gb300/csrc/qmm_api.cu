@@ -49,7 +49,7 @@ int device_smem_optin() {
     return v;
 }
 
-static bool type_ok(qmm_type t) { return t == QMM_Q4_K || t == QMM_Q6_K || t == QMM_Q8_0; }
+static bool type_ok(qmm_type t) { return t == QMM_Q4_K || t == QMM_Q6_K || t == QMM_Q8_0 || t == QMM_Q4_0; }
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }

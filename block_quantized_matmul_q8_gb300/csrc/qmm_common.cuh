@@ -5,15 +5,17 @@
 //   Q4_K 144 B: fp16 d | fp16 dmin | 12 B packed 6-bit scales/mins | 128 B nibbles
 //   Q6_K 210 B: ql[128] | qh[64] | int8 sc[16] | fp16 d
 //   Q8_0 34 B: fp16 d | int8 q[32]
+//   Q4_0 18 B: fp16 d | 16 B nibbles (byte i: weight i low, weight 16+i high; d*(q-8))
 //
 // Work is cut into "units" of 64 consecutive k values of one weight row: a quarter
-// superblock for Q4_K / Q6_K, two blocks for Q8_0.  A unit always lines up with two
+// superblock for Q4_K / Q6_K, two blocks for Q8_0 and Q4_0.  A unit always lines up with two
 // q8_1 activation blocks (2u, 2u+1), so one decode routine serves the GEMV and the
 // CUDA-core GEMM.  A decoded unit holds
 //   q[16]   : 64 signed 8-bit weight codes, 4 per word, in k order
 //   isc[4]  : integer scale of each 16-wide quarter (Q4_K: the 6-bit sub-block scale,
-//             twice per 32-block; Q6_K: the int8 sub-scale; Q8_0: 1)
-//   fd[2]   : fp32 factor of each 32-block's integer dot (Q4_K/Q6_K: d, Q8_0: d of the block)
+//             twice per 32-block; Q6_K: the int8 sub-scale; Q8_0, Q4_0: 1)
+//   fd[2]   : fp32 factor of each 32-block's integer dot (Q4_K/Q6_K: d, Q8_0/Q4_0: d of
+//             the block)
 //   fm[2]   : fp32 factor of each 32-block's min term (Q4_K: dmin*m, otherwise 0)
 // so that one 32-block's term is  fd * d8 * (isc0*dot16_0 + isc1*dot16_1) - fm * s8
 // ([MMQ] sections "dp4a 路径的 Q4_K" and "Q6_K: 子块尺度与 q8_1 块长错位").
@@ -28,6 +30,7 @@ namespace qmm {
 constexpr int kQ4KBytes = 144;
 constexpr int kQ6KBytes = 210;
 constexpr int kQ80Bytes = 34;
+constexpr int kQ40Bytes = 18;
 constexpr int kQ81Bytes = 36;
 
 struct Unit {
@@ -38,9 +41,13 @@ struct Unit {
 };
 
 __host__ __device__ constexpr int block_bytes(int t) {
-    return t == QMM_Q4_K ? kQ4KBytes : t == QMM_Q6_K ? kQ6KBytes : t == QMM_Q8_0 ? kQ80Bytes : 0;
+    return t == QMM_Q4_K ? kQ4KBytes
+           : t == QMM_Q6_K ? kQ6KBytes
+           : t == QMM_Q8_0 ? kQ80Bytes
+           : t == QMM_Q4_0 ? kQ40Bytes
+                           : 0;
 }
-__host__ __device__ constexpr int block_elems(int t) { return t == QMM_Q8_0 ? 32 : 256; }
+__host__ __device__ constexpr int block_elems(int t) { return t == QMM_Q8_0 || t == QMM_Q4_0 ? 32 : 256; }
 
 __device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
 __device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
@@ -245,6 +252,54 @@ __device__ __forceinline__ void decode_q8_0(const uint8_t *row, int u, bool two,
     o.fm[0] = o.fm[1] = 0.f;
 }
 
+// Q4_0 codes of one block from its 16 nibble bytes held in 4 words: the low nibbles
+// are weights 0..15, the high nibbles weights 16..31 ([MMQ] section "Q4_0: 一个
+// get_int_b2 搬进 8 个 4-bit": the two nibble halves of a word go to the front and back
+// halves of the block); q - 8 per byte with one __vsub4, as the load side there does.
+__device__ __forceinline__ void q4_0_codes(const uint32_t (&qs)[4], int *q8) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        q8[i] = (int)__vsub4(qs[i] & 0x0f0f0f0fu, 0x08080808u);
+        q8[4 + i] = (int)__vsub4((qs[i] >> 4) & 0x0f0f0f0fu, 0x08080808u);
+    }
+}
+
+// Q4_0 unit u: blocks 2u and 2u+1 (36 bytes at offset 36u of the row).  Words w[0..8]
+// of a two-block unit: w[0] = d0 | qs0[0..1], w[1..3] = qs0[2..13], w[4] = qs0[14..15] |
+// d1, w[5..8] = qs1.  Rows with an odd block count are only 2-byte aligned; as for
+// Q8_0, a two-block unit is then never the last of its row, and a single-block unit
+// reads its 18 bytes as 4 words plus one 2-byte load.
+__device__ __forceinline__ void q4_0_unit_from_words(const uint32_t (&w)[9], bool two, Unit &o) {
+    uint32_t qa[4], qb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) qa[i] = __funnelshift_r(w[i], w[i + 1], 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) qb[i] = w[5 + i];
+    q4_0_codes(qa, o.q);
+    q4_0_codes(qb, o.q + 8);
+    o.isc[0] = o.isc[1] = o.isc[2] = o.isc[3] = 1;
+    o.fd[0] = half_lo(w[0]);
+    o.fd[1] = two ? half_hi(w[4]) : 0.f;
+    o.fm[0] = o.fm[1] = 0.f;
+}
+
+__device__ __forceinline__ void decode_q4_0(const uint8_t *row, int u, bool two, Unit &o) {
+    const uint8_t *p = row + 36 * u;
+    uint32_t w[9];
+    if (two) {
+        ldg_words_a2<9>(p, w);
+    } else {
+        uint32_t a[4];
+        ldg_words_a2<4>(p, a);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = a[i];
+        w[4] = ldg2(p + 16);
+#pragma unroll
+        for (int i = 5; i < 9; ++i) w[i] = 0u;
+    }
+    q4_0_unit_from_words(w, two, o);
+}
+
 // ---------------------------------------------------------------------------
 // Two-phase decode for latency hiding: load_raw<T> issues only the loads of one unit
 // (no arithmetic on loaded data, so a caller can put many units' loads in flight
@@ -255,9 +310,10 @@ template <int T> struct Raw;
 template <> struct Raw<QMM_Q4_K> { uint4 h, a, b; };
 template <> struct Raw<QMM_Q6_K> { uint32_t ql[17], qh[9], sc[5]; uint32_t shift; };
 template <> struct Raw<QMM_Q8_0> { uint32_t w[18]; uint32_t shift; bool two; };
+template <> struct Raw<QMM_Q4_0> { uint32_t w[10]; uint32_t shift; bool two; };
 
 // units per lane kept in flight by the GEMV
-template <int T> constexpr int kRawChunk = T == QMM_Q4_K ? 5 : T == QMM_Q6_K ? 2 : 3;
+template <int T> constexpr int kRawChunk = T == QMM_Q4_K ? 5 : T == QMM_Q6_K ? 2 : T == QMM_Q4_0 ? 5 : 3;
 
 template <class Ld = LdGlobal>
 __device__ __forceinline__ void load_raw(const uint8_t *row, int u, int, Raw<QMM_Q4_K> &r) {
@@ -384,10 +440,47 @@ __device__ __forceinline__ void convert_raw(const Raw<QMM_Q8_0> &r, int, Unit &o
     o.fm[0] = o.fm[1] = 0.f;
 }
 
+// Q4_0: a unit of two blocks is 36 bytes at 36u, 2-byte aligned when the row's block
+// count is odd (then only single-block units end a row).  Misaligned, the 10 words
+// [36u-2, 36u+38) stay inside the row's bytes plus the next unit's; a single-block unit
+// reads exactly [36u, 36u+18) (or from 36u-2).
+template <class Ld = LdGlobal>
+__device__ __forceinline__ void load_raw(const uint8_t *row, int u, int nblk32, Raw<QMM_Q4_0> &r) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row + 36 * u);
+    const uint32_t mis = (uint32_t)(a & 2u);
+    r.shift = mis * 8u;
+    r.two = 2 * u + 1 < nblk32;
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(a - mis);
+    if (r.two) {
+#pragma unroll
+        for (int i = 0; i < 9; ++i) r.w[i] = Ld::u32(p + i);
+        r.w[9] = mis ? Ld::u32(p + 9) : 0u;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r.w[i] = Ld::u32(p + i);
+        r.w[4] = mis ? Ld::u32(p + 4) : Ld::u16(p + 4);
+#pragma unroll
+        for (int i = 5; i < 10; ++i) r.w[i] = 0u;
+    }
+}
+
+__device__ __forceinline__ void convert_raw(const Raw<QMM_Q4_0> &r, int, Unit &o) {
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) w[i] = __funnelshift_r(r.w[i], r.w[i + 1], r.shift);
+    if (!r.two) {
+        w[4] &= 0xffffu;
+#pragma unroll
+        for (int i = 5; i < 9; ++i) w[i] = 0u;
+    }
+    q4_0_unit_from_words(w, r.two, o);
+}
+
 template <int T>
 __device__ __forceinline__ void decode_unit(const uint8_t *row, int u, int nblk32, Unit &o) {
     if constexpr (T == QMM_Q4_K) decode_q4_K(row, u, o);
     else if constexpr (T == QMM_Q6_K) decode_q6_K(row, u, o);
+    else if constexpr (T == QMM_Q4_0) decode_q4_0(row, u, 2 * u + 1 < nblk32, o);
     else decode_q8_0(row, u, 2 * u + 1 < nblk32, o);
 }
 

@@ -230,6 +230,7 @@ static cudaError_t launch_dp4a(qmm_type t, const DP4AGemmArgs &args, int64_t tot
     case QMM_Q4_K: return launch_dp4a_t<QMM_Q4_K>(args, total_hint, st);
     case QMM_Q6_K: return launch_dp4a_t<QMM_Q6_K>(args, total_hint, st);
     case QMM_Q8_0: return launch_dp4a_t<QMM_Q8_0>(args, total_hint, st);
+    case QMM_Q4_0: return launch_dp4a_t<QMM_Q4_0>(args, total_hint, st);
     }
     return cudaErrorInvalidValue;
 }

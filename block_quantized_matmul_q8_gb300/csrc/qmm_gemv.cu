@@ -567,6 +567,7 @@ int gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int ncols, size_t budget)
     case QMM_Q4_K: rb = gemv_tma_row_bytes<QMM_Q4_K>(n, k); break;
     case QMM_Q6_K: rb = gemv_tma_row_bytes<QMM_Q6_K>(n, k); break;
     case QMM_Q8_0: rb = gemv_tma_row_bytes<QMM_Q8_0>(n, k); break;
+    case QMM_Q4_0: rb = gemv_tma_row_bytes<QMM_Q4_0>(n, k); break;
     default: return 0;
     }
     return rb > 0 ? gemv_tma_stages(rb, k, ncols, budget) : 0;
@@ -698,6 +699,7 @@ cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const v
     case QMM_Q4_K: return launch_gemv_t<QMM_Q4_K>(W, n, k, xq, xf, m, y, st);
     case QMM_Q6_K: return launch_gemv_t<QMM_Q6_K>(W, n, k, xq, xf, m, y, st);
     case QMM_Q8_0: return launch_gemv_t<QMM_Q8_0>(W, n, k, xq, xf, m, y, st);
+    case QMM_Q4_0: return launch_gemv_t<QMM_Q4_0>(W, n, k, xq, xf, m, y, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -735,6 +737,7 @@ bool gemv_id_supported(qmm_type t, int64_t n, int64_t k) {
     case QMM_Q4_K: rb = gemv_tma_row_bytes<QMM_Q4_K>(n, k); break;
     case QMM_Q6_K: rb = gemv_tma_row_bytes<QMM_Q6_K>(n, k); break;
     case QMM_Q8_0: rb = gemv_tma_row_bytes<QMM_Q8_0>(n, k); break;
+    case QMM_Q4_0: rb = gemv_tma_row_bytes<QMM_Q4_0>(n, k); break;
     }
     return n > 0 && rb > 0 && gemv_tma_stages(rb, k, 1, size_t(device_smem_optin())) > 0;
 }
@@ -746,6 +749,7 @@ cudaError_t launch_gemv_id(qmm_type t, const void *W, int64_t n_experts, int64_t
     case QMM_Q4_K: return launch_gemv_id_t<QMM_Q4_K>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
     case QMM_Q6_K: return launch_gemv_id_t<QMM_Q6_K>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
     case QMM_Q8_0: return launch_gemv_id_t<QMM_Q8_0>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
+    case QMM_Q4_0: return launch_gemv_id_t<QMM_Q4_0>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -2,7 +2,7 @@
  * qmm.h -- C ABI of the block-quantized matmul library for GB300 (sm_103a).
  *
  * The library computes y[m][n] = sum_k x[m][k] * dequant(W)[n][k] with W kept in
- * its block-quantized form (Q4_K, Q6_K or Q8_0) and x quantized to q8_1 first.
+ * its block-quantized form (Q4_K, Q6_K, Q8_0 or Q4_0) and x quantized to q8_1 first.
  * Every product is formed from exact integer sub-block dot products that are
  * then folded with the block scales in fp32.
  *
@@ -33,6 +33,10 @@
  *   Q6_K (210 B / 256):      ql[128], qh[64], int8 scales[16], fp16 d;
  *        w = d*sc*(code-32) ([MMQ] section "Q6_K: 6 位数据要多占一半的共享内存").
  *   Q8_0 (34 B / 32):        fp16 d, int8 q[32]; w = d*q.
+ *   Q4_0 (18 B / 32):        fp16 d, 16 B of nibbles, byte i holding weight i in its
+ *        low nibble and weight 16+i in its high nibble; w = d*(q-8), and the integer
+ *        dot runs on the offset codes q-8 ([MMQ] sections "tile_x_sizes" and
+ *        "Q4_0: 一个 get_int_b2 搬进 8 个 4-bit").
  */
 #ifndef QMM_H
 #define QMM_H
@@ -50,7 +54,7 @@
 extern "C" {
 #endif
 
-typedef enum { QMM_Q8_0 = 8, QMM_Q4_K = 12, QMM_Q6_K = 14 } qmm_type;
+typedef enum { QMM_Q4_0 = 2, QMM_Q8_0 = 8, QMM_Q4_K = 12, QMM_Q6_K = 14 } qmm_type;
 
 typedef enum {
     QMM_OK = 0,
@@ -103,7 +107,7 @@ QMM_API qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void 
  *   xq     : q8_1 blocks of x [m][k] as written by qmm_quantize_q8_1.
  *   y      : fp32 [m][n] output, 16-byte aligned; every element is written.
  *   workspace, ws_bytes: at least qmm_workspace_bytes(t, n, k, m, 0, 0) bytes.
- * k % 256 == 0 for Q4_K/Q6_K, k % 32 == 0 for Q8_0.  Paths (each weight byte is read
+ * k % 256 == 0 for Q4_K/Q6_K, k % 32 == 0 for Q8_0/Q4_0.  Paths (each weight byte is read
  * once, every column reusing the decoded weight):
  *   Q4_K, m <= 8:       the bulk-copy GEMV (dp4a);
  *   Q4_K, 9 <= m <= 16: the skinny tensor-core path (weight rows as the MMA's M side);
@@ -111,6 +115,8 @@ QMM_API qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void 
  *   Q6_K/Q8_0, m <= 8:  the bulk-copy GEMV;
  *   Q6_K/Q8_0, m > 8:   the tiled tensor-core GEMM (Q8_0: k % 256 == 0; Q6_K: n % 8
  *                       == 0), otherwise the CUDA-core tiled GEMM;
+ *   Q4_0, m <= 8:       the bulk-copy GEMV (k % 256 == 0, else the direct-load GEMV);
+ *   Q4_0, m > 8:        the CUDA-core tiled GEMM;
  * the tensor-core paths split their work with a stream-K schedule.
  * Accuracy: |y - y_exact| <= 1e-5 * sum over blocks of |block term| per element.
  */
@@ -178,7 +184,7 @@ QMM_API qmm_status qmm_mul_mat_glu(const void *W_gate, const void *W_up, qmm_typ
  * word.  Paths:
  *   n_tokens * top_k <= 32 (decode): one bulk-copy GEMV per (token, slot) pair, the
  *     pair's expert id read on the device (for the shapes the GEMV streams: Q4_K
- *     always, Q8_0 with k/32 % 8 == 0, Q6_K with 16-byte rows or even n);
+ *     always, Q8_0 and Q4_0 with k/32 % 8 == 0, Q6_K with 16-byte rows or even n);
  *   otherwise the pairs are bucketed by expert on the device (a stable counting sort)
  *     and the per-expert tiles are walked by one persistent launch: Q4_K with
  *     k % 256 == 0 on the tensor cores (128-pair tiles, stream-K over the device-built
@@ -273,11 +279,11 @@ QMM_API void qmm_plan_cta_range(const qmm_gemm_plan *plan, int32_t cta, int64_t 
  * given smem_bytes of shared memory per block: the deepest of 8, 6, 4 or 3 stages of 8
  * weight rows that fits.  The consumer groups take the stages in turn, 4 groups for 8
  * and 4 stages, 3 for 6 and 3, so that each stage always goes to the same group.  0
- * when the rows cannot be streamed in whole 16-byte units (Q8_0 unless k/32 is a
- * multiple of 8; Q6_K unless k/256 is a multiple of 8, or of 4 with n even) or when not
- * even 3 stages fit next to the staged activations (Q4_K at one column from k = 15616
- * on, with 227 KB): the call then runs on the direct-load GEMV kernel.  Bad arguments
- * give 0. */
+ * when the rows cannot be streamed in whole 16-byte units (Q8_0 and Q4_0 unless k/32
+ * is a multiple of 8; Q6_K unless k/256 is a multiple of 8, or of 4 with n even) or
+ * when not even 3 stages fit next to the staged activations (Q4_K at one column from
+ * k = 15616 on, with 227 KB): the call then runs on the direct-load GEMV kernel.  Bad
+ * arguments give 0. */
 QMM_API int qmm_gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int32_t ncols, int64_t smem_bytes);
 
 /* ------------------------------------------------------------------ test controls

@@ -42,6 +42,8 @@ def test_sizes():
     assert qmm.qmm_row_bytes("q4_K", 5120) == 20 * 144
     assert qmm.qmm_row_bytes("q6_K", 5120) == 20 * 210
     assert qmm.qmm_row_bytes("q8_0", 96) == 3 * 34
+    assert qmm.qmm_row_bytes("q4_0", 96) == 3 * 18
+    assert qmm.qmm_row_bytes("q4_0", 100) == 0
     assert qmm.qmm_row_bytes("q4_K", 100) == 0
     assert qmm.qmm_row_bytes(99, 256) == 0
 
@@ -144,7 +146,8 @@ def test_plan_partitions_all_work_exactly_once(n, k, m, nsm, mode):
 # Ring depth of the bulk-copy GEMV: stages of 8 weight rows next to the staged
 # activations (ncols units of 64 values, 96 bytes each, plus 1 KB of alignment slack),
 # at most 8, and only depths that 4 or 3 consumer groups split into whole stages each.
-ROW = {"q4_K": lambda k: k // 256 * 144, "q6_K": lambda k: k // 256 * 210, "q8_0": lambda k: k // 32 * 34}
+ROW = {"q4_K": lambda k: k // 256 * 144, "q6_K": lambda k: k // 256 * 210, "q8_0": lambda k: k // 32 * 34,
+       "q4_0": lambda k: k // 32 * 18}
 
 
 def expected_depth(fmt, n, k, ncols, budget):
@@ -162,7 +165,7 @@ def test_gemv_ring_depth_whole_rounds(L):
     budget = 227 * 1024
     seen = set()
     for fmt, ks in (("q4_K", range(256, 40000, 256)), ("q6_K", range(256, 30000, 256)),
-                    ("q8_0", range(32, 20000, 32))):
+                    ("q8_0", range(32, 20000, 32)), ("q4_0", range(32, 30000, 32))):
         for k in ks:
             for ncols in (1, 2, 5, 8):
                 for n in (4096, 4097):

@@ -31,12 +31,12 @@ def two_calls(Wd, fmt, n, k, xd, m):
     return qmm.qmm_mul_mat(Wd, fmt, n, k, xq, m)
 
 
-# (n, k): several 8-row chunks with a ragged tail; Q8_0 k=160 has an odd block count
+# (n, k): several 8-row chunks with a ragged tail; k=160 has an odd block count
 SHAPES = {"q4_K": [(129, 2304), (1000, 512)], "q6_K": [(129, 2304), (37, 256)],
-          "q8_0": [(129, 1056), (33, 160)]}
+          "q8_0": [(129, 1056), (33, 160)], "q4_0": [(129, 2048), (33, 160)]}
 
 
-@pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q8_0", "q4_0"])
 @pytest.mark.parametrize("m", [1, 2, 3, 5, 8, 9, 20])
 @pytest.mark.parametrize("path", [0, 4])
 def test_f32_equals_two_calls_and_oracle(oracle_mod, fmt, m, path):

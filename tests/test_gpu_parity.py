@@ -85,10 +85,13 @@ def test_quantize_near_ties_bitexact(oracle_mod):
 # kernel); Q6_K k = 5120 takes 6 stages (three groups).
 GEMV_SHAPES = {"q4_K": [(1, 256), (7, 512), (129, 2304), (64, 11776), (33, 14336), (20, 16384)],
                "q6_K": [(1, 256), (7, 512), (129, 2304), (130, 2304), (64, 512), (2, 5120)],
-               "q8_0": [(1, 32), (7, 96), (129, 1056), (33, 2048), (130, 256), (64, 5120), (40, 8192)]}
+               "q8_0": [(1, 32), (7, 96), (129, 1056), (33, 2048), (130, 256), (64, 5120), (40, 8192)],
+               # odd block counts (k = 96, 1056: rows only 2-byte aligned, a last unit of one
+               # block) take the direct-load kernel; k % 256 == 0 the bulk copies
+               "q4_0": [(1, 32), (7, 96), (129, 1056), (33, 2048), (130, 256), (64, 4096), (40, 8192)]}
 
 
-@pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q8_0"])
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q8_0", "q4_0"])
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_gemv_parity(oracle_mod, fmt, m):
     for (n, k) in GEMV_SHAPES[fmt]:
@@ -101,7 +104,8 @@ def test_gemv_parity(oracle_mod, fmt, m):
 # ---------------------------------------------------------------- tiled GEMM paths
 
 GEMM_CASES = [("q4_K", 129, 512, 9), ("q4_K", 300, 1024, 65), ("q4_K", 64, 256, 130), ("q4_K", 1, 256, 17),
-              ("q6_K", 129, 512, 17), ("q6_K", 200, 768, 64), ("q8_0", 129, 1056, 33), ("q8_0", 70, 96, 127)]
+              ("q6_K", 129, 512, 17), ("q6_K", 200, 768, 64), ("q8_0", 129, 1056, 33), ("q8_0", 70, 96, 127),
+              ("q4_0", 129, 512, 9), ("q4_0", 300, 1056, 65), ("q4_0", 64, 96, 130), ("q4_0", 1000, 4096, 300)]
 
 
 @pytest.mark.parametrize("fmt,n,k,m", GEMM_CASES)
@@ -173,7 +177,7 @@ def test_moe_invalid_ids_flagged_and_zeroed(oracle_mod):
 
 
 @pytest.mark.parametrize("fmt,n,k", [("q6_K", 130, 2304), ("q6_K", 1000, 5120), ("q8_0", 130, 256),
-                                     ("q8_0", 512, 5120)])
+                                     ("q8_0", 512, 5120), ("q4_0", 130, 2048), ("q4_0", 512, 4096)])
 @pytest.mark.parametrize("m", [1, 3, 8])
 def test_gemv_bulk_and_direct_agree(oracle_mod, fmt, n, k, m):
     """The bulk-copy GEMV (path 1) and the direct-load GEMV (path 4) fold the same
@@ -194,7 +198,8 @@ def test_gemv_bulk_and_direct_agree(oracle_mod, fmt, n, k, m):
                                             ("q4_K", 8, 256, 256, 4, 8), ("q4_K", 8, 256, 256, 11, 3),
                                             ("q6_K", 16, 130, 1024, 2, 4), ("q6_K", 8, 96, 2048, 1, 8),
                                             ("q6_K", 8, 96, 2304, 1, 8),
-                                            ("q8_0", 16, 136, 256, 2, 8), ("q8_0", 8, 100, 512, 1, 2)])
+                                            ("q8_0", 16, 136, 256, 2, 8), ("q8_0", 8, 100, 512, 1, 2),
+                                            ("q4_0", 16, 136, 256, 2, 8), ("q4_0", 8, 100, 96, 1, 8)])
 def test_moe_decode_gemv_parity(oracle_mod, fmt, E, n, k, T_, K):
     moe_check(oracle_mod, E, n, k, T_, K, seed=E + n + T_ + K, fmt=fmt)
 
@@ -207,6 +212,28 @@ def test_moe_decode_gemv_invalid_ids_flagged_and_zeroed(oracle_mod):
 # tensor-core grouped GEMM and the CUDA-core grouped GEMM
 @pytest.mark.parametrize("fmt,E,n,k,T_,K", [("q4_K", 16, 256, 512, 2, 4), ("q4_K", 16, 130, 512, 64, 4),
                                             ("q4_K", 8, 384, 1024, 300, 2), ("q6_K", 8, 130, 512, 40, 2),
-                                            ("q8_0", 8, 64, 256, 50, 3)])
+                                            ("q8_0", 8, 64, 256, 50, 3), ("q4_0", 8, 64, 256, 50, 3),
+                                            ("q4_0", 16, 100, 512, 2, 4)])
 def test_moe_per_slot_parity(oracle_mod, fmt, E, n, k, T_, K):
     moe_check(oracle_mod, E, n, k, T_, K, seed=2 * E + n + T_, fmt=fmt, per_slot=True)
+
+
+# Q4_0 through the grouped CUDA-core MoE GEMM (more than 32 pairs), with skewed routing
+@pytest.mark.parametrize("E,n,k,T_,K", [(8, 130, 512, 70, 4), (16, 64, 1056, 100, 2)])
+def test_moe_q4_0_grouped_parity(oracle_mod, E, n, k, T_, K):
+    moe_check(oracle_mod, E, n, k, T_, K, seed=3 * E + n, fmt="q4_0")
+
+
+@pytest.mark.parametrize("path", [1, 2, 4])
+def test_q4_0_extreme_codes(oracle_mod, path):
+    """Codes 0 and 15 (values -8 and 7) against activations at +-127: the largest
+    integer dots of the format must stay exact on every path."""
+    n, k, m = 130, 512, 9 if path == 2 else 4
+    W, _ = qmm_synth.make_dense("q4_0", n, k, m, seed=6)
+    blk = W.reshape(n, k // 32, 18)
+    blk[0::2, :, 2:] = np.uint8(0x00)
+    blk[1::2, :, 2:] = np.uint8(0xFF)
+    x = np.where(np.random.default_rng(7).random((m, k)) < 0.5, -1.0, 1.0).astype(np.float32)
+    xq = oracle_mod.quantize_q8_1(x)
+    y_ref, T = oracle_mod.mul_mat(W, "q4_0", n, k, xq, m)
+    assert_within(run_mul_mat(W, "q4_0", n, k, xq, m, path=path), y_ref, T, f"q4_0 extreme path={path}")
