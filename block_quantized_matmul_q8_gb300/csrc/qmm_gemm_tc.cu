@@ -100,6 +100,17 @@ template <> struct TcFmt<QMM_Q8_0> {
     static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * 136); }
 };
+// Q4_0: the 256 k values of a step are eight 18-byte blocks (144 bytes, as a Q4_K
+// superblock), a d per 32-block and row; the codes q - 8 are exact fp16 integers.
+template <> struct TcFmt<QMM_Q4_0> {
+    static constexpr uint32_t kRawRow = 8 * kQ40Bytes;  // 144
+    static constexpr uint32_t kRawBuf = 128 * kRawRow;
+    static constexpr bool kMin = false;
+    static constexpr int kUses = 8;
+    static constexpr int kSub = 32;
+    static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
+    static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * 144); }
+};
 // Q6_K: a row is 210 bytes per superblock, so neither a row (210 * k/256 bytes) nor a
 // superblock is a whole number of 16-byte units and the rows cannot be a 2-D tensor map.
 // The raw warp instead issues one 224-byte bulk copy per row: the window starting at the
@@ -613,6 +624,64 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     ptx::mbar_arrive(ptx::smem_u32(&B.st_full[st]));
                     ++w_it;
                 }
+                } else if constexpr (T == QMM_Q4_0) {
+                // Q4_0: the row's 256 k values are 8 blocks of {fp16 d, 16 nibble bytes}, block
+                // b at byte 18b; byte i of a block holds its weight i (low nibble) and 16 + i
+                // (high).  The d of every block goes to the epilogue; a nibble v becomes the
+                // fp16 1024 + v (v | 0x6400), and adding -1032 leaves the exact code v - 8.
+#pragma unroll
+                for (int b = 0; b < 8; ++b) dd[b * 128 + r] = __half2float(*reinterpret_cast<const __half *>(blk + 18 * b));
+                ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
+                const __half2 bias = __float2half2_rn(-1032.f);
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t st = w_it % kStages;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    // blocks 4h .. 4h+3: 72 bytes from byte 72h (rows are 144 bytes apart, so the
+                    // range is 8-byte aligned); block b2's nibbles start at byte 18 b2 + 2 of it,
+                    // on a word boundary for odd b2 and 2 bytes past one for even b2
+                    uint32_t w[18];
+                    const uint2 *src = reinterpret_cast<const uint2 *>(blk + 72 * h);
+#pragma unroll
+                    for (int i2 = 0; i2 < 9; ++i2) {
+                        const uint2 t2 = src[i2];
+                        w[2 * i2] = t2.x;
+                        w[2 * i2 + 1] = t2.y;
+                    }
+                    uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
+#pragma unroll
+                    for (int b2 = 0; b2 < 4; ++b2) {
+                        const int o = (b2 >> 1) * 9;
+                        uint32_t q[4];
+#pragma unroll
+                        for (int i2 = 0; i2 < 4; ++i2)
+                            q[i2] = (b2 & 1) ? w[o + 5 + i2] : __funnelshift_r(w[o + i2], w[o + i2 + 1], 16);
+                        uint8_t *rowdst = wst + (b2 >> 1) * kSlabBytes + r * 128;
+#pragma unroll
+                        for (int cq = 0; cq < 4; ++cq) {  // 16-byte chunk cq: weights 8cq .. 8cq+7
+                            uint32_t pr[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const uint32_t src4 = q[2 * (cq & 1) + e2];
+                                const uint32_t nib = (cq < 2 ? src4 : src4 >> 4) & 0x0f0f0f0fu;
+                                uint32_t lo = __byte_perm(nib, 0x64646464u, 0x4140);
+                                uint32_t hi = __byte_perm(nib, 0x64646464u, 0x4342);
+                                lo = h2bits(__hadd2(*reinterpret_cast<__half2 *>(&lo), bias));
+                                hi = h2bits(__hadd2(*reinterpret_cast<__half2 *>(&hi), bias));
+                                pr[2 * e2] = lo;
+                                pr[2 * e2 + 1] = hi;
+                            }
+                            const int chunk = (b2 & 1) * 4 + cq;  // 16-byte chunk of the 128-byte row
+                            *reinterpret_cast<uint4 *>(rowdst + ((chunk ^ (r & 7)) << 4)) =
+                                make_uint4(pr[0], pr[1], pr[2], pr[3]);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(ptx::smem_u32(&B.st_full[st]));
+                    ++w_it;
+                }
                 } else {
                 // Q8_0: the row's 256 k values are 8 blocks of {fp16 d, int8 q[32]}, block b at
                 // byte 34b.  The d of every block goes to the epilogue; the codes become
@@ -845,6 +914,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_q40_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
+                       const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
+                       const __grid_constant__ CUtensorMap tm_w2, TcArgs a) {
+    gemm_tc_body<QMM_Q4_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, a);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_q6k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
                        const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_w2, TcArgs a) {
@@ -997,7 +1073,7 @@ int64_t gemm_tc_tile_m(int64_t) { return kTM; }
 
 bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
     if (!(k % 256 == 0 && n > 0 && m > 0 && m <= (int64_t(1) << 30))) return false;
-    if (t == QMM_Q4_K || t == QMM_Q8_0) return true;
+    if (t == QMM_Q4_K || t == QMM_Q8_0 || t == QMM_Q4_0) return true;
     // Q6_K's raw map views W as groups of 8 rows, so n must be a multiple of 8
     return t == QMM_Q6_K && n % 8 == 0;
 }
@@ -1015,7 +1091,10 @@ template <int T>
 cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CUtensorMap &tm_dx,
                    const CUtensorMap &tm_w, const CUtensorMap &tm_w2, const TcArgs &args, int ctas, int64_t fixup_tiles,
                    cudaStream_t st) {
-    auto kern = T == QMM_Q4_K ? gemm_tc_q4k_kernel : T == QMM_Q6_K ? gemm_tc_q6k_kernel : gemm_tc_q80_kernel;
+    auto kern = T == QMM_Q4_K   ? gemm_tc_q4k_kernel
+                : T == QMM_Q6_K ? gemm_tc_q6k_kernel
+                : T == QMM_Q4_0 ? gemm_tc_q40_kernel
+                                : gemm_tc_q80_kernel;
     constexpr uint32_t smem = TcMap<T>::kSmemAlloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1070,7 +1149,7 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     if (e != cudaSuccess) return e;
 
     CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
-    const int64_t row_bytes = (k / 256) * block_bytes(t) * (t == QMM_Q8_0 ? 8 : 1);
+    const int64_t row_bytes = (k / 256) * block_bytes(t) * (256 / block_elems(t));
     bool wmap;
     if (t == QMM_Q8_0)  // rows read as uint16 so that one superblock's 272 bytes are a box of 136
         wmap = make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, W, row_bytes / 2, n, TcFmt<QMM_Q8_0>::kRawRow / 2,
@@ -1100,6 +1179,7 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     args.stream_k = p.stream_k;
     const int64_t fixup_tiles = (p.stream_k && p.fixup) ? p.ntiles : 0;
     if (t == QMM_Q8_0) return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
+    if (t == QMM_Q4_0) return run_tc<QMM_Q4_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
     if (t == QMM_Q6_K) return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
     return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
 }

@@ -21,8 +21,9 @@ def _lib():
     qmm.qmm_set_stream_k_mode(0)
 
 
-def run_tc(oracle_mod, n, k, m, sk_mode, seed=0, x=None, fmt="q4_K"):
-    W, xr = qmm_synth.make_dense(fmt, n, k, m, seed=seed)
+def run_tc(oracle_mod, n, k, m, sk_mode, seed=0, x=None, fmt="q4_K", W=None):
+    Wr, xr = qmm_synth.make_dense(fmt, n, k, m, seed=seed)
+    W = Wr if W is None else W
     if x is not None:
         xr = x
     xq = oracle_mod.quantize_q8_1(xr)
@@ -138,3 +139,23 @@ def test_tc_q6_k_odd_n_falls_back(oracle_mod):
         qmm.qmm_set_force_path(0)
     y_ref, T = oracle_mod.mul_mat(W, "q6_K", n, k, xq, m)
     assert_within(y.cpu().numpy(), y_ref, T, "q6_K odd n")
+
+
+# Q4_0 on the tensor cores: offset codes q - 8 as exact fp16, a d per 32-block folded
+# with d8 (k % 256 == 0: a row's 256 values are 144 bytes, one box of the raw map)
+@pytest.mark.parametrize("n,k,m", [(128, 256, 128), (129, 512, 9), (1, 256, 17), (300, 1024, 130), (77, 2048, 200),
+                                   (1000, 4096, 300)])
+@pytest.mark.parametrize("sk", [1, 2])
+def test_tc_q4_0_parity(oracle_mod, n, k, m, sk):
+    run_tc(oracle_mod, n, k, m, sk, seed=5 * n + k + m, fmt="q4_0")
+
+
+def test_tc_q4_0_extreme_codes(oracle_mod):
+    """Codes 0 and 15 (values -8 and 7) against activations at +-127."""
+    n, k, m = 130, 512, 20
+    W, _ = qmm_synth.make_dense("q4_0", n, k, m, seed=4)
+    blk = W.reshape(n, k // 32, 18)
+    blk[:, ::2, 2:] = np.uint8(0x00)
+    blk[:, 1::2, 2:] = np.uint8(0xFF)
+    x = np.where(np.random.default_rng(8).random((m, k)) < 0.5, -1.0, 1.0).astype(np.float32)
+    run_tc(oracle_mod, n, k, m, 1, x=x, W=W, fmt="q4_0")
