@@ -327,10 +327,12 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
         del Wd
         return rows
 
-    def glu(n, k, ms):
+    def glu(n, k, ms, packed=False):
         """Fused gate/up + SwiGLU from q8_1 input: both weights (n rows each) in GB/s at
-        m <= 8, TOPS over both products (2 * m * 2n * k) above."""
-        ms = [m for m in ms if only in f"glu_q4_K_n{n}_k{k}_m{m}"]
+        m <= 8, TOPS over both products (2 * m * 2n * k) above.  packed: the interleaved
+        tensor of qmm_repack_glu (the repack itself is outside the timed region)."""
+        name = "glu_packed" if packed else "glu"
+        ms = [m for m in ms if only in f"{name}_q4_K_n{n}_k{k}_m{m}"]
         if not ms:
             return {}
         rows = {}
@@ -338,15 +340,22 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
         copies = max(1, int(3 * L2_BYTES // W.nbytes) + 1)
         Wg = [torch.from_numpy(W[:n].copy()).to(dev) for _ in range(copies)]
         Wu = [torch.from_numpy(W[n:].copy()).to(dev) for _ in range(copies)]
+        if packed:
+            Wg = [qmm.qmm_repack_glu(g, u, "q4_K", n, k) for g, u in zip(Wg, Wu)]
+            Wu = None
         xq_all = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
         for m in ms:
             xq = xq_all[:m].contiguous()
             y = torch.empty((m, n), device=dev)
             need = qmm.qmm_workspace_bytes_glu("q4_K", n, k, m)
             ws = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
-            fn = lambda i: qmm.qmm_mul_mat_glu(Wg[i % copies], Wu[i % copies], "q4_K", n, k, xq, m, y=y, workspace=ws)
+            if packed:
+                fn = lambda i: qmm.qmm_mul_mat_glu_packed(Wg[i % copies], "q4_K", n, k, xq, m, y=y, workspace=ws)
+            else:
+                fn = lambda i: qmm.qmm_mul_mat_glu(Wg[i % copies], Wu[i % copies], "q4_K", n, k, xq, m, y=y,
+                                                   workspace=ws)
             ms_call = time_graphs(torch, fn, steps, 3, lambda: None) / steps
-            key = f"glu_q4_K_n{n}_k{k}_m{m}"
+            key = f"{name}_q4_K_n{n}_k{k}_m{m}"
             if m <= 8:
                 b = W.nbytes + m * (k // 32) * 36 + m * n * 4
                 rows[key] = {"GB/s": b / (ms_call * 1e-3) / 1e9, "hbm_frac": b / (ms_call * 1e-3) / 1e9 / hbm_peak,
@@ -366,6 +375,7 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
     out.update(dense("q8_0", 5120, 5120, [1, 512]))
     out.update(dense("q4_0", 8192, 4096, [1, 512]))
     out.update(glu(14336, 4096, [1, 512]))
+    out.update(glu(14336, 4096, [1, 512], packed=True))
     # MoE: 128 experts x Q4_K n=1536 k=4096, 512 tokens top-8 Zipf(1.1); and its decode
     # form, one token top-8, whose calls route to disjoint sets of 8 experts in turn (16
     # calls cover all 128 experts, 453 MB, so no call finds its experts in L2)

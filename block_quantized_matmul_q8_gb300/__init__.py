@@ -29,7 +29,8 @@ EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspac
            "qmm_mul_mat", "qmm_mul_mat_id", "qmm_read_device_status", "qmm_tile_efficiency_percent",
            "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode",
            "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32",
-           "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu", "qmm_gemv_ring_stages")
+           "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu", "qmm_gemv_ring_stages",
+           "qmm_repack_glu", "qmm_mul_mat_glu_packed")
 
 
 class QMMError(RuntimeError):
@@ -94,6 +95,10 @@ def lib():
     L.qmm_workspace_bytes_glu.argtypes = [ctypes.c_int, I64, I64, I64]
     L.qmm_mul_mat_glu.restype = ctypes.c_int
     L.qmm_mul_mat_glu.argtypes = [P, P, ctypes.c_int, I64, I64, P, I64, P, P, ctypes.c_size_t, P]
+    L.qmm_mul_mat_glu_packed.restype = ctypes.c_int
+    L.qmm_mul_mat_glu_packed.argtypes = [P, ctypes.c_int, I64, I64, P, I64, P, P, ctypes.c_size_t, P]
+    L.qmm_repack_glu.restype = ctypes.c_int
+    L.qmm_repack_glu.argtypes = [P, P, ctypes.c_int, I64, I64, P, P]
     L.qmm_mul_mat_id_slot.restype = ctypes.c_int
     L.qmm_mul_mat_id_slot.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P, ctypes.c_size_t, P]
     L.qmm_noalloc_scratch_bytes.restype = SZ
@@ -203,6 +208,38 @@ def qmm_mul_mat_glu(W_gate: torch.Tensor, W_up: torch.Tensor, qtype, n: int, k: 
     _check(lib().qmm_mul_mat_glu(_ptr(W_gate), _ptr(W_up), _qtype(qtype), n, k, _ptr(xq), m, _ptr(y),
                                  _ptr(workspace) if workspace is not None else None, ws_bytes, _stream(stream)),
            "qmm_mul_mat_glu")
+    return y
+
+
+def qmm_repack_glu(W_gate: torch.Tensor, W_up: torch.Tensor, qtype, n: int, k: int,
+                   W_gu: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Interleaved copy of a gate/up pair: row 2j = gate row j, row 2j+1 = up row j."""
+    _dev(W_gate, "W_gate")
+    _dev(W_up, "W_up")
+    if W_gu is None:
+        W_gu = torch.empty(2 * W_gate.numel(), dtype=torch.uint8, device=W_gate.device)
+    _dev(W_gu, "W_gu")
+    _check(lib().qmm_repack_glu(_ptr(W_gate), _ptr(W_up), _qtype(qtype), n, k, _ptr(W_gu), _stream(stream)),
+           "qmm_repack_glu")
+    return W_gu
+
+
+def qmm_mul_mat_glu_packed(W_gu: torch.Tensor, qtype, n: int, k: int, xq: torch.Tensor, m: int,
+                           y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """qmm_mul_mat_glu on the interleaved tensor of qmm_repack_glu."""
+    _dev(W_gu, "W_gu")
+    _dev(xq, "xq")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=W_gu.device)
+    _dev(y, "y", torch.float32)
+    need = qmm_workspace_bytes_glu(qtype, n, k, m)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=W_gu.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().qmm_mul_mat_glu_packed(_ptr(W_gu), _qtype(qtype), n, k, _ptr(xq), m, _ptr(y),
+                                        _ptr(workspace) if workspace is not None else None, ws_bytes,
+                                        _stream(stream)), "qmm_mul_mat_glu_packed")
     return y
 
 

@@ -117,6 +117,38 @@ __global__ void glu_combine_kernel(const float *__restrict__ g, const float *__r
         y[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
 }
 
+// The same from one product of an interleaved gate/up tensor: z is [m][2n] with the gate
+// dot of output j in column 2j and the up dot in column 2j+1.
+__global__ void glu_combine_pairs_kernel(const float2 *__restrict__ z, int64_t total, float *__restrict__ y) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const float2 gu = z[i];
+        y[i] = gu.x / (1.0f + expf(-gu.x)) * gu.y;
+    }
+}
+
+// Interleave a gate/up pair row by row: dst row 2j = gate row j, 2j+1 = up row j.  rows
+// of rb bytes; copied in 16-byte units when rb allows (all pointers are 16-byte aligned),
+// else in 2-byte units (every block size is even).
+__global__ void repack_glu_kernel(const uint8_t *__restrict__ wg, const uint8_t *__restrict__ wu, int64_t n,
+                                  int64_t rb, uint8_t *__restrict__ dst) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    if (rb % 16 == 0) {
+        const int64_t per_row = rb / 16, total = 2 * n * per_row;
+        for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+            const int64_t row = i / per_row, c = i - row * per_row;
+            const uint8_t *src = ((row & 1) ? wu : wg) + (row >> 1) * rb;
+            reinterpret_cast<uint4 *>(dst + row * rb)[c] = reinterpret_cast<const uint4 *>(src)[c];
+        }
+    } else {
+        const int64_t per_row = rb / 2, total = 2 * n * per_row;
+        for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+            const int64_t row = i / per_row, c = i - row * per_row;
+            const uint8_t *src = ((row & 1) ? wu : wg) + (row >> 1) * rb;
+            reinterpret_cast<uint16_t *>(dst + row * rb)[c] = reinterpret_cast<const uint16_t *>(src)[c];
+        }
+    }
+}
+
 enum GluPath { kGluGemv = 1, kGluTc = 2, kGluUnfused = 3 };
 static int choose_glu_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
     const int force = g_force_path.load(std::memory_order_relaxed);
@@ -209,38 +241,73 @@ size_t qmm_workspace_bytes_glu(qmm_type t, int64_t n, int64_t k, int64_t m) {
     switch (choose_glu_path(t, n, k, m)) {
     case kGluGemv: return 0;
     case kGluTc: return gemm_tc_glu_workspace_bytes(t, n, k, m);
-    default: return align256(size_t(2) * m * n * 4) + qmm_workspace_bytes(t, n, k, m, 0, 0);
+    // unfused: two products of n rows, or one of 2n rows for the interleaved tensor
+    default: return align256(size_t(2) * m * n * 4) + qmm_workspace_bytes(t, 2 * n, k, m, 0, 0);
     }
 }
 
-qmm_status qmm_mul_mat_glu(const void *W_gate, const void *W_up, qmm_type t, int64_t n, int64_t k, const void *xq,
-                           int64_t m, float *y, void *workspace, size_t ws_bytes, void *stream) {
+static qmm_status mul_mat_glu_common(const void *W_gate, const void *W_up, bool packed, qmm_type t, int64_t n,
+                                     int64_t k, const void *xq, int64_t m, float *y, void *workspace, size_t ws_bytes,
+                                     void *stream) {
     qmm_status s = check_k(t, k);
     if (s != QMM_OK) return s;
     if (n < 0 || m < 0) return QMM_ERR_ARG;
-    if (n > kMaxRows || m > kMaxRows) return QMM_ERR_SHAPE;
+    if (n > kMaxRows / 2 || m > kMaxRows) return QMM_ERR_SHAPE;
     if (n == 0 || m == 0) return QMM_OK;
-    if (!W_gate || !W_up || !xq || !y) return QMM_ERR_ARG;
-    if (!aligned16(W_gate) || !aligned16(W_up) || !aligned16(xq) || !aligned16(y)) return QMM_ERR_ALIGN;
+    if (!W_gate || (!packed && !W_up) || !xq || !y) return QMM_ERR_ARG;
+    if (!aligned16(W_gate) || (!packed && !aligned16(W_up)) || !aligned16(xq) || !aligned16(y)) return QMM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const void *wu = packed ? nullptr : W_up;
     const int path = choose_glu_path(t, n, k, m);
-    if (path == kGluGemv) return cuda_status(launch_gemv_glu(t, W_gate, W_up, n, k, xq, m, y, st));
+    if (path == kGluGemv) return cuda_status(launch_gemv_glu(t, W_gate, wu, n, k, xq, m, y, st));
     const size_t need = qmm_workspace_bytes_glu(t, n, k, m);
     if (!workspace || ws_bytes < need) return QMM_ERR_WORKSPACE;
     if (!aligned256(workspace)) return QMM_ERR_ALIGN;
-    if (path == kGluTc)
-        return cuda_status(launch_gemm_tc_glu(t, W_gate, W_up, n, k, xq, m, y, workspace, ws_bytes, st));
-    // unfused: both products into the workspace, then the combine pass
+    if (path == kGluTc) return cuda_status(launch_gemm_tc_glu(t, W_gate, wu, n, k, xq, m, y, workspace, ws_bytes, st));
+    // unfused: the dots into the workspace, then the combine pass
     float *g = static_cast<float *>(workspace), *u = g + m * n;
     uint8_t *rest = static_cast<uint8_t *>(workspace) + align256(size_t(2) * m * n * 4);
     const size_t rest_bytes = ws_bytes - align256(size_t(2) * m * n * 4);
+    const int64_t total = m * n;
+    const int grid = (int)std::min<int64_t>((total + 255) / 256, int64_t(device_sm_count()) * 8);
+    if (packed) {  // one product of the 2n interleaved rows: [m][2n], gate and up side by side
+        s = mul_mat_q8(W_gate, t, 2 * n, k, xq, m, g, rest, rest_bytes, st);
+        if (s != QMM_OK) return s;
+        glu_combine_pairs_kernel<<<std::max(grid, 1), 256, 0, st>>>(reinterpret_cast<const float2 *>(g), total, y);
+        return cuda_status(cudaGetLastError());
+    }
     s = mul_mat_q8(W_gate, t, n, k, xq, m, g, rest, rest_bytes, st);
     if (s != QMM_OK) return s;
     s = mul_mat_q8(W_up, t, n, k, xq, m, u, rest, rest_bytes, st);
     if (s != QMM_OK) return s;
-    const int64_t total = m * n;
-    const int grid = (int)std::min<int64_t>((total + 255) / 256, int64_t(device_sm_count()) * 8);
     glu_combine_kernel<<<std::max(grid, 1), 256, 0, st>>>(g, u, total, y);
+    return cuda_status(cudaGetLastError());
+}
+
+qmm_status qmm_mul_mat_glu(const void *W_gate, const void *W_up, qmm_type t, int64_t n, int64_t k, const void *xq,
+                           int64_t m, float *y, void *workspace, size_t ws_bytes, void *stream) {
+    return mul_mat_glu_common(W_gate, W_up, false, t, n, k, xq, m, y, workspace, ws_bytes, stream);
+}
+
+qmm_status qmm_mul_mat_glu_packed(const void *W_gu, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m,
+                                  float *y, void *workspace, size_t ws_bytes, void *stream) {
+    return mul_mat_glu_common(W_gu, nullptr, true, t, n, k, xq, m, y, workspace, ws_bytes, stream);
+}
+
+qmm_status qmm_repack_glu(const void *W_gate, const void *W_up, qmm_type t, int64_t n, int64_t k, void *W_gu,
+                          void *stream) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n < 0) return QMM_ERR_ARG;
+    if (n > kMaxRows / 2) return QMM_ERR_SHAPE;
+    if (n == 0) return QMM_OK;
+    if (!W_gate || !W_up || !W_gu) return QMM_ERR_ARG;
+    if (!aligned16(W_gate) || !aligned16(W_up) || !aligned16(W_gu)) return QMM_ERR_ALIGN;
+    const int64_t rb = int64_t(qmm_row_bytes(t, k));
+    const int64_t units = 2 * n * (rb % 16 == 0 ? rb / 16 : rb / 2);
+    const int grid = (int)std::min<int64_t>((units + 255) / 256, int64_t(device_sm_count()) * 8);
+    repack_glu_kernel<<<std::max(grid, 1), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(W_gate), static_cast<const uint8_t *>(W_up), n, rb, static_cast<uint8_t *>(W_gu));
     return cuda_status(cudaGetLastError());
 }
 

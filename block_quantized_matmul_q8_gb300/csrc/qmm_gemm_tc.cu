@@ -174,8 +174,11 @@ struct TcArgs {
     const int32_t *bounds;
     const int32_t *perm;
     // fused gate/up + SwiGLU (n_out > 0, Q4_K): the tile space has n = 2 n_out columns,
-    // column 2j the gate row j (tm_w) and 2j+1 the up row j (tm_w2); y is [m][n_out]
+    // column 2j the gate row j (tm_w) and 2j+1 the up row j (tm_w2); y is [m][n_out].
+    // glu_packed: the rows are stored interleaved (qmm_repack_glu), so column c is row c
+    // of tm_w and the tile loads as in the plain GEMM
     int64_t n_out;
+    int glu_packed;
 };
 
 // Where tile t lives: m0 = first activation row (sorted row in grouped mode), rows =
@@ -449,7 +452,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         regs_dec<kRegsProducer>();
         if (T == QMM_Q6_K || lane == 0) {
             if constexpr (T != QMM_Q6_K) ptx::prefetch_tmap(&tm_w);
-            if (a.n_out) ptx::prefetch_tmap(&tm_w2);
+            if (a.n_out && !a.glu_packed) ptx::prefetch_tmap(&tm_w2);
             int64_t u = ubeg;
             Seg sg;
             uint32_t r_it = 0;
@@ -475,7 +478,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                             ptx::bulk_g2s(sbase + kOffRaw + ri * kRawBytes + r * F::kRawRow, a.W + (p & ~int64_t(15)),
                                           F::kCopyBytes, rbar);
                         }
-                    } else if (a.n_out) {  // GLU: 64 gate rows, then the 64 up rows of the same outputs
+                    } else if (a.n_out && !a.glu_packed) {  // GLU: 64 gate rows, then the 64 up rows of the same outputs
                         ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
                         ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, F::raw_x(sb), n0 / 2, rbar);
                         ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes + 64 * F::kRawRow, &tm_w2, F::raw_x(sb),
@@ -513,8 +516,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     ok = false;
                     break;
                 }
-                // GLU: tile column r is gate row r/2 (r even) or up row r/2 (r odd)
-                const int rsrc = a.n_out ? (r & 1) * 64 + (r >> 1) : r;
+                // GLU from two tensors: tile column r is gate row r/2 (r even) or up row r/2 (r odd)
+                const int rsrc = a.n_out && !a.glu_packed ? (r & 1) * 64 + (r >> 1) : r;
                 const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + rsrc * F::kRawRow;
                 if constexpr (T == QMM_Q6_K)  // the superblock's offset inside its window
                     blk += (int)(F::pos(n0w, sb, a.row_bytes) & 15);
@@ -1198,6 +1201,8 @@ size_t gemm_tc_glu_workspace_bytes(qmm_type t, int64_t n_out, int64_t k, int64_t
 // "「分专家」与「整批」之间: host 侧的代价"), so the schedule is one tile per CTA.
 cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_out, int64_t k, const void *xq,
                                int64_t m, float *y, void *ws, size_t ws_bytes, cudaStream_t st) {
+    // Wu == nullptr: Wg holds the gate and up rows interleaved (2 n_out rows)
+    const bool packed = Wu == nullptr;
     if (!gemm_tc_glu_supported(t, n_out, k, m)) return cudaErrorNotSupported;
     qmm_gemm_plan p{};
     const int nsm = std::min(device_sm_count(), kMaxPartialCtas);
@@ -1217,11 +1222,16 @@ cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64
     if (e != cudaSuccess) return e;
     const int64_t row_bytes = (k / 256) * kQ4KBytes;
     CUtensorMap tm_x, tm_xmin, tm_dx, tm_w, tm_w2;
-    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) ||
-        !make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wg, row_bytes, n_out, kQ4KBytes, kTN / 2,
-                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wu, row_bytes, n_out, kQ4KBytes, kTN / 2,
-                     CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k)) return cudaErrorInvalidValue;
+    if (packed) {
+        if (!make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wg, row_bytes, 2 * n_out, kQ4KBytes, kTN,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        tm_w2 = tm_w;
+    } else if (!make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wg, row_bytes, n_out, kQ4KBytes, kTN / 2,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+               !make_map_2d(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wu, row_bytes, n_out, kQ4KBytes, kTN / 2,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     TcArgs args{};
     args.W = static_cast<const uint8_t *>(Wg);
@@ -1238,6 +1248,7 @@ cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64
     args.ctas = p.ctas;
     args.stream_k = 0;
     args.n_out = n_out;
+    args.glu_packed = packed ? 1 : 0;
     return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, args, p.ctas, 0, st);
 }
 

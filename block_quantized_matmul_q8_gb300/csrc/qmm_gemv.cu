@@ -306,8 +306,10 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
 // GLU: fused gate/up with SwiGLU ([MMQ] sections "「分专家」与「整批」之间: host 侧的代价"
 // and "输出端: 写回与 scale 修正": gate and up rows interleaved so that one thread holds
 // both dots of an output, no stream-K).  n counts outputs; W is the gate and W2 the up
-// weight, each [n] rows.  A chunk holds 4 outputs as 8 staged rows (gate j, up j, ...),
-// one bulk copy per row; the two half-warps of a warp fold one pair and lane 0 writes
+// weight, each [n] rows, or with W2 == nullptr W holds both interleaved (2n rows: gate j
+// at 2j, up j at 2j+1, as qmm_repack_glu writes them).  A chunk holds 4 outputs as 8
+// staged rows (gate j, up j, ...): one bulk copy per row, or one for the chunk when the
+// rows are interleaved; the two half-warps of a warp fold one pair and lane 0 writes
 // silu(gate) * up.
 template <int T, int NC, bool GLU = false>
 __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int64_t n, int k, int64_t row_bytes,
@@ -367,7 +369,10 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
                 const uint32_t bar = ptx::smem_u32(&full[s]);
                 if constexpr (GLU) {
                     ptx::mbar_arrive_expect_tx(bar, uint32_t(2 * (b - a) * row_bytes));
-                    for (int64_t i = 0; i < b - a; ++i) {
+                    if (!W2)  // interleaved gate/up rows (qmm_repack_glu): the chunk is one block
+                        ptx::bulk_g2s(ptx::smem_u32(stages + s * stage_bytes), W + 2 * a * row_bytes,
+                                      uint32_t(2 * (b - a) * row_bytes), bar);
+                    for (int64_t i = 0; W2 && i < b - a; ++i) {
                         const uint32_t dst = ptx::smem_u32(stages + s * stage_bytes + size_t(2 * i) * row_bytes);
                         ptx::bulk_g2s(dst, W + (a + i) * row_bytes, uint32_t(row_bytes), bar);
                         ptx::bulk_g2s(dst + uint32_t(row_bytes), W2 + (a + i) * row_bytes, uint32_t(row_bytes), bar);

@@ -51,6 +51,8 @@ cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const v
                         float *y, cudaStream_t st);
 // Fused gate/up + SwiGLU GEMV (Q4_K, m <= 8): y[m][n] = silu(x Wg^T) * (x Wu^T) from
 // q8_1 activations, both weights read once.
+// Fused gate/up launches take Wu == nullptr for one interleaved tensor (gate row j at
+// 2j, up row j at 2j+1, as qmm_repack_glu writes it) in Wg.
 bool gemv_glu_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
 cudaError_t launch_gemv_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n, int64_t k, const void *xq,
                             int64_t m, float *y, cudaStream_t st);

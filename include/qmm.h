@@ -168,6 +168,29 @@ QMM_API qmm_status qmm_mul_mat_glu(const void *W_gate, const void *W_up, qmm_typ
                                    void *stream);
 
 /*
+ * One-time repack of a gate/up pair into one interleaved tensor (the optional weight
+ * repack; llama.cpp interleaves up and gate rows when it loads its fused tile, [MMQ]
+ * section "输出端: 写回与 scale 修正"; [QMM] section "Q4K 的 8 列重排": a repack keeps a
+ * second copy of the weights, so the caller owns both and may free the pair after):
+ *   W_gu row 2j = W_gate row j, row 2j+1 = W_up row j, bytes copied unchanged.
+ *   W_gate, W_up : [n][k/QK] blocks of type t; W_gu : [2n][k/QK], all 16-byte aligned.
+ * Enqueued on stream like every call; W_gu is ready when the stream reaches it.
+ */
+QMM_API qmm_status qmm_repack_glu(const void *W_gate, const void *W_up, qmm_type t, int64_t n, int64_t k, void *W_gu,
+                                  void *stream);
+
+/*
+ * qmm_mul_mat_glu on the interleaved tensor of qmm_repack_glu: the same y, and to the
+ * bit on the fused paths (Q4_K), which fold the same rows in the same order: the GEMV
+ * then streams each chunk of 4 outputs (gate and up rows) with one copy instead of 8,
+ * and the tensor-core GEMM loads a tile's gate and up rows as one box.  Other types
+ * and shapes: one product of the 2n rows into the workspace and a combine pass, within
+ * the bound of qmm_mul_mat_glu.  workspace: qmm_workspace_bytes_glu(t, n, k, m).
+ */
+QMM_API qmm_status qmm_mul_mat_glu_packed(const void *W_gu, qmm_type t, int64_t n, int64_t k, const void *xq,
+                                          int64_t m, float *y, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Expert-routed matmul ([MMQ] sections "派发路径", "专家边界: 在 GPU 上做分段,
  * 而不是在 host 上", "MoE 的二次账"):
  *   y[t][s][:] = x[t] * dequant(W_experts[ids[t][s]])^T

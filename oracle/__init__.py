@@ -183,6 +183,20 @@ def mul_mat_glu(W_gate, W_up, fmt, n, k, xq, m):
     return y, tol
 
 
+def repack_glu(W_gate, W_up) -> np.ndarray:
+    """The interleaved gate/up tensor, bytes unchanged: row 2j is gate row j and row 2j+1
+    up row j (the row order of the fused tile in [MMQ] section "输出端: 写回与 scale 修正",
+    there in groups of 8 rows, here single rows)."""
+    g = _u8(W_gate)
+    u = _u8(W_up)
+    if g.shape != u.shape or g.ndim != 2:
+        raise ValueError("gate and up must be [n][row bytes] of the same shape")
+    out = np.empty((2 * g.shape[0], g.shape[1]), dtype=np.uint8)
+    out[0::2] = g
+    out[1::2] = u
+    return out
+
+
 def mul_mat_at(W, fmt, n, k, xq, m, rows, cols):
     """Fold at selected output positions (rows = W rows, cols = activation rows)."""
     W = _u8(W)

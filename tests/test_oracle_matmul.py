@@ -261,3 +261,20 @@ def test_mul_mat_glu_pins(oracle_mod):
     Wg.reshape(n, k // 256, 144)[2, :, :4] = 0  # row 2: d = dmin = 0, every term 0
     y2, tol2 = oracle_mod.mul_mat_glu(Wg, Wu, "q4_K", n, k, xq, m)
     assert np.all(y2[:, 2] == 0) and np.all(tol2[:, 2] >= 0)
+
+
+def test_repack_glu_row_order(oracle_mod):
+    """Row 2j of the interleaved tensor is gate row j and row 2j+1 up row j, bytes
+    unchanged; its even and odd rows multiply exactly as the gate and up tensors."""
+    g = np.arange(3 * 4, dtype=np.uint8).reshape(3, 4)
+    u = (100 + np.arange(3 * 4)).astype(np.uint8).reshape(3, 4)
+    p = oracle_mod.repack_glu(g, u)
+    assert p.tolist() == [g[0].tolist(), u[0].tolist(), g[1].tolist(), u[1].tolist(), g[2].tolist(), u[2].tolist()]
+    rng = np.random.default_rng(41)
+    n, k, m = 5, 512, 2
+    Wg = qmm_synth.gen_weights("q4_K", rng, n, k)
+    Wu = qmm_synth.gen_weights("q4_K", rng, n, k)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, m, k))
+    y2, _ = oracle_mod.mul_mat(oracle_mod.repack_glu(Wg, Wu), "q4_K", 2 * n, k, xq, m)
+    assert np.array_equal(y2[:, 0::2], oracle_mod.mul_mat(Wg, "q4_K", n, k, xq, m)[0])
+    assert np.array_equal(y2[:, 1::2], oracle_mod.mul_mat(Wu, "q4_K", n, k, xq, m)[0])
