@@ -30,7 +30,7 @@ EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspac
            "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode",
            "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32",
            "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu", "qmm_gemv_ring_stages",
-           "qmm_repack_glu", "qmm_mul_mat_glu_packed")
+           "qmm_repack_glu", "qmm_mul_mat_glu_packed", "qmm_workspace_bytes_f32_host", "qmm_mul_mat_f32_host")
 
 
 class QMMError(RuntimeError):
@@ -104,6 +104,10 @@ def lib():
     L.qmm_noalloc_scratch_bytes.restype = SZ
     L.qmm_noalloc_scratch_bytes.argtypes = []
     L.qmm_workspace_bytes_f32.restype = SZ
+    L.qmm_workspace_bytes_f32_host.restype = SZ
+    L.qmm_workspace_bytes_f32_host.argtypes = [ctypes.c_int, I64, I64, I64]
+    L.qmm_mul_mat_f32_host.restype = ctypes.c_int
+    L.qmm_mul_mat_f32_host.argtypes = [P, ctypes.c_int, I64, I64, P, I64, P, P, SZ, P]
     L.qmm_workspace_bytes_f32.argtypes = [ctypes.c_int, I64, I64, I64]
     L.qmm_mul_mat_f32.restype = ctypes.c_int
     L.qmm_mul_mat_f32.argtypes = [P, ctypes.c_int, I64, I64, P, I64, P, P, SZ, P]
@@ -241,6 +245,24 @@ def qmm_mul_mat_glu_packed(W_gu: torch.Tensor, qtype, n: int, k: int, xq: torch.
                                         _ptr(workspace) if workspace is not None else None, ws_bytes,
                                         _stream(stream)), "qmm_mul_mat_glu_packed")
     return y
+
+
+def qmm_workspace_bytes_f32_host(qtype, n: int, k: int, m: int) -> int:
+    return int(lib().qmm_workspace_bytes_f32_host(_qtype(qtype), n, k, m))
+
+
+def qmm_mul_mat_f32_host(W: torch.Tensor, qtype, n: int, k: int, x_host: torch.Tensor, m: int, y_host: torch.Tensor,
+                         workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """qmm_mul_mat_f32 with x and y in host memory (pinned for asynchronous copies):
+    the copies and the product are enqueued on the stream by one C call."""
+    _dev(W, "W")
+    _dev(workspace, "workspace", torch.uint8)
+    for t_, name in ((x_host, "x_host"), (y_host, "y_host")):
+        if t_.is_cuda or t_.dtype != torch.float32 or not t_.is_contiguous():
+            raise QMMError(1, f"{name} must be a contiguous fp32 host tensor")
+    _check(lib().qmm_mul_mat_f32_host(_ptr(W), _qtype(qtype), n, k, _ptr(x_host), m, _ptr(y_host), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)), "qmm_mul_mat_f32_host")
+    return y_host
 
 
 def qmm_workspace_bytes_f32(qtype, n: int, k: int, m: int) -> int:

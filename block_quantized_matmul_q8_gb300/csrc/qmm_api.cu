@@ -342,6 +342,42 @@ qmm_status qmm_mul_mat_f32(const void *W, qmm_type t, int64_t n, int64_t k, cons
     return mul_mat_q8(W, t, n, k, xq, m, y, xq + off, ws_bytes - off, st);
 }
 
+// Host-buffer form: x_dev [m][k] and y_dev [m][n] at the head of the workspace, each
+// 256-byte aligned, then the qmm_mul_mat_f32 workspace.
+static size_t host_io_bytes(int64_t n, int64_t k, int64_t m) {
+    return align256(size_t(m) * size_t(k) * 4) + align256(size_t(m) * size_t(n) * 4);
+}
+
+size_t qmm_workspace_bytes_f32_host(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    if (!type_ok(t) || n < 0 || k <= 0 || m < 0 || k % 32) return 0;
+    return host_io_bytes(n, k, m) + qmm_workspace_bytes_f32(t, n, k, m);
+}
+
+qmm_status qmm_mul_mat_f32_host(const void *W, qmm_type t, int64_t n, int64_t k, const float *x_host, int64_t m,
+                                float *y_host, void *workspace, size_t ws_bytes, void *stream) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n < 0 || m < 0) return QMM_ERR_ARG;
+    if (n > kMaxRows || m > kMaxRows) return QMM_ERR_SHAPE;
+    if (n == 0 || m == 0) return QMM_OK;
+    if (!W || !x_host || !y_host) return QMM_ERR_ARG;
+    if (!aligned16(W)) return QMM_ERR_ALIGN;
+    if (!workspace || ws_bytes < qmm_workspace_bytes_f32_host(t, n, k, m)) return QMM_ERR_WORKSPACE;
+    if (!aligned256(workspace)) return QMM_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *base = static_cast<uint8_t *>(workspace);
+    float *x_dev = reinterpret_cast<float *>(base);
+    float *y_dev = reinterpret_cast<float *>(base + align256(size_t(m) * size_t(k) * 4));
+    const size_t io = host_io_bytes(n, k, m);
+    if (cudaMemcpyAsync(x_dev, x_host, size_t(m) * size_t(k) * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    s = qmm_mul_mat_f32(W, t, n, k, x_dev, m, y_dev, base + io, ws_bytes - io, stream);
+    if (s != QMM_OK) return s;
+    if (cudaMemcpyAsync(y_host, y_dev, size_t(m) * size_t(n) * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return QMM_OK;
+}
+
 }  // extern "C"
 
 namespace qmm {

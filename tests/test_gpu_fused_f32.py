@@ -103,3 +103,36 @@ def test_f32_near_ties_equal_two_calls(oracle_mod, m):
     xq = oracle_mod.quantize_q8_1(x)
     y_ref, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
     assert_within(y1.cpu().numpy(), y_ref, T, "f32 near ties")
+
+
+@pytest.mark.parametrize("fmt,n,k,m", [("q4_K", 1000, 512, 1), ("q4_K", 129, 2304, 5), ("q8_0", 33, 160, 20),
+                                       ("q4_0", 129, 2048, 1)])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_f32_host_buffers(oracle_mod, fmt, n, k, m, pinned):
+    """The host-buffer call gives the bits of the device call, from pinned or pageable
+    host memory."""
+    W, x = qmm_synth.make_dense(fmt, n, k, m, seed=n + 3 * m)
+    Wd = to_dev(W)
+    x_h = torch.from_numpy(x)
+    y_h = torch.full((m, n), float("nan"))
+    if pinned:
+        x_h, y_h = x_h.pin_memory(), y_h.pin_memory()
+    ws = torch.empty(max(256, qmm.qmm_workspace_bytes_f32_host(fmt, n, k, m)), dtype=torch.uint8, device=DEV)
+    qmm.qmm_mul_mat_f32_host(Wd, fmt, n, k, x_h, m, y_h, ws)
+    y_d = qmm.qmm_mul_mat_f32(Wd, fmt, n, k, to_dev(x), m)
+    torch.cuda.synchronize()
+    assert np.array_equal(y_h.numpy(), y_d.cpu().numpy())
+    y_ref, T = oracle_mod.mul_mat(W, fmt, n, k, oracle_mod.quantize_q8_1(x), m)
+    assert_within(y_h.numpy(), y_ref, T, f"f32 host {fmt} n={n} k={k} m={m}")
+
+
+def test_f32_host_workspace_errors():
+    n, k, m = 64, 256, 2
+    W, x = qmm_synth.make_dense("q4_K", n, k, m, seed=1)
+    Wd = to_dev(W)
+    need = qmm.qmm_workspace_bytes_f32_host("q4_K", n, k, m)
+    assert need >= 256 * 2
+    short = torch.empty(need - 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(qmm.QMMError) as e:
+        qmm.qmm_mul_mat_f32_host(Wd, "q4_K", n, k, torch.from_numpy(x), m, torch.empty((m, n)), short)
+    assert e.value.code == 5
