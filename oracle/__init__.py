@@ -175,12 +175,24 @@ def mul_mat_glu(W_gate, W_up, fmt, n, k, xq, m):
         tol = 1e-5 * (|silu'(g)| T_g |u| + |silu(g)| T_u) + 2^-20 |y| + 2^-120 |u|."""
     g, Tg = mul_mat(W_gate, fmt, n, k, xq, m)
     u, Tu = mul_mat(W_up, fmt, n, k, xq, m)
+    return _glu(g, Tg, u, Tu)
+
+
+def _glu(g, Tg, u, Tu):
     sg = 1.0 / (1.0 + np.exp(-g))
     a = g * sg
     da = sg * (1.0 + g * (1.0 - sg))
     y = a * u
     tol = 1e-5 * (np.abs(da) * Tg * np.abs(u) + np.abs(a) * Tu) + 2.0 ** -20 * np.abs(y) + 2.0 ** -120 * np.abs(u)
     return y, tol
+
+
+def mul_mat_glu_at(W_gate, W_up, fmt, n, k, xq, m, rows, cols):
+    """mul_mat_glu at selected output positions (rows = output features, cols =
+    activation rows): (y, tol) of length len(rows)."""
+    g, Tg = mul_mat_at(W_gate, fmt, n, k, xq, m, rows, cols)
+    u, Tu = mul_mat_at(W_up, fmt, n, k, xq, m, rows, cols)
+    return _glu(g, Tg, u, Tu)
 
 
 def repack_glu(W_gate, W_up) -> np.ndarray:

@@ -108,3 +108,45 @@ def test_moe_e128_n1536_k4096_t512_top8(oracle_mod):
         y_ref[sel] = yy
         T[sel] = TT
     assert_within(y[t, s, r], y_ref, T, "moe full size (sampled)")
+
+
+def test_q40_n8192_k4096(oracle_mod):
+    dense_case(oracle_mod, "q4_0", 8192, 4096, [1, 512], full_upto=1)
+
+
+def test_moe_decode_e128_n1536_k4096_t1_top8(oracle_mod):
+    """The decode form of the MoE workload (one token, top-8: one GEMV per pair), whole output."""
+    E, n, k, T_, K = 128, 1536, 4096, 1, 8
+    W, x, ids = qmm_synth.make_moe(E, n, k, T_, K, seed=2)
+    xq = oracle_mod.quantize_q8_1(x)
+    ws = torch.empty(max(256, qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, K)), dtype=torch.uint8, device=DEV)
+    y = qmm.qmm_mul_mat_id(torch.from_numpy(W).to(DEV), "q4_K", E, n, k, torch.from_numpy(xq).to(DEV),
+                           torch.from_numpy(ids).to(DEV), K, T_, workspace=ws)
+    assert qmm.qmm_read_device_status(ws) == 0
+    y_ref, T, bad = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, xq, ids)
+    assert bad == 0
+    assert_within(y.cpu().numpy(), y_ref, T, "moe decode full size")
+
+
+@pytest.mark.parametrize("m", [1, 512])
+def test_glu_packed_n14336_k4096(oracle_mod, m):
+    """The fused gate/up rows of the bench on the interleaved tensor: m = 1 whole, m = 512
+    sampled; the same bits as the two-tensor call."""
+    n, k = 14336, 4096
+    W, x = qmm_synth.make_dense("q4_K", 2 * n, k, m, seed=0)
+    Wg, Wu = W[:n].copy(), W[n:].copy()
+    xq = oracle_mod.quantize_q8_1(x)
+    Wg_d, Wu_d, xq_d = (torch.from_numpy(a).to(DEV) for a in (Wg, Wu, xq))
+    y_p = qmm.qmm_mul_mat_glu_packed(qmm.qmm_repack_glu(Wg_d, Wu_d, "q4_K", n, k), "q4_K", n, k, xq_d, m)
+    y_2 = qmm.qmm_mul_mat_glu(Wg_d, Wu_d, "q4_K", n, k, xq_d, m)
+    torch.cuda.synchronize()
+    a = y_p.cpu().numpy()
+    assert np.array_equal(a, y_2.cpu().numpy())
+    if m == 1:
+        y_ref, tol = oracle_mod.mul_mat_glu(Wg, Wu, "q4_K", n, k, xq, m)
+        assert not (np.abs(a - y_ref) > tol).any()
+    else:
+        rng = np.random.default_rng(5)
+        rows, cols = sample_positions(rng, n, m, 1500)
+        ref, tol = oracle_mod.mul_mat_glu_at(Wg, Wu, "q4_K", n, k, xq, m, rows, cols)
+        assert not (np.abs(a[cols, rows] - ref) > tol).any()

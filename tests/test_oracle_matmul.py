@@ -278,3 +278,16 @@ def test_repack_glu_row_order(oracle_mod):
     y2, _ = oracle_mod.mul_mat(oracle_mod.repack_glu(Wg, Wu), "q4_K", 2 * n, k, xq, m)
     assert np.array_equal(y2[:, 0::2], oracle_mod.mul_mat(Wg, "q4_K", n, k, xq, m)[0])
     assert np.array_equal(y2[:, 1::2], oracle_mod.mul_mat(Wu, "q4_K", n, k, xq, m)[0])
+
+
+def test_mul_mat_glu_at_matches_full(oracle_mod):
+    rng = np.random.default_rng(43)
+    n, k, m = 7, 512, 3
+    Wg = qmm_synth.gen_weights("q4_K", rng, n, k)
+    Wu = qmm_synth.gen_weights("q4_K", rng, n, k)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, m, k))
+    y, tol = oracle_mod.mul_mat_glu(Wg, Wu, "q4_K", n, k, xq, m)
+    rows = np.array([0, 6, 3, 5])
+    cols = np.array([2, 0, 1, 2])
+    ya, ta = oracle_mod.mul_mat_glu_at(Wg, Wu, "q4_K", n, k, xq, m, rows, cols)
+    assert np.array_equal(ya, y[cols, rows]) and np.array_equal(ta, tol[cols, rows])
