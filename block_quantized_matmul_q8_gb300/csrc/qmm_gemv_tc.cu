@@ -85,16 +85,55 @@ constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 static_assert(kSmemAlloc <= 227 * 1024, "shared memory map exceeds the per-CTA limit");
 
 struct SkArgs {
-    int64_t n;      // weight rows
+    int64_t n;      // weight rows (grouped: per expert)
     int m;          // activation rows (1..16)
     int64_t nsb;    // superblocks per row
-    int64_t ntiles; // 128-row tiles
-    int64_t nwork;  // ntiles * nsb
+    int64_t ntiles; // 128-row tiles (grouped: per expert)
+    int64_t nwork;  // ntiles * nsb (grouped: set in the kernel from *ncold)
     int ctas;
-    float *y;       // [m][n]
+    float *y;       // [m][n] (grouped: [pairs][n])
     float *partial; // [ctas][2][128][16]
     int *status;
+    // Expert-grouped mode (cold != nullptr, MoE experts with 1..16 pairs): tile c * ntiles
+    // + t is the 128-row tile t of expert cold[c]; its activations are the 16-row slab c
+    // of the gathered buffers, its output column j < count the pair perm[bounds[e] + j].
+    const int32_t *cold;
+    const int32_t *ncold;
+    const int32_t *bounds;
+    const int32_t *perm;
 };
+
+// What a tile addresses: the first W row (in the map over all experts' rows), the first
+// row of its activation slab and of its d8 rows, and the output columns it holds.
+struct SkTile {
+    int64_t wrow0, xrow0, dxrow0;
+    int64_t row0;   // first weight row within its expert (the output feature)
+    int cols;       // valid activation columns
+    int32_t pair0;  // grouped: offset of the expert's pairs in perm
+};
+// the y row of activation column j of a tile: j itself, or its pair
+__device__ __forceinline__ int64_t sk_out_row(const SkArgs &a, const SkTile &tt, int j) {
+    return a.cold ? int64_t(a.perm[tt.pair0 + j]) : int64_t(j);
+}
+__device__ __forceinline__ SkTile sk_tile(const SkArgs &a, int64_t tile) {
+    SkTile r;
+    if (!a.cold) {
+        r.wrow0 = r.row0 = tile * kRows;
+        r.xrow0 = r.dxrow0 = 0;
+        r.cols = a.m;
+        r.pair0 = 0;
+        return r;
+    }
+    const int64_t c = tile / a.ntiles, t = tile - c * a.ntiles;
+    const int e = a.cold[c];
+    r.row0 = t * kRows;
+    r.wrow0 = int64_t(e) * a.n + r.row0;
+    r.xrow0 = c * kNT;
+    r.dxrow0 = c * (a.nsb * 8);
+    r.pair0 = a.bounds[e];
+    r.cols = a.bounds[e + 1] - r.pair0;
+    return r;
+}
 
 struct Barriers {
     uint64_t x_full[kXStages], x_empty[kXStages], w_full[kABufs], w_empty[kABufs];
@@ -129,7 +168,13 @@ __device__ __forceinline__ uint32_t slot_col(uint32_t sbs, int G) { return kSlot
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_tc_q4k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
                        const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
-                       const SkArgs a) {
+                       const SkArgs a_in) {
+    SkArgs a = a_in;
+    if (a.cold) {
+        // the cold list and the gathered activations come from the preceding kernels
+        ptx::grid_dependency_wait();
+        a.nwork = int64_t(*a.ncold) * a.ntiles * a.nsb;
+    }
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ Barriers B;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -187,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sbc = 0;
             bool ok = true;
             while (ok && next_seg(a, u, uend, sg)) {
+                const SkTile tt = sk_tile(a, sg.tile);
                 for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb, ++sbc) {
                     const uint32_t sdi = sbc % kSdRing, ph = (sbc / kSdRing) & 1;
                     if (!ptx::mbar_wait(ptx::smem_u32(&B.sd_empty[sdi]), ph ^ 1, abortp)) {
@@ -195,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t sdbar = ptx::smem_u32(&B.sd_full[sdi]);
                     ptx::mbar_arrive_expect_tx(sdbar, kDXBytes);
-                    ptx::tma_load_2d(sbase + kOffDX + sdi * kDXBytes, &tm_dx, 0, (int)(8 * sb), sdbar);
+                    ptx::tma_load_2d(sbase + kOffDX + sdi * kDXBytes, &tm_dx, 0, (int)(tt.dxrow0 + 8 * sb), sdbar);
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t xi = (2 * sbc + h) % kXStages, xph = ((2 * sbc + h) / kXStages) & 1;
                         if (!ptx::mbar_wait(ptx::smem_u32(&B.x_empty[xi]), xph ^ 1, abortp)) {
@@ -205,9 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t bar = ptx::smem_u32(&B.x_full[xi]);
                         ptx::mbar_arrive_expect_tx(bar, 2 * kXSlab + (h ? kNT * 32u : 0u));
                         const int kx = (int)(256 * sb + 128 * h);
-                        ptx::tma_load_2d(sbase + kOffX + xi * 2 * kXSlab, &tm_x, kx, 0, bar);
-                        ptx::tma_load_2d(sbase + kOffX + xi * 2 * kXSlab + kXSlab, &tm_x, kx + 64, 0, bar);
-                        if (h) ptx::tma_load_2d(sbase + kOffXmin + sdi * (kNT * 32), &tm_xmin, (int)(16 * sb), 0, bar);
+                        const int xr = (int)tt.xrow0;
+                        ptx::tma_load_2d(sbase + kOffX + xi * 2 * kXSlab, &tm_x, kx, xr, bar);
+                        ptx::tma_load_2d(sbase + kOffX + xi * 2 * kXSlab + kXSlab, &tm_x, kx + 64, xr, bar);
+                        if (h) ptx::tma_load_2d(sbase + kOffXmin + sdi * (kNT * 32), &tm_xmin, (int)(16 * sb), xr, bar);
                     }
                 }
             }
@@ -283,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r_it = 0;
             bool ok = true;
             while (ok && next_seg(a, u, uend, sg)) {
-                const int n0 = (int)(sg.tile * kRows);
+                const int n0 = (int)sk_tile(a, sg.tile).wrow0;
                 for (int64_t sb = sg.s0; sb < sg.s1; ++sb, ++r_it) {
                     const uint32_t ri = r_it % kRawStages, ph = (r_it / kRawStages) & 1;
                     if (!ptx::mbar_wait(ptx::smem_u32(&B.raw_empty[ri]), ph ^ 1, abortp)) {
@@ -446,12 +493,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the segment's result: whole tile -> y, part of a tile -> this CTA's partial slot
             const bool full = sg.s0 == 0 && sg.s1 == a.nsb;
             if (full) {
-                const int64_t row = sg.tile * kRows + tl;
+                const SkTile tt = sk_tile(a, sg.tile);
+                const int64_t row = tt.row0 + tl;
                 if (row < a.n) {
 #pragma unroll
                     for (int i = 0; i < kNT / 2; ++i) {
-                        if (2 * i < a.m) a.y[int64_t(2 * i) * a.n + row] = tot[i].x;
-                        if (2 * i + 1 < a.m) a.y[int64_t(2 * i + 1) * a.n + row] = tot[i].y;
+                        if (2 * i < tt.cols) a.y[sk_out_row(a, tt, 2 * i) * a.n + row] = tot[i].x;
+                        if (2 * i + 1 < tt.cols) a.y[sk_out_row(a, tt, 2 * i + 1) * a.n + row] = tot[i].y;
                     }
                 }
             } else {
@@ -513,9 +561,66 @@ __global__ void gemv_tc_prep_kernel(const uint8_t *__restrict__ xq, int m, int k
     }
 }
 
+// The same for the cold experts of an expert-grouped call: slab c (rows 16c .. 16c+15 of
+// xh and smin, d8 rows c*k/32 .. of dxt) holds the activation rows of expert cold[c]'s
+// pairs in their sorted order, zeros past its pair count.  Activation row of pair p:
+// xq row p / x_div.
+__global__ void gemv_tc_prep_grouped_kernel(const uint8_t *__restrict__ xq, int64_t x_div, int k,
+                                            const int32_t *__restrict__ cold, const int32_t *__restrict__ ncold,
+                                            const int32_t *__restrict__ bounds, const int32_t *__restrict__ perm,
+                                            __half *__restrict__ xh, __half *__restrict__ smin,
+                                            float *__restrict__ dxt) {
+    // the pair lists come from the bucketing kernel before this one
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
+    const int nb32 = k / 32;
+    const int64_t per_slot = int64_t(kNT) * nb32;
+    const int64_t total = int64_t(*ncold) * per_slot;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t c = i / per_slot, rem = i - c * per_slot;
+        const int b = (int)(rem / kNT), r = (int)(rem - int64_t(b) * kNT);
+        const int e = cold[c];
+        const int cnt = bounds[e + 1] - bounds[e];
+        const int64_t xr = c * kNT + r;  // row of the gathered buffers
+        uint4 *dst = reinterpret_cast<uint4 *>(xh + xr * k + 32 * b);
+        __half *sp = smin + (xr * (nb32 / 8) + b / 8) * 16;
+        if (r >= cnt) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(0u, 0u, 0u, 0u);
+            dxt[i] = 0.f;
+            sp[b % 8] = __ushort_as_half(0);
+            sp[8 + b % 8] = __ushort_as_half(0);
+            continue;
+        }
+        const int64_t row = int64_t(perm[bounds[e] + r]) / x_div;
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (row * nb32 + b) * kQ81Bytes);
+        const uint32_t dsw = ldg4(src);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t w0 = ldg4(src + 1 + 2 * j), w1 = ldg4(src + 2 + 2 * j);
+            const int8_t *c0 = reinterpret_cast<const int8_t *>(&w0);
+            const int8_t *c1 = reinterpret_cast<const int8_t *>(&w1);
+            uint4 o;
+            o.x = h2bits(__halves2half2(__int2half_rn(c0[0]), __int2half_rn(c0[1])));
+            o.y = h2bits(__halves2half2(__int2half_rn(c0[2]), __int2half_rn(c0[3])));
+            o.z = h2bits(__halves2half2(__int2half_rn(c1[0]), __int2half_rn(c1[1])));
+            o.w = h2bits(__halves2half2(__int2half_rn(c1[2]), __int2half_rn(c1[3])));
+            dst[j] = o;
+        }
+        dxt[i] = half_lo(dsw);
+        sp[b % 8] = __ushort_as_half((unsigned short)(dsw >> 16));
+        sp[8 + b % 8] = __ushort_as_half(0);
+    }
+}
+
 // stream-K fixup: every tile that several CTAs share is summed in CTA order; one thread
 // per weight row, 16 columns.
-__global__ void __launch_bounds__(kRows) gemv_tc_fixup_kernel(const SkArgs a) {
+__global__ void __launch_bounds__(kRows) gemv_tc_fixup_kernel(const SkArgs a_in) {
+    SkArgs a = a_in;
+    if (a.cold) {  // grouped: one block per tile of any expert; only those of the cold ones exist
+        a.nwork = int64_t(*a.ncold) * a.ntiles * a.nsb;
+        if (int64_t(blockIdx.x) * a.nsb >= a.nwork) return;
+    }
     const int64_t t = blockIdx.x;
     const int64_t u0 = t * a.nsb, u1 = u0 + a.nsb - 1;
     auto owner = [&](int64_t uu) {
@@ -544,11 +649,12 @@ __global__ void __launch_bounds__(kRows) gemv_tc_fixup_kernel(const SkArgs a) {
             s[4 * i4 + 3] += v.w;
         }
     }
-    const int64_t row = t * kRows + tl;
+    const SkTile tt = sk_tile(a, t);
+    const int64_t row = tt.row0 + tl;
     if (row >= a.n) return;
 #pragma unroll
     for (int i = 0; i < kNT; ++i)
-        if (i < a.m) a.y[int64_t(i) * a.n + row] = s[i];
+        if (i < tt.cols) a.y[sk_out_row(a, tt, i) * a.n + row] = s[i];
 }
 
 struct SkLayout {
@@ -577,6 +683,89 @@ int sk_ctas(int64_t n, int64_t k) {
 }
 
 }  // namespace
+
+bool gemv_tc_grouped_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k) {
+    // TMA coordinates are 32-bit: the map over all experts' rows and the gathered slabs
+    return t == QMM_Q4_K && k % 256 == 0 && n > 0 && n_experts > 0 && n_experts * n < (int64_t(1) << 31) &&
+           n_experts * kNT * (k / 32) < (int64_t(1) << 31);
+}
+
+namespace {
+struct SkGroupedLayout {
+    size_t xh, smin, dxt, partial, total;
+};
+SkGroupedLayout sk_grouped_layout(int64_t n_experts, int64_t k) {
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    SkGroupedLayout L{};
+    size_t off = 0;
+    L.xh = off;
+    off = al(off + size_t(n_experts) * kNT * k * 2);
+    L.smin = off;
+    off = al(off + size_t(n_experts) * kNT * (k / 256) * 32);
+    L.dxt = off;
+    off = al(off + size_t(n_experts) * (k / 32) * kNT * 4);
+    L.partial = off;
+    off = al(off + size_t(kMaxPartialCtas) * 2 * kRows * kNT * 4);
+    L.total = off;
+    return L;
+}
+}  // namespace
+
+size_t gemv_tc_grouped_bytes(int64_t n_experts, int64_t k) { return sk_grouped_layout(n_experts, k).total; }
+
+cudaError_t launch_gemv_tc_grouped(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                                   int64_t x_div, const int32_t *cold, const int32_t *ncold, const int32_t *bounds,
+                                   const int32_t *perm, float *y, int *status, void *ws, size_t ws_bytes,
+                                   cudaStream_t st) {
+    if (!gemv_tc_grouped_supported(QMM_Q4_K, n_experts, n, k)) return cudaErrorNotSupported;
+    const SkGroupedLayout L = sk_grouped_layout(n_experts, k);
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    __half *xh = reinterpret_cast<__half *>(base + L.xh);
+    __half *smin = reinterpret_cast<__half *>(base + L.smin);
+    float *dxt = reinterpret_cast<float *>(base + L.dxt);
+    const int64_t nprep = n_experts * kNT * (k / 32);
+    const int pgrid = (int)std::min<int64_t>((nprep + 255) / 256, int64_t(device_sm_count()) * 4);
+    cudaError_t e = launch_pdl(gemv_tc_prep_grouped_kernel, dim3(std::max(pgrid, 1)), dim3(256), 0, st,
+                               static_cast<const uint8_t *>(xq), x_div, (int)k, cold, ncold, bounds, perm, xh, smin,
+                               dxt);
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
+    const uint64_t row_bytes = uint64_t(k / 256) * kQ4KBytes;
+    const int64_t xrows = n_experts * kNT;
+    if (!tc_make_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, k, xrows, uint64_t(k) * 2, 64, kNT,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tc_make_map_2d(&tm_xmin, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, smin, (k / 256) * 16, xrows,
+                        uint64_t(k / 256) * 32, 16, kNT, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !tc_make_map_2d(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dxt, kNT, n_experts * (k / 32), kNT * 4, kNT, 8,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !tc_make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, n_experts * n, row_bytes, kQ4KBytes,
+                        kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+
+    SkArgs a{};
+    a.n = n;
+    a.m = kNT;
+    a.nsb = k / 256;
+    a.ntiles = (n + kRows - 1) / kRows;
+    a.nwork = 0;  // set on the device from *ncold
+    a.ctas = std::min(device_sm_count(), kMaxPartialCtas);
+    a.y = y;
+    a.partial = reinterpret_cast<float *>(base + L.partial);
+    a.status = status;
+    a.cold = cold;
+    a.ncold = ncold;
+    a.bounds = bounds;
+    a.perm = perm;
+
+    e = cudaFuncSetAttribute(gemv_tc_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(gemv_tc_q4k_kernel, dim3(a.ctas), dim3(kThreads), kSmemAlloc, st, tm_x, tm_xmin, tm_dx, tm_w, a);
+    if (e != cudaSuccess) return e;
+    gemv_tc_fixup_kernel<<<(unsigned)(n_experts * a.ntiles), kRows, 0, st>>>(a);
+    return cudaGetLastError();
+}
 
 bool gemv_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
     return t == QMM_Q4_K && k % 256 == 0 && n > 0 && m >= 1 && m <= kMaxM;

@@ -67,6 +67,15 @@ cudaError_t launch_gemv_id(qmm_type t, const void *W, int64_t n_experts, int64_t
 // Tensor-core path for skinny activations (Q4_K, 1 <= m <= 16): weights as the MMA's
 // 128-row M side, activations as N = 16; stream-K over (row tile, superblock) units.
 bool gemv_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
+// Expert-grouped skinny path for the cold experts of mul_mat_id (1..16 pairs each): the
+// cold list and its count (on the device) come from the bucketing kernel; x_div as in
+// gemv_id.  y rows are pairs; status receives QMM_ERR_DEVICE if a wait gives up.
+bool gemv_tc_grouped_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k);
+size_t gemv_tc_grouped_bytes(int64_t n_experts, int64_t k);
+cudaError_t launch_gemv_tc_grouped(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+                                   int64_t x_div, const int32_t *cold, const int32_t *ncold, const int32_t *bounds,
+                                   const int32_t *perm, float *y, int *status, void *ws, size_t ws_bytes,
+                                   cudaStream_t st);
 size_t gemv_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m);
 cudaError_t launch_gemv_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
                            void *ws, size_t ws_bytes, cudaStream_t st);

@@ -31,7 +31,7 @@ constexpr int kBucketWarps = kBucketThreads / 32;
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-MoELayout moe_layout(int64_t n_pairs, int64_t n_experts, int tile_tokens, size_t gemm_bytes) {
+MoELayout moe_layout(int64_t n_pairs, int64_t n_experts, int tile_tokens, size_t gemm_bytes, size_t cold_bytes) {
     MoELayout L{};
     size_t off = 0;
     L.status = off;
@@ -43,15 +43,20 @@ MoELayout moe_layout(int64_t n_pairs, int64_t n_experts, int tile_tokens, size_t
     L.tiles = off;
     const int64_t max_tiles = n_pairs / tile_tokens + n_experts + 1;
     off = align256(off + sizeof(MoETile) * size_t(max_tiles));
+    L.cold = off;
+    off = align256(off + sizeof(int32_t) * size_t(n_experts));
     L.gemm = off;
     off = align256(off + gemm_bytes);
+    L.cold_gemm = off;
+    off = align256(off + cold_bytes);
     L.total = off;
     return L;
 }
 
 __global__ void __launch_bounds__(kBucketThreads) moe_bucket_kernel(const int32_t *__restrict__ ids, int64_t n_pairs,
-                                                                    int E, int tile_tokens, int32_t *status,
-                                                                    int32_t *bounds, int32_t *perm, MoETile *tiles) {
+                                                                    int E, int tile_tokens, int cold_max,
+                                                                    int32_t *status, int32_t *bounds, int32_t *perm,
+                                                                    MoETile *tiles, int32_t *cold) {
     extern __shared__ __align__(16) int32_t sm[];
     int32_t *cnt = sm;                          // [E]   counts, then running bases
     int32_t *toff = cnt + E;                    // [E]   tile offsets
@@ -76,28 +81,31 @@ __global__ void __launch_bounds__(kBucketThreads) moe_bucket_kernel(const int32_
     }
     __syncthreads();
 
-    // scan (one thread: E <= kMaxExperts)
+    // scan (one thread: E <= kMaxExperts).  Experts with 1..cold_max pairs get no tiles:
+    // they go to the cold list, in expert order.
     if (tid == 0) {
-        int run = 0, trun = 0;
+        int run = 0, trun = 0, ncold = 0;
         for (int e = 0; e < E; ++e) {
             const int c = cnt[e];
             bounds[e] = run;
             cnt[e] = run;  // running base for pass 2
             toff[e] = trun;
             run += c;
-            trun += (c + tile_tokens - 1) / tile_tokens;
+            if (c > 0 && c <= cold_max) cold[ncold++] = e;
+            else trun += (c + tile_tokens - 1) / tile_tokens;
         }
         bounds[E] = run;
         status[0] = s_bad ? (int32_t)QMM_ERR_IDS : (int32_t)QMM_OK;
         status[1] = trun;
         status[2] = s_bad;
+        status[3] = ncold;
     }
     __syncthreads();
 
     // tile list
     for (int e = warp; e < E; e += kBucketWarps) {
         const int b0 = bounds[e], c = bounds[e + 1] - b0;
-        const int nt = (c + tile_tokens - 1) / tile_tokens;
+        const int nt = c <= cold_max ? 0 : (c + tile_tokens - 1) / tile_tokens;
         for (int t = lane; t < nt; t += 32) {
             MoETile mt;
             mt.expert = e;
@@ -154,30 +162,40 @@ __global__ void moe_zero_invalid_kernel(const int32_t *status, const int32_t *pe
     }
 }
 
-cudaError_t launch_moe_bucket(const int32_t *ids, int64_t n_pairs, int n_experts, int tile_tokens, void *ws,
-                              const MoELayout &L, cudaStream_t st) {
+cudaError_t launch_moe_bucket(const int32_t *ids, int64_t n_pairs, int n_experts, int tile_tokens, int cold_max,
+                              void *ws, const MoELayout &L, cudaStream_t st) {
     uint8_t *base = static_cast<uint8_t *>(ws);
     const size_t smem = sizeof(int32_t) * size_t(n_experts) * (2 + 2 * kBucketWarps);
     cudaError_t e = cudaFuncSetAttribute(moe_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     moe_bucket_kernel<<<1, kBucketThreads, smem, st>>>(
-        ids, n_pairs, n_experts, tile_tokens, reinterpret_cast<int32_t *>(base + L.status),
+        ids, n_pairs, n_experts, tile_tokens, cold_max, reinterpret_cast<int32_t *>(base + L.status),
         reinterpret_cast<int32_t *>(base + L.bounds), reinterpret_cast<int32_t *>(base + L.perm),
-        reinterpret_cast<MoETile *>(base + L.tiles));
+        reinterpret_cast<MoETile *>(base + L.tiles), reinterpret_cast<int32_t *>(base + L.cold));
     return cudaGetLastError();
 }
 
 constexpr int kDp4aTileTokens = 64;   // pairs per token tile of the CUDA-core grouped GEMM
 constexpr int kTcTileTokens = 128;    // pairs per token tile of the tensor-core grouped GEMM
+// Experts with at most this many pairs skip the 128-pair tiles of the tensor-core grouped
+// GEMM (which would hold them in 128 rows) and run on the skinny tensor-core kernel,
+// their pairs as its N = 16 columns.
+constexpr int kColdMaxPairs = 16;
+
+static size_t cold_bytes(qmm_type t, int64_t n_experts, int64_t n, int64_t k) {
+    return gemv_tc_grouped_supported(t, n_experts, n, k) ? gemv_tc_grouped_bytes(n_experts, k) : 0;
+}
 
 size_t moe_dp4a_workspace_bytes(int64_t n_tokens, int64_t n_experts, int64_t top_k) {
-    return moe_layout(n_tokens * top_k, n_experts, kDp4aTileTokens, 0).total;
+    return moe_layout(n_tokens * top_k, n_experts, kDp4aTileTokens, 0, 0).total;
 }
 
 size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k) {
     const int64_t n_pairs = n_tokens * top_k;
     if (gemm_tc_grouped_supported(t, n_experts, n, k))
-        return moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k)).total;
+        return moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k),
+                          cold_bytes(t, n_experts, n, k))
+            .total;
     return moe_dp4a_workspace_bytes(n_tokens, n_experts, top_k);
 }
 
@@ -185,9 +203,9 @@ cudaError_t launch_mul_mat_id_dp4a(qmm_type t, const void *W, int64_t n_experts,
                                    const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
                                    bool x_per_slot, float *y, void *ws, size_t ws_bytes, cudaStream_t st) {
     const int64_t n_pairs = n_tokens * top_k;
-    const MoELayout L = moe_layout(n_pairs, n_experts, kDp4aTileTokens, 0);
+    const MoELayout L = moe_layout(n_pairs, n_experts, kDp4aTileTokens, 0, 0);
     if (ws_bytes < L.total) return cudaErrorInvalidValue;
-    cudaError_t e = launch_moe_bucket(ids, n_pairs, (int)n_experts, kDp4aTileTokens, ws, L, st);
+    cudaError_t e = launch_moe_bucket(ids, n_pairs, (int)n_experts, kDp4aTileTokens, 0, ws, L, st);
     if (e != cudaSuccess) return e;
     uint8_t *base = static_cast<uint8_t *>(ws);
     const int32_t *status = reinterpret_cast<const int32_t *>(base + L.status);
@@ -216,9 +234,12 @@ cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int6
     if (!gemm_tc_grouped_supported(t, n_experts, n, k))
         return launch_mul_mat_id_dp4a(t, W, n_experts, n, k, xq, ids, top_k, n_tokens, x_per_slot, y, ws, ws_bytes,
                                       st);
-    const MoELayout L = moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k));
+    const bool split = gemv_tc_grouped_supported(t, n_experts, n, k);
+    const MoELayout L = moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k),
+                                   cold_bytes(t, n_experts, n, k));
     if (ws_bytes < L.total) return cudaErrorInvalidValue;
-    cudaError_t e = launch_moe_bucket(ids, n_pairs, (int)n_experts, kTcTileTokens, ws, L, st);
+    cudaError_t e =
+        launch_moe_bucket(ids, n_pairs, (int)n_experts, kTcTileTokens, split ? kColdMaxPairs : 0, ws, L, st);
     if (e != cudaSuccess) return e;
     uint8_t *base = static_cast<uint8_t *>(ws);
     int32_t *status = reinterpret_cast<int32_t *>(base + L.status);
@@ -228,10 +249,14 @@ cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int6
     moe_zero_invalid_kernel<<<64, 256, 0, st>>>(status, perm, bounds, (int)n_experts, y, n);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    const int64_t x_div = x_per_slot ? 1 : top_k;
     const int64_t max_token_tiles = n_pairs / kTcTileTokens + n_experts + 1;
-    return launch_gemm_tc_grouped(W, n_experts, n, k, xq, x_per_slot ? 1 : top_k, n_pairs, y, tiles, status + 1,
-                                  max_token_tiles,
-                                  bounds, perm, status, base + L.gemm, L.total - L.gemm, st);
+    e = launch_gemm_tc_grouped(W, n_experts, n, k, xq, x_div, n_pairs, y, tiles, status + 1, max_token_tiles, bounds,
+                               perm, status, base + L.gemm, L.cold_gemm - L.gemm, st);
+    if (e != cudaSuccess || !split) return e;
+    // the cold experts: 16-column slabs on the skinny tensor-core kernel
+    return launch_gemv_tc_grouped(W, n_experts, n, k, xq, x_div, reinterpret_cast<const int32_t *>(base + L.cold),
+                                  status + 3, bounds, perm, y, status, base + L.cold_gemm, L.total - L.cold_gemm, st);
 }
 
 }  // namespace qmm

@@ -237,3 +237,50 @@ def test_q4_0_extreme_codes(oracle_mod, path):
     xq = oracle_mod.quantize_q8_1(x)
     y_ref, T = oracle_mod.mul_mat(W, "q4_0", n, k, xq, m)
     assert_within(run_mul_mat(W, "q4_0", n, k, xq, m, path=path), y_ref, T, f"q4_0 extreme path={path}")
+
+
+# Cold experts (1..16 pairs) run as 16-column slabs on the skinny tensor-core kernel, the
+# others on 128-pair tiles of the grouped GEMM; hand-built routings pin the boundary.
+def moe_check_ids(oracle_mod, E, n, k, ids, seed, per_slot=False):
+    T_, K = ids.shape
+    W = qmm_synth.gen_weights("q4_K", np.random.default_rng(seed), E * n, k).reshape(E, n, -1)
+    x = qmm_synth.gen_x(np.random.default_rng(seed + 1), T_ * K if per_slot else T_, k)
+    xq = oracle_mod.quantize_q8_1(x)
+    y_ref, Tr, bad = oracle_mod.mul_mat_id(W, "q4_K", E, n, k, xq, ids, per_slot=per_slot)
+    ws = torch.empty(qmm.qmm_workspace_bytes("q4_K", n, k, T_, E, K), dtype=torch.uint8, device=DEV)
+    y = torch.full((T_, K, n), float("nan"), device=DEV)
+    call = qmm.qmm_mul_mat_id_slot if per_slot else qmm.qmm_mul_mat_id
+    call(to_dev(W), "q4_K", E, n, k, to_dev(xq), to_dev(ids), K, T_, y=y, workspace=ws)
+    assert qmm.qmm_read_device_status(ws) == (7 if bad else 0)
+    assert_within(y.cpu().numpy(), y_ref, Tr, f"moe ids E={E} n={n} k={k} T={T_} K={K} per_slot={per_slot}")
+
+
+def routing(counts, K, seed, extra_invalid=0):
+    """ids [T][K] giving expert e exactly counts[e] pairs (shuffled), invalid ids appended."""
+    flat = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)] +
+                          [np.full(extra_invalid, -1, np.int32)])
+    pad = (-len(flat)) % K
+    flat = np.concatenate([flat, np.full(pad, len(counts), np.int32)])  # id E: invalid
+    np.random.default_rng(seed).shuffle(flat)
+    return flat.reshape(-1, K)
+
+
+@pytest.mark.parametrize("per_slot", [False, True])
+def test_moe_cold_hot_boundary(oracle_mod, per_slot):
+    counts = [16, 17, 1, 0, 15, 2, 130, 16, 3, 40]
+    moe_check_ids(oracle_mod, len(counts), 130, 512, routing(counts, 4, seed=3), seed=4, per_slot=per_slot)
+
+
+def test_moe_all_cold(oracle_mod):
+    counts = [1 + (e * 7) % 16 for e in range(40)]
+    moe_check_ids(oracle_mod, 40, 256, 768, routing(counts, 8, seed=5), seed=6)
+
+
+def test_moe_cold_with_invalid_ids(oracle_mod):
+    counts = [5, 0, 12, 16, 3, 200]
+    moe_check_ids(oracle_mod, 6, 96, 1024, routing(counts, 2, seed=7, extra_invalid=9), seed=8)
+
+
+@pytest.mark.parametrize("E,n,k,T_,K", [(64, 256, 512, 40, 8), (32, 130, 768, 20, 4), (128, 1536, 256, 64, 8)])
+def test_moe_mostly_cold_parity(oracle_mod, E, n, k, T_, K):
+    moe_check(oracle_mod, E, n, k, T_, K, seed=E + T_)
