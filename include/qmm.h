@@ -230,7 +230,11 @@ QMM_API qmm_status qmm_mul_mat_glu_packed(const void *W_gu, qmm_type t, int64_t 
  *     and the per-expert tiles are walked by one persistent launch: Q4_K with
  *     k % 256 == 0 on the tensor cores (128-pair tiles, stream-K over the device-built
  *     tile list; the workspace then also holds an fp16 copy of the gathered
- *     activations), the other formats on the CUDA-core grouped GEMM.
+ *     activations), the other formats on the CUDA-core grouped GEMM.  For Q4_K the
+ *     experts with 1..16 pairs ([MMQ] section "MoE 的二次账": experts whose few columns
+ *     leave the tiles mostly empty) skip the 128-pair tiles: a second launch runs them
+ *     as 16-column slabs on the skinny tensor-core kernel, the expert list and its
+ *     length read on the device.
  */
 QMM_API qmm_status qmm_mul_mat_id(const void *W_experts, qmm_type t, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                           const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y, void *workspace,
