@@ -30,6 +30,9 @@
 //               that row's TMEM lane (the MMA's A operand: fp16 pairs along the columns),
 //               so the unpacked weights never pass through shared memory; group 1 also
 //               writes the fp16 mins (shared memory), group 0 (d, -dmin) for the epilogue.
+//               A group hands a half to the MMA only once that half's activation slabs
+//               have landed too, so the MMA thread observes one barrier per half (each
+//               completion it waits for idles the tensor pipe for a few hundred cycles).
 //   warps 12-15 epilogue: one weight row per thread, 16 activation columns, the running
 //               sums in registers.
 // Every wait is bounded (qmm_tc_ptx.cuh); a wait that gives up raises the CTA's abort
@@ -283,10 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tc_fence_after();
                     for (int h = 0; ok && h < 2; ++h) {
-                        const uint32_t xi = (2 * sbc + h) % kXStages, xph = ((2 * sbc + h) / kXStages) & 1;
+                        const uint32_t xi = (2 * sbc + h) % kXStages;
                         const uint32_t ai = (2 * sbc + h) % kABufs, aph2 = ((2 * sbc + h) / kABufs) & 1;
-                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.x_full[xi]), xph, abortp) ||
-                            !ptx::mbar_wait_spin(ptx::smem_u32(&B.w_full[ai]), aph2, abortp)) {
+                        // w_full covers the activation half too: its unpack group waited for it
+                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.w_full[ai]), aph2, abortp)) {
                             ok = false;
                             break;
                         }
@@ -427,6 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_st_wait();
                 ptx::fence_proxy_async_smem();  // the mins are read by the MMA (async proxy)
                 ptx::tc_fence_before();
+                // The MMA thread waits only on w_full, so the group first waits for this half's
+                // activation slabs (and, for half 1, the s tile): group h alone waits on the
+                // x barriers of the halves 2s + h, since the x ring is 8 deep.
+                {
+                    const uint32_t xi = (2 * sbc + h) % kXStages, xph = ((2 * sbc + h) / kXStages) & 1;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.x_full[xi]), xph, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 ptx::mbar_arrive(ptx::smem_u32(&B.w_full[ai]));
                 ptx::mbar_arrive(ptx::smem_u32(&B.raw_empty[ri]));
             }
