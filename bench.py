@@ -80,6 +80,28 @@ def gemv_q8_bytes(n, k, m, row_bytes):
     return n * row_bytes + m * (k // 32) * 36 + m * n * 4
 
 
+def int8_tensor_peak():
+    """The GPU's dense int8 tensor-core rate in TOPS: on sm_103a tcgen05 has no int8 kind,
+    so it is the mma.sync s8 rate, measured by peaks/mma_sync_peak.cu and recorded in
+    profiles/mma_sync_peak.json (None when the record is missing)."""
+    p = os.path.join(ROOT, "profiles", "mma_sync_peak.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        return json.load(f).get("int8_mma_sync_tops")
+
+
+def tensor_fracs(tops):
+    """A GEMM row's fractions of the int8 tensor-core rate and of the measured bf16
+    (tcgen05) rate; the path runs kind::f16 MMAs, the bf16 figure is its own dtype's."""
+    out = {}
+    i8 = int8_tensor_peak()
+    if i8:
+        out["int8_tc_frac"] = tops / i8
+    out["fp16_tc_frac"] = tops / measured_peaks()[1]
+    return out
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -323,6 +345,7 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
                              "ms": ms_call}
             else:
                 rows[key] = {"tops": 2 * m * n * k / (ms_call * 1e-3) / 1e12, "ms": ms_call}
+                rows[key].update(tensor_fracs(rows[key]["tops"]))
             rows[key]["l2"] = f"{copies} weight copies ({copies * W.nbytes / 1e6:.0f} MB)"
         del Wd
         return rows
@@ -362,6 +385,7 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
                              "ms": ms_call}
             else:
                 rows[key] = {"tops": 2 * m * 2 * n * k / (ms_call * 1e-3) / 1e12, "ms": ms_call}
+                rows[key].update(tensor_fracs(rows[key]["tops"]))
             rows[key]["l2"] = f"{copies} copies of both weights ({copies * W.nbytes / 1e6:.0f} MB)"
         del Wg, Wu
         return rows
@@ -393,6 +417,7 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
         fn = lambda i: qmm.qmm_mul_mat_id(Wd, "q4_K", E, n, k, xq, idd, Kt, T_, y=y, workspace=ws)
         ms = time_graphs(torch, fn, steps, 3, lambda: None) / steps
         out[key_p] = {"tops": 2 * T_ * Kt * n * k / (ms * 1e-3) / 1e12, "ms": ms, "l2": "weights 453 MB > 3x L2"}
+        out[key_p].update(tensor_fracs(out[key_p]["tops"]))
     if only in key_d:
         order = np.random.default_rng(7).permutation(E).astype(np.int32)
         ids_d = [torch.from_numpy(order[8 * j:8 * j + 8].reshape(1, Kt).copy()).to(dev) for j in range(E // Kt)]
