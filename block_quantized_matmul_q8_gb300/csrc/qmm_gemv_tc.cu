@@ -14,7 +14,11 @@
 //
 // Work is the flattened stream of (128-row tile, superblock) units split evenly over one
 // CTA per SM ([MMQ] section "stream-K 的切法"); tiles shared by CTAs are summed by a fixup
-// kernel in CTA order.  16 warps:
+// kernel in CTA order.  The same kernel serves the cold experts of an expert-routed
+// matmul ([MMQ] section "MoE 的二次账": experts with a few pairs leave wide tiles mostly
+// empty): a tile is then (cold expert, 128 weight rows of it), its 16 columns that
+// expert's pairs, gathered into a 16-row slab, and its outputs go to the pairs' rows;
+// the list of cold experts and its length are read on the device.  16 warps:
 //   warp 0      TMA: fp16 activation slabs (128-byte swizzle, 8 half-superblocks in
 //               flight, since they come from L2 and every superblock needs new ones), the
 //               s tile of the min term, and d8 per superblock (transposed:
