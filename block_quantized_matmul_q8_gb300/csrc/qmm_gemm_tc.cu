@@ -1004,42 +1004,44 @@ __global__ void tc_prep_gather_kernel(const uint8_t *__restrict__ xq, int k, con
 // 4 weight columns per thread.
 constexpr int kFixupParts = 16;
 __global__ void __launch_bounds__(256) tc_fixup_kernel(TcArgs a) {
-    const int64_t t = blockIdx.x;
-    if (a.tiles) {
-        a.nwork = int64_t(*a.ntiles) * a.tiles_n * a.nsb;
-        if (t >= int64_t(*a.ntiles) * a.tiles_n) return;
+    int64_t ntiles = int64_t(gridDim.x);  // dense: one block column per tile
+    if (a.tiles) {  // grouped: the tile count is on the device; the grid strides over it
+        ntiles = int64_t(*a.ntiles) * a.tiles_n;
+        a.nwork = ntiles * a.nsb;
     }
-    const int64_t u0 = t * a.nsb, u1 = u0 + a.nsb - 1;
     auto owner = [&](int64_t uu) {
         int64_t c = uu * a.ctas / a.nwork;
         while (c + 1 < a.ctas && a.nwork * (c + 1) / a.ctas <= uu) ++c;
         while (c > 0 && a.nwork * c / a.ctas > uu) --c;
         return c;
     };
-    const int64_t c0 = owner(u0), c1 = owner(u1);
-    if (c0 == c1) return;  // the tile was written whole by one CTA
-    const TileInfo ti = resolve_tile(a, t);
     const int tl = blockIdx.y * (kTM / kFixupParts) + (threadIdx.x >> 5);  // 8 rows per CTA
     const int cl = 4 * (threadIdx.x & 31);                                 // 4 columns per thread
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t c = c0; c <= c1; ++c) {
-        const int64_t cb = a.nwork * c / a.ctas;
-        if (a.nwork * (c + 1) / a.ctas == cb) continue;  // fewer units than CTAs: c owns nothing
-        const int slotidx = (cb / a.nsb == t) ? 0 : 1;  // tile t is this CTA's first segment?
-        const float4 p = *reinterpret_cast<const float4 *>(a.partial + ((c * 2 + slotidx) * kTM + tl) * kTN + cl);
-        s.x += p.x;
-        s.y += p.y;
-        s.z += p.z;
-        s.w += p.w;
-    }
-    const int64_t col = ti.col0 + cl;
-    if (tl >= ti.rows) return;
-    const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
-    float *dst = a.y + yrow * a.n + col;
-    const float sv[4] = {s.x, s.y, s.z, s.w};
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int64_t u0 = t * a.nsb, u1 = u0 + a.nsb - 1;
+        const int64_t c0 = owner(u0), c1 = owner(u1);
+        if (c0 == c1) continue;  // the tile was written whole by one CTA
+        const TileInfo ti = resolve_tile(a, t);
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t c = c0; c <= c1; ++c) {
+            const int64_t cb = a.nwork * c / a.ctas;
+            if (a.nwork * (c + 1) / a.ctas == cb) continue;  // fewer units than CTAs: c owns nothing
+            const int slotidx = (cb / a.nsb == t) ? 0 : 1;  // tile t is this CTA's first segment?
+            const float4 p = *reinterpret_cast<const float4 *>(a.partial + ((c * 2 + slotidx) * kTM + tl) * kTN + cl);
+            s.x += p.x;
+            s.y += p.y;
+            s.z += p.z;
+            s.w += p.w;
+        }
+        const int64_t col = ti.col0 + cl;
+        if (tl >= ti.rows) continue;
+        const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
+        float *dst = a.y + yrow * a.n + col;
+        const float sv[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if (col + j < a.n) dst[j] = sv[j];
+        for (int j = 0; j < 4; ++j)
+            if (col + j < a.n) dst[j] = sv[j];
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1114,7 +1116,10 @@ cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CU
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (fixup_tiles > 0) {
-        tc_fixup_kernel<<<dim3((unsigned)fixup_tiles, kFixupParts), 256, 0, st>>>(args);
+        // dense: one block column per tile; grouped (the count known on the device only, up
+        // to fixup_tiles): a bounded grid that strides over the tiles
+        const int64_t gx = args.tiles ? std::min<int64_t>(fixup_tiles, int64_t(device_sm_count()) * 2) : fixup_tiles;
+        tc_fixup_kernel<<<dim3((unsigned)gx, kFixupParts), 256, 0, st>>>(args);
         e = cudaGetLastError();
     }
     return e;
