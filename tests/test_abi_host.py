@@ -185,3 +185,42 @@ def test_gemv_ring_depth_whole_rounds(L):
     assert qmm.qmm_gemv_ring_stages("q4_K", 0, 5120, 1, budget) == 0
     assert qmm.qmm_gemv_ring_stages("q4_K", 16, 5000, 1, budget) == 0
     assert qmm.qmm_gemv_ring_stages("q4_K", 16, 5120, 9, budget) == 0
+
+
+def test_newer_calls_argument_errors_need_no_gpu(L):
+    """The fused gate/up calls, the repack, the host-buffer call and the per-slot MoE call
+    refuse bad arguments before anything is enqueued."""
+    P = ctypes.c_void_p
+    # qmm_mul_mat_glu(W_gate, W_up, t, n, k, xq, m, y, ws, ws_bytes, stream)
+    glu = lambda Wg=1024, Wu=2048, t=12, n=8, k=256, xq=4096, m=4, y=8192: L.qmm_mul_mat_glu(
+        P(Wg), P(Wu), t, n, k, P(xq), m, P(y), None, 0, None)
+    assert glu(t=13) == 3 and glu(k=100) == 2 and glu(k=0) == 1 and glu(n=-1) == 1
+    assert glu(Wu=0) == 1 and glu(xq=0) == 1 and glu(Wg=1030) == 4 and glu(y=8196) == 4
+    assert glu(n=0) == 0 and glu(m=0) == 0
+    packed = lambda W=1024, t=12, n=8, k=256, xq=4096, m=4, y=8192: L.qmm_mul_mat_glu_packed(
+        P(W), t, n, k, P(xq), m, P(y), None, 0, None)
+    assert packed(t=13) == 3 and packed(k=100) == 2 and packed(W=0) == 1 and packed(W=1032) == 4
+    assert packed(n=0) == 0 and packed(m=0) == 0
+    # qmm_repack_glu(W_gate, W_up, t, n, k, W_gu, stream)
+    rp = lambda Wg=1024, Wu=2048, t=12, n=8, k=256, out=4096: L.qmm_repack_glu(P(Wg), P(Wu), t, n, k, P(out), None)
+    assert rp(t=13) == 3 and rp(t=2, k=48) == 2 and rp(out=0) == 1 and rp(Wu=2056) == 4 and rp(n=0) == 0
+    # qmm_mul_mat_f32_host(W, t, n, k, x_host, m, y_host, ws, ws_bytes, stream)
+    host = lambda W=1024, t=12, n=8, k=256, x=4096, m=2, y=8192, ws=None, wsb=0: L.qmm_mul_mat_f32_host(
+        P(W), t, n, k, P(x), m, P(y), P(ws) if ws else None, wsb, None)
+    assert host(t=13) == 3 and host(k=100) == 2 and host(x=0) == 1 and host(y=0) == 1
+    assert host(W=1028) == 4 and host(n=0) == 0 and host(m=0) == 0
+    need = L.qmm_workspace_bytes_f32_host(12, 8, 256, 2)
+    assert need >= 2 * 256 and host(ws=1 << 20, wsb=need - 1) == 5 and host(ws=(1 << 20) + 16, wsb=need) == 4
+    # qmm_mul_mat_id_slot: the same checks as qmm_mul_mat_id
+    args = [P(1024), 12, 4, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
+    assert L.qmm_mul_mat_id_slot(*args, None, 0, None) == 5
+    bad_t = [P(1024), 13, 4, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
+    assert L.qmm_mul_mat_id_slot(*bad_t, None, 0, None) == 3
+
+
+def test_q4_0_sizes_and_shapes(L):
+    assert qmm.qmm_row_bytes("q4_0", 4096) == 128 * 18
+    assert qmm.qmm_q8_1_bytes(3, 4096) == 3 * 128 * 36
+    P = ctypes.c_void_p
+    # k must be a multiple of the 32-value block
+    assert L.qmm_mul_mat(P(1024), 2, 8, 48, P(2048), 4, P(4096), None, 0, None) == 2
