@@ -284,3 +284,24 @@ def test_moe_cold_with_invalid_ids(oracle_mod):
 @pytest.mark.parametrize("E,n,k,T_,K", [(64, 256, 512, 40, 8), (32, 130, 768, 20, 4), (128, 1536, 256, 64, 8)])
 def test_moe_mostly_cold_parity(oracle_mod, E, n, k, T_, K):
     moe_check(oracle_mod, E, n, k, T_, K, seed=E + T_)
+
+
+# Long rows: the GEMV stages x in shared memory ((k/64) * 96 bytes per column), so from
+# k = 155136 on a single column no longer fits and m <= 8 goes to the GEMM paths; the
+# largest k the ABI accepts is 2^20.
+@pytest.mark.parametrize("fmt,n,k,m", [("q4_K", 40, 154880, 1), ("q4_K", 40, 155136, 1), ("q4_K", 9, 1 << 20, 1),
+                                       ("q4_K", 9, 1 << 20, 3), ("q8_0", 17, 155136, 2), ("q6_K", 16, 1 << 19, 1),
+                                       ("q4_0", 24, 1 << 20, 2)])
+def test_long_rows_up_to_the_k_limit(oracle_mod, fmt, n, k, m):
+    W, x = qmm_synth.make_dense(fmt, n, k, m, seed=k % 1000 + m)
+    xq = oracle_mod.quantize_q8_1(x)
+    y_ref, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
+    assert_within(run_mul_mat(W, fmt, n, k, xq, m), y_ref, T, f"long rows {fmt} n={n} k={k} m={m}")
+
+
+def test_k_above_the_limit_is_refused():
+    W = torch.zeros(16 * ((1 << 20) + 256) // 256 * 144, dtype=torch.uint8, device=DEV)
+    xq = torch.zeros(((1 << 20) + 256) // 32 * 36, dtype=torch.uint8, device=DEV)
+    with pytest.raises(qmm.QMMError) as e:
+        qmm.qmm_mul_mat(W, "q4_K", 16, (1 << 20) + 256, xq, 1)
+    assert e.value.code == 2
