@@ -469,7 +469,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     }
                     const uint32_t rbar = ptx::smem_u32(&B.raw_full[ri]);
                     if constexpr (T == QMM_Q6_K) {
-                        const int64_t nval = a.n - n0 < 128 ? a.n - n0 : 128;  // rows of W in this tile
+                        // rows of W in this tile: its columns within the expert's (or the matrix's) n
+                        const int64_t cols = a.n - resolve_tile(a, sg.tile).col0;
+                        const int64_t nval = cols < 128 ? cols : 128;
                         if (lane == 0) ptx::mbar_arrive_expect_tx(rbar, (uint32_t)nval * F::kCopyBytes);
                         __syncwarp();
 #pragma unroll 1
@@ -1074,6 +1076,24 @@ TcLayout tc_layout(int64_t m, int64_t k, int64_t partial_ctas) {
 
 }  // namespace
 
+// Bytes of one weight row, and the raw map of `rows` weight rows: one box is the 256 k
+// values of 128 rows (Q8_0 read as uint16, so that a step's 272 bytes are a box of 136).
+// Q6_K has no map: its raw warp bulk-copies from W, which must start on a 16-byte boundary.
+int64_t tc_row_bytes(qmm_type t, int64_t k) { return (k / 256) * block_bytes(t) * (256 / block_elems(t)); }
+
+bool tc_weight_map(qmm_type t, const void *W, int64_t rows, int64_t k, CUtensorMap *tm_w) {
+    const int64_t row_bytes = tc_row_bytes(t, k);
+    if (t == QMM_Q8_0)
+        return make_map_2d(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, W, row_bytes / 2, rows, TcFmt<QMM_Q8_0>::kRawRow / 2,
+                           kTN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (t == QMM_Q6_K) {
+        memset(tm_w, 0, sizeof(*tm_w));
+        return (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
+    }
+    return make_map_2d(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, rows, kQ4KBytes, kTN,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 int64_t gemm_tc_tile_m(int64_t) { return kTM; }
 
 bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
@@ -1157,19 +1177,9 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     if (e != cudaSuccess) return e;
 
     CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
-    const int64_t row_bytes = (k / 256) * block_bytes(t) * (256 / block_elems(t));
-    bool wmap;
-    if (t == QMM_Q8_0)  // rows read as uint16 so that one superblock's 272 bytes are a box of 136
-        wmap = make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, W, row_bytes / 2, n, TcFmt<QMM_Q8_0>::kRawRow / 2,
-                           kTN, CU_TENSOR_MAP_SWIZZLE_NONE);
-    else if (t == QMM_Q6_K) {  // bulk copies from W itself: it must start on a 16-byte boundary
-        memset(&tm_w, 0, sizeof(tm_w));
-        wmap = (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
-    }
-    else
-        wmap = make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, n, kQ4KBytes, kTN,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) || !wmap) return cudaErrorInvalidValue;
+    const int64_t row_bytes = tc_row_bytes(t, k);
+    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) || !tc_weight_map(t, W, n, k, &tm_w))
+        return cudaErrorInvalidValue;
 
     TcArgs args{};
     args.W = static_cast<const uint8_t *>(W);
@@ -1260,14 +1270,16 @@ cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64
 // ---------------------------------------------------------------- expert-grouped mode
 
 bool gemm_tc_grouped_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k) {
-    return t == QMM_Q4_K && k % 256 == 0 && n > 0 && n_experts * n < (int64_t(1) << 31);
+    // the experts' rows are one W of n_experts * n rows, so the dense conditions apply per
+    // expert (Q6_K: n % 8 == 0 keeps every expert's rows, and the end of W, on 16 bytes)
+    return n_experts > 0 && n_experts * n < (int64_t(1) << 31) && gemm_tc_supported(t, n, k, 1);
 }
 
 size_t gemm_tc_grouped_bytes(int64_t n_pairs, int64_t k) {
     return tc_layout(n_pairs, k, device_sm_count() < kMaxPartialCtas ? device_sm_count() : kMaxPartialCtas).total;
 }
 
-cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                                    int64_t x_div, int64_t n_pairs, float *y, const MoETile *tiles,
                                    const int32_t *ntiles, int64_t max_token_tiles, const int32_t *bounds,
                                    const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st) {
@@ -1287,9 +1299,8 @@ cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     if (e != cudaSuccess) return e;
 
     CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
-    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, n_pairs, k) ||
-        !make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, (k / 256) * kQ4KBytes, n_experts * n, kQ4KBytes,
-                     kTN, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!gemm_tc_grouped_supported(t, n_experts, n, k) || !make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, n_pairs, k) ||
+        !tc_weight_map(t, W, n_experts * n, k, &tm_w))
         return cudaErrorInvalidValue;
 
     TcArgs args{};
@@ -1297,7 +1308,7 @@ cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     args.n = n;
     args.m = n_pairs;
     args.k = (int)k;
-    args.row_bytes = (k / 256) * kQ4KBytes;
+    args.row_bytes = tc_row_bytes(t, k);
     args.y = y;
     args.partial = reinterpret_cast<float *>(base + L.partial);
     args.status = status;
@@ -1310,7 +1321,13 @@ cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     args.ntiles = ntiles;
     args.bounds = bounds;
     args.perm = perm;
-    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, max_token_tiles * args.tiles_n, st);
+    const int64_t fixup = max_token_tiles * args.tiles_n;
+    switch (t) {
+    case QMM_Q8_0: return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
+    case QMM_Q4_0: return run_tc<QMM_Q4_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
+    case QMM_Q6_K: return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
+    default: return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
+    }
 }
 
 // ---------------------------------------------------------------- shared with the skinny path

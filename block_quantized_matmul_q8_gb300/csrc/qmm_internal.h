@@ -103,7 +103,7 @@ cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64
 struct MoETile;
 bool gemm_tc_grouped_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k);
 size_t gemm_tc_grouped_bytes(int64_t n_pairs, int64_t k);
-cudaError_t launch_gemm_tc_grouped(const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
+cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                                    int64_t x_div, int64_t n_pairs, float *y, const MoETile *tiles,
                                    const int32_t *ntiles, int64_t max_token_tiles, const int32_t *bounds,
                                    const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st);

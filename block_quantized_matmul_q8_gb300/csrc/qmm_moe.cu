@@ -251,7 +251,7 @@ cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int6
     if (e != cudaSuccess) return e;
     const int64_t x_div = x_per_slot ? 1 : top_k;
     const int64_t max_token_tiles = n_pairs / kTcTileTokens + n_experts + 1;
-    e = launch_gemm_tc_grouped(W, n_experts, n, k, xq, x_div, n_pairs, y, tiles, status + 1, max_token_tiles, bounds,
+    e = launch_gemm_tc_grouped(t, W, n_experts, n, k, xq, x_div, n_pairs, y, tiles, status + 1, max_token_tiles, bounds,
                                perm, status, base + L.gemm, L.cold_gemm - L.gemm, st);
     if (e != cudaSuccess || !split) return e;
     // the cold experts: 16-column slabs on the skinny tensor-core kernel

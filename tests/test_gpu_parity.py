@@ -305,3 +305,17 @@ def test_k_above_the_limit_is_refused():
     with pytest.raises(qmm.QMMError) as e:
         qmm.qmm_mul_mat(W, "q4_K", 16, (1 << 20) + 256, xq, 1)
     assert e.value.code == 2
+
+
+# The grouped tensor-core GEMM for every format it supports (Q6_K: n % 8 == 0), with
+# stream-K splitting tiles over CTAs; Q6_K with n % 8 != 0 stays on the CUDA-core path.
+@pytest.mark.parametrize("fmt,E,n,k,T_,K", [("q8_0", 16, 200, 768, 300, 4), ("q8_0", 8, 64, 256, 50, 3),
+                                            ("q4_0", 12, 130, 1024, 400, 3), ("q6_K", 8, 136, 512, 60, 4),
+                                            ("q6_K", 16, 256, 1024, 300, 2), ("q6_K", 8, 130, 512, 60, 4)])
+def test_moe_grouped_tc_other_formats(oracle_mod, fmt, E, n, k, T_, K):
+    moe_check(oracle_mod, E, n, k, T_, K, seed=E + n + k + T_, fmt=fmt)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0", "q6_K"])
+def test_moe_grouped_tc_other_formats_per_slot(oracle_mod, fmt):
+    moe_check(oracle_mod, 8, 136, 512, 90, 3, seed=11, fmt=fmt, per_slot=True)
