@@ -227,10 +227,10 @@ QMM_API qmm_status qmm_mul_mat_glu_packed(const void *W_gu, qmm_type t, int64_t 
  *     pair's expert id read on the device (for the shapes the GEMV streams: Q4_K
  *     always, Q8_0 and Q4_0 with k/32 % 8 == 0, Q6_K with 16-byte rows or even n);
  *   otherwise the pairs are bucketed by expert on the device (a stable counting sort)
- *     and the per-expert tiles are walked by one persistent launch: Q4_K with
- *     k % 256 == 0 on the tensor cores (128-pair tiles, stream-K over the device-built
- *     tile list; the workspace then also holds an fp16 copy of the gathered
- *     activations), the other formats on the CUDA-core grouped GEMM.  For Q4_K the
+ *     and the per-expert tiles are walked by one persistent launch: with k % 256 == 0
+ *     (and for Q6_K n % 8 == 0) on the tensor cores (128-pair tiles, stream-K over the
+ *     device-built tile list; the workspace then also holds an fp16 copy of the gathered
+ *     activations), other shapes on the CUDA-core grouped GEMM.  For Q4_K the
  *     experts with 1..16 pairs ([MMQ] section "MoE 的二次账": experts whose few columns
  *     leave the tiles mostly empty) skip the 128-pair tiles: a second launch runs them
  *     as 16-column slabs on the skinny tensor-core kernel, the expert list and its
