@@ -3,7 +3,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "qmm.h"
 #include "qmm_common.cuh"
@@ -25,6 +27,26 @@ int current_device() {
     return dev;
 }
 }  // namespace
+
+// The largest dynamic shared-memory size already granted to each kernel on each device:
+// the attribute is set once per (kernel, device, larger size), not on every call.
+cudaError_t ensure_max_dynamic_smem(const void *kern, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, size_t> granted;
+    const int dev = current_device();
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = granted.find({kern, dev});
+        if (it != granted.end() && it->second >= bytes) return cudaSuccess;
+    }
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(mu);
+        size_t &g = granted[{kern, dev}];
+        g = std::max(g, bytes);
+    }
+    return e;
+}
 
 int device_sm_count() {
     const int dev = current_device();

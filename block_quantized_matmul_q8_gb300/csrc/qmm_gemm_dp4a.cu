@@ -213,7 +213,7 @@ template <int T>
 static cudaError_t launch_dp4a_t(const DP4AGemmArgs &args, int64_t total_hint, cudaStream_t st) {
     const size_t smem = sizeof(DP4ASmem);
     auto kern = gemm_dp4a_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);

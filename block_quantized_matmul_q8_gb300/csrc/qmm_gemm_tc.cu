@@ -1121,7 +1121,7 @@ cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CU
                 : T == QMM_Q4_0 ? gemm_tc_q40_kernel
                                 : gemm_tc_q80_kernel;
     constexpr uint32_t smem = TcMap<T>::kSmemAlloc;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     // The setmaxnreg split hands out exactly kThreads x kLaunchRegs registers; a build that
     // launches with fewer registers per thread would leave setmaxnreg.inc waiting forever.

@@ -588,7 +588,7 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x
         kern = gemv_q4k_tma_kernel<NC>;
     else
         kern = gemv_tma_kernel<T, NC>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(W), n,
@@ -601,7 +601,7 @@ static cudaError_t launch_gemv_glu_nc(const void *Wg, const void *Wu, int64_t n,
     const int64_t row_bytes = gemv_tma_row_bytes<QMM_Q4_K>(n, k);
     const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, NC);
     auto kern = gemv_q4k_glu_kernel<NC>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), n));
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(Wg),
@@ -618,7 +618,7 @@ static cudaError_t launch_gemv_id_t(const void *W, int64_t n_experts, int64_t n,
     if (nstages <= 0) return cudaErrorNotSupported;
     const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, 1);
     auto kern = gemv_id_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     // enough CTAs per pair to cover the SMs once, at least 2 rows each
     const int64_t per_pair = std::max<int64_t>(
@@ -634,7 +634,7 @@ static cudaError_t launch_gemv_nc(const void *W, int64_t n, int64_t k, XIn x, fl
     const size_t smem = gemv_smem_bytes(k, NC);
     auto kern = gemv_kernel<T, NC>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = ensure_smem(kern, smem);
         if (e != cudaSuccess) return e;
     }
     int per_sm = 0;

@@ -776,7 +776,7 @@ cudaError_t launch_gemv_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     a.bounds = bounds;
     a.perm = perm;
 
-    e = cudaFuncSetAttribute(gemv_tc_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    e = ensure_smem(gemv_tc_q4k_kernel, kSmemAlloc);
     if (e != cudaSuccess) return e;
     e = launch_pdl(gemv_tc_q4k_kernel, dim3(a.ctas), dim3(kThreads), kSmemAlloc, st, tm_x, tm_xmin, tm_dx, tm_w, a);
     if (e != cudaSuccess) return e;
@@ -834,7 +834,7 @@ cudaError_t launch_gemv_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     a.partial = reinterpret_cast<float *>(base + L.partial);
     a.status = status;
 
-    e = cudaFuncSetAttribute(gemv_tc_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    e = ensure_smem(gemv_tc_q4k_kernel, kSmemAlloc);
     if (e != cudaSuccess) return e;
     e = launch_pdl(gemv_tc_q4k_kernel, dim3(ctas), dim3(kThreads), kSmemAlloc, st, tm_x, tm_xmin, tm_dx, tm_w, a);
     if (e != cudaSuccess) return e;

@@ -12,6 +12,12 @@ namespace qmm {
 
 // SM count of the current device (cached per device).
 int device_sm_count();
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for kern on the current device, skipped
+// when an equal or larger size was already granted
+cudaError_t ensure_max_dynamic_smem(const void *kern, size_t bytes);
+template <class K> inline cudaError_t ensure_smem(K *kern, size_t bytes) {
+    return ensure_max_dynamic_smem(reinterpret_cast<const void *>(kern), bytes);
+}
 
 // Launch kern<<<grid, block, smem, st>>>(args...) with programmatic stream
 // serialization, so that it may start while the previous kernel in the stream is

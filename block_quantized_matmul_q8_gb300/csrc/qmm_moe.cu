@@ -166,7 +166,7 @@ cudaError_t launch_moe_bucket(const int32_t *ids, int64_t n_pairs, int n_experts
                               void *ws, const MoELayout &L, cudaStream_t st) {
     uint8_t *base = static_cast<uint8_t *>(ws);
     const size_t smem = sizeof(int32_t) * size_t(n_experts) * (2 + 2 * kBucketWarps);
-    cudaError_t e = cudaFuncSetAttribute(moe_bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(moe_bucket_kernel, smem);
     if (e != cudaSuccess) return e;
     moe_bucket_kernel<<<1, kBucketThreads, smem, st>>>(
         ids, n_pairs, n_experts, tile_tokens, cold_max, reinterpret_cast<int32_t *>(base + L.status),
