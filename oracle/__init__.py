@@ -41,32 +41,38 @@ def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_LIB_PATH)
-        P = ctypes.c_void_p
-        I64 = ctypes.c_int64
-        L.oracle_half_to_double.restype = ctypes.c_double
-        L.oracle_half_to_double.argtypes = [ctypes.c_uint16]
-        L.oracle_float_to_half.restype = ctypes.c_uint16
-        L.oracle_float_to_half.argtypes = [ctypes.c_float]
-        L.oracle_quantize_q8_1.argtypes = [P, I64, I64, P]
-        L.oracle_dequant_q8_1.argtypes = [P, I64, I64, P]
-        L.oracle_block_bytes.argtypes = [ctypes.c_int]
-        L.oracle_block_elems.argtypes = [ctypes.c_int]
-        L.oracle_q4_K_fields.argtypes = [P, P, P, P, P, P]
-        L.oracle_q6_K_fields.argtypes = [P, P, P, P]
-        L.oracle_dequant.argtypes = [ctypes.c_int, P, I64, I64, P]
-        L.oracle_mul_mat.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P, P]
-        L.oracle_mul_mat_at.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P, P, I64, P, P]
-        L.oracle_brute.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P]
-        L.oracle_bucket.restype = I64
-        L.oracle_bucket.argtypes = [P, I64, I64, I64, P, P]
-        L.oracle_mul_mat_id.restype = I64
-        L.oracle_mul_mat_id.argtypes = [ctypes.c_int, P, I64, I64, I64, P, P, I64, I64, P, P]
-        L.oracle_mul_mat_id_slot.restype = I64
-        L.oracle_mul_mat_id_slot.argtypes = [ctypes.c_int, P, I64, I64, I64, P, P, I64, I64, P, P]
-        L.oracle_set_threads.argtypes = [ctypes.c_int]
-        _lib = L
+        _lib = load(_LIB_PATH)
     return _lib
+
+
+def load(path: str):
+    """A ctypes handle on an oracle library at `path` with every signature declared
+    (lib() uses it for the in-tree build; the mutation tests load planted copies)."""
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    L.oracle_half_to_double.restype = ctypes.c_double
+    L.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_float_to_half.restype = ctypes.c_uint16
+    L.oracle_float_to_half.argtypes = [ctypes.c_float]
+    L.oracle_quantize_q8_1.argtypes = [P, I64, I64, P]
+    L.oracle_dequant_q8_1.argtypes = [P, I64, I64, P]
+    L.oracle_block_bytes.argtypes = [ctypes.c_int]
+    L.oracle_block_elems.argtypes = [ctypes.c_int]
+    L.oracle_q4_K_fields.argtypes = [P, P, P, P, P, P]
+    L.oracle_q6_K_fields.argtypes = [P, P, P, P]
+    L.oracle_dequant.argtypes = [ctypes.c_int, P, I64, I64, P]
+    L.oracle_mul_mat.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P, P]
+    L.oracle_mul_mat_at.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P, P, I64, P, P]
+    L.oracle_brute.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P]
+    L.oracle_bucket.restype = I64
+    L.oracle_bucket.argtypes = [P, I64, I64, I64, P, P]
+    L.oracle_mul_mat_id.restype = I64
+    L.oracle_mul_mat_id.argtypes = [ctypes.c_int, P, I64, I64, I64, P, P, I64, I64, P, P]
+    L.oracle_mul_mat_id_slot.restype = I64
+    L.oracle_mul_mat_id_slot.argtypes = [ctypes.c_int, P, I64, I64, I64, P, P, I64, I64, P, P]
+    L.oracle_set_threads.argtypes = [ctypes.c_int]
+    return L
 
 
 def _p(a: np.ndarray):

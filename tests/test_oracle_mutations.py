@@ -1,0 +1,74 @@
+"""Planted mistakes: each plausible slip in the oracle's arithmetic, made in a temporary
+copy of its C source (on the CPU, never on the product path), must make at least one of
+the oracle's pins fail.  This is what makes the pins evidence: a pin set that a dropped
+term, a wrong sign, a wrong index or a swapped operand slips through would not be."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_formats as F
+import test_oracle_matmul as M
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "qmm_oracle.c")
+
+# (name, original text, planted text, pins that must catch it)
+MUTATIONS = [
+    ("Q4_0 nibble halves swapped",
+     "return (i < 16 ? (qs[i] & 0x0f) : (qs[i - 16] >> 4)) - 8;",
+     "return (i < 16 ? (qs[i] >> 4) : (qs[i - 16] & 0x0f)) - 8;",
+     [F.test_q4_0_nibble_positions_and_offset, F.test_q4_0_decode_all_codes]),
+    ("Q4_0 offset dropped",
+     "return (i < 16 ? (qs[i] & 0x0f) : (qs[i - 16] >> 4)) - 8;",
+     "return (i < 16 ? (qs[i] & 0x0f) : (qs[i - 16] >> 4));",
+     [F.test_q4_0_nibble_positions_and_offset, M.test_q4_0_integer_matmul_special_case]),
+    ("Q4_K min term added instead of subtracted",
+     "acc += t1 - t2;", "acc += t1 + t2;",
+     [M.test_q4_K_min_term_special_case]),
+    ("Q4_K scale of sub-blocks 0-3 read from the min bytes",
+     "*sc = s12[j] & 63;", "*sc = s12[j + 4] & 63;",
+     [F.test_q4_K_scale_packing_roundtrip, M.test_q4_K_integer_matmul_special_case]),
+    ("Q6_K high-bit pair taken from the wrong shift",
+     "int high = (qh[32 * h + l] >> (2 * t)) & 3;", "int high = (qh[32 * h + l] >> t) & 3;",
+     [F.test_q6_K_fields_roundtrip, F.test_q6_K_raw_bit_positions, M.test_q6_K_integer_matmul_special_case]),
+    ("Q8_0 weights read as unsigned",
+     "sumi += (int64_t)(int8_t)blk[2 + i] * (int8_t)xb[4 + i];",
+     "sumi += (int64_t)blk[2 + i] * (int8_t)xb[4 + i];",
+     [M.test_q8_0_integer_matmul_special_case]),
+    ("q8_1 s from the fp32 d instead of the stored fp16 d",
+     "uint16_t sh = oracle_float_to_half(dhf * (float)S);",
+     "uint16_t sh = oracle_float_to_half(d * (float)S);",
+     [lambda o: F.test_q8_1_invariants(o, "normal"), lambda o: F.test_q8_1_invariants(o, "adversarial")]),
+]
+
+
+def _catches(pin, mod):
+    try:
+        pin(mod)
+    except AssertionError:
+        return True
+    return False
+
+
+@pytest.mark.parametrize("name,orig,planted,pins", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, oracle_mod, name, orig, planted, pins):
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"the line to plant in is gone: {orig}"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(orig, planted))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC", "-std=c11",
+                    "-o", str(so), str(mutant_c), "-lm"], check=True)
+    real = oracle.lib()
+    # every pin passes on the real oracle ...
+    for pin in pins:
+        pin(oracle)
+    # ... and at least one fails on the planted copy
+    oracle._lib = oracle.load(str(so))
+    try:
+        caught = [_catches(pin, oracle) for pin in pins]
+    finally:
+        oracle._lib = real
+    assert any(caught), f"no pin catches: {name}"
