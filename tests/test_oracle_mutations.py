@@ -37,6 +37,18 @@ MUTATIONS = [
      "sumi += (int64_t)(int8_t)blk[2 + i] * (int8_t)xb[4 + i];",
      "sumi += (int64_t)blk[2 + i] * (int8_t)xb[4 + i];",
      [M.test_q8_0_integer_matmul_special_case]),
+    ("Q4_K low and high nibbles swapped",
+     "return t < 32 ? (qs[32 * c + t] & 0x0f) : (qs[32 * c + t - 32] >> 4);",
+     "return t < 32 ? (qs[32 * c + t] >> 4) : (qs[32 * c + t - 32] & 0x0f);",
+     [F.test_q4_K_nibble_positions, M.test_q4_K_integer_matmul_special_case]),
+    ("MoE bucketing not stable (pairs of an expert in reverse order)",
+     "            if (ids[i] == e) perm[pos++] = (int32_t)i;",
+     "            if (ids[n_tokens * top_k - 1 - i] == e) perm[pos++] = (int32_t)(n_tokens * top_k - 1 - i);",
+     [M.test_bucket_is_stable_sort]),
+    ("mul_mat_id per-slot x read from the token's row",
+     "int64_t xrow = x_per_slot ? i : i / top_k;",
+     "int64_t xrow = i / top_k;",
+     [M.test_mul_mat_id_per_slot_reduces_to_dense]),
     ("q8_1 s from the fp32 d instead of the stored fp16 d",
      "uint16_t sh = oracle_float_to_half(dhf * (float)S);",
      "uint16_t sh = oracle_float_to_half(d * (float)S);",
