@@ -394,6 +394,7 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
     out.update(dense("q4_K", 17408, 5120, [2, 4, 5, 8]))
     out.update(dense("q4_K", 1024, 2048, [16]))
     out.update(dense("q4_K", 17408, 5120, [16]))
+    out.update(dense("q4_K", 4096, 14336, [1]))  # the prefill shape's down projection: long rows
     out.update(dense("q4_K", 14336, 4096, [512, 2048]))
     out.update(dense("q4_K", 4100, 4096, [512]))
     out.update(dense("q6_K", 151936, 5120, [1, 512]))

@@ -236,6 +236,7 @@ constexpr int kTmaGroupWarps = 4;
 constexpr int kTmaConsumerWarps = kTmaGroups * kTmaGroupWarps;
 constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
 constexpr int kTmaChunkRows = 2 * kTmaGroupWarps;  // one row per half-warp
+constexpr int64_t kTwoRowMinK = 8192;              // the long-row form of the Q4_K body from here
 static_assert(kTmaMaxStages == 8 && kTmaGroups == 4, "ring depths and group splits below assume 8 stages, 4 groups");
 
 // Consumer groups that take a ring of nstages stages (0: no valid split).  Chunk c goes
@@ -299,6 +300,61 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
     asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
+// One 64-value unit of two Q4_K rows against the staged activations, each unit's
+// activation loads shared by both rows (the long-row form of the bulk-copy GEMV below).
+// `two` false: the second row is past the end of the matrix and is not read.
+template <int NC>
+__device__ __forceinline__ void fold_q4k_unit2(const uint8_t *row0, const uint8_t *row1, bool two, int u, int c4,
+                                               const Q4KPairSel &psel, const uint8_t *xs, const float2 *xds, int U,
+                                               float (&acc0)[NC], float (&acc1)[NC]) {
+    const uint8_t *b0 = row0 + (u >> 2) * kQ4KBytes;
+    const uint8_t *b1 = row1 + (u >> 2) * kQ4KBytes;
+    const uint4 hd0 = *reinterpret_cast<const uint4 *>(b0);
+    const uint4 qa0 = *reinterpret_cast<const uint4 *>(b0 + 16 + 32 * c4);
+    const uint4 qb0 = *reinterpret_cast<const uint4 *>(b0 + 32 + 32 * c4);
+    uint4 hd1 = make_uint4(0u, 0u, 0u, 0u), qa1 = hd1, qb1 = hd1;
+    if (two) {
+        hd1 = *reinterpret_cast<const uint4 *>(b1);
+        qa1 = *reinterpret_cast<const uint4 *>(b1 + 16 + 32 * c4);
+        qb1 = *reinterpret_cast<const uint4 *>(b1 + 32 + 32 * c4);
+    }
+    const uint32_t w0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
+    const uint32_t w1[8] = {qa1.x, qa1.y, qa1.z, qa1.w, qb1.x, qb1.y, qb1.z, qb1.w};
+    int sc0a, sc1a, m0a, m1a, sc0b, sc1b, m0b, m1b;
+    q4k_pair_scales(hd0.y, hd0.z, hd0.w, psel, sc0a, sc1a, m0a, m1a);
+    q4k_pair_scales(hd1.y, hd1.z, hd1.w, psel, sc0b, sc1b, m0b, m1b);
+    const float da = half_lo(hd0.x), dmina = half_hi(hd0.x);
+    const float db = half_lo(hd1.x), dminb = half_hi(hd1.x);
+#pragma unroll
+    for (int cc = 0; cc < NC; ++cc) {
+        const int4 *xv = reinterpret_cast<const int4 *>(xs + (size_t(cc) * U + u) * kUnitStride);
+        const float4 ds = reinterpret_cast<const float4 *>(xds + size_t(cc) * 2 * U)[u];
+        const int4 x0 = xv[0], x1 = xv[1], x2 = xv[2], x3 = xv[3];
+        const int xl[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const int xh[8] = {x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+        int sloa = 0, shia = 0, slob = 0, shib = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            sloa = __dp4a((int)(w0[i] & 0x0f0f0f0fu), xl[i], sloa);
+            slob = __dp4a((int)(w1[i] & 0x0f0f0f0fu), xl[i], slob);
+            shia = dp4a_us(w0[i] & 0xf0f0f0f0u, xh[i], shia);  // high nibbles in place: 16 q
+            shib = dp4a_us(w1[i] & 0xf0f0f0f0u, xh[i], shib);
+        }
+        shia >>= 4;
+        shib >>= 4;
+        float t = ds.x * (float)(sc0a * sloa);
+        t = fmaf(ds.z, (float)(sc1a * shia), t);
+        float mm = ds.y * (float)m0a;
+        mm = fmaf(ds.w, (float)m1a, mm);
+        acc0[cc] = fmaf(da, t, fmaf(-dmina, mm, acc0[cc]));
+        t = ds.x * (float)(sc0b * slob);
+        t = fmaf(ds.z, (float)(sc1b * shib), t);
+        mm = ds.y * (float)m0b;
+        mm = fmaf(ds.w, (float)m1b, mm);
+        acc1[cc] = fmaf(db, t, fmaf(-dminb, mm, acc1[cc]));
+    }
+}
+
 // The body of the bulk-copy GEMV for format T.  Q6_K rows (210-byte blocks) keep their
 // chunks 16-byte aligned only from an even row on, so for Q6_K the CTAs' row ranges
 // start on even rows (the host takes this kernel for Q6_K only when n is even or the
@@ -311,7 +367,10 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
 // staged rows (gate j, up j, ...): one bulk copy per row, or one for the chunk when the
 // rows are interleaved; the two half-warps of a warp fold one pair and lane 0 writes
 // silu(gate) * up.
-template <int T, int NC, bool GLU = false>
+// kTwoRows (Q4_K, not GLU): each warp folds its two rows of a chunk together, lanes
+// taking units lane + 32 j, so every unit's staged activations are read once for both
+// rows; chosen by the host for long rows, where a CTA folds few chunks.
+template <int T, int NC, bool GLU = false, bool kTwoRows = false>
 __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int64_t n, int k, int64_t row_bytes,
                                               int nstages, const XIn &x, float *__restrict__ y, int64_t y_ld,
                                               int *status, const uint8_t *__restrict__ W2 = nullptr) {
@@ -413,6 +472,41 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
             float acc[NC];
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) acc[cc] = 0.f;
+            if constexpr (T == QMM_Q4_K && !GLU && kTwoRows) {
+                const int r0w = 2 * gw;  // this warp's rows r0w, r0w + 1 of the chunk
+                float acc1[NC];
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) acc1[cc] = 0.f;
+                if (a + r0w < r1) {
+                    const uint8_t *row0 = stages + s * stage_bytes + size_t(r0w) * row_bytes;
+                    const int c4l = lane & 3;  // units lane + 32 j all take qs chunk lane % 4
+                    const Q4KPairSel pl = q4k_pair_sel(c4l);
+                    for (int u = lane; u < U; u += 32)
+                        fold_q4k_unit2<NC>(row0, row0 + row_bytes, a + r0w + 1 < r1, u, c4l, pl, xs, xds, U, acc,
+                                           acc1);
+                }
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) {
+                    float v0 = acc[cc], v1 = acc1[cc];
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) {
+                        v0 += __shfl_xor_sync(0xffffffffu, v0, o);
+                        v1 += __shfl_xor_sync(0xffffffffu, v1, o);
+                    }
+                    acc[cc] = v0;
+                    acc1[cc] = v1;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(ptx::smem_u32(&empty[s]));  // the stage is read: free it first
+#pragma unroll
+                    for (int cc = 0; cc < NC; ++cc) {
+                        if (a + r0w < r1) y[cc * y_ld + a + r0w] = acc[cc];
+                        if (a + r0w + 1 < r1) y[cc * y_ld + a + r0w + 1] = acc1[cc];
+                    }
+                }
+                continue;
+            }
             if (T == QMM_Q4_K && valid) {
                 const uint8_t *row = stages + s * stage_bytes + size_t(rr) * row_bytes;
                 for (int u = l16; u < U; u += 16) {
@@ -505,6 +599,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
     gemv_tma_body<QMM_Q4_K, NC>(W, n, k, row_bytes, nstages, x, y, y_ld, status);
 }
 
+// Long rows (k >= 8192) at one or two columns: the two-row fold
+template <int NC>
+__global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_long_kernel(const uint8_t *__restrict__ W, int64_t n,
+                                                                           int k, int64_t row_bytes, int nstages,
+                                                                           const XIn x, float *__restrict__ y,
+                                                                           int64_t y_ld, int *status) {
+    gemv_tma_body<QMM_Q4_K, NC, false, true>(W, n, k, row_bytes, nstages, x, y, y_ld, status);
+}
+
 template <int NC>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     gemv_q4k_glu_kernel(const uint8_t *__restrict__ Wg, const uint8_t *__restrict__ Wu, int64_t n, int k,
@@ -584,10 +687,16 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x
     const int64_t row_bytes = gemv_tma_row_bytes<T>(n, k);
     const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, NC);
     void (*kern)(const uint8_t *, int64_t, int, int64_t, int, const XIn, float *, int64_t, int *);
-    if constexpr (T == QMM_Q4_K)
-        kern = gemv_q4k_tma_kernel<NC>;
-    else
+    if constexpr (T == QMM_Q4_K) {
+        // from k = 8192 on, sharing each unit's activation loads between a warp's two rows
+        // pays (4096 x 14336 at one column: 13.7 -> 12.9 us); below it costs a little
+        if constexpr (NC <= 2)
+            kern = k >= kTwoRowMinK ? gemv_q4k_tma_long_kernel<NC> : gemv_q4k_tma_kernel<NC>;
+        else
+            kern = gemv_q4k_tma_kernel<NC>;
+    } else {
         kern = gemv_tma_kernel<T, NC>;
+    }
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));

@@ -82,8 +82,9 @@ def test_quantize_near_ties_bitexact(oracle_mod):
 # copies; the other shapes take the direct-load kernel.
 # Long rows get shallower rings: at one column Q4_K k = 11776 takes 4 stages, k = 14336
 # and Q8_0 k = 8192 take 3 (three consumer groups), Q4_K k = 16384 none (the direct
-# kernel); Q6_K k = 5120 takes 6 stages (three groups).
-GEMV_SHAPES = {"q4_K": [(1, 256), (7, 512), (129, 2304), (64, 11776), (33, 14336), (20, 16384)],
+# kernel); Q6_K k = 5120 takes 6 stages (three groups).  Q4_K rows from k = 8192 on at
+# one or two columns take the two-row fold (a warp's two rows share each unit's x loads).
+GEMV_SHAPES = {"q4_K": [(1, 256), (7, 512), (129, 2304), (45, 8192), (64, 11776), (33, 14336), (20, 16384)],
                "q6_K": [(1, 256), (7, 512), (129, 2304), (130, 2304), (64, 512), (2, 5120)],
                "q8_0": [(1, 32), (7, 96), (129, 1056), (33, 2048), (130, 256), (64, 5120), (40, 8192)],
                # odd block counts (k = 96, 1056: rows only 2-byte aligned, a last unit of one
