@@ -291,3 +291,28 @@ def test_mul_mat_glu_at_matches_full(oracle_mod):
     cols = np.array([2, 0, 1, 2])
     ya, ta = oracle_mod.mul_mat_glu_at(Wg, Wu, "q4_K", n, k, xq, m, rows, cols)
     assert np.array_equal(ya, y[cols, rows]) and np.array_equal(ta, tol[cols, rows])
+
+
+def test_mul_mat_glu_gate_and_up_roles(oracle_mod):
+    """Gate rows equal to the up rows with d and dmin doubled (exact in fp16) make every
+    gate dot exactly twice the up dot, so y = silu(2u) * u: a reference that swapped the
+    two roles (silu(u) * 2u) or ignored the up dot (silu(2u) * 2u) fails; an all-zero up
+    row gives exactly 0 whatever the gate."""
+    rng = np.random.default_rng(62)
+    n, k, m = 5, 512, 3
+    Wu = qmm_synth.gen_q4_K(rng, n, k)
+    blk = Wu.reshape(n, k // 256, 144)
+    blk[:, :, 0:4] = np.minimum(blk[:, :, 0:4], 0x20)  # keep d, dmin small: doubling stays exact
+    Wg = Wu.copy()
+    hv = Wg.reshape(n, k // 256, 144)[:, :, 0:4].copy().view(np.float16)
+    Wg.reshape(n, k // 256, 144)[:, :, 0:4] = (hv * np.float16(2)).view(np.uint8)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, m, k))
+    u, _ = oracle_mod.mul_mat(Wu, "q4_K", n, k, xq, m)
+    g, _ = oracle_mod.mul_mat(Wg, "q4_K", n, k, xq, m)
+    np.testing.assert_allclose(g, 2 * u, rtol=1e-15, atol=0)
+    y, _ = oracle_mod.mul_mat_glu(Wg, Wu, "q4_K", n, k, xq, m)
+    np.testing.assert_allclose(y, 2 * u / (1.0 + np.exp(-2 * u)) * u, rtol=1e-14, atol=0)
+    Wz = Wu.copy()
+    Wz.reshape(n, k // 256, 144)[3, :, 0:4] = 0  # up row 3: d = dmin = 0
+    y3, _ = oracle_mod.mul_mat_glu(Wg, Wz, "q4_K", n, k, xq, m)
+    assert np.all(y3[:, 3] == 0)

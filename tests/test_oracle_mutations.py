@@ -6,6 +6,8 @@ import ctypes
 import os
 import subprocess
 
+import numpy as np
+
 import pytest
 
 import oracle
@@ -83,4 +85,46 @@ def test_planted_mistake_is_caught(tmp_path, oracle_mod, name, orig, planted, pi
         caught = [_catches(pin, oracle) for pin in pins]
     finally:
         oracle._lib = real
+    assert any(caught), f"no pin catches: {name}"
+
+
+# The SwiGLU reference is numpy code: its planted mistakes replace a function of the
+# oracle module for the duration of the check.
+def _glu_mutant(combine):
+    real = oracle._glu
+
+    def glu(g, Tg, u, Tu):
+        _, tol = real(g, Tg, u, Tu)
+        return combine(g, u), tol
+    return glu
+
+
+def _silu(v):
+    v = np.asarray(v, dtype=np.float64)
+    return v / (1.0 + np.exp(-v))
+
+
+PY_MUTATIONS = [
+    ("silu with the sigmoid's sign flipped", "silu",
+     lambda v: np.asarray(v, dtype=np.float64) / (1.0 + np.exp(np.asarray(v, dtype=np.float64))),
+     [M.test_silu_closed_forms]),
+    ("SwiGLU ignoring the up dot", "_glu", _glu_mutant(lambda g, u: _silu(g) * g),
+     [M.test_mul_mat_glu_pins, M.test_mul_mat_glu_gate_and_up_roles]),
+    ("SwiGLU with gate and up swapped", "_glu", _glu_mutant(lambda g, u: _silu(u) * g),
+     [M.test_mul_mat_glu_pins, M.test_mul_mat_glu_gate_and_up_roles]),
+    ("SwiGLU without the silu", "_glu", _glu_mutant(lambda g, u: g * u),
+     [M.test_mul_mat_glu_pins, M.test_mul_mat_glu_gate_and_up_roles]),
+]
+
+
+@pytest.mark.parametrize("name,attr,mutant,pins", PY_MUTATIONS, ids=[m[0] for m in PY_MUTATIONS])
+def test_planted_python_mistake_is_caught(oracle_mod, name, attr, mutant, pins):
+    for pin in pins:
+        pin(oracle)
+    real = getattr(oracle, attr)
+    setattr(oracle, attr, mutant)
+    try:
+        caught = [_catches(pin, oracle) for pin in pins]
+    finally:
+        setattr(oracle, attr, real)
     assert any(caught), f"no pin catches: {name}"
