@@ -51,6 +51,18 @@ MUTATIONS = [
      "int64_t xrow = x_per_slot ? i : i / top_k;",
      "int64_t xrow = i / top_k;",
      [M.test_mul_mat_id_per_slot_reduces_to_dense]),
+    ("Q4_K d and dmin swapped in the fold",
+     "\n            double d = h2d(blk), dmin = h2d(blk + 2);",
+     "\n            double dmin = h2d(blk), d = h2d(blk + 2);",
+     [M.test_q4_K_integer_matmul_special_case, M.test_q4_K_min_term_special_case]),
+    ("Q6_K sub-scale of the 32-block instead of the 16-block",
+     "double t = d * (int8_t)blk[192 + j] * d8 * (double)sumi;",
+     "double t = d * (int8_t)blk[192 + j / 2] * d8 * (double)sumi;",
+     [M.test_q6_K_integer_matmul_special_case]),
+    ("mul_mat_id shared x read from the wrong row",
+     "int64_t xrow = x_per_slot ? i : i / top_k;",
+     "int64_t xrow = x_per_slot ? i : i % top_k;",
+     [M.test_mul_mat_id_reduces_to_dense]),
     ("q8_1 s from the fp32 d instead of the stored fp16 d",
      "uint16_t sh = oracle_float_to_half(dhf * (float)S);",
      "uint16_t sh = oracle_float_to_half(d * (float)S);",
