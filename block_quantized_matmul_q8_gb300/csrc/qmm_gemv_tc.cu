@@ -634,44 +634,46 @@ __global__ void gemv_tc_prep_grouped_kernel(const uint8_t *__restrict__ xq, int6
 // per weight row, 16 columns.
 __global__ void __launch_bounds__(kRows) gemv_tc_fixup_kernel(const SkArgs a_in) {
     SkArgs a = a_in;
-    if (a.cold) {  // grouped: one block per tile of any expert; only those of the cold ones exist
-        a.nwork = int64_t(*a.ncold) * a.ntiles * a.nsb;
-        if (int64_t(blockIdx.x) * a.nsb >= a.nwork) return;
+    int64_t ntiles = gridDim.x;  // dense: one block per tile
+    if (a.cold) {                // grouped: the cold experts' tiles, counted on the device
+        ntiles = int64_t(*a.ncold) * a.ntiles;
+        a.nwork = ntiles * a.nsb;
     }
-    const int64_t t = blockIdx.x;
-    const int64_t u0 = t * a.nsb, u1 = u0 + a.nsb - 1;
     auto owner = [&](int64_t uu) {
         int64_t c = uu * a.ctas / a.nwork;
         while (c + 1 < a.ctas && a.nwork * (c + 1) / a.ctas <= uu) ++c;
         while (c > 0 && a.nwork * c / a.ctas > uu) --c;
         return c;
     };
-    const int64_t c0 = owner(u0), c1 = owner(u1);
-    if (c0 == c1) return;  // the tile was written whole by one CTA
     const int tl = threadIdx.x;
-    float s[kNT];
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int64_t u0 = t * a.nsb, u1 = u0 + a.nsb - 1;
+        const int64_t c0 = owner(u0), c1 = owner(u1);
+        if (c0 == c1) continue;  // the tile was written whole by one CTA
+        float s[kNT];
 #pragma unroll
-    for (int i = 0; i < kNT; ++i) s[i] = 0.f;
-    for (int64_t c = c0; c <= c1; ++c) {
-        const int64_t cb = a.nwork * c / a.ctas;
-        if (a.nwork * (c + 1) / a.ctas == cb) continue;  // c owns no units
-        const int slotidx = (cb / a.nsb == t) ? 0 : 1;   // tile t is this CTA's first segment?
-        const float4 *p = reinterpret_cast<const float4 *>(a.partial + ((c * 2 + slotidx) * kRows + tl) * kNT);
+        for (int i = 0; i < kNT; ++i) s[i] = 0.f;
+        for (int64_t c = c0; c <= c1; ++c) {
+            const int64_t cb = a.nwork * c / a.ctas;
+            if (a.nwork * (c + 1) / a.ctas == cb) continue;  // c owns no units
+            const int slotidx = (cb / a.nsb == t) ? 0 : 1;   // tile t is this CTA's first segment?
+            const float4 *p = reinterpret_cast<const float4 *>(a.partial + ((c * 2 + slotidx) * kRows + tl) * kNT);
 #pragma unroll
-        for (int i4 = 0; i4 < kNT / 4; ++i4) {
-            const float4 v = p[i4];
-            s[4 * i4] += v.x;
-            s[4 * i4 + 1] += v.y;
-            s[4 * i4 + 2] += v.z;
-            s[4 * i4 + 3] += v.w;
+            for (int i4 = 0; i4 < kNT / 4; ++i4) {
+                const float4 v = p[i4];
+                s[4 * i4] += v.x;
+                s[4 * i4 + 1] += v.y;
+                s[4 * i4 + 2] += v.z;
+                s[4 * i4 + 3] += v.w;
+            }
         }
-    }
-    const SkTile tt = sk_tile(a, t);
-    const int64_t row = tt.row0 + tl;
-    if (row >= a.n) return;
+        const SkTile tt = sk_tile(a, t);
+        const int64_t row = tt.row0 + tl;
+        if (row >= a.n) continue;
 #pragma unroll
-    for (int i = 0; i < kNT; ++i)
-        if (i < tt.cols) a.y[sk_out_row(a, tt, i) * a.n + row] = s[i];
+        for (int i = 0; i < kNT; ++i)
+            if (i < tt.cols) a.y[sk_out_row(a, tt, i) * a.n + row] = s[i];
+    }
 }
 
 struct SkLayout {
@@ -780,7 +782,9 @@ cudaError_t launch_gemv_tc_grouped(const void *W, int64_t n_experts, int64_t n, 
     if (e != cudaSuccess) return e;
     e = launch_pdl(gemv_tc_q4k_kernel, dim3(a.ctas), dim3(kThreads), kSmemAlloc, st, tm_x, tm_xmin, tm_dx, tm_w, a);
     if (e != cudaSuccess) return e;
-    gemv_tc_fixup_kernel<<<(unsigned)(n_experts * a.ntiles), kRows, 0, st>>>(a);
+    // at most every expert's tiles are cold: a bounded grid strides over those that are
+    const int64_t fx = std::min<int64_t>(n_experts * a.ntiles, int64_t(device_sm_count()) * 4);
+    gemv_tc_fixup_kernel<<<(unsigned)fx, kRows, 0, st>>>(a);
     return cudaGetLastError();
 }
 
