@@ -82,7 +82,7 @@ def gemv_q8_bytes(n, k, m, row_bytes):
 
 def int8_tensor_peak():
     """The GPU's dense int8 tensor-core rate in TOPS: on sm_103a tcgen05 has no int8 kind,
-    so it is the mma.sync s8 rate, measured by peaks/mma_sync_peak.cu and recorded in
+    so it is the mma.sync s8 rate, measured once by a stand-alone probe and recorded in
     profiles/mma_sync_peak.json (None when the record is missing)."""
     p = os.path.join(ROOT, "profiles", "mma_sync_peak.json")
     if not os.path.exists(p):

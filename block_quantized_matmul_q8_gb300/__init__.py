@@ -30,7 +30,8 @@ EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspac
            "qmm_plan_gemm", "qmm_plan_cta_range", "qmm_set_force_path", "qmm_set_stream_k_mode",
            "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32",
            "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu", "qmm_gemv_ring_stages",
-           "qmm_repack_glu", "qmm_mul_mat_glu_packed", "qmm_workspace_bytes_f32_host", "qmm_mul_mat_f32_host")
+           "qmm_repack_glu", "qmm_mul_mat_glu_packed", "qmm_workspace_bytes_f32_host", "qmm_mul_mat_f32_host",
+           "qmm_get_device_status")
 
 
 class QMMError(RuntimeError):
@@ -77,6 +78,8 @@ def lib():
     L.qmm_mul_mat_id.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P, SZ, P]
     L.qmm_read_device_status.restype = ctypes.c_int
     L.qmm_read_device_status.argtypes = [P, ctypes.POINTER(I32), P]
+    L.qmm_get_device_status.restype = ctypes.c_int
+    L.qmm_get_device_status.argtypes = [P, P]
     L.qmm_tile_efficiency_percent.restype = ctypes.c_int
     L.qmm_tile_efficiency_percent.argtypes = [I64, I64]
     L.qmm_gemv_ring_stages.restype = ctypes.c_int
@@ -341,6 +344,11 @@ def qmm_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     v = ctypes.c_int32(-1)
     _check(lib().qmm_read_device_status(_ptr(workspace), ctypes.byref(v), _stream(stream)), "qmm_read_device_status")
     return v.value
+
+
+def qmm_get_device_status(workspace: torch.Tensor, stream=None) -> int:
+    """The status word of the last mul_mat_id on this workspace (synchronises the stream)."""
+    return int(lib().qmm_get_device_status(_ptr(workspace), _stream(stream)))
 
 
 def qmm_tile_efficiency_percent(ntiles: int, nsm: int) -> int:

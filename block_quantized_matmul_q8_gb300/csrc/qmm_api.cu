@@ -455,6 +455,12 @@ qmm_status qmm_read_device_status(const void *workspace, int32_t *status, void *
     return QMM_OK;
 }
 
+qmm_status qmm_get_device_status(const void *workspace, void *stream) {
+    int32_t v = 0;
+    const qmm_status s = qmm_read_device_status(workspace, &v, stream);
+    return s != QMM_OK ? s : static_cast<qmm_status>(v);
+}
+
 int qmm_tile_efficiency_percent(int64_t ntiles, int64_t nsm) {
     if (ntiles <= 0 || nsm <= 0) return 0;
     const int64_t nwaves = (ntiles + nsm - 1) / nsm;

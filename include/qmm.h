@@ -116,7 +116,8 @@ QMM_API qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void 
  *   Q6_K/Q8_0, m > 8:   the tiled tensor-core GEMM (Q8_0: k % 256 == 0; Q6_K: n % 8
  *                       == 0), otherwise the CUDA-core tiled GEMM;
  *   Q4_0, m <= 8:       the bulk-copy GEMV (k % 256 == 0, else the direct-load GEMV);
- *   Q4_0, m > 8:        the CUDA-core tiled GEMM;
+ *   Q4_0, m > 8:        the tiled tensor-core GEMM when k % 256 == 0, otherwise the
+ *                       CUDA-core tiled GEMM;
  * the tensor-core paths split their work with a stream-K schedule.
  * Accuracy: |y - y_exact| <= 1e-5 * sum over blocks of |block term| per element.
  */
@@ -283,6 +284,14 @@ QMM_API size_t qmm_noalloc_scratch_bytes(void);
  * *status (QMM_OK, QMM_ERR_IDS or QMM_ERR_DEVICE).  This call synchronises
  * `stream`.  Returns QMM_ERR_CUDA if the copy fails. */
 QMM_API qmm_status qmm_read_device_status(const void *workspace, int32_t *status, void *stream);
+
+/* The same status word as the return value: QMM_OK, QMM_ERR_IDS (a routing id was
+ * outside [0, n_experts)) or QMM_ERR_DEVICE (a kernel gave up on a bounded wait), as
+ * written by the last qmm_mul_mat_id / qmm_mul_mat_id_slot enqueued on this workspace
+ * and `stream`.  Synchronises `stream` (a host read of a device flag has to wait for
+ * the writer).  QMM_ERR_ARG for a NULL workspace, QMM_ERR_CUDA if the read fails, so a
+ * caller that must tell a failed read from a device error uses qmm_read_device_status. */
+QMM_API qmm_status qmm_get_device_status(const void *workspace, void *stream);
 
 /* ------------------------------------------------------------------ host-side planning
  * These functions run on the host only and never touch a GPU. */

@@ -94,6 +94,89 @@ def test_q4_0_integer_matmul_special_case(oracle_mod):
     assert np.array_equal(T, blk.sum(axis=2).astype(np.float64))
 
 
+# ---------------------------------------------------------------- the tolerance sum T
+# T is the sum of |block term| over an output's blocks, the scale of the parity bound
+# 1e-5 * T.  With power-of-two d, dmin and d8, int codes and fp16 s, every term is exact
+# in fp64, so T has a closed form in the integer fields: numpy's einsum of the codes
+# gives the per-sub-block dots, and the sums may differ from the oracle's only by the
+# order of fp64 additions.
+
+
+def _pow2(rng, lo, hi, shape):
+    return 2.0 ** rng.integers(lo, hi, shape)
+
+
+def test_q4_K_tolerance_sum_closed_form(oracle_mod):
+    """Q4_K: T = sum_b |d sc_b d8_b sumi_b| + |dmin m_b s_b|, the scale and min terms of
+    each 32-wide sub-block counted separately, with non-unit d, dmin, d8 and s."""
+    rng = np.random.default_rng(27)
+    n, k, m = 4, 512, 3
+    nsb = k // 256
+    D, DM = _pow2(rng, -6, 1, (n, nsb)), _pow2(rng, -6, 1, (n, nsb))
+    SC, MN = rng.integers(0, 64, (n, k // 32)), rng.integers(0, 64, (n, k // 32))
+    Qw = rng.integers(0, 16, (n, k))
+    W = np.stack([np.concatenate([pack_q4_K(D[r, s], DM[r, s], SC[r, 8 * s:8 * s + 8], MN[r, 8 * s:8 * s + 8],
+                                            Qw[r, 256 * s:256 * s + 256]) for s in range(nsb)]) for r in range(n)])
+    Qx = rng.integers(-127, 128, (m, k))
+    D8 = _pow2(rng, -8, -1, (m, k // 32))
+    S8 = rng.uniform(-4, 4, (m, k // 32)).astype(np.float16).astype(np.float64)
+    xq = _q8_1_rows(Qx, D8, S8)
+    y, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    sumi = np.einsum("mbi,nbi->mnb", Qx.reshape(m, -1, 32), Qw.reshape(n, -1, 32))
+    t1 = np.repeat(D, 8, axis=1)[None] * SC[None] * D8[:, None, :] * sumi
+    t2 = np.repeat(DM, 8, axis=1)[None] * MN[None] * S8[:, None, :]
+    np.testing.assert_allclose(T, (np.abs(t1) + np.abs(t2)).sum(axis=2), rtol=1e-15, atol=0)
+    assert np.all(np.abs(y - (t1 - t2).sum(axis=2)) <= 1e-14 * T)
+
+
+def test_q6_K_tolerance_sum_closed_form(oracle_mod):
+    """Q6_K: T = sum_j |d sc_j d8_(j/2) sumi_j| over 16-wide sub-blocks j, the q8_1 d
+    of the 32-block that holds sub-block j."""
+    rng = np.random.default_rng(28)
+    n, k, m = 4, 512, 3
+    nsb = k // 256
+    D = _pow2(rng, -6, 1, (n, nsb))
+    SC = rng.integers(-128, 128, (n, k // 16))
+    V = rng.integers(-32, 32, (n, k))
+    W = np.stack([np.concatenate([pack_q6_K(D[r, s], SC[r, 16 * s:16 * s + 16], V[r, 256 * s:256 * s + 256])
+                                  for s in range(nsb)]) for r in range(n)])
+    Qx = rng.integers(-127, 128, (m, k))
+    D8 = _pow2(rng, -8, -1, (m, k // 32))
+    xq = _q8_1_rows(Qx, D8, rng.uniform(-3, 3, (m, k // 32)))
+    y, T = oracle_mod.mul_mat(W, "q6_K", n, k, xq, m)
+    sumi = np.einsum("mji,nji->mnj", Qx.reshape(m, -1, 16), V.reshape(n, -1, 16))
+    t = np.repeat(D, 16, axis=1)[None] * SC[None] * np.repeat(D8, 2, axis=1)[:, None, :] * sumi
+    np.testing.assert_allclose(T, np.abs(t).sum(axis=2), rtol=1e-15, atol=0)
+    assert np.all(np.abs(y - t.sum(axis=2)) <= 1e-14 * T)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+def test_32_block_tolerance_sum_closed_form(oracle_mod, fmt):
+    """Q8_0 and Q4_0: T = sum_b |d_b d8_b sumi_b| over 32-blocks, with non-unit d and d8
+    (Q4_0's integers are the offset codes q - 8)."""
+    rng = np.random.default_rng(29)
+    n, k, m = 5, 320, 3
+    D = _pow2(rng, -6, 1, (n, k // 32))
+    if fmt == "q8_0":
+        Qw = rng.integers(-128, 128, (n, k))
+        V = Qw
+        W = np.stack([np.concatenate([pack_q8_0(D[r, b], Qw[r, 32 * b:32 * b + 32]) for b in range(k // 32)])
+                      for r in range(n)])
+    else:
+        Qw = rng.integers(0, 16, (n, k))
+        V = Qw - 8
+        W = np.stack([np.concatenate([pack_q4_0(D[r, b], Qw[r, 32 * b:32 * b + 32]) for b in range(k // 32)])
+                      for r in range(n)])
+    Qx = rng.integers(-127, 128, (m, k))
+    D8 = _pow2(rng, -8, -1, (m, k // 32))
+    xq = _q8_1_rows(Qx, D8, rng.uniform(-3, 3, (m, k // 32)))
+    y, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
+    sumi = np.einsum("mbi,nbi->mnb", Qx.reshape(m, -1, 32), V.reshape(n, -1, 32))
+    t = D[None] * D8[:, None, :] * sumi
+    np.testing.assert_allclose(T, np.abs(t).sum(axis=2), rtol=1e-15, atol=0)
+    assert np.all(np.abs(y - t.sum(axis=2)) <= 1e-14 * T)
+
+
 @pytest.mark.parametrize("fmt", ["q6_K", "q8_0", "q4_0"])
 def test_brute_force_agrees(oracle_mod, fmt):
     """Without a min term the fold equals the fp64 matmul of dequantized W and
@@ -316,3 +399,50 @@ def test_mul_mat_glu_gate_and_up_roles(oracle_mod):
     Wz.reshape(n, k // 256, 144)[3, :, 0:4] = 0  # up row 3: d = dmin = 0
     y3, _ = oracle_mod.mul_mat_glu(Wg, Wz, "q4_K", n, k, xq, m)
     assert np.all(y3[:, 3] == 0)
+
+
+def test_mul_mat_glu_tolerance_closed_forms(oracle_mod):
+    """The SwiGLU bound at gate dots where fp64 gives silu and its slope exactly.  Q8_0
+    rows with d = 1 and q8_1 d = 1 make every dot an integer (numpy's int matmul), and:
+      - row 0 holds a gate dot of exactly 0 from two blocks that cancel (T_g > 0):
+        silu(0) = 0 and silu'(0) = 1/2, so y = 0 and tol = 1e-5 T_g |u| / 2 + 2^-120 |u|;
+      - row 1 a gate dot of 40 or more, where e^-g < 2^-57 leaves the fp64 sigmoid at
+        exactly 1: silu(g) = g and silu'(g) = 1, so y = g u and
+        tol = 1e-5 (T_g |u| + g T_u) + 2^-20 |g u| + 2^-120 |u|;
+      - row 2 a gate dot of -746 or less, where e^-g overflows and the sigmoid is exactly
+        0: y = 0 and tol = 2^-120 |u|."""
+    rng = np.random.default_rng(63)
+    n, k, m = 3, 64, 2
+    Qx = rng.integers(-127, 128, (m, 32))
+    Qx[:, 0] = 127                       # no all-zero row
+    Qx = np.concatenate([Qx, Qx], axis=1)  # blocks 0 and 1 of x are equal
+    a = rng.integers(-128, 128, 32)
+    sx = np.sign(Qx[0, :32])
+    Qg = np.stack([np.concatenate([a, -a]),
+                   np.concatenate([sx * 100, sx * 100]),
+                   np.concatenate([-sx * 127, -sx * 127])])
+    Qu = rng.integers(-128, 128, (n, k))
+
+    def rows(Q):
+        return np.stack([np.concatenate([pack_q8_0(1.0, Q[r, 32 * b:32 * b + 32]) for b in range(k // 32)])
+                         for r in range(n)])
+    xq = _q8_1_rows(Qx, np.ones((m, 2)), np.zeros((m, 2)))
+    with np.errstate(over="ignore"):
+        y, tol = oracle_mod.mul_mat_glu(rows(Qg), rows(Qu), "q8_0", n, k, xq, m)
+    g = (Qx @ Qg.T).astype(np.float64)
+    u = (Qx @ Qu.T).astype(np.float64)
+    Tg = np.abs(np.einsum("mbi,nbi->mnb", Qx.reshape(m, 2, 32), Qg.reshape(n, 2, 32))).sum(axis=2)
+    Tu = np.abs(np.einsum("mbi,nbi->mnb", Qx.reshape(m, 2, 32), Qu.reshape(n, 2, 32))).sum(axis=2)
+    assert np.all(g[:, 0] == 0) and np.all(Tg[:, 0] > 0)
+    assert g[0, 1] >= 40 and g[0, 2] <= -746
+    eps = 2.0 ** -120
+    # row 0: silu(0) = 0, slope 1/2
+    assert np.all(y[:, 0] == 0)
+    np.testing.assert_allclose(tol[:, 0], 1e-5 * Tg[:, 0] * np.abs(u[:, 0]) / 2 + eps * np.abs(u[:, 0]), rtol=1e-14)
+    # row 1 (x row 0, whose signs built it): silu(g) = g, slope 1
+    assert y[0, 1] == g[0, 1] * u[0, 1]
+    np.testing.assert_allclose(tol[0, 1], 1e-5 * (Tg[0, 1] * abs(u[0, 1]) + g[0, 1] * Tu[0, 1])
+                               + 2.0 ** -20 * abs(g[0, 1] * u[0, 1]) + eps * abs(u[0, 1]), rtol=1e-14)
+    # row 2: the sigmoid is 0
+    assert y[0, 2] == 0
+    np.testing.assert_allclose(tol[0, 2], eps * abs(u[0, 2]), rtol=1e-14)

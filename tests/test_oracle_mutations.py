@@ -67,6 +67,40 @@ MUTATIONS = [
      "uint16_t sh = oracle_float_to_half(dhf * (float)S);",
      "uint16_t sh = oracle_float_to_half(d * (float)S);",
      [lambda o: F.test_q8_1_invariants(o, "normal"), lambda o: F.test_q8_1_invariants(o, "adversarial")]),
+    # the tolerance sum T, which scales every parity bound: a slip that inflates it would
+    # loosen every GPU comparison without failing any of them
+    ("T taken as |y| instead of the sum of |block terms|",
+     "if (T) *T = tabs;", "if (T) *T = fabs(acc);",
+     [M.test_q4_K_tolerance_sum_closed_form, M.test_q6_K_tolerance_sum_closed_form,
+      lambda o: M.test_32_block_tolerance_sum_closed_form(o, "q8_0")]),
+    ("Q4_K T from the net sub-block term |t1 - t2|",
+     "tabs += fabs(t1) + fabs(t2);", "tabs += fabs(t1 - t2);",
+     [M.test_q4_K_tolerance_sum_closed_form, M.test_q4_K_min_term_special_case]),
+    ("Q4_K T without the scale term",
+     "tabs += fabs(t1) + fabs(t2);", "tabs += fabs(t2);",
+     [M.test_q4_K_tolerance_sum_closed_form, M.test_q4_K_min_term_special_case]),
+    ("Q4_K T as |sum| per superblock",
+     ("double d = h2d(blk), dmin = h2d(blk + 2);\n            for (int b = 0; b < 8; ++b) {",
+      "                tabs += fabs(t1) + fabs(t2);\n            }\n"),
+     ("double d = h2d(blk), dmin = h2d(blk + 2), sb = 0.0;\n            for (int b = 0; b < 8; ++b) {",
+      "                sb += t1 - t2;\n            }\n            tabs += fabs(sb);\n"),
+     [M.test_q4_K_tolerance_sum_closed_form, M.test_q4_K_min_term_special_case]),
+    ("Q6_K T without the q8_1 d",
+     "                acc += t;\n                tabs += fabs(t);",
+     "                acc += t;\n                tabs += fabs(d * (int8_t)blk[192 + j] * (double)sumi);",
+     [M.test_q6_K_tolerance_sum_closed_form]),
+    ("Q8_0 T from |q_w| |q_x| instead of |sumi|",
+     "            for (int i = 0; i < 32; ++i) sumi += (int64_t)(int8_t)blk[2 + i] * (int8_t)xb[4 + i];\n"
+     "            double t = h2d(blk) * h2d(xb) * (double)sumi;\n"
+     "            acc += t;\n"
+     "            tabs += fabs(t);",
+     "            int64_t sabs = 0;\n"
+     "            for (int i = 0; i < 32; ++i) sumi += (int64_t)(int8_t)blk[2 + i] * (int8_t)xb[4 + i];\n"
+     "            for (int i = 0; i < 32; ++i) sabs += llabs((int64_t)(int8_t)blk[2 + i] * (int8_t)xb[4 + i]);\n"
+     "            double t = h2d(blk) * h2d(xb) * (double)sumi;\n"
+     "            acc += t;\n"
+     "            tabs += fabs(h2d(blk) * h2d(xb)) * (double)sabs;",
+     [lambda o: M.test_32_block_tolerance_sum_closed_form(o, "q8_0")]),
 ]
 
 
@@ -81,9 +115,13 @@ def _catches(pin, mod):
 @pytest.mark.parametrize("name,orig,planted,pins", MUTATIONS, ids=[m[0] for m in MUTATIONS])
 def test_planted_mistake_is_caught(tmp_path, oracle_mod, name, orig, planted, pins):
     src = open(SRC).read()
-    assert src.count(orig) == 1, f"the line to plant in is gone: {orig}"
+    # a mistake is one replacement, or a tuple of them made together
+    origs, planteds = (orig, planted) if isinstance(orig, tuple) else ((orig,), (planted,))
+    for o, p in zip(origs, planteds):
+        assert src.count(o) == 1, f"the line to plant in is gone: {o}"
+        src = src.replace(o, p)
     mutant_c = tmp_path / "mutant.c"
-    mutant_c.write_text(src.replace(orig, planted))
+    mutant_c.write_text(src)
     so = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC", "-std=c11",
                     "-o", str(so), str(mutant_c), "-lm"], check=True)
@@ -116,6 +154,17 @@ def _silu(v):
     return v / (1.0 + np.exp(-v))
 
 
+_real_glu = oracle._glu
+
+
+def _glu_tol_mutant(bound):
+    """The real SwiGLU value with a planted mistake in its bound."""
+    def glu(g, Tg, u, Tu):
+        y, tol = _real_glu(g, Tg, u, Tu)
+        return y, bound(g, Tg, u, Tu, tol)
+    return glu
+
+
 PY_MUTATIONS = [
     ("silu with the sigmoid's sign flipped", "silu",
      lambda v: np.asarray(v, dtype=np.float64) / (1.0 + np.exp(np.asarray(v, dtype=np.float64))),
@@ -126,6 +175,18 @@ PY_MUTATIONS = [
      [M.test_mul_mat_glu_pins, M.test_mul_mat_glu_gate_and_up_roles]),
     ("SwiGLU without the silu", "_glu", _glu_mutant(lambda g, u: g * u),
      [M.test_mul_mat_glu_pins, M.test_mul_mat_glu_gate_and_up_roles]),
+    ("SwiGLU bound 100 times too wide", "_glu", _glu_tol_mutant(lambda g, Tg, u, Tu, tol: 100 * tol),
+     [M.test_mul_mat_glu_tolerance_closed_forms]),
+    ("SwiGLU bound without the slope of silu", "_glu",
+     _glu_tol_mutant(lambda g, Tg, u, Tu, tol: 1e-5 * (np.abs(_silu(g)) * Tg * np.abs(u) + np.abs(_silu(g)) * Tu)
+                     + 2.0 ** -20 * np.abs(_silu(g) * u) + 2.0 ** -120 * np.abs(u)),
+     [M.test_mul_mat_glu_tolerance_closed_forms]),
+    ("SwiGLU bound without the fp32 evaluation term", "_glu",
+     _glu_tol_mutant(lambda g, Tg, u, Tu, tol: tol - 2.0 ** -20 * np.abs(_silu(g) * u)),
+     [M.test_mul_mat_glu_tolerance_closed_forms]),
+    ("SwiGLU bound with gate and up bounds swapped", "_glu",
+     _glu_tol_mutant(lambda g, Tg, u, Tu, tol: _real_glu(g, Tu, u, Tg)[1]),
+     [M.test_mul_mat_glu_tolerance_closed_forms]),
 ]
 
 
