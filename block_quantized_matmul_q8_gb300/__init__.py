@@ -31,7 +31,7 @@ EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspac
            "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32",
            "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu", "qmm_gemv_ring_stages",
            "qmm_repack_glu", "qmm_mul_mat_glu_packed", "qmm_workspace_bytes_f32_host", "qmm_mul_mat_f32_host",
-           "qmm_get_device_status")
+           "qmm_get_device_status", "qmm_set_test_fault")
 
 
 class QMMError(RuntimeError):
@@ -90,6 +90,8 @@ def lib():
     L.qmm_plan_cta_range.argtypes = [ctypes.POINTER(GemmPlan), I32, ctypes.POINTER(I64), ctypes.POINTER(I64)]
     L.qmm_set_force_path.restype = None
     L.qmm_set_force_path.argtypes = [ctypes.c_int]
+    L.qmm_set_test_fault.restype = None
+    L.qmm_set_test_fault.argtypes = [ctypes.c_int]
     L.qmm_set_stream_k_mode.restype = None
     L.qmm_set_stream_k_mode.argtypes = [ctypes.c_int]
     L.qmm_mul_mat_id_noalloc.restype = ctypes.c_int
@@ -377,6 +379,10 @@ def qmm_set_force_path(path: int) -> None:
 
 def qmm_set_stream_k_mode(mode: int) -> None:
     lib().qmm_set_stream_k_mode(int(mode))
+
+
+def qmm_set_test_fault(mode: int) -> None:
+    lib().qmm_set_test_fault(int(mode))
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

@@ -20,6 +20,7 @@ std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_smem_optin[kMaxDevices];
 std::atomic<int> g_force_path{0};
 std::atomic<int> g_stream_k_mode{0};
+std::atomic<int> g_test_fault{0};
 
 int current_device() {
     int dev = 0;
@@ -90,6 +91,8 @@ static qmm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMM_OK 
 
 // Which kernel family qmm_mul_mat uses for these sizes.
 enum Path { kGemv = 1, kGemmDp4a = 2, kGemmTc = 3, kGemvDirect = 4, kGemvTc = 5 };
+
+int test_fault_mode() { return g_test_fault.load(std::memory_order_relaxed); }
 
 bool gemv_tma_enabled() { return g_force_path.load(std::memory_order_relaxed) != kGemvDirect; }
 
@@ -525,5 +528,6 @@ void qmm_plan_cta_range(const qmm_gemm_plan *plan, int32_t cta, int64_t *begin, 
 
 void qmm_set_force_path(int path) { g_force_path.store(path, std::memory_order_relaxed); }
 void qmm_set_stream_k_mode(int mode) { g_stream_k_mode.store(mode, std::memory_order_relaxed); }
+void qmm_set_test_fault(int mode) { g_test_fault.store(mode, std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -179,6 +179,11 @@ struct TcArgs {
     // of tm_w and the tile loads as in the plain GEMM
     int64_t n_out;
     int glu_packed;
+    // test switch (qmm_set_test_fault): the activation producer issues nothing, and the
+    // MMA issuer's wait for the first stage gives up after mma_wait_cycles, so the
+    // kernel reports QMM_ERR_DEVICE with no copy in flight
+    int withhold_x;
+    long long mma_wait_cycles;
 };
 
 // Where tile t lives: m0 = first activation row (sorted row in grouped mode), rows =
@@ -333,7 +338,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         regs_dec<kRegsProducer>();
-        if (lane == 0) {
+        if (lane == 0 && !a.withhold_x) {
             ptx::prefetch_tmap(&tm_x);
             if (F::kMin) ptx::prefetch_tmap(&tm_xmin);
             ptx::prefetch_tmap(&tm_dx);
@@ -393,7 +398,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                     for (int h = 0; ok && h < 2; ++h) {
                         const uint32_t st = x_it % kStages, par = (x_it / kStages) & 1;
-                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.st_full[st]), par, abortp)) {
+                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.st_full[st]), par, abortp, a.mma_wait_cycles)) {
                             ok = false;
                             break;
                         }
@@ -1055,6 +1060,12 @@ bool make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The test switch of qmm_set_test_fault, copied into a launch's arguments.
+void tc_test_fault(TcArgs &a) {
+    a.withhold_x = test_fault_mode() == 1 ? 1 : 0;
+    a.mma_wait_cycles = a.withhold_x ? 100000LL : ptx::kWaitCycles;
+}
+
 struct TcLayout {
     size_t status, xh, dx, smin, partial, total;
 };
@@ -1182,6 +1193,7 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
         return cudaErrorInvalidValue;
 
     TcArgs args{};
+    tc_test_fault(args);
     args.W = static_cast<const uint8_t *>(W);
     args.n = n;
     args.m = m;
@@ -1249,6 +1261,7 @@ cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64
                             CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     TcArgs args{};
+    tc_test_fault(args);
     args.W = static_cast<const uint8_t *>(Wg);
     args.n = 2 * n_out;
     args.m = m;
@@ -1304,6 +1317,7 @@ cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts,
         return cudaErrorInvalidValue;
 
     TcArgs args{};
+    tc_test_fault(args);
     args.W = static_cast<const uint8_t *>(W);
     args.n = n;
     args.m = n_pairs;

@@ -129,6 +129,9 @@ cudaError_t launch_mul_mat_id_dp4a(qmm_type t, const void *W, int64_t n_experts,
                                    const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
                                    bool x_per_slot, float *y, void *ws, size_t ws_bytes, cudaStream_t st);
 
+// Test switch of qmm_set_test_fault (0: off).
+int test_fault_mode();
+
 // Offset of the device status word inside a mul_mat_id workspace.
 constexpr size_t kStatusOffset = 0;
 

@@ -219,9 +219,6 @@ cudaError_t launch_mul_mat_id_dp4a(qmm_type t, const void *W, int64_t n_experts,
                                     st);
 }
 
-// Up to this many (token, slot) pairs, one GEMV per pair beats the grouped GEMM, whose
-// 128-pair tiles would each hold one or two pairs.
-constexpr int64_t kMoeGemvMaxPairs = 32;
 
 cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                               const int32_t *ids, int64_t top_k, int64_t n_tokens, bool x_per_slot, float *y,

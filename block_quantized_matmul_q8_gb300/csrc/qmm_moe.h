@@ -19,6 +19,10 @@ struct MoETile {
 // Largest expert count the single-CTA bucketing kernel supports.
 constexpr int kMaxExperts = 512;
 
+// Up to this many (token, slot) pairs, one GEMV per pair beats the grouped GEMM, whose
+// 128-pair tiles would each hold one or two pairs.
+constexpr int64_t kMoeGemvMaxPairs = 32;
+
 // Workspace layout of qmm_mul_mat_id (offsets in bytes, 256-byte aligned pieces).
 struct MoELayout {
     size_t status;   // int32 status word, tile count, invalid-pair count, cold-expert count

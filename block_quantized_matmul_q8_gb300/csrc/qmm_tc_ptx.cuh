@@ -76,14 +76,15 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int *abort,
+                                               long long limit = kWaitCycles) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 0;; ++it) {
         if (mbar_test(bar, parity)) return true;
         if ((it & 63u) == 63u) {
             if (*abort) return false;
-            if (clock64() - t0 > kWaitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort = 1;
                 return false;
             }

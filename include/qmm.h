@@ -260,15 +260,17 @@ QMM_API qmm_status qmm_mul_mat_id_slot(const void *W_experts, qmm_type t, int64_
  * captures).  The pages have no counterpart of this call.
  *   Arguments, layouts and results are those of qmm_mul_mat_id.
  *   Scratch: one file-scope device array of qmm_noalloc_scratch_bytes() (1 MiB),
- *   present in every GPU that loads the library until the process exits.  This call
- *   always runs the CUDA-core grouped GEMM, whose scratch is the bucketing state
- *   alone: 256 B of status, 4*(n_experts+1) B of bounds, 4 B per (token, slot)
- *   pair and 16 B per tile (pairs/64 + n_experts + 1 tiles), each piece rounded up
- *   to 256 B, so up to about 240K pairs fit.  A larger problem is rejected with
- *   QMM_ERR_WORKSPACE and nothing is enqueued.  The call allocates nothing and
- *   frees nothing.
- *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any stream
+ *   present in every GPU that loads the library until the process exits.  Up to 32
+ *   (token, slot) pairs this call runs one GEMV per pair (as qmm_mul_mat_id does),
+ *   which needs only the status word; beyond that it runs the CUDA-core grouped
+ *   GEMM, whose scratch is the bucketing state alone: 256 B of status,
+ *   4*(n_experts+1) B of bounds, 4 B per (token, slot) pair, 16 B per tile
+ *   (pairs/64 + n_experts + 1 tiles) and 4*n_experts B of cold-expert list, each
+ *   piece rounded up to 256 B, so up to about 240K pairs fit (fewer with many
+ *   experts).  A larger problem is rejected with QMM_ERR_WORKSPACE and nothing is
+ *   enqueued.  The call allocates nothing and frees nothing.
+ *   The first call in a device and CUDA context looks up the array's device
+ *   address (with that device current); make that first call before any stream
  *   capture.  Every call on a device shares the array: calls whose work can
  *   overlap on the GPU (different streams without ordering) race on it.
  *   The device status word is kept in the array and is not reported.
@@ -352,6 +354,16 @@ QMM_API void qmm_set_force_path(int path);
 
 /* Stream-K mode for the tensor-core GEMM: 0 = automatic, 1 = never, 2 = always. */
 QMM_API void qmm_set_stream_k_mode(int mode);
+
+/* Failure-detection test switch (an interface of this library; the pages have no
+ * counterpart).  0 = off.  1 = every tensor-core GEMM launch made while it is set
+ * (qmm_mul_mat and the grouped mul_mat_id paths with m > 16) withholds its
+ * activation copies, so that the MMA issuer's bounded wait for the first stage runs
+ * out (after about 10^5 cycles instead of about a second): the kernel stops, frees
+ * its tensor memory and sets QMM_ERR_DEVICE in the workspace's status word, which
+ * qmm_read_device_status / qmm_get_device_status return.  No copy is in flight when
+ * the kernel leaves and the context stays usable; y is unspecified for that call. */
+QMM_API void qmm_set_test_fault(int mode);
 
 #ifdef __cplusplus
 }
