@@ -22,7 +22,7 @@ TYPES = {"q4_0": 2, "q8_0": 8, "q4_K": 12, "q6_K": 14}
 BLOCK = {"q4_0": (32, 18), "q8_0": (32, 34), "q4_K": (256, 144), "q6_K": (256, 210)}
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_ARG", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE", 4: "QMM_ERR_ALIGN",
           5: "QMM_ERR_WORKSPACE", 6: "QMM_ERR_CUDA", 7: "QMM_ERR_IDS", 8: "QMM_ERR_DEVICE"}
-PATH_AUTO, PATH_GEMV, PATH_GEMM_DP4A, PATH_GEMM_TC, PATH_GEMV_DIRECT, PATH_GEMV_TC = 0, 1, 2, 3, 4, 5
+PATH_AUTO, PATH_GEMV, PATH_GEMM_DP4A, PATH_GEMM_TC, PATH_GEMV_DIRECT, PATH_GEMV_TC, PATH_GEMV_MMA = 0, 1, 2, 3, 4, 5, 6
 
 # Every function that include/qmm.h declares.
 EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspace_bytes", "qmm_quantize_q8_1",

@@ -90,7 +90,7 @@ static qmm_status check_k(qmm_type t, int64_t k) {
 static qmm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
 // Which kernel family qmm_mul_mat uses for these sizes.
-enum Path { kGemv = 1, kGemmDp4a = 2, kGemmTc = 3, kGemvDirect = 4, kGemvTc = 5 };
+enum Path { kGemv = 1, kGemmDp4a = 2, kGemmTc = 3, kGemvDirect = 4, kGemvTc = 5, kGemvMma = 6 };
 
 int test_fault_mode() { return g_test_fault.load(std::memory_order_relaxed); }
 
@@ -103,6 +103,7 @@ static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
     if (force == kGemmDp4a) return kGemmDp4a;
     if (force == kGemmTc && gemm_tc_supported(t, n, k, m)) return kGemmTc;
     if (force == kGemvTc && gemv_tc_supported(t, n, k, m)) return kGemvTc;
+    if (force == kGemvMma && gemv_mma_supported(t, n, k, m)) return kGemvMma;
     if (m <= 8 && gemv_fits) return kGemv;
     // skinny activations on the tensor cores (weights as the MMA's M side)
     if (gemv_tc_supported(t, n, k, m)) return kGemvTc;
@@ -410,6 +411,7 @@ qmm_status mul_mat_q8(const void *W, qmm_type t, int64_t n, int64_t k, const voi
                       void *workspace, size_t ws_bytes, cudaStream_t st) {
     switch (choose_path(t, n, k, m)) {
     case kGemv: return cuda_status(launch_gemv(t, W, n, k, xq, nullptr, m, y, st));
+    case kGemvMma: return cuda_status(launch_gemv_mma(t, W, n, k, xq, m, y, st));
     case kGemvTc: {
         const size_t need = gemv_tc_workspace_bytes(t, n, k, m);
         if (!workspace || ws_bytes < need) return QMM_ERR_WORKSPACE;

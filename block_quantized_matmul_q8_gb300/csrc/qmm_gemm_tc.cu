@@ -60,7 +60,7 @@ namespace {
 
 constexpr int kTM = 128;  // activation rows per tile
 constexpr int kTN = 128;  // weight rows per tile
-constexpr int kStages = 2;
+constexpr int kMaxStages = 3;  // deepest activation/weight stage ring of any format
 constexpr int kSlots = 4;          // accumulator slots of 128 TMEM columns: all of TMEM
 constexpr int kPair = 2;           // slots handed over per barrier round trip
 constexpr int kThreads = 768;      // 24 warps = 6 warpgroups
@@ -82,19 +82,25 @@ constexpr int kMaxPartialCtas = 256;
 // per-row factors the unpack hands to the epilogue, raw_x the raw tensor map's x
 // coordinate of superblock sb (in its elements).
 template <int T> struct TcFmt;
-template <> struct TcFmt<QMM_Q4_K> {
+// Stage geometry (all formats but Q6_K): 2 stages of half a superblock, each 2 activation
+// slabs of 64 k values and 2 weight slabs; kScaleD: the weight row's d multiplies the
+// superblock's sum of d8 * slot once, instead of a factor per slot.
+struct TcStages2 {
+    static constexpr int kStages = 2, kStagesPerSb = 2, kXSlabs = 2, kPlanes = 1;
+};
+template <> struct TcFmt<QMM_Q4_K> : TcStages2 {
     static constexpr uint32_t kRawRow = kQ4KBytes;  // raw bytes of one weight row per 256 k
     static constexpr uint32_t kRawBuf = 128 * kRawRow;  // one raw buffer: the tile's 128 rows
-    static constexpr bool kMin = true;
+    static constexpr bool kMin = true, kScaleD = true;
     static constexpr int kUses = 8;
     static constexpr int kSub = 32;  // k values per slot
     static constexpr uint32_t kDDBytes = 2 * 128 * 4;  // d[128], -dmin[128]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * kQ4KBytes); }
 };
-template <> struct TcFmt<QMM_Q8_0> {
+template <> struct TcFmt<QMM_Q8_0> : TcStages2 {
     static constexpr uint32_t kRawRow = 8 * kQ80Bytes;  // 272
     static constexpr uint32_t kRawBuf = 128 * kRawRow;
-    static constexpr bool kMin = false;
+    static constexpr bool kMin = false, kScaleD = false;
     static constexpr int kUses = 8;
     static constexpr int kSub = 32;
     static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
@@ -102,10 +108,10 @@ template <> struct TcFmt<QMM_Q8_0> {
 };
 // Q4_0: the 256 k values of a step are eight 18-byte blocks (144 bytes, as a Q4_K
 // superblock), a d per 32-block and row; the codes q - 8 are exact fp16 integers.
-template <> struct TcFmt<QMM_Q4_0> {
+template <> struct TcFmt<QMM_Q4_0> : TcStages2 {
     static constexpr uint32_t kRawRow = 8 * kQ40Bytes;  // 144
     static constexpr uint32_t kRawBuf = 128 * kRawRow;
-    static constexpr bool kMin = false;
+    static constexpr bool kMin = false, kScaleD = false;
     static constexpr int kUses = 8;
     static constexpr int kSub = 32;
     static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
@@ -117,17 +123,25 @@ template <> struct TcFmt<QMM_Q4_0> {
 // 16-byte boundary at or below the row's superblock (offset <= 14 inside it, the bytes
 // after it belong to the next row).  With n a multiple of 8 the weight tensor ends on a
 // 16-byte boundary, so the last row's last window ends exactly there.  Windows sit 240
-// bytes apart in shared memory: 8 consecutive rows start on different banks.  One slot
-// per 16-wide sub-block, since each has its own int8 scale: the weight operand is the
-// bare 6-bit code (exact), and d * sc joins the fold.
+// bytes apart in shared memory: 8 consecutive rows start on different banks.
+// The int8 sub-scale of every 16 values goes into the operands: with sc = 16 a + b
+// (a = sc >> 4 in -8..7, b = sc & 15), the weight code q (-32..31) becomes two exact fp16
+// planes, 16 q a and q b, and the MMA runs over the same activations once per plane into
+// the same accumulator, which then holds sum sc q x of a whole 32-block (each element adds
+// 0, 16 q a, q b or q sc, all at most 128 |q| in magnitude, so every partial sum stays
+// below 32 * 127 * 32 * 128 < 2^24 and is exact in any order).  One slot per 32-block, as
+// for Q4_K, and only d is left for the fold: twice the MMAs, half the slots and a quarter
+// of the fold work of one slot per 16-wide sub-block.  Stages are a quarter superblock
+// (one activation slab, two weight planes), three deep.
 template <> struct TcFmt<QMM_Q6_K> {
+    static constexpr int kStages = 3, kStagesPerSb = 4, kXSlabs = 1, kPlanes = 2;
     static constexpr uint32_t kRawRow = 240;    // shared-memory stride of the row windows
     static constexpr uint32_t kCopyBytes = 224;  // window bytes per row
     static constexpr uint32_t kRawBuf = 128 * kRawRow;
-    static constexpr bool kMin = false;
-    static constexpr int kUses = 16;
-    static constexpr int kSub = 16;
-    static constexpr uint32_t kDDBytes = 16 * 128 * 4;  // d * sc[16 sub-blocks][128 rows]
+    static constexpr bool kMin = false, kScaleD = true;
+    static constexpr int kUses = 8;
+    static constexpr int kSub = 32;
+    static constexpr uint32_t kDDBytes = 128 * 4;  // d[128 rows]
     // byte offset of superblock sb of weight row `row` from the start of W
     static __device__ __forceinline__ int64_t pos(int64_t row, int64_t sb, int64_t row_bytes) {
         return row * row_bytes + sb * kQ6KBytes;
@@ -140,10 +154,13 @@ template <int T> struct TcMap {
     using F = TcFmt<T>;
     static_assert(F::kUses % (2 * kPair) == 0, "a superblock must start on the first pair of the ring");
     static_assert(F::kRawBuf % 16 == 0, "raw buffers must keep TMA destinations 16-byte aligned");
-    static constexpr uint32_t kOffX = 0;                                 // [stage][2 slabs]
-    static constexpr uint32_t kOffW = kOffX + kStages * 2 * kSlabBytes;  // [stage][2 slabs]
-    static constexpr uint32_t kMinBytes = F::kMin ? kStages * 4096 : 0;
-    static constexpr uint32_t kOffXmin = kOffW + kStages * 2 * kSlabBytes;  // [stage][128][32 B]
+    static_assert(F::kStages <= kMaxStages && (F::kUses / kPair) % F::kStagesPerSb == 0, "stage geometry");
+    static constexpr uint32_t kXStage = F::kXSlabs * kSlabBytes;      // activation slabs of a stage
+    static constexpr uint32_t kWStage = F::kPlanes * kXStage;         // weight slabs of a stage (all planes)
+    static constexpr uint32_t kOffX = 0;                                  // [stage][kXSlabs slabs]
+    static constexpr uint32_t kOffW = kOffX + F::kStages * kXStage;       // [stage][plane][kXSlabs slabs]
+    static constexpr uint32_t kMinBytes = F::kMin ? F::kStages * 4096 : 0;
+    static constexpr uint32_t kOffXmin = kOffW + F::kStages * kWStage;    // [stage][128][32 B]
     static constexpr uint32_t kOffWmin = kOffXmin + kMinBytes;              // [stage][128][32 B]
     static constexpr uint32_t kOffDX = kOffWmin + kMinBytes;                // [2][128][8] fp32 d8
     static constexpr uint32_t kOffDD = kOffDX + 2 * 4096;                   // [2][kDDBytes]
@@ -215,7 +232,7 @@ __device__ __forceinline__ TileInfo resolve_tile(const TcArgs &a, int64_t t) {
 // st_empty when the MMAs reading the stage are done (TMA producer and unpack both wait
 // on it).  sd_full / sd_empty guard the per-superblock scale tiles the same way.
 struct Barriers {
-    uint64_t st_full[kStages], st_empty[kStages];
+    uint64_t st_full[kMaxStages], st_empty[kMaxStages];
     uint64_t acc_full[kSlots / kPair], acc_empty[kSlots / kPair];
     uint64_t sd_full[2], sd_empty[2];
     uint64_t raw_full[2], raw_empty[2];
@@ -305,7 +322,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
 
     if (tid == 0) {
         B.abort = 0;
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < F::kStages; ++s) {
             ptx::mbar_init(ptx::smem_u32(&B.st_full[s]), 1 + 128);
             ptx::mbar_init(ptx::smem_u32(&B.st_empty[s]), 1);
         }
@@ -358,18 +375,20 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     ptx::mbar_arrive_expect_tx(sdbar, 4096);
                     ptx::tma_load_2d(sbase + kOffDX + sdi * 4096, &tm_dx, (int)(8 * sb), m0, sdbar);
                     ++sd_it;
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t st = x_it % kStages;
-                        if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((x_it / kStages) & 1) ^ 1, abortp)) {
+                    for (int h = 0; h < F::kStagesPerSb; ++h) {
+                        const uint32_t st = x_it % F::kStages;
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((x_it / F::kStages) & 1) ^ 1, abortp)) {
                             ok = false;
                             break;
                         }
+                        const bool last = h == F::kStagesPerSb - 1;
                         const uint32_t bar = ptx::smem_u32(&B.st_full[st]);
-                        ptx::mbar_arrive_expect_tx(bar, 2 * kSlabBytes + ((F::kMin && h) ? 4096u : 0u));
-                        const int kx = (int)(256 * sb + 128 * h);
-                        ptx::tma_load_2d(sbase + kOffX + st * 2 * kSlabBytes, &tm_x, kx, m0, bar);
-                        ptx::tma_load_2d(sbase + kOffX + st * 2 * kSlabBytes + kSlabBytes, &tm_x, kx + 64, m0, bar);
-                        if (F::kMin && h)
+                        ptx::mbar_arrive_expect_tx(bar, Mp::kXStage + ((F::kMin && last) ? 4096u : 0u));
+                        const int kx = (int)(256 * sb + 64 * F::kXSlabs * h);
+#pragma unroll
+                        for (int i = 0; i < F::kXSlabs; ++i)
+                            ptx::tma_load_2d(sbase + kOffX + st * Mp::kXStage + i * kSlabBytes, &tm_x, kx + 64 * i, m0, bar);
+                        if (F::kMin && last)
                             ptx::tma_load_2d(sbase + kOffXmin + st * 4096, &tm_xmin, (int)(16 * sb), m0, bar);
                         ++x_it;
                     }
@@ -377,8 +396,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
             }
             // drain: every armed copy must have landed before the CTA may exit
             int dummy = 0;
-            for (uint32_t i = (x_it > kStages ? x_it - kStages : 0); i < x_it; ++i)
-                ptx::mbar_wait(ptx::smem_u32(&B.st_full[i % kStages]), (i / kStages) & 1, &dummy);
+            for (uint32_t i = (x_it > F::kStages ? x_it - F::kStages : 0); i < x_it; ++i)
+                ptx::mbar_wait(ptx::smem_u32(&B.st_full[i % F::kStages]), (i / F::kStages) & 1, &dummy);
             for (uint32_t i = (sd_it > 2 ? sd_it - 2 : 0); i < sd_it; ++i)
                 ptx::mbar_wait(ptx::smem_u32(&B.sd_full[i & 1]), (i >> 1) & 1, &dummy);
         }
@@ -396,16 +415,16 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
             bool ok = true;
             while (ok && next_seg(a, u, uend, sg)) {
                 for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
-                    for (int h = 0; ok && h < 2; ++h) {
-                        const uint32_t st = x_it % kStages, par = (x_it / kStages) & 1;
+                    for (int h = 0; ok && h < F::kStagesPerSb; ++h) {
+                        const uint32_t st = x_it % F::kStages, par = (x_it / F::kStages) & 1;
                         if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.st_full[st]), par, abortp, a.mma_wait_cycles)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint32_t xa = sbase + kOffX + st * 2 * kSlabBytes;
-                        const uint32_t wa = sbase + kOffW + st * 2 * kSlabBytes;
-                        for (int q = 0; q < kGroups / 2; ++q) {  // the pairs of this half
+                        const uint32_t xa = sbase + kOffX + st * Mp::kXStage;
+                        const uint32_t wa = sbase + kOffW + st * Mp::kWStage;
+                        for (int q = 0; q < kGroups / F::kStagesPerSb; ++q) {  // the pairs of this stage
                             const uint32_t e = gq & 1;
                             if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_empty[e]), ((gq >> 1) & 1) ^ 1, abortp)) {
                                 ok = false;
@@ -419,14 +438,17 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                                 for (int t = 0; t < F::kSub / 16; ++t) {  // K16 steps per slot
                                     const int step = (q * kPair + b2) * (F::kSub / 16) + t;  // slab step/4, 32 bytes each
                                     const uint32_t off = (step >> 2) * kSlabBytes + (step & 3) * 32;
-                                    ptx::mma_f16(d, ptx::smem_desc(xa + off, 1024, 2), ptx::smem_desc(wa + off, 1024, 2),
-                                                 idesc, t);
+#pragma unroll
+                                    for (int pl = 0; pl < F::kPlanes; ++pl)  // Q6_K: both weight planes, same activations
+                                        ptx::mma_f16(d, ptx::smem_desc(xa + off, 1024, 2),
+                                                     ptx::smem_desc(wa + pl * Mp::kXStage + off, 1024, 2), idesc,
+                                                     (t | pl) != 0);
                                 }
                             }
                             ptx::mma_commit(ptx::smem_u32(&B.acc_full[e]));
                             ++gq;
                         }
-                        if (F::kMin && ok && h == 1) {  // the min term: a group of one slot
+                        if (F::kMin && ok && h == F::kStagesPerSb - 1) {  // the min term: a group of one slot
                             const uint32_t e = gq & 1;
                             if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_empty[e]), ((gq >> 1) & 1) ^ 1, abortp)) {
                                 ok = false;
@@ -536,12 +558,12 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 dd[128 + r] = -half_hi(hd.x);
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t st = w_it % kStages;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                    const uint32_t st = w_it % F::kStages;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / F::kStages) & 1) ^ 1, abortp)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
+                    uint8_t *wst = smem + kOffW + st * Mp::kWStage;
 #pragma unroll
                     for (int j2 = 0; j2 < 2; ++j2) {  // slab j2 <-> qs chunk c = 2h + j2
                         const int c = 2 * h + j2;
@@ -581,54 +603,74 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     ++w_it;
                 }
                 } else if constexpr (T == QMM_Q6_K) {
-                // Q6_K: d * sc of the 16 sub-blocks for the epilogue (the superblock starts 0 or 2
-                // bytes past a word boundary: its words are read from the boundary below and
-                // shifted), then per half the two 64-value units as exact fp16 codes q - 32.
+                // Q6_K: d for the epilogue (the superblock starts 0 or 2 bytes past a word
+                // boundary: its words are read from the boundary below and shifted), then per
+                // quarter superblock the 64-value unit as two planes of exact fp16 integers,
+                // 16 q (sc >> 4) and q (sc & 15), with q the code - 32 and sc the int8 scale of
+                // its 16 values (sc = 16 (sc >> 4) + (sc & 15)).
                 {
-                    const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 2u), sh = 8u * mis;
-                    uint32_t scw[5];
-#pragma unroll
-                    for (int i2 = 0; i2 < 5; ++i2) scw[i2] = LdShared::u32(blk + 192 - mis + 4 * i2);
-                    const float d = half_lo(mis ? (scw[4] >> 16) : scw[4]);
-#pragma unroll
-                    for (int i2 = 0; i2 < 4; ++i2) {
-                        const uint32_t w4 = __funnelshift_r(scw[i2], scw[i2 + 1], sh);
-#pragma unroll
-                        for (int bb = 0; bb < 4; ++bb)
-                            dd[(4 * i2 + bb) * 128 + r] = d * (float)(int8_t)((w4 >> (8 * bb)) & 0xffu);
-                    }
+                    const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 2u);
+                    const uint32_t dw = LdShared::u32(blk + 208 - mis);
+                    dd[r] = half_lo(mis ? (dw >> 16) : dw);
                 }
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 const __half2 bias = __float2half2_rn(-1152.f);
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t st = w_it % kStages;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                for (int h = 0; h < F::kStagesPerSb; ++h) {  // unit h (64 k values) is stage h of the superblock
+                    const uint32_t st = w_it % F::kStages;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / F::kStages) & 1) ^ 1, abortp)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
-#pragma unroll 1
-                    for (int j2 = 0; j2 < 2; ++j2) {  // slab j2 <-> unit 2h + j2 (64 k values)
-                        Raw<QMM_Q6_K> raw;
-                        Unit w;
-                        load_raw<LdShared>(blk, 2 * h + j2, 0, raw);
-                        convert_raw(raw, 2 * h + j2, w);
-                        uint8_t *rowdst = wst + j2 * kSlabBytes + r * 128;
+                    uint8_t *wst = smem + kOffW + st * Mp::kWStage;
+                    // The unit's words, read chunk by chunk to keep the unpack warps' registers
+                    // low.  Unit h covers k = 64h .. 64h+63: half hh = h >> 1 of the superblock,
+                    // quarters t = 2 (h & 1) and 2 (h & 1) + 1; weight 128 hh + 32 t + l takes the
+                    // nibble t >> 1 of ql[64 hh + 32 (t & 1) + l] and bits 2t, 2t+1 of qh[32 hh + l].
+                    // The superblock starts 0 or 2 bytes past a word boundary: words are read from
+                    // the boundary below and shifted.
+                    const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 2u), fsh = 8u * mis;
+                    const uint8_t *blk4 = blk - mis;
+                    auto wd = [&](int off) {  // the 32-bit word at byte off of the superblock
+                        return __funnelshift_r(LdShared::u32(blk4 + off), LdShared::u32(blk4 + off + 4), fsh);
+                    };
+                    const uint32_t scw = wd(192 + 4 * h);  // the 4 int8 scales of the unit's 16-value sub-blocks
+                    __half2 ha[4], hb[4];
 #pragma unroll
-                        for (int cq = 0; cq < 8; ++cq) {  // 16-byte chunk cq: codes 8cq .. 8cq+7
-                            uint32_t pr[4];
+                    for (int j = 0; j < 4; ++j) {
+                        const int sc = (int)(int8_t)((scw >> (8 * j)) & 0xffu);
+                        ha[j] = __float2half2_rn((float)(16 * (sc >> 4)));
+                        hb[j] = __float2half2_rn((float)(sc & 15));
+                    }
+                    const int hh = h >> 1;
+                    uint8_t *rowa = wst + r * 128, *rowb = wst + kSlabBytes + r * 128;
 #pragma unroll
-                            for (int e2 = 0; e2 < 2; ++e2) {
-                                const uint32_t uu = (uint32_t)w.q[2 * cq + e2] ^ 0x80808080u;
-                                uint32_t lo = __byte_perm(uu, 0x64646464u, 0x4140);
-                                uint32_t hi = __byte_perm(uu, 0x64646464u, 0x4342);
-                                lo = h2bits(__hadd2(*reinterpret_cast<__half2 *>(&lo), bias));
-                                hi = h2bits(__hadd2(*reinterpret_cast<__half2 *>(&hi), bias));
-                                pr[2 * e2] = lo;
-                                pr[2 * e2 + 1] = hi;
-                            }
-                            *reinterpret_cast<uint4 *>(rowdst + ((cq ^ (r & 7)) << 4)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+                    for (int cq = 0; cq < 8; ++cq) {  // 16-byte chunk cq: codes 8cq .. 8cq+7, sub-block cq / 2
+                        const int tt = 2 * (h & 1) + (cq >> 2), l0 = 8 * (cq & 3);
+                        uint32_t code[2];
+#pragma unroll
+                        for (int e2 = 0; e2 < 2; ++e2) {
+                            const uint32_t ql = wd(64 * hh + 32 * (tt & 1) + l0 + 4 * e2);
+                            const uint32_t qh = wd(128 + 32 * hh + l0 + 4 * e2);
+                            const uint32_t lo = (ql >> (4 * (tt >> 1))) & 0x0f0f0f0fu;
+                            const uint32_t hi2 = ((qh >> (2 * tt)) & 0x03030303u) << 4;
+                            code[e2] = __vsub4(lo | hi2, 0x20202020u);  // q - 32 as signed bytes
                         }
+                        uint32_t pa[4], pb[4];
+#pragma unroll
+                        for (int e2 = 0; e2 < 2; ++e2) {
+                            const uint32_t uu = code[e2] ^ 0x80808080u;
+                            uint32_t lo = __byte_perm(uu, 0x64646464u, 0x4140);
+                            uint32_t hi = __byte_perm(uu, 0x64646464u, 0x4342);
+                            const __half2 ql = __hadd2(*reinterpret_cast<__half2 *>(&lo), bias);
+                            const __half2 qh = __hadd2(*reinterpret_cast<__half2 *>(&hi), bias);
+                            pa[2 * e2] = h2bits(__hmul2(ql, ha[cq >> 1]));
+                            pa[2 * e2 + 1] = h2bits(__hmul2(qh, ha[cq >> 1]));
+                            pb[2 * e2] = h2bits(__hmul2(ql, hb[cq >> 1]));
+                            pb[2 * e2 + 1] = h2bits(__hmul2(qh, hb[cq >> 1]));
+                        }
+                        const int sw = (cq ^ (r & 7)) << 4;
+                        *reinterpret_cast<uint4 *>(rowa + sw) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+                        *reinterpret_cast<uint4 *>(rowb + sw) = make_uint4(pb[0], pb[1], pb[2], pb[3]);
                     }
                     ptx::fence_proxy_async_smem();
                     ptx::mbar_arrive(ptx::smem_u32(&B.st_full[st]));
@@ -644,8 +686,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 const __half2 bias = __float2half2_rn(-1032.f);
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t st = w_it % kStages;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                    const uint32_t st = w_it % F::kStages;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / F::kStages) & 1) ^ 1, abortp)) {
                         ok = false;
                         break;
                     }
@@ -660,7 +702,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         w[2 * i2] = t2.x;
                         w[2 * i2 + 1] = t2.y;
                     }
-                    uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
+                    uint8_t *wst = smem + kOffW + st * Mp::kWStage;
 #pragma unroll
                     for (int b2 = 0; b2 < 4; ++b2) {
                         const int o = (b2 >> 1) * 9;
@@ -701,8 +743,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 const __half2 bias = __float2half2_rn(-1152.f);
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t st = w_it % kStages;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / kStages) & 1) ^ 1, abortp)) {
+                    const uint32_t st = w_it % F::kStages;
+                    if (!ptx::mbar_wait(ptx::smem_u32(&B.st_empty[st]), ((w_it / F::kStages) & 1) ^ 1, abortp)) {
                         ok = false;
                         break;
                     }
@@ -716,7 +758,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         w[2 * i2] = t2.x;
                         w[2 * i2 + 1] = t2.y;
                     }
-                    uint8_t *wst = smem + kOffW + st * 2 * kSlabBytes;
+                    uint8_t *wst = smem + kOffW + st * Mp::kWStage;
 #pragma unroll
                     for (int b2 = 0; b2 < 4; ++b2) {
                         const int o = (b2 >> 1) * 17;
@@ -787,7 +829,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 const int dxsw = (tl >> 2) & 1;
                 auto dxv = [&](int c) { return *reinterpret_cast<const float4 *>(dxrow + ((c ^ dxsw) << 4)); };
                 const float *dd = reinterpret_cast<const float *>(smem + kOffDD + sdi * F::kDDBytes);
-                if constexpr (F::kMin) {
+                if constexpr (F::kScaleD) {
                     float2 acc[16];  // columns 2i, 2i+1 of this thread's 32
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[i] = make_float2(0.f, 0.f);
@@ -820,37 +862,48 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         ++ge;
                     }
                     if (!ok) break;
-                    // the min group: total += d * acc + (-dmin) * minslot
-                    const uint32_t e = ge & 1;
-                    if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const float4 *ddd = reinterpret_cast<const float4 *>(dd) + 8 * cq;
-                    const float4 *ddm = reinterpret_cast<const float4 *>(dd + 128) + 8 * cq;
+                    if constexpr (F::kMin) {
+                        // the min group: total += d * acc + (-dmin) * minslot
+                        const uint32_t e = ge & 1;
+                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const float4 *ddd = reinterpret_cast<const float4 *>(dd) + 8 * cq;
+                        const float4 *ddm = reinterpret_cast<const float4 *>(dd + 128) + 8 * cq;
 #pragma unroll
-                    for (int hv = 0; hv < 2; ++hv) {
-                        float vm[16];
-                        ptx::tmem_ld_32x32b_x16(lane_base + kPair * e * kTN + 32 * cq + 16 * hv, vm);
-                        ptx::tmem_ld_wait();
+                        for (int hv = 0; hv < 2; ++hv) {
+                            float vm[16];
+                            ptx::tmem_ld_32x32b_x16(lane_base + kPair * e * kTN + 32 * cq + 16 * hv, vm);
+                            ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int i4 = 0; i4 < 4; ++i4) {
-                            const float4 d4 = ddd[4 * hv + i4], m4 = ddm[4 * hv + i4];
-                            const int i = 8 * hv + 2 * i4;
-                            tot[i] = __ffma2_rn(make_float2(m4.x, m4.y), make_float2(vm[4 * i4], vm[4 * i4 + 1]),
-                                                __ffma2_rn(make_float2(d4.x, d4.y), acc[i], tot[i]));
-                            tot[i + 1] = __ffma2_rn(make_float2(m4.z, m4.w), make_float2(vm[4 * i4 + 2], vm[4 * i4 + 3]),
-                                                    __ffma2_rn(make_float2(d4.z, d4.w), acc[i + 1], tot[i + 1]));
+                            for (int i4 = 0; i4 < 4; ++i4) {
+                                const float4 d4 = ddd[4 * hv + i4], m4 = ddm[4 * hv + i4];
+                                const int i = 8 * hv + 2 * i4;
+                                tot[i] = __ffma2_rn(make_float2(m4.x, m4.y), make_float2(vm[4 * i4], vm[4 * i4 + 1]),
+                                                    __ffma2_rn(make_float2(d4.x, d4.y), acc[i], tot[i]));
+                                tot[i + 1] = __ffma2_rn(make_float2(m4.z, m4.w), make_float2(vm[4 * i4 + 2], vm[4 * i4 + 3]),
+                                                        __ffma2_rn(make_float2(d4.z, d4.w), acc[i + 1], tot[i + 1]));
+                            }
+                        }
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[e]));
+                        ++ge;
+                    } else {
+                        // Q6_K: total += d * acc, d the weight row's (one per column)
+                        const float4 *ddd = reinterpret_cast<const float4 *>(dd) + 8 * cq;
+#pragma unroll
+                        for (int i4 = 0; i4 < 8; ++i4) {
+                            const float4 d4 = ddd[i4];
+                            tot[2 * i4] = __ffma2_rn(make_float2(d4.x, d4.y), acc[2 * i4], tot[2 * i4]);
+                            tot[2 * i4 + 1] = __ffma2_rn(make_float2(d4.z, d4.w), acc[2 * i4 + 1], tot[2 * i4 + 1]);
                         }
                     }
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[e]));
-                    ++ge;
                 } else {
-                    // Q8_0 / Q6_K: total += (d8 * w) * slot with w the per-row factor of the slot's
-                    // sub-block (Q8_0: the block's d; Q6_K: d * sc), two columns per packed op
+                    // Q8_0 / Q4_0: total += (d8 * w) * slot with w the block's d of the slot's
+                    // row, two columns per packed op
 #pragma unroll
                     for (int j = 0; j < kGroups; ++j) {
                         const uint32_t e = ge & 1;

@@ -70,6 +70,12 @@ cudaError_t launch_gemv_id(qmm_type t, const void *W, int64_t n_experts, int64_t
                            int64_t x_div, const int32_t *ids, int64_t n_pairs, float *y, int *status,
                            cudaStream_t st);
 
+// Multi-column GEMV on the warp-level MMA (Q4_K, 2 <= m <= 8, q8_1 activations): 16 weight
+// rows x 8 columns per mma.sync m16n8k16 on exact integer operands, then the fp32 fold.
+bool gemv_mma_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
+cudaError_t launch_gemv_mma(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
+                            cudaStream_t st);
+
 // Tensor-core path for skinny activations (Q4_K, 1 <= m <= 16): weights as the MMA's
 // 128-row M side, activations as N = 16; stream-K over (row tile, superblock) units.
 bool gemv_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m);

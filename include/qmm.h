@@ -348,7 +348,8 @@ QMM_API int qmm_gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int32_t ncols
 /* Path override for qmm_mul_mat: 0 = automatic, 1 = GEMV for any m <= 64,
  * 2 = the CUDA-core (dp4a) tiled GEMM, 3 = the tensor-core GEMM for any m,
  * 4 = GEMV for any m <= 64 with direct global loads only (no bulk copies),
- * 5 = the skinny tensor-core path (Q4_K, m <= 16).  A forced path that does not
+ * 5 = the skinny tensor-core path (Q4_K, m <= 16), 6 = the multi-column mma.sync GEMV
+ * (Q4_K, 2 <= m <= 8).  A forced path that does not
  * support the call's type or sizes falls back to the automatic choice. */
 QMM_API void qmm_set_force_path(int path);
 
