@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qmm_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle_qmm.so")
 
-TYPES = {"q4_0": 2, "q8_0": 8, "q4_K": 12, "q6_K": 14}
+TYPES = {"q4_0": 2, "q8_0": 8, "q4_K": 12, "q5_K": 13, "q6_K": 14}
 _lib = None
 
 
@@ -60,6 +60,7 @@ def load(path: str):
     L.oracle_block_bytes.argtypes = [ctypes.c_int]
     L.oracle_block_elems.argtypes = [ctypes.c_int]
     L.oracle_q4_K_fields.argtypes = [P, P, P, P, P, P]
+    L.oracle_q5_K_fields.argtypes = [P, P, P, P, P, P]
     L.oracle_q6_K_fields.argtypes = [P, P, P, P]
     L.oracle_dequant.argtypes = [ctypes.c_int, P, I64, I64, P]
     L.oracle_mul_mat.argtypes = [ctypes.c_int, P, I64, I64, P, I64, P, P]
@@ -144,6 +145,17 @@ def q4_K_fields(blk: np.ndarray):
     return d.value, dmin.value, sc, mn, q
 
 
+def q5_K_fields(blk: np.ndarray):
+    blk = _u8(blk)
+    d = ctypes.c_double()
+    dmin = ctypes.c_double()
+    sc = np.empty(8, np.int32)
+    mn = np.empty(8, np.int32)
+    q = np.empty(256, np.int32)
+    lib().oracle_q5_K_fields(_p(blk), ctypes.byref(d), ctypes.byref(dmin), _p(sc), _p(mn), _p(q))
+    return d.value, dmin.value, sc, mn, q
+
+
 def q6_K_fields(blk: np.ndarray):
     blk = _u8(blk)
     d = ctypes.c_double()
@@ -212,6 +224,27 @@ def repack_glu(W_gate, W_up) -> np.ndarray:
     out = np.empty((2 * g.shape[0], g.shape[1]), dtype=np.uint8)
     out[0::2] = g
     out[1::2] = u
+    return out
+
+
+def aligned_row_bytes(fmt: str, k: int) -> int:
+    """Row stride of the padded layout: the row's k/QK blocks rounded up to whole 16-byte
+    units, for Q6_K after 14 more bytes (a superblock's 16-byte-aligned 224-byte copy window
+    can reach 14 bytes past the row's last block)."""
+    rb = (k // block_elems(fmt)) * block_bytes(fmt)
+    return -(-(rb + (14 if fmt == "q6_K" else 0)) // 16) * 16
+
+
+def repack_aligned(W, fmt, n, k) -> np.ndarray:
+    """W [n][k/QK blocks] as rows of aligned_row_bytes bytes: the blocks unchanged, the
+    rest of each row zero (the one-time repack of [QMM] section "Q4K 的 8 列重排", here
+    only a change of row stride)."""
+    W = _u8(W).reshape(n, -1)
+    rb = (k // block_elems(fmt)) * block_bytes(fmt)
+    if W.shape[1] != rb:
+        raise ValueError("W must be [n][row bytes]")
+    out = np.zeros((n, aligned_row_bytes(fmt, k)), dtype=np.uint8)
+    out[:, :rb] = W
     return out
 
 

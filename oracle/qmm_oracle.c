@@ -25,6 +25,11 @@
  *     Nibbles: 4 chunks of 32 bytes; in chunk c byte l holds weight 64c+l in its low
  *     nibble and weight 64c+32+l in its high nibble ([MMQ] "dp4a 路径的 Q4_K":
  *     sub-block i of a 32-bit word takes nibble i).
+ *   - Q5_K block = {fp16 d, fp16 dmin, 12 B packed 6-bit scales/mins, qh[32], qs[128]}
+ *     (176 B).  [MMQ] section "Q4_K: 在加载期就把两层 scale 合并成 half2" says Q4_K and
+ *     Q5_K share the 12-byte scale/min rule; the rest is read as Q4_K plus one bit plane:
+ *     qs holds the low 4 bits in Q4_K's nibble order, and the fifth bit of weight 32j + l
+ *     (sub-block j, l = 0..31) is bit j of qh[l]; value d*sc*q - dmin*m with q in 0..31.
  *   - Q6_K block = {ql[128], qh[64], int8 sc[16], fp16 d}; bit placement as pinned by
  *     the index arithmetic in [MMQ] "Q6_K: 6 位数据要多占一半的共享内存"; code - 32.
  *   - Q8_0 block = {fp16 d, int8 q[32]}.
@@ -49,7 +54,7 @@
 
 #define ORACLE_API __attribute__((visibility("default")))
 
-enum { OT_Q4_0 = 2, OT_Q8_0 = 8, OT_Q4_K = 12, OT_Q6_K = 14 };
+enum { OT_Q4_0 = 2, OT_Q8_0 = 8, OT_Q4_K = 12, OT_Q5_K = 13, OT_Q6_K = 14 };
 
 /* ---------------------------------------------------------------- fp16 */
 
@@ -154,6 +159,7 @@ static int block_elems(int type) { return type == OT_Q8_0 || type == OT_Q4_0 ? 3
 static int block_bytes(int type) {
     switch (type) {
     case OT_Q4_K: return 144;
+    case OT_Q5_K: return 176;
     case OT_Q6_K: return 210;
     case OT_Q8_0: return 34;
     case OT_Q4_0: return 18;
@@ -182,6 +188,16 @@ static int q4k_code(const uint8_t *blk, int i) {
     return t < 32 ? (qs[32 * c + t] & 0x0f) : (qs[32 * c + t - 32] >> 4);
 }
 
+/* Q5_K weight i (0..255): its 5-bit code, the Q4_K-ordered nibble of qs plus bit i/32 of
+ * qh[i%32] as the fifth bit. */
+static int q5k_code(const uint8_t *blk, int i) {
+    const uint8_t *qh = blk + 16, *qs = blk + 48;
+    int c = i / 64, t = i % 64;
+    int low = t < 32 ? (qs[32 * c + t] & 0x0f) : (qs[32 * c + t - 32] >> 4);
+    int high = (qh[i % 32] >> (i / 32)) & 1;
+    return low | (high << 4);
+}
+
 /* Q6_K weight i (0..255): its code minus 32, in -32..31. */
 static int q6k_value(const uint8_t *blk, int i) {
     const uint8_t *ql = blk, *qh = blk + 128;
@@ -206,6 +222,14 @@ ORACLE_API int oracle_q4_K_fields(const uint8_t *blk, double *d, double *dmin, i
     return 0;
 }
 
+ORACLE_API int oracle_q5_K_fields(const uint8_t *blk, double *d, double *dmin, int *sc8, int *mn8, int *q256) {
+    *d = h2d(blk);
+    *dmin = h2d(blk + 2);
+    for (int j = 0; j < 8; ++j) q4k_scale_min(blk + 4, j, &sc8[j], &mn8[j]);
+    for (int i = 0; i < 256; ++i) q256[i] = q5k_code(blk, i);
+    return 0;
+}
+
 ORACLE_API int oracle_q6_K_fields(const uint8_t *blk, double *d, int *sc16, int *q256) {
     *d = h2d(blk + 208);
     for (int j = 0; j < 16; ++j) sc16[j] = (int8_t)blk[192 + j];
@@ -224,12 +248,13 @@ ORACLE_API int oracle_dequant(int type, const uint8_t *W, int64_t n, int64_t k, 
         for (int64_t b = 0; b < nb; ++b) {
             const uint8_t *blk = W + (r * nb + b) * bb;
             double *o = out + r * k + b * qk;
-            if (type == OT_Q4_K) {
+            if (type == OT_Q4_K || type == OT_Q5_K) {
                 double d = h2d(blk), dmin = h2d(blk + 2);
                 for (int i = 0; i < 256; ++i) {
                     int sc, mn;
                     q4k_scale_min(blk + 4, i / 32, &sc, &mn);
-                    o[i] = d * sc * q4k_code(blk, i) - dmin * mn;
+                    int q = type == OT_Q4_K ? q4k_code(blk, i) : q5k_code(blk, i);
+                    o[i] = d * sc * q - dmin * mn;
                 }
             } else if (type == OT_Q6_K) {
                 double d = h2d(blk + 208);
@@ -253,6 +278,7 @@ ORACLE_API int oracle_dequant(int type, const uint8_t *W, int64_t n, int64_t k, 
  *
  * Q4_K ([MMQ] "dp4a 路径的 Q4_K"): per 32-wide sub-block b of a superblock,
  *     d*sc_b*d8_b*sumi_b - dmin*m_b*s8_b.
+ * Q5_K: the same with the 5-bit codes.
  * Q6_K ([MMQ] "Q6_K: 子块尺度与 q8_1 块长错位"): per 16-wide sub-block j,
  *     d*sc_j*d8_{j/2}*sumi_j.
  * Q8_0: per 32-block, d_w*d8*sumi.
@@ -260,9 +286,10 @@ ORACLE_API int oracle_dequant(int type, const uint8_t *W, int64_t n, int64_t k, 
  */
 static void fold_one(int type, const uint8_t *wrow, const uint8_t *xrow, int64_t k, double *y, double *T) {
     double acc = 0.0, tabs = 0.0;
-    if (type == OT_Q4_K) {
+    if (type == OT_Q4_K || type == OT_Q5_K) {
+        const int bb = type == OT_Q4_K ? 144 : 176;
         for (int64_t s = 0; s < k / 256; ++s) {
-            const uint8_t *blk = wrow + s * 144;
+            const uint8_t *blk = wrow + s * bb;
             double d = h2d(blk), dmin = h2d(blk + 2);
             for (int b = 0; b < 8; ++b) {
                 const uint8_t *xb = xrow + (s * 8 + b) * 36;
@@ -270,7 +297,10 @@ static void fold_one(int type, const uint8_t *wrow, const uint8_t *xrow, int64_t
                 int sc, mn;
                 q4k_scale_min(blk + 4, b, &sc, &mn);
                 int64_t sumi = 0;
-                for (int i = 0; i < 32; ++i) sumi += (int64_t)q4k_code(blk, 32 * b + i) * (int8_t)xb[4 + i];
+                for (int i = 0; i < 32; ++i) {
+                    int q = type == OT_Q4_K ? q4k_code(blk, 32 * b + i) : q5k_code(blk, 32 * b + i);
+                    sumi += (int64_t)q * (int8_t)xb[4 + i];
+                }
                 double t1 = d * sc * d8 * (double)sumi;
                 double t2 = dmin * mn * s8;
                 acc += t1 - t2;

@@ -33,8 +33,8 @@ import numpy as np
 QK_K = 256
 QK8_0 = 32
 QK8_1 = 32
-BLOCK_BYTES = {"q4_K": 144, "q6_K": 210, "q8_0": 34, "q4_0": 18}
-BLOCK_ELEMS = {"q4_K": QK_K, "q6_K": QK_K, "q8_0": QK8_0, "q4_0": QK8_0}
+BLOCK_BYTES = {"q4_K": 144, "q5_K": 176, "q6_K": 210, "q8_0": 34, "q4_0": 18}
+BLOCK_ELEMS = {"q4_K": QK_K, "q5_K": QK_K, "q6_K": QK_K, "q8_0": QK8_0, "q4_0": QK8_0}
 Q8_1_BLOCK_BYTES = 36
 
 
@@ -64,6 +64,19 @@ def gen_q4_K(rng, n: int, k: int, d_range=(1e-4, 1e-3), dmin_range=(1e-4, 1e-3))
     blk[:, :, 0:2] = _fp16_uniform(rng, (n, nb), *d_range).view(np.uint8).reshape(n, nb, 2)
     blk[:, :, 2:4] = _fp16_uniform(rng, (n, nb), *dmin_range).view(np.uint8).reshape(n, nb, 2)
     return blk.reshape(n, nb * 144)
+
+
+def gen_q5_K(rng, n: int, k: int, d_range=(1e-4, 1e-3), dmin_range=(1e-4, 1e-3)) -> np.ndarray:
+    """Random Q5_K matrix as uint8 of shape (n, k/256*176): the Q4_K recipe (d, dmin fp16
+    uniform, every 12-byte scale pattern, uniform nibbles) with a uniform fifth-bit plane."""
+    nb = k // QK_K
+    if k % QK_K:
+        raise ValueError("k must be a multiple of 256 for Q5_K")
+    blk = np.empty((n, nb, 176), dtype=np.uint8)
+    blk[:, :, 4:] = rng.integers(0, 256, size=(n, nb, 172), dtype=np.uint8)
+    blk[:, :, 0:2] = _fp16_uniform(rng, (n, nb), *d_range).view(np.uint8).reshape(n, nb, 2)
+    blk[:, :, 2:4] = _fp16_uniform(rng, (n, nb), *dmin_range).view(np.uint8).reshape(n, nb, 2)
+    return blk.reshape(n, nb * 176)
 
 
 def gen_q6_K(rng, n: int, k: int, d_range=(1e-5, 1e-4), sc_range=(-64, 63)) -> np.ndarray:
@@ -100,7 +113,7 @@ def gen_q4_0(rng, n: int, k: int, d_range=(1e-3, 1e-2)) -> np.ndarray:
     return blk.reshape(n, nb * 18)
 
 
-GEN = {"q4_K": gen_q4_K, "q6_K": gen_q6_K, "q8_0": gen_q8_0, "q4_0": gen_q4_0}
+GEN = {"q4_K": gen_q4_K, "q5_K": gen_q5_K, "q6_K": gen_q6_K, "q8_0": gen_q8_0, "q4_0": gen_q4_0}
 
 
 def gen_weights(fmt: str, rng, n: int, k: int) -> np.ndarray:

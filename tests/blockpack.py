@@ -11,6 +11,8 @@ forms.  They hold no matmul arithmetic.
   of bytes 8..11, and the top 2 bits of scale / min in the top 2 bits of bytes
   0..3 / 4..7.  Nibbles: weight 64c + l is the low nibble of qs byte 32c + l and
   weight 64c + 32 + l its high nibble (c = 0..3, l = 0..31).
+* Q5_K: {fp16 d, fp16 dmin, 12 B scales/mins, qh[32], qs[128]}: Q4_K's scale rule and
+  nibble order for the low 4 bits; the fifth bit of weight 32j + l is bit j of qh[l].
 * Q6_K: {ql[128], qh[64], int8 sc[16], fp16 d}.  Weight 128h + 32t + l (h = 0..1,
   t = 0..3, l = 0..31) takes its low 4 bits from ql[64h + 32(t&1) + l] (low nibble
   for t < 2, high nibble for t >= 2) and its high 2 bits from bits 2t..2t+1 of
@@ -49,6 +51,22 @@ def pack_q4_K(d: float, dmin: float, sc: np.ndarray, mn: np.ndarray, q: np.ndarr
         for l in range(32):
             qs[32 * c + l] = q[64 * c + l] | (q[64 * c + 32 + l] << 4)
     b[16:] = qs.astype(np.uint8)
+    return b
+
+
+def pack_q5_K(d: float, dmin: float, sc: np.ndarray, mn: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """q: 256 codes in 0..31.  Q4_K's layout for the low 4 bits (and the scales), with the
+    fifth bit of weight 32j + l in bit j of qh[l]: {d, dmin, 12 B scales, qh[32], qs[128]}."""
+    q = np.asarray(q, dtype=np.int64)
+    assert q.shape == (256,) and q.min() >= 0 and q.max() < 32
+    b4 = pack_q4_K(d, dmin, sc, mn, q & 15)
+    qh = np.zeros(32, dtype=np.int64)
+    for i in range(256):
+        qh[i % 32] |= (q[i] >> 4) << (i // 32)
+    b = np.zeros(176, dtype=np.uint8)
+    b[0:16] = b4[0:16]
+    b[16:48] = qh.astype(np.uint8)
+    b[48:] = b4[16:]
     return b
 
 

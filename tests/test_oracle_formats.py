@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import qmm_synth
-from blockpack import pack_q4_0, pack_q4_K, pack_q6_K, pack_q8_0, pack_q8_1, unpack_q8_1
+from blockpack import pack_q4_0, pack_q4_K, pack_q5_K, pack_q6_K, pack_q8_0, pack_q8_1, unpack_q8_1
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -40,8 +40,10 @@ def test_block_sizes_match_pages(oracle_mod):
     q40 = n * (k // oracle_mod.block_elems("q4_0")) * oracle_mod.block_bytes("q4_0")
     assert round(q40 / 1e6, 1) == mb["q4_0"]
     assert oracle_mod.block_elems("q4_0") == 32
-    for fmt in ("q4_K", "q6_K", "q8_0", "q4_0"):
+    for fmt in ("q4_K", "q5_K", "q6_K", "q8_0", "q4_0"):
         assert qmm_synth.BLOCK_BYTES[fmt] == oracle_mod.block_bytes(fmt)
+    # Q5_K: Q4_K's 144 bytes plus a 32-byte plane of fifth bits (one per weight)
+    assert oracle_mod.block_bytes("q5_K") == oracle_mod.block_bytes("q4_K") + 256 // 8
 
 
 # ---------------------------------------------------------------- fp16
@@ -248,3 +250,59 @@ def test_q4_0_decode_all_codes(oracle_mod):
     q = np.concatenate([np.arange(16), np.arange(15, -1, -1)])
     w = oracle_mod.dequant(pack_q4_0(-0.5, q), "q4_0", 1, 32)[0]
     assert np.array_equal(w, -0.5 * (q - 8))
+
+
+# ---------------------------------------------------------------- padded rows
+
+@pytest.mark.parametrize("fmt,k", [("q6_K", 5120), ("q6_K", 1280), ("q8_0", 5120), ("q8_0", 96), ("q4_0", 224),
+                                   ("q4_K", 4096)])
+def test_repack_aligned_round_trip(oracle_mod, fmt, k):
+    """The padded rows hold the original blocks byte for byte, then zeros; the stride is a
+    whole number of 16-byte units, and for Q6_K every superblock's 224-byte copy window
+    (from the 16-byte boundary at or below the superblock) ends inside its own row."""
+    rng = np.random.default_rng(k)
+    n = 7
+    W = qmm_synth.gen_weights(fmt, rng, n, k)
+    rb = (k // oracle_mod.block_elems(fmt)) * oracle_mod.block_bytes(fmt)
+    stride = oracle_mod.aligned_row_bytes(fmt, k)
+    A = oracle_mod.repack_aligned(W, fmt, n, k)
+    assert A.shape == (n, stride) and stride % 16 == 0 and rb <= stride < rb + 16 + (14 if fmt == "q6_K" else 0)
+    assert np.array_equal(A[:, :rb], W.reshape(n, rb)) and not A[:, rb:].any()
+    if fmt == "q6_K":
+        for sb in range(k // 256):
+            assert (210 * sb) // 16 * 16 + 224 <= stride
+    yA, TA = oracle_mod.mul_mat(A[:, :rb].copy(), fmt, n, k, oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, 2, k)), 2)
+    assert np.all(np.isfinite(yA))
+
+
+# ---------------------------------------------------------------- Q5_K
+
+def test_q5_K_raw_bit_positions(oracle_mod):
+    """Raw bytes, no packer: with every scale 1 and d = 1, qs byte 32c + l gives weights
+    64c + l (low nibble) and 64c + 32 + l (high nibble), and bit j of qh[l] adds 16 to
+    weight 32j + l and to no other."""
+    blk = np.zeros(176, np.uint8)
+    blk[0:2] = np.array([1.0], np.float16).view(np.uint8)
+    blk[4:8] = 1                       # sc[0..3] = 1, mins 0
+    blk[12:16] = 1                     # sc[4..7] = 1
+    c, l = 1, 5
+    blk[48 + 32 * c + l] = 0x72        # low nibble 2, high nibble 7
+    j, l2 = 6, 20
+    blk[16 + l2] = 1 << j              # fifth bit of weight 32j + l2
+    w = oracle_mod.dequant(blk, "q5_K", 1, 256)[0]
+    nz = sorted(np.nonzero(w)[0])
+    assert nz == sorted([64 * c + l, 64 * c + 32 + l, 32 * j + l2])
+    assert w[64 * c + l] == 2 and w[64 * c + 32 + l] == 7 and w[32 * j + l2] == 16
+
+
+def test_q5_K_fields_roundtrip(oracle_mod):
+    rng = np.random.default_rng(15)
+    for _ in range(20):
+        q = rng.integers(0, 32, 256)
+        sc, mn = rng.integers(0, 64, 8), rng.integers(0, 64, 8)
+        blk = pack_q5_K(0.5, 0.25, sc, mn, q)
+        d, dmin, sc2, mn2, q2 = oracle_mod.q5_K_fields(blk)
+        assert (d, dmin) == (0.5, 0.25) and np.array_equal(sc2, sc) and np.array_equal(mn2, mn)
+        assert np.array_equal(q2, q)
+        w = oracle_mod.dequant(blk, "q5_K", 1, 256)[0]
+        assert np.array_equal(w, 0.5 * np.repeat(sc, 32) * q - 0.25 * np.repeat(mn, 32))

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import qmm_synth
-from blockpack import pack_q4_0, pack_q4_K, pack_q6_K, pack_q8_0, pack_q8_1
+from blockpack import pack_q4_0, pack_q4_K, pack_q5_K, pack_q6_K, pack_q8_0, pack_q8_1
 
 
 def _q8_1_rows(q: np.ndarray, d: np.ndarray, s: np.ndarray) -> np.ndarray:
@@ -177,6 +177,43 @@ def test_32_block_tolerance_sum_closed_form(oracle_mod, fmt):
     assert np.all(np.abs(y - t.sum(axis=2)) <= 1e-14 * T)
 
 
+def test_q5_K_integer_matmul_special_case(oracle_mod):
+    """d = 1, dmin = 0, all sub-block scales 1 and q8_1 d = 1: the fold is the integer
+    matmul of the 5-bit codes with the int8 activations."""
+    rng = np.random.default_rng(26)
+    n, k, m = 5, 512, 3
+    Qw = rng.integers(0, 32, (n, k))
+    W = np.stack([np.concatenate([pack_q5_K(1.0, 0.0, np.ones(8, int), rng.integers(0, 64, 8),
+                                            Qw[r, 256 * s:256 * s + 256]) for s in range(k // 256)]) for r in range(n)])
+    Qx = rng.integers(-127, 128, (m, k))
+    xq = _q8_1_rows(Qx, np.ones((m, k // 32)), rng.uniform(-3, 3, (m, k // 32)))
+    y, T = oracle_mod.mul_mat(W, "q5_K", n, k, xq, m)
+    assert np.array_equal(y, (Qx @ Qw.T).astype(np.float64))
+
+
+def test_q5_K_tolerance_sum_and_min_term(oracle_mod):
+    """Q5_K with non-unit power-of-two d, dmin, d8 and fp16 s: y and T in closed form,
+    T = sum_b |d sc_b d8_b sumi_b| + |dmin m_b s_b|."""
+    rng = np.random.default_rng(29)
+    n, k, m = 4, 512, 3
+    nsb = k // 256
+    D, DM = _pow2(rng, -6, 1, (n, nsb)), _pow2(rng, -6, 1, (n, nsb))
+    SC, MN = rng.integers(0, 64, (n, k // 32)), rng.integers(0, 64, (n, k // 32))
+    Qw = rng.integers(0, 32, (n, k))
+    W = np.stack([np.concatenate([pack_q5_K(D[r, s], DM[r, s], SC[r, 8 * s:8 * s + 8], MN[r, 8 * s:8 * s + 8],
+                                            Qw[r, 256 * s:256 * s + 256]) for s in range(nsb)]) for r in range(n)])
+    Qx = rng.integers(-127, 128, (m, k))
+    D8 = _pow2(rng, -8, -1, (m, k // 32))
+    S8 = rng.uniform(-4, 4, (m, k // 32)).astype(np.float16).astype(np.float64)
+    xq = _q8_1_rows(Qx, D8, S8)
+    y, T = oracle_mod.mul_mat(W, "q5_K", n, k, xq, m)
+    sumi = np.einsum("mbi,nbi->mnb", Qx.reshape(m, -1, 32), Qw.reshape(n, -1, 32))
+    t1 = np.repeat(D, 8, axis=1)[None] * SC[None] * D8[:, None, :] * sumi
+    t2 = np.repeat(DM, 8, axis=1)[None] * MN[None] * S8[:, None, :]
+    np.testing.assert_allclose(T, (np.abs(t1) + np.abs(t2)).sum(axis=2), rtol=1e-15, atol=0)
+    assert np.all(np.abs(y - (t1 - t2).sum(axis=2)) <= 1e-14 * T)
+
+
 @pytest.mark.parametrize("fmt", ["q6_K", "q8_0", "q4_0"])
 def test_brute_force_agrees(oracle_mod, fmt):
     """Without a min term the fold equals the fp64 matmul of dequantized W and
@@ -208,15 +245,16 @@ def test_brute_force_agrees_q4_K_exact_s(oracle_mod):
     assert np.all(np.abs(yA - yB) <= 1e-12 * T)
 
 
-def test_brute_force_q4_K_s_rounding_bound(oracle_mod):
-    """Q4_K with quantized activations: the fold uses the stored fp16 s, the brute
+@pytest.mark.parametrize("fmt", ["q4_K", "q5_K"])
+def test_brute_force_q4_K_s_rounding_bound(oracle_mod, fmt):
+    """Q4_K and Q5_K with quantized activations: the fold uses the stored fp16 s, the brute
     force d*sum(q); they differ by at most the fp16 rounding of s in the min terms."""
     rng = np.random.default_rng(33)
     n, k, m = 8, 1024, 3
-    W = qmm_synth.gen_q4_K(rng, n, k)
+    W = qmm_synth.gen_weights(fmt, rng, n, k)
     xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, m, k))
-    yA, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
-    yB = oracle_mod.brute(W, "q4_K", n, k, xq, m)
+    yA, T = oracle_mod.mul_mat(W, fmt, n, k, xq, m)
+    yB = oracle_mod.brute(W, fmt, n, k, xq, m)
     assert np.all(np.abs(yA - yB) <= 2.0 ** -10 * T)
 
 

@@ -67,6 +67,15 @@ MUTATIONS = [
      "uint16_t sh = oracle_float_to_half(dhf * (float)S);",
      "uint16_t sh = oracle_float_to_half(d * (float)S);",
      [lambda o: F.test_q8_1_invariants(o, "normal"), lambda o: F.test_q8_1_invariants(o, "adversarial")]),
+    ("Q5_K fifth bit taken from bit l % 8 of qh[i / 8] instead of bit i / 32 of qh[i % 32]",
+     "int high = (qh[i % 32] >> (i / 32)) & 1;", "int high = (qh[i / 8] >> (i % 8)) & 1;",
+     [F.test_q5_K_raw_bit_positions, F.test_q5_K_fields_roundtrip, M.test_q5_K_integer_matmul_special_case]),
+    ("Q5_K fifth bit worth 32 instead of 16",
+     "return low | (high << 4);", "return low | (high << 5);",
+     [F.test_q5_K_raw_bit_positions, M.test_q5_K_integer_matmul_special_case]),
+    ("Q5_K codes read at Q4_K's nibble offset (the qh plane ignored)",
+     "const uint8_t *qh = blk + 16, *qs = blk + 48;", "const uint8_t *qh = blk + 16, *qs = blk + 16;",
+     [F.test_q5_K_raw_bit_positions, M.test_q5_K_integer_matmul_special_case]),
     # the tolerance sum T, which scales every parity bound: a slip that inflates it would
     # loosen every GPU comparison without failing any of them
     ("T taken as |y| instead of the sum of |block terms|",
