@@ -18,8 +18,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqmm.so")
 
-TYPES = {"q4_0": 2, "q8_0": 8, "q4_K": 12, "q6_K": 14}
-BLOCK = {"q4_0": (32, 18), "q8_0": (32, 34), "q4_K": (256, 144), "q6_K": (256, 210)}
+TYPES = {"q4_0": 2, "q8_0": 8, "q4_K": 12, "q5_K": 13, "q6_K": 14}
+BLOCK = {"q4_0": (32, 18), "q8_0": (32, 34), "q4_K": (256, 144), "q5_K": (256, 176), "q6_K": (256, 210)}
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_ARG", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_TYPE", 4: "QMM_ERR_ALIGN",
           5: "QMM_ERR_WORKSPACE", 6: "QMM_ERR_CUDA", 7: "QMM_ERR_IDS", 8: "QMM_ERR_DEVICE"}
 PATH_AUTO, PATH_GEMV, PATH_GEMM_DP4A, PATH_GEMM_TC, PATH_GEMV_DIRECT, PATH_GEMV_TC, PATH_GEMV_MMA = 0, 1, 2, 3, 4, 5, 6
@@ -31,7 +31,8 @@ EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspac
            "qmm_mul_mat_id_noalloc", "qmm_noalloc_scratch_bytes", "qmm_workspace_bytes_f32", "qmm_mul_mat_f32",
            "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu", "qmm_gemv_ring_stages",
            "qmm_repack_glu", "qmm_mul_mat_glu_packed", "qmm_workspace_bytes_f32_host", "qmm_mul_mat_f32_host",
-           "qmm_get_device_status", "qmm_set_test_fault")
+           "qmm_get_device_status", "qmm_set_test_fault", "qmm_aligned_row_bytes", "qmm_repack_aligned",
+           "qmm_workspace_bytes_aligned", "qmm_mul_mat_aligned")
 
 
 class QMMError(RuntimeError):
@@ -90,6 +91,14 @@ def lib():
     L.qmm_plan_cta_range.argtypes = [ctypes.POINTER(GemmPlan), I32, ctypes.POINTER(I64), ctypes.POINTER(I64)]
     L.qmm_set_force_path.restype = None
     L.qmm_set_force_path.argtypes = [ctypes.c_int]
+    L.qmm_aligned_row_bytes.restype = SZ
+    L.qmm_aligned_row_bytes.argtypes = [ctypes.c_int, I64]
+    L.qmm_repack_aligned.restype = ctypes.c_int
+    L.qmm_repack_aligned.argtypes = [P, ctypes.c_int, I64, I64, P, P]
+    L.qmm_workspace_bytes_aligned.restype = SZ
+    L.qmm_workspace_bytes_aligned.argtypes = [ctypes.c_int, I64, I64, I64]
+    L.qmm_mul_mat_aligned.restype = ctypes.c_int
+    L.qmm_mul_mat_aligned.argtypes = [P, ctypes.c_int, I64, I64, P, I64, P, P, SZ, P]
     L.qmm_set_test_fault.restype = None
     L.qmm_set_test_fault.argtypes = [ctypes.c_int]
     L.qmm_set_stream_k_mode.restype = None
@@ -194,6 +203,44 @@ def qmm_mul_mat(W: torch.Tensor, qtype, n: int, k: int, xq: torch.Tensor, m: int
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().qmm_mul_mat(_ptr(W), _qtype(qtype), n, k, _ptr(xq), m, _ptr(y), _ptr(workspace), ws_bytes,
                              _stream(stream)), "qmm_mul_mat")
+    return y
+
+
+def qmm_aligned_row_bytes(qtype, k: int) -> int:
+    return int(lib().qmm_aligned_row_bytes(_qtype(qtype), k))
+
+
+def qmm_repack_aligned(W: torch.Tensor, qtype, n: int, k: int, W_aligned: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """W with its rows padded to whole 16-byte units: uint8 [n, qmm_aligned_row_bytes]."""
+    _dev(W, "W")
+    if W_aligned is None:
+        W_aligned = torch.empty((n, qmm_aligned_row_bytes(qtype, k)), dtype=torch.uint8, device=W.device)
+    _dev(W_aligned, "W_aligned")
+    _check(lib().qmm_repack_aligned(_ptr(W), _qtype(qtype), n, k, _ptr(W_aligned), _stream(stream)),
+           "qmm_repack_aligned")
+    return W_aligned
+
+
+def qmm_workspace_bytes_aligned(qtype, n: int, k: int, m: int) -> int:
+    return int(lib().qmm_workspace_bytes_aligned(_qtype(qtype), n, k, m))
+
+
+def qmm_mul_mat_aligned(W_aligned: torch.Tensor, qtype, n: int, k: int, xq: torch.Tensor, m: int,
+                        y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """qmm_mul_mat on the padded rows of qmm_repack_aligned."""
+    _dev(W_aligned, "W_aligned")
+    _dev(xq, "xq")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=W_aligned.device)
+    _dev(y, "y", torch.float32)
+    need = qmm_workspace_bytes_aligned(qtype, n, k, m)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=W_aligned.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().qmm_mul_mat_aligned(_ptr(W_aligned), _qtype(qtype), n, k, _ptr(xq), m, _ptr(y), _ptr(workspace),
+                                     ws_bytes, _stream(stream)), "qmm_mul_mat_aligned")
     return y
 
 

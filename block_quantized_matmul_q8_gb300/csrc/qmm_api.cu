@@ -3,6 +3,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -72,7 +73,9 @@ int device_smem_optin() {
     return v;
 }
 
-static bool type_ok(qmm_type t) { return t == QMM_Q4_K || t == QMM_Q6_K || t == QMM_Q8_0 || t == QMM_Q4_0; }
+static bool type_ok(qmm_type t) {
+    return t == QMM_Q4_K || t == QMM_Q5_K || t == QMM_Q6_K || t == QMM_Q8_0 || t == QMM_Q4_0;
+}
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -96,18 +99,20 @@ int test_fault_mode() { return g_test_fault.load(std::memory_order_relaxed); }
 
 bool gemv_tma_enabled() { return g_force_path.load(std::memory_order_relaxed) != kGemvDirect; }
 
-static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
+// stride: the row stride of padded rows (qmm_repack_aligned), 0 for natural rows.
+static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t stride = 0) {
     const int force = g_force_path.load(std::memory_order_relaxed);
     const bool gemv_fits = gemv_smem_bytes(k, 1) <= size_t(device_smem_optin());
     if ((force == kGemv || force == kGemvDirect) && gemv_fits && m <= 64) return kGemv;
     if (force == kGemmDp4a) return kGemmDp4a;
-    if (force == kGemmTc && gemm_tc_supported(t, n, k, m)) return kGemmTc;
+    if (force == kGemmTc && gemm_tc_supported(t, n, k, m, stride)) return kGemmTc;
     if (force == kGemvTc && gemv_tc_supported(t, n, k, m)) return kGemvTc;
     if (force == kGemvMma && gemv_mma_supported(t, n, k, m)) return kGemvMma;
     if (m <= 8 && gemv_fits) return kGemv;
-    // skinny activations on the tensor cores (weights as the MMA's M side)
+    // skinny activations on the tensor cores (weights as the MMA's M side; Q4_K, whose rows
+    // are whole 16-byte units and so never padded)
     if (gemv_tc_supported(t, n, k, m)) return kGemvTc;
-    if (gemm_tc_supported(t, n, k, m)) return kGemmTc;
+    if (gemm_tc_supported(t, n, k, m, stride)) return kGemmTc;
     return kGemmDp4a;
 }
 
@@ -115,7 +120,7 @@ static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m) {
 size_t q8_region_bytes(int64_t m, int64_t k) { return ((size_t(m) * size_t(k / 32) * kQ81Bytes) + 255) & ~size_t(255); }
 
 qmm_status mul_mat_q8(const void *W, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                      void *workspace, size_t ws_bytes, cudaStream_t st);
+                      void *workspace, size_t ws_bytes, cudaStream_t st, int64_t stride = 0);
 
 qmm_status moe_check_sizes(qmm_type t, int64_t n_experts, int64_t n, int64_t k, int64_t top_k, int64_t n_tokens) {
     qmm_status s = check_k(t, k);
@@ -172,6 +177,21 @@ __global__ void repack_glu_kernel(const uint8_t *__restrict__ wg, const uint8_t 
             const uint8_t *src = ((row & 1) ? wu : wg) + (row >> 1) * rb;
             reinterpret_cast<uint16_t *>(dst + row * rb)[c] = reinterpret_cast<const uint16_t *>(src)[c];
         }
+    }
+}
+
+// Rows of rb bytes copied to rows of `stride` bytes (a multiple of 16), the tail of each
+// row zero; in units of U bytes, U dividing rb (every block size is even).
+template <int U>
+__global__ void repack_aligned_kernel(const uint8_t *__restrict__ src, int64_t n, int64_t rb, int64_t stride,
+                                      uint8_t *__restrict__ dst) {
+    using V = typename std::conditional<U == 8, uint2, typename std::conditional<U == 4, uint32_t, uint16_t>::type>::type;
+    const int64_t per_row = stride / U, total = n * per_row;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t row = i / per_row, c = i - row * per_row;
+        V v{};
+        if (c * U < rb) v = reinterpret_cast<const V *>(src + row * rb)[c];
+        reinterpret_cast<V *>(dst + row * stride)[c] = v;
     }
 }
 
@@ -408,9 +428,9 @@ qmm_status qmm_mul_mat_f32_host(const void *W, qmm_type t, int64_t n, int64_t k,
 
 namespace qmm {
 qmm_status mul_mat_q8(const void *W, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                      void *workspace, size_t ws_bytes, cudaStream_t st) {
-    switch (choose_path(t, n, k, m)) {
-    case kGemv: return cuda_status(launch_gemv(t, W, n, k, xq, nullptr, m, y, st));
+                      void *workspace, size_t ws_bytes, cudaStream_t st, int64_t stride) {
+    switch (choose_path(t, n, k, m, stride)) {
+    case kGemv: return cuda_status(launch_gemv(t, W, n, k, xq, nullptr, m, y, st, stride));
     case kGemvMma: return cuda_status(launch_gemv_mma(t, W, n, k, xq, m, y, st));
     case kGemvTc: {
         const size_t need = gemv_tc_workspace_bytes(t, n, k, m);
@@ -419,15 +439,15 @@ qmm_status mul_mat_q8(const void *W, qmm_type t, int64_t n, int64_t k, const voi
         return cuda_status(launch_gemv_tc(t, W, n, k, xq, m, y, workspace, ws_bytes, st));
     }
     case kGemmTc: {
-        const size_t need = gemm_tc_workspace_bytes(t, n, k, m);
+        const size_t need = gemm_tc_workspace_bytes(t, n, k, m, stride);
         if (need > 0) {
             if (!workspace || ws_bytes < need) return QMM_ERR_WORKSPACE;
             if (!aligned256(workspace)) return QMM_ERR_ALIGN;
         }
         return cuda_status(launch_gemm_tc(t, W, n, k, xq, m, y, workspace, ws_bytes,
-                                          g_stream_k_mode.load(std::memory_order_relaxed), st));
+                                          g_stream_k_mode.load(std::memory_order_relaxed), st, stride));
     }
-    default: return cuda_status(launch_gemm_dp4a(t, W, n, k, xq, m, y, st));
+    default: return cuda_status(launch_gemm_dp4a(t, W, n, k, xq, m, y, st, stride));
     }
 }
 }  // namespace qmm
@@ -458,6 +478,49 @@ qmm_status qmm_read_device_status(const void *workspace, int32_t *status, void *
     if (cudaStreamSynchronize(st) != cudaSuccess) return QMM_ERR_CUDA;
     *status = v;
     return QMM_OK;
+}
+
+size_t qmm_aligned_row_bytes(qmm_type t, int64_t k) { return type_ok(t) ? size_t(aligned_row_bytes(t, k)) : 0; }
+
+size_t qmm_workspace_bytes_aligned(qmm_type t, int64_t n, int64_t k, int64_t m) {
+    if (!type_ok(t) || n < 0 || k <= 0 || m < 0 || check_k(t, k) != QMM_OK) return 0;
+    const int64_t stride = aligned_row_bytes(t, k);
+    const size_t gemm = gemm_tc_supported(t, n, k, m, stride) ? gemm_tc_workspace_bytes(t, n, k, m, stride) : 0;
+    return std::max(gemm, gemv_tc_workspace_bytes(t, n, k, m));
+}
+
+qmm_status qmm_repack_aligned(const void *W, qmm_type t, int64_t n, int64_t k, void *W_aligned, void *stream) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n < 0) return QMM_ERR_ARG;
+    if (n > kMaxRows) return QMM_ERR_SHAPE;
+    if (n == 0) return QMM_OK;
+    if (!W || !W_aligned) return QMM_ERR_ARG;
+    if (!aligned16(W) || !aligned16(W_aligned)) return QMM_ERR_ALIGN;
+    const int64_t rb = int64_t(qmm_row_bytes(t, k)), stride = aligned_row_bytes(t, k);
+    const int unit = rb % 8 == 0 ? 8 : rb % 4 == 0 ? 4 : 2;
+    const int64_t total = n * (stride / unit);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, int64_t(device_sm_count()) * 8));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint8_t *src = static_cast<const uint8_t *>(W);
+    uint8_t *dst = static_cast<uint8_t *>(W_aligned);
+    if (unit == 8) repack_aligned_kernel<8><<<grid, 256, 0, st>>>(src, n, rb, stride, dst);
+    else if (unit == 4) repack_aligned_kernel<4><<<grid, 256, 0, st>>>(src, n, rb, stride, dst);
+    else repack_aligned_kernel<2><<<grid, 256, 0, st>>>(src, n, rb, stride, dst);
+    return cuda_status(cudaGetLastError());
+}
+
+qmm_status qmm_mul_mat_aligned(const void *W_aligned, qmm_type t, int64_t n, int64_t k, const void *xq, int64_t m,
+                               float *y, void *workspace, size_t ws_bytes, void *stream) {
+    qmm_status s = check_k(t, k);
+    if (s != QMM_OK) return s;
+    if (n < 0 || m < 0) return QMM_ERR_ARG;
+    if (n > kMaxRows || m > kMaxRows) return QMM_ERR_SHAPE;
+    if (n == 0 || m == 0) return QMM_OK;
+    if (!W_aligned || !xq || !y) return QMM_ERR_ARG;
+    if (!aligned16(W_aligned) || !aligned16(xq) || !aligned16(y)) return QMM_ERR_ALIGN;
+    return mul_mat_q8(W_aligned, t, n, k, xq, m, y, workspace, ws_bytes, static_cast<cudaStream_t>(stream),
+                      aligned_row_bytes(t, k));
 }
 
 qmm_status qmm_get_device_status(const void *workspace, void *stream) {

@@ -3,6 +3,8 @@
 // Block layouts (see include/qmm.h):
 //   q8_1 36 B: fp16 d | fp16 s | int8 q[32]
 //   Q4_K 144 B: fp16 d | fp16 dmin | 12 B packed 6-bit scales/mins | 128 B nibbles
+//   Q5_K 176 B: fp16 d | fp16 dmin | 12 B scales/mins | qh[32] | 128 B nibbles (the fifth
+//               bit of weight 32j + l is bit j of qh[l])
 //   Q6_K 210 B: ql[128] | qh[64] | int8 sc[16] | fp16 d
 //   Q8_0 34 B: fp16 d | int8 q[32]
 //   Q4_0 18 B: fp16 d | 16 B nibbles (byte i: weight i low, weight 16+i high; d*(q-8))
@@ -28,6 +30,7 @@
 namespace qmm {
 
 constexpr int kQ4KBytes = 144;
+constexpr int kQ5KBytes = 176;
 constexpr int kQ6KBytes = 210;
 constexpr int kQ80Bytes = 34;
 constexpr int kQ40Bytes = 18;
@@ -42,6 +45,7 @@ struct Unit {
 
 __host__ __device__ constexpr int block_bytes(int t) {
     return t == QMM_Q4_K ? kQ4KBytes
+           : t == QMM_Q5_K ? kQ5KBytes
            : t == QMM_Q6_K ? kQ6KBytes
            : t == QMM_Q8_0 ? kQ80Bytes
            : t == QMM_Q4_0 ? kQ40Bytes
@@ -308,12 +312,59 @@ __device__ __forceinline__ void decode_q4_0(const uint8_t *row, int u, bool two,
 
 template <int T> struct Raw;
 template <> struct Raw<QMM_Q4_K> { uint4 h, a, b; };
+template <> struct Raw<QMM_Q5_K> { uint4 h, qh0, qh1, a, b; };
 template <> struct Raw<QMM_Q6_K> { uint32_t ql[17], qh[9], sc[5]; uint32_t shift; };
 template <> struct Raw<QMM_Q8_0> { uint32_t w[18]; uint32_t shift; bool two; };
 template <> struct Raw<QMM_Q4_0> { uint32_t w[10]; uint32_t shift; bool two; };
 
 // units per lane kept in flight by the GEMV
 template <int T> constexpr int kRawChunk = T == QMM_Q4_K ? 5 : T == QMM_Q6_K ? 2 : T == QMM_Q4_0 ? 5 : 3;
+
+// Q5_K unit u (chunk c = u % 4 of superblock u / 4): the codes of Q4_K's nibbles, each with
+// its fifth bit from the qh plane: weights 64c + l (sub-block 2c) take bit 2c of qh[l],
+// weights 64c + 32 + l (sub-block 2c + 1) bit 2c + 1.  a, b: qs bytes 32c..32c+31; q0, q1:
+// qh bytes 0..31.
+__device__ __forceinline__ void q5k_unit(const uint4 &h, const uint4 &q0, const uint4 &q1, const uint4 &a,
+                                         const uint4 &b, int c, Unit &o) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t qh[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        o.q[i] = (int)((w[i] & 0x0f0f0f0fu) | (((qh[i] >> (2 * c)) & 0x01010101u) << 4));
+        o.q[8 + i] = (int)(((w[i] >> 4) & 0x0f0f0f0fu) | (((qh[i] >> (2 * c + 1)) & 0x01010101u) << 4));
+    }
+    const float d = half_lo(h.x), dmin = half_hi(h.x);
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(h.y, h.z, h.w, 2 * c, sc0, m0);
+    q4k_scale_min(h.y, h.z, h.w, 2 * c + 1, sc1, m1);
+    o.isc[0] = o.isc[1] = sc0;
+    o.isc[2] = o.isc[3] = sc1;
+    o.fd[0] = o.fd[1] = d;
+    o.fm[0] = dmin * (float)m0;
+    o.fm[1] = dmin * (float)m1;
+}
+
+// Q5_K rows are whole 16-byte units (176-byte blocks): every load is 16 bytes, aligned.
+__device__ __forceinline__ void decode_q5_K(const uint8_t *row, int u, Unit &o) {
+    const uint8_t *blk = row + (u >> 2) * kQ5KBytes;
+    const int c = u & 3;
+    q5k_unit(ldg16(blk), ldg16(blk + 16), ldg16(blk + 32), ldg16(blk + 48 + 32 * c), ldg16(blk + 64 + 32 * c), c, o);
+}
+
+template <class Ld = LdGlobal>
+__device__ __forceinline__ void load_raw(const uint8_t *row, int u, int, Raw<QMM_Q5_K> &r) {
+    const uint8_t *blk = row + (u >> 2) * kQ5KBytes;
+    const int c = u & 3;
+    r.h = Ld::u128(blk);
+    r.qh0 = Ld::u128(blk + 16);
+    r.qh1 = Ld::u128(blk + 32);
+    r.a = Ld::u128(blk + 48 + 32 * c);
+    r.b = Ld::u128(blk + 64 + 32 * c);
+}
+
+__device__ __forceinline__ void convert_raw(const Raw<QMM_Q5_K> &r, int u, Unit &o) {
+    q5k_unit(r.h, r.qh0, r.qh1, r.a, r.b, u & 3, o);
+}
 
 template <class Ld = LdGlobal>
 __device__ __forceinline__ void load_raw(const uint8_t *row, int u, int, Raw<QMM_Q4_K> &r) {
@@ -479,6 +530,7 @@ __device__ __forceinline__ void convert_raw(const Raw<QMM_Q4_0> &r, int, Unit &o
 template <int T>
 __device__ __forceinline__ void decode_unit(const uint8_t *row, int u, int nblk32, Unit &o) {
     if constexpr (T == QMM_Q4_K) decode_q4_K(row, u, o);
+    else if constexpr (T == QMM_Q5_K) decode_q5_K(row, u, o);
     else if constexpr (T == QMM_Q6_K) decode_q6_K(row, u, o);
     else if constexpr (T == QMM_Q4_0) decode_q4_0(row, u, 2 * u + 1 < nblk32, o);
     else decode_q8_0(row, u, 2 * u + 1 < nblk32, o);

@@ -231,17 +231,18 @@ static cudaError_t launch_dp4a(qmm_type t, const DP4AGemmArgs &args, int64_t tot
     case QMM_Q6_K: return launch_dp4a_t<QMM_Q6_K>(args, total_hint, st);
     case QMM_Q8_0: return launch_dp4a_t<QMM_Q8_0>(args, total_hint, st);
     case QMM_Q4_0: return launch_dp4a_t<QMM_Q4_0>(args, total_hint, st);
+    case QMM_Q5_K: return launch_dp4a_t<QMM_Q5_K>(args, total_hint, st);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_dp4a(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                             cudaStream_t st) {
+                             cudaStream_t st, int64_t stride) {
     DP4AGemmArgs a{};
     a.W = static_cast<const uint8_t *>(W);
     a.n = n;
     a.k = (int)k;
-    a.row_bytes = (k / block_elems(t)) * block_bytes(t);
+    a.row_bytes = stride > 0 ? stride : (k / block_elems(t)) * block_bytes(t);
     a.xq = static_cast<const uint8_t *>(xq);
     a.y = y;
     a.m = m;

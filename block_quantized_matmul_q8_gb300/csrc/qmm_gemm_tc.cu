@@ -97,6 +97,18 @@ template <> struct TcFmt<QMM_Q4_K> : TcStages2 {
     static constexpr uint32_t kDDBytes = 2 * 128 * 4;  // d[128], -dmin[128]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * kQ4KBytes); }
 };
+// Q5_K: Q4_K's superblock with a 32-byte plane of fifth bits (176 bytes, a whole number
+// of 16-byte units, one tensor-map box per superblock); the operand code * sc stays exact
+// in fp16 (31 * 63 = 1953 < 2048).
+template <> struct TcFmt<QMM_Q5_K> : TcStages2 {
+    static constexpr uint32_t kRawRow = kQ5KBytes;
+    static constexpr uint32_t kRawBuf = 128 * kRawRow;
+    static constexpr bool kMin = true, kScaleD = true;
+    static constexpr int kUses = 8;
+    static constexpr int kSub = 32;
+    static constexpr uint32_t kDDBytes = 2 * 128 * 4;  // d[128], -dmin[128]
+    static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * kQ5KBytes); }
+};
 template <> struct TcFmt<QMM_Q8_0> : TcStages2 {
     static constexpr uint32_t kRawRow = 8 * kQ80Bytes;  // 272
     static constexpr uint32_t kRawBuf = 128 * kRawRow;
@@ -551,7 +563,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 if constexpr (T == QMM_Q6_K)  // the superblock's offset inside its window
                     blk += (int)(F::pos(n0w, sb, a.row_bytes) & 15);
                 float *dd = reinterpret_cast<float *>(smem + kOffDD + ri * F::kDDBytes);
-                if constexpr (T == QMM_Q4_K) {
+                if constexpr (T == QMM_Q4_K || T == QMM_Q5_K) {
+                // Q5_K: the nibbles start 32 bytes later, after the plane of fifth bits
+                constexpr int kQs = T == QMM_Q4_K ? 16 : 48;
                 const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
                 // (d, -dmin) for the epilogue
                 dd[r] = half_lo(hd.x);
@@ -567,8 +581,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
 #pragma unroll
                     for (int j2 = 0; j2 < 2; ++j2) {  // slab j2 <-> qs chunk c = 2h + j2
                         const int c = 2 * h + j2;
-                        const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
-                        const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
+                        const uint4 qa = *reinterpret_cast<const uint4 *>(blk + kQs + 32 * c);
+                        const uint4 qb = *reinterpret_cast<const uint4 *>(blk + kQs + 16 + 32 * c);
                         int sc_lo, m_lo, sc_hi, m_hi;
                         q4k_scale_min(hd.y, hd.z, hd.w, 2 * c, sc_lo, m_lo);
                         q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sc_hi, m_hi);
@@ -576,12 +590,27 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         const __half2 s_hi = __float2half2_rn((float)sc_hi), ns_hi = __float2half2_rn(-1024.f * sc_hi);
                         const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
                         uint8_t *rowdst = wst + j2 * kSlabBytes + r * 128;
+                        if constexpr (T == QMM_Q4_K) {
 #pragma unroll
-                        for (int cq = 0; cq < 4; ++cq) {
-                            const uint4 lo = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 0, s_lo, ns_lo);
-                            const uint4 hi = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 4, s_hi, ns_hi);
-                            *reinterpret_cast<uint4 *>(rowdst + ((cq ^ (r & 7)) << 4)) = lo;
-                            *reinterpret_cast<uint4 *>(rowdst + (((cq + 4) ^ (r & 7)) << 4)) = hi;
+                            for (int cq = 0; cq < 4; ++cq) {
+                                const uint4 lo = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 0, s_lo, ns_lo);
+                                const uint4 hi = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 4, s_hi, ns_hi);
+                                *reinterpret_cast<uint4 *>(rowdst + ((cq ^ (r & 7)) << 4)) = lo;
+                                *reinterpret_cast<uint4 *>(rowdst + (((cq + 4) ^ (r & 7)) << 4)) = hi;
+                            }
+                        } else {  // the fifth bits of the same 32 positions: bits 2c and 2c+1 of qh
+                            const uint4 ha = *reinterpret_cast<const uint4 *>(blk + 16);
+                            const uint4 hb = *reinterpret_cast<const uint4 *>(blk + 32);
+                            const uint32_t q[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+#pragma unroll
+                            for (int cq = 0; cq < 4; ++cq) {
+                                const uint4 lo = nibbles5_to_f16(w[2 * cq], w[2 * cq + 1], q[2 * cq], q[2 * cq + 1], 0,
+                                                                 2 * c, s_lo, ns_lo);
+                                const uint4 hi = nibbles5_to_f16(w[2 * cq], w[2 * cq + 1], q[2 * cq], q[2 * cq + 1], 4,
+                                                                 2 * c + 1, s_hi, ns_hi);
+                                *reinterpret_cast<uint4 *>(rowdst + ((cq ^ (r & 7)) << 4)) = lo;
+                                *reinterpret_cast<uint4 *>(rowdst + (((cq + 4) ^ (r & 7)) << 4)) = hi;
+                            }
                         }
                     }
                     if (h == 1) {  // mins of the 8 sub-blocks as fp16, then 8 zeros (32-byte swizzle)
@@ -970,6 +999,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_q5k_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
+                       const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
+                       const __grid_constant__ CUtensorMap tm_w2, TcArgs a) {
+    gemm_tc_body<QMM_Q5_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, a);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_q80_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xmin,
                        const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_w2, TcArgs a) {
@@ -1145,8 +1181,8 @@ TcLayout tc_layout(int64_t m, int64_t k, int64_t partial_ctas) {
 // Q6_K has no map: its raw warp bulk-copies from W, which must start on a 16-byte boundary.
 int64_t tc_row_bytes(qmm_type t, int64_t k) { return (k / 256) * block_bytes(t) * (256 / block_elems(t)); }
 
-bool tc_weight_map(qmm_type t, const void *W, int64_t rows, int64_t k, CUtensorMap *tm_w) {
-    const int64_t row_bytes = tc_row_bytes(t, k);
+bool tc_weight_map(qmm_type t, const void *W, int64_t rows, int64_t k, CUtensorMap *tm_w, int64_t stride = 0) {
+    const int64_t row_bytes = stride > 0 ? stride : tc_row_bytes(t, k);
     if (t == QMM_Q8_0)
         return make_map_2d(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, W, row_bytes / 2, rows, TcFmt<QMM_Q8_0>::kRawRow / 2,
                            kTN, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -1154,21 +1190,31 @@ bool tc_weight_map(qmm_type t, const void *W, int64_t rows, int64_t k, CUtensorM
         memset(tm_w, 0, sizeof(*tm_w));
         return (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
     }
-    return make_map_2d(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, rows, kQ4KBytes, kTN,
+    // Q4_K, Q5_K and Q4_0: a box of one superblock's raw bytes (144, 176, 144) per row
+    return make_map_2d(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, rows, (uint32_t)tc_row_bytes(t, 256), kTN,
                        CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int64_t gemm_tc_tile_m(int64_t) { return kTM; }
 
-bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
+bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t stride) {
     if (!(k % 256 == 0 && n > 0 && m > 0 && m <= (int64_t(1) << 30))) return false;
-    if (t == QMM_Q4_K || t == QMM_Q8_0 || t == QMM_Q4_0) return true;
-    // Q6_K's raw map views W as groups of 8 rows, so n must be a multiple of 8
-    return t == QMM_Q6_K && n % 8 == 0;
+    if (t == QMM_Q4_K || t == QMM_Q5_K || t == QMM_Q8_0 || t == QMM_Q4_0) return true;
+    // Q6_K's raw windows reach up to 14 bytes past a row's last block: with natural rows the
+    // last row's window must end at the end of W, which n % 8 == 0 gives; rows padded by
+    // qmm_repack_aligned keep every window inside its own row
+    return t == QMM_Q6_K && (n % 8 == 0 || (stride > 0 && stride >= aligned_row_bytes(t, k)));
 }
 
-size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m) {
-    if (!gemm_tc_supported(t, n, k, m)) return 0;
+int64_t aligned_row_bytes(qmm_type t, int64_t k) {
+    if (block_bytes(t) <= 0 || k <= 0 || k % block_elems(t)) return 0;
+    const int64_t rb = (k / block_elems(t)) * block_bytes(t);
+    // Q6_K: room for the 14 bytes that a superblock's 16-byte-aligned copy window can overrun
+    return ((rb + (t == QMM_Q6_K ? 14 : 0) + 15) / 16) * 16;
+}
+
+size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t stride) {
+    if (!gemm_tc_supported(t, n, k, m, stride)) return 0;
     const int64_t nwork = ((n + kTN - 1) / kTN) * ((m + kTM - 1) / kTM) * (k / 256);
     return tc_layout(m, k, std::min<int64_t>(kMaxPartialCtas, nwork)).total;
 }
@@ -1181,6 +1227,7 @@ cudaError_t run_tc(const CUtensorMap &tm_x, const CUtensorMap &tm_xmin, const CU
                    const CUtensorMap &tm_w, const CUtensorMap &tm_w2, const TcArgs &args, int ctas, int64_t fixup_tiles,
                    cudaStream_t st) {
     auto kern = T == QMM_Q4_K   ? gemm_tc_q4k_kernel
+                : T == QMM_Q5_K ? gemm_tc_q5k_kernel
                 : T == QMM_Q6_K ? gemm_tc_q6k_kernel
                 : T == QMM_Q4_0 ? gemm_tc_q40_kernel
                                 : gemm_tc_q80_kernel;
@@ -1220,8 +1267,8 @@ bool make_act_maps(CUtensorMap &tm_x, CUtensorMap &tm_xmin, CUtensorMap &tm_dx, 
 }  // namespace
 
 cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                           void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st) {
-    if (!gemm_tc_supported(t, n, k, m)) return cudaErrorNotSupported;
+                           void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st, int64_t stride) {
+    if (!gemm_tc_supported(t, n, k, m, stride)) return cudaErrorNotSupported;
     qmm_gemm_plan p{};
     const int nsm = std::min(device_sm_count(), kMaxPartialCtas);
     if (qmm_plan_gemm(t, n, k, m, nsm, stream_k_mode, &p) != QMM_OK) return cudaErrorInvalidValue;
@@ -1241,8 +1288,8 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     if (e != cudaSuccess) return e;
 
     CUtensorMap tm_x, tm_xmin, tm_dx, tm_w;
-    const int64_t row_bytes = tc_row_bytes(t, k);
-    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) || !tc_weight_map(t, W, n, k, &tm_w))
+    const int64_t row_bytes = stride > 0 ? stride : tc_row_bytes(t, k);
+    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, m, k) || !tc_weight_map(t, W, n, k, &tm_w, stride))
         return cudaErrorInvalidValue;
 
     TcArgs args{};
@@ -1263,6 +1310,7 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     const int64_t fixup_tiles = (p.stream_k && p.fixup) ? p.ntiles : 0;
     if (t == QMM_Q8_0) return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
     if (t == QMM_Q4_0) return run_tc<QMM_Q4_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
+    if (t == QMM_Q5_K) return run_tc<QMM_Q5_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
     if (t == QMM_Q6_K) return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
     return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
 }
@@ -1392,6 +1440,7 @@ cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts,
     switch (t) {
     case QMM_Q8_0: return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
     case QMM_Q4_0: return run_tc<QMM_Q4_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
+    case QMM_Q5_K: return run_tc<QMM_Q5_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
     case QMM_Q6_K: return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
     default: return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
     }

@@ -676,6 +676,7 @@ int gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int ncols, size_t budget)
     case QMM_Q6_K: rb = gemv_tma_row_bytes<QMM_Q6_K>(n, k); break;
     case QMM_Q8_0: rb = gemv_tma_row_bytes<QMM_Q8_0>(n, k); break;
     case QMM_Q4_0: rb = gemv_tma_row_bytes<QMM_Q4_0>(n, k); break;
+    case QMM_Q5_K: rb = gemv_tma_row_bytes<QMM_Q5_K>(n, k); break;
     default: return 0;
     }
     return rb > 0 ? gemv_tma_stages(rb, k, ncols, budget) : 0;
@@ -683,8 +684,8 @@ int gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int ncols, size_t budget)
 
 template <int T, int NC>
 static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x, float *y, int64_t y_ld,
-                                      int nstages, cudaStream_t st) {
-    const int64_t row_bytes = gemv_tma_row_bytes<T>(n, k);
+                                      int nstages, cudaStream_t st, int64_t stride) {
+    const int64_t row_bytes = stride > 0 ? stride : gemv_tma_row_bytes<T>(n, k);
     const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, NC);
     void (*kern)(const uint8_t *, int64_t, int, int64_t, int, const XIn, float *, int64_t, int *);
     if constexpr (T == QMM_Q4_K) {
@@ -739,7 +740,7 @@ static cudaError_t launch_gemv_id_t(const void *W, int64_t n_experts, int64_t n,
 
 template <int T, int NC>
 static cudaError_t launch_gemv_nc(const void *W, int64_t n, int64_t k, XIn x, float *y, int64_t y_ld,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, int64_t stride) {
     const size_t smem = gemv_smem_bytes(k, NC);
     auto kern = gemv_kernel<T, NC>;
     if (smem > 48 * 1024) {
@@ -753,7 +754,7 @@ static cudaError_t launch_gemv_nc(const void *W, int64_t n, int64_t k, XIn x, fl
     const int64_t npairs = (n + 1) / 2;
     const int64_t need = (npairs + kGemvThreads / 32 - 1) / (kGemvThreads / 32);
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, int64_t(device_sm_count()) * per_sm));
-    const int64_t row_bytes = int64_t(k / block_elems(T)) * block_bytes(T);
+    const int64_t row_bytes = stride > 0 ? stride : int64_t(k / block_elems(T)) * block_bytes(T);
     kern<<<(unsigned)grid, kGemvThreads, smem, st>>>(static_cast<const uint8_t *>(W), n, (int)k, row_bytes, x, y,
                                                      y_ld);
     return cudaGetLastError();
@@ -761,7 +762,7 @@ static cudaError_t launch_gemv_nc(const void *W, int64_t n, int64_t k, XIn x, fl
 
 template <int T>
 static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
-                                 float *y, cudaStream_t st) {
+                                 float *y, cudaStream_t st, int64_t stride) {
     const size_t xrow = size_t(k / 32) * kQ81Bytes;
     const size_t budget = size_t(device_smem_optin());
     int64_t c0 = 0;
@@ -774,32 +775,33 @@ static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void
         xc.xq = xf ? nullptr : static_cast<const uint8_t *>(xq) + c0 * xrow;
         xc.xf = xf ? xf + c0 * k : nullptr;
         float *yc = y + c0 * n;
-        const int64_t trb = gemv_tma_row_bytes<T>(n, k);
+        // rows padded to a 16-byte multiple (stride > 0) always stream in whole units
+        const int64_t trb = stride > 0 ? stride : gemv_tma_row_bytes<T>(n, k);
         const int nst = trb > 0 ? gemv_tma_stages(trb, k, nc, budget) : 0;
         if (nst > 0 && gemv_tma_enabled()) {
             switch (nc) {
-            case 1: e = launch_gemv_tma_nc<T, 1>(W, n, k, xc, yc, n, nst, st); break;
-            case 2: e = launch_gemv_tma_nc<T, 2>(W, n, k, xc, yc, n, nst, st); break;
-            case 3: e = launch_gemv_tma_nc<T, 3>(W, n, k, xc, yc, n, nst, st); break;
-            case 4: e = launch_gemv_tma_nc<T, 4>(W, n, k, xc, yc, n, nst, st); break;
-            case 5: e = launch_gemv_tma_nc<T, 5>(W, n, k, xc, yc, n, nst, st); break;
-            case 6: e = launch_gemv_tma_nc<T, 6>(W, n, k, xc, yc, n, nst, st); break;
-            case 7: e = launch_gemv_tma_nc<T, 7>(W, n, k, xc, yc, n, nst, st); break;
-            default: e = launch_gemv_tma_nc<T, 8>(W, n, k, xc, yc, n, nst, st); break;
+            case 1: e = launch_gemv_tma_nc<T, 1>(W, n, k, xc, yc, n, nst, st, stride); break;
+            case 2: e = launch_gemv_tma_nc<T, 2>(W, n, k, xc, yc, n, nst, st, stride); break;
+            case 3: e = launch_gemv_tma_nc<T, 3>(W, n, k, xc, yc, n, nst, st, stride); break;
+            case 4: e = launch_gemv_tma_nc<T, 4>(W, n, k, xc, yc, n, nst, st, stride); break;
+            case 5: e = launch_gemv_tma_nc<T, 5>(W, n, k, xc, yc, n, nst, st, stride); break;
+            case 6: e = launch_gemv_tma_nc<T, 6>(W, n, k, xc, yc, n, nst, st, stride); break;
+            case 7: e = launch_gemv_tma_nc<T, 7>(W, n, k, xc, yc, n, nst, st, stride); break;
+            default: e = launch_gemv_tma_nc<T, 8>(W, n, k, xc, yc, n, nst, st, stride); break;
             }
             if (e != cudaSuccess) return e;
             c0 += nc;
             continue;
         }
         switch (nc) {
-        case 1: e = launch_gemv_nc<T, 1>(W, n, k, xc, yc, n, st); break;
-        case 2: e = launch_gemv_nc<T, 2>(W, n, k, xc, yc, n, st); break;
-        case 3: e = launch_gemv_nc<T, 3>(W, n, k, xc, yc, n, st); break;
-        case 4: e = launch_gemv_nc<T, 4>(W, n, k, xc, yc, n, st); break;
-        case 5: e = launch_gemv_nc<T, 5>(W, n, k, xc, yc, n, st); break;
-        case 6: e = launch_gemv_nc<T, 6>(W, n, k, xc, yc, n, st); break;
-        case 7: e = launch_gemv_nc<T, 7>(W, n, k, xc, yc, n, st); break;
-        default: e = launch_gemv_nc<T, 8>(W, n, k, xc, yc, n, st); break;
+        case 1: e = launch_gemv_nc<T, 1>(W, n, k, xc, yc, n, st, stride); break;
+        case 2: e = launch_gemv_nc<T, 2>(W, n, k, xc, yc, n, st, stride); break;
+        case 3: e = launch_gemv_nc<T, 3>(W, n, k, xc, yc, n, st, stride); break;
+        case 4: e = launch_gemv_nc<T, 4>(W, n, k, xc, yc, n, st, stride); break;
+        case 5: e = launch_gemv_nc<T, 5>(W, n, k, xc, yc, n, st, stride); break;
+        case 6: e = launch_gemv_nc<T, 6>(W, n, k, xc, yc, n, st, stride); break;
+        case 7: e = launch_gemv_nc<T, 7>(W, n, k, xc, yc, n, st, stride); break;
+        default: e = launch_gemv_nc<T, 8>(W, n, k, xc, yc, n, st, stride); break;
         }
         if (e != cudaSuccess) return e;
         c0 += nc;
@@ -808,12 +810,13 @@ static cudaError_t launch_gemv_t(const void *W, int64_t n, int64_t k, const void
 }
 
 cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
-                        float *y, cudaStream_t st) {
+                        float *y, cudaStream_t st, int64_t stride) {
     switch (t) {
-    case QMM_Q4_K: return launch_gemv_t<QMM_Q4_K>(W, n, k, xq, xf, m, y, st);
-    case QMM_Q6_K: return launch_gemv_t<QMM_Q6_K>(W, n, k, xq, xf, m, y, st);
-    case QMM_Q8_0: return launch_gemv_t<QMM_Q8_0>(W, n, k, xq, xf, m, y, st);
-    case QMM_Q4_0: return launch_gemv_t<QMM_Q4_0>(W, n, k, xq, xf, m, y, st);
+    case QMM_Q4_K: return launch_gemv_t<QMM_Q4_K>(W, n, k, xq, xf, m, y, st, stride);
+    case QMM_Q6_K: return launch_gemv_t<QMM_Q6_K>(W, n, k, xq, xf, m, y, st, stride);
+    case QMM_Q8_0: return launch_gemv_t<QMM_Q8_0>(W, n, k, xq, xf, m, y, st, stride);
+    case QMM_Q4_0: return launch_gemv_t<QMM_Q4_0>(W, n, k, xq, xf, m, y, st, stride);
+    case QMM_Q5_K: return launch_gemv_t<QMM_Q5_K>(W, n, k, xq, xf, m, y, st, stride);
     }
     return cudaErrorInvalidValue;
 }
@@ -852,6 +855,7 @@ bool gemv_id_supported(qmm_type t, int64_t n, int64_t k) {
     case QMM_Q6_K: rb = gemv_tma_row_bytes<QMM_Q6_K>(n, k); break;
     case QMM_Q8_0: rb = gemv_tma_row_bytes<QMM_Q8_0>(n, k); break;
     case QMM_Q4_0: rb = gemv_tma_row_bytes<QMM_Q4_0>(n, k); break;
+    case QMM_Q5_K: rb = gemv_tma_row_bytes<QMM_Q5_K>(n, k); break;
     }
     return n > 0 && rb > 0 && gemv_tma_stages(rb, k, 1, size_t(device_smem_optin())) > 0;
 }
@@ -864,6 +868,7 @@ cudaError_t launch_gemv_id(qmm_type t, const void *W, int64_t n_experts, int64_t
     case QMM_Q6_K: return launch_gemv_id_t<QMM_Q6_K>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
     case QMM_Q8_0: return launch_gemv_id_t<QMM_Q8_0>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
     case QMM_Q4_0: return launch_gemv_id_t<QMM_Q4_0>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
+    case QMM_Q5_K: return launch_gemv_id_t<QMM_Q5_K>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -53,8 +53,10 @@ bool gemv_tma_enabled();
 size_t gemv_smem_bytes(int64_t k, int ncols);
 // ring depth of the bulk-copy GEMV for ncols columns in budget bytes (0: direct kernel)
 int gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int ncols, size_t budget);
+// stride: bytes from one weight row to the next (0: the natural k/QK blocks; > 0: rows
+// padded to a multiple of 16 bytes by qmm_repack_aligned).
 cudaError_t launch_gemv(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, const float *xf, int64_t m,
-                        float *y, cudaStream_t st);
+                        float *y, cudaStream_t st, int64_t stride = 0);
 // Fused gate/up + SwiGLU GEMV (Q4_K, m <= 8): y[m][n] = silu(x Wg^T) * (x Wu^T) from
 // q8_1 activations, both weights read once.
 // Fused gate/up launches take Wu == nullptr for one interleaved tensor (gate row j at
@@ -94,14 +96,16 @@ cudaError_t launch_gemv_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
 
 // CUDA-core tiled GEMM (dp4a), any m.
 cudaError_t launch_gemm_dp4a(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                             cudaStream_t st);
+                             cudaStream_t st, int64_t stride = 0);
 
 // Tensor-core GEMM (tcgen05, kind::f16 on integer-valued operands).
 int64_t gemm_tc_tile_m(int64_t m);
-size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m);
-bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m);
+size_t gemm_tc_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t stride = 0);
+bool gemm_tc_supported(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t stride = 0);
 cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
-                           void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st);
+                           void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st, int64_t stride = 0);
+// Row stride of the padded layout of qmm_repack_aligned (0 for bad arguments).
+int64_t aligned_row_bytes(qmm_type t, int64_t k);
 
 // Fused gate/up + SwiGLU on the tensor-core GEMM (Q4_K): y[m][n_out] = silu(x Wg^T) * (x Wu^T),
 // one whole 128-column tile (64 outputs) per CTA.

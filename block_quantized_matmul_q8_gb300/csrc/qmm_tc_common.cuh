@@ -31,6 +31,27 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w0, uint32_t w1, int sh
     return r;
 }
 
+// Q5_K: the same 8 values with their fifth bits, bit j of the 8 qh bytes that share the
+// nibbles' positions (q0, q1 as w0, w1): (0x6400 | code) is the fp16 1024 + code, code <= 31.
+__device__ __forceinline__ uint4 nibbles5_to_f16(uint32_t w0, uint32_t w1, uint32_t q0, uint32_t q1, int shift, int j,
+                                                 __half2 sc2, __half2 nsc2) {
+    const uint32_t ws[2] = {w0, w1}, qs[2] = {q0, q1};
+    uint32_t p[4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t a0 = __byte_perm(ws[i], 0, 0x4140), a1 = __byte_perm(ws[i], 0, 0x4342);
+        const uint32_t h0 = __byte_perm(qs[i], 0, 0x4140), h1 = __byte_perm(qs[i], 0, 0x4342);
+        p[2 * i] = ((a0 >> shift) & 0x000F000Fu) | (((h0 >> j) & 0x00010001u) << 4) | 0x64006400u;
+        p[2 * i + 1] = ((a1 >> shift) & 0x000F000Fu) | (((h1 >> j) & 0x00010001u) << 4) | 0x64006400u;
+    }
+    uint4 r;
+    r.x = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[0]), sc2, nsc2));
+    r.y = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[1]), sc2, nsc2));
+    r.z = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[2]), sc2, nsc2));
+    r.w = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[3]), sc2, nsc2));
+    return r;
+}
+
 // A 2D tiled tensor map over a row-major [outer][inner] array with the given row
 // stride (host; the driver's encoder is looked up once).  False on any failure.
 bool tc_make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *base, uint64_t inner,

@@ -30,6 +30,11 @@
  *   Q4_K (144 B / 256):      fp16 d, fp16 dmin, 12 B of 6-bit sub-block scales
  *        and mins, 128 B of nibbles; w = d*sc*q - dmin*m
  *        ([MMQ] section "Q4_K: 在加载期就把两层 scale 合并成 half2").
+ *   Q5_K (176 B / 256):      fp16 d, fp16 dmin, 12 B of scales/mins (Q4_K's rule), qh[32],
+ *        128 B of nibbles in Q4_K's order; the fifth bit of weight 32j + l is bit j of
+ *        qh[l]; w = d*sc*q - dmin*m with q in 0..31 ([MMQ] section "Q4_K: 在加载期就把两层
+ *        scale 合并成 half2": Q4_K and Q5_K share the scale unpack; the bit plane's layout
+ *        is this library's reading).
  *   Q6_K (210 B / 256):      ql[128], qh[64], int8 scales[16], fp16 d;
  *        w = d*sc*(code-32) ([MMQ] section "Q6_K: 6 位数据要多占一半的共享内存").
  *   Q8_0 (34 B / 32):        fp16 d, int8 q[32]; w = d*q.
@@ -54,7 +59,7 @@
 extern "C" {
 #endif
 
-typedef enum { QMM_Q4_0 = 2, QMM_Q8_0 = 8, QMM_Q4_K = 12, QMM_Q6_K = 14 } qmm_type;
+typedef enum { QMM_Q4_0 = 2, QMM_Q8_0 = 8, QMM_Q4_K = 12, QMM_Q5_K = 13, QMM_Q6_K = 14 } qmm_type;
 
 typedef enum {
     QMM_OK = 0,
@@ -208,6 +213,35 @@ QMM_API qmm_status qmm_repack_glu(const void *W_gate, const void *W_up, qmm_type
  */
 QMM_API qmm_status qmm_mul_mat_glu_packed(const void *W_gu, qmm_type t, int64_t n, int64_t k, const void *xq,
                                           int64_t m, float *y, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * One-time repack of W into rows padded to whole 16-byte units (the optional weight
+ * repack; [QMM] section "Q4K 的 8 列重排": a one-time repack done when the weights are
+ * loaded, kept as a second copy, so the caller owns both and may free the original).
+ * Blocks are copied unchanged; row r of W_aligned starts at r * qmm_aligned_row_bytes(t, k)
+ * and the bytes after its k/QK blocks are zero.  Q6_K rows (210-byte blocks) and Q8_0/Q4_0
+ * rows (34/18-byte blocks) are generally not whole 16-byte units: padded, every row can
+ * be streamed by 16-byte bulk copies.  Q6_K rows get room for the 14 bytes by which the
+ * tensor-core GEMM's 16-byte-aligned copy window of a superblock can run past its row,
+ * which lifts that path's n % 8 == 0 condition.  Q4_K rows are whole units already, and
+ * padded rows equal W.
+ *   W : [n][k/QK] blocks, 16-byte aligned; W_aligned : n * qmm_aligned_row_bytes(t, k)
+ *       bytes, 16-byte aligned.  Enqueued on stream.
+ */
+QMM_API size_t qmm_aligned_row_bytes(qmm_type t, int64_t k);
+QMM_API qmm_status qmm_repack_aligned(const void *W, qmm_type t, int64_t n, int64_t k, void *W_aligned,
+                                      void *stream);
+
+/*
+ * qmm_mul_mat on the padded rows of qmm_repack_aligned: the same product within the same
+ * bound (the kernels decode the same blocks; only where each row starts differs), with the
+ * bulk-copy GEMV for every Q6_K/Q8_0/Q4_0 shape and the tensor-core GEMM for Q6_K at any n.
+ *   workspace : at least qmm_workspace_bytes_aligned(t, n, k, m) bytes, 256-byte aligned.
+ * Other arguments and errors as qmm_mul_mat.
+ */
+QMM_API size_t qmm_workspace_bytes_aligned(qmm_type t, int64_t n, int64_t k, int64_t m);
+QMM_API qmm_status qmm_mul_mat_aligned(const void *W_aligned, qmm_type t, int64_t n, int64_t k, const void *xq,
+                                       int64_t m, float *y, void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * Expert-routed matmul ([MMQ] sections "派发路径", "专家边界: 在 GPU 上做分段,

@@ -54,7 +54,7 @@ def _mm(L, W=1024, t=12, n=8, k=256, xq=2048, m=4, y=4096, ws=None, wsb=0):
 
 
 def test_argument_errors_need_no_gpu(L):
-    assert _mm(L, t=13) == 3                      # unknown type
+    assert _mm(L, t=99) == 3                      # unknown type
     assert _mm(L, k=100) == 2                     # not a multiple of 256
     assert _mm(L, t=8, k=48) == 2                 # Q8_0 needs k % 32
     assert _mm(L, k=0) == 1
@@ -86,7 +86,7 @@ def test_f32_call_argument_errors_need_no_gpu(L):
     def mm(W=1024, t=12, n=8, k=256, x=2048, m=4, y=4096, ws=None, wsb=0):
         return L.qmm_mul_mat_f32(P(W), t, n, k, P(x), m, P(y), P(ws) if ws else None, wsb, None)
 
-    assert mm(t=13) == 3
+    assert mm(t=99) == 3
     assert mm(k=100) == 2
     assert mm(t=8, k=48) == 2
     assert mm(x=0) == 1
@@ -194,27 +194,27 @@ def test_newer_calls_argument_errors_need_no_gpu(L):
     # qmm_mul_mat_glu(W_gate, W_up, t, n, k, xq, m, y, ws, ws_bytes, stream)
     glu = lambda Wg=1024, Wu=2048, t=12, n=8, k=256, xq=4096, m=4, y=8192: L.qmm_mul_mat_glu(
         P(Wg), P(Wu), t, n, k, P(xq), m, P(y), None, 0, None)
-    assert glu(t=13) == 3 and glu(k=100) == 2 and glu(k=0) == 1 and glu(n=-1) == 1
+    assert glu(t=99) == 3 and glu(k=100) == 2 and glu(k=0) == 1 and glu(n=-1) == 1
     assert glu(Wu=0) == 1 and glu(xq=0) == 1 and glu(Wg=1030) == 4 and glu(y=8196) == 4
     assert glu(n=0) == 0 and glu(m=0) == 0
     packed = lambda W=1024, t=12, n=8, k=256, xq=4096, m=4, y=8192: L.qmm_mul_mat_glu_packed(
         P(W), t, n, k, P(xq), m, P(y), None, 0, None)
-    assert packed(t=13) == 3 and packed(k=100) == 2 and packed(W=0) == 1 and packed(W=1032) == 4
+    assert packed(t=99) == 3 and packed(k=100) == 2 and packed(W=0) == 1 and packed(W=1032) == 4
     assert packed(n=0) == 0 and packed(m=0) == 0
     # qmm_repack_glu(W_gate, W_up, t, n, k, W_gu, stream)
     rp = lambda Wg=1024, Wu=2048, t=12, n=8, k=256, out=4096: L.qmm_repack_glu(P(Wg), P(Wu), t, n, k, P(out), None)
-    assert rp(t=13) == 3 and rp(t=2, k=48) == 2 and rp(out=0) == 1 and rp(Wu=2056) == 4 and rp(n=0) == 0
+    assert rp(t=99) == 3 and rp(t=2, k=48) == 2 and rp(out=0) == 1 and rp(Wu=2056) == 4 and rp(n=0) == 0
     # qmm_mul_mat_f32_host(W, t, n, k, x_host, m, y_host, ws, ws_bytes, stream)
     host = lambda W=1024, t=12, n=8, k=256, x=4096, m=2, y=8192, ws=None, wsb=0: L.qmm_mul_mat_f32_host(
         P(W), t, n, k, P(x), m, P(y), P(ws) if ws else None, wsb, None)
-    assert host(t=13) == 3 and host(k=100) == 2 and host(x=0) == 1 and host(y=0) == 1
+    assert host(t=99) == 3 and host(k=100) == 2 and host(x=0) == 1 and host(y=0) == 1
     assert host(W=1028) == 4 and host(n=0) == 0 and host(m=0) == 0
     need = L.qmm_workspace_bytes_f32_host(12, 8, 256, 2)
     assert need >= 2 * 256 and host(ws=1 << 20, wsb=need - 1) == 5 and host(ws=(1 << 20) + 16, wsb=need) == 4
     # qmm_mul_mat_id_slot: the same checks as qmm_mul_mat_id
     args = [P(1024), 12, 4, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
     assert L.qmm_mul_mat_id_slot(*args, None, 0, None) == 5
-    bad_t = [P(1024), 13, 4, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
+    bad_t = [P(1024), 99, 4, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
     assert L.qmm_mul_mat_id_slot(*bad_t, None, 0, None) == 3
 
 
@@ -224,3 +224,9 @@ def test_q4_0_sizes_and_shapes(L):
     P = ctypes.c_void_p
     # k must be a multiple of the 32-value block
     assert L.qmm_mul_mat(P(1024), 2, 8, 48, P(2048), 4, P(4096), None, 0, None) == 2
+
+
+def test_aligned_row_bytes_matches_oracle(oracle_mod):
+    for fmt, k in [("q6_K", 5120), ("q6_K", 256), ("q8_0", 5120), ("q8_0", 96), ("q4_0", 224), ("q4_K", 4096)]:
+        assert qmm.qmm_aligned_row_bytes(fmt, k) == oracle_mod.aligned_row_bytes(fmt, k)
+    assert qmm.qmm_aligned_row_bytes("q6_K", 100) == 0  # not a whole number of blocks
