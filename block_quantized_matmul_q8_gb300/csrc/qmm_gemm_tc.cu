@@ -195,6 +195,8 @@ struct TcArgs {
     int64_t nsb;
     int64_t nwork;
     int ctas;
+    // 0: one tile per CTA; 1: stream-K; 2 (expert-grouped): whole tiles when the tile
+    // count read on the device fills the CTAs' waves to at least 90%, else stream-K
     int stream_k;
     // expert-grouped mode (tiles != nullptr): the activation arrays hold the (token,
     // slot) pairs in expert-sorted order, W is [E][n] rows, y is [pairs][n]
@@ -253,8 +255,21 @@ struct Barriers {
     int abort;
 };
 
+// Mode 2: whole tiles are worth it when the last wave is nearly full, i.e. when the tiles
+// fill at least 90% of ceil(tiles / ctas) rounds of the CTAs; the fixup kernel takes the
+// same decision from the same numbers.
+__device__ __forceinline__ bool whole_tiles(const TcArgs &a) {
+    if (a.stream_k != 2) return false;
+    const int64_t t = a.nwork / a.nsb, rounds = (t + a.ctas - 1) / a.ctas;
+    return 10 * t >= 9 * rounds * a.ctas;
+}
+
 __device__ __forceinline__ void cta_range(const TcArgs &a, int cta, int64_t &b, int64_t &e) {
-    if (a.stream_k) {
+    if (whole_tiles(a)) {  // a contiguous run of whole tiles: nothing left for the fixup
+        const int64_t t = a.nwork / a.nsb;
+        b = (t * cta / a.ctas) * a.nsb;
+        e = (t * (cta + 1) / a.ctas) * a.nsb;
+    } else if (a.stream_k) {
         b = a.nwork * cta / a.ctas;
         e = a.nwork * (cta + 1) / a.ctas;
     } else {
@@ -651,16 +666,40 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         break;
                     }
                     uint8_t *wst = smem + kOffW + st * Mp::kWStage;
-                    // The unit's words, read chunk by chunk to keep the unpack warps' registers
-                    // low.  Unit h covers k = 64h .. 64h+63: half hh = h >> 1 of the superblock,
+                    // Unit h covers k = 64h .. 64h+63: half hh = h >> 1 of the superblock,
                     // quarters t = 2 (h & 1) and 2 (h & 1) + 1; weight 128 hh + 32 t + l takes the
                     // nibble t >> 1 of ql[64 hh + 32 (t & 1) + l] and bits 2t, 2t+1 of qh[32 hh + l].
-                    // The superblock starts 0 or 2 bytes past a word boundary: words are read from
-                    // the boundary below and shifted.
-                    const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 2u), fsh = 8u * mis;
+                    // The 32 qh bytes stay in registers for the unit, the ql bytes are read 32 at
+                    // a time (one quarter t).
+                    const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 2u), fsh2 = 8u * mis;
                     const uint8_t *blk4 = blk - mis;
                     auto wd = [&](int off) {  // the 32-bit word at byte off of the superblock
-                        return __funnelshift_r(LdShared::u32(blk4 + off), LdShared::u32(blk4 + off + 4), fsh);
+                        return __funnelshift_r(LdShared::u32(blk4 + off), LdShared::u32(blk4 + off + 4), fsh2);
+                    };
+                    // Eight consecutive words of the superblock from byte X (a multiple of 16):
+                    // three aligned 16-byte loads of the window (rows 240 bytes apart, so the 8
+                    // lanes of a quarter warp hit distinct banks), rotated by the superblock's
+                    // word offset in the window and shifted by its odd half-word.
+                    const uint32_t o = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 15u);
+                    const uint8_t *win = blk - o;
+                    const bool rot1 = (o & 4u) != 0, rot2 = (o & 8u) != 0;
+                    const uint32_t fsh = 8u * (o & 3u);
+                    auto span8 = [&](int X, uint32_t(&out)[8]) {
+                        uint32_t v[12];
+#pragma unroll
+                        for (int c = 0; c < 3; ++c) {
+                            const uint4 t4 = *reinterpret_cast<const uint4 *>(win + X + 16 * c);
+                            v[4 * c] = t4.x;
+                            v[4 * c + 1] = t4.y;
+                            v[4 * c + 2] = t4.z;
+                            v[4 * c + 3] = t4.w;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 11; ++i) v[i] = rot1 ? v[i + 1] : v[i];
+#pragma unroll
+                        for (int i = 0; i < 9; ++i) v[i] = rot2 ? v[i + 2] : v[i];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) out[j] = __funnelshift_r(v[j], v[j + 1], fsh);
                     };
                     const uint32_t scw = wd(192 + 4 * h);  // the 4 int8 scales of the unit's 16-value sub-blocks
                     __half2 ha[4], hb[4];
@@ -672,14 +711,21 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     }
                     const int hh = h >> 1;
                     uint8_t *rowa = wst + r * 128, *rowb = wst + kSlabBytes + r * 128;
+                    uint32_t QH[8];
+                    span8(128 + 32 * hh, QH);  // qh[32 hh + l], l = 0..31
 #pragma unroll
-                    for (int cq = 0; cq < 8; ++cq) {  // 16-byte chunk cq: codes 8cq .. 8cq+7, sub-block cq / 2
-                        const int tt = 2 * (h & 1) + (cq >> 2), l0 = 8 * (cq & 3);
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t QL[8];
+                    span8(64 * hh + 32 * c2, QL);  // ql[64 hh + 32 c2 + l]
+#pragma unroll
+                    for (int cq4 = 0; cq4 < 4; ++cq4) {  // 16-byte chunk cq: codes 8cq .. 8cq+7, sub-block cq / 2
+                        const int cq = 4 * c2 + cq4;
+                        const int tt = 2 * (h & 1) + c2;
                         uint32_t code[2];
 #pragma unroll
                         for (int e2 = 0; e2 < 2; ++e2) {
-                            const uint32_t ql = wd(64 * hh + 32 * (tt & 1) + l0 + 4 * e2);
-                            const uint32_t qh = wd(128 + 32 * hh + l0 + 4 * e2);
+                            const uint32_t ql = QL[2 * cq4 + e2];
+                            const uint32_t qh = QH[2 * cq4 + e2];
                             const uint32_t lo = (ql >> (4 * (tt >> 1))) & 0x0f0f0f0fu;
                             const uint32_t hi2 = ((qh >> (2 * tt)) & 0x03030303u) << 4;
                             code[e2] = __vsub4(lo | hi2, 0x20202020u);  // q - 32 as signed bytes
@@ -700,6 +746,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         const int sw = (cq ^ (r & 7)) << 4;
                         *reinterpret_cast<uint4 *>(rowa + sw) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
                         *reinterpret_cast<uint4 *>(rowb + sw) = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+                    }
                     }
                     ptx::fence_proxy_async_smem();
                     ptx::mbar_arrive(ptx::smem_u32(&B.st_full[st]));
@@ -1104,6 +1151,7 @@ __global__ void __launch_bounds__(256) tc_fixup_kernel(TcArgs a) {
     if (a.tiles) {  // grouped: the tile count is on the device; the grid strides over it
         ntiles = int64_t(*a.ntiles) * a.tiles_n;
         a.nwork = ntiles * a.nsb;
+        if (whole_tiles(a)) return;  // every tile was written whole
     }
     auto owner = [&](int64_t uu) {
         int64_t c = uu * a.ctas / a.nwork;
@@ -1431,7 +1479,7 @@ cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts,
     args.nsb = k / 256;
     args.nwork = 0;  // read from the device tile count by the kernels
     args.ctas = ctas;
-    args.stream_k = 1;
+    args.stream_k = 2;
     args.tiles = tiles;
     args.ntiles = ntiles;
     args.bounds = bounds;

@@ -10,10 +10,11 @@
 //
 // Bucketing is a stable counting sort done by one CTA:
 //   pass 1  counts per expert (shared-memory atomics) and invalid ids;
-//   scan    bounds[e] (exclusive prefix) and each expert's tile offset;
+//   scan    bounds[e] (exclusive prefix), each expert's tile offset and the cold list,
+//           one warp-wide scan over runs of consecutive experts;
 //   pass 2  rounds of 1024 pairs; within a warp, lanes with the same expert find
 //           each other with __match_any_sync, a per-(warp, expert) count table is
-//           scanned over warps, and each pair lands at
+//           scanned over warps (one shuffle scan per expert), and each pair lands at
 //           bounds[e] + (earlier rounds) + (earlier warps) + (earlier lanes).
 //   Invalid pairs are appended after the valid ones; their output rows are zeroed.
 #include <cuda_runtime.h>
@@ -53,20 +54,34 @@ MoELayout moe_layout(int64_t n_pairs, int64_t n_experts, int tile_tokens, size_t
     return L;
 }
 
+// Exclusive prefix sum over a warp of one int per lane; returns this lane's prefix and
+// sets total to the sum of all lanes.
+__device__ __forceinline__ int warp_exclusive_scan(int v, int lane, int &total) {
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    total = __shfl_sync(0xffffffffu, incl, 31);
+    return incl - v;
+}
+
 __global__ void __launch_bounds__(kBucketThreads) moe_bucket_kernel(const int32_t *__restrict__ ids, int64_t n_pairs,
                                                                     int E, int tile_tokens, int cold_max,
                                                                     int32_t *status, int32_t *bounds, int32_t *perm,
                                                                     MoETile *tiles, int32_t *cold) {
     extern __shared__ __align__(16) int32_t sm[];
+    const int Ep = (E & ~1) + 1;               // odd row stride of the per-warp tables: no bank conflicts
     int32_t *cnt = sm;                          // [E]   counts, then running bases
     int32_t *toff = cnt + E;                    // [E]   tile offsets
-    int32_t *wcnt = toff + E;                   // [32][E] per-warp counts of a round
-    int32_t *wofs = wcnt + kBucketWarps * E;    // [32][E] per-warp offsets of a round
+    int32_t *wcnt = toff + E;                   // [32][Ep] per-warp counts of a round
+    int32_t *wofs = wcnt + kBucketWarps * Ep;   // [32][Ep] per-warp offsets of a round
     __shared__ int32_t s_bad, s_bad_pos;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     for (int i = tid; i < E; i += kBucketThreads) cnt[i] = 0;
-    for (int i = tid; i < kBucketWarps * E; i += kBucketThreads) wcnt[i] = 0;
+    for (int i = tid; i < kBucketWarps * Ep; i += kBucketThreads) wcnt[i] = 0;
     if (tid == 0) {
         s_bad = 0;
         s_bad_pos = 0;
@@ -81,24 +96,38 @@ __global__ void __launch_bounds__(kBucketThreads) moe_bucket_kernel(const int32_
     }
     __syncthreads();
 
-    // scan (one thread: E <= kMaxExperts).  Experts with 1..cold_max pairs get no tiles:
-    // they go to the cold list, in expert order.
-    if (tid == 0) {
-        int run = 0, trun = 0, ncold = 0;
-        for (int e = 0; e < E; ++e) {
+    // scan (warp 0, E <= kMaxExperts): lane l takes the experts [l * per, (l + 1) * per)
+    // in order, so bounds, tile offsets and the cold list (experts with 1..cold_max
+    // pairs, which get no tiles) all come out in expert order.
+    if (warp == 0) {
+        const int per = (E + 31) / 32, e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int pairs = 0, ntile = 0, ncold = 0;
+        for (int e = e0; e < e1; ++e) {
+            const int c = cnt[e];
+            pairs += c;
+            if (c > 0 && c <= cold_max) ++ncold;
+            else ntile += (c + tile_tokens - 1) / tile_tokens;
+        }
+        int tot_pairs, tot_tiles, tot_cold;
+        int run = warp_exclusive_scan(pairs, lane, tot_pairs);
+        int trun = warp_exclusive_scan(ntile, lane, tot_tiles);
+        int crun = warp_exclusive_scan(ncold, lane, tot_cold);
+        for (int e = e0; e < e1; ++e) {
             const int c = cnt[e];
             bounds[e] = run;
             cnt[e] = run;  // running base for pass 2
             toff[e] = trun;
             run += c;
-            if (c > 0 && c <= cold_max) cold[ncold++] = e;
+            if (c > 0 && c <= cold_max) cold[crun++] = e;
             else trun += (c + tile_tokens - 1) / tile_tokens;
         }
-        bounds[E] = run;
-        status[0] = s_bad ? (int32_t)QMM_ERR_IDS : (int32_t)QMM_OK;
-        status[1] = trun;
-        status[2] = s_bad;
-        status[3] = ncold;
+        if (lane == 0) {
+            bounds[E] = tot_pairs;
+            status[0] = s_bad ? (int32_t)QMM_ERR_IDS : (int32_t)QMM_OK;
+            status[1] = tot_tiles;
+            status[2] = s_bad;
+            status[3] = tot_cold;
+        }
     }
     __syncthreads();
 
@@ -126,20 +155,21 @@ __global__ void __launch_bounds__(kBucketThreads) moe_bucket_kernel(const int32_
         const unsigned grp = __match_any_sync(0xffffffffu, key);
         const unsigned lt = grp & ((1u << lane) - 1u);
         const int rank = __popc(lt);
-        if (valid && lt == 0) wcnt[warp * E + e] = __popc(grp);
+        if (valid && lt == 0) wcnt[warp * Ep + e] = __popc(grp);
         __syncthreads();
-        for (int x = tid; x < E; x += kBucketThreads) {
-            int run = cnt[x];
-            for (int w = 0; w < kBucketWarps; ++w) {
-                const int c = wcnt[w * E + x];
-                wofs[w * E + x] = run;
-                wcnt[w * E + x] = 0;
-                run += c;
-            }
-            cnt[x] = run;
+        // per expert, the warps' counts of this round scanned in warp order: warp w takes
+        // experts w, w + 32, ..., lane l the count of warp l
+        for (int x = warp; x < E; x += kBucketWarps) {
+            const int c = wcnt[lane * Ep + x];
+            int total;
+            const int ex = warp_exclusive_scan(c, lane, total);
+            wofs[lane * Ep + x] = cnt[x] + ex;
+            wcnt[lane * Ep + x] = 0;
+            __syncwarp();
+            if (lane == 0) cnt[x] += total;
         }
         __syncthreads();
-        if (valid) perm[wofs[warp * E + e] + rank] = (int32_t)i;
+        if (valid) perm[wofs[warp * Ep + e] + rank] = (int32_t)i;
         // invalid pairs go after the valid ones, in index order
         const unsigned bad = __ballot_sync(0xffffffffu, i < n_pairs && !valid);
         if (bad) {
@@ -165,7 +195,7 @@ __global__ void moe_zero_invalid_kernel(const int32_t *status, const int32_t *pe
 cudaError_t launch_moe_bucket(const int32_t *ids, int64_t n_pairs, int n_experts, int tile_tokens, int cold_max,
                               void *ws, const MoELayout &L, cudaStream_t st) {
     uint8_t *base = static_cast<uint8_t *>(ws);
-    const size_t smem = sizeof(int32_t) * size_t(n_experts) * (2 + 2 * kBucketWarps);
+    const size_t smem = sizeof(int32_t) * (size_t(n_experts) * 2 + size_t(2 * kBucketWarps) * ((n_experts & ~1) + 1));
     cudaError_t e = ensure_smem(moe_bucket_kernel, smem);
     if (e != cudaSuccess) return e;
     moe_bucket_kernel<<<1, kBucketThreads, smem, st>>>(
