@@ -406,7 +406,8 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
     # form, one token top-8, whose calls route to disjoint sets of 8 experts in turn (16
     # calls cover all 128 experts, 453 MB, so no call finds its experts in L2)
     key_p, key_d = "moe_q4K_e128_n1536_k4096_t512_top8", "moe_decode_q4K_e128_n1536_k4096_t1_top8"
-    if only not in key_p and only not in key_d:
+    key_g, key_gd = "moe_glu_q4K_e128_n1536_k4096_t512_top8", "moe_glu_decode_q4K_e128_n1536_k4096_t1_top8"
+    if not any(only in key for key in (key_p, key_d, key_g, key_gd)):
         return out
     E, n, k, T_, Kt = 128, 1536, 4096, 512, 8
     W, x, ids = qmm_synth.make_moe(E, n, k, T_, Kt, seed=0)
@@ -431,6 +432,32 @@ def secondary(torch, qmm, dev, stream, steps, hbm_peak, only=""):
         b = Kt * n * (k // 256) * 144 + (k // 32) * 36 + Kt * n * 4
         out[key_d] = {"GB/s": b / (ms * 1e-3) / 1e9, "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "ms": ms,
                       "l2": "16 routings cycle through the 128 experts (453 MB)"}
+    if only in key_g or only in key_gd:
+        # the fused gate/up + SwiGLU of the same MoE FFN: a second expert tensor as the up weights
+        Wu = torch.from_numpy(qmm_synth.gen_weights("q4_K", np.random.default_rng(5), E * n, k)).to(dev)
+    if only in key_g:
+        xq = qmm.qmm_quantize_q8_1(torch.from_numpy(x).to(dev))
+        idd = torch.from_numpy(ids).to(dev)
+        y = torch.empty((T_, Kt, n), device=dev)
+        ws = torch.empty(qmm.qmm_workspace_bytes_id_glu("q4_K", n, k, T_, E, Kt), dtype=torch.uint8, device=dev)
+        fn = lambda i: qmm.qmm_mul_mat_id_glu(Wd, Wu, "q4_K", E, n, k, xq, idd, Kt, T_, y=y, workspace=ws)
+        ms = time_graphs(torch, fn, steps, 3, lambda: None) / steps
+        out[key_g] = {"tops": 2 * 2 * T_ * Kt * n * k / (ms * 1e-3) / 1e12, "ms": ms,
+                      "l2": "gate and up weights 906 MB > 3x L2"}
+        out[key_g].update(tensor_fracs(out[key_g]["tops"]))
+    if only in key_gd:
+        order = np.random.default_rng(7).permutation(E).astype(np.int32)
+        ids_d = [torch.from_numpy(order[8 * j:8 * j + 8].reshape(1, Kt).copy()).to(dev) for j in range(E // Kt)]
+        xq1 = qmm.qmm_quantize_q8_1(torch.from_numpy(x[:1]).to(dev))
+        y1 = torch.empty((1, Kt, n), device=dev)
+        ws1 = torch.empty(max(qmm.qmm_workspace_bytes_id_glu("q4_K", n, k, 1, E, Kt), 256), dtype=torch.uint8,
+                          device=dev)
+        fn = lambda i: qmm.qmm_mul_mat_id_glu(Wd, Wu, "q4_K", E, n, k, xq1, ids_d[i % len(ids_d)], Kt, 1, y=y1,
+                                              workspace=ws1)
+        ms = time_graphs(torch, fn, steps, 3, lambda: None) / steps
+        b = 2 * Kt * n * (k // 256) * 144 + (k // 32) * 36 + Kt * n * 4
+        out[key_gd] = {"GB/s": b / (ms * 1e-3) / 1e9, "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm_peak, "ms": ms,
+                       "l2": "16 routings cycle through the 128 experts (906 MB of gate and up weights)"}
     return out
 
 

@@ -32,7 +32,7 @@ EXPORTS = ("qmm_status_string", "qmm_q8_1_bytes", "qmm_row_bytes", "qmm_workspac
            "qmm_mul_mat_id_slot", "qmm_workspace_bytes_glu", "qmm_mul_mat_glu", "qmm_gemv_ring_stages",
            "qmm_repack_glu", "qmm_mul_mat_glu_packed", "qmm_workspace_bytes_f32_host", "qmm_mul_mat_f32_host",
            "qmm_get_device_status", "qmm_set_test_fault", "qmm_aligned_row_bytes", "qmm_repack_aligned",
-           "qmm_workspace_bytes_aligned", "qmm_mul_mat_aligned")
+           "qmm_workspace_bytes_aligned", "qmm_mul_mat_aligned", "qmm_workspace_bytes_id_glu", "qmm_mul_mat_id_glu")
 
 
 class QMMError(RuntimeError):
@@ -115,6 +115,10 @@ def lib():
     L.qmm_repack_glu.argtypes = [P, P, ctypes.c_int, I64, I64, P, P]
     L.qmm_mul_mat_id_slot.restype = ctypes.c_int
     L.qmm_mul_mat_id_slot.argtypes = [P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P, ctypes.c_size_t, P]
+    L.qmm_workspace_bytes_id_glu.restype = SZ
+    L.qmm_workspace_bytes_id_glu.argtypes = [ctypes.c_int, I64, I64, I64, I64, I64]
+    L.qmm_mul_mat_id_glu.restype = ctypes.c_int
+    L.qmm_mul_mat_id_glu.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, P, I64, I64, P, P, ctypes.c_size_t, P]
     L.qmm_noalloc_scratch_bytes.restype = SZ
     L.qmm_noalloc_scratch_bytes.argtypes = []
     L.qmm_workspace_bytes_f32.restype = SZ
@@ -370,6 +374,31 @@ def qmm_mul_mat_id_slot(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, 
     one q8_1 row per (token, slot) pair, row t*top_k + s."""
     return _mul_mat_id(lib().qmm_mul_mat_id_slot, "qmm_mul_mat_id_slot", W, qtype, n_experts, n, k, xq, ids, top_k,
                        n_tokens, y, workspace, stream)
+
+
+def qmm_workspace_bytes_id_glu(qtype, n: int, k: int, n_tokens: int, n_experts: int, top_k: int) -> int:
+    return lib().qmm_workspace_bytes_id_glu(_qtype(qtype), n, k, n_tokens, n_experts, top_k)
+
+
+def qmm_mul_mat_id_glu(W_gate: torch.Tensor, W_up: torch.Tensor, qtype, n_experts: int, n: int, k: int,
+                       xq: torch.Tensor, ids: torch.Tensor, top_k: int, n_tokens: int, y: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[n_tokens, top_k, n] fp32 with y[t, s] = silu(x[t] Wg[e]^T) * (x[t] Wu[e]^T), e = ids[t, s]."""
+    _dev(W_gate, "W_gate")
+    _dev(W_up, "W_up")
+    _dev(xq, "xq")
+    _dev(ids, "ids", torch.int32)
+    if y is None:
+        y = torch.empty((n_tokens, top_k, n), dtype=torch.float32, device=W_gate.device)
+    _dev(y, "y", torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(qmm_workspace_bytes_id_glu(qtype, n, k, n_tokens, n_experts, top_k), 256),
+                                dtype=torch.uint8, device=W_gate.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().qmm_mul_mat_id_glu(_ptr(W_gate), _ptr(W_up), _qtype(qtype), n_experts, n, k, _ptr(xq), _ptr(ids),
+                                    top_k, n_tokens, _ptr(y), _ptr(workspace), ws_bytes, _stream(stream)),
+           "qmm_mul_mat_id_glu")
+    return y
 
 
 def qmm_mul_mat_id_noalloc(W: torch.Tensor, qtype, n_experts: int, n: int, k: int, xq: torch.Tensor,

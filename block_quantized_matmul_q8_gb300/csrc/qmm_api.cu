@@ -468,6 +468,30 @@ qmm_status qmm_mul_mat_id_slot(const void *W_experts, qmm_type t, int64_t n_expe
                              stream);
 }
 
+size_t qmm_workspace_bytes_id_glu(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts,
+                                  int64_t top_k) {
+    if (moe_check_sizes(t, n_experts, n, k, top_k, n_tokens) != QMM_OK) return 0;
+    return moe_glu_workspace_bytes(t, n, k, n_tokens, n_experts, top_k);
+}
+
+qmm_status qmm_mul_mat_id_glu(const void *W_gate, const void *W_up, qmm_type t, int64_t n_experts, int64_t n, int64_t k,
+                              const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, float *y,
+                              void *workspace, size_t ws_bytes, void *stream) {
+    qmm_status s = moe_check_sizes(t, n_experts, n, k, top_k, n_tokens);
+    if (s != QMM_OK) return s;
+    if (!workspace) return QMM_ERR_WORKSPACE;
+    if (!aligned256(workspace)) return QMM_ERR_ALIGN;
+    if (ws_bytes < moe_glu_workspace_bytes(t, n, k, n_tokens, n_experts, top_k)) return QMM_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n == 0 || n_tokens == 0) return cuda_status(cudaMemsetAsync(workspace, 0, 16, st));
+    s = moe_check_pointers(W_gate, xq, ids, y);
+    if (s != QMM_OK) return s;
+    if (!W_up) return QMM_ERR_ARG;
+    if (!aligned16(W_up)) return QMM_ERR_ALIGN;
+    return cuda_status(launch_mul_mat_id_glu(t, W_gate, W_up, n_experts, n, k, xq, ids, top_k, n_tokens, false, y,
+                                             workspace, ws_bytes, st));
+}
+
 qmm_status qmm_read_device_status(const void *workspace, int32_t *status, void *stream) {
     if (!workspace || !status) return QMM_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -196,7 +196,8 @@ struct TcArgs {
     int64_t nwork;
     int ctas;
     // 0: one tile per CTA; 1: stream-K; 2 (expert-grouped): whole tiles when the tile
-    // count read on the device fills the CTAs' waves to at least 90%, else stream-K
+    // count read on the device fills the CTAs' waves to at least 90%, else stream-K;
+    // 3 (expert-grouped): whole tiles always (the fused gate/up needs both dots whole)
     int stream_k;
     // expert-grouped mode (tiles != nullptr): the activation arrays hold the (token,
     // slot) pairs in expert-sorted order, W is [E][n] rows, y is [pairs][n]
@@ -259,6 +260,7 @@ struct Barriers {
 // fill at least 90% of ceil(tiles / ctas) rounds of the CTAs; the fixup kernel takes the
 // same decision from the same numbers.
 __device__ __forceinline__ bool whole_tiles(const TcArgs &a) {
+    if (a.stream_k == 3) return true;
     if (a.stream_k != 2) return false;
     const int64_t t = a.nwork / a.nsb, rounds = (t + a.ctas - 1) / a.ctas;
     return 10 * t >= 9 * rounds * a.ctas;
@@ -299,7 +301,8 @@ __device__ __forceinline__ void store_segment(const TcArgs &a, const Seg &sg, in
     const int64_t col0 = ti.col0 + 32 * cq;
     if (a.n_out) {  // GLU (whole tiles only): columns 2i, 2i+1 are the gate and up dots of output col0/2 + i
         if (tl >= ti.rows) return;
-        float *dst = a.y + int64_t(ti.m0 + tl) * a.n_out + col0 / 2;
+        const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
+        float *dst = a.y + yrow * a.n_out + col0 / 2;
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             if (col0 / 2 + i < a.n_out) dst[i] = tot[i].x / (1.0f + expf(-tot[i].x)) * tot[i].y;
@@ -1492,6 +1495,64 @@ cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts,
     case QMM_Q6_K: return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
     default: return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup, st);
     }
+}
+
+// The fused gate/up form of the grouped GEMM (Q4_K): the tile space of an expert has 2 n
+// columns, column 2j its gate row j (tm_w over the experts' E n gate rows) and 2j + 1 its
+// up row j (tm_w2); a tile's raw rows are 64 gate rows and the 64 up rows of the same
+// outputs, and every tile is computed whole by one CTA (the GLU needs both dots).
+bool gemm_tc_grouped_glu_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k) {
+    return t == QMM_Q4_K && n_experts > 0 && n_experts * n < (int64_t(1) << 30) && k % 256 == 0 && n > 0;
+}
+
+cudaError_t launch_gemm_tc_grouped_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_experts, int64_t n,
+                                       int64_t k, const void *xq, int64_t x_div, int64_t n_pairs, float *y,
+                                       const MoETile *tiles, const int32_t *ntiles, const int32_t *bounds,
+                                       const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st) {
+    if (!gemm_tc_grouped_glu_supported(t, n_experts, n, k)) return cudaErrorNotSupported;
+    const int ctas = std::min(device_sm_count(), kMaxPartialCtas);
+    const TcLayout L = tc_layout(n_pairs, k, 0);
+    if (ws_bytes < L.total) return cudaErrorInvalidValue;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    __half *xh = reinterpret_cast<__half *>(base + L.xh);
+    float *dx = reinterpret_cast<float *>(base + L.dx);
+    __half *smin = reinterpret_cast<__half *>(base + L.smin);
+    const int64_t nblk = n_pairs * (k / 32);
+    const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
+    tc_prep_gather_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), (int)k, perm, bounds,
+                                                             (int)n_experts, (int)x_div, n_pairs, xh, dx, smin);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t row_bytes = (k / 256) * kQ4KBytes;
+    CUtensorMap tm_x, tm_xmin, tm_dx, tm_w, tm_w2;
+    if (!make_act_maps(tm_x, tm_xmin, tm_dx, xh, dx, smin, n_pairs, k) ||
+        !make_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wg, row_bytes, n_experts * n, kQ4KBytes, kTN / 2,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wu, row_bytes, n_experts * n, kQ4KBytes, kTN / 2,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    TcArgs args{};
+    tc_test_fault(args);
+    args.W = static_cast<const uint8_t *>(Wg);
+    args.n = 2 * n;  // tile space: gate and up columns of every output
+    args.m = n_pairs;
+    args.k = (int)k;
+    args.row_bytes = row_bytes;
+    args.y = y;
+    args.partial = nullptr;
+    args.status = status;
+    args.tiles_n = (2 * n + kTN - 1) / kTN;
+    args.nsb = k / 256;
+    args.nwork = 0;  // read from the device tile count by the kernels
+    args.ctas = ctas;
+    args.stream_k = 3;
+    args.tiles = tiles;
+    args.ntiles = ntiles;
+    args.bounds = bounds;
+    args.perm = perm;
+    args.n_out = n;
+    args.glu_packed = 0;
+    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, args, ctas, 0, st);
 }
 
 // ---------------------------------------------------------------- shared with the skinny path

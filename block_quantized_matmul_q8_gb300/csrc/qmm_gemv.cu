@@ -633,11 +633,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const uint8_t 
 // and writes the call's status word, so no reset precedes the launch.  Activation row
 // of pair p: xq row p / x_div (x_div = top_k: shared by a token's slots; 1: one row per
 // slot).
-template <int T>
+// GLU form (Wu != nullptr): W holds the experts' gate rows and Wu their up rows, and the
+// pair's row of y gets silu(gate dot) * up dot ([MMQ] section "「分专家」与「整批」之间:
+// host 侧的代价": the MoE FFN's gate and up products fused, the GLU applied after the dots).
+template <int T, bool GLU = false>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     gemv_id_kernel(const uint8_t *__restrict__ W, int n_experts, int64_t n, int k, int64_t row_bytes, int nstages,
                    const uint8_t *__restrict__ xq, int64_t x_div, const int32_t *__restrict__ ids, int n_pairs,
-                   float *__restrict__ y, int *status) {
+                   float *__restrict__ y, int *status, const uint8_t *__restrict__ Wu = nullptr) {
     const int64_t p = blockIdx.y;
     ptx::grid_dependency_wait();
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32) {
@@ -656,7 +659,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     XIn x;
     x.xq = xq + (p / x_div) * int64_t(k / 32) * kQ81Bytes;
     x.xf = nullptr;
-    gemv_tma_body<T, 1>(W + int64_t(e) * n * row_bytes, n, k, row_bytes, nstages, x, yp, n, status);
+    if constexpr (GLU)
+        gemv_tma_body<T, 1, true>(W + int64_t(e) * n * row_bytes, n, k, row_bytes, nstages, x, yp, n, status,
+                                  Wu + int64_t(e) * n * row_bytes);
+    else
+        gemv_tma_body<T, 1>(W + int64_t(e) * n * row_bytes, n, k, row_bytes, nstages, x, yp, n, status);
 }
 
 // Rows that a bulk-copy GEMV can stream: every chunk must start on and span whole
@@ -735,7 +742,8 @@ static cudaError_t launch_gemv_id_t(const void *W, int64_t n_experts, int64_t n,
         1, std::min<int64_t>((n + 1) / 2, (device_sm_count() + n_pairs - 1) / n_pairs));
     return launch_pdl(kern, dim3((unsigned)per_pair, (unsigned)n_pairs), dim3(kTmaThreads), smem, st,
                       static_cast<const uint8_t *>(W), (int)n_experts, n, (int)k, row_bytes, nstages,
-                      static_cast<const uint8_t *>(xq), x_div, ids, (int)n_pairs, y, status);
+                      static_cast<const uint8_t *>(xq), x_div, ids, (int)n_pairs, y, status,
+                      static_cast<const uint8_t *>(nullptr));
 }
 
 template <int T, int NC>
@@ -871,6 +879,28 @@ cudaError_t launch_gemv_id(qmm_type t, const void *W, int64_t n_experts, int64_t
     case QMM_Q5_K: return launch_gemv_id_t<QMM_Q5_K>(W, n_experts, n, k, xq, x_div, ids, n_pairs, y, status, st);
     }
     return cudaErrorInvalidValue;
+}
+
+// The fused gate/up form of the decode MoE GEMV (Q4_K; both tensors [E][n] rows).
+bool gemv_id_glu_supported(qmm_type t, int64_t n, int64_t k) { return gemv_glu_supported(t, n, k, 1); }
+
+cudaError_t launch_gemv_id_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_experts, int64_t n, int64_t k,
+                               const void *xq, int64_t x_div, const int32_t *ids, int64_t n_pairs, float *y,
+                               int *status, cudaStream_t st) {
+    if (!gemv_id_glu_supported(t, n, k)) return cudaErrorNotSupported;
+    const int64_t row_bytes = gemv_tma_row_bytes<QMM_Q4_K>(n, k);
+    const int nstages = gemv_tma_stages(row_bytes, k, 1, size_t(device_smem_optin()));
+    const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, 1);
+    auto kern = gemv_id_kernel<QMM_Q4_K, true>;
+    cudaError_t e = ensure_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    // enough CTAs per pair to cover the SMs once, at least one output each
+    const int64_t per_pair =
+        std::max<int64_t>(1, std::min<int64_t>(n, (device_sm_count() + n_pairs - 1) / n_pairs));
+    return launch_pdl(kern, dim3((unsigned)per_pair, (unsigned)n_pairs), dim3(kTmaThreads), smem, st,
+                      static_cast<const uint8_t *>(Wg), (int)n_experts, n, (int)k, row_bytes, nstages,
+                      static_cast<const uint8_t *>(xq), x_div, ids, (int)n_pairs, y, status,
+                      static_cast<const uint8_t *>(Wu));
 }
 
 }  // namespace qmm

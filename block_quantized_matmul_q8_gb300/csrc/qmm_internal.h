@@ -71,6 +71,12 @@ bool gemv_id_supported(qmm_type t, int64_t n, int64_t k);
 cudaError_t launch_gemv_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                            int64_t x_div, const int32_t *ids, int64_t n_pairs, float *y, int *status,
                            cudaStream_t st);
+// Its fused gate/up form (Q4_K): pair p's row of y is silu(gate dot) * up dot, with the
+// experts' gate rows in Wg and their up rows in Wu (both [E][n] rows).
+bool gemv_id_glu_supported(qmm_type t, int64_t n, int64_t k);
+cudaError_t launch_gemv_id_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_experts, int64_t n, int64_t k,
+                               const void *xq, int64_t x_div, const int32_t *ids, int64_t n_pairs, float *y,
+                               int *status, cudaStream_t st);
 
 // Multi-column GEMV on the warp-level MMA (Q4_K, 2 <= m <= 8, q8_1 activations): 16 weight
 // rows x 8 columns per mma.sync m16n8k16 on exact integer operands, then the fp32 fold.
@@ -123,6 +129,12 @@ cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts,
                                    int64_t x_div, int64_t n_pairs, float *y, const MoETile *tiles,
                                    const int32_t *ntiles, int64_t max_token_tiles, const int32_t *bounds,
                                    const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st);
+// Its fused gate/up form (Q4_K): y[pair][n] = silu(gate dot) * up dot, whole tiles only.
+bool gemm_tc_grouped_glu_supported(qmm_type t, int64_t n_experts, int64_t n, int64_t k);
+cudaError_t launch_gemm_tc_grouped_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_experts, int64_t n,
+                                       int64_t k, const void *xq, int64_t x_div, int64_t n_pairs, float *y,
+                                       const MoETile *tiles, const int32_t *ntiles, const int32_t *bounds,
+                                       const int32_t *perm, int *status, void *ws, size_t ws_bytes, cudaStream_t st);
 
 // MoE: device bucketing + grouped GEMM, or one GEMV per pair for a handful of pairs.
 // x_per_slot: xq holds one activation row per (token, slot) pair instead of one per token.
@@ -130,6 +142,13 @@ size_t moe_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, i
 cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int64_t n, int64_t k, const void *xq,
                               const int32_t *ids, int64_t top_k, int64_t n_tokens, bool x_per_slot, float *y,
                               void *ws, size_t ws_bytes, cudaStream_t st);
+// Fused gate/up + SwiGLU of mul_mat_id: y[t][s][n] = silu(x Wg[e]^T) * (x Wu[e]^T) with
+// e = ids[t][s]: one fused GEMV per pair for a handful of pairs, the fused grouped
+// tensor-core GEMM (Q4_K), else both products into the workspace and a combine pass.
+size_t moe_glu_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k);
+cudaError_t launch_mul_mat_id_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_experts, int64_t n, int64_t k,
+                                  const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, bool x_per_slot,
+                                  float *y, void *ws, size_t ws_bytes, cudaStream_t st);
 // Argument checks of qmm_mul_mat_id shared by its entry points.
 qmm_status moe_check_sizes(qmm_type t, int64_t n_experts, int64_t n, int64_t k, int64_t top_k, int64_t n_tokens);
 qmm_status moe_check_pointers(const void *W_experts, const void *xq, const int32_t *ids, const float *y);

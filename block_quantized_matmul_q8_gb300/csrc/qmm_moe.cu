@@ -286,4 +286,114 @@ cudaError_t launch_mul_mat_id(qmm_type t, const void *W, int64_t n_experts, int6
                                   status + 3, bounds, perm, y, status, base + L.cold_gemm, L.total - L.cold_gemm, st);
 }
 
+// ---------------------------------------------------------------- fused gate/up (SwiGLU)
+
+// Unfused SwiGLU of two products in the workspace: y = silu(g) * u.
+__global__ void moe_glu_combine_kernel(const float *__restrict__ g, const float *__restrict__ u, int64_t total,
+                                       float *__restrict__ y) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x)
+        y[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
+}
+
+// The cold experts' SwiGLU: rows of their pairs from the gate and up products.
+__global__ void moe_glu_cold_combine_kernel(const int32_t *__restrict__ cold, const int32_t *__restrict__ ncold,
+                                            const int32_t *__restrict__ bounds, const int32_t *__restrict__ perm,
+                                            const float *__restrict__ g, const float *__restrict__ u,
+                                            float *__restrict__ y, int64_t n) {
+    const int nc = *ncold;
+    for (int c = blockIdx.x; c < nc; c += gridDim.x) {
+        const int e = cold[c];
+        for (int j = bounds[e]; j < bounds[e + 1]; ++j) {
+            const int64_t off = int64_t(perm[j]) * n;
+            for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+                const float gv = g[off + i];
+                y[off + i] = gv / (1.0f + expf(-gv)) * u[off + i];
+            }
+        }
+    }
+}
+
+enum MoeGluPath { kMoeGluGemv = 1, kMoeGluTc = 2, kMoeGluUnfused = 3 };
+static int moe_glu_path(qmm_type t, int64_t n_experts, int64_t n, int64_t k, int64_t n_pairs) {
+    if (n_pairs <= kMoeGemvMaxPairs && gemv_id_glu_supported(t, n, k)) return kMoeGluGemv;
+    if (gemm_tc_grouped_glu_supported(t, n_experts, n, k)) return kMoeGluTc;
+    return kMoeGluUnfused;
+}
+
+// Unfused layout: the mul_mat_id workspace first (its status word stays at offset 0),
+// then the gate and up products [pairs][n].
+size_t moe_glu_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts, int64_t top_k) {
+    const int64_t n_pairs = n_tokens * top_k;
+    switch (moe_glu_path(t, n_experts, n, k, n_pairs)) {
+    case kMoeGluGemv: return 256;  // the status word
+    case kMoeGluTc: {
+        // the cold experts' gate and up products after the layout, when they take the skinny kernel
+        const bool split = gemv_tc_grouped_supported(t, n_experts, n, k);
+        return moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k),
+                          cold_bytes(t, n_experts, n, k))
+                   .total +
+               (split ? 2 * align256(size_t(n_pairs) * size_t(n) * 4) : 0);
+    }
+    default:
+        return align256(moe_workspace_bytes(t, n, k, n_tokens, n_experts, top_k)) +
+               2 * align256(size_t(n_pairs) * size_t(n) * 4);
+    }
+}
+
+cudaError_t launch_mul_mat_id_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_experts, int64_t n, int64_t k,
+                                  const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens, bool x_per_slot,
+                                  float *y, void *ws, size_t ws_bytes, cudaStream_t st) {
+    const int64_t n_pairs = n_tokens * top_k;
+    const int64_t x_div = x_per_slot ? 1 : top_k;
+    const int path = moe_glu_path(t, n_experts, n, k, n_pairs);
+    if (ws_bytes < moe_glu_workspace_bytes(t, n, k, n_tokens, n_experts, top_k)) return cudaErrorInvalidValue;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    if (path == kMoeGluGemv)
+        return launch_gemv_id_glu(t, Wg, Wu, n_experts, n, k, xq, x_div, ids, n_pairs, y,
+                                  reinterpret_cast<int32_t *>(base + kStatusOffset), st);
+    if (path == kMoeGluTc) {
+        // experts with more than 16 pairs on the fused grouped GEMM; the others (cold) on the
+        // skinny kernel, once for the gate and once for the up weights, then the combine
+        const bool split = gemv_tc_grouped_supported(t, n_experts, n, k);
+        const MoELayout L = moe_layout(n_pairs, n_experts, kTcTileTokens, gemm_tc_grouped_bytes(n_pairs, k),
+                                       cold_bytes(t, n_experts, n, k));
+        cudaError_t e =
+            launch_moe_bucket(ids, n_pairs, (int)n_experts, kTcTileTokens, split ? kColdMaxPairs : 0, ws, L, st);
+        if (e != cudaSuccess) return e;
+        int32_t *status = reinterpret_cast<int32_t *>(base + L.status);
+        const int32_t *bounds = reinterpret_cast<const int32_t *>(base + L.bounds);
+        const int32_t *perm = reinterpret_cast<const int32_t *>(base + L.perm);
+        const MoETile *tiles = reinterpret_cast<const MoETile *>(base + L.tiles);
+        moe_zero_invalid_kernel<<<64, 256, 0, st>>>(status, perm, bounds, (int)n_experts, y, n);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        e = launch_gemm_tc_grouped_glu(t, Wg, Wu, n_experts, n, k, xq, x_div, n_pairs, y, tiles, status + 1, bounds,
+                                       perm, status, base + L.gemm, L.cold_gemm - L.gemm, st);
+        if (e != cudaSuccess || !split) return e;
+        const int32_t *cold = reinterpret_cast<const int32_t *>(base + L.cold);
+        float *g = reinterpret_cast<float *>(base + L.total);
+        float *u = reinterpret_cast<float *>(base + L.total + align256(size_t(n_pairs) * size_t(n) * 4));
+        for (int h = 0; h < 2; ++h) {
+            e = launch_gemv_tc_grouped(h ? Wu : Wg, n_experts, n, k, xq, x_div, cold, status + 3, bounds, perm,
+                                       h ? u : g, status, base + L.cold_gemm, L.total - L.cold_gemm, st);
+            if (e != cudaSuccess) return e;
+        }
+        const int grid = (int)std::min<int64_t>(n_experts, int64_t(device_sm_count()) * 2);
+        moe_glu_cold_combine_kernel<<<std::max(grid, 1), 256, 0, st>>>(cold, status + 3, bounds, perm, g, u, y, n);
+        return cudaGetLastError();
+    }
+    // unfused: both products through mul_mat_id, then y = silu(g) * u (invalid pairs: 0 * 0)
+    const size_t inner = align256(moe_workspace_bytes(t, n, k, n_tokens, n_experts, top_k));
+    float *g = reinterpret_cast<float *>(base + inner);
+    float *u = reinterpret_cast<float *>(base + inner + align256(size_t(n_pairs) * size_t(n) * 4));
+    cudaError_t e = launch_mul_mat_id(t, Wg, n_experts, n, k, xq, ids, top_k, n_tokens, x_per_slot, g, ws, inner, st);
+    if (e != cudaSuccess) return e;
+    e = launch_mul_mat_id(t, Wu, n_experts, n, k, xq, ids, top_k, n_tokens, x_per_slot, u, ws, inner, st);
+    if (e != cudaSuccess) return e;
+    const int64_t total = n_pairs * n;
+    const int grid = (int)std::min<int64_t>((total + 255) / 256, int64_t(device_sm_count()) * 8);
+    moe_glu_combine_kernel<<<std::max(grid, 1), 256, 0, st>>>(g, u, total, y);
+    return cudaGetLastError();
+}
+
 }  // namespace qmm

@@ -288,6 +288,29 @@ QMM_API qmm_status qmm_mul_mat_id_slot(const void *W_experts, qmm_type t, int64_
                                        void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Expert-routed fused gate/up with SwiGLU ([MMQ] section "「分专家」与「整批」之间: host
+ * 侧的代价": in the MoE FFN the gate and up products of a tile are formed together and
+ * the GLU applied right after the dots; [P0007] Coverage: fused ffn gate/up/SWIGLU):
+ *   y[t][s][j] = silu(g) * u,  g = x[t] . dequant(W_gate[e])[j],  u = x[t] . dequant(W_up[e])[j],
+ *   e = ids[t][s], silu(g) = g / (1 + exp(-g)).
+ *   W_gate, W_up : device, each [n_experts][n][k/QK] blocks of type t (the experts' gate
+ *                  and up weights, one tensor each), 16-byte aligned
+ *   xq, ids, top_k, n_tokens, y : as qmm_mul_mat_id (x shared by a token's slots)
+ *   workspace    : device, 256-byte aligned, at least qmm_workspace_bytes_id_glu(...)
+ *                  bytes; its status word reads as for qmm_mul_mat_id
+ * Paths: one fused GEMV per (token, slot) pair for n_tokens * top_k <= 32 (Q4_K); the
+ * fused expert-grouped tensor-core GEMM (Q4_K; every expert on 128-pair tiles, each tile
+ * computed whole); otherwise both products into the workspace and a combine pass.  An id
+ * outside [0, n_experts) gives a zero row and QMM_ERR_IDS in the status word.  Errors as
+ * qmm_mul_mat_id; W_up must be given.
+ */
+QMM_API size_t qmm_workspace_bytes_id_glu(qmm_type t, int64_t n, int64_t k, int64_t n_tokens, int64_t n_experts,
+                                          int64_t top_k);
+QMM_API qmm_status qmm_mul_mat_id_glu(const void *W_gate, const void *W_up, qmm_type t, int64_t n_experts, int64_t n,
+                                      int64_t k, const void *xq, const int32_t *ids, int64_t top_k, int64_t n_tokens,
+                                      float *y, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * qmm_mul_mat_id without a workspace argument, for callers that cannot allocate
  * device memory where they make this call (a fixed memory pool owned by someone
  * else, a plugin that may not call cudaMalloc, code that runs between graph
@@ -323,7 +346,7 @@ QMM_API qmm_status qmm_read_device_status(const void *workspace, int32_t *status
 
 /* The same status word as the return value: QMM_OK, QMM_ERR_IDS (a routing id was
  * outside [0, n_experts)) or QMM_ERR_DEVICE (a kernel gave up on a bounded wait), as
- * written by the last qmm_mul_mat_id / qmm_mul_mat_id_slot enqueued on this workspace
+ * written by the last qmm_mul_mat_id / qmm_mul_mat_id_slot / qmm_mul_mat_id_glu enqueued on this workspace
  * and `stream`.  Synchronises `stream` (a host read of a device flag has to wait for
  * the writer).  QMM_ERR_ARG for a NULL workspace, QMM_ERR_CUDA if the read fails, so a
  * caller that must tell a failed read from a device error uses qmm_read_device_status. */

@@ -293,5 +293,16 @@ def mul_mat_id(W, fmt, n_experts, n, k, xq, ids, per_slot=False):
     return y, T, int(bad)
 
 
+def mul_mat_id_glu(W_gate, W_up, fmt, n_experts, n, k, xq, ids):
+    """(y, tol, n_invalid), y and tol fp64 [n_tokens][top_k][n]: the expert-routed SwiGLU
+    y[t][s] = silu(g) * u with g, u the folds of expert ids[t][s]'s gate and up rows
+    against token t's row of xq, and tol the bound of mul_mat_glu per element.  Pairs with
+    an invalid id have g = u = 0, hence y = 0 and tol = 0."""
+    g, Tg, bad = mul_mat_id(W_gate, fmt, n_experts, n, k, xq, ids)
+    u, Tu, _ = mul_mat_id(W_up, fmt, n_experts, n, k, xq, ids)
+    y, tol = _glu(g, Tg, u, Tu)
+    return y, tol, bad
+
+
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))

@@ -414,6 +414,31 @@ def test_mul_mat_glu_at_matches_full(oracle_mod):
     assert np.array_equal(ya, y[cols, rows]) and np.array_equal(ta, tol[cols, rows])
 
 
+@pytest.mark.parametrize("fmt", ["q4_K", "q8_0"])
+def test_mul_mat_id_glu_is_the_dense_glu_per_pair(oracle_mod, fmt):
+    """The expert-routed SwiGLU is the (pinned) dense SwiGLU of each pair's expert and
+    token: y[t][s] and its bound equal mul_mat_glu on W_gate[e], W_up[e] and x[t]; a pair
+    with an invalid id has y = 0 and bound 0."""
+    E, n, k, T_, K = 5, 9, 512, 4, 3
+    rng = np.random.default_rng(47)
+    Wg = qmm_synth.gen_weights(fmt, rng, E * n, k).reshape(E, n, -1)
+    Wu = qmm_synth.gen_weights(fmt, rng, E * n, k).reshape(E, n, -1)
+    xq = oracle_mod.quantize_q8_1(qmm_synth.gen_x(rng, T_, k))
+    ids = rng.integers(0, E, size=(T_, K)).astype(np.int32)
+    ids[1, 2] = E  # invalid
+    y, tol, bad = oracle_mod.mul_mat_id_glu(Wg, Wu, fmt, E, n, k, xq, ids)
+    assert bad == 1
+    rb = xq.reshape(T_, -1)
+    for t in range(T_):
+        for s_ in range(K):
+            e = ids[t, s_]
+            if e >= E:
+                assert not y[t, s_].any() and not tol[t, s_].any()
+                continue
+            yd, td = oracle_mod.mul_mat_glu(Wg[e], Wu[e], fmt, n, k, rb[t:t + 1], 1)
+            assert np.array_equal(y[t, s_], yd[0]) and np.array_equal(tol[t, s_], td[0])
+
+
 def test_mul_mat_glu_gate_and_up_roles(oracle_mod):
     """Gate rows equal to the up rows with d and dmin doubled (exact in fp16) make every
     gate dot exactly twice the up dot, so y = silu(2u) * u: a reference that swapped the
