@@ -1,33 +1,46 @@
-// qmm_gemv_mma.cu -- multi-column GEMV (2 <= m <= 8 activation columns) for Q4_K on the
+// qmm_gemv_mma.cu -- multi-column GEMV (1 <= m <= 8 activation columns) for Q4_K on the
 // warp-level tensor-core MMA.
 //
 // The speculative-verify batch of [P0007] ("How", "Speculative decoding": 2-8 columns,
-// each weight unpacked once and reused for every column) has the weight read once and
-// the work per weight growing with the column count.  On CUDA cores every extra column
+// each weight unpacked once and reused for every column) reads the weights once while
+// the work per weight grows with the column count.  On CUDA cores every extra column
 // costs one more set of exact dp4a dots per weight; here the columns are the N = 8 side of
 // an `mma.sync m16n8k16` with fp16 operands and fp32 accumulation, so one instruction forms
-// the dots of 16 weight rows with all 8 columns, and the per-column cost disappears.
+// the dots of 16 weight rows with all 8 columns and the per-column cost disappears.
 //
 // Exactness ([MMQ] sections "dp4a 路径的 Q4_K" and "输出端: 写回与 scale 修正": exact integer
 // sub-block dots, then the fp32 fold with the block scales).  The operands are integers:
 //   B (activations): the q8_1 codes, |q| <= 127, exact in fp16.
 //   A (weights): a nibble byte v becomes the fp16 1024 + (v & 15) for the low nibble and
 //     1024 + (v & 0xf0) = 1024 + 16 q for the high one, by OR-ing the nibble bits into the
-//     exponent pattern of 1024 (two logic ops per 4 bytes, no conversion instructions).
+//     exponent pattern of 1024 (no conversion instructions).
 //   C (accumulator input): -1024 * sum(q_x) of the 32-block, exact.
-// Every product is an integer below 1264 * 127 and every partial sum below 2^24, so the
-// fp32 accumulator ends on exactly sum_i q_w,i q_x,i of the low sub-block (16 times it for
-// the high one) whatever order the tensor core adds in.  The fold is then the method's:
-//   y += d sc_b d8_b sumi_b - dmin m_b s_b   per 32-wide sub-block b.
+// Every product is an integer of at most 1264 * 127 and every partial sum stays below
+// 4064 * 1024 + 32 * 1264 * 127 < 2^24, so the fp32 accumulator ends on exactly
+// sum_i q_w,i q_x,i of a low sub-block (16 times it for a high one) in any order of
+// addition.  The fold is then the method's, per 32-wide sub-block b:
+//   y += d sc_b d8_b sumi_b - dmin m_b s_b,
+// with the min term sum_b m_b s_b of a superblock formed by one more MMA (the 6-bit mins
+// as A, the q8_1 s values as B; 8 real terms, 8 zeros).
 //
-// Layout.  One persistent CTA per SM owns a contiguous range of rows (whole 8-row groups).
-// A producer warp streams chunks of 16 rows x 4 superblocks (576 bytes of each row, one
-// 2-D tensor-map box) through a ring of shared-memory stages.  Each of the 16 consumer
-// warps takes one 64-value unit (two sub-blocks) of every chunk for the tile's 16 rows
-// (MMA M = 16) and keeps its share of the 16 x 8 results in registers over the tile's
-// chunks; at the end of a tile the 16 shares are summed through shared memory.  The
-// activations are staged once per CTA as fp16 in the order of the B fragments, with the
-// per-block factors d8, s and -1024 sum(q) next to them.
+// The k index inside an MMA is a free permutation as long as A and B use the same one:
+// lane (g, t) supplies, for K16 step ks of a 32-byte chunk of nibbles, the 4 bytes
+// 8t + 4ks .. 8t + 4ks + 3 (bytes 0, 2 at MMA positions 2t, 2t+1, bytes 1, 3 at 2t+8, 2t+9,
+// which puts each nibble under its fp16 half with one shift), so a lane's weights for both
+// steps are one 8-byte load per row, and its activations, staged as fp16 in the order
+// 0 2 1 3 of every 4 codes, one 16-byte load.
+//
+// Layout.  One persistent CTA per SM owns a contiguous range of 16-row tiles.  A producer
+// warp streams whole tiles (16 rows x all of k, one bulk copy per row) through a ring of
+// shared-memory stages.  All 16 consumer warps work on every tile, each taking whole
+// superblocks of it (superblock j of tile t goes to warp (t nsb + j) mod 16, so the warps'
+// shares even out over the tiles), and writes its 16 x 8 partial results to its own slot of
+// the stage.  Once all 16 have released the stage, the producer warp sums the 16 slots in
+// warp order (so the result does not depend on timing), writes the tile's outputs and
+// reuses the stage.  Every consumer warp waits for every
+// tile, so a stage's earlier tile has always landed when a warp waits for its next one.
+// The activations are staged once per CTA: the m columns' q8_1 codes as fp16, and per block
+// d8, -1024 sum(q) and s.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -36,44 +49,68 @@
 
 #include "qmm_common.cuh"
 #include "qmm_internal.h"
-#include "qmm_tc_common.cuh"
 #include "qmm_tc_ptx.cuh"
 
 namespace qmm {
 namespace {
 
-constexpr int kMmaWarps = 16;                            // consumer warps: one unit of a chunk each
-constexpr int kMmaThreads = (kMmaWarps + 1) * 32;        // plus the producer warp
-constexpr int kTileRows = 16;                            // MMA M: weight rows of a tile
-constexpr int kChunkSb = 4;                              // superblocks per chunk: 16 units
-constexpr int kRowChunk = kChunkSb * kQ4KBytes;          // 576 bytes of a row per chunk
-constexpr int kStageBytes = kTileRows * kRowChunk;       // 9216
-constexpr int kMaxStages = 16;
-constexpr int kMinStages = 4;
-constexpr int kFacBytes = 4 * 3 * 16;                    // per unit: 4 column pairs x 3 float4
-constexpr int kRedBytes = 2 * kMmaWarps * 32 * 16;       // two buffers of 16 warps x 32 lanes x float4
+constexpr int kMmaWarps = 16;                      // consumer warps
+constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // plus the producer warp
+constexpr int kTileRows = 16;                      // MMA M: weight rows of a tile
+constexpr int kCols = 8;                           // MMA N: activation columns (missing ones zero)
+constexpr int kMaxStages = 8;
+constexpr int kMinStages = 2;
 
-__host__ __device__ inline int64_t mma_units(int64_t k) {  // units staged: whole chunks of 16
-    return ((k / 256 + kChunkSb - 1) / kChunkSb) * kChunkSb * 4;
+// Shared-memory plan for a row length k: rows and activation columns padded so that their
+// strides are 8 words past a multiple of 32 words (the 4 rows or columns that the 16 lanes of
+// a half-warp read start on different bank groups).
+struct MmaPlan {
+    int nstages;
+    int64_t row_stride, x_stride;
+    size_t fixed, stage_bytes, smem;
+};
+// bytes rounded up so that bytes / 4 is `res` past a multiple of 32 (bytes a multiple of 16)
+int64_t pad_to_bank(int64_t bytes, int res) {
+    const int64_t w = (bytes / 4) % 32;
+    return bytes + 4 * ((res - w + 32) % 32);
 }
-
-size_t mma_x_bytes(int64_t k, int m) { return size_t(mma_units(k)) * (size_t(m) * 128 + kFacBytes); }
-
-int mma_stages(int64_t k, int m, size_t budget) {
-    const size_t fixed = 1024 + mma_x_bytes(k, m) + kRedBytes;
-    if (fixed >= budget) return 0;
-    const int st = (int)std::min<size_t>(kMaxStages, (budget - fixed) / kStageBytes);
-    return st >= kMinStages ? st : 0;
+bool mma_plan(int64_t k, int m, size_t budget, MmaPlan &p) {
+    if (k <= 0 || k % 256 || m < 1 || m > kCols) return false;
+    if (budget <= 2048) return false;
+    budget -= 1024;  // the kernel's static shared memory (barriers), rounded up
+    const int64_t nb32 = k / 32, row_bytes = (k / 256) * kQ4KBytes;
+    // weight rows 8 words apart in bank terms: the 4 rows a half-warp reads; fp16 activation
+    // columns 16 words apart: the 2 columns a quarter-warp reads
+    p.row_stride = pad_to_bank(row_bytes, 8);
+    p.x_stride = pad_to_bank(2 * k, 16);
+    // staged codes [m][x_stride], factors [nb32][8] float2, s [8][nb32] fp16
+    p.fixed = 1024 + size_t(m) * p.x_stride + size_t(nb32) * kCols * 8 + size_t(kCols) * nb32 * 2;
+    p.stage_bytes = size_t(kTileRows) * p.row_stride;
+    if (p.fixed >= budget) return false;
+    // per stage: the tile's rows and each consumer warp's 16 x 8 fp32 partial sums
+    const int64_t st = int64_t(budget - p.fixed) / int64_t(p.stage_bytes + kMmaWarps * kTileRows * kCols * 4);
+    p.nstages = (int)std::min<int64_t>(st, kMaxStages);
+    p.smem = p.fixed + size_t(p.nstages) * (p.stage_bytes + kMmaWarps * kTileRows * kCols * 4);
+    return p.nstages >= kMinStages;
 }
 
 // d += A B for one m16n8k16 tile (fp16 operands, fp32 accumulator, in place).
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d = A B + c (c0 for rows g, c1 for rows g + 8 of columns 2t, 2t+1): the first K16 step of a
+// sub-block, the accumulator input read from the factor registers without copies.
+__device__ __forceinline__ void mma_16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1, float c0, float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%10,%11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
 }
 
 // (v & mask) | 0x64006400 in one logic op: the nibble bits under the fp16 pattern of 1024.
@@ -83,36 +120,135 @@ __device__ __forceinline__ uint32_t nib_f16(uint32_t v, uint32_t mask) {
     return r;
 }
 
-// Staged activation column c of unit u: 64 fp16 codes, 16-byte chunk j (j = 0..3 the low
-// 32-block, 4..7 the high one) holding the 8 codes 8(j & 3) .. 8(j & 3) + 7 of its block in
-// the order 0 2 1 3 4 6 5 7, which is the order in which the A fragments take the bytes of a
-// weight word.  Odd columns swap the two halves (chunk j at j ^ 4), so that the 8 lanes of a
-// quarter-warp, 2 columns x 4 chunks, read 8 different bank groups.
-__device__ __forceinline__ int xh_chunk(int c, int j) { return j ^ ((c & 1) << 2); }
+// Four int8 codes (one word) as two fp16 pairs in the order (0, 2), (1, 3).
+__device__ __forceinline__ uint2 codes_f16_0213(uint32_t w) {
+    const int q0 = (int8_t)(w & 0xffu), q1 = (int8_t)((w >> 8) & 0xffu);
+    const int q2 = (int8_t)((w >> 16) & 0xffu), q3 = (int8_t)(w >> 24);
+    const __half2 a = __halves2half2(__int2half_rn(q0), __int2half_rn(q2));
+    const __half2 b = __halves2half2(__int2half_rn(q1), __int2half_rn(q3));
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+}
+
+// Shared-memory accesses by 32-bit shared addresses (the hot loop's address arithmetic stays
+// in 32 bits and every access is a shared one).
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts64(uint32_t a, float2 v) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(v.x), "f"(v.y) : "memory");
+}
+
+// One superblock (j) of the 16-row tile: rows g and g + 8 of the lane (blk, blk8 point at the
+// superblock in the two staged rows), B column g (xg: its staged fp16 codes, xv false for a
+// column past m, whose codes are zero), the factor table and the s values of the column (sg).
+// tot01: (row g, cols 2t, 2t+1), tot23: (row g+8, cols 2t, 2t+1).
+__device__ __forceinline__ void fold_superblock(uint32_t blk, uint32_t blk8, uint32_t xg, bool xv, uint32_t fz,
+                                                uint32_t sg, int j, int t, float2 &tot01, float2 &tot23) {
+    const uint4 h0 = lds128(blk), h8 = lds128(blk8);
+    // the 6-bit scales and mins, four per word: sub-blocks 0..3 and 4..7 (GGUF packing)
+    const uint32_t sl0 = h0.y & 0x3f3f3f3fu, ml0 = h0.z & 0x3f3f3f3fu;
+    const uint32_t sh0 = (h0.w & 0x0f0f0f0fu) | ((h0.y >> 2) & 0x30303030u);
+    const uint32_t mh0 = ((h0.w >> 4) & 0x0f0f0f0fu) | ((h0.z >> 2) & 0x30303030u);
+    const uint32_t sl8 = h8.y & 0x3f3f3f3fu, ml8 = h8.z & 0x3f3f3f3fu;
+    const uint32_t sh8 = (h8.w & 0x0f0f0f0fu) | ((h8.y >> 2) & 0x30303030u);
+    const uint32_t mh8 = ((h8.w >> 4) & 0x0f0f0f0fu) | ((h8.z >> 2) & 0x30303030u);
+    const float d0 = half_lo(h0.x), dmin0 = half_hi(h0.x);
+    const float d8r = half_lo(h8.x), dmin8 = half_hi(h8.x);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {  // 32-byte chunk c of nibbles: sub-blocks 2c (low) and 2c + 1 (high)
+        const uint2 w0 = lds64(blk + 16 + 32 * c + 8 * t), w8 = lds64(blk8 + 16 + 32 * c + 8 * t);
+        const int blo = 8 * j + 2 * c;  // the 32-blocks of x under the two sub-blocks
+        const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 xa = xv ? lds128(xg + 64 * blo + 16 * t) : zero4;
+        const uint4 xb = xv ? lds128(xg + 64 * (blo + 1) + 16 * t) : zero4;
+        // {d8, -1024 sum q} of columns 2t and 2t + 1
+        const float4 fl = lds128f(fz + (blo * kCols + 2 * t) * 8);
+        const float4 fh = lds128f(fz + ((blo + 1) * kCols + 2 * t) * 8);
+        float clo[4], chi[4];
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const uint32_t a = ks ? w0.y : w0.x, a8 = ks ? w8.y : w8.x;
+            const uint32_t as = a >> 8, a8s = a8 >> 8;  // bytes 1, 3 under the halves
+            const uint32_t bl0 = ks ? xa.z : xa.x, bl1 = ks ? xa.w : xa.y;
+            const uint32_t bh0 = ks ? xb.z : xb.x, bh1 = ks ? xb.w : xb.y;
+            const uint32_t l0 = nib_f16(a, 0x000f000fu), l1 = nib_f16(a8, 0x000f000fu);
+            const uint32_t l2 = nib_f16(as, 0x000f000fu), l3 = nib_f16(a8s, 0x000f000fu);
+            const uint32_t h0_ = nib_f16(a, 0x00f000f0u), h1_ = nib_f16(a8, 0x00f000f0u);
+            const uint32_t h2_ = nib_f16(as, 0x00f000f0u), h3_ = nib_f16(a8s, 0x00f000f0u);
+            if (ks == 0) {  // the accumulators start at -1024 sum(q) of each column's block
+                mma_16816_c(clo, l0, l1, l2, l3, bl0, bl1, fl.y, fl.w);
+                mma_16816_c(chi, h0_, h1_, h2_, h3_, bh0, bh1, fh.y, fh.w);
+            } else {
+                mma_16816(clo, l0, l1, l2, l3, bl0, bl1);
+                mma_16816(chi, h0_, h1_, h2_, h3_, bh0, bh1);
+            }
+        }
+        // d sc d8 per (row, column): the high sub-block's dot is 16 times its sumi
+        const uint32_t s0w = c < 2 ? sl0 : sh0, s8w = c < 2 ? sl8 : sh8;
+        const int sb0 = 8 * ((2 * c) & 3), sb1 = 8 * ((2 * c + 1) & 3);
+        const float al0 = d0 * (float)((s0w >> sb0) & 0xffu), ah0 = d0 * 0.0625f * (float)((s0w >> sb1) & 0xffu);
+        const float al8 = d8r * (float)((s8w >> sb0) & 0xffu), ah8 = d8r * 0.0625f * (float)((s8w >> sb1) & 0xffu);
+        const float2 d8l = make_float2(fl.x, fl.z), d8h = make_float2(fh.x, fh.z);
+        tot01 = __ffma2_rn(__fmul2_rn(make_float2(al0, al0), d8l), make_float2(clo[0], clo[1]), tot01);
+        tot01 = __ffma2_rn(__fmul2_rn(make_float2(ah0, ah0), d8h), make_float2(chi[0], chi[1]), tot01);
+        tot23 = __ffma2_rn(__fmul2_rn(make_float2(al8, al8), d8l), make_float2(clo[2], clo[3]), tot23);
+        tot23 = __ffma2_rn(__fmul2_rn(make_float2(ah8, ah8), d8h), make_float2(chi[2], chi[3]), tot23);
+    }
+    // min term: sum_b m_b s_b by one MMA; A row g = mins of sub-blocks 2t, 2t+1 at positions
+    // 2t, 2t+1 (positions 8..15 zero), B column g = the s values of the same blocks
+    const uint32_t sel = (t & 1) ? 0x4342u : 0x4140u;
+    uint32_t m0 = __byte_perm(t < 2 ? ml0 : mh0, 0u, sel) | 0x64006400u;
+    uint32_t m8 = __byte_perm(t < 2 ? ml8 : mh8, 0u, sel) | 0x64006400u;
+    const __half2 k1024 = __float2half2_rn(1024.f);
+    const __half2 mf0 = __hsub2(*reinterpret_cast<__half2 *>(&m0), k1024);
+    const __half2 mf8 = __hsub2(*reinterpret_cast<__half2 *>(&m8), k1024);
+    const uint32_t sv = lds32(sg + 2 * (8 * j + 2 * t));
+    float cm[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_16816(cm, *reinterpret_cast<const uint32_t *>(&mf0), *reinterpret_cast<const uint32_t *>(&mf8), 0u, 0u, sv,
+              0u);
+    tot01 = __ffma2_rn(make_float2(-dmin0, -dmin0), make_float2(cm[0], cm[1]), tot01);
+    tot23 = __ffma2_rn(make_float2(-dmin8, -dmin8), make_float2(cm[2], cm[3]), tot23);
+}
 
 __global__ void __launch_bounds__(kMmaThreads, 1)
-    gemv_q4k_mma_kernel(const __grid_constant__ CUtensorMap tm16, const __grid_constant__ CUtensorMap tm8,
-                        int64_t n, int k, int m, int nstages, const uint8_t *__restrict__ xq, float *__restrict__ y,
-                        int *status) {
+    gemv_q4k_mma_kernel(const uint8_t *__restrict__ W, int64_t n, int k, int m, int nstages, int64_t row_stride,
+                        int64_t x_stride, const uint8_t *__restrict__ xq, float *__restrict__ y, int *status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
     __shared__ int abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nsb = k / 256, cpt = (nsb + kChunkSb - 1) / kChunkSb;  // chunks per tile
-    const int Up = (int)mma_units(k);
-    uint8_t *stages = smem;
-    uint8_t *xh = stages + size_t(nstages) * kStageBytes;        // [Up][m][128 B]
-    uint8_t *fac = xh + size_t(Up) * m * 128;                    // [Up][4 pairs][3 float4]
-    float4 *red = reinterpret_cast<float4 *>(fac + size_t(Up) * kFacBytes);  // [2][16][32]
+    const int nsb = k / 256, nb32 = k / 32;
+    const int64_t row_bytes = int64_t(nsb) * kQ4KBytes;
+    const size_t stage_bytes = size_t(kTileRows) * size_t(row_stride);
+    uint8_t *stages = smem;                                                        // [nstages][16][row_stride]
+    uint8_t *xs = stages + size_t(nstages) * stage_bytes;                          // [m][x_stride] fp16 codes
+    float2 *fz = reinterpret_cast<float2 *>(xs + size_t(m) * x_stride);           // [nb32][8] {d8, -1024 sum q}
+    uint16_t *sh = reinterpret_cast<uint16_t *>(fz + size_t(nb32) * kCols);        // [8][nb32] s (fp16 bits)
+    float *acc = reinterpret_cast<float *>(sh + size_t(kCols) * nb32);             // [nstages][16 warps][16][8]
     volatile int *abortp = &abort_flag;
 
-    // rows of this CTA: whole groups of 8 rows; tiles of 16 rows, the last possibly 8
-    const int64_t ngr = (n + 7) / 8;
-    const int64_t r0 = 8 * (ngr * blockIdx.x / gridDim.x);
-    const int64_t r1 = min(n, 8 * (ngr * (blockIdx.x + 1) / gridDim.x));
-    const int ntiles = (int)((r1 - r0 + kTileRows - 1) / kTileRows);
-    const int nchunks = ntiles * cpt;
+    // this CTA's tiles of 16 rows (the last tile of the matrix may be shorter)
+    const int64_t ntile_all = (n + kTileRows - 1) / kTileRows;
+    const int64_t tb = ntile_all * blockIdx.x / gridDim.x, te = ntile_all * (blockIdx.x + 1) / gridDim.x;
+    const int ntiles = (int)(te - tb);
 
     if (tid == 0) {
         abort_flag = 0;
@@ -128,207 +264,110 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     ptx::grid_launch_dependents();
 
     if (warp == kMmaWarps) {
-        // ---------------- producer: one lane issues every chunk
-        if (lane == 0) {
-            ptx::prefetch_tmap(&tm16);
-            ptx::prefetch_tmap(&tm8);
-            int issued = 0;
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c % nstages;
-                // all 16 consumer warps free a stage at about the same time: probe without
-                // suspending, so the refill does not wait for a wake-up
-                if (c >= nstages && !ptx::mbar_wait_spin(ptx::smem_u32(&empty[s]), ((c / nstages) - 1) & 1, abortp))
-                    break;
-                const int tile = c / cpt, kc = c - tile * cpt;
-                const int64_t row0 = r0 + int64_t(tile) * kTileRows;
-                const bool eight = r1 - row0 <= 8;  // the CTA's last tile holds one 8-row group
-                const uint32_t bar = ptx::smem_u32(&full[s]);
-                ptx::mbar_arrive_expect_tx(bar, eight ? kStageBytes / 2 : kStageBytes);
-                // x: 4-byte elements; a chunk starts at superblock 4 kc, i.e. element 144 kc
-                ptx::tma_load_2d(ptx::smem_u32(stages + size_t(s) * kStageBytes), eight ? &tm8 : &tm16, 144 * kc,
-                                 (int)row0, bar);
-                ++issued;
+        // ---------------- producer warp: copies in, results out
+        // Tile t of the CTA goes to stage t % nstages.  Before a stage takes a new tile, the
+        // 16 consumer warps have released it, so its slots hold the previous tile's partial
+        // sums: the warp adds them in warp order and writes the outputs.
+        auto write_tile = [&](int t, int s) {
+            const int64_t row0 = (tb + t) * kTileRows;
+            const float *a = acc + size_t(s) * kMmaWarps * kTileRows * kCols;
+#pragma unroll
+            for (int i = 0; i < kTileRows * kCols / 32; ++i) {
+                const int e = lane + 32 * i, r = e & 15, c = e >> 4;
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kMmaWarps; ++w) v += a[(w * kTileRows + r) * kCols + c];
+                if (c < m && row0 + r < n) y[int64_t(c) * n + row0 + r] = v;
             }
-            int dummy = 0;  // no copy may still be writing shared memory when the CTA exits
-            for (int c = max(0, issued - nstages); c < issued; ++c)
-                ptx::mbar_wait(ptx::smem_u32(&full[c % nstages]), (c / nstages) & 1, &dummy);
+        };
+        int issued = 0;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % nstages;
+            if (t >= nstages) {
+                ok = __all_sync(0xffffffffu,
+                                ptx::mbar_wait_spin(ptx::smem_u32(&empty[s]), ((t / nstages) - 1) & 1, abortp));
+                if (!ok) break;
+                write_tile(t - nstages, s);
+                __syncwarp();
+            }
+            const int64_t row0 = (tb + t) * kTileRows;
+            const int rows = (int)min((int64_t)kTileRows, n - row0);
+            const uint32_t bar = ptx::smem_u32(&full[s]);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar, uint32_t(rows * row_bytes));
+            __syncwarp();
+            if (lane < rows)
+                ptx::bulk_g2s(ptx::smem_u32(stages + s * stage_bytes + size_t(lane) * row_stride),
+                              W + (row0 + lane) * row_bytes, uint32_t(row_bytes), bar);
+            ++issued;
+        }
+        // every issued copy must have landed before the CTA exits (bounded waits, independent
+        // of the abort flag); then the last tiles' results
+        int dummy = 0;
+        for (int t = max(0, issued - nstages); t < issued; ++t)
+            ptx::mbar_wait(ptx::smem_u32(&full[t % nstages]), (t / nstages) & 1, &dummy);
+        for (int t = max(0, issued - nstages); ok && t < issued; ++t) {
+            const int s = t % nstages;
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&empty[s]), (t / nstages) & 1, abortp));
+            if (ok) write_tile(t, s);
         }
     } else {
-        // ---------------- consumers: stage the activations, then fold the chunks
+        // ---------------- consumers: stage the activations, then fold the tiles
         ptx::grid_dependency_wait();
-        {
-            // one thread per (unit, column, half, 8-value group): 8 codes as fp16 in fragment
-            // order, and per block its d8, s and -1024 sum(q) into the factor table
-            const int nb32 = k / 32;
-            const int total = Up * m * 8;
-            // the loads of kBatch items are issued before the first is used (one memory round
-            // trip per batch, not per item)
-            constexpr int kBatch = 4;
-            for (int i0 = tid; i0 < total; i0 += kBatch * kMmaWarps * 32) {
-              uint32_t ld[kBatch][3];
-#pragma unroll
-              for (int j = 0; j < kBatch; ++j) {
-                const int i = i0 + j * kMmaWarps * 32;
-                ld[j][0] = ld[j][1] = ld[j][2] = 0u;
-                const int half = (i >> 2) & 1, uc = i >> 3, u = uc / m, c = uc - u * m;
-                const int b = 2 * u + half;
-                if (i < total && b < nb32) {
-                    const uint8_t *blk = xq + (size_t(c) * nb32 + b) * kQ81Bytes;
-                    ld[j][0] = *reinterpret_cast<const uint32_t *>(blk);
-                    ld[j][1] = *reinterpret_cast<const uint32_t *>(blk + 4 + 8 * (i & 3));
-                    ld[j][2] = *reinterpret_cast<const uint32_t *>(blk + 8 + 8 * (i & 3));
-                }
-              }
-#pragma unroll
-              for (int j = 0; j < kBatch; ++j) {
-                const int i = i0 + j * kMmaWarps * 32;
-                if (i >= total) break;  // warp-uniform: total is a multiple of 128
-                const int t4 = i & 3, half = (i >> 2) & 1;
-                const int uc = i >> 3, u = uc / m, c = uc - u * m;
-                const uint32_t dsw = ld[j][0], lo = ld[j][1], hi = ld[j][2];
+        for (int i = tid; i < kCols * nb32; i += kMmaWarps * 32) {
+            const int c = i / nb32, b = i - c * nb32;
+            float d8 = 0.f, z = 0.f;
+            uint16_t sbits = 0;
+            if (c < m) {
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (size_t(c) * nb32 + b) * kQ81Bytes);
+                const uint32_t dsw = src[0];
+                uint32_t q[8];
                 int sum = 0;
-                uint32_t h[4];
-                const uint32_t wv[2] = {lo, hi};
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {  // codes 4p .. 4p+3 of the group -> (0, 2), (1, 3)
-                    const int q0 = (int8_t)(wv[p] & 0xff), q1 = (int8_t)((wv[p] >> 8) & 0xff);
-                    const int q2 = (int8_t)((wv[p] >> 16) & 0xff), q3 = (int8_t)(wv[p] >> 24);
-                    sum += q0 + q1 + q2 + q3;
-                    h[2 * p] = h2bits(__halves2half2(__int2half_rn(q0), __int2half_rn(q2)));
-                    h[2 * p + 1] = h2bits(__halves2half2(__int2half_rn(q1), __int2half_rn(q3)));
+                for (int jj = 0; jj < 8; ++jj) {
+                    q[jj] = src[1 + jj];
+                    sum = __dp4a((int)q[jj], 0x01010101, sum);
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(xh + (size_t(u) * m + c) * 128);
-                dst[xh_chunk(c, 4 * half + t4)] = make_uint4(h[0], h[1], h[2], h[3]);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                if (t4 == 0) {
-                    // pair p = c / 2: float4 0 {d8 lo c0, d8 lo c1, d8 hi c0, d8 hi c1}, 1 the same
-                    // for s, 2 for -1024 sum(q)
-                    float *f = reinterpret_cast<float *>(fac + size_t(u) * kFacBytes + (c >> 1) * 48);
-                    const int e = 2 * half + (c & 1);
-                    f[e] = half_lo(dsw);
-                    f[4 + e] = half_hi(dsw);
-                    f[8 + e] = -1024.0f * (float)sum;
+                // 32 codes as fp16, every 4 in the order 0 2 1 3: 64 bytes
+                uint4 *dst = reinterpret_cast<uint4 *>(xs + size_t(c) * x_stride + size_t(b) * 64);
+#pragma unroll
+                for (int jj = 0; jj < 8; jj += 2) {
+                    const uint2 e0 = codes_f16_0213(q[jj]), e1 = codes_f16_0213(q[jj + 1]);
+                    dst[jj / 2] = make_uint4(e0.x, e0.y, e1.x, e1.y);
                 }
-              }
+                d8 = half_lo(dsw);
+                z = -1024.f * (float)sum;
+                sbits = (uint16_t)(dsw >> 16);
             }
-            // the factors of columns m..7 are never read (their B fragments are zero), except
-            // in the odd pair of an odd m: clear that column
-            if (m & 1) {
-                for (int i = tid; i < Up * 2; i += kMmaWarps * 32) {
-                    float *f = reinterpret_cast<float *>(fac + size_t(i >> 1) * kFacBytes + (m >> 1) * 48);
-                    const int e = 2 * (i & 1) + 1;
-                    f[e] = 0.f;
-                    f[4 + e] = 0.f;
-                    f[8 + e] = 0.f;
-                }
-            }
+            fz[size_t(b) * kCols + c] = make_float2(d8, z);
+            sh[size_t(c) * nb32 + b] = sbits;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kMmaWarps * 32) : "memory");
 
-        const int g = lane >> 2, t = lane & 3;
-        const int sbl = warp >> 2, c4 = warp & 3;  // this warp's unit: superblock sbl of the chunk, quarter c4
-        const bool colv = g < m;                   // the B column this lane supplies
-        float tot[4] = {0.f, 0.f, 0.f, 0.f};       // (row g, col 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
-        bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % nstages;
-            const int tile = c / cpt, kc = c - tile * cpt;
-            const int64_t row0 = r0 + int64_t(tile) * kTileRows;
-            const bool eight = r1 - row0 <= 8;
-            // every consumer warp waits for every chunk, so a suspended wait's wake-up delay
-            // would be paid once per chunk: probe without suspending
-            if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait_spin(ptx::smem_u32(&full[s]), (c / nstages) & 1, abortp));
-            const int sb = kc * kChunkSb + sbl;  // superblock within the row
-            if (ok && sb < nsb) {
-                // everything this warp needs from the stage, then the stage goes back
-                const uint8_t *rg = stages + size_t(s) * kStageBytes + size_t(g) * kRowChunk + sbl * kQ4KBytes;
-                const uint4 hd0 = *reinterpret_cast<const uint4 *>(rg);
-                const uint2 wq0 = *reinterpret_cast<const uint2 *>(rg + 16 + 32 * c4 + 8 * t);
-                uint4 hd1 = make_uint4(0u, 0u, 0u, 0u);
-                uint2 wq1 = make_uint2(0u, 0u);
-                if (!eight) {
-                    const uint8_t *rg8 = rg + 8 * kRowChunk;
-                    hd1 = *reinterpret_cast<const uint4 *>(rg8);
-                    wq1 = *reinterpret_cast<const uint2 *>(rg8 + 16 + 32 * c4 + 8 * t);
-                }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));
-
-                const int u = sb * 4 + c4;
-                uint4 xl = make_uint4(0u, 0u, 0u, 0u), xhv = xl;
-                if (colv) {
-                    const uint4 *xc = reinterpret_cast<const uint4 *>(xh + (size_t(u) * m + g) * 128);
-                    xl = xc[xh_chunk(g, t)];
-                    xhv = xc[xh_chunk(g, 4 + t)];
-                }
-                const float4 *fp = reinterpret_cast<const float4 *>(fac + size_t(u) * kFacBytes + t * 48);
-                const float4 f_d8 = fp[0], f_s8 = fp[1], f_z = fp[2];
-
-                // A fragments: rows g (a0, a2) and g + 8 (a1, a3); word p of the lane's 8 bytes
-                // gives K16 step p of both sub-blocks: bytes (0, 2) -> slots (2t, 2t+1), (1, 3) -> (2t+8, 2t+9)
-                // the accumulators start at -1024 sum(q) of the column's 32-block
-                float dlo[4] = {f_z.x, f_z.y, f_z.x, f_z.y};
-                float dhi[4] = {f_z.z, f_z.w, f_z.z, f_z.w};
-                {
-                    const uint32_t w0[2] = {wq0.x, wq0.y}, w1[2] = {wq1.x, wq1.y};
-                    const uint32_t bl[4] = {xl.x, xl.y, xl.z, xl.w}, bh[4] = {xhv.x, xhv.y, xhv.z, xhv.w};
-#pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        const uint32_t u0 = w0[p] >> 8, u1 = w1[p] >> 8;
-                        mma_16816(dlo, nib_f16(w0[p], 0x000f000fu), nib_f16(w1[p], 0x000f000fu),
-                                  nib_f16(u0, 0x000f000fu), nib_f16(u1, 0x000f000fu), bl[2 * p], bl[2 * p + 1]);
-                        mma_16816(dhi, nib_f16(w0[p], 0x00f000f0u), nib_f16(w1[p], 0x00f000f0u),
-                                  nib_f16(u0, 0x00f000f0u), nib_f16(u1, 0x00f000f0u), bh[2 * p], bh[2 * p + 1]);
-                    }
-                }
-                // fold: y += d sc_lo d8_lo sumi_lo + d (sc_hi / 16) d8_hi (16 sumi_hi) - dmin (m_lo s_lo + m_hi s_hi)
-                const uint4 hds[2] = {hd0, hd1};
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const uint4 hd = hds[rr];
-                    int sc_lo, m_lo, sc_hi, m_hi;
-                    q4k_scale_min(hd.y, hd.z, hd.w, 2 * c4, sc_lo, m_lo);
-                    q4k_scale_min(hd.y, hd.z, hd.w, 2 * c4 + 1, sc_hi, m_hi);
-                    const float d = half_lo(hd.x), dmin = half_hi(hd.x);
-                    const float a_lo = d * (float)sc_lo, a_hi = d * (float)sc_hi * 0.0625f;
-                    const float n_lo = -dmin * (float)m_lo, n_hi = -dmin * (float)m_hi;
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int e = 2 * rr + cc;
-                        const float d8l = cc ? f_d8.y : f_d8.x, d8h = cc ? f_d8.w : f_d8.z;
-                        const float s8l = cc ? f_s8.y : f_s8.x, s8h = cc ? f_s8.w : f_s8.z;
-                        float v = fmaf(a_lo * d8l, dlo[e], tot[e]);
-                        v = fmaf(a_hi * d8h, dhi[e], v);
-                        v = fmaf(n_lo, s8l, v);
-                        tot[e] = fmaf(n_hi, s8h, v);
-                    }
-                }
-            } else if (ok) {  // past the row's last superblock: nothing to fold
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));
-            }
-            if (kc == cpt - 1) {
-                // end of a tile: the 16 warps' shares of the 16 x 8 results, summed through
-                // shared memory (every consumer warp takes part, also after an abort, so the
-                // named barriers always match)
-                float4 *rb = red + (tile & 1) * (kMmaWarps * 32);
-                rb[warp * 32 + lane] = make_float4(tot[0], tot[1], tot[2], tot[3]);
-                asm volatile("bar.sync 1, %0;" ::"n"(kMmaWarps * 32) : "memory");
-                if (tid < 128) {
-                    const int row = tid >> 3, col = tid & 7;
-                    const int hl = (row & 7) * 4 + (col >> 1), e = ((row >> 3) << 1) | (col & 1);
-                    float acc = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kMmaWarps; ++w) {
-                        const float4 v = rb[w * 32 + hl];
-                        acc += e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-                    }
-                    const int64_t r = row0 + row;
-                    if (ok && col < m && r < r1) y[int64_t(col) * n + r] = acc;
-                }
-                tot[0] = tot[1] = tot[2] = tot[3] = 0.f;
-            }
+        const int g = lane >> 2, t4 = lane & 3;
+        const bool xv = g < m;  // columns past m: zero codes, nothing staged
+        const uint32_t xg = ptx::smem_u32(xs + size_t(xv ? g : 0) * x_stride);
+        const uint32_t sg = ptx::smem_u32(sh + size_t(g) * nb32);
+        const uint32_t fza = ptx::smem_u32(fz);
+        const uint32_t st0 = ptx::smem_u32(stages), acc0 = ptx::smem_u32(acc);
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % nstages;
+            // all 16 warps wait for every tile and start on it together: probe without
+            // suspending, so that no warp pays a wake-up delay per tile
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_spin(ptx::smem_u32(&full[s]), (t / nstages) & 1, abortp)))
+                break;
+            float2 tot01 = make_float2(0.f, 0.f), tot23 = make_float2(0.f, 0.f);
+            const uint32_t rg = st0 + uint32_t(s * stage_bytes) + uint32_t(g * row_stride);
+            const uint32_t rg8 = rg + uint32_t(8 * row_stride);
+            int j = (int)((warp - (int64_t(t) * nsb) % kMmaWarps + kMmaWarps) % kMmaWarps);
+            for (; j < nsb; j += kMmaWarps)
+                fold_superblock(rg + j * kQ4KBytes, rg8 + j * kQ4KBytes, xg, xv, fza, sg, j, t4, tot01, tot23);
+            // this warp's slot of the stage: rows g and g + 8, columns 2t4, 2t4 + 1
+            const uint32_t a = acc0 + uint32_t(((s * kMmaWarps + warp) * kTileRows) * kCols * 4);
+            sts64(a + 4 * (g * kCols + 2 * t4), tot01);
+            sts64(a + 4 * ((g + 8) * kCols + 2 * t4), tot23);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));
         }
     }
     __syncthreads();
@@ -338,30 +377,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 }  // namespace
 
 bool gemv_mma_supported(qmm_type t, int64_t n, int64_t k, int64_t m) {
-    if (t != QMM_Q4_K || n <= 0 || m < 2 || m > 8 || k % 256 != 0) return false;
-    if (n >= (int64_t(1) << 31) || (k / 256) * int64_t(kQ4KBytes) / 4 >= (int64_t(1) << 31)) return false;
-    return mma_stages(k, (int)m, size_t(device_smem_optin())) > 0;
+    if (t != QMM_Q4_K || n <= 0 || m < 1 || m > 8 || k % 256 != 0) return false;
+    MmaPlan p;
+    return mma_plan(k, (int)m, size_t(device_smem_optin()), p);
 }
 
 cudaError_t launch_gemv_mma(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
                             cudaStream_t st) {
-    if (!gemv_mma_supported(t, n, k, m)) return cudaErrorNotSupported;
-    const int nstages = mma_stages(k, (int)m, size_t(device_smem_optin()));
-    const int64_t row_bytes = (k / 256) * kQ4KBytes;
-    // the weight rows as a 2-D array of 4-byte elements; one box is 576 bytes (4
-    // superblocks) of 16 or 8 rows, zero-filled past the row end and past row n
-    CUtensorMap tm16, tm8;
-    if (!tc_make_map_2d(&tm16, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, W, uint64_t(row_bytes / 4), uint64_t(n),
-                        uint64_t(row_bytes), kRowChunk / 4, kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !tc_make_map_2d(&tm8, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, W, uint64_t(row_bytes / 4), uint64_t(n),
-                        uint64_t(row_bytes), kRowChunk / 4, kTileRows / 2, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    const size_t smem = 1024 + size_t(nstages) * kStageBytes + mma_x_bytes(k, (int)m) + kRedBytes;
-    cudaError_t e = ensure_smem(gemv_q4k_mma_kernel, smem);
+    MmaPlan p;
+    if (!gemv_mma_supported(t, n, k, m) || !mma_plan(k, (int)m, size_t(device_smem_optin()), p))
+        return cudaErrorNotSupported;
+    cudaError_t e = ensure_smem(gemv_q4k_mma_kernel, p.smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 7) / 8));
-    return launch_pdl(gemv_q4k_mma_kernel, dim3((unsigned)grid), dim3(kMmaThreads), smem, st, tm16, tm8, n, (int)k,
-                      (int)m, nstages, static_cast<const uint8_t *>(xq), y, static_cast<int *>(nullptr));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + kTileRows - 1) / kTileRows));
+    return launch_pdl(gemv_q4k_mma_kernel, dim3((unsigned)grid), dim3(kMmaThreads), p.smem, st,
+                      static_cast<const uint8_t *>(W), n, (int)k, (int)m, p.nstages, p.row_stride, p.x_stride,
+                      static_cast<const uint8_t *>(xq), y, static_cast<int *>(nullptr));
 }
 
 }  // namespace qmm

@@ -1,9 +1,9 @@
-"""GPU parity of the multi-column GEMV on mma.sync (Q4_K, 2 <= m <= 8) against the
-oracle, |y - y_oracle| <= 1e-5 T per element, and against the dp4a GEMV on the same
-inputs.  Shapes cover ragged row counts (a CTA's last tile of 8 rows, tiles past row n),
-rows whose last 4-superblock chunk runs past the row end, every column count, and
-activation blocks that stress the exact-integer operands (all-zero blocks, |q| = 127
-everywhere)."""
+"""GPU parity of the multi-column GEMV on mma.sync (Q4_K, 1 <= m <= 8) against the
+oracle, |y - y_oracle| <= 1e-5 T per element, and the dp4a GEMV on the same inputs.
+Shapes cover ragged row counts (tiles of fewer than 16 rows at the end of the matrix and
+of a CTA), one superblock per row (most warps without work in a tile), superblock counts
+below, at and above the 16 consumer warps, every column count, and activation blocks that
+stress the exact-integer operands (all-zero blocks, |q| = 127 everywhere)."""
 import numpy as np
 import pytest
 import torch
@@ -35,13 +35,16 @@ def _run(W, n, k, xq, m, path):
 
 
 @pytest.mark.parametrize("n,k,m", [
-    (300, 1024, 2), (300, 1024, 3), (300, 1024, 4), (300, 1024, 5), (300, 1024, 6), (300, 1024, 7),
-    (300, 1024, 8),
-    (1000, 1280, 3),   # 5 superblocks: the second chunk of every tile is 3/4 past the row end
-    (17, 256, 5),      # one superblock, 17 rows: three 8-row groups on as many CTAs
-    (4104, 5120, 8),   # several 16-row tiles per CTA, ragged group count
-    (2440, 2048, 2),   # 305 groups of 8: CTAs ending on an 8-row tile
-    (8, 768, 7),       # a single 8-row tile
+    (300, 1024, 1), (300, 1024, 2), (300, 1024, 3), (300, 1024, 4), (300, 1024, 5), (300, 1024, 6),
+    (300, 1024, 7), (300, 1024, 8),
+    (17408 // 8, 5120, 8),  # 20 superblocks: more than the 16 consumer warps
+    (1000, 4096, 4),       # 16 superblocks: one per warp
+    (4111, 2048, 1),
+    (1000, 1280, 3),   # 5 superblocks per row
+    (17, 256, 5),      # one superblock, 17 rows: a tile of 16 and a tile of 1
+    (4104, 5120, 8),   # several 16-row tiles per CTA, the last tile 8 rows
+    (2440, 2048, 2),   # 152.5 tiles: CTAs with 1 or 2 tiles, the last one 8 rows
+    (8, 768, 7),       # a single tile of 8 rows
 ])
 def test_gemv_mma_matches_oracle(oracle_mod, n, k, m):
     W, x = qmm_synth.make_dense("q4_K", n, k, m, seed=n + k + m)
@@ -83,3 +86,17 @@ def test_gemv_mma_long_rows(oracle_mod, m):
     xq = oracle_mod.quantize_q8_1(x)
     y_ref, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
     assert_within(_run(W, n, k, xq, m, qmm.PATH_AUTO), y_ref, T, f"long rows m={m}")
+
+
+@pytest.mark.parametrize("m", [5, 8])
+def test_gemv_mma_repeats_bit_exact(oracle_mod, m):
+    """The automatic path at 5..8 columns is the MMA GEMV; its partial sums of a tile are
+    added in a fixed warp order, so two calls give the same bits."""
+    n, k = 3000, 5120
+    W, x = qmm_synth.make_dense("q4_K", n, k, m, seed=3 + m)
+    xq = oracle_mod.quantize_q8_1(x)
+    a = _run(W, n, k, xq, m, qmm.PATH_AUTO)
+    b = _run(W, n, k, xq, m, qmm.PATH_AUTO)
+    assert np.array_equal(a, b)
+    y_ref, T = oracle_mod.mul_mat(W, "q4_K", n, k, xq, m)
+    assert_within(a, y_ref, T, f"auto m={m}")
