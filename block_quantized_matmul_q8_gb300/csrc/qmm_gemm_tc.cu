@@ -605,14 +605,16 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                         q4k_scale_min(hd.y, hd.z, hd.w, 2 * c, sc_lo, m_lo);
                         q4k_scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sc_hi, m_hi);
                         const __half2 s_lo = __float2half2_rn((float)sc_lo), ns_lo = __float2half2_rn(-1024.f * sc_lo);
-                        const __half2 s_hi = __float2half2_rn((float)sc_hi), ns_hi = __float2half2_rn(-1024.f * sc_hi);
+                        // Q4_K takes the high nibbles in place (16 q): scale sc / 16, offset -64 sc
+                        const __half2 s_hi = __float2half2_rn(T == QMM_Q4_K ? 0.0625f * sc_hi : (float)sc_hi);
+                        const __half2 ns_hi = __float2half2_rn(T == QMM_Q4_K ? -64.f * sc_hi : -1024.f * sc_hi);
                         const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
                         uint8_t *rowdst = wst + j2 * kSlabBytes + r * 128;
                         if constexpr (T == QMM_Q4_K) {
 #pragma unroll
-                            for (int cq = 0; cq < 4; ++cq) {
-                                const uint4 lo = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 0, s_lo, ns_lo);
-                                const uint4 hi = nibbles_to_f16(w[2 * cq], w[2 * cq + 1], 4, s_hi, ns_hi);
+                            for (int cq = 0; cq < 4; ++cq) {  // codes in the order 0 2 1 3 of every 4
+                                const uint4 lo = nibbles_to_f16_0213(w[2 * cq], w[2 * cq + 1], false, s_lo, ns_lo);
+                                const uint4 hi = nibbles_to_f16_0213(w[2 * cq], w[2 * cq + 1], true, s_hi, ns_hi);
                                 *reinterpret_cast<uint4 *>(rowdst + ((cq ^ (r & 7)) << 4)) = lo;
                                 *reinterpret_cast<uint4 *>(rowdst + (((cq + 4) ^ (r & 7)) << 4)) = hi;
                             }
@@ -878,8 +880,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         // 16 warps: warp w reads TMEM lanes 32*(w%4).. (one activation row per thread)
         // and one quarter of the 128 columns (32 weight rows).  Slots arrive in pairs;
         // both are read (16 columns at a time) and the pair is handed back before the
-        // next pair is awaited (probing, not suspending: the pairs come every few hundred
-        // cycles).  The segment's total stays in registers.
+        // next pair is awaited.  The waits suspend: 16 warps probing the barrier take issue
+        // slots from the unpack warps (Q6_K at 151936 x 5120, m = 512: 3.45 -> 3.29 ms;
+        // the other formats unchanged).  The segment's total stays in registers.
         regs_inc<kRegsEpilogue>();
         const int ew = warp - kEpiWarp0;  // 0..15
         const int cq = ew >> 2;           // column quarter: columns 32cq .. 32cq+31
@@ -915,7 +918,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
 #pragma unroll
                     for (int j = 0; j < kGroups; ++j) {
                         const uint32_t e = ge & 1;
-                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
                             ok = false;
                             break;
                         }
@@ -944,7 +947,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     if constexpr (F::kMin) {
                         // the min group: total += d * acc + (-dmin) * minslot
                         const uint32_t e = ge & 1;
-                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
                             ok = false;
                             break;
                         }
@@ -986,7 +989,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
 #pragma unroll
                     for (int j = 0; j < kGroups; ++j) {
                         const uint32_t e = ge & 1;
-                        if (!ptx::mbar_wait_spin(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
+                        if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
                             ok = false;
                             break;
                         }
@@ -1076,10 +1079,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_body<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, a);
 }
 
+// Four int8 codes (one word) as two fp16 pairs: (0, 1), (2, 3), or with perm4 (0, 2), (1, 3).
+__device__ __forceinline__ uint2 codes4_f16(uint32_t w, int perm4) {
+    const int8_t *c = reinterpret_cast<const int8_t *>(&w);
+    const int i1 = perm4 ? 2 : 1, i2 = perm4 ? 1 : 2;
+    return make_uint2(h2bits(__halves2half2(__int2half_rn(c[0]), __int2half_rn(c[i1]))),
+                      h2bits(__halves2half2(__int2half_rn(c[i2]), __int2half_rn(c[3]))));
+}
+
 // q8_1 blocks -> fp16 activation codes [m][k], fp32 d8 [m][k/32], fp16 s tile
-// [m][k/256][16] (8 values then 8 zeros) for the tensor-core GEMM.
+// [m][k/256][16] (8 values then 8 zeros) for the tensor-core GEMM.  perm4: every 4 codes in
+// the order 0 2 1 3 (the order of the Q4_K unpack; a slot's dot is the same in any order).
 __global__ void tc_prep_kernel(const uint8_t *__restrict__ xq, int64_t m, int k, __half *__restrict__ xh,
-                               float *__restrict__ dx, __half *__restrict__ smin, int *status) {
+                               float *__restrict__ dx, __half *__restrict__ smin, int *status, int perm4) {
     const int nb32 = k / 32;
     const int64_t total = m * nb32;
     if (blockIdx.x == 0 && threadIdx.x == 0 && status) *status = (int)QMM_OK;
@@ -1091,15 +1103,8 @@ __global__ void tc_prep_kernel(const uint8_t *__restrict__ xq, int64_t m, int k,
         uint4 *dst = reinterpret_cast<uint4 *>(xh + r * k + 32 * b);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t w0 = ldg4(src + 1 + 2 * j), w1 = ldg4(src + 2 + 2 * j);
-            const int8_t *c0 = reinterpret_cast<const int8_t *>(&w0);
-            const int8_t *c1 = reinterpret_cast<const int8_t *>(&w1);
-            uint4 o;
-            o.x = h2bits(__halves2half2(__int2half_rn(c0[0]), __int2half_rn(c0[1])));
-            o.y = h2bits(__halves2half2(__int2half_rn(c0[2]), __int2half_rn(c0[3])));
-            o.z = h2bits(__halves2half2(__int2half_rn(c1[0]), __int2half_rn(c1[1])));
-            o.w = h2bits(__halves2half2(__int2half_rn(c1[2]), __int2half_rn(c1[3])));
-            dst[j] = o;
+            const uint2 a = codes4_f16(ldg4(src + 1 + 2 * j), perm4), b = codes4_f16(ldg4(src + 2 + 2 * j), perm4);
+            dst[j] = make_uint4(a.x, a.y, b.x, b.y);
         }
         dx[i] = half_lo(dsw);
         __half *sp = smin + (r * (nb32 / 8) + b / 8) * 16;
@@ -1114,7 +1119,8 @@ __global__ void tc_prep_kernel(const uint8_t *__restrict__ xq, int64_t m, int k,
 // the GEMM computes them but never stores them.
 __global__ void tc_prep_gather_kernel(const uint8_t *__restrict__ xq, int k, const int32_t *__restrict__ perm,
                                       const int32_t *__restrict__ bounds, int E, int x_div, int64_t n_pairs,
-                                      __half *__restrict__ xh, float *__restrict__ dx, __half *__restrict__ smin) {
+                                      __half *__restrict__ xh, float *__restrict__ dx, __half *__restrict__ smin,
+                                      int perm4) {
     const int nb32 = k / 32;
     const int64_t nvalid = bounds[E];
     const int64_t total = n_pairs * nb32;
@@ -1128,15 +1134,8 @@ __global__ void tc_prep_gather_kernel(const uint8_t *__restrict__ xq, int k, con
         uint4 *dst = reinterpret_cast<uint4 *>(xh + j * k + 32 * b);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint32_t w0 = ldg4(src + 1 + 2 * q), w1 = ldg4(src + 2 + 2 * q);
-            const int8_t *c0 = reinterpret_cast<const int8_t *>(&w0);
-            const int8_t *c1 = reinterpret_cast<const int8_t *>(&w1);
-            uint4 o;
-            o.x = h2bits(__halves2half2(__int2half_rn(c0[0]), __int2half_rn(c0[1])));
-            o.y = h2bits(__halves2half2(__int2half_rn(c0[2]), __int2half_rn(c0[3])));
-            o.z = h2bits(__halves2half2(__int2half_rn(c1[0]), __int2half_rn(c1[1])));
-            o.w = h2bits(__halves2half2(__int2half_rn(c1[2]), __int2half_rn(c1[3])));
-            dst[q] = o;
+            const uint2 a = codes4_f16(ldg4(src + 1 + 2 * q), perm4), b = codes4_f16(ldg4(src + 2 + 2 * q), perm4);
+            dst[q] = make_uint4(a.x, a.y, b.x, b.y);
         }
         dx[i] = half_lo(dsw);
         __half *sp = smin + (j * (nb32 / 8) + b / 8) * 16;
@@ -1230,6 +1229,9 @@ TcLayout tc_layout(int64_t m, int64_t k, int64_t partial_ctas) {
 // Bytes of one weight row, and the raw map of `rows` weight rows: one box is the 256 k
 // values of 128 rows (Q8_0 read as uint16, so that a step's 272 bytes are a box of 136).
 // Q6_K has no map: its raw warp bulk-copies from W, which must start on a 16-byte boundary.
+// The Q4_K unpack writes every 4 weights in the order 0 2 1 3; its activations are staged so.
+int tc_perm4(qmm_type t) { return t == QMM_Q4_K ? 1 : 0; }
+
 int64_t tc_row_bytes(qmm_type t, int64_t k) { return (k / 256) * block_bytes(t) * (256 / block_elems(t)); }
 
 bool tc_weight_map(qmm_type t, const void *W, int64_t rows, int64_t k, CUtensorMap *tm_w, int64_t stride = 0) {
@@ -1334,7 +1336,7 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     const int64_t nblk = m * (k / 32);
     const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
     tc_prep_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), m, (int)k, xh, dx, smin,
-                                                      status);
+                                                      status, tc_perm4(t));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -1396,7 +1398,7 @@ cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64
     const int64_t nblk = m * (k / 32);
     const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
     tc_prep_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), m, (int)k, xh, dx, smin,
-                                                      status);
+                                                      status, 1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t row_bytes = (k / 256) * kQ4KBytes;
@@ -1459,7 +1461,8 @@ cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts,
     const int64_t nblk = n_pairs * (k / 32);
     const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
     tc_prep_gather_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), (int)k, perm, bounds,
-                                                             (int)n_experts, (int)x_div, n_pairs, xh, dx, smin);
+                                                             (int)n_experts, (int)x_div, n_pairs, xh, dx, smin,
+                                                             tc_perm4(t));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -1520,7 +1523,8 @@ cudaError_t launch_gemm_tc_grouped_glu(qmm_type t, const void *Wg, const void *W
     const int64_t nblk = n_pairs * (k / 32);
     const int pgrid = (int)std::min<int64_t>((nblk + 255) / 256, int64_t(device_sm_count()) * 8);
     tc_prep_gather_kernel<<<std::max(pgrid, 1), 256, 0, st>>>(static_cast<const uint8_t *>(xq), (int)k, perm, bounds,
-                                                             (int)n_experts, (int)x_div, n_pairs, xh, dx, smin);
+                                                             (int)n_experts, (int)x_div, n_pairs, xh, dx, smin,
+                                                             1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t row_bytes = (k / 256) * kQ4KBytes;

@@ -31,6 +31,26 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w0, uint32_t w1, int sh
     return r;
 }
 
+// The same 8 values in the order 0 2 1 3 4 6 5 7 (the activation codes of the Q4_K GEMM are
+// staged in that order, and an MMA's dot does not depend on the order of its k): bytes 0, 2
+// of a word already sit under the two halves, bytes 1, 3 after one shift.  Low nibbles as
+// (0x6400 | q) = 1024 + q with (sc, -1024 sc); high nibbles in place, (0x6400 | 16 q) =
+// 1024 + 16 q, with (sc / 16, -64 sc) (both exact in fp16).  Each fma gives q sc exactly.
+__device__ __forceinline__ uint4 nibbles_to_f16_0213(uint32_t w0, uint32_t w1, bool high, __half2 sc2, __half2 nsc2) {
+    const uint32_t mask = high ? 0x00F000F0u : 0x000F000Fu;
+    uint32_t p[4];
+    p[0] = (w0 & mask) | 0x64006400u;
+    p[1] = ((w0 >> 8) & mask) | 0x64006400u;
+    p[2] = (w1 & mask) | 0x64006400u;
+    p[3] = ((w1 >> 8) & mask) | 0x64006400u;
+    uint4 r;
+    r.x = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[0]), sc2, nsc2));
+    r.y = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[1]), sc2, nsc2));
+    r.z = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[2]), sc2, nsc2));
+    r.w = h2bits(__hfma2(*reinterpret_cast<__half2 *>(&p[3]), sc2, nsc2));
+    return r;
+}
+
 // Q5_K: the same 8 values with their fifth bits, bit j of the 8 qh bytes that share the
 // nibbles' positions (q0, q1 as w0, w1): (0x6400 | code) is the fp16 1024 + code, code <= 31.
 __device__ __forceinline__ uint4 nibbles5_to_f16(uint32_t w0, uint32_t w1, uint32_t q0, uint32_t q1, int shift, int j,
