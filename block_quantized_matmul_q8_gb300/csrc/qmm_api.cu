@@ -108,10 +108,10 @@ static int choose_path(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t stri
     if (force == kGemmTc && gemm_tc_supported(t, n, k, m, stride)) return kGemmTc;
     if (force == kGemvTc && gemv_tc_supported(t, n, k, m)) return kGemvTc;
     if (force == kGemvMma && gemv_mma_supported(t, n, k, m)) return kGemvMma;
-    // Q4_K from 5 columns on (natural rows): the MMA GEMV's cost hardly grows with the
-    // columns, the dp4a GEMV's does (17408 x 5120: 21.8 against 23.2 us at 5 columns, 22.5
-    // against 32.6 at 8; at 4 columns the two are even)
-    if (m >= 5 && m <= 8 && stride == 0 && gemv_mma_supported(t, n, k, m)) return kGemvMma;
+    // Q4_K from 6 columns on (natural rows): the MMA GEMV's cost hardly grows with the
+    // columns, the dp4a GEMV's does (17408 x 5120: 21.9 against 22.5 us at 6 columns, 22.6
+    // against 32.3 at 8; at 5 columns the row-pair dp4a GEMV is faster, 20.2 against 21.8)
+    if (m >= 6 && m <= 8 && stride == 0 && gemv_mma_supported(t, n, k, m)) return kGemvMma;
     if (m <= 8 && gemv_fits) return kGemv;
     // skinny activations on the tensor cores (weights as the MMA's M side; Q4_K, whose rows
     // are whole 16-byte units and so never padded)

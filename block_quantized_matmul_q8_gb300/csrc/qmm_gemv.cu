@@ -370,7 +370,7 @@ __device__ __forceinline__ void fold_q4k_unit2(const uint8_t *row0, const uint8_
 // kTwoRows (Q4_K, not GLU): each warp folds its two rows of a chunk together, lanes
 // taking units lane + 32 j, so every unit's staged activations are read once for both
 // rows; chosen by the host for long rows, where a CTA folds few chunks.
-template <int T, int NC, bool GLU = false, bool kTwoRows = false>
+template <int T, int NC, bool GLU = false, bool kTwoRows = false, bool kRowPairs = false>
 __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int64_t n, int k, int64_t row_bytes,
                                               int nstages, const XIn &x, float *__restrict__ y, int64_t y_ld,
                                               int *status, const uint8_t *__restrict__ W2 = nullptr) {
@@ -395,7 +395,10 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
     volatile int *abortp = &abort_flag;
     // the ring protocol needs whole rounds of stages (gemv_ring_groups): any other depth
     // is refused before a copy is issued
-    const int ngroups = gemv_ring_groups(nstages);
+    // kRowPairs: consumer groups of 2 warps (8 groups for a ring of 8 stages), each half-warp
+    // folding two rows of a chunk with every unit's staged activations read once for both
+    constexpr int kGW = kRowPairs ? 2 : kTmaGroupWarps;  // warps per consumer group
+    const int ngroups = kRowPairs ? (nstages == kTmaMaxStages ? kTmaConsumerWarps / kGW : 0) : gemv_ring_groups(nstages);
     if (ngroups == 0) {
         if (tid == 0 && status) atomicExch(status, (int)QMM_ERR_DEVICE);
         return;
@@ -405,7 +408,7 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
         abort_flag = 0;
         for (int s = 0; s < nstages; ++s) {
             ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&empty[s]), kTmaGroupWarps);
+            ptx::mbar_init(ptx::smem_u32(&empty[s]), kGW);
         }
         ptx::fence_mbar_init();
     }
@@ -460,7 +463,7 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
         stage_x<NC>(x, k, U, xs, xds, tid, kTmaConsumerWarps * 32);
         asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumerWarps * 32) : "memory");
 
-        const int grp = warp / kTmaGroupWarps, gw = warp % kTmaGroupWarps;
+        const int grp = warp / kGW, gw = warp % kGW;
         const int rr = 2 * gw + (lane >> 4);  // row within a chunk
         const int c4 = l16 & 3;               // qs chunk of every unit this lane takes (Q4_K)
         const Q4KPairSel psel = q4k_pair_sel(c4);
@@ -472,6 +475,40 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
             float acc[NC];
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc) acc[cc] = 0.f;
+            if constexpr (T == QMM_Q4_K && !GLU && kRowPairs) {
+                // this half-warp's rows ra, ra + 1 of the chunk, lane l16 taking units l16 + 16 j of
+                // both: half the activation loads per weight row of the one-row form
+                const int ra = 2 * (2 * gw + (lane >> 4));
+                float acc1[NC];
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) acc1[cc] = 0.f;
+                if (a + ra < r1) {
+                    const uint8_t *row0 = stages + s * stage_bytes + size_t(ra) * row_bytes;
+                    for (int u = l16; u < U; u += 16)
+                        fold_q4k_unit2<NC>(row0, row0 + row_bytes, a + ra + 1 < r1, u, c4, psel, xs, xds, U, acc, acc1);
+                }
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) {
+                    float v0 = acc[cc], v1 = acc1[cc];
+#pragma unroll
+                    for (int o = 8; o >= 1; o >>= 1) {
+                        v0 += __shfl_xor_sync(0xffffffffu, v0, o);
+                        v1 += __shfl_xor_sync(0xffffffffu, v1, o);
+                    }
+                    acc[cc] = v0;
+                    acc1[cc] = v1;
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&empty[s]));  // the stage is read: free it first
+                if (l16 == 0) {
+#pragma unroll
+                    for (int cc = 0; cc < NC; ++cc) {
+                        if (a + ra < r1) y[cc * y_ld + a + ra] = acc[cc];
+                        if (a + ra + 1 < r1) y[cc * y_ld + a + ra + 1] = acc1[cc];
+                    }
+                }
+                continue;
+            }
             if constexpr (T == QMM_Q4_K && !GLU && kTwoRows) {
                 const int r0w = 2 * gw;  // this warp's rows r0w, r0w + 1 of the chunk
                 float acc1[NC];
@@ -601,6 +638,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_kernel(const uint
 
 // Long rows (k >= 8192) at one or two columns: the two-row fold
 template <int NC>
+__global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_pair_kernel(const uint8_t *__restrict__ W, int64_t n,
+                                                                           int k, int64_t row_bytes, int nstages,
+                                                                           const XIn x, float *__restrict__ y,
+                                                                           int64_t y_ld, int *status) {
+    gemv_tma_body<QMM_Q4_K, NC, false, false, true>(W, n, k, row_bytes, nstages, x, y, y_ld, status);
+}
+template <int NC>
 __global__ void __launch_bounds__(kTmaThreads, 1) gemv_q4k_tma_long_kernel(const uint8_t *__restrict__ W, int64_t n,
                                                                            int k, int64_t row_bytes, int nstages,
                                                                            const XIn x, float *__restrict__ y,
@@ -696,12 +740,19 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x
     const size_t smem = 1024 + size_t(nstages) * kTmaChunkRows * row_bytes + gemv_smem_bytes(k, NC);
     void (*kern)(const uint8_t *, int64_t, int, int64_t, int, const XIn, float *, int64_t, int *);
     if constexpr (T == QMM_Q4_K) {
-        // from k = 8192 on, sharing each unit's activation loads between a warp's two rows
-        // pays (4096 x 14336 at one column: 13.7 -> 12.9 us); below it costs a little
+        // From k = 8192 on at 1-2 columns, each warp folds its two rows together (lanes over
+        // units: 4096 x 14336 at one column 13.7 -> 12.9 us).  Below, with the full ring of 8
+        // stages and q8_1 input, each half-warp folds two rows over its 16 units (17408 x 5120:
+        // 10.27 -> 10.11 us at 1 column, 12.8 -> 12.5 at 2, 23.3 -> 20.2 at 5); from 6 columns
+        // on the row pairs spill and the MMA GEMV takes over.  With the fp32 row quantized in
+        // the prologue the one-row form stays faster (10.8 against 11.1 us).
+        const bool pairs = nstages == kTmaMaxStages && NC <= 5 && x.xf == nullptr;
         if constexpr (NC <= 2)
-            kern = k >= kTwoRowMinK ? gemv_q4k_tma_long_kernel<NC> : gemv_q4k_tma_kernel<NC>;
+            kern = k >= kTwoRowMinK ? gemv_q4k_tma_long_kernel<NC>
+                   : pairs          ? gemv_q4k_tma_pair_kernel<NC>
+                                    : gemv_q4k_tma_kernel<NC>;
         else
-            kern = gemv_q4k_tma_kernel<NC>;
+            kern = pairs ? gemv_q4k_tma_pair_kernel<NC> : gemv_q4k_tma_kernel<NC>;
     } else {
         kern = gemv_tma_kernel<T, NC>;
     }

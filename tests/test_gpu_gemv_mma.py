@@ -88,9 +88,9 @@ def test_gemv_mma_long_rows(oracle_mod, m):
     assert_within(_run(W, n, k, xq, m, qmm.PATH_AUTO), y_ref, T, f"long rows m={m}")
 
 
-@pytest.mark.parametrize("m", [5, 8])
+@pytest.mark.parametrize("m", [6, 8])
 def test_gemv_mma_repeats_bit_exact(oracle_mod, m):
-    """The automatic path at 5..8 columns is the MMA GEMV; its partial sums of a tile are
+    """The automatic path at 6..8 columns is the MMA GEMV; its partial sums of a tile are
     added in a fixed warp order, so two calls give the same bits."""
     n, k = 3000, 5120
     W, x = qmm_synth.make_dense("q4_K", n, k, m, seed=3 + m)
