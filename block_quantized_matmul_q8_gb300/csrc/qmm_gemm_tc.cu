@@ -94,7 +94,7 @@ template <> struct TcFmt<QMM_Q4_K> : TcStages2 {
     static constexpr bool kMin = true, kScaleD = true;
     static constexpr int kUses = 8;
     static constexpr int kSub = 32;  // k values per slot
-    static constexpr uint32_t kDDBytes = 2 * 128 * 4;  // d[128], -dmin[128]
+    static constexpr uint32_t kDDBytes = 2 * 128 * 2;  // fp16 d[128], -dmin[128]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * kQ4KBytes); }
 };
 // Q5_K: Q4_K's superblock with a 32-byte plane of fifth bits (176 bytes, a whole number
@@ -106,7 +106,7 @@ template <> struct TcFmt<QMM_Q5_K> : TcStages2 {
     static constexpr bool kMin = true, kScaleD = true;
     static constexpr int kUses = 8;
     static constexpr int kSub = 32;
-    static constexpr uint32_t kDDBytes = 2 * 128 * 4;  // d[128], -dmin[128]
+    static constexpr uint32_t kDDBytes = 2 * 128 * 2;  // fp16 d[128], -dmin[128]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * kQ5KBytes); }
 };
 template <> struct TcFmt<QMM_Q8_0> : TcStages2 {
@@ -115,7 +115,7 @@ template <> struct TcFmt<QMM_Q8_0> : TcStages2 {
     static constexpr bool kMin = false, kScaleD = false;
     static constexpr int kUses = 8;
     static constexpr int kSub = 32;
-    static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
+    static constexpr uint32_t kDDBytes = 8 * 128 * 2;  // fp16 d[8 blocks][128 rows]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * 136); }
 };
 // Q4_0: the 256 k values of a step are eight 18-byte blocks (144 bytes, as a Q4_K
@@ -126,7 +126,7 @@ template <> struct TcFmt<QMM_Q4_0> : TcStages2 {
     static constexpr bool kMin = false, kScaleD = false;
     static constexpr int kUses = 8;
     static constexpr int kSub = 32;
-    static constexpr uint32_t kDDBytes = 8 * 128 * 4;  // d[8 blocks][128 rows]
+    static constexpr uint32_t kDDBytes = 8 * 128 * 2;  // fp16 d[8 blocks][128 rows]
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * 144); }
 };
 // Q6_K: a row is 210 bytes per superblock, so neither a row (210 * k/256 bytes) nor a
@@ -153,7 +153,7 @@ template <> struct TcFmt<QMM_Q6_K> {
     static constexpr bool kMin = false, kScaleD = true;
     static constexpr int kUses = 8;
     static constexpr int kSub = 32;
-    static constexpr uint32_t kDDBytes = 128 * 4;  // d[128 rows]
+    static constexpr uint32_t kDDBytes = 128 * 2;  // fp16 d[128 rows]
     // byte offset of superblock sb of weight row `row` from the start of W
     static __device__ __forceinline__ int64_t pos(int64_t row, int64_t sb, int64_t row_bytes) {
         return row * row_bytes + sb * kQ6KBytes;
@@ -585,9 +585,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 // Q5_K: the nibbles start 32 bytes later, after the plane of fifth bits
                 constexpr int kQs = T == QMM_Q4_K ? 16 : 48;
                 const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
-                // (d, -dmin) for the epilogue
-                dd[r] = half_lo(hd.x);
-                dd[128 + r] = -half_hi(hd.x);
+                // (d, -dmin) for the epilogue as fp16: d of the 128 rows, then -dmin
+                reinterpret_cast<uint16_t *>(dd)[r] = (uint16_t)(hd.x & 0xffffu);
+                reinterpret_cast<uint16_t *>(dd)[128 + r] = (uint16_t)((hd.x >> 16) ^ 0x8000u);
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t st = w_it % F::kStages;
@@ -660,7 +660,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 {
                     const uint32_t mis = (uint32_t)(reinterpret_cast<uintptr_t>(blk) & 2u);
                     const uint32_t dw = LdShared::u32(blk + 208 - mis);
-                    dd[r] = half_lo(mis ? (dw >> 16) : dw);
+                    reinterpret_cast<uint16_t *>(dd)[r] = (uint16_t)(mis ? (dw >> 16) : (dw & 0xffffu));
                 }
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 const __half2 bias = __float2half2_rn(-1152.f);
@@ -763,7 +763,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 // (high).  The d of every block goes to the epilogue; a nibble v becomes the
                 // fp16 1024 + v (v | 0x6400), and adding -1032 leaves the exact code v - 8.
 #pragma unroll
-                for (int b = 0; b < 8; ++b) dd[b * 128 + r] = __half2float(*reinterpret_cast<const __half *>(blk + 18 * b));
+                for (int b = 0; b < 8; ++b)
+                    reinterpret_cast<__half *>(dd)[b * 128 + r] = *reinterpret_cast<const __half *>(blk + 18 * b);
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 const __half2 bias = __float2half2_rn(-1032.f);
                 for (int h = 0; h < 2; ++h) {
@@ -820,7 +821,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 // byte 34b.  The d of every block goes to the epilogue; the codes become
                 // exact fp16 integers: (q ^ 0x80) | 0x6400 is the fp16 1024 + q + 128.
 #pragma unroll
-                for (int b = 0; b < 8; ++b) dd[b * 128 + r] = __half2float(*reinterpret_cast<const __half *>(blk + 34 * b));
+                for (int b = 0; b < 8; ++b)
+                    reinterpret_cast<__half *>(dd)[b * 128 + r] = *reinterpret_cast<const __half *>(blk + 34 * b);
                 ptx::mbar_arrive(ptx::smem_u32(&B.sd_full[ri]));
                 const __half2 bias = __float2half2_rn(-1152.f);
                 for (int h = 0; h < 2; ++h) {
@@ -945,42 +947,59 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     }
                     if (!ok) break;
                     if constexpr (F::kMin) {
-                        // the min group: total += d * acc + (-dmin) * minslot
+                        // the superblock's fold: total += d * acc + (-dmin) * minslot, with d
+                        // and -dmin the fp16 factors of this thread's 32 weight rows.  d * acc
+                        // is added before the min slot is awaited, and each factor comes as
+                        // four 16-byte loads issued together (loaded one column group at a
+                        // time after the wait, they held each superblock up by ~1K cycles).
+                        const uint4 *dh = reinterpret_cast<const uint4 *>(dd) + 4 * cq;
+                        const uint4 *mh = reinterpret_cast<const uint4 *>(dd) + 16 + 4 * cq;
+                        uint4 hq[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) hq[i] = dh[i];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const __half2 *h = reinterpret_cast<const __half2 *>(&hq[i]);
+#pragma unroll
+                            for (int p = 0; p < 4; ++p)
+                                tot[4 * i + p] = __ffma2_rn(__half22float2(h[p]), acc[4 * i + p], tot[4 * i + p]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) hq[i] = mh[i];
                         const uint32_t e = ge & 1;
                         if (!ptx::mbar_wait(ptx::smem_u32(&B.acc_full[e]), (ge >> 1) & 1, abortp)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
-                        const float4 *ddd = reinterpret_cast<const float4 *>(dd) + 8 * cq;
-                        const float4 *ddm = reinterpret_cast<const float4 *>(dd + 128) + 8 * cq;
+                        float vm[32];
+                        ptx::tmem_ld_32x32b_x32(lane_base + kPair * e * kTN + 32 * cq, vm);
+                        ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int hv = 0; hv < 2; ++hv) {
-                            float vm[16];
-                            ptx::tmem_ld_32x32b_x16(lane_base + kPair * e * kTN + 32 * cq + 16 * hv, vm);
-                            ptx::tmem_ld_wait();
+                        for (int i = 0; i < 4; ++i) {
+                            const __half2 *h = reinterpret_cast<const __half2 *>(&hq[i]);
 #pragma unroll
-                            for (int i4 = 0; i4 < 4; ++i4) {
-                                const float4 d4 = ddd[4 * hv + i4], m4 = ddm[4 * hv + i4];
-                                const int i = 8 * hv + 2 * i4;
-                                tot[i] = __ffma2_rn(make_float2(m4.x, m4.y), make_float2(vm[4 * i4], vm[4 * i4 + 1]),
-                                                    __ffma2_rn(make_float2(d4.x, d4.y), acc[i], tot[i]));
-                                tot[i + 1] = __ffma2_rn(make_float2(m4.z, m4.w), make_float2(vm[4 * i4 + 2], vm[4 * i4 + 3]),
-                                                        __ffma2_rn(make_float2(d4.z, d4.w), acc[i + 1], tot[i + 1]));
-                            }
+                            for (int p = 0; p < 4; ++p)
+                                tot[4 * i + p] = __ffma2_rn(__half22float2(h[p]),
+                                                            make_float2(vm[8 * i + 2 * p], vm[8 * i + 2 * p + 1]),
+                                                            tot[4 * i + p]);
                         }
                         ptx::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&B.acc_empty[e]));
                         ++ge;
                     } else {
-                        // Q6_K: total += d * acc, d the weight row's (one per column)
-                        const float4 *ddd = reinterpret_cast<const float4 *>(dd) + 8 * cq;
+                        // Q6_K: total += d * acc, d the fp16 factor of each weight row (column)
+                        const uint4 *dh = reinterpret_cast<const uint4 *>(dd) + 4 * cq;
+                        uint4 hq[4];
 #pragma unroll
-                        for (int i4 = 0; i4 < 8; ++i4) {
-                            const float4 d4 = ddd[i4];
-                            tot[2 * i4] = __ffma2_rn(make_float2(d4.x, d4.y), acc[2 * i4], tot[2 * i4]);
-                            tot[2 * i4 + 1] = __ffma2_rn(make_float2(d4.z, d4.w), acc[2 * i4 + 1], tot[2 * i4 + 1]);
+                        for (int i = 0; i < 4; ++i) hq[i] = dh[i];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const __half2 *h = reinterpret_cast<const __half2 *>(&hq[i]);
+#pragma unroll
+                            for (int p = 0; p < 4; ++p)
+                                tot[4 * i + p] = __ffma2_rn(__half22float2(h[p]), acc[4 * i + p], tot[4 * i + p]);
                         }
                     }
                 } else {
@@ -1001,21 +1020,25 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                             const float4 d4 = dxv(g32 >> 2);
                             const float dgs = (g32 & 3) == 0 ? d4.x : (g32 & 3) == 1 ? d4.y : (g32 & 3) == 2 ? d4.z : d4.w;
                             const float2 d8 = make_float2(dgs, dgs);
-                            const float4 *dwg = reinterpret_cast<const float4 *>(dd + G * 128 + 32 * cq);
+                            // the block's fp16 d of this thread's 32 weight rows, loaded together
+                            const uint4 *dwg = reinterpret_cast<const uint4 *>(dd) + G * 16 + 4 * cq;
+                            uint4 hq[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) hq[i] = dwg[i];
 #pragma unroll
                             for (int hv = 0; hv < 2; ++hv) {
                                 float v[16];
                                 ptx::tmem_ld_32x32b_x16(lane_base + (kPair * e + b2) * kTN + 32 * cq + 16 * hv, v);
                                 ptx::tmem_ld_wait();
 #pragma unroll
-                                for (int i4 = 0; i4 < 4; ++i4) {
-                                    const float4 w4 = dwg[4 * hv + i4];
-                                    const float2 s0 = __fmul2_rn(d8, make_float2(w4.x, w4.y));
-                                    const float2 s1 = __fmul2_rn(d8, make_float2(w4.z, w4.w));
-                                    tot[8 * hv + 2 * i4] =
-                                        __ffma2_rn(s0, make_float2(v[4 * i4], v[4 * i4 + 1]), tot[8 * hv + 2 * i4]);
-                                    tot[8 * hv + 2 * i4 + 1] =
-                                        __ffma2_rn(s1, make_float2(v[4 * i4 + 2], v[4 * i4 + 3]), tot[8 * hv + 2 * i4 + 1]);
+                                for (int i = 0; i < 2; ++i) {
+                                    const __half2 *h = reinterpret_cast<const __half2 *>(&hq[2 * hv + i]);
+#pragma unroll
+                                    for (int p = 0; p < 4; ++p) {
+                                        const float2 sc = __fmul2_rn(d8, __half22float2(h[p]));
+                                        tot[8 * hv + 4 * i + p] = __ffma2_rn(
+                                            sc, make_float2(v[8 * i + 2 * p], v[8 * i + 2 * p + 1]), tot[8 * hv + 4 * i + p]);
+                                    }
                                 }
                             }
                         }
