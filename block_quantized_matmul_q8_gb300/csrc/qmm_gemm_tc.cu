@@ -1342,6 +1342,18 @@ bool make_act_maps(CUtensorMap &tm_x, CUtensorMap &tm_xmin, CUtensorMap &tm_dx, 
 
 }  // namespace
 
+// More whole tiles than SMs: one persistent CTA per SM takes a contiguous run of them
+// (mode 3), so each SM's pipeline runs on from one tile into the next instead of being
+// refilled by a new CTA (Q4_K 14336 x 4096 at m = 512: 146 -> 141 us, m = 2048: 572 ->
+// 544 us; Q6_K 151936 x 5120: 3.30 -> 3.07 ms; Q4_0: 184 -> 179 us).  Q5_K stays on one CTA
+// per tile, which balances better across SMs for its longer unpack (187 against 198 us).
+static int persistent_whole_tiles(qmm_type t, const qmm_gemm_plan &p, int nsm, TcArgs &args) {
+    if (p.stream_k || p.ntiles <= nsm || t == QMM_Q5_K) return p.ctas;
+    args.stream_k = 3;
+    args.ctas = nsm;
+    return nsm;
+}
+
 cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, const void *xq, int64_t m, float *y,
                            void *ws, size_t ws_bytes, int stream_k_mode, cudaStream_t st, int64_t stride) {
     if (!gemm_tc_supported(t, n, k, m, stride)) return cudaErrorNotSupported;
@@ -1383,12 +1395,13 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
     args.nwork = p.nwork;
     args.ctas = p.ctas;
     args.stream_k = p.stream_k;
+    const int ctas = persistent_whole_tiles(t, p, nsm, args);
     const int64_t fixup_tiles = (p.stream_k && p.fixup) ? p.ntiles : 0;
-    if (t == QMM_Q8_0) return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
-    if (t == QMM_Q4_0) return run_tc<QMM_Q4_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
-    if (t == QMM_Q5_K) return run_tc<QMM_Q5_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
-    if (t == QMM_Q6_K) return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
-    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, p.ctas, fixup_tiles, st);
+    if (t == QMM_Q8_0) return run_tc<QMM_Q8_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup_tiles, st);
+    if (t == QMM_Q4_0) return run_tc<QMM_Q4_0>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup_tiles, st);
+    if (t == QMM_Q5_K) return run_tc<QMM_Q5_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup_tiles, st);
+    if (t == QMM_Q6_K) return run_tc<QMM_Q6_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup_tiles, st);
+    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w, args, ctas, fixup_tiles, st);
 }
 
 // ---------------------------------------------------------------- fused gate/up + SwiGLU
@@ -1402,7 +1415,8 @@ size_t gemm_tc_glu_workspace_bytes(qmm_type t, int64_t n_out, int64_t k, int64_t
 }
 
 // Whole tiles only (the GLU needs both complete dots in one thread, [MMQ] section
-// "「分专家」与「整批」之间: host 侧的代价"), so the schedule is one tile per CTA.
+// "「分专家」与「整批」之间: host 侧的代价"): one tile per CTA, or runs of whole tiles on
+// persistent CTAs when there are more tiles than SMs.
 cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64_t n_out, int64_t k, const void *xq,
                                int64_t m, float *y, void *ws, size_t ws_bytes, cudaStream_t st) {
     // Wu == nullptr: Wg holds the gate and up rows interleaved (2 n_out rows)
@@ -1454,7 +1468,8 @@ cudaError_t launch_gemm_tc_glu(qmm_type t, const void *Wg, const void *Wu, int64
     args.stream_k = 0;
     args.n_out = n_out;
     args.glu_packed = packed ? 1 : 0;
-    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, args, p.ctas, 0, st);
+    const int ctas = persistent_whole_tiles(t, p, nsm, args);
+    return run_tc<QMM_Q4_K>(tm_x, tm_xmin, tm_dx, tm_w, tm_w2, args, ctas, 0, st);
 }
 
 // ---------------------------------------------------------------- expert-grouped mode

@@ -59,6 +59,13 @@ def test_tc_auto_schedule(oracle_mod):
     run_tc(oracle_mod, 1000, 1024, 300, 0, seed=3)
 
 
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q8_0", "q4_0", "q5_K"])
+def test_tc_persistent_whole_tiles(oracle_mod, fmt):
+    """More whole tiles than SMs (16 x 11 = 176, ragged in both dimensions): persistent CTAs
+    that each take a contiguous run of tiles (Q5_K keeps one CTA per tile)."""
+    run_tc(oracle_mod, 2000, 256, 1290, 1, seed=17, fmt=fmt)
+
+
 def test_tc_integer_exactness(oracle_mod):
     """Activations whose q8_1 codes hit +-127 everywhere: the largest integer dots
     (32 * 945 * 127 per sub-block) must still be exact in the fp32 accumulators."""

@@ -49,7 +49,7 @@ def test_glu_gemv(oracle_mod, n, k, m):
 
 
 @pytest.mark.parametrize("n,k,m", [(64, 256, 9), (130, 512, 64), (300, 1024, 129), (1000, 2048, 200),
-                                   (65, 256, 513)])
+                                   (65, 256, 513), (1000, 256, 1290)])
 def test_glu_tensor_core(oracle_mod, n, k, m):
     run_glu(oracle_mod, "q4_K", n, k, m, seed=2 * n + m)
 
@@ -110,7 +110,7 @@ def run_packed(oracle_mod, fmt, n, k, m, path=0, seed=0):
 # The fused paths fold the same rows in the same order from either layout: equal to the bit
 @pytest.mark.parametrize("n,k,m,path", [(1000, 2048, 1, 0), (1001, 512, 3, 0), (777, 1024, 8, 0),
                                         (64, 256, 9, 0), (300, 1024, 129, 0), (65, 256, 513, 0),
-                                        (200, 512, 4, 3)])
+                                        (200, 512, 4, 3), (1000, 256, 1290, 0)])
 def test_glu_packed_fused_bitexact(oracle_mod, n, k, m, path):
     a, b = run_packed(oracle_mod, "q4_K", n, k, m, path=path, seed=n + m)
     assert np.array_equal(a, b)
