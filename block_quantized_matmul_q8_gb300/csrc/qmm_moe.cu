@@ -295,20 +295,22 @@ __global__ void moe_glu_combine_kernel(const float *__restrict__ g, const float 
         y[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
 }
 
-// The cold experts' SwiGLU: rows of their pairs from the gate and up products.
+// The cold experts' SwiGLU: rows of their pairs from the gate and up products.  Block (p, c)
+// takes pair p of cold expert c (a cold expert has at most kColdMaxPairs pairs), so every row
+// has its own block (one block per expert walking its rows one after another took ~95 us).
 __global__ void moe_glu_cold_combine_kernel(const int32_t *__restrict__ cold, const int32_t *__restrict__ ncold,
                                             const int32_t *__restrict__ bounds, const int32_t *__restrict__ perm,
                                             const float *__restrict__ g, const float *__restrict__ u,
                                             float *__restrict__ y, int64_t n) {
     const int nc = *ncold;
-    for (int c = blockIdx.x; c < nc; c += gridDim.x) {
+    for (int c = blockIdx.y; c < nc; c += gridDim.y) {
         const int e = cold[c];
-        for (int j = bounds[e]; j < bounds[e + 1]; ++j) {
-            const int64_t off = int64_t(perm[j]) * n;
-            for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-                const float gv = g[off + i];
-                y[off + i] = gv / (1.0f + expf(-gv)) * u[off + i];
-            }
+        const int j = bounds[e] + (int)blockIdx.x;
+        if (j >= bounds[e + 1]) continue;
+        const int64_t off = int64_t(perm[j]) * n;
+        for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+            const float gv = g[off + i];
+            y[off + i] = gv / (1.0f + expf(-gv)) * u[off + i];
         }
     }
 }
@@ -378,8 +380,8 @@ cudaError_t launch_mul_mat_id_glu(qmm_type t, const void *Wg, const void *Wu, in
                                        h ? u : g, status, base + L.cold_gemm, L.total - L.cold_gemm, st);
             if (e != cudaSuccess) return e;
         }
-        const int grid = (int)std::min<int64_t>(n_experts, int64_t(device_sm_count()) * 2);
-        moe_glu_cold_combine_kernel<<<std::max(grid, 1), 256, 0, st>>>(cold, status + 3, bounds, perm, g, u, y, n);
+        const dim3 grid(kColdMaxPairs, (unsigned)std::min<int64_t>(std::max<int64_t>(n_experts, 1), 65535));
+        moe_glu_cold_combine_kernel<<<grid, 256, 0, st>>>(cold, status + 3, bounds, perm, g, u, y, n);
         return cudaGetLastError();
     }
     // unfused: both products through mul_mat_id, then y = silu(g) * u (invalid pairs: 0 * 0)
