@@ -345,7 +345,10 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
     constexpr int kGroups = F::kUses / kPair;  // slot pairs per superblock (the min group comes on top)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ Barriers B;
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned, derived from the shared array by an offset so that the compiler keeps
+    // every access through it a shared-memory one (a round trip through an integer turned them
+    // into generic loads and stores)
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = ptx::smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abortp = &B.abort;

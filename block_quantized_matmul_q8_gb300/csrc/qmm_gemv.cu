@@ -376,7 +376,7 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
                                               int *status, const uint8_t *__restrict__ W2 = nullptr) {
     constexpr int kCR = GLU ? kTmaChunkRows / 2 : kTmaChunkRows;  // outputs per chunk
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared pointer
     __shared__ __align__(8) uint64_t full[kTmaMaxStages], empty[kTmaMaxStages];
     __shared__ int abort_flag;
     const int U = (int)gemv_units(k);

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     gemv_q4k_mma_kernel(const uint8_t *__restrict__ W, int64_t n, int k, int m, int nstages, int64_t row_stride,
                         int64_t x_stride, const uint8_t *__restrict__ xq, float *__restrict__ y, int *status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared pointer
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
     __shared__ int abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

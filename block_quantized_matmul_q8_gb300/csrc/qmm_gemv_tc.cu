@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ Barriers B;
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared pointer
     const uint32_t sbase = ptx::smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abortp = &B.abort;
