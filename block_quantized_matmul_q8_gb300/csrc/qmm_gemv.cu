@@ -76,6 +76,27 @@ struct XIn {
     const float *xf;  // non-null: quantize these instead of reading xq
 };
 
+// 1/d within 2^-22 (rcp.approx: at most 1 ulp), or 0 where d is outside [2^-100, 2^125) and the
+// quotient must be taken (1/d would be subnormal or huge there, and NaN and infinities fail
+// the test).
+__device__ __forceinline__ float rcp_guarded(float d) {
+    if (!(d >= 0x1p-100f && d < 0x1p+125f)) return 0.0f;
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+// The q8_1 code of v (the integer of q8_1_code) from that reciprocal.  With |v| <= 127.00001 d,
+// t = v rd is within 128 (2^-22 + 2^-24) < 2^-14 of v/d and the IEEE quotient within 2^-17
+// of it, so both round to the same integer unless |t| lies within 2^-11 of a half-integer;
+// there, or when rd == 0, the quotient is computed.
+__device__ __forceinline__ int q8_1_code_rcp(float v, float d, float rd) {
+    if (rd == 0.0f) return q8_1_code(v, d);
+    const float t = v * rd;
+    const float a = fabsf(t);
+    if (fabsf((a - truncf(a)) - 0.5f) < 0x1p-11f) return q8_1_code(v, d);
+    return (int)rintf(t);
+}
+
 template <int NC>
 __device__ __forceinline__ void stage_x(const XIn &x, int k, int U, uint8_t *xs, float2 *xds, int t, int nthreads) {
     const int nb32 = k / 32;
@@ -93,46 +114,53 @@ __device__ __forceinline__ void stage_x(const XIn &x, int k, int U, uint8_t *xs,
         }
         return;
     }
-    // 8 lanes per 32-value block, 4 values (one 16-byte load) per lane: a warp
-    // quantizes 4 blocks per pass, and the loads of kBatch passes are issued before
-    // the first is used.  Max and integer sum are exact in any order, so the result
-    // is the quantizer kernel's to the bit.
-    constexpr int kBatch = 4;
-    const int lane = t & 31, w = t >> 5, nw = nthreads >> 5, g = lane >> 3, l8 = lane & 7;
-    const int ngroups = (total + 3) / 4;
+    // 4 lanes per 32-value block, 8 values (two 16-byte loads) per lane: a warp quantizes
+    // 8 blocks per pass, and the loads of kBatch passes are issued before the first is
+    // used.  Max and integer sum are exact in any order, d is the quantizer's correctly
+    // rounded quotient, and every code is the quantizer's integer (q8_1_code_rcp), so the
+    // staged bytes are the quantizer kernel's to the bit.
+    constexpr int kBatch = 2;
+    const int lane = t & 31, w = t >> 5, nw = nthreads >> 5, g = lane >> 2, l4 = lane & 3;
+    const int ngroups = (total + 7) / 8;
     for (int i0 = w; i0 < ngroups; i0 += nw * kBatch) {
-        float4 v[kBatch];
+        float4 va[kBatch], vb[kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            const int blk = 4 * (i0 + j * nw) + g;
-            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int blk = 8 * (i0 + j * nw) + g;
+            va[j] = vb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (blk < total) {
                 const int c = blk / nb32, b = blk - c * nb32;
-                v[j] = reinterpret_cast<const float4 *>(x.xf + size_t(c) * k + 32 * b)[l8];
+                const float4 *src = reinterpret_cast<const float4 *>(x.xf + size_t(c) * k + 32 * b);
+                va[j] = src[2 * l4];
+                vb[j] = src[2 * l4 + 1];
             }
         }
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
             if (i0 + j * nw >= ngroups) break;  // warp-uniform
-            const int blk = 4 * (i0 + j * nw) + g;
-            float amax = fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w)));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+            const int blk = 8 * (i0 + j * nw) + g;
+            const float4 a4 = va[j], b4 = vb[j];
+            float amax = fmaxf(fmaxf(fmaxf(fabsf(a4.x), fabsf(a4.y)), fmaxf(fabsf(a4.z), fabsf(a4.w))),
+                               fmaxf(fmaxf(fabsf(b4.x), fabsf(b4.y)), fmaxf(fabsf(b4.z), fabsf(b4.w))));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            const float d = q8_1_scale(amax), rd = q8_1_recip(d);
-            const int q0 = q8_1_code_fast(v[j].x, d, rd), q1 = q8_1_code_fast(v[j].y, d, rd);
-            const int q2 = q8_1_code_fast(v[j].z, d, rd), q3 = q8_1_code_fast(v[j].w, d, rd);
-            int S = q0 + q1 + q2 + q3;
-            S += __shfl_xor_sync(0xffffffffu, S, 4);
+            const float d = q8_1_scale(amax), rd = rcp_guarded(d);
+            const int q0 = q8_1_code_rcp(a4.x, d, rd), q1 = q8_1_code_rcp(a4.y, d, rd);
+            const int q2 = q8_1_code_rcp(a4.z, d, rd), q3 = q8_1_code_rcp(a4.w, d, rd);
+            const int q4 = q8_1_code_rcp(b4.x, d, rd), q5 = q8_1_code_rcp(b4.y, d, rd);
+            const int q6 = q8_1_code_rcp(b4.z, d, rd), q7 = q8_1_code_rcp(b4.w, d, rd);
+            int S = ((q0 + q1) + (q2 + q3)) + ((q4 + q5) + (q6 + q7));
             S += __shfl_xor_sync(0xffffffffu, S, 2);
             S += __shfl_xor_sync(0xffffffffu, S, 1);
             if (blk < total) {
                 const int c = blk / nb32, b = blk - c * nb32;
-                const uint32_t packed = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) |
-                                        ((uint32_t(q2) & 0xffu) << 16) | ((uint32_t(q3) & 0xffu) << 24);
-                reinterpret_cast<uint32_t *>(xs + (size_t(c) * U + (b >> 1)) * kUnitStride + 32 * (b & 1))[l8] =
-                    packed;
-                if (l8 == 0) {
+                const uint32_t lo = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) |
+                                    ((uint32_t(q2) & 0xffu) << 16) | ((uint32_t(q3) & 0xffu) << 24);
+                const uint32_t hi = (uint32_t(q4) & 0xffu) | ((uint32_t(q5) & 0xffu) << 8) |
+                                    ((uint32_t(q6) & 0xffu) << 16) | ((uint32_t(q7) & 0xffu) << 24);
+                reinterpret_cast<uint2 *>(xs + (size_t(c) * U + (b >> 1)) * kUnitStride + 32 * (b & 1))[l4] =
+                    make_uint2(lo, hi);
+                if (l4 == 0) {
                     const uint32_t dsw = q8_1_ds_word(d, S);
                     xds[size_t(c) * 2 * U + b] = make_float2(half_lo(dsw), half_hi(dsw));
                 }
