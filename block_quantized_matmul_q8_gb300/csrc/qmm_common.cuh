@@ -67,21 +67,27 @@ __device__ __forceinline__ uint4 ldg16(const void *p) {
 // stored d_h = fp16(d), s_h = fp16(float(d_h) * sum q); a block with d == 0 is all zero.
 __device__ __forceinline__ float q8_1_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
 __device__ __forceinline__ int q8_1_code(float v, float d) { return d != 0.0f ? (int)roundf(__fdiv_rn(v, d)) : 0; }
-// The same code with the division replaced by a product with rd = 1/d (correctly
-// rounded) wherever that cannot change the integer.  With d normal and |v| <= 127.00001 d
-// (v in the block of amax = 127 d), the product t = v*rd is within 2^-16 of v/d
-// (two roundings of relative size 2^-24, |v/d| < 128) and the IEEE quotient within
-// 2^-17, so the two round to the same integer unless |t| lies within 2^-15 of a
-// half-integer; within 2^-14 of one, or when d is tiny or zero (rd == 0), the IEEE
-// quotient is computed after all.
-__device__ __forceinline__ float q8_1_recip(float d) { return d >= 0x1p-100f ? __frcp_rn(d) : 0.0f; }
-__device__ __forceinline__ int q8_1_code_fast(float v, float d, float rd) {
+// The code without a division wherever that cannot change the integer: rd is 1/d within
+// 2^-22 (rcp.approx: at most 1 ulp), or 0 where d is outside [2^-100, 2^125) and the quotient
+// must be taken (1/d would be subnormal or huge there, and NaN and infinities fail the test).
+__device__ __forceinline__ float rcp_guarded(float d) {
+    if (!(d >= 0x1p-100f && d < 0x1p+125f)) return 0.0f;
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+}
+// The q8_1 code of v (the integer of q8_1_code) from that reciprocal.  With |v| <= 127.00001 d,
+// t = v rd is within 128 (2^-22 + 2^-24) < 2^-14 of v/d and the IEEE quotient within 2^-17
+// of it, so both round to the same integer unless |t| lies within 2^-11 of a half-integer;
+// there, or when rd == 0, the quotient is computed.
+__device__ __forceinline__ int q8_1_code_rcp(float v, float d, float rd) {
     if (rd == 0.0f) return q8_1_code(v, d);
     const float t = v * rd;
     const float a = fabsf(t);
-    if (fabsf((a - truncf(a)) - 0.5f) < 0x1p-14f) return q8_1_code(v, d);
-    return (int)rintf(t);  // not within 2^-14 of a tie: the nearest integer either way
+    if (fabsf((a - truncf(a)) - 0.5f) < 0x1p-11f) return q8_1_code(v, d);
+    return (int)rintf(t);
 }
+
 // The (d_h, s_h) word of a block: d_h in the low half, s_h in the high half.
 __device__ __forceinline__ uint32_t q8_1_ds_word(float d, int sum_q) {
     if (d == 0.0f) return 0u;

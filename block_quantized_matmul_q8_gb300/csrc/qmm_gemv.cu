@@ -76,27 +76,6 @@ struct XIn {
     const float *xf;  // non-null: quantize these instead of reading xq
 };
 
-// 1/d within 2^-22 (rcp.approx: at most 1 ulp), or 0 where d is outside [2^-100, 2^125) and the
-// quotient must be taken (1/d would be subnormal or huge there, and NaN and infinities fail
-// the test).
-__device__ __forceinline__ float rcp_guarded(float d) {
-    if (!(d >= 0x1p-100f && d < 0x1p+125f)) return 0.0f;
-    float r;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
-    return r;
-}
-// The q8_1 code of v (the integer of q8_1_code) from that reciprocal.  With |v| <= 127.00001 d,
-// t = v rd is within 128 (2^-22 + 2^-24) < 2^-14 of v/d and the IEEE quotient within 2^-17
-// of it, so both round to the same integer unless |t| lies within 2^-11 of a half-integer;
-// there, or when rd == 0, the quotient is computed.
-__device__ __forceinline__ int q8_1_code_rcp(float v, float d, float rd) {
-    if (rd == 0.0f) return q8_1_code(v, d);
-    const float t = v * rd;
-    const float a = fabsf(t);
-    if (fabsf((a - truncf(a)) - 0.5f) < 0x1p-11f) return q8_1_code(v, d);
-    return (int)rintf(t);
-}
-
 template <int NC>
 __device__ __forceinline__ void stage_x(const XIn &x, int k, int U, uint8_t *xs, float2 *xds, int t, int nthreads) {
     const int nb32 = k / 32;

@@ -69,9 +69,19 @@ def test_quantize_tie_and_scale_edges(oracle_mod):
     assert np.array_equal(got, oracle_mod.quantize_q8_1(x))
 
 
-def test_quantize_near_ties_bitexact(oracle_mod):
-    """Quotients within a few ulps of the rounding ties, over scales from 2^-20 to 2^20."""
-    x = near_tie_rows(21, 4096).reshape(8, -1)
+@pytest.mark.parametrize("nrows,shape", [(4096, (8, -1)), (512, (1, -1))])
+def test_quantize_near_ties_bitexact(oracle_mod, nrows, shape):
+    """Quotients within a few ulps of the rounding ties, over scales from 2^-20 to 2^20: 4096
+    blocks (4 lanes per block) and 512 (a warp per block)."""
+    x = near_tie_rows(21, nrows).reshape(*shape)
+    got = qmm.qmm_quantize_q8_1(to_dev(x)).cpu().numpy()
+    assert np.array_equal(got, oracle_mod.quantize_q8_1(x))
+
+
+def test_quantize_adversarial_many_blocks(oracle_mod):
+    """The adversarial rows repeated past 2048 blocks, so the 4-lanes-per-block form runs."""
+    row = adversarial_x_rows().reshape(1, -1)
+    x = np.tile(row, (max(1, -(-2048 * 32 // row.size)), 1))
     got = qmm.qmm_quantize_q8_1(to_dev(x)).cpu().numpy()
     assert np.array_equal(got, oracle_mod.quantize_q8_1(x))
 
