@@ -557,7 +557,7 @@ def main():
                          "algorithmic_bytes": kb},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": M * K * 4,
                     "d2h_bytes_per_step": M * N * 4, "ms_per_step": ms_e2e / args.steps,
-                    "how": "one qmm_mul_mat_f32_host call per step (eager, no graph): the C ABI enqueues the copy of pinned host x, the GEMV and the copy of y back"},
+                    "how": "one qmm_mul_mat_f32_host call per step (eager, no graph) on page-locked host x and y: the GEMV reads x and writes y in host memory in place (the bytes cross the CPU-GPU link inside the timed region)"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,

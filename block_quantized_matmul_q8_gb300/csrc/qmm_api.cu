@@ -394,6 +394,21 @@ qmm_status qmm_mul_mat_f32(const void *W, qmm_type t, int64_t n, int64_t k, cons
 
 // Host-buffer form: x_dev [m][k] and y_dev [m][n] at the head of the workspace, each
 // 256-byte aligned, then the qmm_mul_mat_f32 workspace.
+constexpr size_t kMappedOutMax = size_t(1) << 20;  // y written in place up to 1 MB
+
+// The device address of a page-locked (registered or cudaHostAlloc'd) host buffer, if it
+// has one and it is `align`-byte aligned; nullptr otherwise (pageable memory, device
+// memory, or a query error, which is cleared).
+static const void *mapped_host(const void *p, size_t align) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+    if (reinterpret_cast<uintptr_t>(a.devicePointer) % align) return nullptr;
+    return a.devicePointer;
+}
 static size_t host_io_bytes(int64_t n, int64_t k, int64_t m) {
     return align256(size_t(m) * size_t(k) * 4) + align256(size_t(m) * size_t(n) * 4);
 }
@@ -416,14 +431,25 @@ qmm_status qmm_mul_mat_f32_host(const void *W, qmm_type t, int64_t n, int64_t k,
     if (!aligned256(workspace)) return QMM_ERR_ALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *base = static_cast<uint8_t *>(workspace);
-    float *x_dev = reinterpret_cast<float *>(base);
-    float *y_dev = reinterpret_cast<float *>(base + align256(size_t(m) * size_t(k) * 4));
     const size_t io = host_io_bytes(n, k, m);
-    if (cudaMemcpyAsync(x_dev, x_host, size_t(m) * size_t(k) * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return QMM_ERR_CUDA;
-    s = qmm_mul_mat_f32(W, t, n, k, x_dev, m, y_dev, base + io, ws_bytes - io, stream);
+    // Page-locked host buffers are mapped into the device's address space: the kernels read
+    // x and write y there in place, over the CPU-GPU link, instead of a copy engine moving
+    // them before and after (a copy is a separate operation on the stream, with its own
+    // start-up, between which the kernel cannot begin).  y goes through a device copy when
+    // it is large.  Pageable buffers always take the copies.
+    const float *x_in = static_cast<const float *>(mapped_host(x_host, 16));
+    float *y_out = size_t(m) * size_t(n) * 4 <= kMappedOutMax ? static_cast<float *>(const_cast<void *>(mapped_host(y_host, 16))) : nullptr;
+    if (!x_in) {
+        float *x_dev = reinterpret_cast<float *>(base);
+        if (cudaMemcpyAsync(x_dev, x_host, size_t(m) * size_t(k) * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return QMM_ERR_CUDA;
+        x_in = x_dev;
+    }
+    float *y_dev = y_out ? y_out : reinterpret_cast<float *>(base + align256(size_t(m) * size_t(k) * 4));
+    s = qmm_mul_mat_f32(W, t, n, k, x_in, m, y_dev, base + io, ws_bytes - io, stream);
     if (s != QMM_OK) return s;
-    if (cudaMemcpyAsync(y_host, y_dev, size_t(m) * size_t(n) * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (!y_out &&
+        cudaMemcpyAsync(y_host, y_dev, size_t(m) * size_t(n) * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return QMM_ERR_CUDA;
     return QMM_OK;
 }

@@ -150,16 +150,17 @@ QMM_API qmm_status qmm_mul_mat_f32(const void *W, qmm_type t, int64_t n, int64_t
                                    float *y, void *workspace, size_t ws_bytes, void *stream);
 
 /*
- * qmm_mul_mat_f32 with x and y in HOST memory: one call enqueues the copy of x to the
- * device, the product and the copy of y back, all on `stream` (an interface of this
+ * qmm_mul_mat_f32 with x and y in HOST memory, all on `stream` (an interface of this
  * library; the pages have no counterpart).  The same y as qmm_mul_mat_f32 to the bit.
- *   x_host : fp32 [m][k]; y_host : fp32 [m][n].  With page-locked host memory the
- *            copies are asynchronous: the host buffers must stay valid, and y_host
- *            unread, until the stream has passed the call.  With pageable y_host the
- *            runtime makes the copy back synchronous, so the call returns with y in
- *            y_host.
+ *   x_host : fp32 [m][k]; y_host : fp32 [m][n].  A page-locked buffer (16-byte aligned;
+ *            y up to 1 MB) is read or written by the kernels in place through its mapped
+ *            device address; any other buffer goes through a copy into or out of the
+ *            workspace.  The host buffers must stay valid, and y_host unread, until the
+ *            stream has passed the call.  With pageable y_host the runtime makes the copy
+ *            back synchronous, so the call returns with y in y_host.
  *   workspace : at least qmm_workspace_bytes_f32_host(t, n, k, m) bytes, 256-byte
- *            aligned: device copies of x and y at its head, then the qmm_mul_mat_f32
+ *            aligned: room for device copies of x and y at its head (used by the
+ *            buffers that are copied), then the qmm_mul_mat_f32
  *            workspace.
  * Errors as qmm_mul_mat_f32; QMM_ERR_CUDA if a copy cannot be enqueued.
  */

@@ -106,17 +106,20 @@ def test_f32_near_ties_equal_two_calls(oracle_mod, m):
 
 
 @pytest.mark.parametrize("fmt,n,k,m", [("q4_K", 1000, 512, 1), ("q4_K", 129, 2304, 5), ("q8_0", 33, 160, 20),
-                                       ("q4_0", 129, 2048, 1)])
-@pytest.mark.parametrize("pinned", [True, False])
+                                       ("q4_0", 129, 2048, 1), ("q4_K", 14336, 256, 20)])
+@pytest.mark.parametrize("pinned", ["both", "x", "none"])
 def test_f32_host_buffers(oracle_mod, fmt, n, k, m, pinned):
-    """The host-buffer call gives the bits of the device call, from pinned or pageable
-    host memory."""
+    """The host-buffer call gives the bits of the device call, from pinned or pageable host
+    memory: page-locked buffers are read and written in place (y only up to 1 MB; the
+    14336-column case takes the copy back), pageable ones through copies."""
     W, x = qmm_synth.make_dense(fmt, n, k, m, seed=n + 3 * m)
     Wd = to_dev(W)
     x_h = torch.from_numpy(x)
     y_h = torch.full((m, n), float("nan"))
-    if pinned:
-        x_h, y_h = x_h.pin_memory(), y_h.pin_memory()
+    if pinned in ("both", "x"):
+        x_h = x_h.pin_memory()
+    if pinned == "both":
+        y_h = y_h.pin_memory()
     ws = torch.empty(max(256, qmm.qmm_workspace_bytes_f32_host(fmt, n, k, m)), dtype=torch.uint8, device=DEV)
     qmm.qmm_mul_mat_f32_host(Wd, fmt, n, k, x_h, m, y_h, ws)
     y_d = qmm.qmm_mul_mat_f32(Wd, fmt, n, k, to_dev(x), m)
