@@ -429,6 +429,7 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
         // ---------------- producer warp: one lane issues every copy
         if (lane == 0) {
             int issued = 0;
+            const int stagger = nchunks >= 6 ? 2 : 1;  // the chunk after which the copy lane waits
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c % nstages;
                 if (c >= nstages && !ptx::mbar_wait(ptx::smem_u32(&empty[s]), ((c / nstages) - 1) & 1, abortp))
@@ -452,11 +453,16 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
                     ptx::bulk_g2s(ptx::smem_u32(stages + s * stage_bytes), W + a * row_bytes, bytes, bar);
                 }
                 ++issued;
-                // Every CTA asks for its first two chunks and lets them land before asking
-                // for the rest: requested all at once, the first chunks of all CTAs queue
-                // behind everyone's later stages and the consumers start about 3 us late
-                // (measured: one launch of the decode GEMV 12.1 -> 10.5 us).
-                if (c == 1 && nchunks > 2 && !ptx::mbar_wait(ptx::smem_u32(&full[1]), 0, abortp)) break;
+                // Every CTA asks for its first chunks and lets them land before asking for
+                // the rest: requested all at once, the first chunks of all CTAs queue behind
+                // everyone's later stages and the consumers start about 3 us late (measured:
+                // one launch of the decode GEMV 12.1 -> 10.5 us).  Three first chunks where a
+                // CTA has 6 or more (17408 x 5120 from q8_1 9.5 -> 9.1 us, 2-4 columns 3-5%
+                // faster), two where it has fewer (4096 x 14336 and Q8_0 5120 x 5120 lose 7-8%
+                // with three).
+                if (c == stagger && nchunks > stagger + 1 &&
+                    !ptx::mbar_wait(ptx::smem_u32(&full[stagger]), 0, abortp))
+                    break;
             }
             // no copy may still be writing shared memory when the CTA exits: wait for the
             // last nstages issued chunks (each wait bounded, independent of the abort flag)
