@@ -88,6 +88,26 @@ __device__ __forceinline__ int q8_1_code_rcp(float v, float d, float rd) {
     return (int)rintf(t);
 }
 
+// The codes of N values of one block (a lane's share of it), as q8_1_code_rcp gives them
+// but with one test per share: r = rint(v rd) is the code unless some product lies within
+// 2^-11 of a half-integer (|t - r| > 1/2 - 2^-11) or rd == 0, and then every code of the
+// share is taken from the quotient.
+template <int N>
+__device__ __forceinline__ void q8_1_codes_rcp(const float (&v)[N], float d, float rd, int (&q)[N]) {
+    float far = 0.0f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float t = v[i] * rd;
+        const float r = rintf(t);
+        far = fmaxf(far, fabsf(t - r));
+        q[i] = (int)r;
+    }
+    if (rd == 0.0f || far > 0.5f - 0x1p-11f) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) q[i] = q8_1_code(v[i], d);
+    }
+}
+
 // The (d_h, s_h) word of a block: d_h in the low half, s_h in the high half.
 __device__ __forceinline__ uint32_t q8_1_ds_word(float d, int sum_q) {
     if (d == 0.0f) return 0u;

@@ -66,10 +66,10 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restr
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         const float d = q8_1_scale(amax), rd = rcp_guarded(d);
-        const int q0 = q8_1_code_rcp(a4.x, d, rd), q1 = q8_1_code_rcp(a4.y, d, rd);
-        const int q2 = q8_1_code_rcp(a4.z, d, rd), q3 = q8_1_code_rcp(a4.w, d, rd);
-        const int q4 = q8_1_code_rcp(b4.x, d, rd), q5 = q8_1_code_rcp(b4.y, d, rd);
-        const int q6 = q8_1_code_rcp(b4.z, d, rd), q7 = q8_1_code_rcp(b4.w, d, rd);
+        const float vv[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+        int qq[8];
+        q8_1_codes_rcp(vv, d, rd, qq);
+        const int q0 = qq[0], q1 = qq[1], q2 = qq[2], q3 = qq[3], q4 = qq[4], q5 = qq[5], q6 = qq[6], q7 = qq[7];
         int S = ((q0 + q1) + (q2 + q3)) + ((q4 + q5) + (q6 + q7));
         S += __shfl_xor_sync(0xffffffffu, S, 2);
         S += __shfl_xor_sync(0xffffffffu, S, 1);
