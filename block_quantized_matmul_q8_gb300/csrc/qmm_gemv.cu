@@ -371,9 +371,9 @@ __device__ __forceinline__ void fold_q4k_unit2(const uint8_t *row0, const uint8_
 // both dots of an output, no stream-K).  n counts outputs; W is the gate and W2 the up
 // weight, each [n] rows, or with W2 == nullptr W holds both interleaved (2n rows: gate j
 // at 2j, up j at 2j+1, as qmm_repack_glu writes them).  A chunk holds 4 outputs as 8
-// staged rows (gate j, up j, ...): one bulk copy per row, or one for the chunk when the
-// rows are interleaved; the two half-warps of a warp fold one pair and lane 0 writes
-// silu(gate) * up.
+// staged rows: the 4 gate rows and then the 4 up rows, a bulk copy each (one copy per row
+// took 19.5 us for 2 x 14336 x 4096 at one column), or the interleaved pairs in one copy;
+// the two half-warps of a warp fold one pair and lane 0 writes silu(gate) * up.
 // kTwoRows (Q4_K, not GLU): each warp folds its two rows of a chunk together, lanes
 // taking units lane + 32 j, so every unit's staged activations are read once for both
 // rows; chosen by the host for long rows, where a CTA folds few chunks.
@@ -442,10 +442,11 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
                     if (!W2)  // interleaved gate/up rows (qmm_repack_glu): the chunk is one block
                         ptx::bulk_g2s(ptx::smem_u32(stages + s * stage_bytes), W + 2 * a * row_bytes,
                                       uint32_t(2 * (b - a) * row_bytes), bar);
-                    for (int64_t i = 0; W2 && i < b - a; ++i) {
-                        const uint32_t dst = ptx::smem_u32(stages + s * stage_bytes + size_t(2 * i) * row_bytes);
-                        ptx::bulk_g2s(dst, W + (a + i) * row_bytes, uint32_t(row_bytes), bar);
-                        ptx::bulk_g2s(dst + uint32_t(row_bytes), W2 + (a + i) * row_bytes, uint32_t(row_bytes), bar);
+                    if (W2) {  // two tensors: the chunk's gate rows, then its up rows, a copy each
+                        const uint32_t dst = ptx::smem_u32(stages + s * stage_bytes);
+                        ptx::bulk_g2s(dst, W + a * row_bytes, uint32_t((b - a) * row_bytes), bar);
+                        ptx::bulk_g2s(dst + uint32_t(kCR * row_bytes), W2 + a * row_bytes, uint32_t((b - a) * row_bytes),
+                                      bar);
                     }
                 } else {
                     const uint32_t bytes = uint32_t((b - a) * row_bytes);
@@ -477,7 +478,10 @@ __device__ __forceinline__ void gemv_tma_body(const uint8_t *__restrict__ W, int
         asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumerWarps * 32) : "memory");
 
         const int grp = warp / kGW, gw = warp % kGW;
-        const int rr = 2 * gw + (lane >> 4);  // row within a chunk
+        // staged row of this half-warp: GLU from two tensors stages the chunk's gate rows
+        // and then its up rows, so output gw's pair is rows gw and kCR + gw; interleaved
+        // (and plain) chunks hold row pairs side by side
+        const int rr = (GLU && W2) ? ((lane >> 4) ? kCR + gw : gw) : 2 * gw + (lane >> 4);
         const int c4 = l16 & 3;               // qs chunk of every unit this lane takes (Q4_K)
         const Q4KPairSel psel = q4k_pair_sel(c4);
         for (int c = grp; grp < ngroups && c < nchunks; c += ngroups) {
