@@ -160,6 +160,10 @@ template <> struct TcFmt<QMM_Q6_K> {
     }
 };
 
+// Q6_K row groups: one box of 16 rows x 240 bytes per row residue mod 8
+constexpr uint32_t kQ6GroupBox = 16 * TcFmt<QMM_Q6_K>::kRawRow;
+static_assert(8 * kQ6GroupBox == TcFmt<QMM_Q6_K>::kRawBuf && kQ6GroupBox % 128 == 0, "Q6_K group boxes");
+
 // dynamic shared memory map (offsets from a 1024-aligned base)
 constexpr uint32_t kSlabBytes = 128 * 128;  // 128 rows x 64 fp16
 template <int T> struct TcMap {
@@ -216,6 +220,10 @@ struct TcArgs {
     // kernel reports QMM_ERR_DEVICE with no copy in flight
     int withhold_x;
     long long mma_wait_cycles;
+    // Q6_K with its rows in whole groups of 8 (tm_w maps each group as one row of 8 row
+    // lengths): the raw superblock of a tile's 128 rows comes as 8 boxes, one per row
+    // residue mod 8, instead of 128 bulk copies
+    int q6_groups;
 };
 
 // Where tile t lives: m0 = first activation row (sorted row in grouped mode), rows =
@@ -293,12 +301,21 @@ __device__ __forceinline__ bool next_seg(const TcArgs &a, int64_t &u, int64_t en
     return true;
 }
 
+// Q6_K by row groups (TcArgs::q6_groups): tile column c holds weight row q6_perm(c), so that
+// the 8 unpack threads of a quarter warp, which take 8 consecutive columns, read 8 different
+// rows of one row-group box (distinct banks) while writing their own columns as before.
+__device__ __forceinline__ int q6_perm(int c) { return 64 * (c >> 6) + 8 * (c & 7) + ((c >> 3) & 7); }
+
 // One epilogue thread's 32 results of a segment: a whole tile goes to y, part of a
-// tile to this CTA's partial slot (0 for its first segment, 1 for its last).
+// tile to this CTA's partial slot (0 for its first segment, 1 for its last).  With row
+// groups (rowgrp) column 32 cq + 8 jj + j is weight row 64 (cq / 2) + 4 (cq % 2) + 8 j + jj:
+// four consecutive rows for each j; partial slots are kept in weight-row order.
 __device__ __forceinline__ void store_segment(const TcArgs &a, const Seg &sg, int seg_i, int tl, int cq,
-                                              const float2 (&tot)[16]) {
+                                              const float2 (&tot)[16], bool rowgrp) {
     const TileInfo ti = resolve_tile(a, sg.tile);
     const int64_t col0 = ti.col0 + 32 * cq;
+    auto val = [&](int i) { return (i & 1) ? tot[i >> 1].y : tot[i >> 1].x; };
+    const int gbase = 64 * (cq >> 1) + 4 * (cq & 1);  // rowgrp: first weight row of the thread's groups
     if (a.n_out) {  // GLU (whole tiles only): columns 2i, 2i+1 are the gate and up dots of output col0/2 + i
         if (tl >= ti.rows) return;
         const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
@@ -311,6 +328,21 @@ __device__ __forceinline__ void store_segment(const TcArgs &a, const Seg &sg, in
     if (sg.s0 == 0 && sg.s1 == a.nsb) {
         if (tl >= ti.rows) return;
         const int64_t yrow = a.tiles ? int64_t(a.perm[ti.m0 + tl]) : int64_t(ti.m0 + tl);
+        if (rowgrp) {
+            float *dst = a.y + yrow * a.n + ti.col0 + gbase;
+            if ((a.n % 4 == 0) && (ti.col0 + 128 <= a.n)) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4 *>(dst + 8 * j) = make_float4(val(j), val(8 + j), val(16 + j), val(24 + j));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (ti.col0 + gbase + 8 * j + jj < a.n) dst[8 * j + jj] = val(8 * jj + j);
+            }
+            return;
+        }
         float *dst = a.y + yrow * a.n + col0;
         if ((a.n % 4 == 0) && (col0 + 32 <= a.n)) {
 #pragma unroll
@@ -326,8 +358,14 @@ __device__ __forceinline__ void store_segment(const TcArgs &a, const Seg &sg, in
         }
     } else {
         const int slotidx = seg_i == 0 ? 0 : 1;
-        float4 *dst =
-            reinterpret_cast<float4 *>(a.partial + ((int64_t(blockIdx.x) * 2 + slotidx) * kTM + tl) * kTN + 32 * cq);
+        float *prow = a.partial + ((int64_t(blockIdx.x) * 2 + slotidx) * kTM + tl) * kTN;
+        if (rowgrp) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4 *>(prow + gbase + 8 * j) = make_float4(val(j), val(8 + j), val(16 + j), val(24 + j));
+            return;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(prow + 32 * cq);
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4)
             dst[i4] = make_float4(tot[2 * i4].x, tot[2 * i4].y, tot[2 * i4 + 1].x, tot[2 * i4 + 1].y);
@@ -511,7 +549,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         // spread over the 32 lanes.
         regs_dec<kRegsProducer>();
         if (T == QMM_Q6_K || lane == 0) {
-            if constexpr (T != QMM_Q6_K) ptx::prefetch_tmap(&tm_w);
+            if (T != QMM_Q6_K || a.q6_groups) ptx::prefetch_tmap(&tm_w);
             if (a.n_out && !a.glu_packed) ptx::prefetch_tmap(&tm_w2);
             int64_t u = ubeg;
             Seg sg;
@@ -529,6 +567,21 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                     }
                     const uint32_t rbar = ptx::smem_u32(&B.raw_full[ri]);
                     if constexpr (T == QMM_Q6_K) {
+                      if (a.q6_groups) {
+                        // box res: rows n0 + res, n0 + res + 8, ... (16 of them, 240 bytes each
+                        // from the 16-byte boundary at or below the superblock), where rows
+                        // past the matrix read as zeros.  One copy per 128 rows instead of
+                        // 128 (151936 x 5120 at m = 512: the per-row copies cost about 24%).
+                        if (lane == 0) {
+                            ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
+#pragma unroll 1
+                            for (int res = 0; res < 8; ++res)
+                                ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes + res * kQ6GroupBox, &tm_w,
+                                                 (int)(((int64_t)res * a.row_bytes + sb * kQ6KBytes) & ~int64_t(15)),
+                                                 n0 / 8, rbar);
+                        }
+                        __syncwarp();
+                      } else {
                         // rows of W in this tile: its columns within the expert's (or the matrix's) n
                         const int64_t cols = a.n - resolve_tile(a, sg.tile).col0;
                         const int64_t nval = cols < 128 ? cols : 128;
@@ -540,6 +593,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                             ptx::bulk_g2s(sbase + kOffRaw + ri * kRawBytes + r * F::kRawRow, a.W + (p & ~int64_t(15)),
                                           F::kCopyBytes, rbar);
                         }
+                      }
                     } else if (a.n_out && !a.glu_packed) {  // GLU: 64 gate rows, then the 64 up rows of the same outputs
                         ptx::mbar_arrive_expect_tx(rbar, kRawBytes);
                         ptx::tma_load_2d(sbase + kOffRaw + ri * kRawBytes, &tm_w, F::raw_x(sb), n0 / 2, rbar);
@@ -569,7 +623,9 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         uint32_t w_it = 0, sb_it = 0;
         bool ok = true;
         while (ok && next_seg(a, u, uend, sg)) {
-            const int64_t n0w = resolve_tile(a, sg.tile).n0w + r;  // this thread's row of W
+            // this thread's row of W: tile column r, or with Q6_K row groups weight row q6_perm(r)
+            const int wr = (T == QMM_Q6_K && a.q6_groups) ? q6_perm(r) : r;
+            const int64_t n0w = resolve_tile(a, sg.tile).n0w + wr;
             (void)n0w;
             for (int64_t sb = sg.s0; ok && sb < sg.s1; ++sb) {
                 const uint32_t ri = sb_it & 1;
@@ -581,8 +637,11 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 // GLU from two tensors: tile column r is gate row r/2 (r even) or up row r/2 (r odd)
                 const int rsrc = a.n_out && !a.glu_packed ? (r & 1) * 64 + (r >> 1) : r;
                 const uint8_t *blk = smem + kOffRaw + ri * kRawBytes + rsrc * F::kRawRow;
-                if constexpr (T == QMM_Q6_K)  // the superblock's offset inside its window
-                    blk += (int)(F::pos(n0w, sb, a.row_bytes) & 15);
+                if constexpr (T == QMM_Q6_K) {
+                    if (a.q6_groups)  // weight row wr: box wr % 8, its row wr / 8
+                        blk = smem + kOffRaw + ri * kRawBytes + (wr & 7) * kQ6GroupBox + (wr >> 3) * F::kRawRow;
+                    blk += (int)(F::pos(n0w, sb, a.row_bytes) & 15);  // the superblock's offset inside its window
+                }
                 float *dd = reinterpret_cast<float *>(smem + kOffDD + ri * F::kDDBytes);
                 if constexpr (T == QMM_Q4_K || T == QMM_Q5_K) {
                 // Q5_K: the nibbles start 32 bytes later, after the plane of fifth bits
@@ -1057,7 +1116,7 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
                 ++sd_it;
             }
             if (!ok) break;
-            store_segment(a, sg, seg_i, tl, cq, tot);
+            store_segment(a, sg, seg_i, tl, cq, tot, T == QMM_Q6_K && a.q6_groups);
             ++seg_i;
         }
     }
@@ -1260,14 +1319,26 @@ int tc_perm4(qmm_type t) { return t == QMM_Q4_K ? 1 : 0; }
 
 int64_t tc_row_bytes(qmm_type t, int64_t k) { return (k / 256) * block_bytes(t) * (256 / block_elems(t)); }
 
+// Q6_K raw superblocks by row-group boxes (TcArgs::q6_groups): rows in whole groups of 8
+// whose 8 row lengths make a multiple of 16 bytes
+bool q6_row_groups(qmm_type t, int64_t rows, int64_t row_bytes) {
+    return t == QMM_Q6_K && rows % 8 == 0 && (8 * row_bytes) % 16 == 0;
+}
+
 bool tc_weight_map(qmm_type t, const void *W, int64_t rows, int64_t k, CUtensorMap *tm_w, int64_t stride = 0) {
     const int64_t row_bytes = stride > 0 ? stride : tc_row_bytes(t, k);
     if (t == QMM_Q8_0)
         return make_map_2d(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, W, row_bytes / 2, rows, TcFmt<QMM_Q8_0>::kRawRow / 2,
                            kTN, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (t == QMM_Q6_K) {
+        // rows in whole groups of 8: each group is one row of the map (8 row lengths, a
+        // multiple of 16 bytes), read as 240-byte boxes of 16 groups; otherwise the kernel
+        // copies each row's window itself
         memset(tm_w, 0, sizeof(*tm_w));
-        return (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
+        if ((reinterpret_cast<uintptr_t>(W) & 15u) != 0) return false;
+        if (!q6_row_groups(t, rows, row_bytes)) return true;
+        return make_map_2d(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, uint64_t(8 * row_bytes), uint64_t(rows / 8),
+                           TcFmt<QMM_Q6_K>::kRawRow, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     // Q4_K, Q5_K and Q4_0: a box of one superblock's raw bytes (144, 176, 144) per row
     return make_map_2d(tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, row_bytes, rows, (uint32_t)tc_row_bytes(t, 256), kTN,
@@ -1385,6 +1456,7 @@ cudaError_t launch_gemm_tc(qmm_type t, const void *W, int64_t n, int64_t k, cons
 
     TcArgs args{};
     tc_test_fault(args);
+    args.q6_groups = q6_row_groups(t, n, row_bytes) ? 1 : 0;
     args.W = static_cast<const uint8_t *>(W);
     args.n = n;
     args.m = m;
@@ -1519,6 +1591,7 @@ cudaError_t launch_gemm_tc_grouped(qmm_type t, const void *W, int64_t n_experts,
     args.m = n_pairs;
     args.k = (int)k;
     args.row_bytes = tc_row_bytes(t, k);
+    args.q6_groups = q6_row_groups(t, n_experts * n, args.row_bytes) ? 1 : 0;
     args.y = y;
     args.partial = reinterpret_cast<float *>(base + L.partial);
     args.status = status;

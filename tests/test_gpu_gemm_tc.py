@@ -100,9 +100,10 @@ def test_tc_q8_0_extreme_codes(oracle_mod):
     assert_within(y.cpu().numpy(), y_ref, T, "tc q8_0 extreme codes")
 
 
-# Q6_K on the tensor cores: 6-bit codes q - 32 as exact fp16, one slot per 16-wide
-# sub-block, d * sc (int8) folded with d8.  n must be a multiple of 8 (the raw copies
-# are 16-byte windows of the row-major weight rows).
+# Q6_K on the tensor cores: 6-bit codes q - 32 in two exact fp16 planes per 32-block slot,
+# d folded with d8.  n a multiple of 8: the raw superblocks arrive as boxes of row groups
+# (one map row per 8 weight rows) and the tile columns are permuted to match, through
+# whole tiles and stream-K partial slots alike.
 @pytest.mark.parametrize("n,k,m", [(128, 256, 128), (136, 512, 9), (8, 256, 17), (1000, 1024, 300),
                                    (2048, 768, 200)])
 @pytest.mark.parametrize("sk", [1, 2])
