@@ -130,12 +130,12 @@ template <> struct TcFmt<QMM_Q4_0> : TcStages2 {
     static __device__ __forceinline__ int raw_x(int64_t sb) { return (int)(sb * 144); }
 };
 // Q6_K: a row is 210 bytes per superblock, so neither a row (210 * k/256 bytes) nor a
-// superblock is a whole number of 16-byte units and the rows cannot be a 2-D tensor map.
-// The raw warp instead issues one 224-byte bulk copy per row: the window starting at the
-// 16-byte boundary at or below the row's superblock (offset <= 14 inside it, the bytes
-// after it belong to the next row).  With n a multiple of 8 the weight tensor ends on a
-// 16-byte boundary, so the last row's last window ends exactly there.  Windows sit 240
-// bytes apart in shared memory: 8 consecutive rows start on different banks.
+// superblock is a whole number of 16-byte units and the rows cannot be the rows of a 2-D
+// tensor map; 8 rows always are.  With n a multiple of 8 the map's row is a group of 8 weight
+// rows and the raw warp loads 8 boxes per superblock (TcArgs::q6_groups); otherwise it issues
+// one 224-byte bulk copy per row.  Either way a row's data is the window starting at the
+// 16-byte boundary at or below its superblock (offset <= 14 inside it, the bytes after it
+// belong to the next row), and windows sit 240 bytes apart in shared memory.
 // The int8 sub-scale of every 16 values goes into the operands: with sc = 16 a + b
 // (a = sc >> 4 in -8..7, b = sc & 15), the weight code q (-32..31) becomes two exact fp16
 // planes, 16 q a and q b, and the MMA runs over the same activations once per plane into
@@ -545,8 +545,8 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
         // ------------------------------------------------------------ raw weight TMA
         // The raw superblock of the tile's 128 weight rows, one per superblock, into a
         // 2-deep ring; independent of the activation stream so neither waits on the other.
-        // Q4_K / Q8_0: one tensor-map box (lane 0); Q6_K: one bulk copy per valid row,
-        // spread over the 32 lanes.
+        // Q4_K / Q8_0: one tensor-map box (lane 0); Q6_K: 8 row-group boxes (lane 0), or
+        // one bulk copy per valid row spread over the 32 lanes.
         regs_dec<kRegsProducer>();
         if (T == QMM_Q6_K || lane == 0) {
             if (T != QMM_Q6_K || a.q6_groups) ptx::prefetch_tmap(&tm_w);
@@ -615,9 +615,10 @@ __device__ __forceinline__ void gemm_tc_body(const CUtensorMap &tm_x, const CUte
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ weight unpack
         // One weight row per thread, reading the raw superblock that the TMA warp put in
-        // shared memory (rows 144 bytes apart: 8 consecutive rows hit distinct banks).
+        // shared memory (rows 144 bytes apart: 8 consecutive rows hit distinct banks); with
+        // Q6_K row groups the thread of tile column r takes weight row q6_perm(r).
         regs_dec<kRegsUnpack>();
-        const int r = tid - 32 * kUnpackWarp0;  // weight row within the tile
+        const int r = tid - 32 * kUnpackWarp0;  // tile column (weight row within the tile)
         int64_t u = ubeg;
         Seg sg;
         uint32_t w_it = 0, sb_it = 0;
