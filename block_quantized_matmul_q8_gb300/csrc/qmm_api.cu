@@ -130,7 +130,9 @@ qmm_status moe_check_sizes(qmm_type t, int64_t n_experts, int64_t n, int64_t k, 
     qmm_status s = check_k(t, k);
     if (s != QMM_OK) return s;
     if (n_experts <= 0 || top_k <= 0 || n < 0 || n_tokens < 0) return QMM_ERR_ARG;
-    if (n_experts > kMaxExperts || n > kMaxRows || n_tokens * top_k > kMaxRows) return QMM_ERR_SHAPE;
+    // the pair count n_tokens * top_k, compared without forming a product that could overflow
+    if (n_experts > kMaxExperts || n > kMaxRows || top_k > kMaxRows || n_tokens > kMaxRows / top_k)
+        return QMM_ERR_SHAPE;
     return QMM_OK;
 }
 
@@ -259,7 +261,10 @@ size_t qmm_row_bytes(qmm_type t, int64_t k) {
 
 size_t qmm_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t n_experts, int64_t top_k) {
     if (!type_ok(t) || n < 0 || k <= 0 || m < 0) return 0;
-    if (n_experts > 0) return moe_workspace_bytes(t, n, k, m, n_experts, top_k);
+    if (n_experts > 0)
+        return moe_check_sizes(t, n_experts, n, k, top_k, m) == QMM_OK ? moe_workspace_bytes(t, n, k, m, n_experts, top_k)
+                                                                        : 0;
+    if (n > kMaxRows || m > kMaxRows || check_k(t, k) != QMM_OK) return 0;
     // enough for every path the call may take (the forced ones included)
     const size_t gemm = gemm_tc_supported(t, n, k, m) ? gemm_tc_workspace_bytes(t, n, k, m) : 0;
     return std::max(gemm, gemv_tc_workspace_bytes(t, n, k, m));

@@ -88,7 +88,7 @@ QMM_API size_t qmm_row_bytes(qmm_type t, int64_t k);
  * paths keep one partial-sum slot per SM, so the figure depends on the SM count:
  * size the workspace with the device current on which the call will run).  The
  * workspace must be 256-byte aligned device memory; its contents need no
- * initialisation. */
+ * initialisation.  0 for a type or sizes that the call rejects. */
 QMM_API size_t qmm_workspace_bytes(qmm_type t, int64_t n, int64_t k, int64_t m, int64_t n_experts, int64_t top_k);
 
 /*

@@ -78,6 +78,10 @@ def test_argument_errors_need_no_gpu(L):
     assert L.qmm_mul_mat_id(*bad_e, P(1 << 20), ws_need, None) == 1
     many = [P(1024), 12, 100000, 8, 256, P(2048), P(4096), 2, 3, P(8192)]
     assert L.qmm_mul_mat_id(*many, P(1 << 20), 1 << 40, None) == 2
+    # pair counts past 2^31 - 1, including ones whose product overflows int64
+    for T_, K in ((1 << 31, 1), (1 << 30, 2), (1 << 62, 4), (3, 1 << 62), (1 << 40, 1 << 40)):
+        huge = [P(1024), 12, 4, 8, 256, P(2048), P(4096), K, T_, P(8192)]
+        assert L.qmm_mul_mat_id(*huge, P(1 << 20), 1 << 40, None) == 2, (T_, K)
 
 
 def test_f32_call_argument_errors_need_no_gpu(L):
