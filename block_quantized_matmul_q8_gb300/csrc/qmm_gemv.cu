@@ -762,8 +762,13 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x
         // stages and q8_1 input, each half-warp folds two rows over its 16 units (17408 x 5120:
         // 10.27 -> 10.11 us at 1 column, 12.8 -> 12.5 at 2, 23.3 -> 20.2 at 5); from 6 columns
         // on the row pairs spill and the MMA GEMV takes over.  With the fp32 row quantized in
-        // the prologue the one-row form stays faster (10.8 against 11.1 us).
-        const bool pairs = nstages == kTmaMaxStages && NC <= 5 && x.xf == nullptr;
+        // the prologue, the row pairs win where a CTA has at most 96 rows (14336 x 4096: 7.50 ->
+        // 7.07 us, 4096 x 5120: 4.77 -> 4.53, 2048 x 4096: 3.50 -> 3.42) and the one-row form
+        // where it has more (17408 x 5120, 115 rows: 9.81 against 10.00 us).  Both forms sum
+        // each row in the same order, so the choice does not change y.
+        const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
+        const bool pairs = nstages == kTmaMaxStages && NC <= 5 &&
+                           (x.xf == nullptr || (NC == 1 && n <= 96 * grid));
         if constexpr (NC <= 2)
             kern = k >= kTwoRowMinK ? gemv_q4k_tma_long_kernel<NC>
                    : pairs          ? gemv_q4k_tma_pair_kernel<NC>
@@ -775,7 +780,7 @@ static cudaError_t launch_gemv_tma_nc(const void *W, int64_t n, int64_t k, XIn x
     }
     cudaError_t e = ensure_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(device_sm_count(), (n + 1) / 2));  // as above
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, st, static_cast<const uint8_t *>(W), n,
                       (int)k, row_bytes, nstages, x, y, y_ld, static_cast<int *>(nullptr));
 }
