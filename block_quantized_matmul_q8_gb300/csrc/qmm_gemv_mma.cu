@@ -34,10 +34,12 @@
 // warp streams whole tiles (16 rows x all of k, one bulk copy per row) through a ring of
 // shared-memory stages.  All 16 consumer warps work on every tile, each taking whole
 // superblocks of it (superblock j of tile t goes to warp (t nsb + j) mod 16, so the warps'
-// shares even out over the tiles), and writes its 16 x 8 partial results to its own slot of
-// the stage.  Once all 16 have released the stage, the producer warp sums the 16 slots in
-// warp order (so the result does not depend on timing), writes the tile's outputs and
-// reuses the stage.  Every consumer warp waits for every
+// shares even out over the tiles), and writes its 16 x 8 partial results to its own slot in
+// the tile's set of partial sums (set t mod (nstages + 1)).  Once all 16 have released the
+// stage, the producer warp first reuses it for the next tile's copy, then sums the released
+// tile's 16 slots in warp order (so the result does not depend on timing) and writes its
+// outputs.  The set it reads is the one that tile t + 1 will write, whose copy the producer
+// has not issued yet, so no consumer writes it meanwhile.  Every consumer warp waits for every
 // tile, so a stage's earlier tile has always landed when a warp waits for its next one.
 // The activations are staged once per CTA: the m columns' q8_1 codes as fp16, and per block
 // d8, -1024 sum(q) and s.
@@ -83,8 +85,10 @@ bool mma_plan(int64_t k, int m, size_t budget, MmaPlan &p) {
     // columns 16 words apart: the 2 columns a quarter-warp reads
     p.row_stride = pad_to_bank(row_bytes, 8);
     p.x_stride = pad_to_bank(2 * k, 16);
-    // staged codes [m][x_stride], factors [nb32][8] float2, s [8][nb32] fp16
-    p.fixed = 1024 + size_t(m) * p.x_stride + size_t(nb32) * kCols * 8 + size_t(kCols) * nb32 * 2;
+    // staged codes [m][x_stride], factors [nb32][8] float2, s [8][nb32] fp16, and the one set
+    // of partial sums beyond one per stage
+    p.fixed = 1024 + size_t(m) * p.x_stride + size_t(nb32) * kCols * 8 + size_t(kCols) * nb32 * 2 +
+              size_t(kMmaWarps) * kTileRows * kCols * 4;
     p.stage_bytes = size_t(kTileRows) * p.row_stride;
     if (p.fixed >= budget) return false;
     // per stage: the tile's rows and each consumer warp's 16 x 8 fp32 partial sums
@@ -242,7 +246,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     uint8_t *xs = stages + size_t(nstages) * stage_bytes;                          // [m][x_stride] fp16 codes
     float2 *fz = reinterpret_cast<float2 *>(xs + size_t(m) * x_stride);           // [nb32][8] {d8, -1024 sum q}
     uint16_t *sh = reinterpret_cast<uint16_t *>(fz + size_t(nb32) * kCols);        // [8][nb32] s (fp16 bits)
-    float *acc = reinterpret_cast<float *>(sh + size_t(kCols) * nb32);             // [nstages][16 warps][16][8]
+    float *acc = reinterpret_cast<float *>(sh + size_t(kCols) * nb32);             // [nstages + 1][16 warps][16][8]
+    const int nacc = nstages + 1;
     volatile int *abortp = &abort_flag;
 
     // this CTA's tiles of 16 rows (the last tile of the matrix may be shorter)
@@ -265,12 +270,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
     if (warp == kMmaWarps) {
         // ---------------- producer warp: copies in, results out
-        // Tile t of the CTA goes to stage t % nstages.  Before a stage takes a new tile, the
-        // 16 consumer warps have released it, so its slots hold the previous tile's partial
-        // sums: the warp adds them in warp order and writes the outputs.
-        auto write_tile = [&](int t, int s) {
+        // Tile t of the CTA goes to stage t % nstages and its partial sums to set t % nacc.
+        // Once the 16 consumer warps have released a stage, the warp issues the stage's next
+        // copy, then adds the released tile's slots in warp order and writes its outputs.
+        auto write_tile = [&](int t) {
             const int64_t row0 = (tb + t) * kTileRows;
-            const float *a = acc + size_t(s) * kMmaWarps * kTileRows * kCols;
+            const float *a = acc + size_t(t % nacc) * kMmaWarps * kTileRows * kCols;
 #pragma unroll
             for (int i = 0; i < kTileRows * kCols / 32; ++i) {
                 const int e = lane + 32 * i, r = e & 15, c = e >> 4;
@@ -288,8 +293,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 ok = __all_sync(0xffffffffu,
                                 ptx::mbar_wait_spin(ptx::smem_u32(&empty[s]), ((t / nstages) - 1) & 1, abortp));
                 if (!ok) break;
-                write_tile(t - nstages, s);
-                __syncwarp();
             }
             const int64_t row0 = (tb + t) * kTileRows;
             const int rows = (int)min((int64_t)kTileRows, n - row0);
@@ -300,6 +303,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                 ptx::bulk_g2s(ptx::smem_u32(stages + s * stage_bytes + size_t(lane) * row_stride),
                               W + (row0 + lane) * row_bytes, uint32_t(row_bytes), bar);
             ++issued;
+            if (t >= nstages) {
+                write_tile(t - nstages);
+                __syncwarp();
+            }
         }
         // every issued copy must have landed before the CTA exits (bounded waits, independent
         // of the abort flag); then the last tiles' results
@@ -309,7 +316,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int t = max(0, issued - nstages); ok && t < issued; ++t) {
             const int s = t % nstages;
             ok = __all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_u32(&empty[s]), (t / nstages) & 1, abortp));
-            if (ok) write_tile(t, s);
+            if (ok) write_tile(t);
         }
     } else {
         // ---------------- consumers: stage the activations, then fold the tiles
@@ -363,7 +370,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             for (; j < nsb; j += kMmaWarps)
                 fold_superblock(rg + j * kQ4KBytes, rg8 + j * kQ4KBytes, xg, xv, fza, sg, j, t4, tot01, tot23);
             // this warp's slot of the stage: rows g and g + 8, columns 2t4, 2t4 + 1
-            const uint32_t a = acc0 + uint32_t(((s * kMmaWarps + warp) * kTileRows) * kCols * 4);
+            const uint32_t a = acc0 + uint32_t((((t % nacc) * kMmaWarps + warp) * kTileRows) * kCols * 4);
             sts64(a + 4 * (g * kCols + 2 * t4), tot01);
             sts64(a + 4 * ((g + 8) * kCols + 2 * t4), tot23);
             __syncwarp();
