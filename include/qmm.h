@@ -2,7 +2,7 @@
  * qmm.h -- C ABI of the block-quantized matmul library for GB300 (sm_103a).
  *
  * The library computes y[m][n] = sum_k x[m][k] * dequant(W)[n][k] with W kept in
- * its block-quantized form (Q4_K, Q6_K, Q8_0 or Q4_0) and x quantized to q8_1 first.
+ * its block-quantized form (Q4_K, Q5_K, Q6_K, Q8_0 or Q4_0) and x quantized to q8_1 first.
  * Every product is formed from exact integer sub-block dot products that are
  * then folded with the block scales in fp32.
  *
@@ -12,11 +12,13 @@
  *   [QMM]   "QTensor 与 QMatMul" (candle 0.11.0 notes)
  *
  * Conventions shared by every call
- *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *     keeps no reference to them after a call returns and allocates no device
- *     memory per call: scratch lives in the caller's workspace.
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except the host
+ *     buffers of qmm_mul_mat_f32_host.  The library keeps no reference to them after
+ *     a call returns and allocates no device memory per call: scratch lives in the
+ *     caller's workspace.
  *   - Every call enqueues its work on `stream` (a cudaStream_t; NULL = legacy
- *     default stream) and returns without synchronising the host.
+ *     default stream) and returns without synchronising the host, except the two
+ *     status reads and qmm_mul_mat_f32_host with a pageable y_host.
  *   - Row-major layouts.  W is [n] rows of k/QK blocks, one row per output
  *     feature, as PyTorch Linear stores weights ([QMM] section "QMatMul:
  *     三种形态": weights are stored [n, k]).  x is [m][k] fp32, y is [m][n] fp32.
@@ -112,11 +114,14 @@ QMM_API qmm_status qmm_quantize_q8_1(const float *x, int64_t m, int64_t k, void 
  *   xq     : q8_1 blocks of x [m][k] as written by qmm_quantize_q8_1.
  *   y      : fp32 [m][n] output, 16-byte aligned; every element is written.
  *   workspace, ws_bytes: at least qmm_workspace_bytes(t, n, k, m, 0, 0) bytes.
- * k % 256 == 0 for Q4_K/Q6_K, k % 32 == 0 for Q8_0/Q4_0.  Paths (each weight byte is read
- * once, every column reusing the decoded weight):
- *   Q4_K, m <= 8:       the bulk-copy GEMV (dp4a);
+ * k % 256 == 0 for Q4_K/Q5_K/Q6_K, k % 32 == 0 for Q8_0/Q4_0.  Paths (each weight byte is
+ * read once, every column reusing the decoded weight):
+ *   Q4_K, m <= 5:       the bulk-copy GEMV (dp4a);
+ *   Q4_K, 6 <= m <= 8:  the multi-column GEMV on the warp-level MMA (the columns as its N
+ *                       side) where its two tile stages fit shared memory, else the above;
  *   Q4_K, 9 <= m <= 16: the skinny tensor-core path (weight rows as the MMA's M side);
  *   Q4_K, m > 16:       the tiled tensor-core GEMM;
+ *   Q5_K, m <= 8:       the bulk-copy GEMV; m > 8: the tiled tensor-core GEMM;
  *   Q6_K/Q8_0, m <= 8:  the bulk-copy GEMV;
  *   Q6_K/Q8_0, m > 8:   the tiled tensor-core GEMM (Q8_0: k % 256 == 0; Q6_K: n % 8
  *                       == 0), otherwise the CUDA-core tiled GEMM;
