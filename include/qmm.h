@@ -212,7 +212,7 @@ QMM_API qmm_status qmm_repack_glu(const void *W_gate, const void *W_up, qmm_type
 /*
  * qmm_mul_mat_glu on the interleaved tensor of qmm_repack_glu: the same y, and to the
  * bit on the fused paths (Q4_K), which fold the same rows in the same order: the GEMV
- * then streams each chunk of 4 outputs (gate and up rows) with one copy instead of 8,
+ * then streams each chunk of 4 outputs (gate and up rows) with one copy instead of two,
  * and the tensor-core GEMM loads a tile's gate and up rows as one box.  Other types
  * and shapes: one product of the 2n rows into the workspace and a combine pass, within
  * the bound of qmm_mul_mat_glu.  workspace: qmm_workspace_bytes_glu(t, n, k, m).
@@ -269,9 +269,10 @@ QMM_API qmm_status qmm_mul_mat_aligned(const void *W_aligned, qmm_type t, int64_
  *     always, Q8_0 and Q4_0 with k/32 % 8 == 0, Q6_K with 16-byte rows or even n);
  *   otherwise the pairs are bucketed by expert on the device (a stable counting sort)
  *     and the per-expert tiles are walked by one persistent launch: with k % 256 == 0
- *     (and for Q6_K n % 8 == 0) on the tensor cores (128-pair tiles, stream-K over the
- *     device-built tile list; the workspace then also holds an fp16 copy of the gathered
- *     activations), other shapes on the CUDA-core grouped GEMM.  For Q4_K the
+ *     (and for Q6_K n % 8 == 0) on the tensor cores (128-pair tiles from a device-built
+ *     list, whole tiles per CTA when they fill 90% of the CTAs' rounds, else stream-K;
+ *     the workspace then also holds an fp16 copy of the gathered activations), other
+ *     shapes on the CUDA-core grouped GEMM.  For Q4_K the
  *     experts with 1..16 pairs ([MMQ] section "MoE 的二次账": experts whose few columns
  *     leave the tiles mostly empty) skip the 128-pair tiles: a second launch runs them
  *     as 16-column slabs on the skinny tensor-core kernel, the expert list and its
@@ -397,7 +398,8 @@ QMM_API void qmm_plan_cta_range(const qmm_gemm_plan *plan, int32_t cta, int64_t 
  * reading W), for one launch of ncols (1..8) activation columns,
  * given smem_bytes of shared memory per block: the deepest of 8, 6, 4 or 3 stages of 8
  * weight rows that fits.  The consumer groups take the stages in turn, 4 groups for 8
- * and 4 stages, 3 for 6 and 3, so that each stage always goes to the same group.  0
+ * and 4 stages (8 groups of 2 warps in the Q4_K row-pair form), 3 for 6 and 3, so that
+ * each stage always goes to the same group.  0
  * when the rows cannot be streamed in whole 16-byte units (Q8_0 and Q4_0 unless k/32
  * is a multiple of 8; Q6_K unless k/256 is a multiple of 8, or of 4 with n even) or
  * when not even 3 stages fit next to the staged activations (Q4_K at one column from
@@ -412,7 +414,7 @@ QMM_API int qmm_gemv_ring_stages(qmm_type t, int64_t n, int64_t k, int32_t ncols
  * 2 = the CUDA-core (dp4a) tiled GEMM, 3 = the tensor-core GEMM for any m,
  * 4 = GEMV for any m <= 64 with direct global loads only (no bulk copies),
  * 5 = the skinny tensor-core path (Q4_K, m <= 16), 6 = the multi-column mma.sync GEMV
- * (Q4_K, 2 <= m <= 8).  A forced path that does not
+ * (Q4_K, 1 <= m <= 8).  A forced path that does not
  * support the call's type or sizes falls back to the automatic choice. */
 QMM_API void qmm_set_force_path(int path);
 
