@@ -48,6 +48,19 @@ def test_sizes():
     assert qmm.qmm_row_bytes(99, 256) == 0
 
 
+def test_workspace_bytes_zero_for_rejected_sizes(L):
+    # the sizes the calls reject get 0, not a figure computed from them
+    assert L.qmm_workspace_bytes(99, 8, 256, 4, 0, 0) == 0            # unknown type
+    assert L.qmm_workspace_bytes(12, 8, 100, 4, 0, 0) == 0            # k not whole superblocks
+    assert L.qmm_workspace_bytes(12, 8, 1 << 21, 4, 0, 0) == 0        # k above the limit
+    assert L.qmm_workspace_bytes(12, 1 << 31, 256, 4, 0, 0) == 0      # n above 2^31 - 1
+    assert L.qmm_workspace_bytes(12, 8, 256, 1 << 31, 0, 0) == 0      # m above 2^31 - 1
+    assert L.qmm_workspace_bytes(12, 8, 256, 1 << 62, 4, 4) == 0      # pairs past 2^31 - 1, product overflows
+    assert L.qmm_workspace_bytes(12, 8, 256, 3, 100000, 2) == 0       # too many experts
+    assert L.qmm_workspace_bytes(12, 8, 256, 3, 4, 2) > 0
+    assert L.qmm_workspace_bytes_id_glu(12, 8, 256, 1 << 62, 4, 4) == 0
+
+
 def _mm(L, W=1024, t=12, n=8, k=256, xq=2048, m=4, y=4096, ws=None, wsb=0):
     P = ctypes.c_void_p
     return L.qmm_mul_mat(P(W), t, n, k, P(xq), m, P(y), P(ws) if ws else None, wsb, None)
